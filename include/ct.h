@@ -1,0 +1,141 @@
+/*
+ * ct.h -- C ABI of the GB300 (sm_103a) forward transposed-convolution library
+ * (libct.so).
+ *
+ * What it computes (POPCORNBENCH reasoning traces, cited by task id):
+ *   [l1_p79] trace Kimi-K2.6__l1_p79, ConvTranspose1d with dilation 2: the
+ *            output-length formula and the scatter rule
+ *            y[n, oc, i*s - p + k*d] += x[n, ic, i] * w[ic, oc, k].
+ *   [l1_p72] trace Kimi-K2.6__l1_p72, ConvTranspose3d with groups=4 and an
+ *            asymmetric kernel: weight layout (C_in, C_out/groups, kD, kH, kW),
+ *            grouped channel mapping, direct accumulation without flipping.
+ *   [l2_p26] trace Kimi-K2.6__l2_p26, ConvTranspose3d + add + x*hardswish(x):
+ *            t = convT(x) + bias + add;  out = t * hardswish(t),
+ *            hardswish(t) = t * clamp(t + 3, 0, 6) / 6.
+ *
+ * For every spatial dimension d:
+ *     L_out[d] = (L_in[d] - 1)*s[d] - 2*p[d] + dl[d]*(k[d] - 1) + op[d] + 1
+ * and
+ *     y[n, oc, o] = bias[oc] + sum over ic in oc's group, taps k with
+ *                   o = i*s - p + k*dl for an input position 0 <= i < L_in
+ *                   of x[n, ic, i] * w[ic, oc mod (C_out/groups), k]
+ * (per-dimension relations, product over dimensions).  An output no tap
+ * reaches holds bias[oc] (or 0 without bias); the output_padding tail is
+ * computed by the same rule.
+ *
+ * Layouts (all contiguous, row-major, owned by the caller, device memory):
+ *     x    (N, C_in, L)              or (N, C_in, D, H, W)       dtype CT_F32 or CT_BF16
+ *     w    (C_in, C_out/groups, k)   or (C_in, C_out/groups, kD, kH, kW)   same dtype as x
+ *     bias (C_out,)  fp32, may be NULL
+ *     add  shape of y, fp32 (fused entry point only)
+ *     y    (N, C_out, L_out) or (N, C_out, D_out, H_out, W_out), always fp32
+ * y must not overlap x, w or bias.  y may be the same buffer as add (each
+ * element of add is read before the same thread writes that element of y).
+ *
+ * Execution: every forward call only validates its arguments on the host,
+ * then enqueues kernels on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream) and returns; nothing is synchronised and nothing is
+ * allocated.  Paths that need scratch memory (the bf16 tensor-core path)
+ * take it from the caller-supplied `workspace` of at least the size that
+ * ct_workspace_size_* reports (256-byte aligned); other paths need none and
+ * accept workspace = NULL, ws_bytes = 0.
+ *
+ * Errors: argument and shape errors are returned synchronously before any
+ * launch and leave y untouched.  A failed launch returns CT_ERR_CUDA.  The
+ * bf16 tensor-core kernel bounds every wait; a wait that runs out records
+ * CT_ERR_DEVICE_TIMEOUT in a device status word, read (and cleared) by
+ * ct_last_device_error().
+ */
+#ifndef CT_H
+#define CT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CT_OK = 0,
+    CT_ERR_ARG = 1,            /* NULL pointer, non-positive size, bad dtype        */
+    CT_ERR_SHAPE = 2,          /* groups do not divide channels, L_out <= 0,        */
+                               /* output_padding >= max(stride, dilation), p < 0 ... */
+    CT_ERR_ALIGN = 3,          /* a pointer is not aligned to its element size      */
+    CT_ERR_WORKSPACE = 4,      /* workspace missing, too small or not 256-B aligned */
+    CT_ERR_UNSUPPORTED = 5,    /* valid operator this build does not run            */
+    CT_ERR_CUDA = 6,           /* a CUDA runtime call or launch failed              */
+    CT_ERR_DEVICE_TIMEOUT = 7  /* a bounded device-side wait ran out                */
+} ct_status;
+
+typedef enum { CT_F32 = 0, CT_BF16 = 1 } ct_dtype;
+
+/* Output length of one spatial dimension ([l1_p79] output-length formula),
+ * or -1 if the parameters are invalid (k, s, dl < 1; p, op < 0; result < 1). */
+int64_t ct_out_len(int64_t L_in, int k, int s, int p, int op, int dl);
+
+/* Scratch bytes a forward call with these arguments needs (0 for the FP32
+ * paths).  Same argument meaning as the forward calls below. */
+ct_status ct_workspace_size_1d(int N, int C_in, int C_out, int L_in, int k, int groups,
+                               int stride, int padding, int output_padding, int dilation,
+                               ct_dtype dtype, size_t *bytes);
+ct_status ct_workspace_size_3d(int N, int C_in, int C_out, const int in_dhw[3],
+                               const int k_dhw[3], int groups, const int stride[3],
+                               const int padding[3], const int output_padding[3],
+                               const int dilation[3], ct_dtype dtype, size_t *bytes);
+
+/* ConvTranspose1d forward ([l1_p79]).  x (N, C_in, L_in), w (C_in,
+ * C_out/groups, k), bias (C_out) or NULL, y (N, C_out, L_out) fp32. */
+ct_status ct_forward_1d(const void *x, const void *w, const float *bias, float *y,
+                        int N, int C_in, int C_out, int L_in, int k, int groups,
+                        int stride, int padding, int output_padding, int dilation,
+                        ct_dtype dtype, void *workspace, size_t ws_bytes, void *stream);
+
+/* ConvTranspose3d forward ([l1_p72]).  in_dhw = (D, H, W) of x, k_dhw the
+ * kernel extent; stride, padding, output_padding, dilation per (D, H, W). */
+ct_status ct_forward_3d(const void *x, const void *w, const float *bias, float *y,
+                        int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
+                        int groups, const int stride[3], const int padding[3],
+                        const int output_padding[3], const int dilation[3],
+                        ct_dtype dtype, void *workspace, size_t ws_bytes, void *stream);
+
+/* Fused ConvTranspose3d + add + x*hardswish(x) ([l2_p26]):
+ *     t = convT(x) + bias + add;  y = t * (t * clamp(t + 3, 0, 6) / 6).
+ * add has the shape of y (fp32) and must not be NULL; y may equal add. */
+ct_status ct_forward_3d_add_hswish(const void *x, const void *w, const float *bias,
+                                   const float *add, float *y,
+                                   int N, int C_in, int C_out, const int in_dhw[3],
+                                   const int k_dhw[3], int groups, const int stride[3],
+                                   const int padding[3], const int output_padding[3],
+                                   const int dilation[3], ct_dtype dtype,
+                                   void *workspace, size_t ws_bytes, void *stream);
+
+/* Name of the kernel family the 1-D / 3-D / fused call with these arguments
+ * would launch ("gather_generic", "phase1d_f32", "phase3d_f32", "umma_bf16",
+ * ...), or NULL if the arguments are invalid.  Host only; launches nothing.
+ * `fused` selects the add + hardswish variant for the 3-D query. */
+const char *ct_path_1d(int N, int C_in, int C_out, int L_in, int k, int groups, int stride,
+                       int padding, int output_padding, int dilation, ct_dtype dtype);
+const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
+                       int groups, const int stride[3], const int padding[3],
+                       const int output_padding[3], const int dilation[3], ct_dtype dtype,
+                       int fused);
+
+/* Process-wide path override for testing the dispatcher: 0 = automatic
+ * (default), 1 = always use the generic gather kernel.  Not thread-safe
+ * against concurrent forward calls. */
+void ct_set_path_override(int mode);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *ct_status_str(ct_status s);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device: CT_OK, or CT_ERR_DEVICE_TIMEOUT if a bounded wait in a
+ * kernel ran out since the last query; CT_ERR_CUDA if synchronising failed. */
+ct_status ct_last_device_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CT_H */

@@ -1,0 +1,131 @@
+"""Host-side tests of the C ABI (no GPU): the library loads, exports every
+symbol include/ct.h declares, validates arguments before any launch, and its
+host logic (output lengths, kernel selection, workspace sizes) is right."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as ora
+import transposed_convolution_convtranspose_gb300 as ct
+from transposed_convolution_convtranspose_gb300 import build as ctbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ctbuild.build()
+    return ct.load()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(ct_\w+)\s*\(", txt))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert {"ct_forward_1d", "ct_forward_3d", "ct_forward_3d_add_hswish"} <= syms
+    raw = ctypes.CDLL(ct.LIB_PATH)
+    for s in sorted(syms):
+        assert hasattr(raw, s), "libct.so does not export %s" % s
+    assert set(ct.EXPORTED) <= syms
+
+
+def test_binding_names_match_abi(lib):
+    for s in declared_symbols():
+        assert hasattr(ct, s), "binding lacks %s" % s
+
+
+def test_out_len_matches_oracle(lib):
+    rng = np.random.default_rng(0)
+    for _ in range(2000):
+        L, k, s, p, dl = (int(rng.integers(1, 50)), int(rng.integers(1, 8)), int(rng.integers(1, 5)),
+                          int(rng.integers(0, 6)), int(rng.integers(1, 4)))
+        op = int(rng.integers(0, max(s, dl)))
+        want = ora.out_len(L, k, s, p, op, dl)
+        got = ct.ct_out_len(L, k, s, p, op, dl)
+        assert got == (want if want >= 1 else -1)
+    assert ct.ct_out_len(131072, 3, 2, 1, 0, 2) == 262145
+    assert ct.ct_out_len(0, 3, 2, 1, 0, 2) == -1
+    assert ct.ct_out_len(4, 0, 2, 1, 0, 2) == -1
+
+
+FAKE = 0x10000000   # never dereferenced: every call below fails validation first
+
+
+def call1d(lib, **kw):
+    a = dict(x=FAKE, w=FAKE + (1 << 24), bias=None, y=FAKE + (1 << 26), N=2, C_in=4, C_out=8,
+             L_in=16, k=3, groups=1, stride=2, padding=1, output_padding=0, dilation=2,
+             dtype=ct.CT_F32)
+    a.update(kw)
+    return lib.ct_forward_1d(a["x"], a["w"], a["bias"], a["y"], a["N"], a["C_in"], a["C_out"],
+                             a["L_in"], a["k"], a["groups"], a["stride"], a["padding"],
+                             a["output_padding"], a["dilation"], a["dtype"], None, 0, None)
+
+
+def test_argument_errors_before_launch(lib):
+    assert call1d(lib, x=None) == 1
+    assert call1d(lib, y=None) == 1
+    assert call1d(lib, dtype=7) == 1
+    assert call1d(lib, C_in=0) == 1
+    assert call1d(lib, groups=3) == 2            # 3 does not divide 4
+    assert call1d(lib, k=0) == 2
+    assert call1d(lib, stride=0) == 2
+    assert call1d(lib, padding=-1) == 2
+    assert call1d(lib, output_padding=2) == 2    # op >= max(s, dl)
+    assert call1d(lib, L_in=1, k=1, padding=1) == 2   # L_out <= 0
+    assert call1d(lib, x=FAKE + 2) == 3          # misaligned fp32
+    assert call1d(lib, y=FAKE + 16) == 1         # y overlaps x
+    assert call1d(lib, N=0) == 0                 # empty batch: valid, nothing launched
+
+
+def test_fused_requires_add(lib):
+    i3 = ct._I3
+    st = lib.ct_forward_3d_add_hswish(FAKE, FAKE + (1 << 24), None, None, FAKE + (1 << 26), 1, 4,
+                                      4, i3(2, 2, 2), i3(3, 3, 3), 1, i3(2, 2, 2), i3(1, 1, 1),
+                                      i3(1, 1, 1), i3(1, 1, 1), ct.CT_F32, None, 0, None)
+    assert st == 1
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert ct.ct_status_str(code).startswith(ct.CT_STATUS[code])
+
+
+def test_path_selection(lib):
+    # the tiny and the long 1-D workloads
+    for N, L in ((2, 64), (16, 131072)):
+        p = ct.ct_path_1d(N, 32 if N == 16 else 4, 64 if N == 16 else 8, L, 3, 1, 2, 1, 0, 2, ct.CT_F32)
+        assert p in ("phase1d_f32", "gather_generic")
+    assert ct.ct_path_1d(1, 4, 8, 0, 3, 1, 2, 1, 0, 2, ct.CT_F32) is None
+    p3 = ct.ct_path_3d(8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3), (1, 1, 1),
+                       (1, 1, 1), ct.CT_F32)
+    assert p3 in ("phase3d_f32", "gather_generic")
+    ct.ct_set_path_override(1)
+    try:
+        assert ct.ct_path_3d(8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3),
+                             (1, 1, 1), (1, 1, 1), ct.CT_F32) == "gather_generic"
+    finally:
+        ct.ct_set_path_override(0)
+
+
+def test_workspace_sizes(lib):
+    assert ct.ct_workspace_size_1d(16, 32, 64, 131072, 3, 1, 2, 1, 0, 2, ct.CT_F32) == 0
+    nb = ct.ct_workspace_size_3d(16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1),
+                                 (0, 0, 0), (1, 1, 1), ct.CT_BF16)
+    path = ct.ct_path_3d(16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1),
+                         (0, 0, 0), (1, 1, 1), ct.CT_BF16)
+    if path == "umma_bf16":
+        # channels-last x copy plus phase-packed weights, both bf16
+        assert nb >= 16 * 256 * 16 ** 3 * 2 + 8 * 128 * 8 * 256 * 2
+    else:
+        assert nb == 0

@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  fp32: |err| <= 1e-4 (1 + |ref|); bf16 inputs with fp32
+accumulation: |err| <= 2e-2 (|ref| + rms(ref)); integer-valued inputs: exact."""
+import numpy as np
+import pytest
+
+import ctcase as cc
+import oracle_pins
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = workloads.CONFIG_ORDER
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from transposed_convolution_convtranspose_gb300 import build
+    build.build()
+    import transposed_convolution_convtranspose_gb300 as ct
+    ct.load()
+    torch.cuda.set_device(0)
+    yield
+    ct.ct_last_device_error(torch.cuda.current_stream())
+
+
+def _sync():
+    import torch
+    torch.cuda.synchronize()
+
+
+def path_of(c):
+    import transposed_convolution_convtranspose_gb300 as ct
+    dt = ct.CT_BF16 if c["dtype"] == "bf16" else ct.CT_F32
+    if c["nd"] == 1:
+        return ct.ct_path_1d(c["N"], c["C_in"], c["C_out"], c["L"][0], c["K"][0], c["G"], c["S"][0],
+                             c["P"][0], c["OP"][0], c["DL"][0], dt)
+    return ct.ct_path_3d(c["N"], c["C_in"], c["C_out"], c["L"], c["K"], c["G"], c["S"], c["P"],
+                         c["OP"], c["DL"], dt, c["add"])
+
+
+# Reduced-batch versions of every workload, compared element by element.  The
+# bf16 workload is also reduced in space (8^3 input) so the scatter oracle
+# finishes in seconds; its full spatial size is covered by the sampled test.
+REDUCED = {"convT1d_tiny": dict(N=2), "convT1d_L131072": dict(N=1),
+           "convT3d_grouped": dict(N=2), "convT3d_add_hswish": dict(N=2),
+           "convT3d_bf16_dense": dict(N=1, L=[8, 8, 8])}
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_config_reduced_full_compare(name):
+    c = cc.case_from_config(name, N=REDUCED[name]["N"])
+    if "L" in REDUCED[name]:
+        c["L"] = REDUCED[name]["L"]
+    t = cc.make_inputs(c, seed=100 + CONFIGS.index(name), bound=workloads.CONFIGS[name]["bound"])
+    y = cc.run_gpu(c, t).cpu().numpy()
+    ref = cc.run_oracle(c, t)
+    cc.assert_close(y, ref, c["dtype"], "%s reduced (%s)" % (name, path_of(c)))
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_config_integer_exact(name):
+    """Integer inputs in [-3, 3]: every partial sum is an integer below 2^24,
+    so the conv + bias result is exact in any order (the fused epilogue's
+    division by 6 is compared at fp32 tolerance instead)."""
+    c = cc.case_from_config(name, N=1)
+    if name == "convT3d_bf16_dense":
+        c["L"] = [8, 8, 8]
+    t = cc.make_inputs(c, seed=200 + CONFIGS.index(name), int_range=3)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    ref = cc.run_oracle(c, t)
+    if c["add"]:
+        cc.assert_close(y, ref, "f32", name)
+    else:
+        assert y.shape == ref.shape
+        assert np.array_equal(y.astype(np.float64), ref), "%s: not bit-exact (%s)" % (name, path_of(c))
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_config_full_size_sampled(name):
+    """The exact workload shapes, through the same entry point the benchmark
+    times, checked on sampled outputs (plus corners) by the pointwise oracle."""
+    import torch
+    c = cc.case_from_config(name)
+    t = workloads.config_inputs(name)
+    y = cc.run_gpu(c, t)
+    _sync()
+    shape = cc.out_shape(c)
+    assert list(y.shape) == shape
+    idx = cc.sample_indices(shape, 3000, seed=7)
+    got = y.reshape(-1)[torch.from_numpy(idx).to(y.device)].cpu().numpy()
+    ref = cc.oracle_at(c, t, idx)
+    cc.assert_close(got, ref, c["dtype"], "%s full size sampled (%s)" % (name, path_of(c)))
+    assert bool(torch.isfinite(y).all())
+    if name in ("convT1d_tiny", "convT1d_L131072"):
+        # no tap lands on an even output for (k3, s2, p1, d2): bias or exactly 0
+        ev = y[:, :, 0::2]
+        want = (torch.from_numpy(t["bias"]).to(y.device)[None, :, None].expand_as(ev)
+                if t["bias"] is not None else torch.zeros_like(ev))
+        assert torch.equal(ev, want)
+    del y
+    torch.cuda.empty_cache()
+
+
+def _random_cases(n, seed, nd_choices=(1, 3), scale=1):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        nd = nd_choices[i % len(nd_choices)]
+        r = oracle_pins.random_case(rng, nd)
+        c = dict(nd=nd, N=r["N"], C_in=r["C_in"] * scale, C_out=r["C_out"] * scale, G=r["G"],
+                 L=[v * (3 if nd == 1 else 1) for v in r["L"]], K=r["K"], S=r["S"], P=r["P"],
+                 OP=r["OP"], DL=r["DL"], bias=bool(i % 2), add=False, dtype="f32")
+        # recheck validity after scaling L
+        Lo = cc.out_shape(c)
+        if min(Lo[2:]) >= 1:
+            out.append(c)
+    return out
+
+
+@pytest.mark.parametrize("forced_generic", [False, True])
+def test_random_small_shapes(forced_generic):
+    import transposed_convolution_convtranspose_gb300 as ct
+    cases = _random_cases(80, seed=31) + _random_cases(20, seed=32, scale=4)
+    ct.ct_set_path_override(1 if forced_generic else 0)
+    try:
+        for k, c in enumerate(cases):
+            t = cc.make_inputs(c, seed=300 + k)
+            y = cc.run_gpu(c, t).cpu().numpy()
+            cc.assert_close(y, cc.run_oracle(c, t), "f32", "random case %d %r" % (k, c))
+    finally:
+        ct.ct_set_path_override(0)
+
+
+def test_random_fused_and_bf16_generic():
+    cases = []
+    for k, c in enumerate(_random_cases(30, seed=41, nd_choices=(3,))):
+        c = dict(c)
+        if k % 2:
+            c["add"] = True
+        else:
+            c["dtype"] = "bf16"
+        cases.append(c)
+    for k, c in enumerate(cases):
+        t = cc.make_inputs(c, seed=400 + k)
+        y = cc.run_gpu(c, t).cpu().numpy()
+        cc.assert_close(y, cc.run_oracle(c, t), c["dtype"], "case %d %r" % (k, c))
+
+
+EDGE = [
+    # 1-D: single input, unit kernel, stride larger than kernel (empty phases),
+    # large dilation, maximal output_padding, depthwise groups, ragged lengths
+    dict(nd=1, N=1, C_in=1, C_out=1, G=1, L=[1], K=[1], S=[1], P=[0], OP=[0], DL=[1]),
+    dict(nd=1, N=3, C_in=2, C_out=4, G=1, L=[7], K=[2], S=[5], P=[0], OP=[4], DL=[1]),
+    dict(nd=1, N=2, C_in=6, C_out=6, G=6, L=[33], K=[3], S=[2], P=[1], OP=[1], DL=[1]),
+    dict(nd=1, N=1, C_in=4, C_out=8, G=2, L=[50], K=[4], S=[3], P=[2], OP=[3], DL=[4]),
+    dict(nd=1, N=2, C_in=32, C_out=64, G=1, L=[4999], K=[3], S=[2], P=[1], OP=[0], DL=[2]),
+    dict(nd=1, N=1, C_in=32, C_out=64, G=1, L=[1], K=[3], S=[2], P=[1], OP=[0], DL=[2]),
+    dict(nd=1, N=1, C_in=32, C_out=64, G=1, L=[2], K=[3], S=[2], P=[1], OP=[1], DL=[2]),
+    # 3-D: unit spatial dims, asymmetric everything, kernel 1, ragged W
+    dict(nd=3, N=1, C_in=2, C_out=3, G=1, L=[1, 1, 1], K=[1, 1, 1], S=[1, 1, 1], P=[0, 0, 0],
+         OP=[0, 0, 0], DL=[1, 1, 1]),
+    dict(nd=3, N=2, C_in=4, C_out=6, G=2, L=[3, 4, 5], K=[2, 3, 4], S=[3, 1, 2], P=[1, 0, 2],
+         OP=[2, 0, 1], DL=[1, 2, 1]),
+    dict(nd=3, N=1, C_in=32, C_out=32, G=4, L=[5, 7, 9], K=[3, 5, 7], S=[2, 2, 2], P=[1, 2, 3],
+         OP=[1, 1, 1], DL=[1, 1, 1]),
+    dict(nd=3, N=1, C_in=32, C_out=64, G=1, L=[3, 5, 7], K=[3, 3, 3], S=[2, 2, 2], P=[1, 1, 1],
+         OP=[1, 1, 1], DL=[1, 1, 1]),
+    dict(nd=3, N=1, C_in=32, C_out=64, G=1, L=[1, 1, 1], K=[3, 3, 3], S=[2, 2, 2], P=[1, 1, 1],
+         OP=[1, 1, 1], DL=[1, 1, 1]),
+]
+
+
+@pytest.mark.parametrize("k", range(len(EDGE)))
+@pytest.mark.parametrize("bias", [False, True])
+def test_edge_cases(k, bias):
+    c = dict(EDGE[k], bias=bias, add=False, dtype="f32")
+    t = cc.make_inputs(c, seed=500 + k)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), "f32", "edge %d (%s)" % (k, path_of(c)))
+
+
+def test_fused_in_place_and_edges():
+    for k, shape in enumerate([[2, 3, 4], [1, 1, 1], [5, 3, 16]]):
+        c = dict(nd=3, N=2, C_in=32, C_out=64, G=1, L=shape, K=[3, 3, 3], S=[2, 2, 2],
+                 P=[1, 1, 1], OP=[1, 1, 1], DL=[1, 1, 1], bias=True, add=True, dtype="f32")
+        t = cc.make_inputs(c, seed=600 + k)
+        ref = cc.run_oracle(c, t)
+        y = cc.run_gpu(c, t, inplace_add=True).cpu().numpy()
+        cc.assert_close(y, ref, "f32", "fused in place %r (%s)" % (shape, path_of(c)))
+
+
+def test_empty_batch_is_a_no_op():
+    import torch
+    import transposed_convolution_convtranspose_gb300 as ct
+    x = torch.zeros((0, 4, 16), device="cuda")
+    w = torch.ones((4, 8, 3), device="cuda")
+    y = torch.full((0, 8, 33), 5.0, device="cuda")
+    ct.ct_forward_1d(x, w, None, y, 0, 4, 8, 16, 3, 1, 2, 1, 0, 2, ct.CT_F32)
+    ct.ct_last_device_error(torch.cuda.current_stream())
+
+
+def test_repeat_is_deterministic():
+    name = "convT3d_add_hswish"
+    c = cc.case_from_config(name, N=2)
+    t = cc.make_inputs(c, seed=700)
+    y1 = cc.run_gpu(c, t)
+    y2 = cc.run_gpu(c, t)
+    import torch
+    assert torch.equal(y1, y2)

@@ -1,0 +1,302 @@
+"""Python binding of libct.so, the GB300 (sm_103a) forward transposed-convolution library.
+
+The functions named ``ct_*`` are the C entry points of ``include/ct.h`` with
+the same names and arguments; they only marshal arguments (a device pointer
+may be given as an int or as a torch tensor, whose ``data_ptr()`` is used) and
+raise :class:`CTError` on a non-zero status.  Every step of the computation
+runs in the library's CUDA kernels.  The ``conv_transpose*`` helpers allocate
+the fp32 output (and the workspace, if the chosen path needs one) with torch
+and call the corresponding entry point on torch's current stream.
+
+There is no fallback: if ``libct.so`` has not been built, every call raises.
+Build it with ``python -m transposed_convolution_convtranspose_gb300.build``.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libct.so")
+
+CT_F32 = 0
+CT_BF16 = 1
+
+CT_STATUS = {0: "CT_OK", 1: "CT_ERR_ARG", 2: "CT_ERR_SHAPE", 3: "CT_ERR_ALIGN",
+             4: "CT_ERR_WORKSPACE", 5: "CT_ERR_UNSUPPORTED", 6: "CT_ERR_CUDA",
+             7: "CT_ERR_DEVICE_TIMEOUT"}
+
+EXPORTED = ["ct_out_len", "ct_workspace_size_1d", "ct_workspace_size_3d", "ct_forward_1d",
+            "ct_forward_3d", "ct_forward_3d_add_hswish", "ct_path_1d", "ct_path_3d",
+            "ct_set_path_override", "ct_status_str", "ct_last_device_error"]
+
+
+class CTError(RuntimeError):
+    def __init__(self, code, where=""):
+        self.code = int(code)
+        self.name = CT_STATUS.get(self.code, "unknown")
+        msg = _status_str(self.code)
+        super().__init__("%s%s" % (where + ": " if where else "", msg))
+
+
+_lib = None
+_load_error = None
+
+_I = ctypes.c_int
+_P = ctypes.c_void_p
+_I3 = ctypes.c_int * 3
+
+
+def _setup(lib):
+    lib.ct_out_len.restype = ctypes.c_int64
+    lib.ct_out_len.argtypes = [ctypes.c_int64, _I, _I, _I, _I, _I]
+    lib.ct_workspace_size_1d.restype = _I
+    lib.ct_workspace_size_1d.argtypes = [_I] * 10 + [_I, ctypes.POINTER(ctypes.c_size_t)]
+    lib.ct_workspace_size_3d.restype = _I
+    lib.ct_workspace_size_3d.argtypes = [_I, _I, _I, _I3, _I3, _I, _I3, _I3, _I3, _I3, _I,
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.ct_forward_1d.restype = _I
+    lib.ct_forward_1d.argtypes = [_P, _P, _P, _P] + [_I] * 10 + [_I, _P, ctypes.c_size_t, _P]
+    lib.ct_forward_3d.restype = _I
+    lib.ct_forward_3d.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I3, _I3, _I, _I3, _I3, _I3, _I3,
+                                  _I, _P, ctypes.c_size_t, _P]
+    lib.ct_forward_3d_add_hswish.restype = _I
+    lib.ct_forward_3d_add_hswish.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I3, _I3, _I, _I3,
+                                             _I3, _I3, _I3, _I, _P, ctypes.c_size_t, _P]
+    lib.ct_path_1d.restype = ctypes.c_char_p
+    lib.ct_path_1d.argtypes = [_I] * 10 + [_I]
+    lib.ct_path_3d.restype = ctypes.c_char_p
+    lib.ct_path_3d.argtypes = [_I, _I, _I, _I3, _I3, _I, _I3, _I3, _I3, _I3, _I, _I]
+    lib.ct_set_path_override.restype = None
+    lib.ct_set_path_override.argtypes = [_I]
+    lib.ct_status_str.restype = ctypes.c_char_p
+    lib.ct_status_str.argtypes = [_I]
+    lib.ct_last_device_error.restype = _I
+    lib.ct_last_device_error.argtypes = [_P]
+    return lib
+
+
+def load(path=LIB_PATH):
+    """Load (or return the already loaded) libct.so; raises if it is missing."""
+    global _lib, _load_error
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libct.so is not built (%s); run `python -m "
+                           "transposed_convolution_convtranspose_gb300.build`" % path)
+    _lib = _setup(ctypes.CDLL(path))
+    return _lib
+
+
+def _status_str(code):
+    try:
+        return load().ct_status_str(int(code)).decode()
+    except Exception:
+        return CT_STATUS.get(int(code), "status %d" % int(code))
+
+
+def _ptr(v):
+    if v is None:
+        return None
+    if isinstance(v, int):
+        return v or None
+    return v.data_ptr() or None   # torch tensor
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None  # torch.cuda.Stream
+
+
+def _i3(v):
+    v = tuple(int(t) for t in v)
+    if len(v) != 3:
+        raise ValueError("expected 3 values (D, H, W)")
+    return _I3(*v)
+
+
+def _check(code, where):
+    if code != 0:
+        raise CTError(code, where)
+
+
+# ------------------------------------------------------------------ raw ABI
+def ct_out_len(L_in, k, s, p, op, dl):
+    return int(load().ct_out_len(int(L_in), int(k), int(s), int(p), int(op), int(dl)))
+
+
+def ct_workspace_size_1d(N, C_in, C_out, L_in, k, groups, stride, padding, output_padding,
+                         dilation, dtype):
+    out = ctypes.c_size_t(0)
+    _check(load().ct_workspace_size_1d(N, C_in, C_out, L_in, k, groups, stride, padding,
+                                       output_padding, dilation, dtype, ctypes.byref(out)),
+           "ct_workspace_size_1d")
+    return int(out.value)
+
+
+def ct_workspace_size_3d(N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding,
+                         output_padding, dilation, dtype):
+    out = ctypes.c_size_t(0)
+    _check(load().ct_workspace_size_3d(N, C_in, C_out, _i3(in_dhw), _i3(k_dhw), groups,
+                                       _i3(stride), _i3(padding), _i3(output_padding),
+                                       _i3(dilation), dtype, ctypes.byref(out)),
+           "ct_workspace_size_3d")
+    return int(out.value)
+
+
+def ct_forward_1d(x, w, bias, y, N, C_in, C_out, L_in, k, groups, stride, padding,
+                  output_padding, dilation, dtype, workspace=None, ws_bytes=0, stream=None):
+    _check(load().ct_forward_1d(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), N, C_in, C_out, L_in, k,
+                                groups, stride, padding, output_padding, dilation, dtype,
+                                _ptr(workspace), int(ws_bytes), _stream(stream)),
+           "ct_forward_1d")
+
+
+def ct_forward_3d(x, w, bias, y, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding,
+                  output_padding, dilation, dtype, workspace=None, ws_bytes=0, stream=None):
+    _check(load().ct_forward_3d(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), N, C_in, C_out,
+                                _i3(in_dhw), _i3(k_dhw), groups, _i3(stride), _i3(padding),
+                                _i3(output_padding), _i3(dilation), dtype, _ptr(workspace),
+                                int(ws_bytes), _stream(stream)),
+           "ct_forward_3d")
+
+
+def ct_forward_3d_add_hswish(x, w, bias, add, y, N, C_in, C_out, in_dhw, k_dhw, groups, stride,
+                             padding, output_padding, dilation, dtype, workspace=None,
+                             ws_bytes=0, stream=None):
+    _check(load().ct_forward_3d_add_hswish(_ptr(x), _ptr(w), _ptr(bias), _ptr(add), _ptr(y), N,
+                                           C_in, C_out, _i3(in_dhw), _i3(k_dhw), groups,
+                                           _i3(stride), _i3(padding), _i3(output_padding),
+                                           _i3(dilation), dtype, _ptr(workspace), int(ws_bytes),
+                                           _stream(stream)),
+           "ct_forward_3d_add_hswish")
+
+
+def ct_path_1d(N, C_in, C_out, L_in, k, groups, stride, padding, output_padding, dilation, dtype):
+    r = load().ct_path_1d(N, C_in, C_out, L_in, k, groups, stride, padding, output_padding,
+                          dilation, dtype)
+    return None if r is None else r.decode()
+
+
+def ct_path_3d(N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding, output_padding, dilation,
+               dtype, fused=False):
+    r = load().ct_path_3d(N, C_in, C_out, _i3(in_dhw), _i3(k_dhw), groups, _i3(stride),
+                          _i3(padding), _i3(output_padding), _i3(dilation), dtype, int(bool(fused)))
+    return None if r is None else r.decode()
+
+
+def ct_set_path_override(mode):
+    load().ct_set_path_override(int(mode))
+
+
+def ct_status_str(code):
+    return load().ct_status_str(int(code)).decode()
+
+
+def ct_last_device_error(stream=None):
+    code = load().ct_last_device_error(_stream(stream))
+    _check(code, "ct_last_device_error")
+
+
+# ------------------------------------------------------------------ helpers (torch allocation)
+def _triple(v):
+    if isinstance(v, int):
+        return (v, v, v)
+    v = tuple(int(t) for t in v)
+    if len(v) != 3:
+        raise ValueError("expected an int or 3 values")
+    return v
+
+
+def _need(t, name):
+    if t is None:
+        return
+    if not t.is_cuda or not t.is_contiguous():
+        raise CTError(1, "%s must be a contiguous CUDA tensor" % name)
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return CT_F32
+    if t.dtype == torch.bfloat16:
+        return CT_BF16
+    raise TypeError("x and w must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _workspace(nbytes, device):
+    import torch
+    if nbytes == 0:
+        return None
+    # 256-byte aligned: torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def conv_transpose1d(x, w, bias=None, stride=1, padding=0, output_padding=0, dilation=1,
+                     groups=1, out=None):
+    import torch
+    for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (out, "out")):
+        _need(t, nm)
+    N, C_in, L_in = x.shape
+    k = w.shape[2]
+    C_out = w.shape[1] * groups
+    dt = _dtype_code(x)
+    L_out = ct_out_len(L_in, k, stride, padding, output_padding, dilation)
+    if L_out < 1:
+        raise CTError(2, "conv_transpose1d")
+    y = out if out is not None else torch.empty((N, C_out, L_out), dtype=torch.float32,
+                                                device=x.device)
+    nb = ct_workspace_size_1d(N, C_in, C_out, L_in, k, groups, stride, padding, output_padding,
+                              dilation, dt)
+    ws = _workspace(nb, x.device)
+    ct_forward_1d(x, w, bias, y, N, C_in, C_out, L_in, k, groups, stride, padding,
+                  output_padding, dilation, dt, ws, nb, torch.cuda.current_stream(x.device))
+    return y
+
+
+def _out3(x, w, groups, stride, padding, output_padding, dilation):
+    S, P, OP, D = _triple(stride), _triple(padding), _triple(output_padding), _triple(dilation)
+    K = tuple(w.shape[2:])
+    L = tuple(x.shape[2:])
+    Lo = tuple(ct_out_len(L[i], K[i], S[i], P[i], OP[i], D[i]) for i in range(3))
+    if min(Lo) < 1:
+        raise CTError(2, "conv_transpose3d")
+    return S, P, OP, D, K, L, Lo
+
+
+def conv_transpose3d(x, w, bias=None, stride=1, padding=0, output_padding=0, dilation=1,
+                     groups=1, out=None):
+    import torch
+    for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (out, "out")):
+        _need(t, nm)
+    N, C_in = x.shape[:2]
+    C_out = w.shape[1] * groups
+    dt = _dtype_code(x)
+    S, P, OP, D, K, L, Lo = _out3(x, w, groups, stride, padding, output_padding, dilation)
+    y = out if out is not None else torch.empty((N, C_out) + Lo, dtype=torch.float32,
+                                                device=x.device)
+    nb = ct_workspace_size_3d(N, C_in, C_out, L, K, groups, S, P, OP, D, dt)
+    ws = _workspace(nb, x.device)
+    ct_forward_3d(x, w, bias, y, N, C_in, C_out, L, K, groups, S, P, OP, D, dt, ws, nb,
+                  torch.cuda.current_stream(x.device))
+    return y
+
+
+def conv_transpose3d_add_hswish(x, w, bias, add, stride=1, padding=0, output_padding=0,
+                                dilation=1, groups=1, out=None):
+    import torch
+    for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (add, "add"), (out, "out")):
+        _need(t, nm)
+    N, C_in = x.shape[:2]
+    C_out = w.shape[1] * groups
+    dt = _dtype_code(x)
+    S, P, OP, D, K, L, Lo = _out3(x, w, groups, stride, padding, output_padding, dilation)
+    if tuple(add.shape) != (N, C_out) + Lo or add.dtype != torch.float32:
+        raise CTError(1, "conv_transpose3d_add_hswish: add must be fp32 with the output's shape")
+    y = out if out is not None else torch.empty_like(add)
+    nb = ct_workspace_size_3d(N, C_in, C_out, L, K, groups, S, P, OP, D, dt)
+    ws = _workspace(nb, x.device)
+    ct_forward_3d_add_hswish(x, w, bias, add, y, N, C_in, C_out, L, K, groups, S, P, OP, D, dt,
+                             ws, nb, torch.cuda.current_stream(x.device))
+    return y

@@ -1,0 +1,304 @@
+// ct_api.cu -- the C ABI of libct.so: argument validation, output shapes,
+// stride-phase tables, kernel selection and launch.  Declarations and the
+// contract of every entry point are in include/ct.h.
+#include <string.h>
+
+#include <atomic>
+
+#include "ct_internal.h"
+
+namespace ct {
+
+__device__ unsigned int g_ct_status;   // CT_OK or CT_ERR_DEVICE_TIMEOUT
+
+unsigned int *device_status_ptr()
+{
+    static unsigned int *cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ct_status) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<unsigned int *>(p);
+    }
+    return cache[dev];
+}
+
+// Output length of one dimension ([l1_p79] output-length formula).
+static int64_t out_len(int64_t L_in, int64_t k, int64_t s, int64_t p, int64_t op, int64_t dl)
+{
+    return (L_in - 1) * s - 2 * p + dl * (k - 1) + op + 1;
+}
+
+bool build_phase_dim(int L_out, int K, int S, int P, int DL, PhaseDim *pd)
+{
+    if (S < 1 || S > kMaxS) return false;
+    memset(pd, 0, sizeof(*pd));
+    pd->S = S;
+    for (int r = 0; r < S; ++r) {
+        pd->Q[r] = (r < L_out) ? (L_out - r + S - 1) / S : 0;
+        for (int k = 0; k < K; ++k) {
+            const int num = r + P - k * DL;
+            // floor-exact divisibility test, also for negative numerators
+            const int rem = ((num % S) + S) % S;
+            if (rem != 0) continue;
+            if (pd->ntap[r] >= kMaxTaps) return false;
+            pd->k[r][pd->ntap[r]] = k;
+            pd->delta[r][pd->ntap[r]] = (num - rem) / S;
+            ++pd->ntap[r];
+        }
+    }
+    return true;
+}
+
+static std::atomic<int> g_override{0};
+
+}  // namespace ct
+
+using namespace ct;
+
+namespace {
+
+constexpr int64_t kMaxDim = 1 << 30;
+
+ct_status make_problem(int nd, int N, int C_in, int C_out, const int *Li, const int *K, int G,
+                       const int *S, const int *P, const int *OP, const int *DL, ct_dtype dtype,
+                       bool has_bias, bool has_add, Problem *pb)
+{
+    if (nd != 1 && nd != 3) return CT_ERR_ARG;
+    if (dtype != CT_F32 && dtype != CT_BF16) return CT_ERR_ARG;
+    if (N < 0 || C_in < 1 || C_out < 1 || G < 1) return CT_ERR_ARG;
+    if (C_in % G || C_out % G) return CT_ERR_SHAPE;
+    Problem p;
+    p.nd = nd; p.N = N; p.C_in = C_in; p.C_out = C_out; p.G = G;
+    p.Cig = C_in / G; p.Cog = C_out / G;
+    p.dtype = dtype; p.has_bias = has_bias; p.has_add = has_add;
+    for (int d = 0; d < 3; ++d) {
+        p.Li[d] = 1; p.K[d] = 1; p.S[d] = 1; p.P[d] = 0; p.OP[d] = 0; p.DL[d] = 1; p.Lo[d] = 1;
+    }
+    for (int d = 0; d < nd; ++d) {
+        const int e = 3 - nd + d;
+        if (Li[d] < 1 || K[d] < 1 || S[d] < 1 || DL[d] < 1) return CT_ERR_SHAPE;
+        if (P[d] < 0 || OP[d] < 0) return CT_ERR_SHAPE;
+        if (OP[d] >= (S[d] > DL[d] ? S[d] : DL[d])) return CT_ERR_SHAPE;
+        const int64_t lo = out_len(Li[d], K[d], S[d], P[d], OP[d], DL[d]);
+        if (lo < 1) return CT_ERR_SHAPE;
+        if (lo > kMaxDim || Li[d] > kMaxDim) return CT_ERR_UNSUPPORTED;
+        p.Li[e] = Li[d]; p.K[e] = K[d]; p.S[e] = S[d]; p.P[e] = P[d]; p.OP[e] = OP[d];
+        p.DL[e] = DL[d]; p.Lo[e] = (int)lo;
+    }
+    // element counts must fit int64 comfortably
+    const double ye = (double)N * C_out * (double)p.Lo[0] * p.Lo[1] * p.Lo[2];
+    const double xe = (double)N * C_in * (double)p.Li[0] * p.Li[1] * p.Li[2];
+    if (ye > 4e18 || xe > 4e18) return CT_ERR_UNSUPPORTED;
+    *pb = p;
+    return CT_OK;
+}
+
+enum class Path { Generic, Phase1d, Phase3d, Umma };
+
+Path choose_path(const Problem &pb, const Args *a)
+{
+    if (g_override.load() == 1) return Path::Generic;
+    if (pb.dtype == CT_F32) {
+        if (pb.nd == 1 && phase1d_supported(pb, a)) return Path::Phase1d;
+        if (pb.nd == 3 && phase3d_supported(pb, a)) return Path::Phase3d;
+    } else {
+        if (pb.nd == 3 && umma_supported(pb, a)) return Path::Umma;
+    }
+    return Path::Generic;
+}
+
+const char *path_name(Path p)
+{
+    switch (p) {
+    case Path::Generic: return "gather_generic";
+    case Path::Phase1d: return "phase1d_f32";
+    case Path::Phase3d: return "phase3d_f32";
+    case Path::Umma: return "umma_bf16";
+    }
+    return "gather_generic";
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool overlaps(const void *a, size_t an, const void *b, size_t bn)
+{
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+ct_status run(const Problem &pb, Args a)
+{
+    const size_t esz = pb.dtype == CT_BF16 ? 2 : 4;
+    if (!a.x || !a.w || !a.y) return CT_ERR_ARG;
+    if (pb.has_add && !a.add) return CT_ERR_ARG;
+    if (!aligned(a.x, esz) || !aligned(a.w, esz) || !aligned(a.y, 4) ||
+        (a.bias && !aligned(a.bias, 4)) || (a.add && !aligned(a.add, 4)))
+        return CT_ERR_ALIGN;
+    const size_t yb = (size_t)pb.y_elems() * 4;
+    const size_t xb = (size_t)pb.x_elems() * esz;
+    const size_t wb = (size_t)pb.C_in * pb.Cog * pb.kvol() * esz;
+    if (overlaps(a.y, yb, a.x, xb) || overlaps(a.y, yb, a.w, wb) ||
+        (a.bias && overlaps(a.y, yb, a.bias, (size_t)pb.C_out * 4)))
+        return CT_ERR_ARG;
+    if (a.add && a.add != a.y && overlaps(a.y, yb, a.add, yb)) return CT_ERR_ARG;
+    if (pb.N == 0) return CT_OK;   // empty batch: nothing to compute
+
+    const Path path = choose_path(pb, &a);
+    if (path == Path::Umma) {
+        const size_t need = umma_workspace_bytes(pb);
+        if (a.ws_bytes < need || !a.ws || !aligned(a.ws, 256)) return CT_ERR_WORKSPACE;
+    }
+    cudaError_t e = cudaSuccess;
+    switch (path) {
+    case Path::Generic: e = launch_gather_generic(pb, a); break;
+    case Path::Phase1d: e = launch_phase1d(pb, a); break;
+    case Path::Phase3d: e = launch_phase3d(pb, a); break;
+    case Path::Umma: e = launch_umma(pb, a); break;
+    }
+    return e == cudaSuccess ? CT_OK : CT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t ct_out_len(int64_t L_in, int k, int s, int p, int op, int dl)
+{
+    if (L_in < 1 || k < 1 || s < 1 || dl < 1 || p < 0 || op < 0) return -1;
+    const int64_t lo = out_len(L_in, k, s, p, op, dl);
+    return lo >= 1 ? lo : -1;
+}
+
+ct_status ct_workspace_size_1d(int N, int C_in, int C_out, int L_in, int k, int groups,
+                               int stride, int padding, int output_padding, int dilation,
+                               ct_dtype dtype, size_t *bytes)
+{
+    if (!bytes) return CT_ERR_ARG;
+    Problem pb;
+    ct_status st = make_problem(1, N, C_in, C_out, &L_in, &k, groups, &stride, &padding,
+                                &output_padding, &dilation, dtype, false, false, &pb);
+    if (st != CT_OK) return st;
+    *bytes = choose_path(pb, nullptr) == Path::Umma ? umma_workspace_bytes(pb) : 0;
+    return CT_OK;
+}
+
+ct_status ct_workspace_size_3d(int N, int C_in, int C_out, const int in_dhw[3],
+                               const int k_dhw[3], int groups, const int stride[3],
+                               const int padding[3], const int output_padding[3],
+                               const int dilation[3], ct_dtype dtype, size_t *bytes)
+{
+    if (!bytes || !in_dhw || !k_dhw || !stride || !padding || !output_padding || !dilation)
+        return CT_ERR_ARG;
+    Problem pb;
+    ct_status st = make_problem(3, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding,
+                                output_padding, dilation, dtype, false, false, &pb);
+    if (st != CT_OK) return st;
+    *bytes = choose_path(pb, nullptr) == Path::Umma ? umma_workspace_bytes(pb) : 0;
+    return CT_OK;
+}
+
+ct_status ct_forward_1d(const void *x, const void *w, const float *bias, float *y,
+                        int N, int C_in, int C_out, int L_in, int k, int groups,
+                        int stride, int padding, int output_padding, int dilation,
+                        ct_dtype dtype, void *workspace, size_t ws_bytes, void *stream)
+{
+    Problem pb;
+    ct_status st = make_problem(1, N, C_in, C_out, &L_in, &k, groups, &stride, &padding,
+                                &output_padding, &dilation, dtype, bias != nullptr, false, &pb);
+    if (st != CT_OK) return st;
+    Args a{x, w, bias, nullptr, y, workspace, ws_bytes, (cudaStream_t)stream};
+    return run(pb, a);
+}
+
+ct_status ct_forward_3d(const void *x, const void *w, const float *bias, float *y,
+                        int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
+                        int groups, const int stride[3], const int padding[3],
+                        const int output_padding[3], const int dilation[3],
+                        ct_dtype dtype, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!in_dhw || !k_dhw || !stride || !padding || !output_padding || !dilation)
+        return CT_ERR_ARG;
+    Problem pb;
+    ct_status st = make_problem(3, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding,
+                                output_padding, dilation, dtype, bias != nullptr, false, &pb);
+    if (st != CT_OK) return st;
+    Args a{x, w, bias, nullptr, y, workspace, ws_bytes, (cudaStream_t)stream};
+    return run(pb, a);
+}
+
+ct_status ct_forward_3d_add_hswish(const void *x, const void *w, const float *bias,
+                                   const float *add, float *y,
+                                   int N, int C_in, int C_out, const int in_dhw[3],
+                                   const int k_dhw[3], int groups, const int stride[3],
+                                   const int padding[3], const int output_padding[3],
+                                   const int dilation[3], ct_dtype dtype,
+                                   void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!in_dhw || !k_dhw || !stride || !padding || !output_padding || !dilation)
+        return CT_ERR_ARG;
+    if (!add) return CT_ERR_ARG;
+    Problem pb;
+    ct_status st = make_problem(3, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding,
+                                output_padding, dilation, dtype, bias != nullptr, true, &pb);
+    if (st != CT_OK) return st;
+    Args a{x, w, bias, add, y, workspace, ws_bytes, (cudaStream_t)stream};
+    return run(pb, a);
+}
+
+const char *ct_path_1d(int N, int C_in, int C_out, int L_in, int k, int groups, int stride,
+                       int padding, int output_padding, int dilation, ct_dtype dtype)
+{
+    Problem pb;
+    if (make_problem(1, N, C_in, C_out, &L_in, &k, groups, &stride, &padding, &output_padding,
+                     &dilation, dtype, false, false, &pb) != CT_OK)
+        return nullptr;
+    return path_name(choose_path(pb, nullptr));
+}
+
+const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
+                       int groups, const int stride[3], const int padding[3],
+                       const int output_padding[3], const int dilation[3], ct_dtype dtype,
+                       int fused)
+{
+    if (!in_dhw || !k_dhw || !stride || !padding || !output_padding || !dilation) return nullptr;
+    Problem pb;
+    if (make_problem(3, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding, output_padding,
+                     dilation, dtype, false, fused != 0, &pb) != CT_OK)
+        return nullptr;
+    return path_name(choose_path(pb, nullptr));
+}
+
+void ct_set_path_override(int mode) { g_override.store(mode == 1 ? 1 : 0); }
+
+const char *ct_status_str(ct_status s)
+{
+    switch (s) {
+    case CT_OK: return "CT_OK";
+    case CT_ERR_ARG: return "CT_ERR_ARG: invalid argument (null pointer, bad size, dtype or overlap)";
+    case CT_ERR_SHAPE: return "CT_ERR_SHAPE: inconsistent shape or convolution parameters";
+    case CT_ERR_ALIGN: return "CT_ERR_ALIGN: pointer not aligned to its element size";
+    case CT_ERR_WORKSPACE: return "CT_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    case CT_ERR_UNSUPPORTED: return "CT_ERR_UNSUPPORTED: valid operator not supported by this build";
+    case CT_ERR_CUDA: return "CT_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case CT_ERR_DEVICE_TIMEOUT: return "CT_ERR_DEVICE_TIMEOUT: a bounded device-side wait ran out";
+    }
+    return "unknown ct_status";
+}
+
+ct_status ct_last_device_error(void *stream)
+{
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CT_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_ct_status, sizeof(v)) != cudaSuccess) return CT_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_ct_status, &zero, sizeof(zero)) != cudaSuccess) return CT_ERR_CUDA;
+        return CT_ERR_DEVICE_TIMEOUT;
+    }
+    return CT_OK;
+}
+
+}  // extern "C"

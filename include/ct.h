@@ -29,6 +29,8 @@
  *     bias (C_out,)  fp32, may be NULL
  *     add  shape of y, fp32 (fused entry point only)
  *     y    (N, C_out, L_out) or (N, C_out, D_out, H_out, W_out), always fp32
+ * N may be 0: the call then validates the other arguments, launches nothing
+ * and accepts NULL x, y and add.
  * y must not overlap x, w or bias.  y may be the same buffer as add (each
  * element of add is read before the same thread writes that element of y).
  *

@@ -132,6 +132,7 @@ bool overlaps(const void *a, size_t an, const void *b, size_t bn)
 ct_status run(const Problem &pb, Args a)
 {
     const size_t esz = pb.dtype == CT_BF16 ? 2 : 4;
+    if (pb.N == 0) return CT_OK;   // empty batch: nothing to compute, x/y may be NULL
     if (!a.x || !a.w || !a.y) return CT_ERR_ARG;
     if (pb.has_add && !a.add) return CT_ERR_ARG;
     if (!aligned(a.x, esz) || !aligned(a.w, esz) || !aligned(a.y, 4) ||
@@ -144,7 +145,6 @@ ct_status run(const Problem &pb, Args a)
         (a.bias && overlaps(a.y, yb, a.bias, (size_t)pb.C_out * 4)))
         return CT_ERR_ARG;
     if (a.add && a.add != a.y && overlaps(a.y, yb, a.add, yb)) return CT_ERR_ARG;
-    if (pb.N == 0) return CT_OK;   // empty batch: nothing to compute
 
     const Path path = choose_path(pb, &a);
     if (path == Path::Umma) {

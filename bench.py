@@ -1,0 +1,591 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 transposed-convolution library.
+
+Default workload: ConvTranspose1d fp32, N=16, C_in=32, C_out=64, k=3, s=2,
+p=1, d=2, L_in=131072 (L_out=262145), no bias -- inputs resident in HBM, one
+step = one forward pass over the whole batch through the C ABI.
+
+Prints ONE JSON line (rank 0).  `value` is throughput in GFLOP/s of
+algorithmic work (2 x the multiply-adds whose tap lands inside the output),
+summed over ranks; GB/s of algorithmic bytes (every tensor read or written
+once) is reported beside it.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.  `--table` prints one line per
+workload (the five sizes of the workload set) for the roofline table.
+
+Multi-GPU (torchrun): every rank runs the full workload on its own GPU
+(independent replicas, weak scaling), barrier + synchronise around the
+timed region, time = max over ranks, value = units of all ranks / time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+HEADLINE = "convT1d_L131072"
+METRIC = "ConvTranspose fwd GFLOP/s (and GB/s) on 1 GB300; % of roofline vs CPU oracle"
+L2_BYTES = 129 * 1024 * 1024
+SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+# ----------------------------------------------------------------------------- work model
+def out_len(L, k, s, p, op, d):
+    return (L - 1) * s - 2 * p + d * (k - 1) + op + 1
+
+
+def landed_pairs(L_in, k, s, p, op, d):
+    """Number of (input position, tap) pairs of one dimension whose target
+    o = i*s - p + k*d lies inside [0, L_out)."""
+    Lo = out_len(L_in, k, s, p, op, d)
+    n = 0
+    for kk in range(k):
+        # i in [0, L_in) with 0 <= i*s - p + kk*d < Lo
+        lo = max(0, -(-(p - kk * d) // s))
+        hi = min(L_in - 1, (Lo - 1 + p - kk * d) // s)
+        n += max(0, hi - lo + 1)
+    return n
+
+
+def work_model(cfg, N=None):
+    """Algorithmic FLOPs (2 per landed multiply-add) and bytes (each tensor
+    read or written once) of one forward pass."""
+    N = cfg["N"] if N is None else N
+    nd = cfg["nd"]
+    pairs = 1
+    Lo = []
+    for d in range(nd):
+        args = (cfg["L_in"][d], cfg["k"][d], cfg["stride"][d], cfg["padding"][d],
+                cfg["output_padding"][d], cfg["dilation"][d])
+        pairs *= landed_pairs(*args)
+        Lo.append(out_len(*args))
+    Cog = cfg["C_out"] // cfg["groups"]
+    macs = N * cfg["C_in"] * Cog * pairs
+    esz = 2 if cfg["dtype"] == "bf16" else 4
+    x_b = N * cfg["C_in"] * int(np.prod(cfg["L_in"])) * esz
+    w_b = cfg["C_in"] * Cog * int(np.prod(cfg["k"])) * esz
+    y_e = N * cfg["C_out"] * int(np.prod(Lo))
+    b_b = cfg["C_out"] * 4 if cfg["bias"] else 0
+    add_b = y_e * 4 if cfg["add"] else 0
+    return dict(flops=2 * macs, bytes=x_b + w_b + b_b + add_b + y_e * 4, x_bytes=x_b, w_bytes=w_b,
+                bias_bytes=b_b, add_bytes=add_b, y_bytes=y_e * 4, out_shape=[N, cfg["C_out"]] + Lo)
+
+
+# ----------------------------------------------------------------------------- peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)), source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_sustained=1700.0, sm_max_mhz=2070.0,
+                    source="fallback")
+
+
+def fp32_alu_peak_tflops(sm_mhz):
+    # FFMA: 128 FP32 lanes per SM, 2 FLOP per lane per clock
+    return SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for_smi(local):
+    """nvidia-smi -i accepts a UUID; torch's device index may differ from
+    nvidia-smi's numbering when only some GPUs are visible."""
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(local)
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value, ws):
+    """Max of a float over ranks (identity without a process group)."""
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(units_all_ranks, max_seconds):
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    return units_all_ranks / max_seconds if max_seconds > 0 else float("nan")
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def _inputs_to_device(cfg_name, dev, pinned=False):
+    import torch
+    t = workloads.config_inputs(cfg_name)
+    cfg = workloads.CONFIGS[cfg_name]
+    host = {}
+    if cfg["dtype"] == "bf16":
+        host["x"] = torch.from_numpy(t["x_bits"].view(np.int16)).view(torch.bfloat16)
+        host["w"] = torch.from_numpy(t["w_bits"].view(np.int16)).view(torch.bfloat16)
+    else:
+        host["x"] = torch.from_numpy(t["x"])
+        host["w"] = torch.from_numpy(t["w"])
+    host["bias"] = torch.from_numpy(t["bias"]) if t["bias"] is not None else None
+    host["add"] = torch.from_numpy(t["add"]) if t["add"] is not None else None
+    if pinned:
+        host = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
+    devt = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
+    return host, devt
+
+
+class Runner:
+    """One forward pass of a workload through the C ABI, buffers pre-allocated."""
+
+    def __init__(self, cfg_name, dev):
+        import torch
+        import transposed_convolution_convtranspose_gb300 as ct
+        self.ct = ct
+        self.cfg = workloads.CONFIGS[cfg_name]
+        self.name = cfg_name
+        self.dev = dev
+        self.host, self.d = _inputs_to_device(cfg_name, dev, pinned=True)
+        wm = work_model(self.cfg)
+        self.wm = wm
+        self.y = torch.empty(wm["out_shape"], dtype=torch.float32, device=dev)
+        self.y_host = torch.empty(wm["out_shape"], dtype=torch.float32).pin_memory()
+        c = self.cfg
+        self.dt = ct.CT_BF16 if c["dtype"] == "bf16" else ct.CT_F32
+        if c["nd"] == 1:
+            self.ws_bytes = ct.ct_workspace_size_1d(c["N"], c["C_in"], c["C_out"], c["L_in"][0], c["k"][0],
+                                                    c["groups"], c["stride"][0], c["padding"][0],
+                                                    c["output_padding"][0], c["dilation"][0], self.dt)
+            self.path = ct.ct_path_1d(c["N"], c["C_in"], c["C_out"], c["L_in"][0], c["k"][0],
+                                      c["groups"], c["stride"][0], c["padding"][0],
+                                      c["output_padding"][0], c["dilation"][0], self.dt)
+        else:
+            self.ws_bytes = ct.ct_workspace_size_3d(c["N"], c["C_in"], c["C_out"], c["L_in"], c["k"],
+                                                    c["groups"], c["stride"], c["padding"],
+                                                    c["output_padding"], c["dilation"], self.dt)
+            self.path = ct.ct_path_3d(c["N"], c["C_in"], c["C_out"], c["L_in"], c["k"], c["groups"],
+                                      c["stride"], c["padding"], c["output_padding"], c["dilation"],
+                                      self.dt, c["add"])
+        self.ws = (torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+                   if self.ws_bytes else None)
+        # kernels the library launches per forward pass on this path
+        self.launches_per_step = {"umma_bf16": 3}.get(self.path, 1)
+
+    def forward(self, stream):
+        c, d, ct = self.cfg, self.d, self.ct
+        if c["nd"] == 1:
+            ct.ct_forward_1d(d["x"], d["w"], d["bias"], self.y, c["N"], c["C_in"], c["C_out"],
+                             c["L_in"][0], c["k"][0], c["groups"], c["stride"][0], c["padding"][0],
+                             c["output_padding"][0], c["dilation"][0], self.dt, self.ws,
+                             self.ws_bytes, stream)
+        elif c["add"]:
+            ct.ct_forward_3d_add_hswish(d["x"], d["w"], d["bias"], d["add"], self.y, c["N"],
+                                        c["C_in"], c["C_out"], c["L_in"], c["k"], c["groups"],
+                                        c["stride"], c["padding"], c["output_padding"],
+                                        c["dilation"], self.dt, self.ws, self.ws_bytes, stream)
+        else:
+            ct.ct_forward_3d(d["x"], d["w"], d["bias"], self.y, c["N"], c["C_in"], c["C_out"],
+                             c["L_in"], c["k"], c["groups"], c["stride"], c["padding"],
+                             c["output_padding"], c["dilation"], self.dt, self.ws, self.ws_bytes,
+                             stream)
+
+    def h2d(self):
+        for k in ("x", "w", "bias", "add"):
+            if self.host[k] is not None:
+                self.d[k].copy_(self.host[k], non_blocking=True)
+
+    def d2h(self):
+        self.y_host.copy_(self.y, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.host.values() if v is not None)
+
+    def d2h_bytes(self):
+        return self.y.numel() * 4
+
+
+def time_steps(fn, steps, warmup, ws, flush=None, graph=True):
+    """Device time of `steps` forward passes (CUDA events on the stream the
+    work runs on), max over ranks.  With graph=True one forward pass (the
+    library's whole launch sequence) is captured once in a CUDA graph and
+    replayed, so host-side argument handling stays out of the device clock."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    run = fn
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()                       # one more eager pass on the capture stream
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=s):
+                fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        run = g.replay
+        run()
+        torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    barrier(ws)
+    torch.cuda.synchronize()
+    if flush is None:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+    else:
+        ms = 0.0
+        for _ in range(steps):
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
+    barrier(ws)
+    torch.cuda.synchronize()
+    return reduce_max(ms / 1e3, ws)
+
+
+def dtype_of(cfg):
+    return "bf16-in/f32-acc" if cfg["dtype"] == "bf16" else "f32"
+
+
+def traffic_for(name, path):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (profiles/traffic.json), or None when no capture matches."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d.get("%s/%s" % (name, path))
+        return None if e is None else e.get("bytes_per_launch")
+    except Exception:
+        return None
+
+
+def roofline(name, cfg, path, wm, sec, peaks):
+    """Roofline entry for the dominant kernel of the step."""
+    traffic = traffic_for(name, path)
+    if cfg["dtype"] == "bf16" and path == "umma_bf16":
+        achieved = wm["flops"] / sec / 1e12
+        peak = peaks["bf16_tflops"]
+        return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": peaks["source"] + " cuBLAS bf16 burst"}
+    ai = wm["flops"] / wm["bytes"]
+    alu_peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
+    ridge = alu_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if ai >= ridge:
+        achieved = wm["flops"] / sec / 1e12
+        return {"bound": "alu", "achieved": round(achieved, 2), "peak": round(alu_peak, 2),
+                "unit": "TFLOP/s", "frac": round(achieved / alu_peak, 4), "traffic": traffic,
+                "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x %.0f MHz max SM clock"
+                % peaks["sm_max_mhz"]}
+    achieved = wm["bytes"] / sec / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "peak_source": peaks["source"] + " copy bandwidth"}
+
+
+def run_gpu_arm(args, ws, rank, local):
+    import torch
+    import transposed_convolution_convtranspose_gb300 as ct
+    from transposed_convolution_convtranspose_gb300 import build
+    build.build()
+    ct.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    name = args.config
+    r = Runner(name, dev)
+    wm = r.wm
+    big = wm["bytes"] > L2_BYTES
+    flush_buf = None if big else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = None if big else (lambda: flush_buf.add_(1.0))
+
+    sampler = ClockSampler(gpu_id_for_smi(local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    t_dev = time_steps(lambda: r.forward(torch.cuda.current_stream()), args.steps, args.warmup, ws,
+                       flush, graph=not args.no_graph)
+    clocks = sampler.stop() if sampler else None
+
+    # end-to-end through the public API: H2D of the step's inputs from pinned
+    # host memory, the forward call, D2H of the output -- all timed
+    def e2e_step():
+        r.h2d()
+        r.forward(torch.cuda.current_stream())
+        r.d2h()
+    e2e_steps = max(1, min(args.steps, 5))
+    t_e2e = time_steps(e2e_step, e2e_steps, 1, ws, graph=False)
+    ct.ct_last_device_error(torch.cuda.current_stream())
+
+    peaks = measured_peaks()
+    sec = t_dev / args.steps
+    units = wm["flops"]
+    value = aggregate(units * ws * args.steps / 1e9, t_dev)        # GFLOP/s, all ranks
+    gbs = aggregate(wm["bytes"] * ws * args.steps / 1e9, t_dev)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(r.cfg),
+        "data": "synthetic (seeded numpy PCG64; x~N(0,1), w~U(-b,b))",
+        "config": {"workload": name, "desc": r.cfg["desc"], "global_batch": r.cfg["N"] * ws,
+                   "parallelism": "replicas" if ws > 1 else "single",
+                   "l2": ("inputs larger than L2 (%.0f MB per step)" % (wm["bytes"] / 1e6)) if big
+                   else "L2 flushed between steps", "path": r.path,
+                   "timing": "CUDA graph replay" if not args.no_graph else "eager calls"},
+        "gbps": round(gbs, 1),
+        "roofline": roofline(name, r.cfg, r.path, wm, sec, peaks),
+        "e2e": {"value": round(aggregate(units * ws * e2e_steps / 1e9, t_e2e), 1), "unit": "GFLOP/s",
+                "h2d_bytes_per_step": r.h2d_bytes(), "d2h_bytes_per_step": r.d2h_bytes()},
+        "gpu_launches": r.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    return res, r
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _slice_cfg(cfg, frac):
+    """The workload with batch 1 and its outermost spatial input extent cut to
+    a fraction (same channels, kernel, stride, padding, dilation)."""
+    c = dict(cfg)
+    L = list(cfg["L_in"])
+    L[0] = max(1, int(round(L[0] * frac)))
+    c["L_in"] = tuple(L)
+    c["N"] = 1
+    return c
+
+
+def _oracle_run(cfg, t):
+    import oracle
+    kw = dict(stride=tuple(cfg["stride"]), padding=tuple(cfg["padding"]),
+              output_padding=tuple(cfg["output_padding"]), dilation=tuple(cfg["dilation"]),
+              groups=cfg["groups"])
+    y = oracle.conv_transpose(t["x"], t["w"], t["bias"], **kw)
+    if cfg["add"]:
+        y = oracle.add_hswish(y, t["add"])
+    return y
+
+
+def _sample_inputs(cfg, seed):
+    x_shape = (1, cfg["C_in"]) + tuple(cfg["L_in"])
+    w_shape = (cfg["C_in"], cfg["C_out"] // cfg["groups"]) + tuple(cfg["k"])
+    add_shape = None
+    if cfg["add"]:
+        add_shape = tuple(work_model(cfg, N=1)["out_shape"])
+    return workloads.make_tensors(seed, x_shape, w_shape, cfg["bound"],
+                                  bias_len=cfg["C_out"] if cfg["bias"] else None,
+                                  add_shape=add_shape, dtype=cfg["dtype"])
+
+
+def oracle_sample_plan(name, seconds):
+    """Pick the fraction of one batch item that the oracle finishes in about
+    `seconds` (calibrated on a 1/64 slice)."""
+    import oracle
+    oracle.build_oracle()
+    cfg = workloads.CONFIGS[name]
+    small = _slice_cfg(cfg, 1.0 / 64)
+    t = _sample_inputs(small, cfg["seed"])
+    t0 = time.perf_counter()
+    _oracle_run(small, t)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    frac = min(1.0, max(1.0 / 64, seconds / (dt * 64)))
+    return _slice_cfg(cfg, frac), frac
+
+
+def oracle_time(scfg, name):
+    """Run the single-threaded oracle once on the sampled workload; returns
+    (GFLOP/s of algorithmic work, seconds)."""
+    t = _sample_inputs(scfg, workloads.CONFIGS[name]["seed"])
+    t0 = time.perf_counter()
+    _oracle_run(scfg, t)
+    sec = time.perf_counter() - t0
+    return work_model(scfg, N=1)["flops"] / sec / 1e9, sec
+
+
+def sample_desc(scfg, name, frac):
+    return ("batch 1 of %s with the outermost input extent cut to %s (%.3f of one batch item "
+            "of %d), single-threaded C oracle in float64" % (name, tuple(scfg["L_in"]), frac,
+                                                             workloads.CONFIGS[name]["N"]))
+
+
+def run_reference_arm(args):
+    """The CPU oracle as the reference arm: every step is one bounded sample."""
+    cfg = workloads.CONFIGS[args.config]
+    per_step = max(0.2, min(20.0, args.ref_seconds / (args.steps + args.warmup)))
+    scfg, frac = oracle_sample_plan(args.config, per_step)
+    for _ in range(args.warmup):
+        oracle_time(scfg, args.config)
+    runs = [oracle_time(scfg, args.config) for _ in range(args.steps)]
+    tot = sum(s for _, s in runs)
+    value = work_model(scfg, N=1)["flops"] * len(runs) / tot / 1e9
+    desc = sample_desc(scfg, args.config, frac)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / len(runs) * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded numpy PCG64)",
+        "config": {"workload": args.config, "desc": cfg["desc"]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": desc + ", per step"},
+        "e2e": {"value": round(value, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=HEADLINE, choices=list(workloads.CONFIGS))
+    ap.add_argument("--table", action="store_true", help="one line per workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of a CUDA graph")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="total oracle time budget of the reference arm")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        # the oracle runs on rank 0 only; other ranks exit without work
+        if rank == 0:
+            print(json.dumps(run_reference_arm(args)), flush=True)
+        return 0
+
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+
+    if args.table:
+        import torch
+        for name in workloads.CONFIG_ORDER:
+            a2 = argparse.Namespace(**vars(args))
+            a2.config = name
+            res, r = run_gpu_arm(a2, ws, rank, local)
+            del r
+            torch.cuda.empty_cache()
+            if rank == 0:
+                print(json.dumps(res), flush=True)
+        return 0
+
+    res, r = run_gpu_arm(args, ws, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            scfg, frac = oracle_sample_plan(args.config, args.cpu_seconds)
+            v, sec = oracle_time(scfg, args.config)
+            res["cpu_baseline"] = {"value": round(v, 4), "unit": "GFLOP/s", "cores": 1,
+                                   "kind": "oracle", "sample": sample_desc(scfg, args.config, frac),
+                                   "seconds": round(sec, 2)}
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

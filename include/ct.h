@@ -112,6 +112,38 @@ ct_status ct_forward_3d_add_hswish(const void *x, const void *w, const float *bi
                                    const int dilation[3], ct_dtype dtype,
                                    void *workspace, size_t ws_bytes, void *stream);
 
+/* The same bf16 ConvTranspose3d as ct_forward_3d, for callers that cannot
+ * allocate device memory: no workspace argument, and no cudaMalloc, cudaFree
+ * or other allocating call inside.  The pages have no counterpart of this
+ * entry point; it serves callers such as an engine that reserves all device
+ * memory at start-up and forbids allocation afterwards, a plugin running
+ * inside a host framework that owns the device memory pool, or an
+ * allocation-free real-time loop -- none of them can hand ct_forward_3d a
+ * freshly allocated workspace.
+ *
+ * Scratch: a buffer of CT_NOALLOC_SCRATCH_BYTES (48 MiB) that the library
+ * owns, a static device array that every GPU which loads libct.so keeps
+ * until the process exits.  The first call on a device looks up the
+ * buffer's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call on a device
+ * shares the one buffer, so calls that overlap on the GPU (different
+ * streams, or other threads) race and must be serialised by the caller.
+ * Each call rewrites every scratch byte it reads, so no state carries over
+ * from the last call and nothing needs clearing.
+ *
+ * Arguments and layouts as ct_forward_3d with dtype CT_BF16.  Returns
+ * CT_ERR_UNSUPPORTED when the arguments do not take the bf16 tensor-core
+ * path (other paths need no scratch: use ct_forward_3d), CT_ERR_WORKSPACE
+ * when the problem needs more scratch than CT_NOALLOC_SCRATCH_BYTES
+ * (2*(N*C_in*D*H*W + 8*C_out*(k/2)^3*C_in) bytes, each part rounded up to
+ * 256), CT_ERR_CUDA when the set-up or a launch fails. */
+#define CT_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
+ct_status ct_forward_3d_noalloc(const void *x, const void *w, const float *bias, float *y,
+                                int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
+                                int groups, const int stride[3], const int padding[3],
+                                const int output_padding[3], const int dilation[3],
+                                ct_dtype dtype, void *stream);
+
 /* Name of the kernel family the 1-D / 3-D / fused call with these arguments
  * would launch ("gather_generic", "phase1d_f32", "phase3d_f32", "umma_bf16",
  * ...), or NULL if the arguments are invalid.  Host only; launches nothing.

@@ -26,7 +26,11 @@ CT_STATUS = {0: "CT_OK", 1: "CT_ERR_ARG", 2: "CT_ERR_SHAPE", 3: "CT_ERR_ALIGN",
 
 EXPORTED = ["ct_out_len", "ct_workspace_size_1d", "ct_workspace_size_3d", "ct_forward_1d",
             "ct_forward_3d", "ct_forward_3d_add_hswish", "ct_path_1d", "ct_path_3d",
-            "ct_set_path_override", "ct_status_str", "ct_last_device_error"]
+            "ct_set_path_override", "ct_status_str", "ct_last_device_error",
+            "ct_forward_3d_noalloc"]
+
+# bytes of the library-owned scratch buffer used by ct_forward_3d_noalloc
+CT_NOALLOC_SCRATCH_BYTES = 48 * 1024 * 1024
 
 
 class CTError(RuntimeError):
@@ -61,6 +65,9 @@ def _setup(lib):
     lib.ct_forward_3d_add_hswish.restype = _I
     lib.ct_forward_3d_add_hswish.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I3, _I3, _I, _I3,
                                              _I3, _I3, _I3, _I, _P, ctypes.c_size_t, _P]
+    lib.ct_forward_3d_noalloc.restype = _I
+    lib.ct_forward_3d_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I3, _I3, _I, _I3, _I3, _I3,
+                                          _I3, _I, _P]
     lib.ct_path_1d.restype = ctypes.c_char_p
     lib.ct_path_1d.argtypes = [_I] * 10 + [_I]
     lib.ct_path_3d.restype = ctypes.c_char_p
@@ -171,6 +178,16 @@ def ct_forward_3d_add_hswish(x, w, bias, add, y, N, C_in, C_out, in_dhw, k_dhw, 
                                            _i3(dilation), dtype, _ptr(workspace), int(ws_bytes),
                                            _stream(stream)),
            "ct_forward_3d_add_hswish")
+
+
+def ct_forward_3d_noalloc(x, w, bias, y, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding,
+                          output_padding, dilation, dtype, stream=None):
+    """ct_forward_3d for callers that cannot allocate: the bf16 tensor-core
+    path with the library's own fixed scratch buffer instead of a workspace."""
+    _check(load().ct_forward_3d_noalloc(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), N, C_in, C_out,
+                                        _i3(in_dhw), _i3(k_dhw), groups, _i3(stride), _i3(padding),
+                                        _i3(output_padding), _i3(dilation), dtype, _stream(stream)),
+           "ct_forward_3d_noalloc")
 
 
 def ct_path_1d(N, C_in, C_out, L_in, k, groups, stride, padding, output_padding, dilation, dtype):

@@ -163,6 +163,19 @@ ct_status run(const Problem &pb, Args a)
 
 }  // namespace
 
+// Internal access for other translation units (declared in ct_internal.h).
+namespace ct {
+ct_status make_problem_3d(int N, int C_in, int C_out, const int *in_dhw, const int *k_dhw, int groups,
+                          const int *stride, const int *padding, const int *output_padding,
+                          const int *dilation, ct_dtype dtype, bool has_bias, Problem *pb)
+{
+    return make_problem(3, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding, output_padding,
+                        dilation, dtype, has_bias, false, pb);
+}
+bool takes_umma_path(const Problem &pb, const Args *a) { return choose_path(pb, a) == Path::Umma; }
+ct_status run_problem(const Problem &pb, const Args &a) { return run(pb, a); }
+}  // namespace ct
+
 extern "C" {
 
 int64_t ct_out_len(int64_t L_in, int k, int s, int p, int op, int dl)

@@ -55,6 +55,13 @@ bool build_phase_dim(int L_out, int K, int S, int P, int DL, PhaseDim *pd);
 // waits).  Valid on the current device after the first call.
 unsigned int *device_status_ptr();
 
+// Validation, path choice and launch of ct_api.cu, for other entry points.
+ct_status make_problem_3d(int N, int C_in, int C_out, const int *in_dhw, const int *k_dhw, int groups,
+                          const int *stride, const int *padding, const int *output_padding,
+                          const int *dilation, ct_dtype dtype, bool has_bias, Problem *pb);
+bool takes_umma_path(const Problem &pb, const Args *a);
+ct_status run_problem(const Problem &pb, const Args &a);
+
 // ---- generic gather kernel (any valid problem; fp32 or bf16 inputs) ----
 cudaError_t launch_gather_generic(const Problem &pb, const Args &a);
 

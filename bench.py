@@ -202,9 +202,9 @@ def aggregate(units_all_ranks, max_seconds):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def _inputs_to_device(cfg_name, dev, pinned=False):
+def _inputs_to_device(cfg_name, dev, pinned=False, batch=None):
     import torch
-    t = workloads.config_inputs(cfg_name)
+    t = workloads.config_inputs(cfg_name, N=batch)
     cfg = workloads.CONFIGS[cfg_name]
     host = {}
     if cfg["dtype"] == "bf16":
@@ -224,14 +224,18 @@ def _inputs_to_device(cfg_name, dev, pinned=False):
 class Runner:
     """One forward pass of a workload through the C ABI, buffers pre-allocated."""
 
-    def __init__(self, cfg_name, dev):
+    def __init__(self, cfg_name, dev, batch=None):
         import torch
         import transposed_convolution_convtranspose_gb300 as ct
         self.ct = ct
-        self.cfg = workloads.CONFIGS[cfg_name]
+        self.cfg = dict(workloads.CONFIGS[cfg_name])
+        if batch is not None:
+            self.cfg["N"] = batch
+            if self.cfg["add"]:
+                self.cfg["out_shape"] = (batch,) + tuple(self.cfg["out_shape"][1:])
         self.name = cfg_name
         self.dev = dev
-        self.host, self.d = _inputs_to_device(cfg_name, dev, pinned=True)
+        self.host, self.d = _inputs_to_device(cfg_name, dev, pinned=True, batch=batch)
         wm = work_model(self.cfg)
         self.wm = wm
         self.y = torch.empty(wm["out_shape"], dtype=torch.float32, device=dev)
@@ -391,7 +395,7 @@ def run_gpu_arm(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     name = args.config
-    r = Runner(name, dev)
+    r = Runner(name, dev, batch=args.batch)
     wm = r.wm
     big = wm["bytes"] > L2_BYTES
     flush_buf = None if big else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -424,13 +428,15 @@ def run_gpu_arm(args, ws, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(r.cfg),
         "data": "synthetic (seeded numpy PCG64; x~N(0,1), w~U(-b,b))",
-        "config": {"workload": name, "desc": r.cfg["desc"], "global_batch": r.cfg["N"] * ws,
+        "config": {"workload": name if args.batch is None else "%s (batch %d)" % (name, args.batch),
+                   "desc": r.cfg["desc"], "global_batch": r.cfg["N"] * ws,
                    "parallelism": "replicas" if ws > 1 else "single",
                    "l2": ("inputs larger than L2 (%.0f MB per step)" % (wm["bytes"] / 1e6)) if big
                    else "L2 flushed between steps", "path": r.path,
                    "timing": "CUDA graph replay" if not args.no_graph else "eager calls"},
         "gbps": round(gbs, 1),
-        "roofline": roofline(name, r.cfg, r.path, wm, sec, peaks),
+        "roofline": roofline(name if args.batch is None else name + "@N%d" % args.batch,
+                             r.cfg, r.path, wm, sec, peaks),
         "e2e": {"value": round(aggregate(units * ws * e2e_steps / 1e9, t_e2e), 1), "unit": "GFLOP/s",
                 "h2d_bytes_per_step": r.h2d_bytes(), "d2h_bytes_per_step": r.d2h_bytes()},
         "gpu_launches": r.launches_per_step * args.steps,
@@ -538,6 +544,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=HEADLINE, choices=list(workloads.CONFIGS))
     ap.add_argument("--table", action="store_true", help="one line per workload")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (small cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

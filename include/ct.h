@@ -145,8 +145,8 @@ ct_status ct_forward_3d_noalloc(const void *x, const void *w, const float *bias,
                                 ct_dtype dtype, void *stream);
 
 /* Name of the kernel family the 1-D / 3-D / fused call with these arguments
- * would launch ("gather_generic", "phase1d_f32", "phase3d_f32", "umma_bf16",
- * ...), or NULL if the arguments are invalid.  Host only; launches nothing.
+ * would launch ("gather_generic", "phase1d_f32", "tc1d_tf32x3", "phase3d_f32",
+ * "umma_bf16", ...), or NULL if the arguments are invalid.  Host only; launches nothing.
  * `fused` selects the add + hardswish variant for the 3-D query. */
 const char *ct_path_1d(int N, int C_in, int C_out, int L_in, int k, int groups, int stride,
                        int padding, int output_padding, int dilation, ct_dtype dtype);
@@ -156,8 +156,9 @@ const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const in
                        int fused);
 
 /* Process-wide path override for testing the dispatcher: 0 = automatic
- * (default), 1 = always use the generic gather kernel.  Not thread-safe
- * against concurrent forward calls. */
+ * (default), 1 = always use the generic gather kernel, 2 = automatic but
+ * without the FP32 tensor-core path (the FFMA phase kernels instead).  Not
+ * thread-safe against concurrent forward calls. */
 void ct_set_path_override(int mode);
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -105,7 +105,13 @@ def test_path_selection(lib):
     # the tiny and the long 1-D workloads
     for N, L in ((2, 64), (16, 131072)):
         p = ct.ct_path_1d(N, 32 if N == 16 else 4, 64 if N == 16 else 8, L, 3, 1, 2, 1, 0, 2, ct.CT_F32)
-        assert p in ("phase1d_f32", "gather_generic")
+        assert p in ("tc1d_tf32x3", "phase1d_f32", "gather_generic")
+    assert ct.ct_path_1d(16, 32, 64, 131072, 3, 1, 2, 1, 0, 2, ct.CT_F32) == "tc1d_tf32x3"
+    ct.ct_set_path_override(2)
+    try:
+        assert ct.ct_path_1d(16, 32, 64, 131072, 3, 1, 2, 1, 0, 2, ct.CT_F32) == "phase1d_f32"
+    finally:
+        ct.ct_set_path_override(0)
     assert ct.ct_path_1d(1, 4, 8, 0, 3, 1, 2, 1, 0, 2, ct.CT_F32) is None
     p3 = ct.ct_path_3d(8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3), (1, 1, 1),
                        (1, 1, 1), ct.CT_F32)

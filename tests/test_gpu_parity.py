@@ -211,3 +211,44 @@ def test_repeat_is_deterministic():
     y2 = cc.run_gpu(c, t)
     import torch
     assert torch.equal(y1, y2)
+
+
+TC1D = [
+    # (C_in, C_out, L_in, k, s, p, op, d): C_in = 32 and d a multiple of s take
+    # the FP32 tensor-core path; ragged lengths end tiles mid-way
+    (32, 64, 131072 // 64, 3, 2, 1, 0, 2),
+    (32, 64, 1000, 3, 2, 1, 1, 2),
+    (32, 16, 516, 3, 2, 0, 0, 2),
+    (32, 32, 256, 4, 2, 2, 1, 2),
+    (32, 48, 300, 2, 2, 1, 0, 4),
+    (32, 64, 128, 3, 1, 1, 0, 1),
+    (32, 64, 131, 3, 2, 1, 0, 2),
+    (32, 64, 260, 1, 2, 0, 1, 2),
+    (32, 32, 4, 3, 2, 1, 0, 2),
+    (32, 64, 1, 3, 2, 1, 0, 2),
+]
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+@pytest.mark.parametrize("k", range(len(TC1D)))
+def test_fp32_1d_tensor_core_and_ffma_paths(k, mode):
+    """The FP32 1-D shapes the tensor-core path takes, through that path
+    (mode 0) and through the FFMA phase kernel (mode 2), against the oracle."""
+    import transposed_convolution_convtranspose_gb300 as ct
+    C_in, C_out, L, kk, s, p, op, d = TC1D[k]
+    c = dict(nd=1, N=2, C_in=C_in, C_out=C_out, G=1, L=[L], K=[kk], S=[s], P=[p], OP=[op],
+             DL=[d], bias=bool(k % 2), add=False, dtype="f32")
+    ct.ct_set_path_override(mode)
+    try:
+        path = path_of(c)
+        if mode == 0 and L % 4 == 0:
+            assert path == "tc1d_tf32x3", path
+        t = cc.make_inputs(c, seed=800 + k)
+        y = cc.run_gpu(c, t).cpu().numpy()
+        cc.assert_close(y, cc.run_oracle(c, t), "f32", "1-D case %r (%s)" % (TC1D[k], path))
+        ti = cc.make_inputs(c, seed=850 + k, int_range=3)
+        yi = cc.run_gpu(c, ti).cpu().numpy()
+        assert np.array_equal(yi.astype(np.float64), cc.run_oracle(c, ti)), \
+            "integer inputs not exact for %r (%s)" % (TC1D[k], path)
+    finally:
+        ct.ct_set_path_override(0)

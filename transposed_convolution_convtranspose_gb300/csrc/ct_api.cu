@@ -96,12 +96,14 @@ ct_status make_problem(int nd, int N, int C_in, int C_out, const int *Li, const 
     return CT_OK;
 }
 
-enum class Path { Generic, Phase1d, Phase3d, Umma };
+enum class Path { Generic, Phase1d, Phase3d, Umma, Tc1d };
 
 Path choose_path(const Problem &pb, const Args *a)
 {
-    if (g_override.load() == 1) return Path::Generic;
+    const int ov = g_override.load();
+    if (ov == 1) return Path::Generic;
     if (pb.dtype == CT_F32) {
+        if (ov != 2 && pb.nd == 1 && tc1d_supported(pb, a)) return Path::Tc1d;
         if (pb.nd == 1 && phase1d_supported(pb, a)) return Path::Phase1d;
         if (pb.nd == 3 && phase3d_supported(pb, a)) return Path::Phase3d;
     } else {
@@ -117,6 +119,7 @@ const char *path_name(Path p)
     case Path::Phase1d: return "phase1d_f32";
     case Path::Phase3d: return "phase3d_f32";
     case Path::Umma: return "umma_bf16";
+    case Path::Tc1d: return "tc1d_tf32x3";
     }
     return "gather_generic";
 }
@@ -157,6 +160,7 @@ ct_status run(const Problem &pb, Args a)
     case Path::Phase1d: e = launch_phase1d(pb, a); break;
     case Path::Phase3d: e = launch_phase3d(pb, a); break;
     case Path::Umma: e = launch_umma(pb, a); break;
+    case Path::Tc1d: e = launch_tc1d(pb, a); break;
     }
     return e == cudaSuccess ? CT_OK : CT_ERR_CUDA;
 }
@@ -284,7 +288,7 @@ const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const in
     return path_name(choose_path(pb, nullptr));
 }
 
-void ct_set_path_override(int mode) { g_override.store(mode == 1 ? 1 : 0); }
+void ct_set_path_override(int mode) { g_override.store(mode == 1 || mode == 2 ? mode : 0); }
 
 const char *ct_status_str(ct_status s)
 {

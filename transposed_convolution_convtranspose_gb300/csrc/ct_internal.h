@@ -65,6 +65,10 @@ ct_status run_problem(const Problem &pb, const Args &a);
 // ---- generic gather kernel (any valid problem; fp32 or bf16 inputs) ----
 cudaError_t launch_gather_generic(const Problem &pb, const Args &a);
 
+// ---- FP32 1-D on the tensor cores (3-term tf32 split) ----
+bool tc1d_supported(const Problem &pb, const Args *a);
+cudaError_t launch_tc1d(const Problem &pb, const Args &a);
+
 // ---- phase-decomposed FP32 1-D kernel ----
 bool phase1d_supported(const Problem &pb, const Args *a);
 cudaError_t launch_phase1d(const Problem &pb, const Args &a);

@@ -392,6 +392,7 @@ def run_gpu_arm(args, ws, rank, local):
     from transposed_convolution_convtranspose_gb300 import build
     build.build()
     ct.load()
+    ct.ct_set_path_override(args.path_override)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     name = args.config
@@ -544,6 +545,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=HEADLINE, choices=list(workloads.CONFIGS))
     ap.add_argument("--table", action="store_true", help="one line per workload")
+    ap.add_argument("--path-override", type=int, default=0,
+                    help="library path override: 0 automatic, 1 generic kernel, 2 no FP32 tensor-core path")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (small cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

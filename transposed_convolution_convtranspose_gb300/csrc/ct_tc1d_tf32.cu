@@ -5,36 +5,30 @@
 // even ones hold the bias; the gather index relation i = (o + p - k*d)/s):
 // when the dilation is a multiple of the stride, every tap belongs to one
 // residue class r* and output q of that class reads input i = q + e_j with
-// e_j = base - j*(d/s).  The taps are concatenated along the GEMM's N
-// dimension:
-//     D[i][(j, oc)] = sum_ic x[ic][i] * w[ic][oc][k_j]          (dense, K = C_in)
-//     y[s*q + r*][oc] = bias[oc] + sum_j D[q + e_j][(j, oc)]     (a row shift per tap)
-// so the contraction is one GEMM on the tensor cores and the tap shifts move
-// into the epilogue (warp shuffles across TMEM lanes and a small shared-memory
-// exchange at warp edges).  A tile's 128 GEMM rows are input positions
-// q0 - 4 .. q0 + 123 and it produces the 120 outputs q0 .. q0 + 119, so every
-// shifted row it needs is its own (neighbouring tiles overlap by 8 rows).
-// The other residues hold the bias.
+// e_j = base - j*(d/s).  Per tile of 128 outputs the sum over taps and input
+// channels is one GEMM with K = taps x C_in:
+//     y[s*q + r*][oc] = bias[oc] + sum_j sum_ic x[ic][q + e_j] * w[ic][oc][k_j]
+// A tile is stored once, position-major, for positions q0-4 .. q0+131; the
+// A operand of tap j is the same tile read from row 4 + e_j on: only the
+// shared-memory descriptor's start address moves (the 128-byte swizzle
+// follows absolute address bits, so the base-offset field stays 0), and no
+// shifted copy is made.  The other residues hold the bias.
 //
 // Precision: each fp32 operand is split as v = hi + lo with hi = v rounded to
 // tf32 (cvt.rna) and lo = v - hi (exact in fp32); three MMAs accumulate
 // hi*hi + hi*lo + lo*hi in fp32 in TMEM.  The dropped lo*lo term and the
 // tf32 rounding of lo are each below 2^-21 of a product.
 //
-// Roles (persistent CTA of 384 threads, one per SM):
-//   warp 0      TMA producer: x tile [C_in = 32][128 positions] as four
-//               32 x 32 boxes (positions contiguous, 128-byte swizzle);
-//               boxes past the end of the input read zeros
-//   warp 1      TMEM allocation and MMA issue: 4 K-steps x 3 split terms of
-//               tcgen05.mma M=128, N=taps*C_out, K=8 into one of two TMEM
+// Roles (persistent CTA of 256 threads, one per SM):
+//   warp 0      TMA producer: x box [C_in = 32][136 positions] per tile (no
+//               swizzle); positions outside the input read zeros
+//   warp 1      TMEM allocation and MMA issue: taps x 4 K-steps x 3 split
+//               terms of tcgen05.mma M=128, N=C_out, K=8 into one of two TMEM
 //               accumulators (double-buffered across tiles)
-//   warps 2-3   split + transpose: x tile -> position-major (K-major) hi and
-//               lo tiles, 128-byte swizzled; the weights once, as hi/lo
-//               K-major swizzled tiles
-//   warps 4-11  epilogue, two groups of four warps taking alternate chunks of
-//               16 channels: tcgen05.ld, tap shifts, bias, assemble each
-//               channel's s*120 consecutive outputs in shared memory and write
-//               them with TMA bulk stores (cp.async.bulk)
+//   warps 2-3   split + transpose: x box -> position-major (K-major) hi and lo
+//               tiles, 128-byte swizzled; the weights once, per tap, the same way
+//   warps 4-7   epilogue: tcgen05.ld, bias, assemble each channel's s*128
+//               consecutive outputs in shared memory, TMA bulk stores
 // Every mbarrier wait is bounded; a timeout records CT_ERR_DEVICE_TIMEOUT in
 // the device status word and the roles unwind.
 #include <string.h>
@@ -46,28 +40,26 @@
 namespace ct {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int BM = 128;          // positions per tile (UMMA M)
-constexpr int PAD = 4;           // tile rows before the first output (a 16-byte TMA start)
-constexpr int TQ = BM - 2 * PAD; // outputs q per tile; rows cover q + e for |e| <= PAD
-constexpr int CI = 32;           // input channels = GEMM K
+constexpr int kThreads = 256;
+constexpr int BM = 128;          // outputs per tile (UMMA M)
+constexpr int PAD = 4;           // stored rows before the first output (16-byte TMA start)
+constexpr int XR = BM + 2 * PAD; // stored input positions per tile
+constexpr int CI = 32;           // input channels (one 128-byte K row)
 constexpr int NS = 2;            // x-tile stages
 constexpr int MAXT = 4;          // taps
-constexpr int MAXR = 2;          // |row shift| supported
-constexpr int MAXS = 2;          // stride supported (output run = MAXS * BM)
+constexpr int MAXS = 2;          // stride (an output run is s*128 long)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct TParams {
     int N, C_in, C_out, Cog, K;
     int L_in, L_out, S;
     int nT;                      // taps
-    int e[MAXT];                 // row shift of tap j: output q reads D row q + e_j
+    int e[MAXT];                 // input offset of tap j: output q reads q + e_j
     int k_of[MAXT];              // kernel index of tap j
     int rstar;                   // residue receiving the taps
-    int R;                       // max |e_j| (>= 1)
-    int ntq;                     // q tiles per row
+    int ntq;                     // tiles per row
     int ntiles;
-    int ncol;                    // nT * Cog (accumulator columns)
+    uint32_t tmem_cols;          // allocated TMEM columns (2 accumulators of C_out)
     uint32_t idesc;
 };
 
@@ -79,14 +71,17 @@ __device__ __forceinline__ float tf32_hi(float v)
     return __uint_as_float(r);
 }
 
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+// K-major, 128-byte swizzle: rows of 128 bytes, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr)
 {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-    d |= (uint64_t)1 << 46;      // descriptor version (sm_100 family)
-    d |= (uint64_t)2 << 61;      // 128-byte swizzle
+    d |= (uint64_t)1 << 16;                       // leading byte offset (unused)
+    d |= (uint64_t)(1024 >> 4) << 32;             // stride byte offset
+    d |= (uint64_t)1 << 46;                       // descriptor version (sm_100 family)
+    // base offset 0: the swizzle follows the absolute shared-memory address, so a
+    // start row inside an atom needs no phase correction
+    d |= (uint64_t)2 << 61;                       // 128-byte swizzle
     return d;
 }
 
@@ -130,48 +125,38 @@ __device__ __forceinline__ void bulk_store(float *g, const float *s, unsigned by
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
 
 // byte offset of element (row, k) in a K-major 128-byte-swizzled tile of
-// 32-bit elements (rows of 32 elements = 128 B, 8-row atoms of 1024 B; the
-// 16-byte chunk index is XORed with the row index within the atom)
+// 32-bit elements (the 16-byte chunk index is XORed with the row's phase)
 __device__ __forceinline__ uint32_t sw128_off(int row, int k)
 {
     return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((((k >> 2) ^ row) & 7) << 4) + (k & 3) * 4);
 }
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ---------------
-constexpr uint32_t kXTile = BM * CI * 4;                 // 16 KB per x stage
-constexpr uint32_t kWTile = 256 * CI * 4;                // up to 256 B rows (32 KB)
+constexpr uint32_t kXRaw = CI * XR * 4;                  // TMA box [32][136] fp32
+constexpr uint32_t kXK = XR * 128;                       // K-major 136 rows (17 atoms)
+constexpr uint32_t kWTile = 256 * 128;                   // up to taps*C_out = 256 rows
 constexpr int kChunk = 16;                               // output channels per epilogue chunk
-constexpr int kRowF = MAXS * TQ + 8;                     // floats per staged output row
-constexpr uint32_t kStage = kChunk * kRowF * 4;          // one staging buffer
-constexpr int kEdgeRows = 5 * 2 * MAXR;                  // rows next to the 5 warp edges
-constexpr uint32_t kEdge = MAXT * kEdgeRows * kChunk * 4;
+constexpr int kRowF = MAXS * BM + 8;                     // floats per staged output row
+constexpr uint32_t kStage = kChunk * kRowF * 4;
 
-constexpr uint32_t OFF_XT = 0;                            // raw TMA tiles (positions contiguous)
-constexpr uint32_t OFF_XHI = OFF_XT + NS * kXTile;        // K-major hi
-constexpr uint32_t OFF_XLO = OFF_XHI + NS * kXTile;       // K-major lo
-constexpr uint32_t OFF_WHI = OFF_XLO + NS * kXTile;
+constexpr uint32_t OFF_XT = 0;
+constexpr uint32_t OFF_XHI = OFF_XT + NS * kXRaw;
+constexpr uint32_t OFF_XLO = OFF_XHI + NS * kXK;
+constexpr uint32_t OFF_WHI = OFF_XLO + NS * kXK;
 constexpr uint32_t OFF_WLO = OFF_WHI + kWTile;
-constexpr uint32_t OFF_STG = OFF_WLO + kWTile;            // one staging buffer per epilogue group
-constexpr uint32_t OFF_EDGE = OFF_STG + 2 * kStage;       // 2 groups x 2 parities
-constexpr uint32_t kSmemBytes = OFF_EDGE + 4 * kEdge + 1024;   // + alignment slack
+constexpr uint32_t OFF_STG = OFF_WLO + kWTile;
+constexpr uint32_t kSmemBytes = OFF_STG + 2 * kStage + 1024;   // + alignment slack
+static_assert(kXRaw % 1024 == 0 && kXK % 1024 == 0, "1024-byte aligned tiles");
 static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
 
-// slot of tile row t among the rows within R of the warp edges 32, 64, 96
-__device__ __forceinline__ int edge_slot(int t, int R)
-{
-    const int u = t + R;
-    return (u >> 5) * (2 * R) + (u & 31);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
-tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restrict__ x,
-                 const float *__restrict__ w, const float *__restrict__ bias, float *__restrict__ y,
-                 TParams p, unsigned int *status)
+tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restrict__ w,
+                 const float *__restrict__ bias, float *__restrict__ y, TParams p, unsigned int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_x[NS], xt_free[NS], split_x[NS], empty_x[NS], acc_full[2],
@@ -190,7 +175,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
         }
         for (int a = 0; a < 2; ++a) {
             dev::mbar_init(&acc_full[a], 1);
-            dev::mbar_init(&acc_empty[a], 256);
+            dev::mbar_init(&acc_empty[a], 128);
         }
         dev::mbar_init(&w_ready, 64);
         dev::fence_mbar_init();
@@ -198,7 +183,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                          dev::smem_u32(&tmem_slot)),
-                     "r"(512)
+                     "r"(p.tmem_cols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
@@ -223,13 +208,9 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
                     break;
                 }
                 const int n = tile / p.ntq, qt = tile % p.ntq;
-                const int r0 = qt * TQ - PAD;           // position of tile row 0
-                uint8_t *dst = sm + OFF_XT + s * kXTile;
-                dev::mbar_arrive_expect_tx(&full_x[s], kXTile);
-                // x viewed as (L_in, C_in, N): box of 32 positions x 32 channels
-#pragma unroll
-                for (int b = 0; b < BM / 32; ++b)
-                    dev::tma_load_3d(dst + b * (32 * CI * 4), &tmx, &full_x[s], r0 + 32 * b, 0, n);
+                dev::mbar_arrive_expect_tx(&full_x[s], kXRaw);
+                // x viewed as (L_in, C_in, N): positions q0 - PAD .. q0 + BM + PAD - 1
+                dev::tma_load_3d(sm + OFF_XT + s * kXRaw, &tmx, &full_x[s], qt * BM - PAD, 0, n);
                 ++issued;
             }
             if (failed)
@@ -252,20 +233,22 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
                     break;
                 }
                 tc_after();
-                const uint32_t xhi = dev::smem_u32(sm + OFF_XHI + s * kXTile);
-                const uint32_t xlo = dev::smem_u32(sm + OFF_XLO + s * kXTile);
-                const uint32_t d = tmem + (uint32_t)(a * 256);
+                const uint32_t xhi = dev::smem_u32(sm + OFF_XHI + s * kXK);
+                const uint32_t xlo = dev::smem_u32(sm + OFF_XLO + s * kXK);
+                const uint32_t d = tmem + (uint32_t)(a * p.Cog);
+                for (int j = 0; j < p.nT; ++j) {
+                    const uint32_t arow = (uint32_t)(PAD + p.e[j]) * 128u;   // tap j's first row
+                    const uint32_t boff = (uint32_t)(j * p.Cog) * 128u;        // tap j's weight rows
 #pragma unroll
-                for (int kk = 0; kk < CI / 8; ++kk) {
-                    // A and B K-major: rows of 32 channels (128 B), 8-row atoms
-                    // 1 KB apart; 8 channels = 32 bytes along the row
-                    const uint64_t ahi = desc_sw128(xhi + kk * 32, 16, 1024);
-                    const uint64_t alo = desc_sw128(xlo + kk * 32, 16, 1024);
-                    const uint64_t bhi = desc_sw128(whi + kk * 32, 16, 1024);
-                    const uint64_t blo = desc_sw128(wlo + kk * 32, 16, 1024);
-                    mma_tf32(d, ahi, bhi, p.idesc, kk > 0 ? 1u : 0u);
-                    mma_tf32(d, ahi, blo, p.idesc, 1u);
-                    mma_tf32(d, alo, bhi, p.idesc, 1u);
+                    for (int kk = 0; kk < CI / 8; ++kk) {
+                        const uint64_t ahi = desc_sw128(xhi + arow + kk * 32);
+                        const uint64_t alo = desc_sw128(xlo + arow + kk * 32);
+                        const uint64_t bhi = desc_sw128(whi + boff + kk * 32);
+                        const uint64_t blo = desc_sw128(wlo + boff + kk * 32);
+                        mma_tf32(d, ahi, bhi, p.idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_tf32(d, ahi, blo, p.idesc, 1u);
+                        mma_tf32(d, alo, bhi, p.idesc, 1u);
+                    }
                 }
                 mma_commit(&empty_x[s]);
                 mma_commit(&acc_full[a]);
@@ -273,10 +256,10 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
     } else if (warp < 4) {
-        // ---------------- split warps (64 threads)
+        // ---------------- split + transpose warps (64 threads)
         const int st = threadIdx.x - 64;
-        // weights once: B row n = j*Cog + oc, column ic; hi/lo, K-major swizzled
-        for (int e = st; e < p.ncol * CI; e += 64) {
+        // weights once: tap j's rows j*Cog + oc, K = ic; hi/lo, K-major swizzled
+        for (int e = st; e < p.nT * p.Cog * CI; e += 64) {
             const int n = e / CI, ic = e % CI;
             const int j = n / p.Cog, oc = n % p.Cog;
             const float v = __ldg(w + ((int64_t)ic * p.Cog + oc) * p.K + p.k_of[j]);
@@ -296,31 +279,23 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
                 ok = false;
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
             if (ok) {
-                // raw tile: box b = m/32 holds [32 channels][32 positions], 128-byte
-                // swizzled; write position-major (K-major) hi and lo tiles
-                const uint8_t *xt = sm + OFF_XT + s * kXTile;
-                uint8_t *xh = sm + OFF_XHI + s * kXTile;
-                uint8_t *xl = sm + OFF_XLO + s * kXTile;
-                for (int h = 0; h < BM / 64; ++h) {
-                    const int m = st + 64 * h;
-                    const int b = m >> 5, mm = m & 31;
+                const float *xt = reinterpret_cast<const float *>(sm + OFF_XT + s * kXRaw);   // [ic][pos]
+                uint8_t *xh = sm + OFF_XHI + s * kXK;
+                uint8_t *xl = sm + OFF_XLO + s * kXK;
+                for (int e = st; e < XR * (CI / 4); e += 64) {
+                    const int pos = e % XR, cg = e / XR;
+                    float4 hv, lv;
+                    float *hp = &hv.x, *lp = &lv.x;
 #pragma unroll
-                    for (int cg = 0; cg < CI / 4; ++cg) {
-                        float4 hv, lv;
-                        float *hp = &hv.x, *lp = &lv.x;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int c = 4 * cg + u;
-                            const float v = *reinterpret_cast<const float *>(
-                                xt + b * 4096 + c * 128 + ((((mm >> 2) ^ c) & 7) << 4) + (mm & 3) * 4);
-                            const float hi = tf32_hi(v);
-                            hp[u] = hi;
-                            lp[u] = v - hi;
-                        }
-                        const uint32_t off = sw128_off(m, 4 * cg);
-                        *reinterpret_cast<float4 *>(xh + off) = hv;
-                        *reinterpret_cast<float4 *>(xl + off) = lv;
+                    for (int u = 0; u < 4; ++u) {
+                        const float v = xt[(4 * cg + u) * XR + pos];
+                        const float hi = tf32_hi(v);
+                        hp[u] = hi;
+                        lp[u] = v - hi;
                     }
+                    const uint32_t off = sw128_off(pos, 4 * cg);
+                    *reinterpret_cast<float4 *>(xh + off) = hv;
+                    *reinterpret_cast<float4 *>(xl + off) = lv;
                 }
                 fence_async_smem();
             }
@@ -328,24 +303,15 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             dev::mbar_arrive(&split_x[s]);
         }
     } else {
-        // ---------------- epilogue: two groups of 4 warps (warps 4-7, 8-11); group g
-        // takes channel chunks g, g+2, ...; thread = TMEM lane = tile row
-        const int grp = (warp - 4) >> 2;
-        const int et = (threadIdx.x - 128) & 127;   // tile row of this thread
-        const int ew = warp & 3;                    // TMEM lane quarter
-        const int R = p.R;
-        const int bar_id = 1 + grp;
-        float *stg = reinterpret_cast<float *>(sm + OFF_STG + grp * kStage);
-        float *edge0 = reinterpret_cast<float *>(sm + OFF_EDGE + grp * 2 * kEdge);
-        const int nchunk = p.Cog / kChunk;
-        const int u = et - PAD;                     // output q - q0 of this row
-        const bool has_out = u >= 0 && u < TQ;
+        // ---------------- epilogue (128 threads; thread = TMEM lane = output row)
+        const int et = threadIdx.x - 128;
+        const int ew = warp & 3;
+        float *stg0 = reinterpret_cast<float *>(sm + OFF_STG);
         bool ok = true;
-        int chunk_seq = 0;                          // this group's chunk counter (edge parity)
+        int cs = 0;                                 // chunk counter (staging parity)
         for (int k = 0; k < ntile_cta; ++k) {
             const int tile = blockIdx.x + k * gridDim.x;
             const int n = tile / p.ntq, qt = tile % p.ntq;
-            const int q0 = qt * TQ;
             const int a = k & 1;
             if (ok && !dev::mbar_wait_bounded(&acc_full[a], (k >> 1) & 1, kWaitLimitNs)) {
                 atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
@@ -353,83 +319,46 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             }
             ok = __all_sync(0xffffffffu, ok);      // warp-uniform before .sync.aligned loads
             tc_after();
-            const int o0 = p.S * q0;                // first output position of the run
-            const int nvalid = min(p.S * TQ, p.L_out - o0);
-            if (grp >= nchunk) {                    // nothing to read in this tile
-                tc_before();
-                dev::mbar_arrive(&acc_empty[a]);
-            }
-            for (int ci = grp; ci < nchunk; ci += 2, ++chunk_seq) {
+            const int o0 = p.S * qt * BM;           // first output position of the run
+            const int nvalid = min(p.S * BM, p.L_out - o0);
+            for (int c0 = 0; c0 < p.Cog; c0 += kChunk, ++cs) {
                 __syncwarp();
-                const int c0 = ci * kChunk;
-                float *edge = edge0 + (chunk_seq & 1) * (kEdge / 4);
-                // 1) this row's D values of every tap for channels c0 .. c0+15
-                float d[MAXT][16];
+                float *stg = stg0 + (cs & 1) * (kStage / 4);
+                float v[16];
+                if (ok) {
+                    tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * p.Cog + c0), v);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                for (int j = 0; j < MAXT; ++j)
-                    if (j < p.nT && ok)
-                        tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * 256 + j * p.Cog + c0), d[j]);
-                tmem_wait_ld();
-                if (!ok) {
-#pragma unroll
-                    for (int j = 0; j < MAXT; ++j)
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) d[j][i] = 0.f;
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
                 }
-                if (ci + 2 >= nchunk) {
-                    // this group's last chunk of the tile: done with accumulator a
+                if (c0 + kChunk >= p.Cog) {         // done with accumulator a
                     tc_before();
                     dev::mbar_arrive(&acc_empty[a]);
                 }
-                // 2) rows next to warp edges go to shared memory for the neighbours
-                if (lane < R || lane >= 32 - R) {
-                    const int slot = edge_slot(et, R);
+                // the copies issued two chunks ago must have read this staging buffer
+                if (et < kChunk) bulk_wait_read1();
+                named_bar(1, 128);
+                // stage: residue r* gets acc + bias, the other residues the bias
+                const int64_t g00 = ((int64_t)n * p.C_out + c0) * p.L_out + o0;
 #pragma unroll
-                    for (int j = 0; j < MAXT; ++j)
-                        if (j < p.nT)
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) edge[(j * kEdgeRows + slot) * kChunk + i] = d[j][i];
-                }
-                // the previous chunk's bulk copies must have read the staging buffer
-                if (et < kChunk) bulk_wait_read0();
-                named_bar(bar_id, 128);
-                // 3) v[oc] = sum_j D[row + e_j][(j, oc)]
-                float v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.f;
-#pragma unroll
-                for (int j = 0; j < MAXT; ++j) {
-                    if (j >= p.nT) continue;
-                    const int ej = p.e[j];
-                    const int src = lane + ej;
-                    const int row = et + ej;
-                    const bool inwarp = src >= 0 && src < 32;
-                    const bool use_edge = !inwarp && row >= 0 && row < BM;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float sh = __shfl_sync(0xffffffffu, d[j][i], src & 31);
-                        v[i] += use_edge ? edge[(j * kEdgeRows + edge_slot(row, R)) * kChunk + i] : sh;
-                    }
-                }
-                // 4) stage every channel's run: residue r* gets v + bias, others the bias
-                if (has_out) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int oc = c0 + i;
-                        const int64_t g0 = ((int64_t)n * p.C_out + oc) * p.L_out + o0;
-                        const int ph = (int)(g0 & 3);
-                        const float b = bias ? __ldg(bias + oc) : 0.f;
-                        float *row = stg + i * kRowF + ph + p.S * u;
-                        for (int r = 0; r < p.S; ++r) row[r] = (r == p.rstar ? v[i] : 0.f) + b;
+                for (int i = 0; i < 16; ++i) {
+                    const int ph = (int)((g00 + (int64_t)i * p.L_out) & 3);
+                    const float b = bias ? __ldg(bias + c0 + i) : 0.f;
+                    float *row = stg + i * kRowF + ph + p.S * et;
+                    if (p.S == 2) {
+                        row[0] = (p.rstar == 0 ? v[i] : 0.f) + b;
+                        row[1] = (p.rstar == 1 ? v[i] : 0.f) + b;
+                    } else {
+                        row[0] = v[i] + b;
                     }
                 }
                 fence_async_smem();
-                named_bar(bar_id, 128);
-                // 5) one thread per channel writes its run: bulk body, scalar ends
+                named_bar(1, 128);
+                // one thread per channel writes its run: bulk body, scalar ends
                 if (et < kChunk) {
                     if (nvalid > 0) {
-                        const int oc = c0 + et;
-                        const int64_t g0 = ((int64_t)n * p.C_out + oc) * p.L_out + o0;
+                        const int64_t g0 = g00 + (int64_t)et * p.L_out;
                         const int ph = (int)(g0 & 3);
                         const float *row = stg + et * kRowF + ph;
                         const int head = min((4 - ph) & 3, nvalid);
@@ -449,49 +378,45 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
     __syncthreads();
     if (warp == 1) {
         __syncwarp();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(512) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(p.tmem_cols)
+                     : "memory");
     }
 }
 
 // ---- host side --------------------------------------------------------------------
-struct TPlan {
-    TParams p;
-};
-
-bool make_tplan(const Problem &pb, const Args *a, TPlan *out)
+bool make_tplan(const Problem &pb, const Args *a, TParams *out)
 {
     if (pb.nd != 1 || pb.dtype != CT_F32 || pb.G != 1) return false;
     const int S = pb.S[2], K = pb.K[2], DL = pb.DL[2], P = pb.P[2];
     if (S < 1 || S > MAXS || DL % S != 0 || K > MAXT) return false;
-    if (pb.Cig != CI || pb.Cog % kChunk != 0 || K * pb.Cog > 256) return false;
+    if (pb.Cig != CI || pb.Cog % kChunk != 0 || pb.Cog > 256 || K * pb.Cog > 256) return false;
     if (pb.Li[2] % 4 != 0) return false;                 // TMA: 16-byte row strides of x
     if (a && (((uintptr_t)a->x % 16) || ((uintptr_t)a->y % 16))) return false;
     TParams p;
     memset(&p, 0, sizeof(p));
     p.N = pb.N; p.C_in = pb.C_in; p.C_out = pb.C_out; p.Cog = pb.Cog; p.K = K;
     p.L_in = pb.Li[2]; p.L_out = pb.Lo[2]; p.S = S; p.nT = K;
-    // every tap has k*dl == 0 (mod s): class c = 0, residue r* = (-p) mod s,
-    // base floor((r* + p)/s), tap k reads q + base - k*dl/s
+    // every tap has k*dl == 0 (mod s): residue r* = (-p) mod s receives them,
+    // tap k reads q + floor((r* + p)/s) - k*dl/s
     p.rstar = ((-P) % S + S) % S;
     const int base = (p.rstar + P) / S;
-    p.R = 1;
     for (int j = 0; j < K; ++j) {
         p.k_of[j] = j;
         p.e[j] = base - j * (DL / S);
-        const int ae = p.e[j] < 0 ? -p.e[j] : p.e[j];
-        if (ae > MAXR || ae > PAD) return false;
-        if (ae > p.R) p.R = ae;
+        if (p.e[j] < -PAD || p.e[j] > PAD) return false;
     }
-    p.ncol = K * pb.Cog;
     const int nq = (p.L_out + S - 1) / S;
-    p.ntq = (nq + TQ - 1) / TQ;
+    p.ntq = (nq + BM - 1) / BM;
     const int64_t tiles = (int64_t)pb.N * p.ntq;
     if (tiles > 0x7fffffff) return false;
     p.ntiles = (int)tiles;
-    // tcgen05 instruction descriptor: D fp32, A/B tf32, both K-major
-    p.idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(p.ncol >> 3) << 17) |
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(2 * pb.Cog)) cols <<= 1;
+    p.tmem_cols = cols;
+    // tcgen05 instruction descriptor: D fp32, A/B tf32, both K-major, N = C_out, M = 128
+    p.idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(pb.Cog >> 3) << 17) |
               ((uint32_t)(BM >> 4) << 24);
-    out->p = p;
+    *out = p;
     return true;
 }
 
@@ -499,21 +424,20 @@ bool make_tplan(const Problem &pb, const Args *a, TPlan *out)
 
 bool tc1d_supported(const Problem &pb, const Args *a)
 {
-    TPlan pl;
-    return make_tplan(pb, a, &pl);
+    TParams p;
+    return make_tplan(pb, a, &p);
 }
 
 cudaError_t launch_tc1d(const Problem &pb, const Args &a)
 {
-    TPlan pl;
-    if (!make_tplan(pb, &a, &pl)) return cudaErrorNotSupported;
-    const TParams &p = pl.p;
+    TParams p;
+    if (!make_tplan(pb, &a, &p)) return cudaErrorNotSupported;
     CUtensorMap tmx;
     const uint64_t dims[3] = {(uint64_t)p.L_in, (uint64_t)p.C_in, (uint64_t)p.N};
     const uint64_t strides[2] = {(uint64_t)p.L_in * 4, (uint64_t)p.L_in * p.C_in * 4};
-    const uint32_t box[3] = {32u, (uint32_t)CI, 1u};
+    const uint32_t box[3] = {(uint32_t)XR, (uint32_t)CI, 1u};
     if (!encode_tiled(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.x, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     int per_sm = 0;
     cudaError_t e = prepare_kernel((const void *)&tc1d_tf32_kernel, kThreads, kSmemBytes, &per_sm);
@@ -523,8 +447,7 @@ cudaError_t launch_tc1d(const Problem &pb, const Args &a)
     if (grid > p.ntiles) grid = p.ntiles;
     unsigned int *status = device_status_ptr();
     if (!status) return cudaErrorInvalidValue;
-    tc1d_tf32_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tmx, static_cast<const float *>(a.x),
-                                                               static_cast<const float *>(a.w), a.bias,
+    tc1d_tf32_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tmx, static_cast<const float *>(a.w), a.bias,
                                                                a.y, p, status);
     return cudaGetLastError();
 }

@@ -371,6 +371,15 @@ def roofline(name, cfg, path, wm, sec, peaks):
         return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peaks["source"] + " cuBLAS bf16 burst"}
+    if path == "tc1d_tf32x3":
+        # FP32 on the tensor cores (3 tf32 products per multiply-add): the tensor
+        # time (3x the FLOPs at the tf32 rate, half the bf16 rate) stays below the
+        # HBM time, so the kernel's roofline is its HBM bytes
+        achieved = wm["bytes"] / sec / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": peaks["source"] + " copy bandwidth",
+                "tensor_time_floor_us": round(3 * wm["flops"] / (peaks["bf16_tflops"] / 2 * 1e12) * 1e6, 1)}
     ai = wm["flops"] / wm["bytes"]
     alu_peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
     ridge = alu_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)

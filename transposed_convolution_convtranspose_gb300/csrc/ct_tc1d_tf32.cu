@@ -19,16 +19,20 @@
 // hi*hi + hi*lo + lo*hi in fp32 in TMEM.  The dropped lo*lo term and the
 // tf32 rounding of lo are each below 2^-21 of a product.
 //
-// Roles (persistent CTA of 256 threads, one per SM):
+// Roles (persistent CTA of 320 threads, one per SM):
 //   warp 0      TMA producer: x box [C_in = 32][136 positions] per tile (no
 //               swizzle); positions outside the input read zeros
 //   warp 1      TMEM allocation and MMA issue: taps x 4 K-steps x 3 split
 //               terms of tcgen05.mma M=128, N=C_out, K=8 into one of two TMEM
 //               accumulators (double-buffered across tiles)
-//   warps 2-3   split + transpose: x box -> position-major (K-major) hi and lo
+//   warps 2-5   split + transpose: x box -> position-major (K-major) hi and lo
 //               tiles, 128-byte swizzled; the weights once, per tap, the same way
-//   warps 4-7   epilogue: tcgen05.ld, bias, assemble each channel's s*128
-//               consecutive outputs in shared memory, TMA bulk stores
+//   warps 6-9   epilogue, one TMEM lane quarter (32 outputs q) each: tcgen05.ld,
+//               bias, and per channel the s*32 consecutive outputs rebuilt by
+//               two warp shuffles and written as two coalesced 128-byte stores
+//               (y rows start at arbitrary 4-byte offsets, so no vector or
+//               tensor store applies; every store instruction still covers
+//               whole sectors except at its two ends)
 // Every mbarrier wait is bounded; a timeout records CT_ERR_DEVICE_TIMEOUT in
 // the device status word and the roles unwind.
 #include <string.h>
@@ -40,7 +44,7 @@
 namespace ct {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;
 constexpr int BM = 128;          // outputs per tile (UMMA M)
 constexpr int PAD = 4;           // stored rows before the first output (16-byte TMA start)
 constexpr int XR = BM + 2 * PAD; // stored input positions per tile
@@ -118,16 +122,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
-__device__ __forceinline__ void bulk_store(float *g, const float *s, unsigned bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(g),
-                 "r"(dev::smem_u32(s)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
-__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
 
 // byte offset of element (row, k) in a K-major 128-byte-swizzled tile of
 // 32-bit elements (the 16-byte chunk index is XORed with the row's phase)
@@ -140,17 +134,14 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int k)
 constexpr uint32_t kXRaw = CI * XR * 4;                  // TMA box [32][136] fp32
 constexpr uint32_t kXK = XR * 128;                       // K-major 136 rows (17 atoms)
 constexpr uint32_t kWTile = 256 * 128;                   // up to taps*C_out = 256 rows
-constexpr int kChunk = 16;                               // output channels per epilogue chunk
-constexpr int kRowF = MAXS * BM + 8;                     // floats per staged output row
-constexpr uint32_t kStage = kChunk * kRowF * 4;
+constexpr int kChunk = 16;                               // output channels per TMEM load
 
 constexpr uint32_t OFF_XT = 0;
 constexpr uint32_t OFF_XHI = OFF_XT + NS * kXRaw;
 constexpr uint32_t OFF_XLO = OFF_XHI + NS * kXK;
 constexpr uint32_t OFF_WHI = OFF_XLO + NS * kXK;
 constexpr uint32_t OFF_WLO = OFF_WHI + kWTile;
-constexpr uint32_t OFF_STG = OFF_WLO + kWTile;
-constexpr uint32_t kSmemBytes = OFF_STG + 2 * kStage + 1024;   // + alignment slack
+constexpr uint32_t kSmemBytes = OFF_WLO + kWTile + 1024;   // + alignment slack
 static_assert(kXRaw % 1024 == 0 && kXK % 1024 == 0, "1024-byte aligned tiles");
 static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
 
@@ -169,15 +160,15 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
         dev::prefetch_tensormap(&tmx);
         for (int s = 0; s < NS; ++s) {
             dev::mbar_init(&full_x[s], 1);
-            dev::mbar_init(&xt_free[s], 64);
-            dev::mbar_init(&split_x[s], 64);
+            dev::mbar_init(&xt_free[s], 128);
+            dev::mbar_init(&split_x[s], 128);
             dev::mbar_init(&empty_x[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             dev::mbar_init(&acc_full[a], 1);
-            dev::mbar_init(&acc_empty[a], 128);
+            dev::mbar_init(&acc_empty[a], 128);   // the 4 epilogue warps
         }
-        dev::mbar_init(&w_ready, 64);
+        dev::mbar_init(&w_ready, 128);
         dev::fence_mbar_init();
     }
     if (warp == 1) {
@@ -255,11 +246,11 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             }
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
-    } else if (warp < 4) {
-        // ---------------- split + transpose warps (64 threads)
+    } else if (warp < 6) {
+        // ---------------- split + transpose warps (128 threads)
         const int st = threadIdx.x - 64;
         // weights once: tap j's rows j*Cog + oc, K = ic; hi/lo, K-major swizzled
-        for (int e = st; e < p.nT * p.Cog * CI; e += 64) {
+        for (int e = st; e < p.nT * p.Cog * CI; e += 128) {
             const int n = e / CI, ic = e % CI;
             const int j = n / p.Cog, oc = n % p.Cog;
             const float v = __ldg(w + ((int64_t)ic * p.Cog + oc) * p.K + p.k_of[j]);
@@ -282,7 +273,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
                 const float *xt = reinterpret_cast<const float *>(sm + OFF_XT + s * kXRaw);   // [ic][pos]
                 uint8_t *xh = sm + OFF_XHI + s * kXK;
                 uint8_t *xl = sm + OFF_XLO + s * kXK;
-                for (int e = st; e < XR * (CI / 4); e += 64) {
+                for (int e = st; e < XR * (CI / 4); e += 128) {
                     const int pos = e % XR, cg = e / XR;
                     float4 hv, lv;
                     float *hp = &hv.x, *lp = &lv.x;
@@ -303,12 +294,10 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             dev::mbar_arrive(&split_x[s]);
         }
     } else {
-        // ---------------- epilogue (128 threads; thread = TMEM lane = output row)
-        const int et = threadIdx.x - 128;
-        const int ew = warp & 3;
-        float *stg0 = reinterpret_cast<float *>(sm + OFF_STG);
+        // ---------------- epilogue: warps 6-9, each on its own TMEM lane quarter
+        // (32 rows = 32 consecutive outputs q); no shared memory, no CTA barrier
+        const int ew = warp & 3;                    // lanes 32*ew .. 32*ew + 31
         bool ok = true;
-        int cs = 0;                                 // chunk counter (staging parity)
         for (int k = 0; k < ntile_cta; ++k) {
             const int tile = blockIdx.x + k * gridDim.x;
             const int n = tile / p.ntq, qt = tile % p.ntq;
@@ -319,11 +308,11 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             }
             ok = __all_sync(0xffffffffu, ok);      // warp-uniform before .sync.aligned loads
             tc_after();
-            const int o0 = p.S * qt * BM;           // first output position of the run
-            const int nvalid = min(p.S * BM, p.L_out - o0);
-            for (int c0 = 0; c0 < p.Cog; c0 += kChunk, ++cs) {
-                __syncwarp();
-                float *stg = stg0 + (cs & 1) * (kStage / 4);
+            // this warp's outputs: positions o_w .. o_w + s*32 - 1 of every channel row
+            const int o_w = p.S * (qt * BM + 32 * ew);
+            const int nv = min(p.S * 32, p.L_out - o_w);   // may be <= 0 past the end
+            float *yw = y + (int64_t)n * p.C_out * p.L_out + o_w;
+            for (int c0 = 0; c0 < p.Cog; c0 += kChunk) {
                 float v[16];
                 if (ok) {
                     tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * p.Cog + c0), v);
@@ -336,42 +325,25 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
                     tc_before();
                     dev::mbar_arrive(&acc_empty[a]);
                 }
-                // the copies issued two chunks ago must have read this staging buffer
-                if (et < kChunk) bulk_wait_read1();
-                named_bar(1, 128);
-                // stage: residue r* gets acc + bias, the other residues the bias
-                const int64_t g00 = ((int64_t)n * p.C_out + c0) * p.L_out + o0;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int ph = (int)((g00 + (int64_t)i * p.L_out) & 3);
-                    const float b = bias ? __ldg(bias + c0 + i) : 0.f;
-                    float *row = stg + i * kRowF + ph + p.S * et;
+                    const int oc = c0 + i;
+                    const float b = bias ? __ldg(bias + oc) : 0.f;
+                    float *row = yw + (int64_t)oc * p.L_out;
                     if (p.S == 2) {
-                        row[0] = (p.rstar == 0 ? v[i] : 0.f) + b;
-                        row[1] = (p.rstar == 1 ? v[i] : 0.f) + b;
+                        // lane l writes positions o_w + l and o_w + 32 + l: output q
+                        // (l >> 1) resp. 16 + (l >> 1) of this warp, residue l & 1
+                        const float s0 = __shfl_sync(0xffffffffu, v[i], lane >> 1);
+                        const float s1 = __shfl_sync(0xffffffffu, v[i], 16 + (lane >> 1));
+                        const bool hit = (lane & 1) == p.rstar;
+                        if (lane < nv) __stcs(row + lane, (hit ? s0 : 0.f) + b);
+                        if (32 + lane < nv) __stcs(row + 32 + lane, (hit ? s1 : 0.f) + b);
                     } else {
-                        row[0] = v[i] + b;
+                        if (lane < nv) __stcs(row + lane, v[i] + b);
                     }
-                }
-                fence_async_smem();
-                named_bar(1, 128);
-                // one thread per channel writes its run: bulk body, scalar ends
-                if (et < kChunk) {
-                    if (nvalid > 0) {
-                        const int64_t g0 = g00 + (int64_t)et * p.L_out;
-                        const int ph = (int)(g0 & 3);
-                        const float *row = stg + et * kRowF + ph;
-                        const int head = min((4 - ph) & 3, nvalid);
-                        const int body = ((nvalid - head) >> 2) << 2;
-                        for (int t = 0; t < head; ++t) y[g0 + t] = row[t];
-                        if (body > 0) bulk_store(y + g0 + head, row + head, (unsigned)body * 4u);
-                        for (int t = head + body; t < nvalid; ++t) y[g0 + t] = row[t];
-                    }
-                    bulk_commit();
                 }
             }
         }
-        if (et < kChunk) bulk_wait_all();
     }
 
     tc_before();

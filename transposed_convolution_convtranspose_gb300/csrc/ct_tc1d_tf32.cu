@@ -19,7 +19,7 @@
 // hi*hi + hi*lo + lo*hi in fp32 in TMEM.  The dropped lo*lo term and the
 // tf32 rounding of lo are each below 2^-21 of a product.
 //
-// Roles (persistent CTA of 320 threads, one per SM):
+// Roles (persistent CTA of 448 threads, one per SM):
 //   warp 0      TMA producer: x box [C_in = 32][136 positions] per tile (no
 //               swizzle); positions outside the input read zeros
 //   warp 1      TMEM allocation and MMA issue: taps x 4 K-steps x 3 split
@@ -27,9 +27,10 @@
 //               accumulators (double-buffered across tiles)
 //   warps 2-5   split + transpose: x box -> position-major (K-major) hi and lo
 //               tiles, 128-byte swizzled; the weights once, per tap, the same way
-//   warps 6-9   epilogue, one TMEM lane quarter (32 outputs q) each: tcgen05.ld,
-//               bias, and per channel the s*32 consecutive outputs rebuilt by
-//               two warp shuffles and written as two coalesced 128-byte stores
+//   warps 6-13  epilogue, two warps per TMEM lane quarter (32 outputs q) taking
+//               alternate 16-channel chunks: tcgen05.ld, bias, and per channel
+//               the s*32 consecutive outputs rebuilt by two warp shuffles and
+//               written as two coalesced 128-byte stores
 //               (y rows start at arbitrary 4-byte offsets, so no vector or
 //               tensor store applies; every store instruction still covers
 //               whole sectors except at its two ends)
@@ -44,7 +45,7 @@
 namespace ct {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int BM = 128;          // outputs per tile (UMMA M)
 constexpr int PAD = 4;           // stored rows before the first output (16-byte TMA start)
 constexpr int XR = BM + 2 * PAD; // stored input positions per tile
@@ -135,6 +136,7 @@ constexpr uint32_t kXRaw = CI * XR * 4;                  // TMA box [32][136] fp
 constexpr uint32_t kXK = XR * 128;                       // K-major 136 rows (17 atoms)
 constexpr uint32_t kWTile = 256 * 128;                   // up to taps*C_out = 256 rows
 constexpr int kChunk = 16;                               // output channels per TMEM load
+constexpr int kBatch = 4;                                // TMEM loads in flight per warp
 
 constexpr uint32_t OFF_XT = 0;
 constexpr uint32_t OFF_XHI = OFF_XT + NS * kXRaw;
@@ -166,7 +168,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
         }
         for (int a = 0; a < 2; ++a) {
             dev::mbar_init(&acc_full[a], 1);
-            dev::mbar_init(&acc_empty[a], 128);   // the 4 epilogue warps
+            dev::mbar_init(&acc_empty[a], 256);   // the 8 epilogue warps
         }
         dev::mbar_init(&w_ready, 128);
         dev::fence_mbar_init();
@@ -294,9 +296,13 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             dev::mbar_arrive(&split_x[s]);
         }
     } else {
-        // ---------------- epilogue: warps 6-9, each on its own TMEM lane quarter
-        // (32 rows = 32 consecutive outputs q); no shared memory, no CTA barrier
+        // ---------------- epilogue: warps 6-13, two per TMEM lane quarter (32 rows =
+        // 32 consecutive outputs q); the two take alternate 16-channel chunks.
+        // All TMEM loads of a batch are issued before one wait, the accumulator
+        // is released, then the stores run from registers.
         const int ew = warp & 3;                    // lanes 32*ew .. 32*ew + 31
+        const int half = (warp - 6) >> 2;           // 0 or 1
+        const int nchunk = p.Cog / kChunk;
         bool ok = true;
         for (int k = 0; k < ntile_cta; ++k) {
             const int tile = blockIdx.x + k * gridDim.x;
@@ -312,36 +318,53 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             const int o_w = p.S * (qt * BM + 32 * ew);
             const int nv = min(p.S * 32, p.L_out - o_w);   // may be <= 0 past the end
             float *yw = y + (int64_t)n * p.C_out * p.L_out + o_w;
-            for (int c0 = 0; c0 < p.Cog; c0 += kChunk) {
-                float v[16];
-                if (ok) {
-                    tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * p.Cog + c0), v);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            // chunks half, half + 2, ... in batches of up to kBatch chunks
+            int ci = half;
+            bool released = false;
+            while (true) {
+                float v[kBatch][16];
+                int nb = 0;
+                for (; nb < kBatch && ci + 2 * nb < nchunk; ++nb) {
+                    if (ok)
+                        tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * p.Cog + (ci + 2 * nb) * kChunk),
+                                  v[nb]);
                 }
-                if (c0 + kChunk >= p.Cog) {         // done with accumulator a
+                if (ok && nb > 0) tmem_wait_ld();
+                if (!ok)
+#pragma unroll
+                    for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[b][i] = 0.f;
+                const bool last = ci + 2 * nb >= nchunk;
+                if (last && !released) {            // done with accumulator a
                     tc_before();
                     dev::mbar_arrive(&acc_empty[a]);
+                    released = true;
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int oc = c0 + i;
-                    const float b = bias ? __ldg(bias + oc) : 0.f;
-                    float *row = yw + (int64_t)oc * p.L_out;
-                    if (p.S == 2) {
-                        // lane l writes positions o_w + l and o_w + 32 + l: output q
-                        // (l >> 1) resp. 16 + (l >> 1) of this warp, residue l & 1
-                        const float s0 = __shfl_sync(0xffffffffu, v[i], lane >> 1);
-                        const float s1 = __shfl_sync(0xffffffffu, v[i], 16 + (lane >> 1));
-                        const bool hit = (lane & 1) == p.rstar;
-                        if (lane < nv) __stcs(row + lane, (hit ? s0 : 0.f) + b);
-                        if (32 + lane < nv) __stcs(row + 32 + lane, (hit ? s1 : 0.f) + b);
-                    } else {
-                        if (lane < nv) __stcs(row + lane, v[i] + b);
+                for (int b = 0; b < kBatch; ++b) {
+                    if (b >= nb) break;
+                    const int c0 = (ci + 2 * b) * kChunk;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int oc = c0 + i;
+                        const float bb = bias ? __ldg(bias + oc) : 0.f;
+                        float *row = yw + (int64_t)oc * p.L_out;
+                        if (p.S == 2) {
+                            // lane l writes positions o_w + l and o_w + 32 + l: output q
+                            // (l >> 1) resp. 16 + (l >> 1) of this warp, residue l & 1
+                            const float s0 = __shfl_sync(0xffffffffu, v[b][i], lane >> 1);
+                            const float s1 = __shfl_sync(0xffffffffu, v[b][i], 16 + (lane >> 1));
+                            const bool hit = (lane & 1) == p.rstar;
+                            if (lane < nv) __stcs(row + lane, (hit ? s0 : 0.f) + bb);
+                            if (32 + lane < nv) __stcs(row + 32 + lane, (hit ? s1 : 0.f) + bb);
+                        } else {
+                            if (lane < nv) __stcs(row + lane, v[b][i] + bb);
+                        }
                     }
                 }
+                ci += 2 * nb;
+                if (last) break;
             }
         }
     }

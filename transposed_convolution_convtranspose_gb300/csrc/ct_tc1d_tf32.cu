@@ -19,7 +19,7 @@
 // hi*hi + hi*lo + lo*hi in fp32 in TMEM.  The dropped lo*lo term and the
 // tf32 rounding of lo are each below 2^-21 of a product.
 //
-// Roles (persistent CTA of 448 threads, one per SM):
+// Roles (persistent CTA of 32 * (6 + 4 * EPW) threads, one per SM):
 //   warp 0      TMA producer: x box [C_in = 32][136 positions] per tile (no
 //               swizzle); positions outside the input read zeros
 //   warp 1      TMEM allocation and MMA issue: taps x 4 K-steps x 3 split
@@ -27,8 +27,8 @@
 //               accumulators (double-buffered across tiles)
 //   warps 2-5   split + transpose: x box -> position-major (K-major) hi and lo
 //               tiles, 128-byte swizzled; the weights once, per tap, the same way
-//   warps 6-13  epilogue, two warps per TMEM lane quarter (32 outputs q) taking
-//               alternate 16-channel chunks: tcgen05.ld, bias, and per channel
+//   warps 6..   epilogue, EPW warps per TMEM lane quarter (32 outputs q)
+//               taking interleaved 16-channel chunks: tcgen05.ld, bias, and per channel
 //               the s*32 consecutive outputs rebuilt by two warp shuffles and
 //               written as two coalesced 128-byte stores
 //               (y rows start at arbitrary 4-byte offsets, so no vector or
@@ -45,7 +45,8 @@
 namespace ct {
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int EPW = 4;           // epilogue warps per TMEM lane quarter
+constexpr int kThreads = 32 * (6 + 4 * EPW);
 constexpr int BM = 128;          // outputs per tile (UMMA M)
 constexpr int PAD = 4;           // stored rows before the first output (16-byte TMA start)
 constexpr int XR = BM + 2 * PAD; // stored input positions per tile
@@ -136,7 +137,7 @@ constexpr uint32_t kXRaw = CI * XR * 4;                  // TMA box [32][136] fp
 constexpr uint32_t kXK = XR * 128;                       // K-major 136 rows (17 atoms)
 constexpr uint32_t kWTile = 256 * 128;                   // up to taps*C_out = 256 rows
 constexpr int kChunk = 16;                               // output channels per TMEM load
-constexpr int kBatch = 4;                                // TMEM loads in flight per warp
+constexpr int kBatch = 2;                                // TMEM loads in flight per warp
 
 constexpr uint32_t OFF_XT = 0;
 constexpr uint32_t OFF_XHI = OFF_XT + NS * kXRaw;
@@ -168,7 +169,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
         }
         for (int a = 0; a < 2; ++a) {
             dev::mbar_init(&acc_full[a], 1);
-            dev::mbar_init(&acc_empty[a], 256);   // the 8 epilogue warps
+            dev::mbar_init(&acc_empty[a], 128 * EPW);   // every epilogue thread
         }
         dev::mbar_init(&w_ready, 128);
         dev::fence_mbar_init();
@@ -301,7 +302,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
         // All TMEM loads of a batch are issued before one wait, the accumulator
         // is released, then the stores run from registers.
         const int ew = warp & 3;                    // lanes 32*ew .. 32*ew + 31
-        const int half = (warp - 6) >> 2;           // 0 or 1
+        const int half = (warp - 6) >> 2;           // 0 .. EPW-1
         const int nchunk = p.Cog / kChunk;
         bool ok = true;
         for (int k = 0; k < ntile_cta; ++k) {
@@ -324,9 +325,9 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             while (true) {
                 float v[kBatch][16];
                 int nb = 0;
-                for (; nb < kBatch && ci + 2 * nb < nchunk; ++nb) {
+                for (; nb < kBatch && ci + EPW * nb < nchunk; ++nb) {
                     if (ok)
-                        tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * p.Cog + (ci + 2 * nb) * kChunk),
+                        tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * p.Cog + (ci + EPW * nb) * kChunk),
                                   v[nb]);
                 }
                 if (ok && nb > 0) tmem_wait_ld();
@@ -335,7 +336,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
                     for (int b = 0; b < kBatch; ++b)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) v[b][i] = 0.f;
-                const bool last = ci + 2 * nb >= nchunk;
+                const bool last = ci + EPW * nb >= nchunk;
                 if (last && !released) {            // done with accumulator a
                     tc_before();
                     dev::mbar_arrive(&acc_empty[a]);
@@ -344,7 +345,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b) {
                     if (b >= nb) break;
-                    const int c0 = (ci + 2 * b) * kChunk;
+                    const int c0 = (ci + EPW * b) * kChunk;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int oc = c0 + i;
@@ -363,7 +364,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
                         }
                     }
                 }
-                ci += 2 * nb;
+                ci += EPW * nb;
                 if (last) break;
             }
         }

@@ -259,7 +259,7 @@ class Runner:
         self.ws = (torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
                    if self.ws_bytes else None)
         # kernels the library launches per forward pass on this path
-        self.launches_per_step = {"umma_bf16": 3}.get(self.path, 1)
+        self.launches_per_step = {"umma_bf16": 3, "tc3d_tf32x3": 3}.get(self.path, 1)
 
     def forward(self, stream):
         c, d, ct = self.cfg, self.d, self.ct
@@ -371,15 +371,25 @@ def roofline(name, cfg, path, wm, sec, peaks):
         return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peaks["source"] + " cuBLAS bf16 burst"}
-    if path == "tc1d_tf32x3":
-        # FP32 on the tensor cores (3 tf32 products per multiply-add): the tensor
-        # time (3x the FLOPs at the tf32 rate, half the bf16 rate) stays below the
-        # HBM time, so the kernel's roofline is its HBM bytes
-        achieved = wm["bytes"] / sec / 1e9
-        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "peak_source": peaks["source"] + " copy bandwidth",
-                "tensor_time_floor_us": round(3 * wm["flops"] / (peaks["bf16_tflops"] / 2 * 1e12) * 1e6, 1)}
+    if path in ("tc1d_tf32x3", "tc3d_tf32x3"):
+        # FP32 on the tensor cores: 3 tf32 products per multiply-add at the tf32
+        # rate (half the bf16 rate).  The roofline is the slower of that tensor
+        # time and the HBM time of the algorithmic bytes.
+        tensor_s = 3 * wm["flops"] / (peaks["bf16_tflops"] / 2 * 1e12)
+        hbm_s = wm["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        if hbm_s >= tensor_s:
+            achieved = wm["bytes"] / sec / 1e9
+            return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                    "peak_source": peaks["source"] + " copy bandwidth",
+                    "tensor_time_floor_us": round(tensor_s * 1e6, 1)}
+        achieved = 3 * wm["flops"] / sec / 1e12
+        peak = peaks["bf16_tflops"] / 2
+        return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
+                "unit": "TFLOP/s (tf32, 3 products per multiply-add)",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": peaks["source"] + " cuBLAS bf16 burst / 2 (tf32)",
+                "hbm_time_floor_us": round(hbm_s * 1e6, 1)}
     ai = wm["flops"] / wm["bytes"]
     alu_peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])
     ridge = alu_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)

@@ -37,10 +37,13 @@
  * Execution: every forward call only validates its arguments on the host,
  * then enqueues kernels on `stream` (a cudaStream_t; NULL = the legacy
  * default stream) and returns; nothing is synchronised and nothing is
- * allocated.  Paths that need scratch memory (the bf16 tensor-core path)
- * take it from the caller-supplied `workspace` of at least the size that
- * ct_workspace_size_* reports (256-byte aligned); other paths need none and
- * accept workspace = NULL, ws_bytes = 0.
+ * allocated.  The tensor-core paths keep repacked operands in scratch memory
+ * taken from the caller-supplied `workspace` of at least the size that
+ * ct_workspace_size_* reports (256-byte aligned).  The bf16 path requires it
+ * (CT_ERR_WORKSPACE otherwise); a FP32 3-D call given less than the reported
+ * size runs the FFMA kernel instead, with the same results up to rounding.
+ * Paths that report 0 accept workspace = NULL, ws_bytes = 0.  The workspace
+ * is overwritten; calls that share one must not overlap on the GPU.
  *
  * Errors: argument and shape errors are returned synchronously before any
  * launch and leave y untouched.  A failed launch returns CT_ERR_CUDA.  The
@@ -76,8 +79,9 @@ typedef enum { CT_F32 = 0, CT_BF16 = 1 } ct_dtype;
  * or -1 if the parameters are invalid (k, s, dl < 1; p, op < 0; result < 1). */
 int64_t ct_out_len(int64_t L_in, int k, int s, int p, int op, int dl);
 
-/* Scratch bytes a forward call with these arguments needs (0 for the FP32
- * paths).  Same argument meaning as the forward calls below. */
+/* Scratch bytes a forward call with these arguments needs to take its
+ * fastest path (0 when that path needs none).  Same argument meaning as the
+ * forward calls below. */
 ct_status ct_workspace_size_1d(int N, int C_in, int C_out, int L_in, int k, int groups,
                                int stride, int padding, int output_padding, int dilation,
                                ct_dtype dtype, size_t *bytes);
@@ -145,9 +149,10 @@ ct_status ct_forward_3d_noalloc(const void *x, const void *w, const float *bias,
                                 ct_dtype dtype, void *stream);
 
 /* Name of the kernel family the 1-D / 3-D / fused call with these arguments
- * would launch ("gather_generic", "phase1d_f32", "tc1d_tf32x3", "phase3d_f32",
- * "umma_bf16", ...), or NULL if the arguments are invalid.  Host only; launches nothing.
- * `fused` selects the add + hardswish variant for the 3-D query. */
+ * would launch when given the workspace ct_workspace_size_* reports
+ * ("gather_generic", "phase1d_f32", "tc1d_tf32x3", "phase3d_f32", "tc3d_tf32x3",
+ * "umma_bf16"), or NULL if the arguments are invalid.  Host only; launches
+ * nothing.  `fused` selects the add + hardswish variant for the 3-D query. */
 const char *ct_path_1d(int N, int C_in, int C_out, int L_in, int k, int groups, int stride,
                        int padding, int output_padding, int dilation, ct_dtype dtype);
 const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
@@ -157,7 +162,7 @@ const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const in
 
 /* Process-wide path override for testing the dispatcher: 0 = automatic
  * (default), 1 = always use the generic gather kernel, 2 = automatic but
- * without the FP32 tensor-core path (the FFMA phase kernels instead).  Not
+ * without the FP32 tensor-core paths (the FFMA phase kernels instead).  Not
  * thread-safe against concurrent forward calls. */
 void ct_set_path_override(int mode);
 

@@ -122,10 +122,27 @@ def test_path_selection(lib):
                              (1, 1, 1), (1, 1, 1), ct.CT_F32) == "gather_generic"
     finally:
         ct.ct_set_path_override(0)
+    # the fused workload: FP32 tensor-core path, FFMA kernel under override 2
+    fused = (128, 32, 64, (16, 16, 16), (3, 3, 3), 1, (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1),
+             ct.CT_F32, 1)
+    assert ct.ct_path_3d(*fused) == "tc3d_tf32x3"
+    ct.ct_set_path_override(2)
+    try:
+        assert ct.ct_path_3d(*fused) == "phase3d_f32"
+    finally:
+        ct.ct_set_path_override(0)
 
 
 def test_workspace_sizes(lib):
     assert ct.ct_workspace_size_1d(16, 32, 64, 131072, 3, 1, 2, 1, 0, 2, ct.CT_F32) == 0
+    # FP32 3-D tensor-core path: channels-last hi and lo copies of x, hi and lo
+    # per-tap weight panels
+    nf = ct.ct_workspace_size_3d(128, 32, 64, (16, 16, 16), (3, 3, 3), 1, (2, 2, 2), (1, 1, 1),
+                                 (1, 1, 1), (1, 1, 1), ct.CT_F32)
+    assert nf >= 2 * 128 * 32 * 16 ** 3 * 4 + 2 * 27 * 64 * 32 * 4
+    # the grouped workload has no tensor-core path: no workspace
+    assert ct.ct_workspace_size_3d(8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3),
+                                   (1, 1, 1), (1, 1, 1), ct.CT_F32) == 0
     nb = ct.ct_workspace_size_3d(16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1),
                                  (0, 0, 0), (1, 1, 1), ct.CT_BF16)
     path = ct.ct_path_3d(16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1),

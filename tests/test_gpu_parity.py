@@ -150,6 +150,83 @@ def test_random_fused_and_bf16_generic():
         cc.assert_close(y, cc.run_oracle(c, t), c["dtype"], "case %d %r" % (k, c))
 
 
+# Shapes for the bf16 tensor-core path: stride 2, even kernel extents (taps
+# per dimension 1..4), even and odd padding (input W offsets shared by both W
+# phases or not), C_out from 16 (one 16-channel chunk, N = 2 C_out = 32) to
+# 256 (N = 2 C_out too wide for one MMA, a single TMEM accumulator), ragged
+# H blocks and odd D, and one case with several tiles per persistent CTA.
+UMMA = [
+    dict(N=1, C_in=64, C_out=16, L=[2, 3, 8], K=[4] * 3, P=[1] * 3, OP=[1, 0, 0]),
+    dict(N=1, C_in=64, C_out=32, L=[3, 2, 4], K=[2] * 3, P=[0] * 3, OP=[0, 1, 0]),
+    dict(N=1, C_in=64, C_out=48, L=[2, 2, 9], K=[2] * 3, P=[1] * 3, OP=[0, 0, 0]),
+    dict(N=2, C_in=128, C_out=128, L=[2, 4, 16], K=[4] * 3, P=[1] * 3, OP=[0, 0, 0]),
+    dict(N=1, C_in=64, C_out=256, L=[2, 2, 8], K=[4] * 3, P=[1] * 3, OP=[1, 1, 0]),
+    dict(N=1, C_in=64, C_out=64, L=[2, 3, 4], K=[6] * 3, P=[2] * 3, OP=[0, 0, 0]),
+    dict(N=1, C_in=64, C_out=64, L=[2, 2, 4], K=[8] * 3, P=[3] * 3, OP=[0, 0, 0]),
+    dict(N=1, C_in=64, C_out=96, L=[2, 3, 7], K=[4] * 3, P=[0] * 3, OP=[0, 0, 0]),
+    dict(N=1, C_in=64, C_out=64, L=[3, 5, 16], K=[4] * 3, P=[1] * 3, OP=[1, 1, 0]),
+    dict(N=8, C_in=64, C_out=16, L=[16, 16, 16], K=[2] * 3, P=[0] * 3, OP=[0, 0, 0]),
+]
+
+
+@pytest.mark.parametrize("k", range(len(UMMA)))
+def test_bf16_tensor_core_shapes(k):
+    c = dict(nd=3, G=1, S=[2, 2, 2], DL=[1, 1, 1], bias=bool(k % 2 == 0), add=False,
+             dtype="bf16", **UMMA[k])
+    assert path_of(c) == "umma_bf16", (c, path_of(c))
+    t = cc.make_inputs(c, seed=700 + k)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), "bf16", "umma case %d %r" % (k, c))
+
+
+# Shapes for the FP32 3-D tensor-core path (stride 2, dilation 1, kernel
+# extents 2..4 mixed across dimensions, padding even and odd): C_in 32 and 64
+# (one and two K blocks), C_out 16 (one chunk) to 128 (a single set of TMEM
+# accumulators), odd D and H output extents, and a case with several units
+# per persistent CTA; every case runs plain and with the fused add epilogue.
+TC3D = [
+    dict(N=2, C_in=32, C_out=64, L=[3, 4, 8], K=[3, 3, 3], P=[1, 1, 1], OP=[1, 1, 1]),
+    dict(N=1, C_in=64, C_out=32, L=[2, 3, 4], K=[4, 4, 4], P=[1, 1, 1], OP=[0, 0, 0]),
+    dict(N=1, C_in=32, C_out=16, L=[3, 2, 8], K=[2, 3, 4], P=[0, 1, 1], OP=[1, 0, 0]),
+    dict(N=1, C_in=32, C_out=128, L=[2, 2, 4], K=[3, 3, 3], P=[1, 1, 1], OP=[1, 1, 1]),
+    dict(N=1, C_in=32, C_out=48, L=[2, 5, 16], K=[3, 3, 3], P=[0, 2, 1], OP=[0, 1, 1]),
+    dict(N=16, C_in=32, C_out=16, L=[8, 16, 16], K=[2, 2, 2], P=[0, 0, 0], OP=[0, 0, 0]),
+]
+
+
+@pytest.mark.parametrize("add", [False, True])
+@pytest.mark.parametrize("k", range(len(TC3D)))
+def test_fp32_3d_tensor_core_shapes(k, add):
+    c = dict(nd=3, G=1, S=[2, 2, 2], DL=[1, 1, 1], bias=bool(k % 2 == 0), add=add, dtype="f32",
+             **TC3D[k])
+    assert path_of(c) == "tc3d_tf32x3", (c, path_of(c))
+    t = cc.make_inputs(c, seed=800 + k + (50 if add else 0))
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), "f32", "tc3d case %d add=%s %r" % (k, add, c))
+
+
+def test_fp32_3d_without_workspace_takes_ffma():
+    """A call given no workspace runs the FFMA kernel, with the same result."""
+    import torch
+    import transposed_convolution_convtranspose_gb300 as ct
+    c = dict(nd=3, G=1, S=[2, 2, 2], DL=[1, 1, 1], bias=True, add=True, dtype="f32", **TC3D[0])
+    t = cc.make_inputs(c, seed=870)
+    x, w, b, a = cc.to_device(t, c, "cuda:0")
+    y = torch.empty(cc.out_shape(c), device="cuda:0")
+    ct.ct_forward_3d_add_hswish(x, w, b, a, y, c["N"], c["C_in"], c["C_out"], c["L"], c["K"], 1,
+                                c["S"], c["P"], c["OP"], c["DL"], ct.CT_F32, None, 0,
+                                torch.cuda.current_stream())
+    ref = cc.run_oracle(c, t)
+    cc.assert_close(y.cpu().numpy(), ref, "f32", "fused without workspace")
+    ct.ct_set_path_override(2)
+    try:
+        assert path_of(c) == "phase3d_f32"
+        y2 = cc.run_gpu(c, t).cpu().numpy()
+    finally:
+        ct.ct_set_path_override(0)
+    cc.assert_close(y2, ref, "f32", "fused, FFMA kernel forced")
+
+
 EDGE = [
     # 1-D: single input, unit kernel, stride larger than kernel (empty phases),
     # large dilation, maximal output_padding, depthwise groups, ragged lengths

@@ -96,7 +96,7 @@ ct_status make_problem(int nd, int N, int C_in, int C_out, const int *Li, const 
     return CT_OK;
 }
 
-enum class Path { Generic, Phase1d, Phase3d, Umma, Tc1d };
+enum class Path { Generic, Phase1d, Phase3d, Umma, Tc1d, Tc3d };
 
 Path choose_path(const Problem &pb, const Args *a)
 {
@@ -105,6 +105,12 @@ Path choose_path(const Problem &pb, const Args *a)
     if (pb.dtype == CT_F32) {
         if (ov != 2 && pb.nd == 1 && tc1d_supported(pb, a)) return Path::Tc1d;
         if (pb.nd == 1 && phase1d_supported(pb, a)) return Path::Phase1d;
+        // the 3-D tensor-core path works in the caller's workspace: a call without
+        // enough of it takes the FFMA kernel (a query without arguments, a == NULL,
+        // reports the tensor-core path and its workspace size)
+        if (ov != 2 && pb.nd == 3 && tc3d_supported(pb, a) &&
+            (!a || (a->ws && ((uintptr_t)a->ws % 256) == 0 && a->ws_bytes >= tc3d_workspace_bytes(pb))))
+            return Path::Tc3d;
         if (pb.nd == 3 && phase3d_supported(pb, a)) return Path::Phase3d;
     } else {
         if (pb.nd == 3 && umma_supported(pb, a)) return Path::Umma;
@@ -120,11 +126,22 @@ const char *path_name(Path p)
     case Path::Phase3d: return "phase3d_f32";
     case Path::Umma: return "umma_bf16";
     case Path::Tc1d: return "tc1d_tf32x3";
+    case Path::Tc3d: return "tc3d_tf32x3";
     }
     return "gather_generic";
 }
 
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Scratch bytes of the path a call with these arguments takes when given it.
+size_t workspace_bytes(const Problem &pb)
+{
+    switch (choose_path(pb, nullptr)) {
+    case Path::Umma: return umma_workspace_bytes(pb);
+    case Path::Tc3d: return tc3d_workspace_bytes(pb);
+    default: return 0;
+    }
+}
 
 bool overlaps(const void *a, size_t an, const void *b, size_t bn)
 {
@@ -161,6 +178,7 @@ ct_status run(const Problem &pb, Args a)
     case Path::Phase3d: e = launch_phase3d(pb, a); break;
     case Path::Umma: e = launch_umma(pb, a); break;
     case Path::Tc1d: e = launch_tc1d(pb, a); break;
+    case Path::Tc3d: e = launch_tc3d(pb, a); break;
     }
     return e == cudaSuccess ? CT_OK : CT_ERR_CUDA;
 }
@@ -198,7 +216,7 @@ ct_status ct_workspace_size_1d(int N, int C_in, int C_out, int L_in, int k, int 
     ct_status st = make_problem(1, N, C_in, C_out, &L_in, &k, groups, &stride, &padding,
                                 &output_padding, &dilation, dtype, false, false, &pb);
     if (st != CT_OK) return st;
-    *bytes = choose_path(pb, nullptr) == Path::Umma ? umma_workspace_bytes(pb) : 0;
+    *bytes = workspace_bytes(pb);
     return CT_OK;
 }
 
@@ -213,7 +231,7 @@ ct_status ct_workspace_size_3d(int N, int C_in, int C_out, const int in_dhw[3],
     ct_status st = make_problem(3, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding,
                                 output_padding, dilation, dtype, false, false, &pb);
     if (st != CT_OK) return st;
-    *bytes = choose_path(pb, nullptr) == Path::Umma ? umma_workspace_bytes(pb) : 0;
+    *bytes = workspace_bytes(pb);
     return CT_OK;
 }
 

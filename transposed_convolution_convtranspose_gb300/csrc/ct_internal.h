@@ -69,6 +69,11 @@ cudaError_t launch_gather_generic(const Problem &pb, const Args &a);
 bool tc1d_supported(const Problem &pb, const Args *a);
 cudaError_t launch_tc1d(const Problem &pb, const Args &a);
 
+// ---- FP32 3-D on the tensor cores (3-term tf32 split; workspace) ----
+bool tc3d_supported(const Problem &pb, const Args *a);
+size_t tc3d_workspace_bytes(const Problem &pb);
+cudaError_t launch_tc3d(const Problem &pb, const Args &a);
+
 // ---- phase-decomposed FP32 1-D kernel ----
 bool phase1d_supported(const Problem &pb, const Args *a);
 cudaError_t launch_phase1d(const Problem &pb, const Args &a);

@@ -87,7 +87,12 @@ cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *blocks
         }
     };
     static std::unordered_map<Key, int, Hash> cache;
+    // The shared-memory limit is an attribute of the function on a device, not
+    // of a launch: keep it at the largest size requested so far, so that a
+    // smaller request never lowers it under a larger one that was cached.
+    static std::unordered_map<Key, size_t, Hash> limit;
     const Key key{fn, dev, threads, smem};
+    const Key fkey{fn, dev, 0, 0};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = cache.find(key);
@@ -96,12 +101,16 @@ cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *blocks
             return cudaSuccess;
         }
     }
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto lt = limit.find(fkey);
+    if (lt == limit.end() || lt->second < smem) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        limit[fkey] = smem;
+    }
     int per = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, threads, smem);
     if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(g_mu);
     cache[key] = per;
     *blocks_per_sm = per;
     return cudaSuccess;

@@ -13,34 +13,42 @@
 //
 // Operands (caller's workspace, written by the two prep kernels):
 //   x (N, C_in, D, H, W) -> x_hi, x_lo (N, D, H, W, C_in), channels-last
-//   w (C_in, C_out, kD, kH, kW) -> w_p [tap][hi, lo][C_out][C_in]
+//   w (C_in, C_out, kD, kH, kW) -> weight panels, K-major (C_in fastest)
 // with hi = v rounded to tf32 (cvt.rna) and lo = v - hi (exact in fp32);
 // three MMAs per product accumulate hi*hi + hi*lo + lo*hi in fp32 in TMEM;
 // the dropped lo*lo term and the tf32 truncation of lo are each below 2^-21
 // of a product.
 //
-// GEMM kernel: persistent, one CTA per SM, warp-specialised.  A unit of work
-// is 128 positions (whole W rows of MH H rows of one D plane) and one D
-// residue rD, with all four (rH, rW) phases as four accumulators of C_out
-// TMEM columns; two such sets alternate across units when they fit, so the
-// epilogue of one unit overlaps the MMAs of the next.
-//   warps 0-3  TMA producers, two per ring, taking turns stage by stage (one
-//              thread's TMA stream completes about one box at a time).  For
-//              every distinct input offset (dd, dh, dw) the unit reads, an A
-//              stage (the hi and lo tiles: 5-D boxes of 128 positions x 32
-//              channels at that offset; boxes reaching outside the input read
-//              zeros, which is the boundary handling), then one B stage (one
-//              box: the hi and lo C_out x 32 weight tiles) per phase tap that
-//              reads that offset.  A and B stages have separate rings.
-//   warp 4     TMEM allocation and MMA issue: per B stage, for each 8-wide
-//              K step, three tcgen05.mma (M = 128, N = C_out, K = 8) into the
-//              phase's accumulator.
-//   warps 5-12 epilogue, two per TMEM lane quarter taking alternate
-//              16-channel chunks, one H phase at a time: the add values are
-//              loaded first, then tcgen05.ld of the two W phases, bias, the
-//              fused epilogue, and each position's even and odd W outputs
-//              stored as one float2 (a warp writes two whole output rows per
-//              channel and H phase).
+// Schedule.  A unit of work is 128 positions (whole W rows of MH H rows of
+// one D plane) and one D residue rD, with the four (rH, rW) phases as four
+// accumulators of C_out TMEM columns side by side (two such sets alternate
+// across units when they fit, so the epilogue of one unit overlaps the MMAs
+// of the next).  Every distinct input offset (dd, dh, dw) the unit reads is
+// one A tile; the phases that read it with some tap form runs of adjacent
+// accumulators, and the weights of a run are stored as one panel -- hi rows
+// of its phases, then lo rows -- so that one MMA with N = run length x C_out
+// serves the whole run.  An MMA instruction costs the issuing thread about
+// 100 clocks whatever its N, so wide runs are what keeps the tensor cores
+// busy; the issue loop carries ring slots and parities as counters.
+//
+// Roles (persistent CTA, one per SM):
+//   warp 0      TMA producer of the A ring (hi and lo 5-D boxes of 128
+//               positions x 32 channels at the offset; boxes reaching outside
+//               the input read zeros, which is the boundary handling)
+//   warps 1-2   TMA producers of the B ring, taking turns (a run's panel is
+//               one box); one thread's TMA stream completes about one box at
+//               a time, and every ring slot has exactly one producer, which
+//               refills it only after waiting for its previous round, so a
+//               parity wait never has to tell two phases apart
+//   warp 3      TMEM allocation and MMA issue
+//   warps 4-11  epilogue, in chunks of 16 channels of a unit (16 channels x
+//               the unit's 2 MH output rows x the whole W extent, 32 KB): the
+//               add values arrive in one of three shared-memory buffers by a
+//               TMA load two chunks ahead; warp w reads TMEM lane quarter
+//               w mod 4 for one H phase, adds bias (and applies the fused
+//               epilogue) in place, writing each position's even and odd W
+//               outputs as one float2; one thread stores the chunk with a TMA
+//               store (rows and planes past the output are clipped)
 // Every mbarrier wait is bounded: a timeout records CT_ERR_DEVICE_TIMEOUT in
 // the device status word and the roles unwind (each producer waits, bounded,
 // for its own TMA copies and the MMA issuer for its own MMAs before the TMEM
@@ -57,28 +65,36 @@ namespace {
 
 constexpr int BM = 128;          // positions per unit (UMMA M)
 constexpr int CK = 32;           // fp32 K per stage: one 128-byte swizzle row
-constexpr int MAXE = 18;         // A stages of a unit per K block at most (2 x 3 x 3)
-constexpr int NA = 4;            // A stages
-constexpr int MAXB = 8;          // B stages at most
-constexpr int NPA = 2;           // producer warps of the A ring (stage g loaded by warp g mod NPA)
-constexpr int NPB = 2;           // producer warps of the B ring
+constexpr int NA = 2;            // A stages (one producer warp)
+constexpr int NB = 2;            // B stages
+constexpr int NE = 3;            // epilogue chunk buffers (16 channels of a unit, 32 KB each)
+constexpr int NPB = 2;           // B producer warps: warp q loads the B stages g with g mod NPB == q
+constexpr int MAXE = 18;         // input offsets per D residue (2 x 3 x 3 for extents <= 4)
+constexpr int MAXR = 64;         // runs per D residue
+constexpr int MAXBLK = 128;      // C_out-row blocks of the weight panels (2 x taps)
 constexpr int EPW = 2;           // epilogue warps per TMEM lane quarter
-constexpr int kMmaWarp = NPA + NPB;
+constexpr int kAWarp = 0;
+constexpr int kBWarp0 = 1;
+constexpr int kMmaWarp = kBWarp0 + NPB;
 constexpr int kEpiWarp0 = kMmaWarp + 1;
 constexpr int kThreads = 32 * (kEpiWarp0 + 4 * EPW);
-// Every stage slot has exactly one producer warp (ring sizes are multiples of
-// the producer counts), which refills it only after waiting for the slot's
-// previous round, so a parity wait never has to tell two phases apart.
-static_assert(NA % NPA == 0, "one producer per A slot");
-static_assert(MAXB % NPB == 0, "one producer per B slot");
 constexpr uint32_t kATile = BM * CK * 4;       // one of hi / lo: 16 KB
+constexpr uint32_t kEChunk = 16 * 4 * BM * 4;  // 16 channels x 4 phases x 128 positions, fp32: 32 KB
+constexpr int kEpiThreads = 32 * 4 * EPW;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+static_assert(NB % NPB == 0, "one producer per B slot");
 
-// One input offset read by a unit and the phase taps that read it.
-struct AEntry {
-    int8_t dd, dh, dw, nuse;
-    int8_t tap[4];               // weight tap (kd*K1 + kh)*K2 + kw
-    int8_t ph[4];                // accumulator rH*2 + rW
+// One input offset a unit reads; its runs are run[rd][run0 .. run0 + nrun).
+struct Entry {
+    int8_t dd, dh, dw, nrun;
+    int16_t run0, pad;
+};
+// Adjacent accumulators p0 .. p0 + len - 1 served by one weight panel whose
+// hi rows start at row brow (lo rows follow after len x C_out rows).  fresh:
+// the first MMA of the run writes (rather than adds to) its accumulators.
+struct Run {
+    int8_t p0, len, fresh, pad;
+    int brow;
 };
 
 struct T3Params {
@@ -87,14 +103,21 @@ struct T3Params {
     int QD, QH, QW, MH, n_qhb;
     int n_kb;                    // C_in / 32
     int nunits;
-    int nb;                      // B stages
     int nacc;                    // accumulator sets (1 or 2)
     uint32_t acc_cols;           // 4 x C_out
     uint32_t tmem_cols;
-    uint32_t idesc;
-    uint32_t b_bytes;            // one of hi / lo: C_out x 128
-    int nA[2];                   // entries per D residue
-    AEntry ent[2][MAXE];
+    uint32_t bslot;              // bytes of a B ring slot
+    uint32_t idesc[5];           // instruction descriptor for N = len x C_out, len 1..4
+    int nE[2];
+    Entry ent[2][MAXE];
+    Run run[2][MAXR];
+};
+
+// Weight panel rows: block b (C_out rows) holds tap blk_tap[b], hi or lo.
+struct WPanels {
+    int C_in, C_out, ntap, nblk;
+    int8_t blk_tap[MAXBLK];
+    int8_t blk_lo[MAXBLK];
 };
 
 __device__ __forceinline__ float tf32_hi(float v)
@@ -150,24 +173,21 @@ prep_x_kernel(const float *__restrict__ x, float *__restrict__ xhi, float *__res
     }
 }
 
-// w (C_in, C_out, K0, K1, K2) -> w_p [tap][hi, lo][C_out][C_in], tap = (kd*K1 + kh)*K2 + kw:
-// the hi and lo panels of a tap are adjacent, so one box of 2*C_out rows
-// brings both.
+// w (C_in, C_out, K0, K1, K2) -> weight panels [block][C_out][C_in]: block b
+// holds the hi or lo part of tap blk_tap[b].
 __global__ void __launch_bounds__(256)
-prep_w_kernel(const float *__restrict__ w, float *__restrict__ wp, int C_in, int C_out, int ntap)
+prep_w_kernel(const float *__restrict__ w, float *__restrict__ wp, WPanels q)
 {
-    const int64_t total = (int64_t)ntap * C_out * C_in;
+    const int64_t per = (int64_t)q.C_out * q.C_in;
+    const int64_t total = (int64_t)q.nblk * per;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
-        const int ic = (int)(e % C_in);
-        const int64_t r = e / C_in;
-        const int oc = (int)(r % C_out);
-        const int tap = (int)(r / C_out);
-        const float v = __ldg(w + ((int64_t)ic * C_out + oc) * ntap + tap);
+        const int b = (int)(e / per);
+        const int64_t r = e % per;
+        const int oc = (int)(r / q.C_in), ic = (int)(r % q.C_in);
+        const float v = __ldg(w + ((int64_t)ic * q.C_out + oc) * q.ntap + q.blk_tap[b]);
         const float h = tf32_hi(v);
-        const int64_t o = ((int64_t)tap * 2 * C_out + oc) * C_in + ic;
-        wp[o] = h;
-        wp[o + (int64_t)C_out * C_in] = v - h;
+        wp[e] = q.blk_lo[b] ? v - h : h;
     }
 }
 
@@ -192,27 +212,35 @@ __device__ __forceinline__ UnitCoord unit_coord(int u, const T3Params &p)
 template <bool ADD>
 __global__ void __launch_bounds__(kThreads, 1)
 tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant__ CUtensorMap tmXl,
-                 const __grid_constant__ CUtensorMap tmW, const float *__restrict__ bias, const float *add,
-                 float *y, T3Params p, unsigned int *status)
+                 const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
+                 const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmW4,
+                 const __grid_constant__ CUtensorMap tmAdd, const __grid_constant__ CUtensorMap tmY,
+                 const float *__restrict__ bias, const __grid_constant__ T3Params p, unsigned int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t a_full[NA], a_empty[NA], b_full[MAXB], b_empty[MAXB], acc_full[2],
-        acc_empty[2], drain_bar;
+    __shared__ __align__(8) uint64_t a_full[NA], a_empty[NA], b_full[NB], b_empty[NB], acc_full[2],
+        acc_empty[2], drain_bar, e_full[NE];
     __shared__ uint32_t tmem_slot;
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = sm;                                  // NA x (hi, lo)
-    uint8_t *sB = sm + NA * 2 * kATile;                // nb x (hi, lo)
+    uint8_t *sB = sm + NA * 2 * kATile;                // NB x bslot
+    uint8_t *sE = sB + NB * p.bslot;                   // NE x kEChunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         dev::prefetch_tensormap(&tmXh);
         dev::prefetch_tensormap(&tmXl);
-        dev::prefetch_tensormap(&tmW);
+        dev::prefetch_tensormap(&tmW1);
+        dev::prefetch_tensormap(&tmW2);
+        dev::prefetch_tensormap(&tmW3);
+        dev::prefetch_tensormap(&tmW4);
+        dev::prefetch_tensormap(&tmY);
+        if (ADD) dev::prefetch_tensormap(&tmAdd);
         for (int s = 0; s < NA; ++s) {
             dev::mbar_init(&a_full[s], 1);
             dev::mbar_init(&a_empty[s], 1);
         }
-        for (int s = 0; s < p.nb; ++s) {
+        for (int s = 0; s < NB; ++s) {
             dev::mbar_init(&b_full[s], 1);
             dev::mbar_init(&b_empty[s], 1);
         }
@@ -221,6 +249,7 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
             dev::mbar_init(&acc_empty[a], 32 * 4 * EPW);   // every epilogue thread
         }
         dev::mbar_init(&drain_bar, 1);
+        for (int b = 0; b < NE; ++b) dev::mbar_init(&e_full[b], 1);
         dev::fence_mbar_init();
     }
     if (warp == kMmaWarp) tc::tmem_alloc(&tmem_slot, p.tmem_cols);
@@ -230,48 +259,57 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
     const uint32_t tmem = tmem_slot;
     const int nunit_cta =
         p.nunits > (int)blockIdx.x ? (p.nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const uint32_t b_stage = 2 * p.b_bytes;
+    const int C_out = p.C_out, n_kb = p.n_kb;
 
-    if (warp < NPA + NPB) {
-        // ---------------- TMA producers.  One thread's TMA stream completes about one
-        // box at a time, so the A ring has NPA producer warps and the B ring NPB,
-        // warp q of a ring loading its stages q, q + NP, ... in the ring's order.
+    if (warp == kAWarp || (warp >= kBWarp0 && warp < kBWarp0 + NPB)) {
+        // ---------------- TMA producers
         if (lane == 0) {
-            const bool isA = warp < NPA;
-            const int q = isA ? warp : warp - NPA;
-            const int np = isA ? NPA : NPB;
-            const int nst = isA ? NA : p.nb;
+            const bool isA = warp == kAWarp;
+            const int q = isA ? 0 : warp - kBWarp0;
+            const int np = isA ? 1 : NPB;
+            const int nst = isA ? NA : NB;
             uint64_t *fullb = isA ? a_full : b_full;
             uint64_t *emptyb = isA ? a_empty : b_empty;
-            int g = 0, last = -1;                     // position in the ring's sequence
+            int g = 0, s = 0, last = -1;             // ring position, slot
+            uint32_t round_par = 0;                  // parity of g / nst
             bool failed = false;
             for (int k = 0; k < nunit_cta && !failed; ++k) {
                 const UnitCoord u = unit_coord((int)blockIdx.x + k * (int)gridDim.x, p);
                 const int qh0 = u.qhb * p.MH;
-                const int ne = p.nA[u.rd];
+                const int ne = p.nE[u.rd];
                 for (int e = 0; e < ne && !failed; ++e) {
-                    const AEntry &en = p.ent[u.rd][e];
-                    for (int kb = 0; kb < p.n_kb && !failed; ++kb) {
-                        const int nload = isA ? 1 : en.nuse;
-                        for (int j = 0; j < nload; ++j, ++g) {
-                            if (g % np != q) continue;
-                            const int s = g % nst;
-                            if (g >= nst && !dev::mbar_wait_bounded(&emptyb[s], ((g / nst) - 1) & 1, kWaitLimitNs)) {
-                                failed = true;
-                                break;
+                    const Entry &en = p.ent[u.rd][e];
+                    for (int kb = 0; kb < n_kb && !failed; ++kb) {
+                        const int nload = isA ? 1 : en.nrun;
+                        for (int j = 0; j < nload; ++j) {
+                            if (isA || (g & (NPB - 1)) == q) {
+                                if (g >= nst &&
+                                    !dev::mbar_wait_bounded(&emptyb[s], round_par ^ 1u, kWaitLimitNs)) {
+                                    failed = true;
+                                    break;
+                                }
+                                if (isA) {
+                                    uint8_t *ah = sA + (size_t)s * 2 * kATile;
+                                    dev::mbar_arrive_expect_tx(&fullb[s], 2 * kATile);
+                                    dev::tma_load_5d(ah, &tmXh, &fullb[s], kb * CK, en.dw, qh0 + en.dh,
+                                                     u.qd + en.dd, u.n);
+                                    dev::tma_load_5d(ah + kATile, &tmXl, &fullb[s], kb * CK, en.dw, qh0 + en.dh,
+                                                     u.qd + en.dd, u.n);
+                                } else {
+                                    // the run's panel exactly: a box of 2 x len x C_out rows
+                                    const Run &ru = p.run[u.rd][en.run0 + j];
+                                    const CUtensorMap *tm = ru.len == 1 ? &tmW1 : ru.len == 2 ? &tmW2
+                                                          : ru.len == 3 ? &tmW3 : &tmW4;
+                                    dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * ru.len * C_out) * 128u);
+                                    dev::tma_load_2d(sB + (size_t)s * p.bslot, tm, &fullb[s], kb * CK, ru.brow);
+                                }
+                                last = g;
                             }
-                            if (isA) {
-                                uint8_t *ah = sA + (size_t)s * 2 * kATile;
-                                dev::mbar_arrive_expect_tx(&fullb[s], 2 * kATile);
-                                dev::tma_load_5d(ah, &tmXh, &fullb[s], kb * CK, en.dw, qh0 + en.dh, u.qd + en.dd, u.n);
-                                dev::tma_load_5d(ah + kATile, &tmXl, &fullb[s], kb * CK, en.dw, qh0 + en.dh,
-                                                 u.qd + en.dd, u.n);
-                            } else {
-                                dev::mbar_arrive_expect_tx(&fullb[s], b_stage);
-                                dev::tma_load_2d(sB + (size_t)s * b_stage, &tmW, &fullb[s], kb * CK,
-                                                 en.tap[j] * 2 * p.C_out);
+                            ++g;
+                            if (++s == nst) {
+                                s = 0;
+                                round_par ^= 1u;
                             }
-                            last = g;
                         }
                     }
                 }
@@ -287,9 +325,12 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
         // ---------------- MMA issuer
         if (lane == 0) {
             bool ok = true;
-            int ga = 0, gb = 0;
+            const uint32_t sAb = dev::smem_u32(sA), sBb = dev::smem_u32(sB);
+            const uint32_t bslot = p.bslot;
+            int sa = 0, sb = 0;
+            uint32_t pa = 0, pb = 0;
             for (int k = 0; k < nunit_cta && ok; ++k) {
-                const UnitCoord u = unit_coord((int)blockIdx.x + k * (int)gridDim.x, p);
+                const int rd = unit_coord((int)blockIdx.x + k * (int)gridDim.x, p).rd;
                 const int a = p.nacc == 2 ? (k & 1) : 0;
                 const int use = p.nacc == 2 ? (k >> 1) : k;     // earlier units in accumulator set a
                 if (use > 0 && !dev::mbar_wait_bounded(&acc_empty[a], (use - 1) & 1, kWaitLimitNs)) {
@@ -298,45 +339,48 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
                 }
                 tc::fence_after();
                 const uint32_t d = tmem + (uint32_t)a * p.acc_cols;
-                uint32_t init = 0;                              // accumulators written so far
-                const int ne = p.nA[u.rd];
+                const int ne = p.nE[rd];
                 for (int e = 0; e < ne && ok; ++e) {
-                    const AEntry &en = p.ent[u.rd][e];
-                    for (int kb = 0; kb < p.n_kb && ok; ++kb) {
-                        const int sa = ga % NA;
-                        if (!dev::mbar_wait_bounded(&a_full[sa], (ga / NA) & 1, kWaitLimitNs)) {
+                    const Entry &en = p.ent[rd][e];
+                    for (int kb = 0; kb < n_kb && ok; ++kb) {
+                        if (!dev::mbar_wait_bounded(&a_full[sa], pa, kWaitLimitNs)) {
                             ok = false;
                             break;
                         }
                         tc::fence_after();
-                        const uint32_t ah = dev::smem_u32(sA + (size_t)sa * 2 * kATile);
+                        const uint32_t ah = sAb + (uint32_t)sa * 2u * kATile;
                         const uint64_t dah = tc::desc_sw128(ah), dal = tc::desc_sw128(ah + kATile);
-                        for (int j = 0; j < en.nuse; ++j) {
-                            const int sb = gb % p.nb;
-                            if (!dev::mbar_wait_bounded(&b_full[sb], (gb / p.nb) & 1, kWaitLimitNs)) {
+                        for (int j = 0; j < en.nrun; ++j) {
+                            const Run &ru = p.run[rd][en.run0 + j];
+                            if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
                                 ok = false;
                                 break;
                             }
                             tc::fence_after();
-                            const uint32_t bh = dev::smem_u32(sB + (size_t)sb * b_stage);
-                            const uint64_t dbh = tc::desc_sw128(bh), dbl = tc::desc_sw128(bh + p.b_bytes);
-                            const int ph = en.ph[j];
-                            const uint32_t dd = d + (uint32_t)(ph * p.C_out);
-                            const bool first = !((init >> ph) & 1u);
+                            const uint32_t bh = sBb + (uint32_t)sb * bslot;
+                            const uint64_t dbh = tc::desc_sw128(bh);
+                            const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(ru.len * C_out) * 128u);
+                            const uint32_t id = p.idesc[ru.len];
+                            const uint32_t dd = d + (uint32_t)(ru.p0 * C_out);
+                            const uint32_t acc0 = (ru.fresh && kb == 0) ? 0u : 1u;
 #pragma unroll
                             for (int kk = 0; kk < CK / 8; ++kk) {
                                 // advance 8 tf32 = 32 bytes along K inside the swizzle atom
-                                const uint64_t ko = (uint64_t)(kk * 2);
-                                tc::mma_tf32(dd, dah + ko, dbh + ko, p.idesc, (first && kk == 0) ? 0u : 1u);
-                                tc::mma_tf32(dd, dah + ko, dbl + ko, p.idesc, 1u);
-                                tc::mma_tf32(dd, dal + ko, dbh + ko, p.idesc, 1u);
+                                tc::mma_tf32(dd, dah + 2 * kk, dbh + 2 * kk, id, kk ? 1u : acc0);
+                                tc::mma_tf32(dd, dah + 2 * kk, dbl + 2 * kk, id, 1u);
+                                tc::mma_tf32(dd, dal + 2 * kk, dbh + 2 * kk, id, 1u);
                             }
-                            init |= 1u << ph;
                             tc::commit(&b_empty[sb]);
-                            ++gb;
+                            if (++sb == NB) {
+                                sb = 0;
+                                pb ^= 1u;
+                            }
                         }
                         tc::commit(&a_empty[sa]);
-                        ++ga;
+                        if (++sa == NA) {
+                            sa = 0;
+                            pa ^= 1u;
+                        }
                     }
                 }
                 if (ok) tc::commit(&acc_full[a]);
@@ -347,13 +391,31 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
     } else {
-        // ---------------- epilogue: EPW warps per TMEM lane quarter (32 positions); a
-        // warp reaches the lanes of quarter warp mod 4
+        // ---------------- epilogue.  A unit's output, 16 channels at a time (a chunk:
+        // 16 channels x 2 MH rows x the whole W extent, 32 KB), goes through one of NE
+        // shared-memory buffers: the add values arrive there by TMA two chunks
+        // ahead, the warps combine them in place with the accumulators, and one
+        // TMA store writes the chunk.  Warp w reads TMEM lane quarter w mod 4 and
+        // handles H phase rH = (w - first epilogue warp) / 4.
         const int ew = warp & 3;
-        const int half = (warp - kEpiWarp0) >> 2;
-        const int nchunk = p.C_out / 16;
-        const int64_t sp = (int64_t)p.Lo0 * p.Lo1 * p.Lo2;
+        const int rh = (warp - kEpiWarp0) >> 2;
+        const bool leader = warp == kEpiWarp0 && lane == 0;
+        const int nchunk = C_out / 16;
+        const int total = nunit_cta * nchunk;          // chunks of this CTA
+        const int Lo2 = p.Lo2, rows = 2 * p.MH;
+        const int cstride = rows * Lo2 / 2;            // float2 between channels of a chunk
         bool ok = true;
+        // leader: TMA load of chunk gc's add values into buffer gc mod NE
+        auto load_add = [&](int gc) {
+            const UnitCoord v = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
+            const int b = gc % NE;
+            dev::mbar_arrive_expect_tx(&e_full[b], kEChunk);
+            dev::tma_load_4d(sE + (size_t)b * kEChunk, &tmAdd, &e_full[b], 0, 2 * v.qhb * p.MH, 2 * v.qd + v.rd,
+                             v.n * C_out + (gc % nchunk) * 16);
+        };
+        if (ADD && leader)
+            for (int gc = 0; gc < 2 && gc < total; ++gc) load_add(gc);
+        int gc = 0;
         for (int k = 0; k < nunit_cta; ++k) {
             const UnitCoord u = unit_coord((int)blockIdx.x + k * (int)gridDim.x, p);
             const int a = p.nacc == 2 ? (k & 1) : 0;
@@ -365,54 +427,59 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
             ok = __all_sync(0xffffffffu, ok);        // warp-uniform before .sync.aligned loads
             tc::fence_after();
             const int m = ew * 32 + lane;
-            const int qh = u.qhb * p.MH + m / p.QW, qw = m % p.QW;
-            const int od = 2 * u.qd + u.rd;
+            const int row = 2 * (m / p.QW) + rh, qw = m % p.QW;
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols;
-            bool released = false;
-            for (int ci = half; ci < nchunk; ci += EPW) {
-                const int c0 = ci * 16;
+            for (int c = 0; c < nchunk; ++c, ++gc) {
+                const int b = gc % NE;
+                float2 *q = reinterpret_cast<float2 *>(sE + (size_t)b * kEChunk) + (row * Lo2 + 2 * qw) / 2;
+                if (ADD && ok && !dev::mbar_wait_bounded(&e_full[b], (gc / NE) & 1, kWaitLimitNs)) {
+                    atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
+                    ok = false;
+                }
+                ok = __all_sync(0xffffffffu, ok);
+                float v0[16], v1[16];
+                if (ok) {
+                    tc::tmem_ld16(tbase + (uint32_t)((rh * 2) * C_out + c * 16), v0);
+                    tc::tmem_ld16(tbase + (uint32_t)((rh * 2 + 1) * C_out + c * 16), v1);
+                    tc::tmem_wait_ld();
+                }
+                if (c == nchunk - 1) {                  // the unit's last loads: free the accumulators
+                    tc::fence_before();
+                    dev::mbar_arrive(&acc_empty[a]);
+                }
+                if (ok) {
 #pragma unroll
-                for (int rh = 0; rh < 2; ++rh) {
-                    const int oh = 2 * qh + rh;
-                    const bool valid = od < p.Lo0 && oh < p.Lo1;
-                    const int64_t off =
-                        (int64_t)u.n * p.C_out * sp + ((int64_t)od * p.Lo1 + oh) * p.Lo2 + 2 * qw + (int64_t)c0 * sp;
-                    float2 av[16];
-                    if (ADD) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            av[i] = (ok && valid) ? __ldcs(reinterpret_cast<const float2 *>(add + off + (int64_t)i * sp))
-                                                  : make_float2(0.f, 0.f);
-                    }
-                    float v0[16], v1[16];
-                    if (ok) {
-                        tc::tmem_ld16(tbase + (uint32_t)((rh * 2) * p.C_out + c0), v0);
-                        tc::tmem_ld16(tbase + (uint32_t)((rh * 2 + 1) * p.C_out + c0), v1);
-                        tc::tmem_wait_ld();
-                    }
-                    if (rh == 1 && ci + EPW >= nchunk) {   // the warp's last loads: free the accumulators
-                        tc::fence_before();
-                        dev::mbar_arrive(&acc_empty[a]);
-                        released = true;
-                    }
-                    if (ok && valid) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float bb = bias ? __ldg(bias + c0 + i) : 0.f;
-                            float t0 = v0[i] + bb, t1 = v1[i] + bb;
-                            if (ADD) {
-                                t0 = add_hswish(t0, av[i].x);
-                                t1 = add_hswish(t1, av[i].y);
-                            }
-                            __stcs(reinterpret_cast<float2 *>(y + off + (int64_t)i * sp), make_float2(t0, t1));
+                    for (int i = 0; i < 16; ++i) {
+                        const float bb = bias ? __ldg(bias + c * 16 + i) : 0.f;
+                        float t0 = v0[i] + bb, t1 = v1[i] + bb;
+                        if (ADD) {
+                            const float2 av = q[i * cstride];
+                            t0 = add_hswish(t0, av.x);
+                            t1 = add_hswish(t1, av.y);
                         }
+                        q[i * cstride] = make_float2(t0, t1);
                     }
                 }
+                dev::fence_proxy_async();
+                dev::named_bar_sync(1, kEpiThreads);
+                if (leader) {
+                    if (ok) {
+                        // rows and planes past the output are clipped by the store
+                        dev::tma_store_4d(&tmY, sE + (size_t)b * kEChunk, 0, 2 * u.qhb * p.MH, 2 * u.qd + u.rd,
+                                          u.n * C_out + c * 16);
+                    }
+                    dev::bulk_commit();
+                    dev::bulk_wait_read<1>();           // chunk gc - 1's store has read its buffer
+                    if (ADD && ok && gc + 2 < total) load_add(gc + 2);
+                }
             }
-            if (!released) {                          // a warp without chunks (C_out < 32)
-                tc::fence_before();
-                dev::mbar_arrive(&acc_empty[a]);
-            }
+        }
+        if (leader) {
+            dev::bulk_wait_all();
+            // add loads this warp issued that nobody consumed (only after a timeout)
+            if (ADD)
+                for (int r = total - 2 > 0 ? total - 2 : 0; r < total; ++r)
+                    dev::mbar_wait_bounded(&e_full[r % NE], (r / NE) & 1, kWaitLimitNs);
         }
     }
 
@@ -425,8 +492,9 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
 // ---- host side ------------------------------------------------------------------
 struct T3Plan {
     T3Params p;
+    WPanels wq;
+    int maxlen;                  // longest run
     size_t x_bytes, w_bytes, smem;
-    int ntap;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -452,8 +520,9 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     for (int d = 0; d < 3; ++d)
         if (pb.S[d] != 2 || pb.DL[d] != 1 || pb.K[d] < 2 || pb.K[d] > 4) return false;
     if (pb.C_in % CK != 0 || pb.C_out % 16 != 0 || pb.C_out < 16 || pb.C_out > 128) return false;
-    if (pb.Lo[2] % 2 != 0 || pb.in_sp() % 4 != 0) return false;
-    if (a && (((uintptr_t)a->x % 16) || ((uintptr_t)a->y % 8) || (a->add && ((uintptr_t)a->add % 8))))
+    // the epilogue moves whole output rows by TMA: 16-byte rows and bases
+    if (pb.Lo[2] % 4 != 0 || pb.in_sp() % 4 != 0) return false;
+    if (a && (((uintptr_t)a->x % 16) || ((uintptr_t)a->y % 16) || (a->add && ((uintptr_t)a->add % 16))))
         return false;
     T3Params p;
     memset(&p, 0, sizeof(p));
@@ -489,55 +558,94 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
                     uo[d][nu[d]++] = td[d][r][j];
                 }
             }
+    // runs of adjacent accumulators: at most 4 phases, N = len x C_out <= 256 and
+    // a panel of 2 x len x C_out rows <= 256 (one TMA box)
+    const int maxlen = 128 / pb.C_out < 4 ? 128 / pb.C_out : 4;
+    WPanels wq;
+    memset(&wq, 0, sizeof(wq));
+    int nblk = 0;
     for (int rd = 0; rd < 2; ++rd) {
-        int ne = 0;
+        int ne = 0, nr = 0;
+        uint32_t init = 0;                        // accumulators written by earlier runs
         for (int jd = 0; jd < nt[0][rd]; ++jd)
             for (int ih = 0; ih < nu[1]; ++ih)
                 for (int iw = 0; iw < nu[2]; ++iw) {
-                    AEntry en;
+                    // phases reading offset (dd, dh, dw), with their taps
+                    int tap_of[4] = {-1, -1, -1, -1};
+                    for (int rh = 0; rh < 2; ++rh)
+                        for (int jh = 0; jh < nt[1][rh]; ++jh) {
+                            if (td[1][rh][jh] != uo[1][ih]) continue;
+                            for (int rw = 0; rw < 2; ++rw)
+                                for (int jw = 0; jw < nt[2][rw]; ++jw) {
+                                    if (td[2][rw][jw] != uo[2][iw]) continue;
+                                    tap_of[rh * 2 + rw] =
+                                        (tk[0][rd][jd] * pb.K[1] + tk[1][rh][jh]) * pb.K[2] + tk[2][rw][jw];
+                                }
+                        }
+                    Entry en;
                     memset(&en, 0, sizeof(en));
                     en.dd = (int8_t)td[0][rd][jd];
                     en.dh = (int8_t)uo[1][ih];
                     en.dw = (int8_t)uo[2][iw];
-                    for (int rh = 0; rh < 2; ++rh)
-                        for (int jh = 0; jh < nt[1][rh]; ++jh) {
-                            if (td[1][rh][jh] != en.dh) continue;
-                            for (int rw = 0; rw < 2; ++rw)
-                                for (int jw = 0; jw < nt[2][rw]; ++jw) {
-                                    if (td[2][rw][jw] != en.dw) continue;
-                                    if (en.nuse >= 4) return false;
-                                    const int tap = (tk[0][rd][jd] * pb.K[1] + tk[1][rh][jh]) * pb.K[2] + tk[2][rw][jw];
-                                    en.tap[en.nuse] = (int8_t)tap;
-                                    en.ph[en.nuse] = (int8_t)(rh * 2 + rw);
-                                    ++en.nuse;
-                                }
+                    en.run0 = (int16_t)nr;
+                    int ph = 0;
+                    while (ph < 4) {
+                        if (tap_of[ph] < 0) {
+                            ++ph;
+                            continue;
                         }
-                    if (en.nuse == 0) continue;
+                        // a run: adjacent phases with a tap here, the same written state,
+                        // at most maxlen long
+                        const bool st = (init >> ph) & 1u;
+                        int len = 1;
+                        while (ph + len < 4 && len < maxlen && tap_of[ph + len] >= 0 &&
+                               (((init >> (ph + len)) & 1u) != 0) == st)
+                            ++len;
+                        if (nr >= MAXR || nblk + 2 * len > MAXBLK) return false;
+                        Run ru;
+                        memset(&ru, 0, sizeof(ru));
+                        ru.p0 = (int8_t)ph;
+                        ru.len = (int8_t)len;
+                        ru.fresh = st ? 0 : 1;
+                        ru.brow = nblk * pb.C_out;
+                        for (int hl = 0; hl < 2; ++hl)
+                            for (int i = 0; i < len; ++i) {
+                                wq.blk_tap[nblk] = (int8_t)tap_of[ph + i];
+                                wq.blk_lo[nblk] = (int8_t)hl;
+                                ++nblk;
+                            }
+                        for (int i = 0; i < len; ++i) init |= 1u << (ph + i);
+                        p.run[rd][nr++] = ru;
+                        ++en.nrun;
+                        ph += len;
+                    }
+                    if (en.nrun == 0) continue;
                     if (ne >= MAXE) return false;
                     p.ent[rd][ne++] = en;
                 }
-        p.nA[rd] = ne;
+        if (init != 0xFu) return false;           // every accumulator of the unit is written
+        p.nE[rd] = ne;
     }
+    wq.C_in = pb.C_in;
+    wq.C_out = pb.C_out;
+    wq.ntap = pb.kvol();
+    wq.nblk = nblk;
+    for (int len = 1; len <= 4; ++len)
+        p.idesc[len] = len * pb.C_out <= 256 ? tc::idesc(2, len * pb.C_out, BM) : 0u;
     p.acc_cols = (uint32_t)(4 * pb.C_out);
     p.nacc = 8 * pb.C_out <= 512 ? 2 : 1;
     uint32_t cols = 32;
     while (cols < (uint32_t)p.nacc * p.acc_cols) cols <<= 1;
     p.tmem_cols = cols;
-    p.idesc = tc::idesc(2, pb.C_out, BM);
-    p.b_bytes = (uint32_t)pb.C_out * CK * 4;
-    const size_t budget = 227 * 1024 - 2048;           // alignment slack, static shared memory
-    const size_t a_area = (size_t)NA * 2 * kATile;
-    if (budget < a_area) return false;
-    int nb = (int)((budget - a_area) / (2 * p.b_bytes));
-    if (nb > MAXB) nb = MAXB;
-    nb -= nb % NPB;                                     // one producer per B slot
-    if (nb < NPB || nb < 2) return false;
-    p.nb = nb;
+    p.bslot = (uint32_t)(2 * maxlen * pb.C_out) * 128u;
+    const size_t smem = (size_t)NA * 2 * kATile + (size_t)NB * p.bslot + (size_t)NE * kEChunk + 1024;
+    if (smem > 227 * 1024 - 1024) return false;   // room for the static barriers
     out->p = p;
-    out->ntap = pb.kvol();
+    out->wq = wq;
+    out->maxlen = maxlen;
     out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * 4);
-    out->w_bytes = align256((size_t)out->ntap * 2 * pb.C_out * pb.C_in * 4);   // hi and lo panels
-    out->smem = a_area + (size_t)nb * 2 * p.b_bytes + 1024;
+    out->w_bytes = align256((size_t)nblk * pb.C_out * pb.C_in * 4);
+    out->smem = smem;
     return true;
 }
 
@@ -573,28 +681,49 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     prep_x_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const float *>(a.x), xhi, xlo, pb.C_in, SP);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // 2) weights -> per-tap K-major hi / lo
-    const int64_t wtot = (int64_t)pl.ntap * pb.C_out * pb.C_in;
+    // 2) weights -> run panels, hi / lo
+    const int64_t wtot = (int64_t)pl.wq.nblk * pb.C_out * pb.C_in;
     int wblocks = (int)((wtot + 255) / 256);
     if (wblocks > 4 * sm_count()) wblocks = 4 * sm_count();
-    prep_w_kernel<<<wblocks, 256, 0, a.stream>>>(static_cast<const float *>(a.w), wp, pb.C_in, pb.C_out, pl.ntap);
+    prep_w_kernel<<<wblocks, 256, 0, a.stream>>>(static_cast<const float *>(a.w), wp, pl.wq);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // 3) tensor maps: A over x_hi / x_lo (C, W, H, D, N), B over w_p (C_in, ntap*2*C_out)
-    CUtensorMap tmXh, tmXl, tmW;
+    // 3) tensor maps: A over x_hi / x_lo (C, W, H, D, N); B over the panels
+    // (C_in, rows), one map per run length len (a box of 2 x len x C_out rows:
+    // the run's hi and lo panels)
+    CUtensorMap tmXh, tmXl, tmW[4];
     const uint64_t adims[5] = {(uint64_t)pb.C_in, (uint64_t)pb.Li[2], (uint64_t)pb.Li[1], (uint64_t)pb.Li[0],
                                (uint64_t)pb.N};
     const uint64_t astr[4] = {(uint64_t)pb.C_in * 4, (uint64_t)pb.C_in * pb.Li[2] * 4,
                               (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * 4,
                               (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * pb.Li[0] * 4};
     const uint32_t abox[5] = {(uint32_t)CK, (uint32_t)p.QW, (uint32_t)p.MH, 1u, 1u};
-    const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)pl.ntap * 2 * pb.C_out};
+    const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)pl.wq.nblk * pb.C_out};
     const uint64_t bstr[1] = {(uint64_t)pb.C_in * 4};
-    const uint32_t bbox[2] = {(uint32_t)CK, (uint32_t)(2 * pb.C_out)};
     if (!encode_tiled(&tmXh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xhi, adims, astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&tmXl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xlo, adims, astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, wp, bdims, bstr, bbox, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_tiled(&tmXl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xlo, adims, astr, abox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    for (int len = 1; len <= 4; ++len) {
+        // lengths beyond the longest run keep a valid map of the longest box
+        const int l = len <= pl.maxlen ? len : pl.maxlen;
+        const uint32_t bbox[2] = {(uint32_t)CK, (uint32_t)(2 * l * pb.C_out)};
+        if (!encode_tiled(&tmW[len - 1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, wp, bdims, bstr, bbox,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+
+    // add and y viewed as (W, H, D, N*C_out); a box is one chunk: the whole W
+    // extent, the unit's 2 MH rows, one D plane, 16 channels
+    CUtensorMap tmAdd, tmY;
+    const uint64_t ydims[4] = {(uint64_t)pb.Lo[2], (uint64_t)pb.Lo[1], (uint64_t)pb.Lo[0],
+                               (uint64_t)pb.N * pb.C_out};
+    const uint64_t ystr[3] = {(uint64_t)pb.Lo[2] * 4, (uint64_t)pb.Lo[2] * pb.Lo[1] * 4,
+                              (uint64_t)pb.out_sp() * 4};
+    const uint32_t ybox[4] = {(uint32_t)pb.Lo[2], (uint32_t)(2 * p.MH), 1u, 16u};
+    if (!encode_tiled(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, ydims, ystr, ybox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tiled(&tmAdd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.add ? a.add : a.y, ydims, ystr, ybox,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
     const void *fn = a.add ? (const void *)&tc3d_tf32_kernel<true> : (const void *)&tc3d_tf32_kernel<false>;
@@ -607,11 +736,11 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     int grid = sm_count();
     if (grid > p.nunits) grid = p.nunits;
     if (a.add)
-        tc3d_tf32_kernel<true><<<grid, kThreads, pl.smem, a.stream>>>(tmXh, tmXl, tmW, a.bias, a.add, a.y, p,
-                                                                      status);
+        tc3d_tf32_kernel<true><<<grid, kThreads, pl.smem, a.stream>>>(tmXh, tmXl, tmW[0], tmW[1], tmW[2], tmW[3],
+                                                                      tmAdd, tmY, a.bias, p, status);
     else
-        tc3d_tf32_kernel<false><<<grid, kThreads, pl.smem, a.stream>>>(tmXh, tmXl, tmW, a.bias, nullptr, a.y, p,
-                                                                       status);
+        tc3d_tf32_kernel<false><<<grid, kThreads, pl.smem, a.stream>>>(tmXh, tmXl, tmW[0], tmW[1], tmW[2], tmW[3],
+                                                                       tmAdd, tmY, a.bias, p, status);
     return cudaGetLastError();
 }
 

@@ -35,20 +35,22 @@
 //   warp 0      TMA producer of the A ring (hi and lo 5-D boxes of 128
 //               positions x 32 channels at the offset; boxes reaching outside
 //               the input read zeros, which is the boundary handling)
-//   warps 1-2   TMA producers of the B ring, taking turns (a run's panel is
-//               one box); one thread's TMA stream completes about one box at
-//               a time, and every ring slot has exactly one producer, which
-//               refills it only after waiting for its previous round, so a
-//               parity wait never has to tell two phases apart
-//   warp 3      TMEM allocation and MMA issue
-//   warps 4-11  epilogue, in chunks of 16 channels of a unit (16 channels x
+//   warp 1      TMA producer of the B ring (a run's panel is one box).  Each
+//               ring slot has exactly one producer, which refills it only after
+//               waiting for its previous round, so a parity wait never has to
+//               tell two phases apart
+//   warp 2      TMEM allocation and MMA issue
+//   warps 3-18  epilogue, in chunks of 16 channels of a unit (16 channels x
 //               the unit's 2 MH output rows x the whole W extent, 32 KB): the
 //               add values arrive in one of three shared-memory buffers by a
 //               TMA load two chunks ahead; warp w reads TMEM lane quarter
-//               w mod 4 for one H phase, adds bias (and applies the fused
-//               epilogue) in place, writing each position's even and odd W
-//               outputs as one float2; one thread stores the chunk with a TMA
-//               store (rows and planes past the output are clipped)
+//               w mod 4 for one H phase and 8 channels, adds bias (and
+//               applies the fused epilogue) in place, writing each position's
+//               even and odd W outputs as one float2
+//   warp 19     chunk mover: makes chunks ready two ahead (the TMA load of the
+//               add values, or the release of the buffer) and stores each
+//               written chunk with one TMA store (rows and planes past the
+//               output are clipped)
 // Every mbarrier wait is bounded: a timeout records CT_ERR_DEVICE_TIMEOUT in
 // the device status word and the roles unwind (each producer waits, bounded,
 // for its own TMA copies and the MMA issuer for its own MMAs before the TMEM
@@ -68,16 +70,17 @@ constexpr int CK = 32;           // fp32 K per stage: one 128-byte swizzle row
 constexpr int NA = 2;            // A stages (one producer warp)
 constexpr int NB = 2;            // B stages
 constexpr int NE = 3;            // epilogue chunk buffers (16 channels of a unit, 32 KB each)
-constexpr int NPB = 2;           // B producer warps: warp q loads the B stages g with g mod NPB == q
+constexpr int NPB = 1;           // B producer warps: warp q loads the B stages g with g mod NPB == q
 constexpr int MAXE = 18;         // input offsets per D residue (2 x 3 x 3 for extents <= 4)
 constexpr int MAXR = 64;         // runs per D residue
 constexpr int MAXBLK = 128;      // C_out-row blocks of the weight panels (2 x taps)
-constexpr int EPW = 2;           // epilogue warps per TMEM lane quarter
+constexpr int EPW = 4;           // epilogue warps per TMEM lane quarter (H phase x channel half)
 constexpr int kAWarp = 0;
 constexpr int kBWarp0 = 1;
 constexpr int kMmaWarp = kBWarp0 + NPB;
 constexpr int kEpiWarp0 = kMmaWarp + 1;
-constexpr int kThreads = 32 * (kEpiWarp0 + 4 * EPW);
+constexpr int kStoreWarp = kEpiWarp0 + 4 * EPW;
+constexpr int kThreads = 32 * (kStoreWarp + 1);
 constexpr uint32_t kATile = BM * CK * 4;       // one of hi / lo: 16 KB
 constexpr uint32_t kEChunk = 16 * 4 * BM * 4;  // 16 channels x 4 phases x 128 positions, fp32: 32 KB
 constexpr int kEpiThreads = 32 * 4 * EPW;
@@ -219,8 +222,9 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t a_full[NA], a_empty[NA], b_full[NB], b_empty[NB], acc_full[2],
-        acc_empty[2], drain_bar, e_full[NE];
+        acc_empty[2], drain_bar, e_full[NE], c_full[NE];
     __shared__ uint32_t tmem_slot;
+    __shared__ float s_bias[128];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = sm;                                  // NA x (hi, lo)
     uint8_t *sB = sm + NA * 2 * kATile;                // NB x bslot
@@ -249,10 +253,14 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
             dev::mbar_init(&acc_empty[a], 32 * 4 * EPW);   // every epilogue thread
         }
         dev::mbar_init(&drain_bar, 1);
-        for (int b = 0; b < NE; ++b) dev::mbar_init(&e_full[b], 1);
+        for (int b = 0; b < NE; ++b) {
+            dev::mbar_init(&e_full[b], 1);               // buffer ready for its chunk
+            dev::mbar_init(&c_full[b], kEpiThreads);     // chunk written by every epilogue thread
+        }
         dev::fence_mbar_init();
     }
     if (warp == kMmaWarp) tc::tmem_alloc(&tmem_slot, p.tmem_cols);
+    for (int i = threadIdx.x; i < p.C_out; i += blockDim.x) s_bias[i] = bias ? bias[i] : 0.f;
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -390,34 +398,64 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
             if (!dev::mbar_wait_bounded(&drain_bar, 0, kWaitLimitNs)) ok = false;
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
-    } else {
-        // ---------------- epilogue.  A unit's output, 16 channels at a time (a chunk:
-        // 16 channels x 2 MH rows x the whole W extent, 32 KB), goes through one of NE
-        // shared-memory buffers: the add values arrive there by TMA two chunks
-        // ahead, the warps combine them in place with the accumulators, and one
-        // TMA store writes the chunk.  Warp w reads TMEM lane quarter w mod 4 and
-        // handles H phase rH = (w - first epilogue warp) / 4.
-        const int ew = warp & 3;
-        const int rh = (warp - kEpiWarp0) >> 2;
-        const bool leader = warp == kEpiWarp0 && lane == 0;
+    } else if (warp == kStoreWarp) {
+        // ---------------- chunk mover.  Buffer gc mod NE holds chunk gc (16 channels of a
+        // unit: 16 x 2 MH rows x the whole W extent, 32 KB).  Chunk gc is made ready
+        // two chunks ahead -- its add values loaded by TMA, or (no add) the buffer
+        // released -- and stored by TMA once the epilogue warps have written it.
         const int nchunk = C_out / 16;
-        const int total = nunit_cta * nchunk;          // chunks of this CTA
-        const int Lo2 = p.Lo2, rows = 2 * p.MH;
-        const int cstride = rows * Lo2 / 2;            // float2 between channels of a chunk
+        const int total = nunit_cta * nchunk;
         bool ok = true;
-        // leader: TMA load of chunk gc's add values into buffer gc mod NE
-        auto load_add = [&](int gc) {
-            const UnitCoord v = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
+        auto ready = [&](int gc) {
             const int b = gc % NE;
-            dev::mbar_arrive_expect_tx(&e_full[b], kEChunk);
-            dev::tma_load_4d(sE + (size_t)b * kEChunk, &tmAdd, &e_full[b], 0, 2 * v.qhb * p.MH, 2 * v.qd + v.rd,
-                             v.n * C_out + (gc % nchunk) * 16);
+            if (ADD) {
+                const UnitCoord v = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
+                dev::mbar_arrive_expect_tx(&e_full[b], kEChunk);
+                dev::tma_load_4d(sE + (size_t)b * kEChunk, &tmAdd, &e_full[b], 0, 2 * v.qhb * p.MH, 2 * v.qd + v.rd,
+                                 v.n * C_out + (gc % nchunk) * 16);
+            } else {
+                dev::mbar_arrive(&e_full[b]);
+            }
         };
-        if (ADD && leader)
-            for (int gc = 0; gc < 2 && gc < total; ++gc) load_add(gc);
+        if (lane == 0) {
+            for (int gc = 0; gc < 2 && gc < total; ++gc) ready(gc);
+            for (int gc = 0; gc < total && ok; ++gc) {
+                // the epilogue threads wrote chunk gc (they run at most two chunks ahead,
+                // so the parity of a buffer's barrier is unambiguous)
+                if (!dev::mbar_wait_bounded(&c_full[gc % NE], (gc / NE) & 1, kWaitLimitNs)) {
+                    atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                const UnitCoord u = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
+                // rows and planes past the output are clipped by the store
+                dev::tma_store_4d(&tmY, sE + (size_t)(gc % NE) * kEChunk, 0, 2 * u.qhb * p.MH, 2 * u.qd + u.rd,
+                                  u.n * C_out + (gc % nchunk) * 16);
+                dev::bulk_commit();
+                dev::bulk_wait_read<1>();               // chunk gc - 1's store has read its buffer
+                if (gc + 2 < total) ready(gc + 2);      // into that buffer
+            }
+            dev::bulk_wait_all();
+            // loads this thread issued that nobody consumed (only after a timeout)
+            if (ADD)
+                for (int r = total - 2 > 0 ? total - 2 : 0; r < total; ++r)
+                    dev::mbar_wait_bounded(&e_full[r % NE], (r / NE) & 1, kWaitLimitNs);
+        }
+    } else {
+        // ---------------- epilogue: warp w reads TMEM lane quarter w mod 4; the four
+        // warps of a quarter take (H phase, channel half) = ((e >> 2) & 1, e >> 3),
+        // e = w - first epilogue warp.  Per chunk a warp waits for the buffer, adds
+        // bias (and applies the fused epilogue) in place for its 8 channels, and
+        // signals the chunk mover.
+        const int ew = warp & 3;
+        const int ei = warp - kEpiWarp0;
+        const int rh = (ei >> 2) & 1, ch = ei >> 3;
+        const int nchunk = C_out / 16;
+        const int Lo2 = p.Lo2;
+        const int cstride = 2 * p.MH * Lo2 / 2;         // float2 between channels of a chunk
+        bool ok = true;
         int gc = 0;
         for (int k = 0; k < nunit_cta; ++k) {
-            const UnitCoord u = unit_coord((int)blockIdx.x + k * (int)gridDim.x, p);
             const int a = p.nacc == 2 ? (k & 1) : 0;
             const int use = p.nacc == 2 ? (k >> 1) : k;
             if (ok && !dev::mbar_wait_bounded(&acc_full[a], use & 1, kWaitLimitNs)) {
@@ -431,55 +469,45 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols;
             for (int c = 0; c < nchunk; ++c, ++gc) {
                 const int b = gc % NE;
-                float2 *q = reinterpret_cast<float2 *>(sE + (size_t)b * kEChunk) + (row * Lo2 + 2 * qw) / 2;
-                if (ADD && ok && !dev::mbar_wait_bounded(&e_full[b], (gc / NE) & 1, kWaitLimitNs)) {
+                const int c0 = c * 16 + ch * 8;             // this warp's first channel
+                float2 *q = reinterpret_cast<float2 *>(sE + (size_t)b * kEChunk) + (row * Lo2 + 2 * qw) / 2 +
+                            ch * 8 * cstride;
+                float v0[8], v1[8];
+                if (ok) {
+                    tc::tmem_ld8(tbase + (uint32_t)((rh * 2) * C_out + c0), v0);
+                    tc::tmem_ld8(tbase + (uint32_t)((rh * 2 + 1) * C_out + c0), v1);
+                }
+                if (ok && !dev::mbar_wait_bounded(&e_full[b], (gc / NE) & 1, kWaitLimitNs)) {
                     atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
                     ok = false;
                 }
                 ok = __all_sync(0xffffffffu, ok);
-                float v0[16], v1[16];
-                if (ok) {
-                    tc::tmem_ld16(tbase + (uint32_t)((rh * 2) * C_out + c * 16), v0);
-                    tc::tmem_ld16(tbase + (uint32_t)((rh * 2 + 1) * C_out + c * 16), v1);
-                    tc::tmem_wait_ld();
-                }
+                tc::tmem_wait_ld();
                 if (c == nchunk - 1) {                  // the unit's last loads: free the accumulators
                     tc::fence_before();
                     dev::mbar_arrive(&acc_empty[a]);
                 }
                 if (ok) {
+                    // all loads first, then the arithmetic and the stores
+                    float2 av[8];
+                    if (ADD) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float bb = bias ? __ldg(bias + c * 16 + i) : 0.f;
+                        for (int i = 0; i < 8; ++i) av[i] = q[i * cstride];
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float bb = s_bias[c0 + i];
                         float t0 = v0[i] + bb, t1 = v1[i] + bb;
                         if (ADD) {
-                            const float2 av = q[i * cstride];
-                            t0 = add_hswish(t0, av.x);
-                            t1 = add_hswish(t1, av.y);
+                            t0 = add_hswish(t0, av[i].x);
+                            t1 = add_hswish(t1, av[i].y);
                         }
                         q[i * cstride] = make_float2(t0, t1);
                     }
                 }
                 dev::fence_proxy_async();
-                dev::named_bar_sync(1, kEpiThreads);
-                if (leader) {
-                    if (ok) {
-                        // rows and planes past the output are clipped by the store
-                        dev::tma_store_4d(&tmY, sE + (size_t)b * kEChunk, 0, 2 * u.qhb * p.MH, 2 * u.qd + u.rd,
-                                          u.n * C_out + c * 16);
-                    }
-                    dev::bulk_commit();
-                    dev::bulk_wait_read<1>();           // chunk gc - 1's store has read its buffer
-                    if (ADD && ok && gc + 2 < total) load_add(gc + 2);
-                }
+                dev::mbar_arrive(&c_full[b]);
             }
-        }
-        if (leader) {
-            dev::bulk_wait_all();
-            // add loads this warp issued that nobody consumed (only after a timeout)
-            if (ADD)
-                for (int r = total - 2 > 0 ? total - 2 : 0; r < total; ++r)
-                    dev::mbar_wait_bounded(&e_full[r % NE], (r / NE) & 1, kWaitLimitNs);
         }
     }
 

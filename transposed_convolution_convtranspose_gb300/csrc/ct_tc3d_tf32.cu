@@ -195,15 +195,20 @@ prep_w_kernel(const float *__restrict__ w, float *__restrict__ wp, WPanels q)
 }
 
 // ---- GEMM kernel ----------------------------------------------------------------
-// unit -> (n, qd, qh block, rD); the two D residues of one position block are
-// neighbours, so the A tiles they share are reused from L2
+// unit -> (n, qd, qh block, rD).  The two D residues of one position block are
+// neighbours (their shared A tiles are reused from L2).  Units are dealt to the
+// CTAs round-robin; rD = 1 has more taps than rD = 0 when the kernel extent is
+// odd, and with an even grid a CTA would see one residue only, so the residue
+// bit is flipped on every other round (each round's block of grid-size units is
+// closed under flipping its low bit, so this permutes the units) and every CTA
+// gets both residues in turn.
 struct UnitCoord {
     int n, qd, qhb, rd;
 };
 __device__ __forceinline__ UnitCoord unit_coord(int u, const T3Params &p)
 {
     UnitCoord c;
-    c.rd = u & 1;
+    c.rd = (u ^ (u / (int)gridDim.x)) & 1;
     u >>= 1;
     c.qhb = u % p.n_qhb;
     u /= p.n_qhb;
@@ -763,6 +768,7 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.nunits) grid = p.nunits;
+    if (grid > 1 && (grid & 1)) --grid;   // an even grid: the residue flip of unit_coord permutes units
     if (a.add)
         tc3d_tf32_kernel<true><<<grid, kThreads, pl.smem, a.stream>>>(tmXh, tmXl, tmW[0], tmW[1], tmW[2], tmW[3],
                                                                       tmAdd, tmY, a.bias, p, status);

@@ -26,10 +26,13 @@
 //              boundary handling -- plus the B tiles (C_out x 64 of w_p) of
 //              every W phase whose tap reads that same input offset, so an
 //              input W offset both W phases read is fetched once for both.
-//   warp 4     TMEM allocation and MMA issue: tcgen05.mma kind::f16 (M = 128,
-//              K = 16); one N = 2 x C_out MMA where both W phases share the
-//              A tile, else N = C_out into the phase's half of the accumulator.
-//   warps 5-12 epilogue, two per TMEM lane quarter taking alternate
+//   warps 4-5  TMEM allocation and MMA issue, one warp per accumulator taking
+//              alternate tiles (one thread issues an MMA only every ~100+
+//              clocks; two warps nearly double the rate): tcgen05.mma
+//              kind::f16 (M = 128, K = 16); one N = 2 x C_out MMA where both
+//              W phases share the A tile, else N = C_out into the phase's half
+//              of the accumulator.
+//   warps 6-13 epilogue, two per TMEM lane quarter taking alternate
 //              16-channel chunks: tcgen05.ld, bias, and each position's even
 //              and odd W outputs written as one float2 (a warp writes two
 //              whole 128-byte output rows per channel).
@@ -54,9 +57,10 @@ constexpr int MAXST = 8;     // pipeline stages at most
 constexpr int MAXWE = 5;     // distinct input W offsets of a tile at most (taps per dimension + 1)
 constexpr int NPROD = 4;     // TMA producer warps at most (stage g is loaded by warp g mod nprod)
 constexpr int EPW = 2;       // epilogue warps per TMEM lane quarter
-constexpr int kMmaWarp = NPROD;
-constexpr int kEpiWarp0 = NPROD + 1;
-constexpr int kThreads = 32 * (NPROD + 1 + 4 * EPW);
+constexpr int NMMA = 2;      // MMA-issuing warps at most (one per TMEM accumulator)
+constexpr int kMmaWarp0 = NPROD;
+constexpr int kEpiWarp0 = NPROD + NMMA;
+constexpr int kThreads = 32 * (NPROD + NMMA + 4 * EPW);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct UParams {
@@ -66,7 +70,7 @@ struct UParams {
     int nT;                  // taps per dimension and class (kernel extent / 2)
     int n_kb;                // C_in / BK
     int ntiles;
-    int nst;                 // pipeline stages (a multiple of nprod)
+    int nst;                 // pipeline stages (a multiple of nprod and of nacc)
     int nprod;               // producer warps in use: stage slot s is loaded only by warp s mod nprod
     int nacc;                // TMEM accumulators (1 or 2)
     uint32_t acc_cols;       // columns of one accumulator (2 x C_out)
@@ -106,7 +110,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                  const float *__restrict__ bias, float *__restrict__ y, UParams p, unsigned int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[MAXST], empty_bar[MAXST], acc_full[2], acc_empty[2], drain_bar;
+    __shared__ __align__(8) uint64_t full_bar[MAXST], empty_bar[MAXST], acc_full[2], acc_empty[2], drain_bar[NMMA];
     __shared__ uint32_t tmem_slot;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -122,10 +126,10 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             dev::mbar_init(&acc_full[a], 1);
             dev::mbar_init(&acc_empty[a], 32 * 4 * EPW);   // every epilogue thread
         }
-        dev::mbar_init(&drain_bar, 1);
+        for (int j = 0; j < NMMA; ++j) dev::mbar_init(&drain_bar[j], 1);
         dev::fence_mbar_init();
     }
-    if (warp == kMmaWarp) tc::tmem_alloc(&tmem_slot, p.tmem_cols);
+    if (warp == kMmaWarp0) tc::tmem_alloc(&tmem_slot, p.tmem_cols);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -133,6 +137,11 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int ntile_cta =
         p.ntiles > (int)blockIdx.x ? (p.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int stages_per_tile = p.nT * p.nT * p.n_kb * p.nwe;
+    // With two accumulators, two warps issue MMAs, each for alternate tiles (one
+    // thread issues an MMA only every ~100+ clocks, two nearly double the rate).
+    // The ring then carries the two tiles of a pair interleaved stage by stage:
+    // stage i of tile k sits at g = (k / ni) * ni * spt + i * ni + k mod ni.
+    const int ni = p.nacc;
 
     if (warp < NPROD) {
         // ---------------- TMA producers: a TMA stream of one thread completes about
@@ -141,13 +150,15 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // so every stage slot has one producer, which reuses it only after waiting
         // for the slot's previous round: a parity wait never skips a phase.
         if (lane == 0 && warp < p.nprod) {
-            const int total = ntile_cta * stages_per_tile;
+            const int total = (ntile_cta + ni - 1) / ni * ni * stages_per_tile;
             int g = warp, last = -1;
             bool failed = false;
             int kc = -1, qh0 = 0, ph0 = 0;
             TileCoord tcd;
             for (; g < total; g += p.nprod) {
-                const int k = g / stages_per_tile, i = g % stages_per_tile;
+                const int pr = g / (ni * stages_per_tile), rr = g % (ni * stages_per_tile);
+                const int i = rr / ni, k = pr * ni + rr % ni;
+                if (k >= ntile_cta) continue;          // the missing partner of a last, lone tile
                 if (k != kc) {
                     kc = k;
                     tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
@@ -182,11 +193,12 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 for (int q = last; q >= 0 && q > last - p.nst; q -= p.nprod)
                     dev::mbar_wait_bounded(&full_bar[q % p.nst], (q / p.nst) & 1, kWaitLimitNs);
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer.  An MMA costs the issuing thread about 100
+    } else if (warp < kMmaWarp0 + NMMA) {
+        // ---------------- MMA issuers.  An MMA costs the issuing thread about 100
         // clocks at best, so the loop carries its ring slot, parity and W-offset
         // index as counters (no division) and keeps the per-offset flags in registers.
-        if (lane == 0) {
+        const int j = warp - kMmaWarp0;
+        if (lane == 0 && j < ni) {
             bool ok = true;
             uint32_t m0 = 0, m1 = 0;                    // W offsets read by phase 0 / phase 1
             for (int e = 0; e < p.nwe; ++e) {
@@ -197,11 +209,11 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const uint32_t idesc1 = p.idesc1, idesc2 = p.idesc2, stage_bytes = p.stage_bytes;
             const uint32_t a_bytes = p.a_bytes, b_bytes = p.b_bytes, c_out = (uint32_t)p.C_out;
             const int nst = p.nst, nwe = p.nwe;
-            int s = 0;
+            int s = j;                                  // ring position g = j, j + ni, ...
             uint32_t par = 0;
-            for (int k = 0; k < ntile_cta && ok; ++k) {
-                const int a = p.nacc == 2 ? (k & 1) : 0;
-                const int use = p.nacc == 2 ? (k >> 1) : k;    // earlier tiles in accumulator a
+            for (int k = j; k < ntile_cta && ok; k += ni) {
+                const int a = j;
+                const int use = k / ni;                        // earlier tiles in accumulator a
                 if (use > 0 && !dev::mbar_wait_bounded(&acc_empty[a], (use - 1) & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -240,8 +252,9 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     init0 = init0 || h0;
                     init1 = init1 || h1;
                     tc::commit(&empty_bar[s]);
-                    if (++s == nst) {
-                        s = 0;
+                    s += ni;                                   // nst is a multiple of ni
+                    if (s >= nst) {
+                        s -= nst;
                         par ^= 1u;
                     }
                     if (++e == nwe) e = 0;
@@ -249,8 +262,8 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (ok) tc::commit(&acc_full[a]);
             }
             // every MMA issued has to complete before the TMEM is freed
-            tc::commit(&drain_bar);
-            if (!dev::mbar_wait_bounded(&drain_bar, 0, kWaitLimitNs)) ok = false;
+            tc::commit(&drain_bar[j]);
+            if (!dev::mbar_wait_bounded(&drain_bar[j], 0, kWaitLimitNs)) ok = false;
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
     } else {
@@ -322,7 +335,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __syncwarp();
     tc::fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) tc::tmem_dealloc(tmem, p.tmem_cols);
+    if (warp == kMmaWarp0) tc::tmem_dealloc(tmem, p.tmem_cols);
 }
 
 // ---- repack kernels ------------------------------------------------------------
@@ -535,7 +548,12 @@ bool make_uplan(const Problem &pb, UPlan *out)
     if (p.nst > MAXST) p.nst = MAXST;
     if (p.nst < 2) return false;
     p.nprod = p.nst < NPROD ? p.nst : NPROD;
-    p.nst -= p.nst % p.nprod;               // one producer per stage slot
+    {
+        // one producer per stage slot, and the issuers' interleaved stages on fixed slots
+        const int l = (p.nacc == 2 && p.nprod % 2) ? 2 * p.nprod : p.nprod;
+        p.nst -= p.nst % l;
+        if (p.nst < l) return false;
+    }
     out->p = p;
     out->wq = wq;
     out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * 2);

@@ -352,12 +352,20 @@ def dtype_of(cfg):
 
 def traffic_for(name, path):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary (profiles/traffic.json), or None when no capture matches."""
+    capture (profiles/traffic.json), or None when no capture matches or the
+    kernel's source file has changed since the capture."""
+    import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         e = d.get("%s/%s" % (name, path))
-        return None if e is None else e.get("bytes_per_launch")
+        if e is None:
+            return None
+        src = os.path.join(ROOT, "transposed_convolution_convtranspose_gb300", "csrc", e["kernel_source"])
+        with open(src, "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != e["source_sha1"]:
+                return None
+        return e.get("bytes_per_launch")
     except Exception:
         return None
 

@@ -7,39 +7,54 @@
 // dimension and an even kernel extent, every output residue class
 // (rD, rH, rW) receives the same number of taps per dimension, and
 //     y[n, oc, 2q + r] = bias[oc] + sum_{taps t, ic} x[n, ic, q + delta_t] * w[ic, oc, k_t]
-// is a GEMM per phase: M = positions q (N*QD*QH*QW), N = C_out,
-// K = taps x C_in.  Two repack kernels prepare the operands in the caller's
-// workspace:
-//   x  (N, C, D, H, W)  ->  x_cl (N, D, H, W, C)           channels-last, bf16
-//   w  (C, C_out, kD, kH, kW) -> w_p [phase][oc][tap][ic]   K-major, bf16
+// is a GEMM per phase: M = positions q, N = C_out, K = taps x C_in.  Two
+// repack kernels prepare the operands in the caller's workspace:
+//   x (N, C, D, H, W)          ->  x_t (N, D, W, H, C)   bf16, channels fastest, then H
+//   w (C, C_out, kD, kH, kW)   ->  weight panels, K-major (C_in fastest)
 //
-// GEMM kernel: persistent, one CTA per SM, warp-specialised.  A tile is 128
-// output positions (whole W rows of one D plane) of one (rD, rH) phase pair,
-// with both W phases side by side along N (2 x C_out TMEM columns; two such
-// accumulators alternate across tiles when they fit, so the epilogue of one
-// tile overlaps the MMAs of the next).
-//   warps 0-3  TMA producers, taking turns stage by stage (one thread's TMA
-//              stream completes about one box at a time, so one producer
-//              cannot keep the tensor cores fed).  A stage holds one A tile -- 128 positions x 64
-//              input channels, a 5-D box of x_cl at the tap's input offset;
-//              boxes reaching outside the input read zeros, which is the
-//              boundary handling -- plus the B tiles (C_out x 64 of w_p) of
-//              every W phase whose tap reads that same input offset, so an
-//              input W offset both W phases read is fetched once for both.
-//   warps 4-5  TMEM allocation and MMA issue, one warp per accumulator taking
-//              alternate tiles (one thread issues an MMA only every ~100+
-//              clocks; two warps nearly double the rate): tcgen05.mma
-//              kind::f16 (M = 128, K = 16); one N = 2 x C_out MMA where both
-//              W phases share the A tile, else N = C_out into the phase's half
-//              of the accumulator.
-//   warps 6-13 epilogue, two per TMEM lane quarter taking alternate
-//              16-channel chunks: tcgen05.ld, bias, and each position's even
-//              and odd W outputs written as one float2 (a warp writes two
-//              whole 128-byte output rows per channel).
-// Every mbarrier wait is bounded: a timeout records CT_ERR_DEVICE_TIMEOUT in
-// the device status word and the roles unwind (the producer waits, bounded,
-// for its own TMA copies and the MMA issuer for its own MMAs before the TMEM
-// is freed).
+// Tile: 128 output positions q = 16 consecutive qw x 8 consecutive qh of
+// one D plane, for one (rD, rH) phase pair with both W phases side by side
+// along N (2 x C_out TMEM columns).  TMEM row m holds position
+// (qw, qh) = (m / 8, m mod 8), so each 8-row swizzle group of the A operand
+// is one qw column of 8 consecutive qh -- contiguous in x_t.  When two
+// accumulators fit, a unit of work is a pair of tiles (two neighbouring
+// 8-row qh blocks): they share every input window and weight panel, and
+// each of two MMA-issuing warps computes one of them.
+//
+// Operand A without shifted copies: per (D tap, K block) one TMA box brings
+// the unit's input window, (8 x tiles + H halo) x (16 + W halo) positions x
+// 64 channels, 128-byte swizzled, rows ordered (w, h).  The A operand of
+// input offset (dh, dw) for tile j is that window read from start row
+// (dw - dw_lo) * hspan + (dh - dh_lo) + 8 j with a stride of hspan rows
+// between groups: only the shared-memory descriptor's start address and
+// stride-byte-offset change (the 128-byte swizzle is a function of the
+// absolute shared-memory address, so rows read from any start line up with
+// how the TMA wrote them).  Boxes reaching outside the input read zeros,
+// which is the boundary handling.
+//
+// Operand B: for every (phase pair, D tap, H tap, input W offset) one panel
+// with the C_out rows of each W phase whose tap reads that offset (W phase 0
+// first), so that one box brings it and, where both W phases read the
+// offset, one MMA of N = 2 x C_out covers both.
+//
+// Roles (persistent CTA, one per SM):
+//   warp 0      TMA producer of the A ring (input windows)
+//   warps 1-4   TMA producers of the B ring (weight panels), one per slot
+//               (one thread's TMA stream completes about one box at a time)
+//   warps 5-6   TMEM allocation and MMA issue, one warp per tile of the
+//               pair and its accumulator (one thread issues an MMA only every
+//               ~100+ clocks; two warps nearly double the rate); both consume
+//               every stage
+//   warps 7-14  epilogue, two per TMEM lane quarter: with a tile pair, half
+//               j drains tile j; with single tiles the halves take alternate
+//               16-channel chunks.  tcgen05.ld, bias, and each position's even
+//               and odd W outputs written as one float2
+// Every ring slot has exactly one producer, which refills it only after
+// waiting for its previous round, so a parity wait never has to tell two
+// phases apart.  Every mbarrier wait is bounded: a timeout records
+// CT_ERR_DEVICE_TIMEOUT in the device status word and the roles unwind (the
+// producers wait, bounded, for their own TMA copies and the MMA issuers for
+// their own MMAs before the TMEM is freed).
 #include <string.h>
 
 #include "ct_internal.h"
@@ -51,80 +66,115 @@ namespace ct {
 namespace {
 
 constexpr int BM = 128;      // positions per tile (UMMA M)
+constexpr int QWT = 16;      // qw per tile (TMEM row m: qw = m / 8)
+constexpr int MHT = 8;       // qh per tile (one 8-row swizzle group per qw)
 constexpr int BK = 64;       // bf16 elements of K per stage (one 128-byte swizzle row)
 constexpr int UK = 16;       // K of one tcgen05.mma kind::f16
-constexpr int MAXST = 8;     // pipeline stages at most
-constexpr int MAXWE = 5;     // distinct input W offsets of a tile at most (taps per dimension + 1)
-constexpr int NPROD = 4;     // TMA producer warps at most (stage g is loaded by warp g mod nprod)
-constexpr int EPW = 2;       // epilogue warps per TMEM lane quarter
+constexpr int NA = 2;        // A ring slots (input windows of a tile pair)
+constexpr int MAXB = 4;      // B ring slots at most
+constexpr int NPB = 4;       // B producer warps at most (slot s loaded by warp s mod npb)
 constexpr int NMMA = 2;      // MMA-issuing warps at most (one per TMEM accumulator)
-constexpr int kMmaWarp0 = NPROD;
-constexpr int kEpiWarp0 = NPROD + NMMA;
-constexpr int kThreads = 32 * (NPROD + NMMA + 4 * EPW);
+constexpr int MAXWE = 5;     // distinct input W offsets of a tile at most (taps per dimension + 1)
+constexpr int EPW = 2;       // epilogue warps per TMEM lane quarter
+constexpr int kAWarp = 0;
+constexpr int kBWarp0 = 1;
+constexpr int kMmaWarp0 = kBWarp0 + NPB;
+constexpr int kEpiWarp0 = kMmaWarp0 + NMMA;
+constexpr int kThreads = 32 * (kEpiWarp0 + 4 * EPW);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct UParams {
     int N, C_in, C_out;
     int Lo0, Lo1, Lo2;
-    int QD, QH, QW, MH, n_qhb;
+    int QD, QH, QW, n_qhp, n_qwb;   // n_qhp: pairs of 8-row qh blocks
     int nT;                  // taps per dimension and class (kernel extent / 2)
     int n_kb;                // C_in / BK
     int ntiles;
-    int nst;                 // pipeline stages (a multiple of nprod and of nacc)
-    int nprod;               // producer warps in use: stage slot s is loaded only by warp s mod nprod
-    int nacc;                // TMEM accumulators (1 or 2)
+    int nacc;                // TMEM accumulators = MMA issuers = tiles per pair (1 or 2)
+    int nb, npb;             // B ring slots and B producers (nb a multiple of npb)
+    int b_split;             // 1: a two-phase panel (2 x C_out > 256 rows) comes as two boxes
     uint32_t acc_cols;       // columns of one accumulator (2 x C_out)
     uint32_t tmem_cols;      // allocated TMEM columns (power of 2 >= nacc x acc_cols)
     uint32_t idesc1;         // instruction descriptor, N = C_out
     uint32_t idesc2;         // instruction descriptor, N = 2 x C_out (0: too wide)
-    uint32_t a_bytes;        // A tile bytes
-    uint32_t b_bytes;        // B tile bytes (one W phase)
-    uint32_t stage_bytes;    // A + two B tiles
+    uint32_t a_slot;         // bytes of an A ring slot (one input window, 1024-aligned)
+    uint32_t b_bytes;        // bytes of one W phase's rows of a panel (C_out x 128)
+    uint32_t sbo;            // A descriptor stride between 8-row groups: hspan x 128
+    int hspan, wspan;        // input window extents (H, W) of a tile pair
+    int dh_lo, dw_lo;        // smallest H / W input offset
     int delta[3][2][4];      // input offset of tap j for residue r, per dimension
     // distinct input W offsets of a tile: offset we_delta[e] is read by tap
     // we_j[r][e] of W phase r (-1: phase r does not read it)
     int nwe;
     int we_delta[MAXWE];
     int we_j[2][MAXWE];
+    int we_prefix[MAXWE];    // panel rows before entry e within its block, in C_out units
+    int blk_units;           // C_out-row units of one (phase pair, D tap, H tap) block
 };
 
-// tile -> (n, qd, qh block, rD, rH); the four (rD, rH) phases of one input
-// region are neighbours, so their A tiles are reused from L2
+// unit -> (n, qd, qh block pair, qw block, rD, rH); tile j of the pair is qh
+// block 2 * qhp + j.  The four (rD, rH) phases of one position block are
+// neighbours, so their input windows are reused from L2
 struct TileCoord {
-    int n, qd, qhb, rD, rH;
+    int n, qd, qhp, qwb, rD, rH;
 };
 __device__ __forceinline__ TileCoord tile_coord(int t, const UParams &p)
 {
     TileCoord c;
     c.rH = t & 1; t >>= 1;
     c.rD = t & 1; t >>= 1;
-    c.qhb = t % p.n_qhb; t /= p.n_qhb;
+    c.qwb = t % p.n_qwb; t /= p.n_qwb;
+    c.qhp = t % p.n_qhp; t /= p.n_qhp;
     c.qd = t % p.QD; t /= p.QD;
     c.n = t;
     return c;
 }
 
+// K-major, 128-byte swizzled operand with 8-row groups `sbo` bytes apart
+__device__ __forceinline__ uint64_t desc_sw128_sbo(uint32_t saddr, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;                       // leading byte offset (unused)
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;   // stride byte offset
+    d |= (uint64_t)1 << 46;                       // descriptor version (sm_100 family)
+    d |= (uint64_t)2 << 61;                       // 128-byte swizzle
+    return d;
+}
+
 // ---- GEMM kernel -------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
-umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const float *__restrict__ bias, float *__restrict__ y, UParams p, unsigned int *status)
+umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB1,
+                 const __grid_constant__ CUtensorMap tmB2, const float *__restrict__ bias, float *__restrict__ y,
+                 const __grid_constant__ UParams p, unsigned int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[MAXST], empty_bar[MAXST], acc_full[2], acc_empty[2], drain_bar[NMMA];
+    __shared__ __align__(8) uint64_t a_full[NA], a_empty[NA], b_full[MAXB], b_empty[MAXB], acc_full[2],
+        acc_empty[2], drain_bar[NMMA];
     __shared__ uint32_t tmem_slot;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;                                // NA x a_slot
+    uint8_t *sB = smem + (size_t)NA * p.a_slot;        // nb x 2 x b_bytes
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t b_slot = 2 * p.b_bytes;
 
     if (threadIdx.x == 0) {
         dev::prefetch_tensormap(&tmA);
-        dev::prefetch_tensormap(&tmB);
-        for (int s = 0; s < p.nst; ++s) {
-            dev::mbar_init(&full_bar[s], 1);
-            dev::mbar_init(&empty_bar[s], 1);
+        dev::prefetch_tensormap(&tmB1);
+        dev::prefetch_tensormap(&tmB2);
+        // a stage is released by every issuer, an accumulator by the epilogue
+        // threads that read it (all of them with one tile per unit, half with two)
+        for (int s = 0; s < NA; ++s) {
+            dev::mbar_init(&a_full[s], 1);
+            dev::mbar_init(&a_empty[s], p.nacc);
+        }
+        for (int s = 0; s < p.nb; ++s) {
+            dev::mbar_init(&b_full[s], 1);
+            dev::mbar_init(&b_empty[s], p.nacc);
         }
         for (int a = 0; a < 2; ++a) {
             dev::mbar_init(&acc_full[a], 1);
-            dev::mbar_init(&acc_empty[a], 32 * 4 * EPW);   // every epilogue thread
+            dev::mbar_init(&acc_empty[a], 32 * 4 * EPW / p.nacc);
         }
         for (int j = 0; j < NMMA; ++j) dev::mbar_init(&drain_bar[j], 1);
         dev::fence_mbar_init();
@@ -136,67 +186,78 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const uint32_t tmem = tmem_slot;
     const int ntile_cta =
         p.ntiles > (int)blockIdx.x ? (p.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int stages_per_tile = p.nT * p.nT * p.n_kb * p.nwe;
-    // With two accumulators, two warps issue MMAs, each for alternate tiles (one
-    // thread issues an MMA only every ~100+ clocks, two nearly double the rate).
-    // The ring then carries the two tiles of a pair interleaved stage by stage:
-    // stage i of tile k sits at g = (k / ni) * ni * spt + i * ni + k mod ni.
+    // stages per unit: A = (D tap, K block); B = (D tap, K block, H tap, W offset).
+    // A unit is a pair of tiles (two 8-row qh blocks) when two accumulators fit:
+    // both issuers consume every stage, issuer j computing tile j from the shared
+    // input window (8 rows further down for tile 1) and the shared weight panel.
+    const int spa = p.nT * p.n_kb;
+    const int spb = spa * p.nT * p.nwe;
     const int ni = p.nacc;
 
-    if (warp < NPROD) {
-        // ---------------- TMA producers: a TMA stream of one thread completes about
-        // one box at a time, so nprod warps take turns, warp q loading the stages
-        // g = q, q + nprod, ... of this CTA's sequence.  nst is a multiple of nprod,
-        // so every stage slot has one producer, which reuses it only after waiting
-        // for the slot's previous round: a parity wait never skips a phase.
-        if (lane == 0 && warp < p.nprod) {
-            const int total = (ntile_cta + ni - 1) / ni * ni * stages_per_tile;
-            int g = warp, last = -1;
+    if (warp == kAWarp || (warp >= kBWarp0 && warp < kBWarp0 + NPB)) {
+        // ---------------- TMA producers
+        const bool isA = warp == kAWarp;
+        const int q = isA ? 0 : warp - kBWarp0;
+        if (lane == 0 && (isA || q < p.npb)) {
+            const int np = isA ? 1 : p.npb;
+            const int nst = isA ? NA : p.nb;
+            const int sp = isA ? spa : spb;
+            uint64_t *fullb = isA ? a_full : b_full;
+            uint64_t *emptyb = isA ? a_empty : b_empty;
+            const int total = ntile_cta * sp;
+            int last = -1, kc = -1;
             bool failed = false;
-            int kc = -1, qh0 = 0, ph0 = 0;
             TileCoord tcd;
-            for (; g < total; g += p.nprod) {
-                const int pr = g / (ni * stages_per_tile), rr = g % (ni * stages_per_tile);
-                const int i = rr / ni, k = pr * ni + rr % ni;
-                if (k >= ntile_cta) continue;          // the missing partner of a last, lone tile
+            tcd.n = tcd.qd = tcd.qhp = tcd.qwb = tcd.rD = tcd.rH = 0;
+            for (int g = q; g < total; g += np) {
+                const int k = g / sp, i = g % sp;
                 if (k != kc) {
                     kc = k;
                     tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
-                    qh0 = tcd.qhb * p.MH;
-                    ph0 = (tcd.rD * 2 + tcd.rH) * 2;
                 }
-                const int e = i % p.nwe;
-                int r = i / p.nwe;
-                const int kb = r % p.n_kb; r /= p.n_kb;
-                const int jh = r % p.nT, jd = r / p.nT;
-                const int s = g % p.nst;
-                if (g >= p.nst && !dev::mbar_wait_bounded(&empty_bar[s], ((g / p.nst) - 1) & 1, kWaitLimitNs)) {
-                    atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
+                const int s = g % nst;
+                if (g >= nst && !dev::mbar_wait_bounded(&emptyb[s], ((g / nst) - 1) & 1, kWaitLimitNs)) {
                     failed = true;
                     break;
                 }
-                const int j0 = p.we_j[0][e], j1 = p.we_j[1][e];
-                uint8_t *a_s = smem + (size_t)s * p.stage_bytes;
-                uint8_t *b_s = a_s + p.a_bytes;
-                dev::mbar_arrive_expect_tx(&full_bar[s], p.a_bytes + p.b_bytes * (uint32_t)((j0 >= 0) + (j1 >= 0)));
-                dev::tma_load_5d(a_s, &tmA, &full_bar[s], kb * BK, p.we_delta[e],
-                                 qh0 + p.delta[1][tcd.rH][jh], tcd.qd + p.delta[0][tcd.rD][jd], tcd.n);
-                const int tap0 = (jd * p.nT + jh) * p.nT;
-                if (j0 >= 0)
-                    dev::tma_load_2d(b_s, &tmB, &full_bar[s], (tap0 + j0) * p.C_in + kb * BK, ph0 * p.C_out);
-                if (j1 >= 0)
-                    dev::tma_load_2d(b_s + p.b_bytes, &tmB, &full_bar[s], (tap0 + j1) * p.C_in + kb * BK,
-                                     (ph0 + 1) * p.C_out);
+                if (isA) {
+                    const int jd = i / p.n_kb, kb = i % p.n_kb;
+                    dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(p.hspan * p.wspan) * 128u);
+                    // x_t viewed as (C, H, W, D, N): the window from (qh0 + dh_lo, qw0 + dw_lo)
+                    dev::tma_load_5d(sA + (size_t)s * p.a_slot, &tmA, &fullb[s], kb * BK,
+                                     tcd.qhp * ni * MHT + p.dh_lo, tcd.qwb * QWT + p.dw_lo,
+                                     tcd.qd + p.delta[0][tcd.rD][jd], tcd.n);
+                } else {
+                    const int e = i % p.nwe;
+                    int r = i / p.nwe;
+                    const int jh = r % p.nT;
+                    r /= p.nT;
+                    const int kb = r % p.n_kb, jd = r / p.n_kb;
+                    const bool both = p.we_j[0][e] >= 0 && p.we_j[1][e] >= 0;
+                    const int ph2 = tcd.rD * 2 + tcd.rH;
+                    const int brow = (((ph2 * p.nT + jd) * p.nT + jh) * p.blk_units + p.we_prefix[e]) * p.C_out;
+                    dev::mbar_arrive_expect_tx(&fullb[s], both ? 2 * p.b_bytes : p.b_bytes);
+                    if (both && p.b_split) {
+                        dev::tma_load_2d(sB + (size_t)s * b_slot, &tmB1, &fullb[s], kb * BK, brow);
+                        dev::tma_load_2d(sB + (size_t)s * b_slot + p.b_bytes, &tmB1, &fullb[s], kb * BK,
+                                         brow + p.C_out);
+                    } else {
+                        dev::tma_load_2d(sB + (size_t)s * b_slot, both ? &tmB2 : &tmB1, &fullb[s], kb * BK, brow);
+                    }
+                }
                 last = g;
             }
-            if (failed)   // let this warp's copies still in flight land before shared memory goes away
-                for (int q = last; q >= 0 && q > last - p.nst; q -= p.nprod)
-                    dev::mbar_wait_bounded(&full_bar[q % p.nst], (q / p.nst) & 1, kWaitLimitNs);
+            if (failed) {
+                atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
+                // let this warp's copies still in flight land before shared memory goes away
+                for (int r = last; r >= 0 && r > last - nst; r -= np)
+                    dev::mbar_wait_bounded(&fullb[r % nst], (r / nst) & 1, kWaitLimitNs);
+            }
         }
     } else if (warp < kMmaWarp0 + NMMA) {
         // ---------------- MMA issuers.  An MMA costs the issuing thread about 100
-        // clocks at best, so the loop carries its ring slot, parity and W-offset
-        // index as counters (no division) and keeps the per-offset flags in registers.
+        // clocks at best, so the loop carries ring slots, parities and indices as
+        // counters and keeps the per-offset data in registers.
         const int j = warp - kMmaWarp0;
         if (lane == 0 && j < ni) {
             bool ok = true;
@@ -205,61 +266,79 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (p.we_j[0][e] >= 0) m0 |= 1u << e;
                 if (p.we_j[1][e] >= 0) m1 |= 1u << e;
             }
-            const uint32_t sbase = dev::smem_u32(smem);
-            const uint32_t idesc1 = p.idesc1, idesc2 = p.idesc2, stage_bytes = p.stage_bytes;
-            const uint32_t a_bytes = p.a_bytes, b_bytes = p.b_bytes, c_out = (uint32_t)p.C_out;
-            const int nst = p.nst, nwe = p.nwe;
-            int s = j;                                  // ring position g = j, j + ni, ...
-            uint32_t par = 0;
-            for (int k = j; k < ntile_cta && ok; k += ni) {
-                const int a = j;
-                const int use = k / ni;                        // earlier tiles in accumulator a
-                if (use > 0 && !dev::mbar_wait_bounded(&acc_empty[a], (use - 1) & 1, kWaitLimitNs)) {
+            const uint32_t sAb = dev::smem_u32(sA), sBb = dev::smem_u32(sB);
+            const uint32_t idesc1 = p.idesc1, idesc2 = p.idesc2, a_slot = p.a_slot, b_bytes = p.b_bytes;
+            const uint32_t sbo = p.sbo, c_out = (uint32_t)p.C_out;
+            const int nwe = p.nwe, nT = p.nT, n_kb = p.n_kb, nb = p.nb;
+            const uint32_t trow = (uint32_t)(j * MHT) * 128u;   // tile j's rows in the window
+            int sa = 0, sb = 0;
+            uint32_t pa = 0, pb = 0;
+            for (int k = 0; k < ntile_cta && ok; ++k) {
+                const TileCoord tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
+                if (k > 0 && !dev::mbar_wait_bounded(&acc_empty[j], (k - 1) & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after();
-                const uint32_t d0 = tmem + (uint32_t)a * p.acc_cols;
+                const uint32_t d0 = tmem + (uint32_t)j * p.acc_cols;
                 const uint32_t d1 = d0 + c_out;
                 bool init0 = false, init1 = false;
-                int e = 0;
-                for (int i = 0; i < stages_per_tile; ++i) {
-                    if (!dev::mbar_wait_bounded(&full_bar[s], par, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after();
-                    const bool h0 = (m0 >> e) & 1u, h1 = (m1 >> e) & 1u;
-                    const uint32_t a_addr = sbase + (uint32_t)s * stage_bytes;
-                    const uint64_t da = tc::desc_sw128(a_addr);
-                    const uint64_t db0 = tc::desc_sw128(a_addr + a_bytes);
-                    const uint64_t db1 = tc::desc_sw128(a_addr + a_bytes + b_bytes);
-                    if (h0 && h1 && idesc2 && init0 == init1) {
-                        // both halves in one MMA (they hold the same number of terms)
+                for (int jd = 0; jd < nT && ok; ++jd)
+                    for (int kb = 0; kb < n_kb && ok; ++kb) {
+                        if (!dev::mbar_wait_bounded(&a_full[sa], pa, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after();
+                        const uint32_t wbase = sAb + (uint32_t)sa * a_slot;
+                        for (int jh = 0; jh < nT && ok; ++jh) {
+                            const uint32_t hoff = (uint32_t)(p.delta[1][tcd.rH][jh] - p.dh_lo) * 128u;
+                            for (int e = 0; e < nwe; ++e) {
+                                if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc::fence_after();
+                                const bool h0 = (m0 >> e) & 1u, h1 = (m1 >> e) & 1u;
+                                // window column of this W offset: (dw - dw_lo) * hspan rows
+                                const uint32_t aw = (uint32_t)((p.we_delta[e] - p.dw_lo) * p.hspan) * 128u;
+                                const uint64_t da = desc_sw128_sbo(wbase + aw + hoff + trow, sbo);
+                                const uint32_t bb = sBb + (uint32_t)sb * 2u * b_bytes;
+                                const uint64_t db0 = tc::desc_sw128(bb);
+                                const uint64_t db1 = tc::desc_sw128(bb + (h0 ? b_bytes : 0u));
+                                if (h0 && h1 && idesc2 && init0 == init1) {
+                                    // both W phases in one MMA (they hold the same number of terms)
 #pragma unroll
-                        for (int kk = 0; kk < BK / UK; ++kk)   // 16 bf16 = 32 bytes along K per step
-                            tc::mma_bf16(d0, da + 2 * kk, db0 + 2 * kk, idesc2, (init0 || kk) ? 1u : 0u);
-                    } else {
-                        if (h0)
+                                    for (int kk = 0; kk < BK / UK; ++kk)   // 16 bf16 = 32 bytes along K
+                                        tc::mma_bf16(d0, da + 2 * kk, db0 + 2 * kk, idesc2, (init0 || kk) ? 1u : 0u);
+                                } else {
+                                    if (h0)
 #pragma unroll
-                            for (int kk = 0; kk < BK / UK; ++kk)
-                                tc::mma_bf16(d0, da + 2 * kk, db0 + 2 * kk, idesc1, (init0 || kk) ? 1u : 0u);
-                        if (h1)
+                                        for (int kk = 0; kk < BK / UK; ++kk)
+                                            tc::mma_bf16(d0, da + 2 * kk, db0 + 2 * kk, idesc1,
+                                                         (init0 || kk) ? 1u : 0u);
+                                    if (h1)
 #pragma unroll
-                            for (int kk = 0; kk < BK / UK; ++kk)
-                                tc::mma_bf16(d1, da + 2 * kk, db1 + 2 * kk, idesc1, (init1 || kk) ? 1u : 0u);
+                                        for (int kk = 0; kk < BK / UK; ++kk)
+                                            tc::mma_bf16(d1, da + 2 * kk, db1 + 2 * kk, idesc1,
+                                                         (init1 || kk) ? 1u : 0u);
+                                }
+                                init0 = init0 || h0;
+                                init1 = init1 || h1;
+                                tc::commit(&b_empty[sb]);
+                                if (++sb == nb) {
+                                    sb = 0;
+                                    pb ^= 1u;
+                                }
+                            }
+                        }
+                        tc::commit(&a_empty[sa]);
+                        if (++sa == NA) {
+                            sa = 0;
+                            pa ^= 1u;
+                        }
                     }
-                    init0 = init0 || h0;
-                    init1 = init1 || h1;
-                    tc::commit(&empty_bar[s]);
-                    s += ni;                                   // nst is a multiple of ni
-                    if (s >= nst) {
-                        s -= nst;
-                        par ^= 1u;
-                    }
-                    if (++e == nwe) e = 0;
-                }
-                if (ok) tc::commit(&acc_full[a]);
+                if (ok) tc::commit(&acc_full[j]);
             }
             // every MMA issued has to complete before the TMEM is freed
             tc::commit(&drain_bar[j]);
@@ -267,45 +346,47 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
     } else {
-        // ---------------- epilogue: EPW warps per TMEM lane quarter (32 positions);
-        // a warp reaches the lanes of quarter warp mod 4
+        // ---------------- epilogue: EPW warps per TMEM lane quarter (32 positions:
+        // 4 qw x 8 qh); a warp reaches the lanes of quarter warp mod 4.  With two
+        // tiles per unit, half j of the warps drains tile j (accumulator j) and
+        // takes every 16-channel chunk; with one, the halves take alternate chunks.
         const int ew = warp & 3;
         const int half = (warp - kEpiWarp0) >> 2;
+        const int a = ni == 2 ? half : 0;
+        const int cfirst = ni == 2 ? 0 : half, cstep = ni == 2 ? 1 : EPW;
         const int nchunk = p.C_out / 16;
         const int64_t sp = (int64_t)p.Lo0 * p.Lo1 * p.Lo2;
         bool ok = true;
         for (int k = 0; k < ntile_cta; ++k) {
             const TileCoord tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
-            const int a = p.nacc == 2 ? (k & 1) : 0;
-            const int use = p.nacc == 2 ? (k >> 1) : k;
-            if (ok && !dev::mbar_wait_bounded(&acc_full[a], use & 1, kWaitLimitNs)) {
+            if (ok && !dev::mbar_wait_bounded(&acc_full[a], k & 1, kWaitLimitNs)) {
                 atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
                 ok = false;
             }
             ok = __all_sync(0xffffffffu, ok);        // warp-uniform before .sync.aligned loads
             tc::fence_after();
             const int m = ew * 32 + lane;
-            const int qh = tcd.qhb * p.MH + m / p.QW, qw = m % p.QW;
+            const int qw = tcd.qwb * QWT + (m >> 3), qh = (tcd.qhp * ni + a) * MHT + (m & 7);
             const int od = 2 * tcd.qd + tcd.rD, oh = 2 * qh + tcd.rH;
-            const bool valid = od < p.Lo0 && oh < p.Lo1;
+            const bool valid = qw < p.QW && od < p.Lo0 && oh < p.Lo1;
             float *yrow = y + (int64_t)tcd.n * p.C_out * sp + ((int64_t)od * p.Lo1 + oh) * p.Lo2 + 2 * qw;
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols;
-            // chunks half, half + EPW, ..., two per batch; the accumulator is
-            // released as soon as the warp's last batch is in registers
+            // two chunks per batch; the accumulator is released as soon as the
+            // warp's last batch is in registers
             bool released = false;
-            for (int ci = half; ci < nchunk; ci += 2 * EPW) {
-                const bool two = ci + EPW < nchunk;
+            for (int ci = cfirst; ci < nchunk; ci += 2 * cstep) {
+                const bool two = ci + cstep < nchunk;
                 float v0[2][16], v1[2][16];
                 if (ok) {
                     tc::tmem_ld16(tbase + (uint32_t)(ci * 16), v0[0]);
                     tc::tmem_ld16(tbase + (uint32_t)(p.C_out + ci * 16), v1[0]);
                     if (two) {
-                        tc::tmem_ld16(tbase + (uint32_t)((ci + EPW) * 16), v0[1]);
-                        tc::tmem_ld16(tbase + (uint32_t)(p.C_out + (ci + EPW) * 16), v1[1]);
+                        tc::tmem_ld16(tbase + (uint32_t)((ci + cstep) * 16), v0[1]);
+                        tc::tmem_ld16(tbase + (uint32_t)(p.C_out + (ci + cstep) * 16), v1[1]);
                     }
                     tc::tmem_wait_ld();
                 }
-                if (ci + 2 * EPW >= nchunk) {
+                if (ci + 2 * cstep >= nchunk) {
                     tc::fence_before();
                     dev::mbar_arrive(&acc_empty[a]);
                     released = true;
@@ -314,7 +395,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
                         if (b == 1 && !two) break;
-                        const int c0 = (ci + b * EPW) * 16;
+                        const int c0 = (ci + b * cstep) * 16;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int oc = c0 + i;
@@ -369,40 +450,43 @@ __device__ __forceinline__ void repack_load_pairs(const bf16_t *__restrict__ src
     }
 }
 
-// x (N, C, S) -> x_cl (N, S, C), S = D*H*W; S a multiple of 8, C of 64.
+// x (N, C, D, H, W) -> x_t (N, D, W, H, C); D*H*W a multiple of 8, C of 64.
 __global__ void __launch_bounds__(256)
-repack_x_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xcl, int C, int64_t SP)
+repack_x_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, int C, int D, int H, int W)
 {
     __shared__ uint32_t tile[RB][33];
+    const int64_t SP = (int64_t)D * H * W;
     const int n = blockIdx.z;
     const int c0 = blockIdx.y * RB;
     const int64_t s0 = (int64_t)blockIdx.x * RB;
     const int ncols = (int)((SP - s0) < RB ? (SP - s0) : RB);
     repack_load_pairs(x + ((int64_t)n * C + c0) * SP + s0, SP, ncols, tile);
     __syncthreads();
-    bf16_t *xd = xcl + ((int64_t)n * SP + s0) * C + c0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         const int o = threadIdx.x + 256 * t;
         const int q = o & 7, row = o >> 3;
         if (row < ncols) {
+            const int64_t s = s0 + row;                 // (d, h, w) of the source position
+            const int w = (int)(s % W), h = (int)((s / W) % H), d = (int)(s / ((int64_t)W * H));
+            const int64_t dst = ((((int64_t)n * D + d) * W + w) * H + h) * C + c0 + 8 * q;
             const uint4 v = make_uint4(tile[row][4 * q], tile[row][4 * q + 1], tile[row][4 * q + 2],
                                        tile[row][4 * q + 3]);
-            *reinterpret_cast<uint4 *>(xd + (int64_t)row * C + 8 * q) = v;
+            *reinterpret_cast<uint4 *>(xt + dst) = v;
         }
     }
 }
 
-// The same move, one bf16 at a time, for S not a multiple of 8.
+// The same move, one bf16 at a time, for D*H*W not a multiple of 8.
 __global__ void __launch_bounds__(256)
-repack_x_scalar_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xcl, int C, int64_t SP)
+repack_x_scalar_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, int C, int D, int H, int W)
 {
     __shared__ bf16_t tile[64][66];
+    const int64_t SP = (int64_t)D * H * W;
     const int n = blockIdx.z;
     const int c0 = blockIdx.y * 64;
     const int64_t s0 = (int64_t)blockIdx.x * 64;
     const bf16_t *xs = x + (int64_t)n * C * SP;
-    bf16_t *xd = xcl + (int64_t)n * C * SP;
     for (int e = threadIdx.x; e < 64 * 64; e += 256) {
         const int c = e >> 6, s = e & 63;
         tile[c][s] = (c0 + c < C && s0 + s < SP) ? xs[(int64_t)(c0 + c) * SP + s0 + s] : (bf16_t)0;
@@ -410,19 +494,27 @@ repack_x_scalar_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xcl, i
     __syncthreads();
     for (int e = threadIdx.x; e < 64 * 64; e += 256) {
         const int s = e >> 6, c = e & 63;
-        if (c0 + c < C && s0 + s < SP) xd[(s0 + s) * C + c0 + c] = tile[c][s];
+        if (c0 + c < C && s0 + s < SP) {
+            const int64_t ss = s0 + s;
+            const int w = (int)(ss % W), h = (int)((ss / W) % H), d = (int)(ss / ((int64_t)W * H));
+            xt[((((int64_t)n * D + d) * W + w) * H + h) * C + c0 + c] = tile[c][s];
+        }
     }
 }
 
 struct WPackParams {
     int C_in, C_out, K0, K1, K2, nT;
-    int k[3][2][4];          // tap k of index j for residue r, per dimension
     int r_of[3][8];          // residue and tap index that kernel index k belongs to
     int j_of[3][8];
+    int e_of[2][4];          // W offset entry read by tap j of W phase r
+    int half_of[2][4];       // 1 if that phase's rows follow W phase 0's rows in the panel
+    int we_prefix[MAXWE];
+    int blk_units;
 };
 
-// w (C_in, C_out, K0, K1, K2) -> w_p[phase][oc][tap][ic], phase = (rD, rH, rW),
-// tap = (jd, jh, jw), ic fastest.  Every kernel index (kd, kh, kw) belongs to
+// w (C_in, C_out, K0, K1, K2) -> weight panels: for every (phase pair, D tap,
+// H tap, W offset entry), the C_out rows of each W phase reading that offset
+// (phase 0 first), C_in fastest.  Every kernel index (kd, kh, kw) belongs to
 // exactly one (phase, tap), so each (ic, oc) row of kD*kH*kW weights is
 // scattered once.  Block = (64 input channels, one oc); columns = kernel
 // indices in chunks of 64 (kD*kH*kW is a multiple of 8: even extents).
@@ -433,7 +525,6 @@ repack_w_kernel(const bf16_t *__restrict__ w, bf16_t *__restrict__ wp, WPackPara
     const int ic0 = blockIdx.x * RB;
     const int oc = blockIdx.y;
     const int kvol = q.K0 * q.K1 * q.K2;
-    const int ntap = q.nT * q.nT * q.nT;
     const int64_t row_stride = (int64_t)q.C_out * kvol;
     for (int kc = 0; kc < kvol; kc += RB) {
         const int ncols = (kvol - kc) < RB ? (kvol - kc) : RB;
@@ -447,12 +538,14 @@ repack_w_kernel(const bf16_t *__restrict__ w, bf16_t *__restrict__ wp, WPackPara
             if (row < ncols) {
                 const int k = kc + row;
                 const int kw = k % q.K2, kh = (k / q.K2) % q.K1, kd = k / (q.K1 * q.K2);
-                const int ph = (q.r_of[0][kd] << 2) | (q.r_of[1][kh] << 1) | q.r_of[2][kw];
-                const int tap = (q.j_of[0][kd] * q.nT + q.j_of[1][kh]) * q.nT + q.j_of[2][kw];
+                const int ph2 = (q.r_of[0][kd] << 1) | q.r_of[1][kh];
+                const int rw = q.r_of[2][kw], jw = q.j_of[2][kw];
+                const int e = q.e_of[rw][jw];
+                const int unit = ((ph2 * q.nT + q.j_of[0][kd]) * q.nT + q.j_of[1][kh]) * q.blk_units +
+                                 q.we_prefix[e] + q.half_of[rw][jw];
                 const uint4 v = make_uint4(tile[row][4 * qq], tile[row][4 * qq + 1],
                                            tile[row][4 * qq + 2], tile[row][4 * qq + 3]);
-                *reinterpret_cast<uint4 *>(wp + (((int64_t)ph * q.C_out + oc) * ntap + tap) * q.C_in +
-                                           ic0 + 8 * qq) = v;
+                *reinterpret_cast<uint4 *>(wp + ((int64_t)unit * q.C_out + oc) * q.C_in + ic0 + 8 * qq) = v;
             }
         }
     }
@@ -482,14 +575,15 @@ bool make_uplan(const Problem &pb, UPlan *out)
     p.N = pb.N; p.C_in = pb.C_in; p.C_out = pb.C_out;
     p.Lo0 = pb.Lo[0]; p.Lo1 = pb.Lo[1]; p.Lo2 = pb.Lo[2];
     p.QW = p.Lo2 / 2;
-    if (p.QW > BM || BM % p.QW != 0) return false;
-    p.MH = BM / p.QW;
     p.QD = (p.Lo0 + 1) / 2;
     p.QH = (p.Lo1 + 1) / 2;
-    p.n_qhb = (p.QH + p.MH - 1) / p.MH;
+    p.n_qwb = (p.QW + QWT - 1) / QWT;
+    p.nacc = 4 * pb.C_out <= 512 ? 2 : 1;     // tiles per unit
+    const int n_qhb = (p.QH + MHT - 1) / MHT;
+    p.n_qhp = (n_qhb + p.nacc - 1) / p.nacc;
     p.nT = pb.K[0] / 2;
     p.n_kb = pb.C_in / BK;
-    const int64_t tiles = (int64_t)pb.N * p.QD * p.n_qhb * 4;
+    const int64_t tiles = (int64_t)pb.N * p.QD * p.n_qhp * p.n_qwb * 4;
     if (tiles > 0x7fffffff || tiles == 0) return false;
     p.ntiles = (int)tiles;
     // residue r of a stride-2 dimension takes the taps k == (r + p) mod 2, i.e.
@@ -502,25 +596,33 @@ bool make_uplan(const Problem &pb, UPlan *out)
             const int base = (r + pb.P[d] - c) / 2;
             for (int j = 0; j < p.nT; ++j) {
                 p.delta[d][r][j] = base - j;
-                wq.k[d][r][j] = c + 2 * j;
                 wq.r_of[d][c + 2 * j] = r;
                 wq.j_of[d][c + 2 * j] = j;
             }
         }
     }
-    wq.C_in = pb.C_in; wq.C_out = pb.C_out; wq.nT = p.nT;
-    wq.K0 = pb.K[0]; wq.K1 = pb.K[1]; wq.K2 = pb.K[2];
+    // input windows: H and W offsets span [lo, hi]
+    int lo[3], hi[3];
+    for (int d = 1; d < 3; ++d) {
+        lo[d] = hi[d] = p.delta[d][0][0];
+        for (int r = 0; r < 2; ++r)
+            for (int j = 0; j < p.nT; ++j) {
+                lo[d] = p.delta[d][r][j] < lo[d] ? p.delta[d][r][j] : lo[d];
+                hi[d] = p.delta[d][r][j] > hi[d] ? p.delta[d][r][j] : hi[d];
+            }
+    }
+    p.dh_lo = lo[1];
+    p.dw_lo = lo[2];
+    p.hspan = p.nacc * MHT + hi[1] - lo[1];
+    p.wspan = QWT + hi[2] - lo[2];
+    if (p.hspan > 256 || p.wspan > 256) return false;
+    p.sbo = (uint32_t)p.hspan * 128u;
+    p.a_slot = (uint32_t)((p.hspan * p.wspan * 128 + 1023) & ~1023);
     // distinct input W offsets: the two W residues' offsets differ by 0 or 1, so
     // there are at most nT + 1; offsets both phases read come first, so the first
     // MMA of a tile initialises both halves of the accumulator at once
-    int lo = p.delta[2][0][0], hi = p.delta[2][0][0];
-    for (int r = 0; r < 2; ++r)
-        for (int j = 0; j < p.nT; ++j) {
-            lo = p.delta[2][r][j] < lo ? p.delta[2][r][j] : lo;
-            hi = p.delta[2][r][j] > hi ? p.delta[2][r][j] : hi;
-        }
     for (int pass = 0; pass < 3; ++pass)
-        for (int dv = lo; dv <= hi; ++dv) {
+        for (int dv = lo[2]; dv <= hi[2]; ++dv) {
             int jr[2] = {-1, -1};
             for (int r = 0; r < 2; ++r)
                 for (int j = 0; j < p.nT; ++j)
@@ -533,32 +635,49 @@ bool make_uplan(const Problem &pb, UPlan *out)
             p.we_j[1][p.nwe] = jr[1];
             ++p.nwe;
         }
+    // panel rows of each entry within a (phase pair, D tap, H tap) block
+    int units = 0;
+    for (int e = 0; e < p.nwe; ++e) {
+        p.we_prefix[e] = units;
+        wq.we_prefix[e] = units;
+        for (int r = 0; r < 2; ++r) {
+            const int jj = p.we_j[r][e];
+            if (jj < 0) continue;
+            wq.e_of[r][jj] = e;
+            wq.half_of[r][jj] = (r == 1 && p.we_j[0][e] >= 0) ? 1 : 0;
+            ++units;
+        }
+    }
+    if (units != 2 * p.nT) return false;        // every (W phase, tap) in exactly one panel
+    p.blk_units = units;
+    wq.blk_units = units;
+    wq.C_in = pb.C_in; wq.C_out = pb.C_out; wq.nT = p.nT;
+    wq.K0 = pb.K[0]; wq.K1 = pb.K[1]; wq.K2 = pb.K[2];
     p.idesc1 = tc::idesc(1, pb.C_out, BM);
     p.idesc2 = 2 * pb.C_out <= 256 ? tc::idesc(1, 2 * pb.C_out, BM) : 0u;
     p.acc_cols = (uint32_t)(2 * pb.C_out);
-    p.nacc = 4 * pb.C_out <= 512 ? 2 : 1;
     uint32_t cols = 32;
     while (cols < (uint32_t)p.nacc * p.acc_cols) cols <<= 1;
     p.tmem_cols = cols;
-    p.a_bytes = (uint32_t)(BM * BK * 2);
     p.b_bytes = (uint32_t)pb.C_out * BK * 2;
-    p.stage_bytes = p.a_bytes + 2 * p.b_bytes;
-    const size_t budget = 227 * 1024 - 2048;     // alignment slack, static shared memory
-    p.nst = (int)(budget / p.stage_bytes);
-    if (p.nst > MAXST) p.nst = MAXST;
-    if (p.nst < 2) return false;
-    p.nprod = p.nst < NPROD ? p.nst : NPROD;
-    {
-        // one producer per stage slot, and the issuers' interleaved stages on fixed slots
-        const int l = (p.nacc == 2 && p.nprod % 2) ? 2 * p.nprod : p.nprod;
-        p.nst -= p.nst % l;
-        if (p.nst < l) return false;
-    }
+    p.b_split = 2 * pb.C_out > 256 ? 1 : 0;
+    // deepest B ring that fits (room left for the static barriers); one producer
+    // per slot
+    const size_t budget = 227 * 1024 - 2048;
+    const size_t a_area = (size_t)NA * p.a_slot;
+    if (budget < a_area) return false;
+    int nb = (int)((budget - a_area) / (2 * p.b_bytes));
+    if (nb > MAXB) nb = MAXB;
+    if (nb < 2) return false;
+    p.nb = nb;
+    p.npb = nb < NPB ? nb : NPB;
+    while (p.nb % p.npb) --p.npb;
+    const size_t smem = a_area + (size_t)nb * 2 * p.b_bytes + 1024;
     out->p = p;
     out->wq = wq;
     out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * 2);
     out->w_bytes = align256((size_t)8 * pb.C_out * p.nT * p.nT * p.nT * pb.C_in * 2);
-    out->smem = (size_t)p.nst * p.stage_bytes + 1024;
+    out->smem = smem;
     return true;
 }
 
@@ -584,41 +703,46 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     UPlan pl;
     if (!make_uplan(pb, &pl)) return cudaErrorNotSupported;
     const UParams &p = pl.p;
-    bf16_t *xcl = static_cast<bf16_t *>(a.ws);
+    bf16_t *xt = static_cast<bf16_t *>(a.ws);
     bf16_t *wp = reinterpret_cast<bf16_t *>(static_cast<uint8_t *>(a.ws) + pl.x_bytes);
 
-    // 1) x -> channels-last
+    // 1) x -> (N, D, W, H, C)
     const int64_t SP = pb.in_sp();
     dim3 gx((unsigned)((SP + 63) / 64), (unsigned)((pb.C_in + 63) / 64), (unsigned)pb.N);
     if (gx.x > 0x7fffffffu || gx.y > 65535 || gx.z > 65535) return cudaErrorInvalidConfiguration;
     if (SP % 8 == 0)
-        repack_x_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.x), xcl, pb.C_in, SP);
+        repack_x_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.x), xt, pb.C_in, pb.Li[0],
+                                                  pb.Li[1], pb.Li[2]);
     else
-        repack_x_scalar_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.x), xcl, pb.C_in, SP);
+        repack_x_scalar_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.x), xt, pb.C_in, pb.Li[0],
+                                                         pb.Li[1], pb.Li[2]);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // 2) weights -> per-phase K-major
+    // 2) weights -> panels
     dim3 gw((unsigned)(pb.C_in / RB), (unsigned)pb.C_out);
     repack_w_kernel<<<gw, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.w), wp, pl.wq);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // 3) tensor maps: A over x_cl (C, W, H, D, N), B over w_p (K, 8*C_out)
-    CUtensorMap tmA, tmB;
-    const uint64_t adims[5] = {(uint64_t)pb.C_in, (uint64_t)pb.Li[2], (uint64_t)pb.Li[1],
-                               (uint64_t)pb.Li[0], (uint64_t)pb.N};
-    const uint64_t astr[4] = {(uint64_t)pb.C_in * 2, (uint64_t)pb.C_in * pb.Li[2] * 2,
-                              (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * 2,
-                              (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * pb.Li[0] * 2};
-    const uint32_t abox[5] = {(uint32_t)BK, (uint32_t)p.QW, (uint32_t)p.MH, 1u, 1u};
-    if (!encode_tiled(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xcl, adims, astr, abox,
+    // 3) tensor maps: A over x_t viewed as (C, H, W, D, N), one input window per
+    // box; B over the panels (K = C_in, rows), boxes of C_out and 2 x C_out rows
+    CUtensorMap tmA, tmB1, tmB2;
+    const uint64_t adims[5] = {(uint64_t)pb.C_in, (uint64_t)pb.Li[1], (uint64_t)pb.Li[2], (uint64_t)pb.Li[0],
+                               (uint64_t)pb.N};
+    const uint64_t astr[4] = {(uint64_t)pb.C_in * 2, (uint64_t)pb.C_in * pb.Li[1] * 2,
+                              (uint64_t)pb.C_in * pb.Li[1] * pb.Li[2] * 2,
+                              (uint64_t)pb.C_in * pb.Li[1] * pb.Li[2] * pb.Li[0] * 2};
+    const uint32_t abox[5] = {(uint32_t)BK, (uint32_t)p.hspan, (uint32_t)p.wspan, 1u, 1u};
+    if (!encode_tiled(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xt, adims, astr, abox,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const int ntap = p.nT * p.nT * p.nT;
-    const uint64_t bdims[2] = {(uint64_t)ntap * pb.C_in, (uint64_t)8 * pb.C_out};
-    const uint64_t bstr[1] = {(uint64_t)ntap * pb.C_in * 2};
-    const uint32_t bbox[2] = {(uint32_t)BK, (uint32_t)pb.C_out};
-    if (!encode_tiled(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wp, bdims, bstr, bbox,
+    const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)8 * p.nT * p.nT * p.nT * pb.C_out};
+    const uint64_t bstr[1] = {(uint64_t)pb.C_in * 2};
+    const uint32_t bbox1[2] = {(uint32_t)BK, (uint32_t)pb.C_out};
+    const uint32_t bbox2[2] = {(uint32_t)BK, (uint32_t)(2 * pb.C_out <= 256 ? 2 * pb.C_out : pb.C_out)};
+    if (!encode_tiled(&tmB1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wp, bdims, bstr, bbox1,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wp, bdims, bstr, bbox2,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
@@ -630,7 +754,7 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.ntiles) grid = p.ntiles;
-    umma_ct3d_kernel<<<grid, kThreads, pl.smem, a.stream>>>(tmA, tmB, a.bias, a.y, p, status);
+    umma_ct3d_kernel<<<grid, kThreads, pl.smem, a.stream>>>(tmA, tmB1, tmB2, a.bias, a.y, p, status);
     return cudaGetLastError();
 }
 

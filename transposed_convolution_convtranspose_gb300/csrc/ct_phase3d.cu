@@ -236,8 +236,8 @@ __device__ __forceinline__ void compute_stage(const float *buf, float (&acc)[S][
     }
 }
 
-template <int S, int KD, int KH, int KW, int PW, int OCT, int RT, bool ADD>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int S, int KD, int KH, int KW, int PW, int OCT, int RT, bool ADD, int MB>
+__global__ void __launch_bounds__(kThreads, MB)
 phase3d_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restrict__ w,
                const float *__restrict__ bias, const float *add, float *y, P3Params p,
                unsigned int *status)
@@ -366,25 +366,26 @@ phase3d_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restrict_
 // ---- host side --------------------------------------------------------------
 struct Variant3 {
     int S, KD, KH, KW, PW, OCT, RT;
+    int MB;                       // CTAs per SM the variant is built for (registers, shared memory)
     const void *fn_plain, *fn_add;
     int dmin_w, dmax_w;
 };
 
-template <int S, int KD, int KH, int KW, int PW, int OCT, int RT>
+template <int S, int KD, int KH, int KW, int PW, int OCT, int RT, int MB>
 Variant3 V3()
 {
     using W = WDim<S, KW, PW>;
-    return Variant3{S, KD, KH, KW, PW, OCT, RT,
-                    (const void *)&phase3d_kernel<S, KD, KH, KW, PW, OCT, RT, false>,
-                    (const void *)&phase3d_kernel<S, KD, KH, KW, PW, OCT, RT, true>,
+    return Variant3{S, KD, KH, KW, PW, OCT, RT, MB,
+                    (const void *)&phase3d_kernel<S, KD, KH, KW, PW, OCT, RT, false, MB>,
+                    (const void *)&phase3d_kernel<S, KD, KH, KW, PW, OCT, RT, true, MB>,
                     W::dmin(), W::dmax()};
 }
 
 const Variant3 &variant(int i)
 {
     static const Variant3 v[] = {
-        V3<2, 3, 3, 3, 1, 16, 1>(),   // k3 s2 p1 (the fused l2_p26 shape)
-        V3<2, 3, 5, 7, 3, 8, 1>(),    // k(3,5,7) s2 p(.,.,3) (the grouped l1_p72 shape)
+        V3<2, 3, 3, 3, 1, 16, 1, 1>(),   // k3 s2 p1 (the fused l2_p26 shape)
+        V3<2, 3, 5, 7, 3, 8, 1, 2>(),    // k(3,5,7) s2 p(.,.,3) (the grouped l1_p72 shape): 2 CTAs per SM
     };
     return v[i];
 }
@@ -492,7 +493,7 @@ bool make_plan3(const Problem &pb, const Args *a, Plan3 *out)
         const size_t wch = (size_t)c * ndmax * nhmax * v->KW * v->OCT;
         const size_t st = (xfl + wch + 255) & ~(size_t)255;
         const size_t tot = 2 * st * sizeof(float) + 1024;
-        if (tot <= (size_t)kSmemOptin) {
+        if (tot <= (size_t)(kSmemOptin / v->MB - (v->MB > 1 ? 1024 : 0))) {
             icc = c;
             p.xfl = (int)xfl;
             p.stage = (int)st;

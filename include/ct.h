@@ -174,6 +174,16 @@ const char *ct_status_str(ct_status s);
  * kernel ran out since the last query; CT_ERR_CUDA if synchronising failed. */
 ct_status ct_last_device_error(void *stream);
 
+/* Failure-detection self-test: launches on `stream` a one-thread kernel that
+ * waits on an mbarrier nothing arrives at, with a limit of `limit_ns`
+ * nanoseconds (1 .. 1e9), the same bounded wait every pipelined kernel of the
+ * library uses.  The wait runs out, CT_ERR_DEVICE_TIMEOUT is recorded in the
+ * device status word, and the kernel returns normally: the context stays
+ * usable and the next ct_last_device_error() reports the timeout.  No
+ * fault, no hang.  Returns CT_ERR_ARG for a limit out of range, CT_ERR_CUDA
+ * if the launch fails. */
+ct_status ct_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

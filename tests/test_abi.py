@@ -152,3 +152,11 @@ def test_workspace_sizes(lib):
         assert nb >= 16 * 256 * 16 ** 3 * 2 + 8 * 128 * 8 * 256 * 2
     else:
         assert nb == 0
+
+
+def test_selftest_rejects_out_of_range_limits(lib):
+    # argument checks come before anything touches a device
+    for bad in (0, 2_000_000_000):
+        with pytest.raises(ct.CTError) as ei:
+            ct.ct_selftest_wait_timeout(bad)
+        assert ei.value.code == ct.CT_ERR_ARG

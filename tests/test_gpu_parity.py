@@ -329,3 +329,21 @@ def test_fp32_1d_tensor_core_and_ffma_paths(k, mode):
             "integer inputs not exact for %r (%s)" % (TC1D[k], path)
     finally:
         ct.ct_set_path_override(0)
+
+
+def test_bounded_wait_timeout_reports_and_recovers():
+    """A kernel whose bounded mbarrier wait runs out records the timeout in the
+    device status word; the host reads it once, and the context stays usable."""
+    import torch
+    import transposed_convolution_convtranspose_gb300 as ct
+    s = torch.cuda.current_stream()
+    assert ct.ct_last_device_error_code(s) == ct.CT_OK        # clear any earlier state
+    ct.ct_selftest_wait_timeout(1_000_000, s)                  # 1 ms limit, nothing arrives
+    assert ct.ct_last_device_error_code(s) == ct.CT_ERR_DEVICE_TIMEOUT
+    assert ct.ct_last_device_error_code(s) == ct.CT_OK         # read and cleared
+    # the context still runs the tensor-core kernels correctly
+    c = dict(nd=3, G=1, S=[2, 2, 2], DL=[1, 1, 1], bias=True, add=True, dtype="f32", **TC3D[0])
+    t = cc.make_inputs(c, seed=880)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), "f32", "after a reported timeout")
+    assert ct.ct_last_device_error_code(s) == ct.CT_OK

@@ -20,6 +20,8 @@ LIB_PATH = os.path.join(_HERE, "libct.so")
 CT_F32 = 0
 CT_BF16 = 1
 
+CT_OK, CT_ERR_ARG, CT_ERR_SHAPE, CT_ERR_ALIGN = 0, 1, 2, 3
+CT_ERR_WORKSPACE, CT_ERR_UNSUPPORTED, CT_ERR_CUDA, CT_ERR_DEVICE_TIMEOUT = 4, 5, 6, 7
 CT_STATUS = {0: "CT_OK", 1: "CT_ERR_ARG", 2: "CT_ERR_SHAPE", 3: "CT_ERR_ALIGN",
              4: "CT_ERR_WORKSPACE", 5: "CT_ERR_UNSUPPORTED", 6: "CT_ERR_CUDA",
              7: "CT_ERR_DEVICE_TIMEOUT"}
@@ -27,7 +29,7 @@ CT_STATUS = {0: "CT_OK", 1: "CT_ERR_ARG", 2: "CT_ERR_SHAPE", 3: "CT_ERR_ALIGN",
 EXPORTED = ["ct_out_len", "ct_workspace_size_1d", "ct_workspace_size_3d", "ct_forward_1d",
             "ct_forward_3d", "ct_forward_3d_add_hswish", "ct_path_1d", "ct_path_3d",
             "ct_set_path_override", "ct_status_str", "ct_last_device_error",
-            "ct_forward_3d_noalloc"]
+            "ct_forward_3d_noalloc", "ct_selftest_wait_timeout"]
 
 # bytes of the library-owned scratch buffer used by ct_forward_3d_noalloc
 CT_NOALLOC_SCRATCH_BYTES = 48 * 1024 * 1024
@@ -78,6 +80,8 @@ def _setup(lib):
     lib.ct_status_str.argtypes = [_I]
     lib.ct_last_device_error.restype = _I
     lib.ct_last_device_error.argtypes = [_P]
+    lib.ct_selftest_wait_timeout.restype = _I
+    lib.ct_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _P]
     return lib
 
 
@@ -214,6 +218,15 @@ def ct_status_str(code):
 def ct_last_device_error(stream=None):
     code = load().ct_last_device_error(_stream(stream))
     _check(code, "ct_last_device_error")
+
+
+def ct_last_device_error_code(stream=None):
+    """The status code of ct_last_device_error (synchronises, reads and clears)."""
+    return int(load().ct_last_device_error(_stream(stream)))
+
+
+def ct_selftest_wait_timeout(limit_ns, stream=None):
+    _check(load().ct_selftest_wait_timeout(int(limit_ns), _stream(stream)), "ct_selftest_wait_timeout")
 
 
 # ------------------------------------------------------------------ helpers (torch allocation)

@@ -13,29 +13,32 @@
 //   w (C, C_out, kD, kH, kW)   ->  weight panels, K-major (C_in fastest)
 //
 // Tile: 128 output positions q = 16 consecutive qw x 8 consecutive qh of
-// one D plane, for one (rD, rH) phase pair with both W phases side by side
-// along N (2 x C_out TMEM columns).  TMEM row m holds position
+// one D plane, for one (rD, rH) phase pair; its accumulator is two halves of
+// C_out TMEM columns, one per W phase.  TMEM row m holds position
 // (qw, qh) = (m / 8, m mod 8), so each 8-row swizzle group of the A operand
 // is one qw column of 8 consecutive qh -- contiguous in x_t.  When two
 // accumulators fit, a unit of work is a pair of tiles (two neighbouring
 // 8-row qh blocks): they share every input window and weight panel, and
 // each of two MMA-issuing warps computes one of them.
 //
-// Operand A without shifted copies: per (D tap, K block) one TMA box brings
-// the unit's input window, (8 x tiles + H halo) x (16 + W halo) positions x
-// 64 channels, 128-byte swizzled, rows ordered (w, h).  The A operand of
-// input offset (dh, dw) for tile j is that window read from start row
-// (dw - dw_lo) * hspan + (dh - dh_lo) + 8 j with a stride of hspan rows
+// Order within a unit: all of W phase 0, then all of W phase 1.  The TMEM
+// holds no second accumulator to switch to while one is drained, so the
+// halves take turns instead: phase 0's half is drained while phase 1 is
+// computed, and phase 1's half while the next unit's phase 0 is computed.
+//
+// Operand A without shifted copies: per (W phase, D tap, K block) one TMA
+// box brings the unit's input window, (8 x tiles + H halo) x (16 + nT - 1)
+// positions x 64 channels, 128-byte swizzled, rows ordered (w, h).  The A
+// operand of input offset (dh, dw) for tile j is that window read from start
+// row (dw - wlo) * hspan + (dh - dh_lo) + 8 j with a stride of hspan rows
 // between groups: only the shared-memory descriptor's start address and
 // stride-byte-offset change (the 128-byte swizzle is a function of the
 // absolute shared-memory address, so rows read from any start line up with
 // how the TMA wrote them).  Boxes reaching outside the input read zeros,
 // which is the boundary handling.
 //
-// Operand B: for every (phase pair, D tap, H tap, input W offset) one panel
-// with the C_out rows of each W phase whose tap reads that offset (W phase 0
-// first), so that one box brings it and, where both W phases read the
-// offset, one MMA of N = 2 x C_out covers both.
+// Operand B: for every (phase pair, D tap, H tap, W phase, W tap) one panel
+// of C_out rows, K-major, one box each.
 //
 // Roles (persistent CTA, one per SM):
 //   warp 0      TMA producer of the A ring (input windows)
@@ -47,8 +50,7 @@
 //               every stage
 //   warps 7-14  epilogue, two per TMEM lane quarter: with a tile pair, half
 //               j drains tile j; with single tiles the halves take alternate
-//               16-channel chunks.  tcgen05.ld, bias, and each position's even
-//               and odd W outputs written as one float2
+//               16-channel chunks.  tcgen05.ld, bias, 4-byte stores
 // Every ring slot has exactly one producer, which refills it only after
 // waiting for its previous round, so a parity wait never has to tell two
 // phases apart.  Every mbarrier wait is bounded: a timeout records
@@ -70,11 +72,10 @@ constexpr int QWT = 16;      // qw per tile (TMEM row m: qw = m / 8)
 constexpr int MHT = 8;       // qh per tile (one 8-row swizzle group per qw)
 constexpr int BK = 64;       // bf16 elements of K per stage (one 128-byte swizzle row)
 constexpr int UK = 16;       // K of one tcgen05.mma kind::f16
-constexpr int NA = 2;        // A ring slots (input windows of a tile pair)
-constexpr int MAXB = 4;      // B ring slots at most
+constexpr int MAXA = 3;      // A ring slots at most (input windows of a tile pair)
+constexpr int MAXB = 8;      // B ring slots at most
 constexpr int NPB = 4;       // B producer warps at most (slot s loaded by warp s mod npb)
 constexpr int NMMA = 2;      // MMA-issuing warps at most (one per TMEM accumulator)
-constexpr int MAXWE = 5;     // distinct input W offsets of a tile at most (taps per dimension + 1)
 constexpr int EPW = 2;       // epilogue warps per TMEM lane quarter
 constexpr int kAWarp = 0;
 constexpr int kBWarp0 = 1;
@@ -91,24 +92,18 @@ struct UParams {
     int n_kb;                // C_in / BK
     int ntiles;
     int nacc;                // TMEM accumulators = MMA issuers = tiles per pair (1 or 2)
-    int nb, npb;             // B ring slots and B producers (nb a multiple of npb)
-    int b_split;             // 1: a two-phase panel (2 x C_out > 256 rows) comes as two boxes
-    uint32_t acc_cols;       // columns of one accumulator (2 x C_out)
+    int na, nb, npb;         // A ring slots, B ring slots, B producers (nb a multiple of npb)
+    uint32_t acc_cols;       // columns of one accumulator (2 x C_out: W phase 0, then W phase 1)
     uint32_t tmem_cols;      // allocated TMEM columns (power of 2 >= nacc x acc_cols)
-    uint32_t idesc1;         // instruction descriptor, N = C_out
-    uint32_t idesc2;         // instruction descriptor, N = 2 x C_out (0: too wide)
+    uint32_t idesc;          // instruction descriptor, N = C_out
     uint32_t a_slot;         // bytes of an A ring slot (one input window, 1024-aligned)
-    uint32_t b_bytes;        // bytes of one W phase's rows of a panel (C_out x 128)
+    uint32_t b_bytes;        // bytes of one weight panel (C_out rows x 128)
+    int wg;                  // W taps per B stage (nT when nT x C_out rows fit one box, else 1)
     uint32_t sbo;            // A descriptor stride between 8-row groups: hspan x 128
-    int hspan, wspan;        // input window extents (H, W) of a tile pair
-    int dh_lo, dw_lo;        // smallest H / W input offset
+    int hspan, wspan;        // input window extents (H, W) of a tile pair and one W phase
+    int dh_lo;               // smallest H input offset
+    int wlo[2];              // smallest W input offset of each W phase (its window's start)
     int delta[3][2][4];      // input offset of tap j for residue r, per dimension
-    // distinct input W offsets of a tile: offset we_delta[e] is read by tap
-    // we_j[r][e] of W phase r (-1: phase r does not read it)
-    int nwe;
-    int we_delta[MAXWE];
-    int we_j[2][MAXWE];
-    int we_prefix[MAXWE];    // panel rows before entry e within its block, in C_out units
     int blk_units;           // C_out-row units of one (phase pair, D tap, H tap) block
 };
 
@@ -144,27 +139,26 @@ __device__ __forceinline__ uint64_t desc_sw128_sbo(uint32_t saddr, uint32_t sbo)
 
 // ---- GEMM kernel -------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
-umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB1,
-                 const __grid_constant__ CUtensorMap tmB2, const float *__restrict__ bias, float *__restrict__ y,
-                 const __grid_constant__ UParams p, unsigned int *status)
+umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const float *__restrict__ bias, float *__restrict__ y, const __grid_constant__ UParams p,
+                 unsigned int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t a_full[NA], a_empty[NA], b_full[MAXB], b_empty[MAXB], acc_full[2],
-        acc_empty[2], drain_bar[NMMA];
+    __shared__ __align__(8) uint64_t a_full[MAXA], a_empty[MAXA], b_full[MAXB], b_empty[MAXB], acc_full[2][2],
+        acc_empty[2][2], drain_bar[NMMA];
     __shared__ uint32_t tmem_slot;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = smem;                                // NA x a_slot
-    uint8_t *sB = smem + (size_t)NA * p.a_slot;        // nb x 2 x b_bytes
+    uint8_t *sA = smem;                                // na x a_slot
+    uint8_t *sB = smem + (size_t)p.na * p.a_slot;      // nb x (wg x b_bytes)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t b_slot = 2 * p.b_bytes;
 
     if (threadIdx.x == 0) {
         dev::prefetch_tensormap(&tmA);
-        dev::prefetch_tensormap(&tmB1);
-        dev::prefetch_tensormap(&tmB2);
-        // a stage is released by every issuer, an accumulator by the epilogue
-        // threads that read it (all of them with one tile per unit, half with two)
-        for (int s = 0; s < NA; ++s) {
+        dev::prefetch_tensormap(&tmB);
+        // a stage is released by every issuer, an accumulator half by the
+        // epilogue threads that read it (all of them with one tile per unit,
+        // half with two)
+        for (int s = 0; s < p.na; ++s) {
             dev::mbar_init(&a_full[s], 1);
             dev::mbar_init(&a_empty[s], p.nacc);
         }
@@ -172,10 +166,11 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             dev::mbar_init(&b_full[s], 1);
             dev::mbar_init(&b_empty[s], p.nacc);
         }
-        for (int a = 0; a < 2; ++a) {
-            dev::mbar_init(&acc_full[a], 1);
-            dev::mbar_init(&acc_empty[a], 32 * 4 * EPW / p.nacc);
-        }
+        for (int a = 0; a < 2; ++a)
+            for (int r = 0; r < 2; ++r) {
+                dev::mbar_init(&acc_full[a][r], 1);
+                dev::mbar_init(&acc_empty[a][r], 32 * 4 * EPW / p.nacc);
+            }
         for (int j = 0; j < NMMA; ++j) dev::mbar_init(&drain_bar[j], 1);
         dev::fence_mbar_init();
     }
@@ -186,12 +181,15 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const uint32_t tmem = tmem_slot;
     const int ntile_cta =
         p.ntiles > (int)blockIdx.x ? (p.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    // stages per unit: A = (D tap, K block); B = (D tap, K block, H tap, W offset).
+    // stages per unit, W phase 0 first, then W phase 1:
+    //   A = (W phase, D tap, K block), B = (W phase, D tap, K block, H tap, W tap).
     // A unit is a pair of tiles (two 8-row qh blocks) when two accumulators fit:
     // both issuers consume every stage, issuer j computing tile j from the shared
     // input window (8 rows further down for tile 1) and the shared weight panel.
-    const int spa = p.nT * p.n_kb;
-    const int spb = spa * p.nT * p.nwe;
+    const int nT = p.nT, n_kb = p.n_kb;
+    const int spa = 2 * nT * n_kb;
+    const int spb = spa * nT * (nT / p.wg);
+    const uint32_t b_slot = (uint32_t)p.wg * p.b_bytes;
     const int ni = p.nacc;
 
     if (warp == kAWarp || (warp >= kBWarp0 && warp < kBWarp0 + NPB)) {
@@ -200,7 +198,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int q = isA ? 0 : warp - kBWarp0;
         if (lane == 0 && (isA || q < p.npb)) {
             const int np = isA ? 1 : p.npb;
-            const int nst = isA ? NA : p.nb;
+            const int nst = isA ? p.na : p.nb;
             const int sp = isA ? spa : spb;
             uint64_t *fullb = isA ? a_full : b_full;
             uint64_t *emptyb = isA ? a_empty : b_empty;
@@ -221,29 +219,28 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     break;
                 }
                 if (isA) {
-                    const int jd = i / p.n_kb, kb = i % p.n_kb;
+                    const int wr = i / (nT * n_kb), r = i % (nT * n_kb);
+                    const int jd = r / n_kb, kb = r % n_kb;
                     dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(p.hspan * p.wspan) * 128u);
-                    // x_t viewed as (C, H, W, D, N): the window from (qh0 + dh_lo, qw0 + dw_lo)
+                    // x_t viewed as (C, H, W, D, N): W phase wr's window from
+                    // (qh0 + dh_lo, qw0 + wlo[wr])
                     dev::tma_load_5d(sA + (size_t)s * p.a_slot, &tmA, &fullb[s], kb * BK,
-                                     tcd.qhp * ni * MHT + p.dh_lo, tcd.qwb * QWT + p.dw_lo,
+                                     tcd.qhp * ni * MHT + p.dh_lo, tcd.qwb * QWT + p.wlo[wr],
                                      tcd.qd + p.delta[0][tcd.rD][jd], tcd.n);
                 } else {
-                    const int e = i % p.nwe;
-                    int r = i / p.nwe;
-                    const int jh = r % p.nT;
-                    r /= p.nT;
-                    const int kb = r % p.n_kb, jd = r / p.n_kb;
-                    const bool both = p.we_j[0][e] >= 0 && p.we_j[1][e] >= 0;
+                    int r = i;
+                    const int jw = (r % (nT / p.wg)) * p.wg;
+                    r /= nT / p.wg;
+                    const int jh = r % nT;
+                    r /= nT;
+                    const int kb = r % n_kb;
+                    r /= n_kb;
+                    const int jd = r % nT, wr = r / nT;
                     const int ph2 = tcd.rD * 2 + tcd.rH;
-                    const int brow = (((ph2 * p.nT + jd) * p.nT + jh) * p.blk_units + p.we_prefix[e]) * p.C_out;
-                    dev::mbar_arrive_expect_tx(&fullb[s], both ? 2 * p.b_bytes : p.b_bytes);
-                    if (both && p.b_split) {
-                        dev::tma_load_2d(sB + (size_t)s * b_slot, &tmB1, &fullb[s], kb * BK, brow);
-                        dev::tma_load_2d(sB + (size_t)s * b_slot + p.b_bytes, &tmB1, &fullb[s], kb * BK,
-                                         brow + p.C_out);
-                    } else {
-                        dev::tma_load_2d(sB + (size_t)s * b_slot, both ? &tmB2 : &tmB1, &fullb[s], kb * BK, brow);
-                    }
+                    const int brow = (((ph2 * nT + jd) * nT + jh) * p.blk_units + wr * nT + jw) * p.C_out;
+                    // the panels of W taps jw .. jw + wg - 1 are consecutive rows
+                    dev::mbar_arrive_expect_tx(&fullb[s], b_slot);
+                    dev::tma_load_2d(sB + (size_t)s * b_slot, &tmB, &fullb[s], kb * BK, brow);
                 }
                 last = g;
             }
@@ -257,88 +254,76 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     } else if (warp < kMmaWarp0 + NMMA) {
         // ---------------- MMA issuers.  An MMA costs the issuing thread about 100
         // clocks at best, so the loop carries ring slots, parities and indices as
-        // counters and keeps the per-offset data in registers.
+        // counters and keeps the per-offset data in registers.  A tile's
+        // accumulator is two halves of C_out columns, one per W phase; W phase 0
+        // is computed first, so its half is drained while W phase 1 runs, and
+        // phase 1's half while the next unit's phase 0 runs.
         const int j = warp - kMmaWarp0;
         if (lane == 0 && j < ni) {
             bool ok = true;
-            uint32_t m0 = 0, m1 = 0;                    // W offsets read by phase 0 / phase 1
-            for (int e = 0; e < p.nwe; ++e) {
-                if (p.we_j[0][e] >= 0) m0 |= 1u << e;
-                if (p.we_j[1][e] >= 0) m1 |= 1u << e;
-            }
             const uint32_t sAb = dev::smem_u32(sA), sBb = dev::smem_u32(sB);
-            const uint32_t idesc1 = p.idesc1, idesc2 = p.idesc2, a_slot = p.a_slot, b_bytes = p.b_bytes;
+            const uint32_t idesc = p.idesc, a_slot = p.a_slot, b_bytes = p.b_bytes;
+            const int wg = p.wg;
             const uint32_t sbo = p.sbo, c_out = (uint32_t)p.C_out;
-            const int nwe = p.nwe, nT = p.nT, n_kb = p.n_kb, nb = p.nb;
+            const int na = p.na, nb = p.nb;
             const uint32_t trow = (uint32_t)(j * MHT) * 128u;   // tile j's rows in the window
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
             for (int k = 0; k < ntile_cta && ok; ++k) {
                 const TileCoord tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
-                if (k > 0 && !dev::mbar_wait_bounded(&acc_empty[j], (k - 1) & 1, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after();
-                const uint32_t d0 = tmem + (uint32_t)j * p.acc_cols;
-                const uint32_t d1 = d0 + c_out;
-                bool init0 = false, init1 = false;
-                for (int jd = 0; jd < nT && ok; ++jd)
-                    for (int kb = 0; kb < n_kb && ok; ++kb) {
-                        if (!dev::mbar_wait_bounded(&a_full[sa], pa, kWaitLimitNs)) {
-                            ok = false;
-                            break;
-                        }
-                        tc::fence_after();
-                        const uint32_t wbase = sAb + (uint32_t)sa * a_slot;
-                        for (int jh = 0; jh < nT && ok; ++jh) {
-                            const uint32_t hoff = (uint32_t)(p.delta[1][tcd.rH][jh] - p.dh_lo) * 128u;
-                            for (int e = 0; e < nwe; ++e) {
-                                if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc::fence_after();
-                                const bool h0 = (m0 >> e) & 1u, h1 = (m1 >> e) & 1u;
-                                // window column of this W offset: (dw - dw_lo) * hspan rows
-                                const uint32_t aw = (uint32_t)((p.we_delta[e] - p.dw_lo) * p.hspan) * 128u;
-                                const uint64_t da = desc_sw128_sbo(wbase + aw + hoff + trow, sbo);
-                                const uint32_t bb = sBb + (uint32_t)sb * 2u * b_bytes;
-                                const uint64_t db0 = tc::desc_sw128(bb);
-                                const uint64_t db1 = tc::desc_sw128(bb + (h0 ? b_bytes : 0u));
-                                if (h0 && h1 && idesc2 && init0 == init1) {
-                                    // both W phases in one MMA (they hold the same number of terms)
+                for (int wr = 0; wr < 2 && ok; ++wr) {
+                    if (k > 0 && !dev::mbar_wait_bounded(&acc_empty[j][wr], (k - 1) & 1, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t d = tmem + (uint32_t)j * p.acc_cols + (uint32_t)wr * c_out;
+                    // W tap jw reads window column nT - 1 - jw: (nT - 1 - jw) * hspan rows in
+                    const uint32_t awstep = (uint32_t)p.hspan * 128u;
+                    const uint32_t aw0 = (uint32_t)(nT - 1) * awstep;
+                    bool init = false;
+                    for (int jd = 0; jd < nT && ok; ++jd)
+                        for (int kb = 0; kb < n_kb && ok; ++kb) {
+                            if (!dev::mbar_wait_bounded(&a_full[sa], pa, kWaitLimitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            tc::fence_after();
+                            const uint32_t wbase = sAb + (uint32_t)sa * a_slot + trow;
+                            for (int jh = 0; jh < nT && ok; ++jh) {
+                                const uint32_t hoff = (uint32_t)(p.delta[1][tcd.rH][jh] - p.dh_lo) * 128u;
+                                for (int jw0 = 0; jw0 < nT; jw0 += wg) {
+                                    if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    tc::fence_after();
+                                    const uint32_t bslot = sBb + (uint32_t)sb * (uint32_t)wg * b_bytes;
+                                    for (int t = 0; t < wg; ++t) {
+                                        const int jw = jw0 + t;
+                                        const uint64_t da =
+                                            desc_sw128_sbo(wbase + aw0 - (uint32_t)jw * awstep + hoff, sbo);
+                                        const uint64_t db = tc::desc_sw128(bslot + (uint32_t)t * b_bytes);
 #pragma unroll
-                                    for (int kk = 0; kk < BK / UK; ++kk)   // 16 bf16 = 32 bytes along K
-                                        tc::mma_bf16(d0, da + 2 * kk, db0 + 2 * kk, idesc2, (init0 || kk) ? 1u : 0u);
-                                } else {
-                                    if (h0)
-#pragma unroll
-                                        for (int kk = 0; kk < BK / UK; ++kk)
-                                            tc::mma_bf16(d0, da + 2 * kk, db0 + 2 * kk, idesc1,
-                                                         (init0 || kk) ? 1u : 0u);
-                                    if (h1)
-#pragma unroll
-                                        for (int kk = 0; kk < BK / UK; ++kk)
-                                            tc::mma_bf16(d1, da + 2 * kk, db1 + 2 * kk, idesc1,
-                                                         (init1 || kk) ? 1u : 0u);
-                                }
-                                init0 = init0 || h0;
-                                init1 = init1 || h1;
-                                tc::commit(&b_empty[sb]);
-                                if (++sb == nb) {
-                                    sb = 0;
-                                    pb ^= 1u;
+                                        for (int kk = 0; kk < BK / UK; ++kk)   // 16 bf16 = 32 bytes along K
+                                            tc::mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (init || kk) ? 1u : 0u);
+                                        init = true;
+                                    }
+                                    tc::commit(&b_empty[sb]);
+                                    if (++sb == nb) {
+                                        sb = 0;
+                                        pb ^= 1u;
+                                    }
                                 }
                             }
+                            tc::commit(&a_empty[sa]);
+                            if (++sa == na) {
+                                sa = 0;
+                                pa ^= 1u;
+                            }
                         }
-                        tc::commit(&a_empty[sa]);
-                        if (++sa == NA) {
-                            sa = 0;
-                            pa ^= 1u;
-                        }
-                    }
-                if (ok) tc::commit(&acc_full[j]);
+                    if (ok) tc::commit(&acc_full[j][wr]);
+                }
             }
             // every MMA issued has to complete before the TMEM is freed
             tc::commit(&drain_bar[j]);
@@ -350,6 +335,10 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // 4 qw x 8 qh); a warp reaches the lanes of quarter warp mod 4.  With two
         // tiles per unit, half j of the warps drains tile j (accumulator j) and
         // takes every 16-channel chunk; with one, the halves take alternate chunks.
+        // Each W phase half is drained as soon as it is complete: every output is
+        // one 4-byte store, the even and odd W outputs of a position coming from
+        // the two halves about half a unit apart (ordinary stores, so the line
+        // stays in L2 until both halves have been written).
         const int ew = warp & 3;
         const int half = (warp - kEpiWarp0) >> 2;
         const int a = ni == 2 ? half : 0;
@@ -359,56 +348,58 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         bool ok = true;
         for (int k = 0; k < ntile_cta; ++k) {
             const TileCoord tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
-            if (ok && !dev::mbar_wait_bounded(&acc_full[a], k & 1, kWaitLimitNs)) {
-                atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
-                ok = false;
-            }
-            ok = __all_sync(0xffffffffu, ok);        // warp-uniform before .sync.aligned loads
-            tc::fence_after();
             const int m = ew * 32 + lane;
             const int qw = tcd.qwb * QWT + (m >> 3), qh = (tcd.qhp * ni + a) * MHT + (m & 7);
             const int od = 2 * tcd.qd + tcd.rD, oh = 2 * qh + tcd.rH;
             const bool valid = qw < p.QW && od < p.Lo0 && oh < p.Lo1;
-            float *yrow = y + (int64_t)tcd.n * p.C_out * sp + ((int64_t)od * p.Lo1 + oh) * p.Lo2 + 2 * qw;
-            const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols;
-            // two chunks per batch; the accumulator is released as soon as the
-            // warp's last batch is in registers
-            bool released = false;
-            for (int ci = cfirst; ci < nchunk; ci += 2 * cstep) {
-                const bool two = ci + cstep < nchunk;
-                float v0[2][16], v1[2][16];
-                if (ok) {
-                    tc::tmem_ld16(tbase + (uint32_t)(ci * 16), v0[0]);
-                    tc::tmem_ld16(tbase + (uint32_t)(p.C_out + ci * 16), v1[0]);
-                    if (two) {
-                        tc::tmem_ld16(tbase + (uint32_t)((ci + cstep) * 16), v0[1]);
-                        tc::tmem_ld16(tbase + (uint32_t)(p.C_out + (ci + cstep) * 16), v1[1]);
+            for (int wr = 0; wr < 2; ++wr) {
+                if (ok && !dev::mbar_wait_bounded(&acc_full[a][wr], k & 1, kWaitLimitNs)) {
+                    atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
+                    ok = false;
+                }
+                ok = __all_sync(0xffffffffu, ok);    // warp-uniform before .sync.aligned loads
+                tc::fence_after();
+                float *yrow = y + (int64_t)tcd.n * p.C_out * sp + ((int64_t)od * p.Lo1 + oh) * p.Lo2 + 2 * qw + wr;
+                const uint32_t tbase =
+                    tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols + (uint32_t)wr * p.C_out;
+                // four chunks per batch; the half is released as soon as the
+                // warp's last batch is in registers
+                bool released = false;
+                for (int ci = cfirst; ci < nchunk; ci += 4 * cstep) {
+                    float v[4][16];
+                    int nc = 0;
+                    if (ok) {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            if (ci + b * cstep < nchunk) {
+                                tc::tmem_ld16(tbase + (uint32_t)((ci + b * cstep) * 16), v[b]);
+                                nc = b + 1;
+                            }
+                        tc::tmem_wait_ld();
                     }
-                    tc::tmem_wait_ld();
-                }
-                if (ci + 2 * cstep >= nchunk) {
-                    tc::fence_before();
-                    dev::mbar_arrive(&acc_empty[a]);
-                    released = true;
-                }
-                if (ok && valid) {
+                    if (ci + 4 * cstep >= nchunk) {
+                        tc::fence_before();
+                        dev::mbar_arrive(&acc_empty[a][wr]);
+                        released = true;
+                    }
+                    if (ok && valid) {
 #pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        if (b == 1 && !two) break;
-                        const int c0 = (ci + b * cstep) * 16;
+                        for (int b = 0; b < 4; ++b) {
+                            if (b >= nc) break;
+                            const int c0 = (ci + b * cstep) * 16;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int oc = c0 + i;
-                            const float bb = bias ? __ldg(bias + oc) : 0.f;
-                            __stcs(reinterpret_cast<float2 *>(yrow + (int64_t)oc * sp),
-                                   make_float2(v0[b][i] + bb, v1[b][i] + bb));
+                            for (int i = 0; i < 16; ++i) {
+                                const int oc = c0 + i;
+                                const float bb = bias ? __ldg(bias + oc) : 0.f;
+                                yrow[(int64_t)oc * sp] = v[b][i] + bb;
+                            }
                         }
                     }
                 }
-            }
-            if (!released) {                          // a warp without chunks (C_out < 32)
-                tc::fence_before();
-                dev::mbar_arrive(&acc_empty[a]);
+                if (!released) {                      // a warp without chunks (C_out < 32)
+                    tc::fence_before();
+                    dev::mbar_arrive(&acc_empty[a][wr]);
+                }
             }
         }
     }
@@ -506,15 +497,11 @@ struct WPackParams {
     int C_in, C_out, K0, K1, K2, nT;
     int r_of[3][8];          // residue and tap index that kernel index k belongs to
     int j_of[3][8];
-    int e_of[2][4];          // W offset entry read by tap j of W phase r
-    int half_of[2][4];       // 1 if that phase's rows follow W phase 0's rows in the panel
-    int we_prefix[MAXWE];
     int blk_units;
 };
 
 // w (C_in, C_out, K0, K1, K2) -> weight panels: for every (phase pair, D tap,
-// H tap, W offset entry), the C_out rows of each W phase reading that offset
-// (phase 0 first), C_in fastest.  Every kernel index (kd, kh, kw) belongs to
+// H tap), the C_out rows of each (W phase, W tap), C_in fastest.  Every kernel index (kd, kh, kw) belongs to
 // exactly one (phase, tap), so each (ic, oc) row of kD*kH*kW weights is
 // scattered once.  Block = (64 input channels, one oc); columns = kernel
 // indices in chunks of 64 (kD*kH*kW is a multiple of 8: even extents).
@@ -540,9 +527,8 @@ repack_w_kernel(const bf16_t *__restrict__ w, bf16_t *__restrict__ wp, WPackPara
                 const int kw = k % q.K2, kh = (k / q.K2) % q.K1, kd = k / (q.K1 * q.K2);
                 const int ph2 = (q.r_of[0][kd] << 1) | q.r_of[1][kh];
                 const int rw = q.r_of[2][kw], jw = q.j_of[2][kw];
-                const int e = q.e_of[rw][jw];
                 const int unit = ((ph2 * q.nT + q.j_of[0][kd]) * q.nT + q.j_of[1][kh]) * q.blk_units +
-                                 q.we_prefix[e] + q.half_of[rw][jw];
+                                 rw * q.nT + jw;
                 const uint4 v = make_uint4(tile[row][4 * qq], tile[row][4 * qq + 1],
                                            tile[row][4 * qq + 2], tile[row][4 * qq + 3]);
                 *reinterpret_cast<uint4 *>(wp + ((int64_t)unit * q.C_out + oc) * q.C_in + ic0 + 8 * qq) = v;
@@ -601,78 +587,52 @@ bool make_uplan(const Problem &pb, UPlan *out)
             }
         }
     }
-    // input windows: H and W offsets span [lo, hi]
-    int lo[3], hi[3];
-    for (int d = 1; d < 3; ++d) {
-        lo[d] = hi[d] = p.delta[d][0][0];
-        for (int r = 0; r < 2; ++r)
-            for (int j = 0; j < p.nT; ++j) {
-                lo[d] = p.delta[d][r][j] < lo[d] ? p.delta[d][r][j] : lo[d];
-                hi[d] = p.delta[d][r][j] > hi[d] ? p.delta[d][r][j] : hi[d];
-            }
-    }
-    p.dh_lo = lo[1];
-    p.dw_lo = lo[2];
-    p.hspan = p.nacc * MHT + hi[1] - lo[1];
-    p.wspan = QWT + hi[2] - lo[2];
+    // input windows: H offsets span [lo, hi] for both H phases; each W phase
+    // reads nT consecutive W offsets, its window starting at the lowest
+    int lo = p.delta[1][0][0], hi = lo;
+    for (int r = 0; r < 2; ++r)
+        for (int j = 0; j < p.nT; ++j) {
+            lo = p.delta[1][r][j] < lo ? p.delta[1][r][j] : lo;
+            hi = p.delta[1][r][j] > hi ? p.delta[1][r][j] : hi;
+        }
+    p.dh_lo = lo;
+    p.hspan = p.nacc * MHT + hi - lo;
+    p.wspan = QWT + p.nT - 1;
     if (p.hspan > 256 || p.wspan > 256) return false;
+    // W tap j of a phase reads offset wlo + nT - 1 - j: window column nT - 1 - j
+    for (int r = 0; r < 2; ++r) p.wlo[r] = p.delta[2][r][p.nT - 1];
     p.sbo = (uint32_t)p.hspan * 128u;
     p.a_slot = (uint32_t)((p.hspan * p.wspan * 128 + 1023) & ~1023);
-    // distinct input W offsets: the two W residues' offsets differ by 0 or 1, so
-    // there are at most nT + 1; offsets both phases read come first, so the first
-    // MMA of a tile initialises both halves of the accumulator at once
-    for (int pass = 0; pass < 3; ++pass)
-        for (int dv = lo[2]; dv <= hi[2]; ++dv) {
-            int jr[2] = {-1, -1};
-            for (int r = 0; r < 2; ++r)
-                for (int j = 0; j < p.nT; ++j)
-                    if (p.delta[2][r][j] == dv) jr[r] = j;
-            const int cat = (jr[0] >= 0 && jr[1] >= 0) ? 0 : (jr[0] >= 0 ? 1 : (jr[1] >= 0 ? 2 : 3));
-            if (cat != pass) continue;
-            if (p.nwe >= MAXWE) return false;
-            p.we_delta[p.nwe] = dv;
-            p.we_j[0][p.nwe] = jr[0];
-            p.we_j[1][p.nwe] = jr[1];
-            ++p.nwe;
-        }
-    // panel rows of each entry within a (phase pair, D tap, H tap) block
-    int units = 0;
-    for (int e = 0; e < p.nwe; ++e) {
-        p.we_prefix[e] = units;
-        wq.we_prefix[e] = units;
-        for (int r = 0; r < 2; ++r) {
-            const int jj = p.we_j[r][e];
-            if (jj < 0) continue;
-            wq.e_of[r][jj] = e;
-            wq.half_of[r][jj] = (r == 1 && p.we_j[0][e] >= 0) ? 1 : 0;
-            ++units;
-        }
-    }
-    if (units != 2 * p.nT) return false;        // every (W phase, tap) in exactly one panel
-    p.blk_units = units;
-    wq.blk_units = units;
+    // panels: per (phase pair, D tap, H tap) block, the C_out rows of each
+    // (W phase, W tap)
+    p.blk_units = 2 * p.nT;
+    wq.blk_units = p.blk_units;
     wq.C_in = pb.C_in; wq.C_out = pb.C_out; wq.nT = p.nT;
     wq.K0 = pb.K[0]; wq.K1 = pb.K[1]; wq.K2 = pb.K[2];
-    p.idesc1 = tc::idesc(1, pb.C_out, BM);
-    p.idesc2 = 2 * pb.C_out <= 256 ? tc::idesc(1, 2 * pb.C_out, BM) : 0u;
+    p.idesc = tc::idesc(1, pb.C_out, BM);
     p.acc_cols = (uint32_t)(2 * pb.C_out);
     uint32_t cols = 32;
     while (cols < (uint32_t)p.nacc * p.acc_cols) cols <<= 1;
     p.tmem_cols = cols;
     p.b_bytes = (uint32_t)pb.C_out * BK * 2;
-    p.b_split = 2 * pb.C_out > 256 ? 1 : 0;
-    // deepest B ring that fits (room left for the static barriers); one producer
-    // per slot
+    p.wg = p.nT * pb.C_out <= 256 ? p.nT : 1;
+    const size_t b_slot = (size_t)p.wg * p.b_bytes;
+    // three A slots when at least four B slots still fit, else two; the deepest
+    // B ring that fits (room left for the static barriers), one producer per slot
     const size_t budget = 227 * 1024 - 2048;
-    const size_t a_area = (size_t)NA * p.a_slot;
+    p.na = MAXA;
+    while (p.na > 2 && (size_t)p.na * p.a_slot + 4 * b_slot > budget) --p.na;
+    const size_t a_area = (size_t)p.na * p.a_slot;
     if (budget < a_area) return false;
-    int nb = (int)((budget - a_area) / (2 * p.b_bytes));
+    int nb = (int)((budget - a_area) / b_slot);
     if (nb > MAXB) nb = MAXB;
     if (nb < 2) return false;
+    if (nb >= 8) { nb = 8; p.npb = 4; }
+    else if (nb >= 6) { nb = 6; p.npb = 3; }
+    else if (nb >= 4) { nb = 4; p.npb = 4; }
+    else p.npb = nb;
     p.nb = nb;
-    p.npb = nb < NPB ? nb : NPB;
-    while (p.nb % p.npb) --p.npb;
-    const size_t smem = a_area + (size_t)nb * 2 * p.b_bytes + 1024;
+    const size_t smem = a_area + (size_t)nb * b_slot + 1024;
     out->p = p;
     out->wq = wq;
     out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * 2);
@@ -687,7 +647,7 @@ bool umma_supported(const Problem &pb, const Args *a)
 {
     UPlan pl;
     if (!make_uplan(pb, &pl)) return false;
-    if (a && (((uintptr_t)a->y % 8) || ((uintptr_t)a->x % 16) || ((uintptr_t)a->w % 16))) return false;
+    if (a && (((uintptr_t)a->y % 4) || ((uintptr_t)a->x % 16) || ((uintptr_t)a->w % 16))) return false;
     return true;
 }
 
@@ -725,8 +685,8 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     if (e != cudaSuccess) return e;
 
     // 3) tensor maps: A over x_t viewed as (C, H, W, D, N), one input window per
-    // box; B over the panels (K = C_in, rows), boxes of C_out and 2 x C_out rows
-    CUtensorMap tmA, tmB1, tmB2;
+    // box; B over the panels (K = C_in, rows), boxes of wg x C_out rows
+    CUtensorMap tmA, tmB;
     const uint64_t adims[5] = {(uint64_t)pb.C_in, (uint64_t)pb.Li[1], (uint64_t)pb.Li[2], (uint64_t)pb.Li[0],
                                (uint64_t)pb.N};
     const uint64_t astr[4] = {(uint64_t)pb.C_in * 2, (uint64_t)pb.C_in * pb.Li[1] * 2,
@@ -738,11 +698,8 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
         return cudaErrorInvalidValue;
     const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)8 * p.nT * p.nT * p.nT * pb.C_out};
     const uint64_t bstr[1] = {(uint64_t)pb.C_in * 2};
-    const uint32_t bbox1[2] = {(uint32_t)BK, (uint32_t)pb.C_out};
-    const uint32_t bbox2[2] = {(uint32_t)BK, (uint32_t)(2 * pb.C_out <= 256 ? 2 * pb.C_out : pb.C_out)};
-    if (!encode_tiled(&tmB1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wp, bdims, bstr, bbox1,
-                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wp, bdims, bstr, bbox2,
+    const uint32_t bbox[2] = {(uint32_t)BK, (uint32_t)(p.wg * pb.C_out)};
+    if (!encode_tiled(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wp, bdims, bstr, bbox,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
@@ -754,7 +711,7 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.ntiles) grid = p.ntiles;
-    umma_ct3d_kernel<<<grid, kThreads, pl.smem, a.stream>>>(tmA, tmB1, tmB2, a.bias, a.y, p, status);
+    umma_ct3d_kernel<<<grid, kThreads, pl.smem, a.stream>>>(tmA, tmB, a.bias, a.y, p, status);
     return cudaGetLastError();
 }
 

@@ -259,7 +259,7 @@ class Runner:
         self.ws = (torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
                    if self.ws_bytes else None)
         # kernels the library launches per forward pass on this path
-        self.launches_per_step = {"umma_bf16": 3, "tc3d_tf32x3": 3}.get(self.path, 1)
+        self.launches_per_step = {"umma_bf16": 3, "tc3d_tf32x3": 3, "tc3dg_tf32x3": 3}.get(self.path, 1)
 
     def forward(self, stream):
         c, d, ct = self.cfg, self.d, self.ct
@@ -379,7 +379,7 @@ def roofline(name, cfg, path, wm, sec, peaks):
         return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peaks["source"] + " cuBLAS bf16 burst"}
-    if path in ("tc1d_tf32x3", "tc3d_tf32x3"):
+    if path in ("tc1d_tf32x3", "tc3d_tf32x3", "tc3dg_tf32x3"):
         # FP32 on the tensor cores: 3 tf32 products per multiply-add at the tf32
         # rate (half the bf16 rate).  The roofline is the slower of that tensor
         # time and the HBM time of the algorithmic bytes.

@@ -113,9 +113,15 @@ def test_path_selection(lib):
     finally:
         ct.ct_set_path_override(0)
     assert ct.ct_path_1d(1, 4, 8, 0, 3, 1, 2, 1, 0, 2, ct.CT_F32) is None
-    p3 = ct.ct_path_3d(8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3), (1, 1, 1),
-                       (1, 1, 1), ct.CT_F32)
-    assert p3 in ("phase3d_f32", "gather_generic")
+    # the grouped workload: the grouped FP32 tensor-core path, the FFMA kernel
+    # under override 2
+    grouped = (8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3), (1, 1, 1), (1, 1, 1), ct.CT_F32)
+    assert ct.ct_path_3d(*grouped) == "tc3dg_tf32x3"
+    ct.ct_set_path_override(2)
+    try:
+        assert ct.ct_path_3d(*grouped) == "phase3d_f32"
+    finally:
+        ct.ct_set_path_override(0)
     ct.ct_set_path_override(1)
     try:
         assert ct.ct_path_3d(8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3),
@@ -140,9 +146,11 @@ def test_workspace_sizes(lib):
     nf = ct.ct_workspace_size_3d(128, 32, 64, (16, 16, 16), (3, 3, 3), 1, (2, 2, 2), (1, 1, 1),
                                  (1, 1, 1), (1, 1, 1), ct.CT_F32)
     assert nf >= 2 * 128 * 32 * 16 ** 3 * 4 + 2 * 27 * 64 * 32 * 4
-    # the grouped workload has no tensor-core path: no workspace
-    assert ct.ct_workspace_size_3d(8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3),
-                                   (1, 1, 1), (1, 1, 1), ct.CT_F32) == 0
+    # the grouped workload: (N, D, W, H, 32) hi and lo copies of x and one
+    # hi + lo panel per input offset (24 offsets, 1920 rows of 32 floats)
+    ng = ct.ct_workspace_size_3d(8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3),
+                                 (1, 1, 1), (1, 1, 1), ct.CT_F32)
+    assert ng >= 2 * 8 * 32 * 16 * 32 * 32 * 4 + 1920 * 32 * 4
     nb = ct.ct_workspace_size_3d(16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1),
                                  (0, 0, 0), (1, 1, 1), ct.CT_BF16)
     path = ct.ct_path_3d(16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1),

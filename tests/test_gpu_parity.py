@@ -205,6 +205,38 @@ def test_fp32_3d_tensor_core_shapes(k, add):
     cc.assert_close(y, cc.run_oracle(c, t), "f32", "tc3d case %d add=%s %r" % (k, add, c))
 
 
+# Shapes for the FP32 3-D tensor-core path of 32 input channels in groups
+# (one MMA-issuing warp per group, K steps of the shared 128-byte rows):
+# 4 groups of 8 with the asymmetric (3, 5, 7) kernel and ragged qw / qh
+# blocks, 2 groups of 16 with even kernels, one group with kernels beyond the
+# dense path's range or 8 output channels, a kernel of extent 1 along D (odd
+# residues receive no tap: bias only), and a case with several units per
+# persistent CTA (both accumulator sets, ring wrap-around).
+TC3DG = [
+    dict(N=1, C_in=32, C_out=32, G=4, L=[3, 5, 8], K=[3, 5, 7], P=[1, 2, 3], OP=[1, 1, 1]),
+    dict(N=2, C_in=32, C_out=32, G=2, L=[2, 4, 8], K=[2, 4, 6], P=[0, 1, 2], OP=[0, 1, 0]),
+    dict(N=1, C_in=32, C_out=16, G=1, L=[2, 3, 4], K=[5, 5, 5], P=[2, 2, 2], OP=[1, 1, 1]),
+    dict(N=1, C_in=32, C_out=8, G=1, L=[3, 3, 4], K=[3, 3, 3], P=[1, 1, 1], OP=[1, 1, 1]),
+    dict(N=1, C_in=32, C_out=32, G=4, L=[3, 4, 6], K=[1, 3, 5], P=[0, 1, 2], OP=[0, 0, 1]),
+    dict(N=8, C_in=32, C_out=32, G=4, L=[16, 16, 16], K=[3, 5, 7], P=[1, 2, 3], OP=[1, 1, 1]),
+]
+
+
+@pytest.mark.parametrize("k", range(len(TC3DG)))
+def test_fp32_3d_grouped_tensor_core_shapes(k):
+    c = dict(nd=3, S=[2, 2, 2], DL=[1, 1, 1], bias=bool(k % 2 == 0), add=False, dtype="f32", **TC3DG[k])
+    assert path_of(c) == "tc3dg_tf32x3", (c, path_of(c))
+    t = cc.make_inputs(c, seed=900 + k)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), "f32", "tc3dg case %d %r" % (k, c))
+    if k < 3:
+        # small integers are exact in the tf32 part, so the split and the fp32
+        # accumulation reproduce the oracle bit for bit
+        ti = cc.make_inputs(c, seed=950 + k, int_range=3)
+        yi = cc.run_gpu(c, ti).cpu().numpy()
+        assert np.array_equal(yi.astype(np.float64), cc.run_oracle(c, ti)), "tc3dg integer case %d" % k
+
+
 def test_fp32_3d_without_workspace_takes_ffma():
     """A call given no workspace runs the FFMA kernel, with the same result."""
     import torch

@@ -96,7 +96,7 @@ ct_status make_problem(int nd, int N, int C_in, int C_out, const int *Li, const 
     return CT_OK;
 }
 
-enum class Path { Generic, Phase1d, Phase3d, Umma, Tc1d, Tc3d };
+enum class Path { Generic, Phase1d, Phase3d, Umma, Tc1d, Tc3d, Tc3dg };
 
 Path choose_path(const Problem &pb, const Args *a)
 {
@@ -111,6 +111,9 @@ Path choose_path(const Problem &pb, const Args *a)
         if (ov != 2 && pb.nd == 3 && tc3d_supported(pb, a) &&
             (!a || (a->ws && ((uintptr_t)a->ws % 256) == 0 && a->ws_bytes >= tc3d_workspace_bytes(pb))))
             return Path::Tc3d;
+        if (ov != 2 && pb.nd == 3 && tc3dg_supported(pb, a) &&
+            (!a || (a->ws && ((uintptr_t)a->ws % 256) == 0 && a->ws_bytes >= tc3dg_workspace_bytes(pb))))
+            return Path::Tc3dg;
         if (pb.nd == 3 && phase3d_supported(pb, a)) return Path::Phase3d;
     } else {
         if (pb.nd == 3 && umma_supported(pb, a)) return Path::Umma;
@@ -127,6 +130,7 @@ const char *path_name(Path p)
     case Path::Umma: return "umma_bf16";
     case Path::Tc1d: return "tc1d_tf32x3";
     case Path::Tc3d: return "tc3d_tf32x3";
+    case Path::Tc3dg: return "tc3dg_tf32x3";
     }
     return "gather_generic";
 }
@@ -139,6 +143,7 @@ size_t workspace_bytes(const Problem &pb)
     switch (choose_path(pb, nullptr)) {
     case Path::Umma: return umma_workspace_bytes(pb);
     case Path::Tc3d: return tc3d_workspace_bytes(pb);
+    case Path::Tc3dg: return tc3dg_workspace_bytes(pb);
     default: return 0;
     }
 }
@@ -179,6 +184,7 @@ ct_status run(const Problem &pb, Args a)
     case Path::Umma: e = launch_umma(pb, a); break;
     case Path::Tc1d: e = launch_tc1d(pb, a); break;
     case Path::Tc3d: e = launch_tc3d(pb, a); break;
+    case Path::Tc3dg: e = launch_tc3dg(pb, a); break;
     }
     return e == cudaSuccess ? CT_OK : CT_ERR_CUDA;
 }

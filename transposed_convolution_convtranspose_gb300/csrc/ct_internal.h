@@ -74,6 +74,12 @@ bool tc3d_supported(const Problem &pb, const Args *a);
 size_t tc3d_workspace_bytes(const Problem &pb);
 cudaError_t launch_tc3d(const Problem &pb, const Args &a);
 
+// ---- FP32 3-D, 32 input channels in 1/2/4 groups, on the tensor cores
+// (3-term tf32 split, one MMA-issuing warp per group; workspace) ----
+bool tc3dg_supported(const Problem &pb, const Args *a);
+size_t tc3dg_workspace_bytes(const Problem &pb);
+cudaError_t launch_tc3dg(const Problem &pb, const Args &a);
+
 // ---- phase-decomposed FP32 1-D kernel ----
 bool phase1d_supported(const Problem &pb, const Args *a);
 cudaError_t launch_phase1d(const Problem &pb, const Args &a);

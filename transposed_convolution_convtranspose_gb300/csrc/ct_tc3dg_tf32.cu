@@ -178,14 +178,13 @@ __device__ __forceinline__ uint64_t desc_sbo(uint32_t saddr, uint32_t sbo)
 // tile of pitch 33); a thread then writes 4 channels of one position: a
 // 16-byte store of the tf32 parts and two 8-byte stores of the bf16 hi and lo.
 // D*H*W is a multiple of 4.
-__global__ void __launch_bounds__(256)
-prepg_x_kernel(const float *__restrict__ x, float *__restrict__ xhi, uint16_t *__restrict__ xc, int D, int H,
-               int W, int Cig)
+__device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, float *__restrict__ xhi,
+                                              uint16_t *__restrict__ xc, int D, int H, int W, int Cig, int bx,
+                                              int n)
 {
     __shared__ float tile[64][33];
     const int64_t SP = (int64_t)D * H * W;
-    const int n = blockIdx.z;
-    const int64_t s0 = (int64_t)blockIdx.x * 64;
+    const int64_t s0 = (int64_t)bx * 64;
     const int ncols = (int)((SP - s0) < 64 ? (SP - s0) : 64);
     const float *xs = x + (int64_t)n * CK * SP + s0;
 #pragma unroll
@@ -234,13 +233,14 @@ prepg_x_kernel(const float *__restrict__ x, float *__restrict__ xhi, uint16_t *_
 // floats per row, the weights rounded to tf32.  Part 1: 64 bf16 per row, per
 // group [lo of its Cig channels | hi of them] (hi = the tf32 rounding, lo =
 // the remainder), the partner of the [hi | lo] order of x_c.
-__global__ void __launch_bounds__(256)
-prepg_w_kernel(const float *__restrict__ w, uint8_t *__restrict__ wp, GPanels q)
+constexpr int kWSlices = 8;      // blocks per (entry, part) of the panel prep
+
+__device__ __forceinline__ void prepg_w_block(const float *__restrict__ w, uint8_t *__restrict__ wp,
+                                              const GPanels &q, int e, int hl, int z)
 {
-    const int e = blockIdx.x, hl = blockIdx.y;
     const int R = q.enq[e] * 2 * q.Cog;
     const int ncol = hl ? 2 * CK : CK;
-    for (int idx = threadIdx.x + blockIdx.z * blockDim.x; idx < R * ncol; idx += blockDim.x * gridDim.z) {
+    for (int idx = threadIdx.x + z * blockDim.x; idx < R * ncol; idx += blockDim.x * kWSlices) {
         const int rr = idx / ncol, k = idx % ncol;
         const int i = rr / (2 * q.Cog);
         const int rW = (rr / q.Cog) & 1, oc_l = rr % q.Cog;
@@ -265,6 +265,25 @@ prepg_w_kernel(const float *__restrict__ w, uint8_t *__restrict__ wp, GPanels q)
             reinterpret_cast<uint16_t *>(row)[k] = (uint16_t)bf16_bits(want_lo ? v - hv : hv);
         else
             reinterpret_cast<float *>(row)[k] = hv;
+    }
+}
+
+// Both preps in one launch: blocks [0, nxb) move x (nbx per image), the rest
+// build the panels (kWSlices per (entry, part)).  The GEMM kernel is launched
+// as its programmatic dependent, so its CTAs may be scheduled while this
+// kernel drains.
+__global__ void __launch_bounds__(256)
+prepg_kernel(const float *__restrict__ x, float *__restrict__ xhi, uint16_t *__restrict__ xc, int D, int H, int W,
+             int Cig, int nbx, int nxb, const float *__restrict__ w, uint8_t *__restrict__ wp,
+             const __grid_constant__ GPanels q)
+{
+    dev::griddep_launch_dependents();
+    const int b = (int)blockIdx.x;
+    if (b < nxb) {
+        prepg_x_block(x, xhi, xc, D, H, W, Cig, b % nbx, b / nbx);
+    } else {
+        const int r = b - nxb;
+        prepg_w_block(w, wp, q, r / (2 * kWSlices), (r / kWSlices) & 1, r % kWSlices);
     }
 }
 
@@ -346,6 +365,8 @@ tc3dg_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constan
     const uint32_t tmem = tmem_slot;
     const int nunit_cta =
         p.nunits > (int)blockIdx.x ? (p.nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    // the operands in the workspace come from the prep kernel
+    dev::griddep_wait();
 
     if (warp == kAWarp || (warp >= kBWarp0 && warp < kBWarp0 + NPB)) {
         // ---------------- TMA producers
@@ -735,17 +756,18 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
     uint16_t *xc = reinterpret_cast<uint16_t *>(ws + pl.x_bytes);
     uint8_t *wp = ws + 2 * pl.x_bytes;
 
-    // 1) x -> (N, D, W, H, 32) tf32 parts and (N, D, W, H, 64) bf16 [hi | lo]
+    // 1) one launch: x -> (N, D, W, H, 32) tf32 parts and (N, D, W, H, 64) bf16
+    // [hi | lo]; weights -> one panel per input offset (tf32 rows, then bf16
+    // correction rows)
     const int64_t SP = pb.in_sp();
-    dim3 gx((unsigned)((SP + 63) / 64), 1u, (unsigned)pb.N);
-    if (gx.x > 0x7fffffffu || gx.z > 65535) return cudaErrorInvalidConfiguration;
-    prepg_x_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const float *>(a.x), xhi, xc, pb.Li[0], pb.Li[1],
-                                             pb.Li[2], pb.Cig);
+    const int64_t nbx = (SP + 63) / 64;
+    const int64_t nxb = nbx * pb.N;
+    const int64_t nblocks = nxb + (int64_t)p.ne * 2 * kWSlices;
+    if (nblocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    prepg_kernel<<<(unsigned)nblocks, 256, 0, a.stream>>>(static_cast<const float *>(a.x), xhi, xc, pb.Li[0],
+                                                         pb.Li[1], pb.Li[2], pb.Cig, (int)nbx, (int)nxb,
+                                                         static_cast<const float *>(a.w), wp, pl.wq);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // 2) weights -> one panel per input offset: tf32 rows, then bf16 correction rows
-    prepg_w_kernel<<<dim3((unsigned)p.ne, 2u, 8u), 256, 0, a.stream>>>(static_cast<const float *>(a.w), wp, pl.wq);
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     // 3) tensor maps: A over x_t (fp32) and x_c (bf16) viewed as (C, H, W, D, N),
@@ -781,9 +803,8 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.nunits) grid = p.nunits;
-    tc3dg_tf32_kernel<<<grid, kThreads, pl.smem, a.stream>>>(tmXh, tmXc, tmW[0], tmW[1], a.bias,
-                                                           a.y, p, status);
-    return cudaGetLastError();
+    return launch_dependent(tc3dg_tf32_kernel, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXh, tmXc,
+                            tmW[0], tmW[1], a.bias, a.y, p, status);
 }
 
 }  // namespace ct

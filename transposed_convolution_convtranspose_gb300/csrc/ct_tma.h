@@ -23,11 +23,41 @@ int sm_count();
 // and the resulting blocks per SM (cached).
 cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *blocks_per_sm);
 
+// Launch `kernel` on `stream` as a programmatic dependent of the kernel
+// launched on the stream just before it: its CTAs may start (and run their
+// prologue) while that kernel drains; they must execute dev::griddep_wait()
+// before touching anything it writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args &&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 }  // namespace ct
 
 #ifdef __CUDACC__
 namespace ct {
 namespace dev {
+
+// Wait until the kernel this one depends on (launch_dependent) has completed
+// and its writes are visible; a no-op for an ordinary launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Let the dependent kernel's CTAs be scheduled before this kernel completes.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

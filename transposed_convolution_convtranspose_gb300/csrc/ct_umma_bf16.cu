@@ -178,6 +178,8 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    // the operands in the workspace come from the repack kernel(s)
+    dev::griddep_wait();
     const uint32_t tmem = tmem_slot;
     const int ntile_cta =
         p.ntiles > (int)blockIdx.x ? (p.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -442,14 +444,14 @@ __device__ __forceinline__ void repack_load_pairs(const bf16_t *__restrict__ src
 }
 
 // x (N, C, D, H, W) -> x_t (N, D, W, H, C); D*H*W a multiple of 8, C of 64.
-__global__ void __launch_bounds__(256)
-repack_x_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, int C, int D, int H, int W)
+// Block (bx, by, n): positions bx*64.., channels by*64...
+__device__ __forceinline__ void repack_x_block(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, int C, int D,
+                                               int H, int W, int bx, int by, int n)
 {
     __shared__ uint32_t tile[RB][33];
     const int64_t SP = (int64_t)D * H * W;
-    const int n = blockIdx.z;
-    const int c0 = blockIdx.y * RB;
-    const int64_t s0 = (int64_t)blockIdx.x * RB;
+    const int c0 = by * RB;
+    const int64_t s0 = (int64_t)bx * RB;
     const int ncols = (int)((SP - s0) < RB ? (SP - s0) : RB);
     repack_load_pairs(x + ((int64_t)n * C + c0) * SP + s0, SP, ncols, tile);
     __syncthreads();
@@ -505,12 +507,11 @@ struct WPackParams {
 // exactly one (phase, tap), so each (ic, oc) row of kD*kH*kW weights is
 // scattered once.  Block = (64 input channels, one oc); columns = kernel
 // indices in chunks of 64 (kD*kH*kW is a multiple of 8: even extents).
-__global__ void __launch_bounds__(256)
-repack_w_kernel(const bf16_t *__restrict__ w, bf16_t *__restrict__ wp, WPackParams q)
+__device__ __forceinline__ void repack_w_block(const bf16_t *__restrict__ w, bf16_t *__restrict__ wp,
+                                               const WPackParams &q, int bx, int oc)
 {
     __shared__ uint32_t tile[RB][33];
-    const int ic0 = blockIdx.x * RB;
-    const int oc = blockIdx.y;
+    const int ic0 = bx * RB;
     const int kvol = q.K0 * q.K1 * q.K2;
     const int64_t row_stride = (int64_t)q.C_out * kvol;
     for (int kc = 0; kc < kvol; kc += RB) {
@@ -535,6 +536,31 @@ repack_w_kernel(const bf16_t *__restrict__ w, bf16_t *__restrict__ wp, WPackPara
             }
         }
     }
+}
+
+// Both repacks in one launch: blocks [0, nxb) move x (nbx x nby per image),
+// the rest the weights (C_in / 64 per output channel).  The GEMM kernel is
+// launched as its programmatic dependent.
+__global__ void __launch_bounds__(256)
+repack_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, int C, int D, int H, int W, int nbx, int nby,
+              int nxb, const bf16_t *__restrict__ w, bf16_t *__restrict__ wp, const __grid_constant__ WPackParams q)
+{
+    dev::griddep_launch_dependents();
+    const int b = (int)blockIdx.x;
+    if (b < nxb) {
+        const int per = nbx * nby;
+        repack_x_block(x, xt, C, D, H, W, (b % per) % nbx, (b % per) / nbx, b / per);
+    } else {
+        const int r = b - nxb, nwx = q.C_in / RB;
+        repack_w_block(w, wp, q, r % nwx, r / nwx);
+    }
+}
+
+// The weight repack alone (after the scalar x repack).
+__global__ void __launch_bounds__(256)
+repack_w_kernel(const bf16_t *__restrict__ w, bf16_t *__restrict__ wp, const __grid_constant__ WPackParams q)
+{
+    repack_w_block(w, wp, q, (int)blockIdx.x, (int)blockIdx.y);
 }
 
 // ---- host side ------------------------------------------------------------------
@@ -666,21 +692,28 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     bf16_t *xt = static_cast<bf16_t *>(a.ws);
     bf16_t *wp = reinterpret_cast<bf16_t *>(static_cast<uint8_t *>(a.ws) + pl.x_bytes);
 
-    // 1) x -> (N, D, W, H, C)
+    // 1) x -> (N, D, W, H, C) and weights -> panels: one launch when D*H*W is
+    // a multiple of 8, else the scalar x repack and the weight repack
     const int64_t SP = pb.in_sp();
-    dim3 gx((unsigned)((SP + 63) / 64), (unsigned)((pb.C_in + 63) / 64), (unsigned)pb.N);
-    if (gx.x > 0x7fffffffu || gx.y > 65535 || gx.z > 65535) return cudaErrorInvalidConfiguration;
-    if (SP % 8 == 0)
-        repack_x_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.x), xt, pb.C_in, pb.Li[0],
-                                                  pb.Li[1], pb.Li[2]);
-    else
+    const int64_t nbx = (SP + 63) / 64, nby = (pb.C_in + 63) / 64;
+    cudaError_t e;
+    if (SP % 8 == 0) {
+        const int64_t nxb = nbx * nby * pb.N;
+        const int64_t nblocks = nxb + (int64_t)(pb.C_in / RB) * pb.C_out;
+        if (nblocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+        repack_kernel<<<(unsigned)nblocks, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.x), xt, pb.C_in,
+                                                              pb.Li[0], pb.Li[1], pb.Li[2], (int)nbx, (int)nby,
+                                                              (int)nxb, static_cast<const bf16_t *>(a.w), wp, pl.wq);
+    } else {
+        dim3 gx((unsigned)nbx, (unsigned)nby, (unsigned)pb.N);
+        if (gx.x > 0x7fffffffu || gx.y > 65535 || gx.z > 65535) return cudaErrorInvalidConfiguration;
         repack_x_scalar_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.x), xt, pb.C_in, pb.Li[0],
                                                          pb.Li[1], pb.Li[2]);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // 2) weights -> panels
-    dim3 gw((unsigned)(pb.C_in / RB), (unsigned)pb.C_out);
-    repack_w_kernel<<<gw, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.w), wp, pl.wq);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        repack_w_kernel<<<dim3((unsigned)(pb.C_in / RB), (unsigned)pb.C_out), 256, 0, a.stream>>>(
+            static_cast<const bf16_t *>(a.w), wp, pl.wq);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -711,8 +744,8 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.ntiles) grid = p.ntiles;
-    umma_ct3d_kernel<<<grid, kThreads, pl.smem, a.stream>>>(tmA, tmB, a.bias, a.y, p, status);
-    return cudaGetLastError();
+    return launch_dependent(umma_ct3d_kernel, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmA, tmB,
+                            a.bias, a.y, p, status);
 }
 
 }  // namespace ct

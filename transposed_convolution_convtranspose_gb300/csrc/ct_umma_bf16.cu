@@ -50,7 +50,8 @@
 //               every stage
 //   warps 7-14  epilogue, two per TMEM lane quarter: with a tile pair, half
 //               j drains tile j; with single tiles the halves take alternate
-//               16-channel chunks.  tcgen05.ld, bias, 4-byte stores
+//               16-channel chunks.  tcgen05.ld, bias; W phase 0 written as
+//               (output, 0) float2 pairs, W phase 1 into the odd slots
 // Every ring slot has exactly one producer, which refills it only after
 // waiting for its previous round, so a parity wait never has to tell two
 // phases apart.  Every mbarrier wait is bounded: a timeout records
@@ -337,10 +338,12 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // 4 qw x 8 qh); a warp reaches the lanes of quarter warp mod 4.  With two
         // tiles per unit, half j of the warps drains tile j (accumulator j) and
         // takes every 16-channel chunk; with one, the halves take alternate chunks.
-        // Each W phase half is drained as soon as it is complete: every output is
-        // one 4-byte store, the even and odd W outputs of a position coming from
-        // the two halves about half a unit apart (ordinary stores, so the line
-        // stays in L2 until both halves have been written).
+        // Each W phase half is drained as soon as it is complete.  W phase 0
+        // writes each position's pair (even output, 0) as one float2 -- whole
+        // 32-byte sectors, so L2 need not fetch the rest of a sector from DRAM,
+        // and ordinary stores keep the lines in L2 -- and W phase 1, about half a
+        // unit later, overwrites the odd outputs with 4-byte streaming stores.
+        // Both stores of a position come from the same thread, in that order.
         const int ew = warp & 3;
         const int half = (warp - kEpiWarp0) >> 2;
         const int a = ni == 2 ? half : 0;
@@ -361,7 +364,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 ok = __all_sync(0xffffffffu, ok);    // warp-uniform before .sync.aligned loads
                 tc::fence_after();
-                float *yrow = y + (int64_t)tcd.n * p.C_out * sp + ((int64_t)od * p.Lo1 + oh) * p.Lo2 + 2 * qw + wr;
+                float *yrow = y + (int64_t)tcd.n * p.C_out * sp + ((int64_t)od * p.Lo1 + oh) * p.Lo2 + 2 * qw;
                 const uint32_t tbase =
                     tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols + (uint32_t)wr * p.C_out;
                 // four chunks per batch; the half is released as soon as the
@@ -393,7 +396,10 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                             for (int i = 0; i < 16; ++i) {
                                 const int oc = c0 + i;
                                 const float bb = bias ? __ldg(bias + oc) : 0.f;
-                                yrow[(int64_t)oc * sp] = v[b][i] + bb;
+                                if (wr == 0)
+                                    *reinterpret_cast<float2 *>(yrow + (int64_t)oc * sp) = make_float2(v[b][i] + bb, 0.f);
+                                else
+                                    __stcs(yrow + (int64_t)oc * sp + 1, v[b][i] + bb);
                             }
                         }
                     }
@@ -673,7 +679,7 @@ bool umma_supported(const Problem &pb, const Args *a)
 {
     UPlan pl;
     if (!make_uplan(pb, &pl)) return false;
-    if (a && (((uintptr_t)a->y % 4) || ((uintptr_t)a->x % 16) || ((uintptr_t)a->w % 16))) return false;
+    if (a && (((uintptr_t)a->y % 8) || ((uintptr_t)a->x % 16) || ((uintptr_t)a->w % 16))) return false;
     return true;
 }
 

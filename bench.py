@@ -122,6 +122,12 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # nvidia-smi takes a while to start: wait (bounded) for its first
+            # sample, so that even a timed region shorter than the sampling
+            # interval has samples right before and after it
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.005)
         except Exception:
             self.proc = None
 
@@ -132,6 +138,10 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
+        n0 = len(self.lines)
+        t0 = time.time()
+        while len(self.lines) == n0 and time.time() - t0 < 0.5 and self.proc.poll() is None:
+            time.sleep(0.005)             # one more sample, taken after the timed region
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)

@@ -48,9 +48,9 @@
 //               pair and its accumulator (one thread issues an MMA only every
 //               ~100+ clocks; two warps nearly double the rate); both consume
 //               every stage
-//   warps 7-14  epilogue, two per TMEM lane quarter: with a tile pair, half
-//               j drains tile j; with single tiles the halves take alternate
-//               16-channel chunks.  tcgen05.ld, bias; W phase 0 written as
+//   warps 7-22  epilogue, four per TMEM lane quarter: with a tile pair, two
+//               of them drain each tile, taking alternate 16-channel chunks;
+//               with single tiles the four take alternate chunks.  tcgen05.ld, bias; W phase 0 written as
 //               (output, 0) float2 pairs, W phase 1 into the odd slots
 // Every ring slot has exactly one producer, which refills it only after
 // waiting for its previous round, so a parity wait never has to tell two
@@ -77,7 +77,8 @@ constexpr int MAXA = 3;      // A ring slots at most (input windows of a tile pa
 constexpr int MAXB = 8;      // B ring slots at most
 constexpr int NPB = 4;       // B producer warps at most (slot s loaded by warp s mod npb)
 constexpr int NMMA = 2;      // MMA-issuing warps at most (one per TMEM accumulator)
-constexpr int EPW = 2;       // epilogue warps per TMEM lane quarter
+constexpr int EPW = 4;       // epilogue warps per TMEM lane quarter
+constexpr int EB = 2;        // 16-channel chunks per epilogue batch (registers)
 constexpr int kAWarp = 0;
 constexpr int kBWarp0 = 1;
 constexpr int kMmaWarp0 = kBWarp0 + NPB;
@@ -148,6 +149,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __shared__ __align__(8) uint64_t a_full[MAXA], a_empty[MAXA], b_full[MAXB], b_empty[MAXB], acc_full[2][2],
         acc_empty[2][2], drain_bar[NMMA];
     __shared__ uint32_t tmem_slot;
+    __shared__ float s_bias[256];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;                                // na x a_slot
     uint8_t *sB = smem + (size_t)p.na * p.a_slot;      // nb x (wg x b_bytes)
@@ -176,6 +178,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         dev::fence_mbar_init();
     }
     if (warp == kMmaWarp0) tc::tmem_alloc(&tmem_slot, p.tmem_cols);
+    for (int i = threadIdx.x; i < p.C_out; i += blockDim.x) s_bias[i] = bias ? bias[i] : 0.f;
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -345,9 +348,11 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // unit later, overwrites the odd outputs with 4-byte streaming stores.
         // Both stores of a position come from the same thread, in that order.
         const int ew = warp & 3;
-        const int half = (warp - kEpiWarp0) >> 2;
-        const int a = ni == 2 ? half : 0;
-        const int cfirst = ni == 2 ? 0 : half, cstep = ni == 2 ? 1 : EPW;
+        const int grp = (warp - kEpiWarp0) >> 2;            // 0 .. EPW - 1
+        // two tiles: groups of even index drain tile 0, odd tile 1, and split its
+        // chunks EPW / 2 ways; one tile: the EPW groups split the chunks
+        const int a = ni == 2 ? (grp & 1) : 0;
+        const int cfirst = ni == 2 ? (grp >> 1) : grp, cstep = ni == 2 ? EPW / 2 : EPW;
         const int nchunk = p.C_out / 16;
         const int64_t sp = (int64_t)p.Lo0 * p.Lo1 * p.Lo2;
         bool ok = true;
@@ -367,44 +372,45 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 float *yrow = y + (int64_t)tcd.n * p.C_out * sp + ((int64_t)od * p.Lo1 + oh) * p.Lo2 + 2 * qw;
                 const uint32_t tbase =
                     tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols + (uint32_t)wr * p.C_out;
-                // four chunks per batch; the half is released as soon as the
-                // warp's last batch is in registers
+                // EB chunks per batch; the half is released as soon as the warp's
+                // last batch is in registers
                 bool released = false;
-                for (int ci = cfirst; ci < nchunk; ci += 4 * cstep) {
-                    float v[4][16];
+                for (int ci = cfirst; ci < nchunk; ci += EB * cstep) {
+                    float v[EB][16];
                     int nc = 0;
                     if (ok) {
 #pragma unroll
-                        for (int b = 0; b < 4; ++b)
+                        for (int b = 0; b < EB; ++b)
                             if (ci + b * cstep < nchunk) {
                                 tc::tmem_ld16(tbase + (uint32_t)((ci + b * cstep) * 16), v[b]);
                                 nc = b + 1;
                             }
                         tc::tmem_wait_ld();
                     }
-                    if (ci + 4 * cstep >= nchunk) {
+                    if (ci + EB * cstep >= nchunk) {
                         tc::fence_before();
                         dev::mbar_arrive(&acc_empty[a][wr]);
                         released = true;
                     }
                     if (ok && valid) {
 #pragma unroll
-                        for (int b = 0; b < 4; ++b) {
+                        for (int b = 0; b < EB; ++b) {
                             if (b >= nc) break;
                             const int c0 = (ci + b * cstep) * 16;
+                            float *yc = yrow + (int64_t)c0 * sp;
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
-                                const int oc = c0 + i;
-                                const float bb = bias ? __ldg(bias + oc) : 0.f;
+                                const float bb = s_bias[c0 + i];
                                 if (wr == 0)
-                                    *reinterpret_cast<float2 *>(yrow + (int64_t)oc * sp) = make_float2(v[b][i] + bb, 0.f);
+                                    *reinterpret_cast<float2 *>(yc) = make_float2(v[b][i] + bb, 0.f);
                                 else
-                                    __stcs(yrow + (int64_t)oc * sp + 1, v[b][i] + bb);
+                                    __stcs(yc + 1, v[b][i] + bb);
+                                yc += sp;
                             }
                         }
                     }
                 }
-                if (!released) {                      // a warp without chunks (C_out < 32)
+                if (!released) {                      // a warp without chunks
                     tc::fence_before();
                     dev::mbar_arrive(&acc_empty[a][wr]);
                 }
@@ -651,7 +657,7 @@ bool make_uplan(const Problem &pb, UPlan *out)
     const size_t b_slot = (size_t)p.wg * p.b_bytes;
     // three A slots when at least four B slots still fit, else two; the deepest
     // B ring that fits (room left for the static barriers), one producer per slot
-    const size_t budget = 227 * 1024 - 2048;
+    const size_t budget = 227 * 1024 - 3072;
     p.na = MAXA;
     while (p.na > 2 && (size_t)p.na * p.a_slot + 4 * b_slot > budget) --p.na;
     const size_t a_area = (size_t)p.na * p.a_slot;

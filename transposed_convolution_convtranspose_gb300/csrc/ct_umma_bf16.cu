@@ -9,17 +9,18 @@
 //     y[n, oc, 2q + r] = bias[oc] + sum_{taps t, ic} x[n, ic, q + delta_t] * w[ic, oc, k_t]
 // is a GEMM per phase: M = positions q, N = C_out, K = taps x C_in.  Two
 // repack kernels prepare the operands in the caller's workspace:
-//   x (N, C, D, H, W)          ->  x_t (N, D, W, H, C)   bf16, channels fastest, then H
+//   x (N, C, D, H, W)          ->  x_t (N, D, H, W, C)   bf16, channels fastest
 //   w (C, C_out, kD, kH, kW)   ->  weight panels, K-major (C_in fastest)
 //
-// Tile: 128 output positions q = 16 consecutive qw x 8 consecutive qh of
+// Tile: 128 output positions q = 8 consecutive qw x 16 consecutive qh of
 // one D plane, for one (rD, rH) phase pair; its accumulator is two halves of
 // C_out TMEM columns, one per W phase.  TMEM row m holds position
-// (qw, qh) = (m / 8, m mod 8), so each 8-row swizzle group of the A operand
-// is one qw column of 8 consecutive qh -- contiguous in x_t.  When two
-// accumulators fit, a unit of work is a pair of tiles (two neighbouring
-// 8-row qh blocks): they share every input window and weight panel, and
-// each of two MMA-issuing warps computes one of them.
+// (qw, qh) = (m mod 8, m / 8), so each 8-row swizzle group of the A operand
+// is 8 consecutive qw of one qh row -- contiguous in x_t -- and a warp's 32
+// TMEM lanes are 4 qh rows of 8 qw: its stores cover 4 rows x 64 bytes.
+// When two accumulators fit, a unit of work is a pair of tiles (two
+// neighbouring 8-column qw blocks): they share every input window and weight
+// panel, and each of two MMA-issuing warps computes one of them.
 //
 // Order within a unit: all of W phase 0, then all of W phase 1.  The TMEM
 // holds no second accumulator to switch to while one is drained, so the
@@ -27,10 +28,10 @@
 // computed, and phase 1's half while the next unit's phase 0 is computed.
 //
 // Operand A without shifted copies: per (W phase, D tap, K block) one TMA
-// box brings the unit's input window, (8 x tiles + H halo) x (16 + nT - 1)
-// positions x 64 channels, 128-byte swizzled, rows ordered (w, h).  The A
+// box brings the unit's input window, (16 + H halo) x (8 x tiles + nT - 1)
+// positions x 64 channels, 128-byte swizzled, rows ordered (h, w).  The A
 // operand of input offset (dh, dw) for tile j is that window read from start
-// row (dw - wlo) * hspan + (dh - dh_lo) + 8 j with a stride of hspan rows
+// row (dh - dh_lo) * wspan + (dw - wlo) + 8 j with a stride of wspan rows
 // between groups: only the shared-memory descriptor's start address and
 // stride-byte-offset change (the 128-byte swizzle is a function of the
 // absolute shared-memory address, so rows read from any start line up with
@@ -50,8 +51,9 @@
 //               every stage
 //   warps 7-22  epilogue, four per TMEM lane quarter: with a tile pair, two
 //               of them drain each tile, taking alternate 16-channel chunks;
-//               with single tiles the four take alternate chunks.  tcgen05.ld, bias; W phase 0 written as
-//               (output, 0) float2 pairs, W phase 1 into the odd slots
+//               with single tiles the four take alternate chunks.
+//               tcgen05.ld, bias; W phase 0 written as (output, 0) float2
+//               pairs, W phase 1 into the odd slots
 // Every ring slot has exactly one producer, which refills it only after
 // waiting for its previous round, so a parity wait never has to tell two
 // phases apart.  Every mbarrier wait is bounded: a timeout records
@@ -69,8 +71,8 @@ namespace ct {
 namespace {
 
 constexpr int BM = 128;      // positions per tile (UMMA M)
-constexpr int QWT = 16;      // qw per tile (TMEM row m: qw = m / 8)
-constexpr int MHT = 8;       // qh per tile (one 8-row swizzle group per qw)
+constexpr int QWT = 8;       // qw per tile (one 8-row swizzle group per qh; TMEM row m: qw = m mod 8)
+constexpr int MHT = 16;      // qh per tile (TMEM row m: qh = m / 8)
 constexpr int BK = 64;       // bf16 elements of K per stage (one 128-byte swizzle row)
 constexpr int UK = 16;       // K of one tcgen05.mma kind::f16
 constexpr int MAXA = 3;      // A ring slots at most (input windows of a tile pair)
@@ -89,7 +91,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 struct UParams {
     int N, C_in, C_out;
     int Lo0, Lo1, Lo2;
-    int QD, QH, QW, n_qhp, n_qwb;   // n_qhp: pairs of 8-row qh blocks
+    int QD, QH, QW, n_qhb, n_qwp;   // n_qwp: pairs of 8-column qw blocks
     int nT;                  // taps per dimension and class (kernel extent / 2)
     int n_kb;                // C_in / BK
     int ntiles;
@@ -101,7 +103,7 @@ struct UParams {
     uint32_t a_slot;         // bytes of an A ring slot (one input window, 1024-aligned)
     uint32_t b_bytes;        // bytes of one weight panel (C_out rows x 128)
     int wg;                  // W taps per B stage (nT when nT x C_out rows fit one box, else 1)
-    uint32_t sbo;            // A descriptor stride between 8-row groups: hspan x 128
+    uint32_t sbo;            // A descriptor stride between 8-row groups (qh): wspan x 128
     int hspan, wspan;        // input window extents (H, W) of a tile pair and one W phase
     int dh_lo;               // smallest H input offset
     int wlo[2];              // smallest W input offset of each W phase (its window's start)
@@ -109,19 +111,19 @@ struct UParams {
     int blk_units;           // C_out-row units of one (phase pair, D tap, H tap) block
 };
 
-// unit -> (n, qd, qh block pair, qw block, rD, rH); tile j of the pair is qh
-// block 2 * qhp + j.  The four (rD, rH) phases of one position block are
+// unit -> (n, qd, qh block, qw block pair, rD, rH); tile j of the pair is qw
+// block 2 * qwp + j.  The four (rD, rH) phases of one position block are
 // neighbours, so their input windows are reused from L2
 struct TileCoord {
-    int n, qd, qhp, qwb, rD, rH;
+    int n, qd, qhb, qwp, rD, rH;
 };
 __device__ __forceinline__ TileCoord tile_coord(int t, const UParams &p)
 {
     TileCoord c;
     c.rH = t & 1; t >>= 1;
     c.rD = t & 1; t >>= 1;
-    c.qwb = t % p.n_qwb; t /= p.n_qwb;
-    c.qhp = t % p.n_qhp; t /= p.n_qhp;
+    c.qwp = t % p.n_qwp; t /= p.n_qwp;
+    c.qhb = t % p.n_qhb; t /= p.n_qhb;
     c.qd = t % p.QD; t /= p.QD;
     c.n = t;
     return c;
@@ -212,7 +214,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             int last = -1, kc = -1;
             bool failed = false;
             TileCoord tcd;
-            tcd.n = tcd.qd = tcd.qhp = tcd.qwb = tcd.rD = tcd.rH = 0;
+            tcd.n = tcd.qd = tcd.qhb = tcd.qwp = tcd.rD = tcd.rH = 0;
             for (int g = q; g < total; g += np) {
                 const int k = g / sp, i = g % sp;
                 if (k != kc) {
@@ -228,10 +230,10 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const int wr = i / (nT * n_kb), r = i % (nT * n_kb);
                     const int jd = r / n_kb, kb = r % n_kb;
                     dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(p.hspan * p.wspan) * 128u);
-                    // x_t viewed as (C, H, W, D, N): W phase wr's window from
-                    // (qh0 + dh_lo, qw0 + wlo[wr])
+                    // x_t viewed as (C, W, H, D, N): W phase wr's window from
+                    // (qw0 + wlo[wr], qh0 + dh_lo)
                     dev::tma_load_5d(sA + (size_t)s * p.a_slot, &tmA, &fullb[s], kb * BK,
-                                     tcd.qhp * ni * MHT + p.dh_lo, tcd.qwb * QWT + p.wlo[wr],
+                                     tcd.qwp * ni * QWT + p.wlo[wr], tcd.qhb * MHT + p.dh_lo,
                                      tcd.qd + p.delta[0][tcd.rD][jd], tcd.n);
                 } else {
                     int r = i;
@@ -272,7 +274,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int wg = p.wg;
             const uint32_t sbo = p.sbo, c_out = (uint32_t)p.C_out;
             const int na = p.na, nb = p.nb;
-            const uint32_t trow = (uint32_t)(j * MHT) * 128u;   // tile j's rows in the window
+            const uint32_t trow = (uint32_t)(j * QWT) * 128u;   // tile j's columns in the window
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
             for (int k = 0; k < ntile_cta && ok; ++k) {
@@ -284,8 +286,8 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     }
                     tc::fence_after();
                     const uint32_t d = tmem + (uint32_t)j * p.acc_cols + (uint32_t)wr * c_out;
-                    // W tap jw reads window column nT - 1 - jw: (nT - 1 - jw) * hspan rows in
-                    const uint32_t awstep = (uint32_t)p.hspan * 128u;
+                    // W tap jw reads window column nT - 1 - jw: that many rows in
+                    const uint32_t awstep = 128u;
                     const uint32_t aw0 = (uint32_t)(nT - 1) * awstep;
                     bool init = false;
                     for (int jd = 0; jd < nT && ok; ++jd)
@@ -297,7 +299,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                             tc::fence_after();
                             const uint32_t wbase = sAb + (uint32_t)sa * a_slot + trow;
                             for (int jh = 0; jh < nT && ok; ++jh) {
-                                const uint32_t hoff = (uint32_t)(p.delta[1][tcd.rH][jh] - p.dh_lo) * 128u;
+                                const uint32_t hoff = (uint32_t)((p.delta[1][tcd.rH][jh] - p.dh_lo) * p.wspan) * 128u;
                                 for (int jw0 = 0; jw0 < nT; jw0 += wg) {
                                     if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
                                         ok = false;
@@ -359,7 +361,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         for (int k = 0; k < ntile_cta; ++k) {
             const TileCoord tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
             const int m = ew * 32 + lane;
-            const int qw = tcd.qwb * QWT + (m >> 3), qh = (tcd.qhp * ni + a) * MHT + (m & 7);
+            const int qw = (tcd.qwp * ni + a) * QWT + (m & 7), qh = tcd.qhb * MHT + (m >> 3);
             const int od = 2 * tcd.qd + tcd.rD, oh = 2 * qh + tcd.rH;
             const bool valid = qw < p.QW && od < p.Lo0 && oh < p.Lo1;
             for (int wr = 0; wr < 2; ++wr) {
@@ -455,7 +457,7 @@ __device__ __forceinline__ void repack_load_pairs(const bf16_t *__restrict__ src
     }
 }
 
-// x (N, C, D, H, W) -> x_t (N, D, W, H, C); D*H*W a multiple of 8, C of 64.
+// x (N, C, D, H, W) -> x_t (N, D, H, W, C); D*H*W a multiple of 8, C of 64.
 // Block (bx, by, n): positions bx*64.., channels by*64...
 __device__ __forceinline__ void repack_x_block(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, int C, int D,
                                                int H, int W, int bx, int by, int n)
@@ -474,7 +476,7 @@ __device__ __forceinline__ void repack_x_block(const bf16_t *__restrict__ x, bf1
         if (row < ncols) {
             const int64_t s = s0 + row;                 // (d, h, w) of the source position
             const int w = (int)(s % W), h = (int)((s / W) % H), d = (int)(s / ((int64_t)W * H));
-            const int64_t dst = ((((int64_t)n * D + d) * W + w) * H + h) * C + c0 + 8 * q;
+            const int64_t dst = ((((int64_t)n * D + d) * H + h) * W + w) * C + c0 + 8 * q;
             const uint4 v = make_uint4(tile[row][4 * q], tile[row][4 * q + 1], tile[row][4 * q + 2],
                                        tile[row][4 * q + 3]);
             *reinterpret_cast<uint4 *>(xt + dst) = v;
@@ -502,7 +504,7 @@ repack_x_scalar_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, in
         if (c0 + c < C && s0 + s < SP) {
             const int64_t ss = s0 + s;
             const int w = (int)(ss % W), h = (int)((ss / W) % H), d = (int)(ss / ((int64_t)W * H));
-            xt[((((int64_t)n * D + d) * W + w) * H + h) * C + c0 + c] = tile[c][s];
+            xt[((((int64_t)n * D + d) * H + h) * W + w) * C + c0 + c] = tile[c][s];
         }
     }
 }
@@ -601,13 +603,12 @@ bool make_uplan(const Problem &pb, UPlan *out)
     p.QW = p.Lo2 / 2;
     p.QD = (p.Lo0 + 1) / 2;
     p.QH = (p.Lo1 + 1) / 2;
-    p.n_qwb = (p.QW + QWT - 1) / QWT;
     p.nacc = 4 * pb.C_out <= 512 ? 2 : 1;     // tiles per unit
-    const int n_qhb = (p.QH + MHT - 1) / MHT;
-    p.n_qhp = (n_qhb + p.nacc - 1) / p.nacc;
+    p.n_qhb = (p.QH + MHT - 1) / MHT;
+    p.n_qwp = ((p.QW + QWT - 1) / QWT + p.nacc - 1) / p.nacc;
     p.nT = pb.K[0] / 2;
     p.n_kb = pb.C_in / BK;
-    const int64_t tiles = (int64_t)pb.N * p.QD * p.n_qhp * p.n_qwb * 4;
+    const int64_t tiles = (int64_t)pb.N * p.QD * p.n_qhb * p.n_qwp * 4;
     if (tiles > 0x7fffffff || tiles == 0) return false;
     p.ntiles = (int)tiles;
     // residue r of a stride-2 dimension takes the taps k == (r + p) mod 2, i.e.
@@ -634,12 +635,12 @@ bool make_uplan(const Problem &pb, UPlan *out)
             hi = p.delta[1][r][j] > hi ? p.delta[1][r][j] : hi;
         }
     p.dh_lo = lo;
-    p.hspan = p.nacc * MHT + hi - lo;
-    p.wspan = QWT + p.nT - 1;
+    p.hspan = MHT + hi - lo;
+    p.wspan = p.nacc * QWT + p.nT - 1;
     if (p.hspan > 256 || p.wspan > 256) return false;
     // W tap j of a phase reads offset wlo + nT - 1 - j: window column nT - 1 - j
     for (int r = 0; r < 2; ++r) p.wlo[r] = p.delta[2][r][p.nT - 1];
-    p.sbo = (uint32_t)p.hspan * 128u;
+    p.sbo = (uint32_t)p.wspan * 128u;
     p.a_slot = (uint32_t)((p.hspan * p.wspan * 128 + 1023) & ~1023);
     // panels: per (phase pair, D tap, H tap) block, the C_out rows of each
     // (W phase, W tap)
@@ -704,7 +705,7 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     bf16_t *xt = static_cast<bf16_t *>(a.ws);
     bf16_t *wp = reinterpret_cast<bf16_t *>(static_cast<uint8_t *>(a.ws) + pl.x_bytes);
 
-    // 1) x -> (N, D, W, H, C) and weights -> panels: one launch when D*H*W is
+    // 1) x -> (N, D, H, W, C) and weights -> panels: one launch when D*H*W is
     // a multiple of 8, else the scalar x repack and the weight repack
     const int64_t SP = pb.in_sp();
     const int64_t nbx = (SP + 63) / 64, nby = (pb.C_in + 63) / 64;
@@ -729,15 +730,15 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // 3) tensor maps: A over x_t viewed as (C, H, W, D, N), one input window per
+    // 3) tensor maps: A over x_t viewed as (C, W, H, D, N), one input window per
     // box; B over the panels (K = C_in, rows), boxes of wg x C_out rows
     CUtensorMap tmA, tmB;
-    const uint64_t adims[5] = {(uint64_t)pb.C_in, (uint64_t)pb.Li[1], (uint64_t)pb.Li[2], (uint64_t)pb.Li[0],
+    const uint64_t adims[5] = {(uint64_t)pb.C_in, (uint64_t)pb.Li[2], (uint64_t)pb.Li[1], (uint64_t)pb.Li[0],
                                (uint64_t)pb.N};
-    const uint64_t astr[4] = {(uint64_t)pb.C_in * 2, (uint64_t)pb.C_in * pb.Li[1] * 2,
-                              (uint64_t)pb.C_in * pb.Li[1] * pb.Li[2] * 2,
-                              (uint64_t)pb.C_in * pb.Li[1] * pb.Li[2] * pb.Li[0] * 2};
-    const uint32_t abox[5] = {(uint32_t)BK, (uint32_t)p.hspan, (uint32_t)p.wspan, 1u, 1u};
+    const uint64_t astr[4] = {(uint64_t)pb.C_in * 2, (uint64_t)pb.C_in * pb.Li[2] * 2,
+                              (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * 2,
+                              (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * pb.Li[0] * 2};
+    const uint32_t abox[5] = {(uint32_t)BK, (uint32_t)p.wspan, (uint32_t)p.hspan, 1u, 1u};
     if (!encode_tiled(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xt, adims, astr, abox,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;

@@ -135,13 +135,12 @@ __device__ __forceinline__ float tf32_hi(float v)
 // Block = 32 channels x 64 positions: 16-byte loads of 4 positions of one
 // channel (a warp reads 2 x 256 contiguous bytes), a shared tile of pitch 33,
 // 16-byte stores of 4 channels of one position (a warp writes 4 x 128 bytes).
-__global__ void __launch_bounds__(256)
-prep_x_kernel(const float *__restrict__ x, float *__restrict__ xhi, float *__restrict__ xlo, int C, int64_t SP)
+__device__ __forceinline__ void prep_x_block(const float *__restrict__ x, float *__restrict__ xhi,
+                                             float *__restrict__ xlo, int C, int64_t SP, int bx, int by, int n)
 {
     __shared__ float tile[64][33];
-    const int n = blockIdx.z;
-    const int c0 = blockIdx.y * 32;
-    const int64_t s0 = (int64_t)blockIdx.x * 64;
+    const int c0 = by * 32;
+    const int64_t s0 = (int64_t)bx * 64;
     const int ncols = (int)((SP - s0) < 64 ? (SP - s0) : 64);
     const float *xs = x + ((int64_t)n * C + c0) * SP + s0;
 #pragma unroll
@@ -178,19 +177,36 @@ prep_x_kernel(const float *__restrict__ x, float *__restrict__ xhi, float *__res
 
 // w (C_in, C_out, K0, K1, K2) -> weight panels [block][C_out][C_in]: block b
 // holds the hi or lo part of tap blk_tap[b].
-__global__ void __launch_bounds__(256)
-prep_w_kernel(const float *__restrict__ w, float *__restrict__ wp, WPanels q)
+__device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float *__restrict__ wp, const WPanels &q,
+                                             int bw, int nbw)
 {
     const int64_t per = (int64_t)q.C_out * q.C_in;
     const int64_t total = (int64_t)q.nblk * per;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
+    for (int64_t e = (int64_t)bw * blockDim.x + threadIdx.x; e < total; e += (int64_t)nbw * blockDim.x) {
         const int b = (int)(e / per);
         const int64_t r = e % per;
         const int oc = (int)(r / q.C_in), ic = (int)(r % q.C_in);
         const float v = __ldg(w + ((int64_t)ic * q.C_out + oc) * q.ntap + q.blk_tap[b]);
         const float h = tf32_hi(v);
         wp[e] = q.blk_lo[b] ? v - h : h;
+    }
+}
+
+// Both preps in one launch: blocks [0, nxb) move x (nbx x nby per image), the
+// remaining nbw blocks build the panels.  The GEMM kernel is launched as its
+// programmatic dependent.
+__global__ void __launch_bounds__(256)
+prep_kernel(const float *__restrict__ x, float *__restrict__ xhi, float *__restrict__ xlo, int C, int64_t SP,
+            int nbx, int nby, int nxb, const float *__restrict__ w, float *__restrict__ wp,
+            const __grid_constant__ WPanels q, int nbw)
+{
+    dev::griddep_launch_dependents();
+    const int b = (int)blockIdx.x;
+    if (b < nxb) {
+        const int per = nbx * nby;
+        prep_x_block(x, xhi, xlo, C, SP, (b % per) % nbx, (b % per) / nbx, b / per);
+    } else {
+        prep_w_block(w, wp, q, b - nxb, nbw);
     }
 }
 
@@ -269,6 +285,8 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    // the operands in the workspace come from the prep kernel
+    dev::griddep_wait();
     const uint32_t tmem = tmem_slot;
     const int nunit_cta =
         p.nunits > (int)blockIdx.x ? (p.nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -707,19 +725,18 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     float *xlo = reinterpret_cast<float *>(ws + pl.x_bytes);
     float *wp = reinterpret_cast<float *>(ws + 2 * pl.x_bytes);
 
-    // 1) x -> channels-last hi / lo
+    // 1) one launch: x -> channels-last hi / lo, weights -> run panels hi / lo
     const int64_t SP = pb.in_sp();
-    dim3 gx((unsigned)((SP + 63) / 64), (unsigned)(pb.C_in / 32), (unsigned)pb.N);
-    if (gx.x > 0x7fffffffu || gx.y > 65535 || gx.z > 65535) return cudaErrorInvalidConfiguration;
-    prep_x_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const float *>(a.x), xhi, xlo, pb.C_in, SP);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // 2) weights -> run panels, hi / lo
+    const int64_t nbx = (SP + 63) / 64, nby = pb.C_in / 32;
+    const int64_t nxb = nbx * nby * pb.N;
     const int64_t wtot = (int64_t)pl.wq.nblk * pb.C_out * pb.C_in;
-    int wblocks = (int)((wtot + 255) / 256);
-    if (wblocks > 4 * sm_count()) wblocks = 4 * sm_count();
-    prep_w_kernel<<<wblocks, 256, 0, a.stream>>>(static_cast<const float *>(a.w), wp, pl.wq);
-    e = cudaGetLastError();
+    int nbw = (int)((wtot + 255) / 256);
+    if (nbw > 4 * sm_count()) nbw = 4 * sm_count();
+    if (nxb + nbw > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    prep_kernel<<<(unsigned)(nxb + nbw), 256, 0, a.stream>>>(static_cast<const float *>(a.x), xhi, xlo, pb.C_in, SP,
+                                                            (int)nbx, (int)nby, (int)nxb,
+                                                            static_cast<const float *>(a.w), wp, pl.wq, nbw);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     // 3) tensor maps: A over x_hi / x_lo (C, W, H, D, N); B over the panels
@@ -770,12 +787,10 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     if (grid > p.nunits) grid = p.nunits;
     if (grid > 1 && (grid & 1)) --grid;   // an even grid: the residue flip of unit_coord permutes units
     if (a.add)
-        tc3d_tf32_kernel<true><<<grid, kThreads, pl.smem, a.stream>>>(tmXh, tmXl, tmW[0], tmW[1], tmW[2], tmW[3],
-                                                                      tmAdd, tmY, a.bias, p, status);
-    else
-        tc3d_tf32_kernel<false><<<grid, kThreads, pl.smem, a.stream>>>(tmXh, tmXl, tmW[0], tmW[1], tmW[2], tmW[3],
-                                                                       tmAdd, tmY, a.bias, p, status);
-    return cudaGetLastError();
+        return launch_dependent(tc3d_tf32_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXh,
+                                tmXl, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
+    return launch_dependent(tc3d_tf32_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXh,
+                            tmXl, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
 }
 
 }  // namespace ct

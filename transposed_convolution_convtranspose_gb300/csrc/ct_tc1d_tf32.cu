@@ -19,15 +19,18 @@
 // hi*hi + hi*lo + lo*hi in fp32 in TMEM.  The dropped lo*lo term and the
 // tf32 rounding of lo are each below 2^-21 of a product.
 //
-// Roles (persistent CTA of 32 * (6 + 4 * EPW) threads, one per SM):
+// Roles (persistent CTA of 32 * (7 + 4 * EPW) threads, one per SM):
 //   warp 0      TMA producer: x box [C_in = 32][136 positions] per tile (no
 //               swizzle); positions outside the input read zeros
-//   warp 1      TMEM allocation and MMA issue: taps x 4 K-steps x 3 split
-//               terms of tcgen05.mma M=128, N=C_out, K=8 into one of two TMEM
-//               accumulators (double-buffered across tiles)
+//   warps 1, 6  MMA issue (warp 1 also allocates the TMEM): taps x 4 K-steps
+//               x 3 split terms of tcgen05.mma M=128, N=C_out, K=8 per tile
+//               into one of two TMEM accumulators; warp 1 issues the even
+//               tiles, warp 6 the odd ones, each with its own split stage and
+//               accumulator (one issuing thread manages an MMA only every
+//               ~140 clocks, which bounded the kernel with a single issuer)
 //   warps 2-5   split + transpose: x box -> position-major (K-major) hi and lo
 //               tiles, 128-byte swizzled; the weights once, per tap, the same way
-//   warps 6..   epilogue, EPW warps per TMEM lane quarter (32 outputs q)
+//   warps 7..   epilogue, EPW warps per TMEM lane quarter (32 outputs q)
 //               taking interleaved 16-channel chunks: tcgen05.ld, bias, and per channel
 //               the s*32 consecutive outputs rebuilt by two warp shuffles and
 //               written as two coalesced 128-byte stores
@@ -46,12 +49,15 @@ namespace ct {
 namespace {
 
 constexpr int EPW = 4;           // epilogue warps per TMEM lane quarter
-constexpr int kThreads = 32 * (6 + 4 * EPW);
+constexpr int kEpiWarp0 = 7;     // warps 0-6: producer, MMA issuer 0, transposers, MMA issuer 1
+constexpr int kThreads = 32 * (kEpiWarp0 + 4 * EPW);
 constexpr int BM = 128;          // outputs per tile (UMMA M)
 constexpr int PAD = 4;           // stored rows before the first output (16-byte TMA start)
 constexpr int XR = BM + 2 * PAD; // stored input positions per tile
 constexpr int CI = 32;           // input channels (one 128-byte K row)
-constexpr int NS = 2;            // x-tile stages
+constexpr int NS = 2;            // raw x-box stages (TMA destinations)
+constexpr int NSS = 2;           // split (hi / lo K-major) stages: one per MMA issuer
+constexpr int NACC = 2;          // TMEM accumulators: one per MMA issuer
 constexpr int MAXT = 4;          // taps
 constexpr int MAXS = 2;          // stride (an output run is s*128 long)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -65,7 +71,7 @@ struct TParams {
     int rstar;                   // residue receiving the taps
     int ntq;                     // tiles per row
     int ntiles;
-    uint32_t tmem_cols;          // allocated TMEM columns (2 accumulators of C_out)
+    uint32_t tmem_cols;          // allocated TMEM columns (nacc accumulators of C_out)
     uint32_t idesc;
 };
 
@@ -135,26 +141,28 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int k)
 // ---- shared memory layout (offsets from a 1024-byte aligned base) ---------------
 constexpr uint32_t kXRaw = CI * XR * 4;                  // TMA box [32][136] fp32
 constexpr uint32_t kXK = XR * 128;                       // K-major 136 rows (17 atoms)
-constexpr uint32_t kWTile = 256 * 128;                   // up to taps*C_out = 256 rows
+constexpr int kWRows = 256;                              // taps * C_out at most
+constexpr uint32_t kWTile = kWRows * 128;
 constexpr int kChunk = 16;                               // output channels per TMEM load
 constexpr int kBatch = 2;                                // TMEM loads in flight per warp
 
 constexpr uint32_t OFF_XT = 0;
-constexpr uint32_t OFF_XHI = OFF_XT + NS * kXRaw;
-constexpr uint32_t OFF_XLO = OFF_XHI + NS * kXK;
-constexpr uint32_t OFF_WHI = OFF_XLO + NS * kXK;
+constexpr uint32_t OFF_XHI = OFF_XT + NS * kXRaw;     // NSS stages
+constexpr uint32_t OFF_XLO = OFF_XHI + NSS * kXK;
+constexpr uint32_t OFF_WHI = OFF_XLO + NSS * kXK;
 constexpr uint32_t OFF_WLO = OFF_WHI + kWTile;
 constexpr uint32_t kSmemBytes = OFF_WLO + kWTile + 1024;   // + alignment slack
 static_assert(kXRaw % 1024 == 0 && kXK % 1024 == 0, "1024-byte aligned tiles");
 static_assert(kSmemBytes <= 227 * 1024 - 256, "shared memory budget");
+static_assert(NSS % 2 == 0 && NACC % 2 == 0, "issuer k mod 2 owns the split stages and accumulators of its parity");
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restrict__ w,
                  const float *__restrict__ bias, float *__restrict__ y, TParams p, unsigned int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_x[NS], xt_free[NS], split_x[NS], empty_x[NS], acc_full[2],
-        acc_empty[2], w_ready;
+    __shared__ __align__(8) uint64_t full_x[NS], xt_free[NS], split_x[NSS], empty_x[NSS], acc_full[NACC],
+        acc_empty[NACC], w_ready;
     __shared__ uint32_t tmem_slot;
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -164,10 +172,12 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
         for (int s = 0; s < NS; ++s) {
             dev::mbar_init(&full_x[s], 1);
             dev::mbar_init(&xt_free[s], 128);
+        }
+        for (int s = 0; s < NSS; ++s) {
             dev::mbar_init(&split_x[s], 128);
             dev::mbar_init(&empty_x[s], 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < NACC; ++a) {
             dev::mbar_init(&acc_full[a], 1);
             dev::mbar_init(&acc_empty[a], 128 * EPW);   // every epilogue thread
         }
@@ -211,18 +221,24 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
                 for (int k = issued - NS > 0 ? issued - NS : 0; k < issued; ++k)
                     dev::mbar_wait_bounded(&full_x[k % NS], (k / NS) & 1, kWaitLimitNs);
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer
+    } else if (warp == 1 || warp == 6) {
+        // ---------------- MMA issuers: warp 1 takes the even tiles of this CTA,
+        // warp 6 the odd ones -- each owns the split stages and accumulators of
+        // its parity; one thread issues an MMA only every ~140 clocks, so the two
+        // issue streams run side by side.  (Two accumulators and two split
+        // stages per issuer measured slower than one of each.)
         if (lane == 0) {
             bool ok = dev::mbar_wait_bounded(&w_ready, 0, kWaitLimitNs);
             const uint32_t whi = dev::smem_u32(sm + OFF_WHI), wlo = dev::smem_u32(sm + OFF_WLO);
-            for (int k = 0; k < ntile_cta && ok; ++k) {
-                const int s = k % NS, a = k & 1;
-                if (k >= 2 && !dev::mbar_wait_bounded(&acc_empty[a], ((k >> 1) - 1) & 1, kWaitLimitNs)) {
+            for (int k = warp == 1 ? 0 : 1; k < ntile_cta && ok; k += 2) {
+                // tile k: x stage k mod 2 (this issuer's), accumulator k mod 4 (this
+                // issuer alternates between its two)
+                const int s = k % NSS, a = k % NACC;
+                if (k >= NACC && !dev::mbar_wait_bounded(&acc_empty[a], ((k / NACC) - 1) & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
-                if (!dev::mbar_wait_bounded(&split_x[s], (k / NS) & 1, kWaitLimitNs)) {
+                if (!dev::mbar_wait_bounded(&split_x[s], (k / NSS) & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
@@ -250,7 +266,7 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
     } else if (warp < 6) {
-        // ---------------- split + transpose warps (128 threads)
+        // ---------------- split + transpose warps (128 threads: warps 2-5)
         const int st = threadIdx.x - 64;
         // weights once: tap j's rows j*Cog + oc, K = ic; hi/lo, K-major swizzled
         for (int e = st; e < p.nT * p.Cog * CI; e += 128) {
@@ -266,16 +282,16 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
         dev::mbar_arrive(&w_ready);
         bool ok = true;
         for (int k = 0; k < ntile_cta; ++k) {
-            const int s = k % NS;
+            const int s = k % NS, ss = k % NSS;
             if (ok && !dev::mbar_wait_bounded(&full_x[s], (k / NS) & 1, kWaitLimitNs)) ok = false;
-            // the MMAs of tile k - NS must be done reading this stage's hi/lo tiles
-            if (ok && k >= NS && !dev::mbar_wait_bounded(&empty_x[s], ((k / NS) - 1) & 1, kWaitLimitNs))
+            // the MMAs of tile k - NSS must be done reading split stage ss
+            if (ok && k >= NSS && !dev::mbar_wait_bounded(&empty_x[ss], ((k / NSS) - 1) & 1, kWaitLimitNs))
                 ok = false;
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
             if (ok) {
                 const float *xt = reinterpret_cast<const float *>(sm + OFF_XT + s * kXRaw);   // [ic][pos]
-                uint8_t *xh = sm + OFF_XHI + s * kXK;
-                uint8_t *xl = sm + OFF_XLO + s * kXK;
+                uint8_t *xh = sm + OFF_XHI + ss * kXK;
+                uint8_t *xl = sm + OFF_XLO + ss * kXK;
                 for (int e = st; e < XR * (CI / 4); e += 128) {
                     const int pos = e % XR, cg = e / XR;
                     float4 hv, lv;
@@ -294,22 +310,22 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
                 fence_async_smem();
             }
             dev::mbar_arrive(&xt_free[s]);
-            dev::mbar_arrive(&split_x[s]);
+            dev::mbar_arrive(&split_x[ss]);
         }
     } else {
-        // ---------------- epilogue: warps 6-13, two per TMEM lane quarter (32 rows =
+        // ---------------- epilogue: EPW warps per TMEM lane quarter (32 rows =
         // 32 consecutive outputs q); the two take alternate 16-channel chunks.
         // All TMEM loads of a batch are issued before one wait, the accumulator
         // is released, then the stores run from registers.
         const int ew = warp & 3;                    // lanes 32*ew .. 32*ew + 31
-        const int half = (warp - 6) >> 2;           // 0 .. EPW-1
+        const int half = (warp - kEpiWarp0) >> 2;   // 0 .. EPW-1
         const int nchunk = p.Cog / kChunk;
         bool ok = true;
         for (int k = 0; k < ntile_cta; ++k) {
             const int tile = blockIdx.x + k * gridDim.x;
             const int n = tile / p.ntq, qt = tile % p.ntq;
-            const int a = k & 1;
-            if (ok && !dev::mbar_wait_bounded(&acc_full[a], (k >> 1) & 1, kWaitLimitNs)) {
+            const int a = k % NACC;
+            if (ok && !dev::mbar_wait_bounded(&acc_full[a], (k / NACC) & 1, kWaitLimitNs)) {
                 atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
                 ok = false;
             }
@@ -385,7 +401,7 @@ bool make_tplan(const Problem &pb, const Args *a, TParams *out)
     if (pb.nd != 1 || pb.dtype != CT_F32 || pb.G != 1) return false;
     const int S = pb.S[2], K = pb.K[2], DL = pb.DL[2], P = pb.P[2];
     if (S < 1 || S > MAXS || DL % S != 0 || K > MAXT) return false;
-    if (pb.Cig != CI || pb.Cog % kChunk != 0 || pb.Cog > 256 || K * pb.Cog > 256) return false;
+    if (pb.Cig != CI || pb.Cog % kChunk != 0 || pb.Cog > 256 || K * pb.Cog > kWRows) return false;
     if (pb.Li[2] % 4 != 0) return false;                 // TMA: 16-byte row strides of x
     if (a && (((uintptr_t)a->x % 16) || ((uintptr_t)a->y % 16))) return false;
     TParams p;
@@ -407,7 +423,7 @@ bool make_tplan(const Problem &pb, const Args *a, TParams *out)
     if (tiles > 0x7fffffff) return false;
     p.ntiles = (int)tiles;
     uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * pb.Cog)) cols <<= 1;
+    while (cols < (uint32_t)(NACC * pb.Cog)) cols <<= 1;
     p.tmem_cols = cols;
     // tcgen05 instruction descriptor: D fp32, A/B tf32, both K-major, N = C_out, M = 128
     p.idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(pb.Cog >> 3) << 17) |

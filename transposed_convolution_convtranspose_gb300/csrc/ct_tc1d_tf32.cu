@@ -144,7 +144,6 @@ constexpr uint32_t kXK = XR * 128;                       // K-major 136 rows (17
 constexpr int kWRows = 256;                              // taps * C_out at most
 constexpr uint32_t kWTile = kWRows * 128;
 constexpr int kChunk = 16;                               // output channels per TMEM load
-constexpr int kBatch = 2;                                // TMEM loads in flight per warp
 
 constexpr uint32_t OFF_XT = 0;
 constexpr uint32_t OFF_XHI = OFF_XT + NS * kXRaw;     // NSS stages
@@ -158,7 +157,8 @@ static_assert(NSS % 2 == 0 && NACC % 2 == 0, "issuer k mod 2 owns the split stag
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restrict__ w,
-                 const float *__restrict__ bias, float *__restrict__ y, TParams p, unsigned int *status)
+                 const float *__restrict__ bias, float *__restrict__ y, const __grid_constant__ TParams p,
+                 unsigned int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_x[NS], xt_free[NS], split_x[NSS], empty_x[NSS], acc_full[NACC],
@@ -314,9 +314,9 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
         }
     } else {
         // ---------------- epilogue: EPW warps per TMEM lane quarter (32 rows =
-        // 32 consecutive outputs q); the two take alternate 16-channel chunks.
-        // All TMEM loads of a batch are issued before one wait, the accumulator
-        // is released, then the stores run from registers.
+        // 32 consecutive outputs q) taking interleaved 16-channel chunks; the
+        // accumulator is released once the warp's last chunk is in registers,
+        // then the stores run from registers.
         const int ew = warp & 3;                    // lanes 32*ew .. 32*ew + 31
         const int half = (warp - kEpiWarp0) >> 2;   // 0 .. EPW-1
         const int nchunk = p.Cog / kChunk;
@@ -335,53 +335,44 @@ tc1d_tf32_kernel(const __grid_constant__ CUtensorMap tmx, const float *__restric
             const int o_w = p.S * (qt * BM + 32 * ew);
             const int nv = min(p.S * 32, p.L_out - o_w);   // may be <= 0 past the end
             float *yw = y + (int64_t)n * p.C_out * p.L_out + o_w;
-            // chunks half, half + 2, ... in batches of up to kBatch chunks
-            int ci = half;
-            bool released = false;
-            while (true) {
-                float v[kBatch][16];
-                int nb = 0;
-                for (; nb < kBatch && ci + EPW * nb < nchunk; ++nb) {
-                    if (ok)
-                        tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * p.Cog + (ci + EPW * nb) * kChunk),
-                                  v[nb]);
+            // chunks half, half + EPW, ...: one TMEM load of 16 channels at a time
+            // (compile-time register indices throughout: a runtime index into
+            // the value array would put it in local memory)
+            for (int ci = half; ci < nchunk; ci += EPW) {
+                float v[16];
+                if (ok) {
+                    tmem_ld16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(a * p.Cog + ci * kChunk), v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
                 }
-                if (ok && nb > 0) tmem_wait_ld();
-                if (!ok)
-#pragma unroll
-                    for (int b = 0; b < kBatch; ++b)
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[b][i] = 0.f;
-                const bool last = ci + EPW * nb >= nchunk;
-                if (last && !released) {            // done with accumulator a
+                if (ci + EPW >= nchunk) {             // done with accumulator a
                     tc_before();
                     dev::mbar_arrive(&acc_empty[a]);
-                    released = true;
                 }
+                const int c0 = ci * kChunk;
 #pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    if (b >= nb) break;
-                    const int c0 = (ci + EPW * b) * kChunk;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int oc = c0 + i;
-                        const float bb = bias ? __ldg(bias + oc) : 0.f;
-                        float *row = yw + (int64_t)oc * p.L_out;
-                        if (p.S == 2) {
-                            // lane l writes positions o_w + l and o_w + 32 + l: output q
-                            // (l >> 1) resp. 16 + (l >> 1) of this warp, residue l & 1
-                            const float s0 = __shfl_sync(0xffffffffu, v[b][i], lane >> 1);
-                            const float s1 = __shfl_sync(0xffffffffu, v[b][i], 16 + (lane >> 1));
-                            const bool hit = (lane & 1) == p.rstar;
-                            if (lane < nv) __stcs(row + lane, (hit ? s0 : 0.f) + bb);
-                            if (32 + lane < nv) __stcs(row + 32 + lane, (hit ? s1 : 0.f) + bb);
-                        } else {
-                            if (lane < nv) __stcs(row + lane, v[b][i] + bb);
-                        }
+                for (int i = 0; i < 16; ++i) {
+                    const int oc = c0 + i;
+                    const float bb = bias ? __ldg(bias + oc) : 0.f;
+                    float *row = yw + (int64_t)oc * p.L_out;
+                    if (p.S == 2) {
+                        // lane l writes positions o_w + l and o_w + 32 + l: output q
+                        // (l >> 1) resp. 16 + (l >> 1) of this warp, residue l & 1
+                        const float s0 = __shfl_sync(0xffffffffu, v[i], lane >> 1);
+                        const float s1 = __shfl_sync(0xffffffffu, v[i], 16 + (lane >> 1));
+                        const bool hit = (lane & 1) == p.rstar;
+                        if (lane < nv) __stcs(row + lane, (hit ? s0 : 0.f) + bb);
+                        if (32 + lane < nv) __stcs(row + 32 + lane, (hit ? s1 : 0.f) + bb);
+                    } else {
+                        if (lane < nv) __stcs(row + lane, v[i] + bb);
                     }
                 }
-                ci += EPW * nb;
-                if (last) break;
+            }
+            if (half >= nchunk) {                     // a warp without chunks
+                tc_before();
+                dev::mbar_arrive(&acc_empty[a]);
             }
         }
     }

@@ -1,6 +1,6 @@
 // ct_tc3d_tf32.cu -- FP32 ConvTranspose3d, plain or with the fused
 // add + t*hardswish(t) epilogue, on the tensor cores (tcgen05 kind::tf32)
-// with a 3-term split that keeps fp32-level accuracy.
+// with a split into tf32 and bf16 terms that keeps fp32-level accuracy.
 //
 // Method ([l1_p72] stride-phase classes: residue r of a dimension receives
 // the taps k with (r + p - k) even, reading input q + (r + p - k)/2;
@@ -12,12 +12,15 @@
 // -- for 128 positions q a GEMM with M = 128, N = C_out, K = C_in per tap.
 //
 // Operands (caller's workspace, written by the two prep kernels):
-//   x (N, C_in, D, H, W) -> x_hi, x_lo (N, D, H, W, C_in), channels-last
+//   x (N, C_in, D, H, W) -> x_hi (N, D, H, W, C_in) tf32 and x_c (N, D, H, W,
+//                           2 C_in) bf16, channels-last
 //   w (C_in, C_out, kD, kH, kW) -> weight panels, K-major (C_in fastest)
-// with hi = v rounded to tf32 (cvt.rna) and lo = v - hi (exact in fp32);
-// three MMAs per product accumulate hi*hi + hi*lo + lo*hi in fp32 in TMEM;
-// the dropped lo*lo term and the tf32 truncation of lo are each below 2^-21
-// of a product.
+// with hi = v rounded to tf32 (cvt.rna) and lo = v - hi (exact in fp32); per
+// K step a kind::tf32 MMA accumulates hi*hi and ONE kind::f16 MMA over twice
+// the K accumulates both corrections hi*lo + lo*hi, on bf16 copies of
+// [x_hi | x_lo] and [w_lo | w_hi] of the step's 8 channels (the corrections
+// are ~2^-11 of a product, so their bf16 factors leave ~2^-19 of it; the
+// dropped lo*lo term is below 2^-21).
 //
 // Schedule.  A unit of work is 128 positions (whole W rows of MH H rows of
 // one D plane) and one D residue rD, with the four (rH, rW) phases as four
@@ -25,15 +28,15 @@
 // across units when they fit, so the epilogue of one unit overlaps the MMAs
 // of the next).  Every distinct input offset (dd, dh, dw) the unit reads is
 // one A tile; the phases that read it with some tap form runs of adjacent
-// accumulators, and the weights of a run are stored as one panel -- hi rows
-// of its phases, then lo rows -- so that one MMA with N = run length x C_out
+// accumulators, and the weights of a run are stored as one panel -- tf32 rows
+// of its phases, then bf16 correction rows -- so that one MMA with N = run length x C_out
 // serves the whole run.  An MMA instruction costs the issuing thread about
 // 100 clocks whatever its N, so wide runs are what keeps the tensor cores
 // busy; the issue loop carries ring slots and parities as counters.
 //
 // Roles (persistent CTA, one per SM):
-//   warp 0      TMA producer of the A ring (hi and lo 5-D boxes of 128
-//               positions x 32 channels at the offset; boxes reaching outside
+//   warp 0      TMA producer of the A ring (x_hi and x_c 5-D boxes of 128
+//               positions x 128 bytes of channels at the offset; boxes reaching outside
 //               the input read zeros, which is the boundary handling)
 //   warp 1      TMA producer of the B ring (a run's panel is one box).  Each
 //               ring slot has exactly one producer, which refills it only after
@@ -55,6 +58,7 @@
 // the device status word and the roles unwind (each producer waits, bounded,
 // for its own TMA copies and the MMA issuer for its own MMAs before the TMEM
 // is freed).
+#include <cuda_bf16.h>
 #include <string.h>
 
 #include "ct_internal.h"
@@ -81,7 +85,7 @@ constexpr int kMmaWarp = kBWarp0 + NPB;
 constexpr int kEpiWarp0 = kMmaWarp + 1;
 constexpr int kStoreWarp = kEpiWarp0 + 4 * EPW;
 constexpr int kThreads = 32 * (kStoreWarp + 1);
-constexpr uint32_t kATile = BM * CK * 4;       // one of hi / lo: 16 KB
+constexpr uint32_t kATile = BM * CK * 4;       // the tf32 tile or the bf16 correction tile: 16 KB
 constexpr uint32_t kEChunk = 16 * 4 * BM * 4;  // 16 channels x 4 phases x 128 positions, fp32: 32 KB
 constexpr int kEpiThreads = 32 * 4 * EPW;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -93,7 +97,7 @@ struct Entry {
     int16_t run0, pad;
 };
 // Adjacent accumulators p0 .. p0 + len - 1 served by one weight panel whose
-// hi rows start at row brow (lo rows follow after len x C_out rows).  fresh:
+// tf32 rows start at row brow (correction rows follow after len x C_out rows).  fresh:
 // the first MMA of the run writes (rather than adds to) its accumulators.
 struct Run {
     int8_t p0, len, fresh, pad;
@@ -110,13 +114,15 @@ struct T3Params {
     uint32_t acc_cols;           // 4 x C_out
     uint32_t tmem_cols;
     uint32_t bslot;              // bytes of a B ring slot
-    uint32_t idesc[5];           // instruction descriptor for N = len x C_out, len 1..4
+    uint32_t idesc[5];           // kind::tf32 instruction descriptor for N = len x C_out, len 1..4
+    uint32_t idesc_b[5];         // kind::f16 (bf16), the same N
     int nE[2];
     Entry ent[2][MAXE];
     Run run[2][MAXR];
 };
 
-// Weight panel rows: block b (C_out rows) holds tap blk_tap[b], hi or lo.
+// Weight panel rows: block b (C_out rows) holds tap blk_tap[b]: its tf32 part
+// (blk_lo 0) or its bf16 correction rows (blk_lo 1).
 struct WPanels {
     int C_in, C_out, ntap, nblk;
     int8_t blk_tap[MAXBLK];
@@ -131,12 +137,20 @@ __device__ __forceinline__ float tf32_hi(float v)
 }
 
 // ---- prep kernels ------------------------------------------------------------
-// x (N, C, S) -> x_hi, x_lo (N, S, C); S = D*H*W a multiple of 4, C of 32.
-// Block = 32 channels x 64 positions: 16-byte loads of 4 positions of one
-// channel (a warp reads 2 x 256 contiguous bytes), a shared tile of pitch 33,
-// 16-byte stores of 4 channels of one position (a warp writes 4 x 128 bytes).
+// x (N, C, S) -> x_hi (N, S, C) tf32 and x_c (N, S, 2C) bf16 where, per 32
+// channels and K step of 8, x_c holds [bf16(hi) of the 8 | bf16(lo) of the 8];
+// S = D*H*W a multiple of 4, C of 32.  Block = 32 channels x 64 positions:
+// 16-byte loads of 4 positions of one channel (a warp reads 2 x 256
+// contiguous bytes), a shared tile of pitch 33, then per thread 4 channels of
+// one position: a 16-byte store of the tf32 parts, two 8-byte stores of the
+// bf16 ones.
+__device__ __forceinline__ uint32_t bf16_bits(float v)
+{
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
 __device__ __forceinline__ void prep_x_block(const float *__restrict__ x, float *__restrict__ xhi,
-                                             float *__restrict__ xlo, int C, int64_t SP, int bx, int by, int n)
+                                             uint16_t *__restrict__ xc, int C, int64_t SP, int bx, int by, int n)
 {
     __shared__ float tile[64][33];
     const int c0 = by * 32;
@@ -161,22 +175,28 @@ __device__ __forceinline__ void prep_x_block(const float *__restrict__ x, float 
         const int idx = threadIdx.x + 256 * it;
         const int q = idx & 7, pos = idx >> 3;
         if (pos < ncols) {
-            float h[4], l[4];
+            float h[4];
+            uint32_t hb[4], lb[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float v = tile[pos][4 * q + i];
                 h[i] = tf32_hi(v);
-                l[i] = v - h[i];
+                hb[i] = bf16_bits(h[i]);
+                lb[i] = bf16_bits(v - h[i]);
             }
             const int64_t o = ob + (int64_t)pos * C + 4 * q;
             *reinterpret_cast<float4 *>(xhi + o) = make_float4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<float4 *>(xlo + o) = make_float4(l[0], l[1], l[2], l[3]);
+            // channels 4q..4q+3 of this block: K step q / 2, elements 4 (q & 1) ..
+            uint16_t *cr = xc + 2 * (ob + (int64_t)pos * C) + (q >> 1) * 16 + (q & 1) * 4;
+            *reinterpret_cast<uint2 *>(cr) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+            *reinterpret_cast<uint2 *>(cr + 8) = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
         }
     }
 }
 
-// w (C_in, C_out, K0, K1, K2) -> weight panels [block][C_out][C_in]: block b
-// holds the hi or lo part of tap blk_tap[b].
+// w (C_in, C_out, K0, K1, K2) -> weight panels [block][C_out][C_in x 4 bytes]:
+// block b holds tap blk_tap[b] as tf32 values, or (blk_lo) as bf16 rows of
+// [bf16(lo) | bf16(hi)] per K step of 8 input channels.
 __device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float *__restrict__ wp, const WPanels &q,
                                              int bw, int nbw)
 {
@@ -188,7 +208,15 @@ __device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float 
         const int oc = (int)(r / q.C_in), ic = (int)(r % q.C_in);
         const float v = __ldg(w + ((int64_t)ic * q.C_out + oc) * q.ntap + q.blk_tap[b]);
         const float h = tf32_hi(v);
-        wp[e] = q.blk_lo[b] ? v - h : h;
+        if (!q.blk_lo[b]) {
+            wp[e] = h;
+        } else {
+            // the row's bf16 view: K step ic / 8 of its 32-channel block
+            uint16_t *row = reinterpret_cast<uint16_t *>(wp + (e - ic));
+            const int kb = ic >> 5, kk = (ic & 31) >> 3, el = ic & 7;
+            row[kb * 64 + kk * 16 + el] = (uint16_t)bf16_bits(v - h);
+            row[kb * 64 + kk * 16 + 8 + el] = (uint16_t)bf16_bits(h);
+        }
     }
 }
 
@@ -196,7 +224,7 @@ __device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float 
 // remaining nbw blocks build the panels.  The GEMM kernel is launched as its
 // programmatic dependent.
 __global__ void __launch_bounds__(256)
-prep_kernel(const float *__restrict__ x, float *__restrict__ xhi, float *__restrict__ xlo, int C, int64_t SP,
+prep_kernel(const float *__restrict__ x, float *__restrict__ xhi, uint16_t *__restrict__ xc, int C, int64_t SP,
             int nbx, int nby, int nxb, const float *__restrict__ w, float *__restrict__ wp,
             const __grid_constant__ WPanels q, int nbw)
 {
@@ -204,7 +232,7 @@ prep_kernel(const float *__restrict__ x, float *__restrict__ xhi, float *__restr
     const int b = (int)blockIdx.x;
     if (b < nxb) {
         const int per = nbx * nby;
-        prep_x_block(x, xhi, xlo, C, SP, (b % per) % nbx, (b % per) / nbx, b / per);
+        prep_x_block(x, xhi, xc, C, SP, (b % per) % nbx, (b % per) / nbx, b / per);
     } else {
         prep_w_block(w, wp, q, b - nxb, nbw);
     }
@@ -235,7 +263,7 @@ __device__ __forceinline__ UnitCoord unit_coord(int u, const T3Params &p)
 
 template <bool ADD>
 __global__ void __launch_bounds__(kThreads, 1)
-tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant__ CUtensorMap tmXl,
+tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant__ CUtensorMap tmXc,
                  const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
                  const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmW4,
                  const __grid_constant__ CUtensorMap tmAdd, const __grid_constant__ CUtensorMap tmY,
@@ -247,14 +275,14 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
     __shared__ uint32_t tmem_slot;
     __shared__ float s_bias[128];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = sm;                                  // NA x (hi, lo)
+    uint8_t *sA = sm;                                  // NA x (tf32 tile, bf16 correction tile)
     uint8_t *sB = sm + NA * 2 * kATile;                // NB x bslot
     uint8_t *sE = sB + NB * p.bslot;                   // NE x kEChunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         dev::prefetch_tensormap(&tmXh);
-        dev::prefetch_tensormap(&tmXl);
+        dev::prefetch_tensormap(&tmXc);
         dev::prefetch_tensormap(&tmW1);
         dev::prefetch_tensormap(&tmW2);
         dev::prefetch_tensormap(&tmW3);
@@ -324,7 +352,7 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
                                     dev::mbar_arrive_expect_tx(&fullb[s], 2 * kATile);
                                     dev::tma_load_5d(ah, &tmXh, &fullb[s], kb * CK, en.dw, qh0 + en.dh,
                                                      u.qd + en.dd, u.n);
-                                    dev::tma_load_5d(ah + kATile, &tmXl, &fullb[s], kb * CK, en.dw, qh0 + en.dh,
+                                    dev::tma_load_5d(ah + kATile, &tmXc, &fullb[s], kb * 2 * CK, en.dw, qh0 + en.dh,
                                                      u.qd + en.dd, u.n);
                                 } else {
                                     // the run's panel exactly: a box of 2 x len x C_out rows
@@ -391,15 +419,15 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
                             const uint32_t bh = sBb + (uint32_t)sb * bslot;
                             const uint64_t dbh = tc::desc_sw128(bh);
                             const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(ru.len * C_out) * 128u);
-                            const uint32_t id = p.idesc[ru.len];
+                            const uint32_t id = p.idesc[ru.len], idb = p.idesc_b[ru.len];
                             const uint32_t dd = d + (uint32_t)(ru.p0 * C_out);
                             const uint32_t acc0 = (ru.fresh && kb == 0) ? 0u : 1u;
 #pragma unroll
                             for (int kk = 0; kk < CK / 8; ++kk) {
                                 // advance 8 tf32 = 32 bytes along K inside the swizzle atom
-                                tc::mma_tf32(dd, dah + 2 * kk, dbh + 2 * kk, id, kk ? 1u : acc0);
-                                tc::mma_tf32(dd, dah + 2 * kk, dbl + 2 * kk, id, 1u);
-                                tc::mma_tf32(dd, dal + 2 * kk, dbh + 2 * kk, id, 1u);
+                                // 32 bytes per step: 8 tf32, or 16 bf16 (the 8 channels' hi and lo)
+                                tc::mma_tf32(dd, dah + 2 * kk, dbh + 2 * kk, id, kk ? 1u : acc0);   // hi x hi
+                                tc::mma_bf16(dd, dal + 2 * kk, dbl + 2 * kk, idb, 1u);             // corrections
                             }
                             tc::commit(&b_empty[sb]);
                             if (++sb == NB) {
@@ -681,8 +709,10 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     wq.C_out = pb.C_out;
     wq.ntap = pb.kvol();
     wq.nblk = nblk;
-    for (int len = 1; len <= 4; ++len)
+    for (int len = 1; len <= 4; ++len) {
         p.idesc[len] = len * pb.C_out <= 256 ? tc::idesc(2, len * pb.C_out, BM) : 0u;
+        p.idesc_b[len] = len * pb.C_out <= 256 ? tc::idesc(1, len * pb.C_out, BM) : 0u;
+    }
     p.acc_cols = (uint32_t)(4 * pb.C_out);
     p.nacc = 8 * pb.C_out <= 512 ? 2 : 1;
     uint32_t cols = 32;
@@ -722,10 +752,10 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     const T3Params &p = pl.p;
     uint8_t *ws = static_cast<uint8_t *>(a.ws);
     float *xhi = reinterpret_cast<float *>(ws);
-    float *xlo = reinterpret_cast<float *>(ws + pl.x_bytes);
+    uint16_t *xc = reinterpret_cast<uint16_t *>(ws + pl.x_bytes);
     float *wp = reinterpret_cast<float *>(ws + 2 * pl.x_bytes);
 
-    // 1) one launch: x -> channels-last hi / lo, weights -> run panels hi / lo
+    // 1) one launch: x -> channels-last tf32 + bf16 corrections, weights -> run panels
     const int64_t SP = pb.in_sp();
     const int64_t nbx = (SP + 63) / 64, nby = pb.C_in / 32;
     const int64_t nxb = nbx * nby * pb.N;
@@ -733,26 +763,30 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     int nbw = (int)((wtot + 255) / 256);
     if (nbw > 4 * sm_count()) nbw = 4 * sm_count();
     if (nxb + nbw > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    prep_kernel<<<(unsigned)(nxb + nbw), 256, 0, a.stream>>>(static_cast<const float *>(a.x), xhi, xlo, pb.C_in, SP,
+    prep_kernel<<<(unsigned)(nxb + nbw), 256, 0, a.stream>>>(static_cast<const float *>(a.x), xhi, xc, pb.C_in, SP,
                                                             (int)nbx, (int)nby, (int)nxb,
                                                             static_cast<const float *>(a.w), wp, pl.wq, nbw);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // 3) tensor maps: A over x_hi / x_lo (C, W, H, D, N); B over the panels
+    // 3) tensor maps: A over x_hi (C, W, H, D, N) fp32 and x_c (2C, W, H, D, N)
+    // bf16 -- 128-byte rows either way; B over the panels
     // (C_in, rows), one map per run length len (a box of 2 x len x C_out rows:
     // the run's hi and lo panels)
-    CUtensorMap tmXh, tmXl, tmW[4];
+    CUtensorMap tmXh, tmXc, tmW[4];
     const uint64_t adims[5] = {(uint64_t)pb.C_in, (uint64_t)pb.Li[2], (uint64_t)pb.Li[1], (uint64_t)pb.Li[0],
                                (uint64_t)pb.N};
     const uint64_t astr[4] = {(uint64_t)pb.C_in * 4, (uint64_t)pb.C_in * pb.Li[2] * 4,
                               (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * 4,
                               (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * pb.Li[0] * 4};
     const uint32_t abox[5] = {(uint32_t)CK, (uint32_t)p.QW, (uint32_t)p.MH, 1u, 1u};
+    const uint64_t cdims[5] = {(uint64_t)pb.C_in * 2, (uint64_t)pb.Li[2], (uint64_t)pb.Li[1], (uint64_t)pb.Li[0],
+                               (uint64_t)pb.N};
+    const uint32_t cbox[5] = {(uint32_t)CK * 2, (uint32_t)p.QW, (uint32_t)p.MH, 1u, 1u};
     const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)pl.wq.nblk * pb.C_out};
     const uint64_t bstr[1] = {(uint64_t)pb.C_in * 4};
     if (!encode_tiled(&tmXh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xhi, adims, astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&tmXl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xlo, adims, astr, abox, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_tiled(&tmXc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc, cdims, astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     for (int len = 1; len <= 4; ++len) {
         // lengths beyond the longest run keep a valid map of the longest box
@@ -788,9 +822,9 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     if (grid > 1 && (grid & 1)) --grid;   // an even grid: the residue flip of unit_coord permutes units
     if (a.add)
         return launch_dependent(tc3d_tf32_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXh,
-                                tmXl, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
+                                tmXc, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
     return launch_dependent(tc3d_tf32_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXh,
-                            tmXl, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
+                            tmXc, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
 }
 
 }  // namespace ct

@@ -259,6 +259,13 @@ class Runner:
             self.path = ct.ct_path_1d(c["N"], c["C_in"], c["C_out"], c["L_in"][0], c["k"][0],
                                       c["groups"], c["stride"][0], c["padding"][0],
                                       c["output_padding"][0], c["dilation"][0], self.dt)
+        elif c["nd"] == 2:
+            self.ws_bytes = ct.ct_workspace_size_2d(c["N"], c["C_in"], c["C_out"], c["L_in"], c["k"],
+                                                    c["groups"], c["stride"], c["padding"],
+                                                    c["output_padding"], c["dilation"], self.dt)
+            self.path = ct.ct_path_2d(c["N"], c["C_in"], c["C_out"], c["L_in"], c["k"], c["groups"],
+                                      c["stride"], c["padding"], c["output_padding"], c["dilation"],
+                                      self.dt, c["add"])
         else:
             self.ws_bytes = ct.ct_workspace_size_3d(c["N"], c["C_in"], c["C_out"], c["L_in"], c["k"],
                                                     c["groups"], c["stride"], c["padding"],
@@ -278,6 +285,12 @@ class Runner:
                              c["L_in"][0], c["k"][0], c["groups"], c["stride"][0], c["padding"][0],
                              c["output_padding"][0], c["dilation"][0], self.dt, self.ws,
                              self.ws_bytes, stream)
+        elif c["nd"] == 2:
+            fwd = ct.ct_forward_2d_add_hswish if c["add"] else ct.ct_forward_2d
+            extra = (d["add"],) if c["add"] else ()
+            fwd(d["x"], d["w"], d["bias"], *extra, self.y, c["N"], c["C_in"], c["C_out"], c["L_in"],
+                c["k"], c["groups"], c["stride"], c["padding"], c["output_padding"], c["dilation"],
+                self.dt, self.ws, self.ws_bytes, stream)
         elif c["add"]:
             ct.ct_forward_3d_add_hswish(d["x"], d["w"], d["bias"], d["add"], self.y, c["N"],
                                         c["C_in"], c["C_out"], c["L_in"], c["k"], c["groups"],
@@ -390,10 +403,13 @@ def roofline(name, cfg, path, wm, sec, peaks):
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peaks["source"] + " cuBLAS bf16 burst"}
     if path in ("tc1d_tf32x3", "tc3d_tf32x3", "tc3dg_tf32x3"):
-        # FP32 on the tensor cores: 3 tf32 products per multiply-add at the tf32
-        # rate (half the bf16 rate).  The roofline is the slower of that tensor
-        # time and the HBM time of the algorithmic bytes.
-        tensor_s = 3 * wm["flops"] / (peaks["bf16_tflops"] / 2 * 1e12)
+        # FP32 on the tensor cores.  The 1-D kernel does 3 tf32 products per
+        # multiply-add at the tf32 rate (half the bf16 rate); the 3-D kernels one
+        # tf32 product plus one bf16 MMA over twice the K (the two corrections),
+        # i.e. the time of 2 + 2 bf16 products.  The roofline is the slower of
+        # that tensor time and the HBM time of the algorithmic bytes.
+        bf16_products = 6 if path == "tc1d_tf32x3" else 4
+        tensor_s = bf16_products * wm["flops"] / (peaks["bf16_tflops"] * 1e12)
         hbm_s = wm["bytes"] / (peaks["hbm_gbs"] * 1e9)
         if hbm_s >= tensor_s:
             achieved = wm["bytes"] / sec / 1e9
@@ -401,12 +417,12 @@ def roofline(name, cfg, path, wm, sec, peaks):
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                     "peak_source": peaks["source"] + " copy bandwidth",
                     "tensor_time_floor_us": round(tensor_s * 1e6, 1)}
-        achieved = 3 * wm["flops"] / sec / 1e12
-        peak = peaks["bf16_tflops"] / 2
+        achieved = bf16_products * wm["flops"] / sec / 1e12
+        peak = peaks["bf16_tflops"]
         return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1),
-                "unit": "TFLOP/s (tf32, 3 products per multiply-add)",
+                "unit": "TFLOP/s (bf16-equivalent: %d bf16 products per multiply-add)" % bf16_products,
                 "frac": round(achieved / peak, 4), "traffic": traffic,
-                "peak_source": peaks["source"] + " cuBLAS bf16 burst / 2 (tf32)",
+                "peak_source": peaks["source"] + " cuBLAS bf16 burst",
                 "hbm_time_floor_us": round(hbm_s * 1e6, 1)}
     ai = wm["flops"] / wm["bytes"]
     alu_peak = fp32_alu_peak_tflops(peaks["sm_max_mhz"])

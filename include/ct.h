@@ -89,6 +89,10 @@ ct_status ct_workspace_size_3d(int N, int C_in, int C_out, const int in_dhw[3],
                                const int k_dhw[3], int groups, const int stride[3],
                                const int padding[3], const int output_padding[3],
                                const int dilation[3], ct_dtype dtype, size_t *bytes);
+ct_status ct_workspace_size_2d(int N, int C_in, int C_out, const int in_hw[2], const int k_hw[2],
+                               int groups, const int stride[2], const int padding[2],
+                               const int output_padding[2], const int dilation[2], ct_dtype dtype,
+                               size_t *bytes);
 
 /* ConvTranspose1d forward ([l1_p79]).  x (N, C_in, L_in), w (C_in,
  * C_out/groups, k), bias (C_out) or NULL, y (N, C_out, L_out) fp32. */
@@ -104,6 +108,31 @@ ct_status ct_forward_3d(const void *x, const void *w, const float *bias, float *
                         int groups, const int stride[3], const int padding[3],
                         const int output_padding[3], const int dilation[3],
                         ct_dtype dtype, void *workspace, size_t ws_bytes, void *stream);
+
+/* ConvTranspose2d forward ([l1_p72]: its ConvTranspose2d asides -- every input
+ * element scatter-adds weight x value into the output, unflipped, and the
+ * output size (H - 1)s - 2p + d(k - 1) + op + 1 per dimension).  x (N, C_in, H,
+ * W), w (C_in, C_out/groups, kH, kW), bias (C_out) or NULL, y (N, C_out, H_out,
+ * W_out) fp32; in_hw = (H, W), the other arrays per (H, W).  Computed as the 3-D
+ * operator with a unit D dimension (extent 1, stride 1, no padding), which has
+ * the same memory layouts, so it takes the same kernels; workspace as
+ * ct_workspace_size_2d reports.  Errors as ct_forward_3d. */
+ct_status ct_forward_2d(const void *x, const void *w, const float *bias, float *y,
+                        int N, int C_in, int C_out, const int in_hw[2], const int k_hw[2],
+                        int groups, const int stride[2], const int padding[2],
+                        const int output_padding[2], const int dilation[2],
+                        ct_dtype dtype, void *workspace, size_t ws_bytes, void *stream);
+
+/* ConvTranspose2d + add + x*hardswish(x): the epilogue of
+ * ct_forward_3d_add_hswish on the 2-D operator of ct_forward_2d.  add has the
+ * shape of y (fp32) and must not be NULL; y may equal add. */
+ct_status ct_forward_2d_add_hswish(const void *x, const void *w, const float *bias,
+                                   const float *add, float *y,
+                                   int N, int C_in, int C_out, const int in_hw[2],
+                                   const int k_hw[2], int groups, const int stride[2],
+                                   const int padding[2], const int output_padding[2],
+                                   const int dilation[2], ct_dtype dtype,
+                                   void *workspace, size_t ws_bytes, void *stream);
 
 /* Fused ConvTranspose3d + add + x*hardswish(x) ([l2_p26]):
  *     t = convT(x) + bias + add;  y = t * (t * clamp(t + 3, 0, 6) / 6).
@@ -148,14 +177,18 @@ ct_status ct_forward_3d_noalloc(const void *x, const void *w, const float *bias,
                                 const int output_padding[3], const int dilation[3],
                                 ct_dtype dtype, void *stream);
 
-/* Name of the kernel family the 1-D / 3-D / fused call with these arguments
+/* Name of the kernel family the 1-D / 2-D / 3-D / fused call with these arguments
  * would launch when given the workspace ct_workspace_size_* reports
  * ("gather_generic", "phase1d_f32", "tc1d_tf32x3", "phase3d_f32", "tc3d_tf32x3",
  * "tc3dg_tf32x3" -- 32 input channels in 1, 2 or 4 groups -- or "umma_bf16"),
  * or NULL if the arguments are invalid.  Host only; launches
- * nothing.  `fused` selects the add + hardswish variant for the 3-D query. */
+ * nothing.  `fused` selects the add + hardswish variant for the 2-D and 3-D queries. */
 const char *ct_path_1d(int N, int C_in, int C_out, int L_in, int k, int groups, int stride,
                        int padding, int output_padding, int dilation, ct_dtype dtype);
+const char *ct_path_2d(int N, int C_in, int C_out, const int in_hw[2], const int k_hw[2],
+                       int groups, const int stride[2], const int padding[2],
+                       const int output_padding[2], const int dilation[2], ct_dtype dtype,
+                       int fused);
 const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
                        int groups, const int stride[3], const int padding[3],
                        const int output_padding[3], const int dilation[3], ct_dtype dtype,

@@ -63,6 +63,11 @@ def run_gpu(c, t, dev="cuda:0", inplace_add=False):
     kw = kwargs(c)
     if c["nd"] == 1:
         y = ct.conv_transpose1d(x, w, b, **kw)
+    elif c["nd"] == 2:
+        if c["add"]:
+            y = ct.conv_transpose2d_add_hswish(x, w, b, a, out=a if inplace_add else None, **kw)
+        else:
+            y = ct.conv_transpose2d(x, w, b, **kw)
     elif c["add"]:
         y = ct.conv_transpose3d_add_hswish(x, w, b, a, out=a if inplace_add else None, **kw)
     else:

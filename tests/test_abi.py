@@ -139,6 +139,37 @@ def test_path_selection(lib):
         ct.ct_set_path_override(0)
 
 
+def test_path_selection_2d(lib):
+    """A 2-D call is the 3-D operator with a unit D dimension: dense stride-2
+    layers take the tensor-core kernels, the rest the generic kernel."""
+    dense = (32, 64, 64, (128, 128), (4, 4), 1, (2, 2), (1, 1), (0, 0), (1, 1))
+    assert ct.ct_path_2d(*dense, ct.CT_F32) == "tc3d_tf32x3"
+    assert ct.ct_path_2d(*dense, ct.CT_F32, fused=True) == "tc3d_tf32x3"
+    assert ct.ct_path_2d(*dense, ct.CT_BF16) == "umma_bf16"
+    # kH * kW = 4: the bf16 weight repack needs multiples of 8 -> generic
+    assert ct.ct_path_2d(1, 64, 32, (4, 8), (2, 2), 1, (2, 2), (0, 0), (0, 0), (1, 1),
+                         ct.CT_BF16) == "gather_generic"
+    assert ct.ct_path_2d(2, 6, 4, (5, 7), (3, 2), 2, (2, 3), (1, 0), (1, 2), (1, 1),
+                         ct.CT_F32) == "gather_generic"
+    ct.ct_set_path_override(2)
+    try:
+        assert ct.ct_path_2d(*dense, ct.CT_F32) == "gather_generic"
+    finally:
+        ct.ct_set_path_override(0)
+    assert ct.ct_path_2d(1, 4, 8, (0, 4), (3, 3), 1, (2, 2), (1, 1), (0, 0), (1, 1), ct.CT_F32) is None
+    with pytest.raises(ct.CTError) as e:
+        ct.ct_workspace_size_2d(1, 4, 8, (4, 4), (3, 3), 1, (2, 2), (1, 1), (2, 0), (1, 1), ct.CT_F32)
+    assert e.value.code == ct.CT_ERR_SHAPE
+    # the same layer through the 2-D and the 3-D entry (unit D) needs the same workspace
+    n2 = ct.ct_workspace_size_2d(*dense, ct.CT_F32)
+    n3 = ct.ct_workspace_size_3d(32, 64, 64, (1, 128, 128), (1, 4, 4), 1, (1, 2, 2), (0, 1, 1),
+                                 (0, 0, 0), (1, 1, 1), ct.CT_F32)
+    assert n2 == n3 >= 2 * 32 * 64 * 128 * 128 * 4
+    nb2 = ct.ct_workspace_size_2d(*dense, ct.CT_BF16)
+    # channels-last bf16 x plus the weight panels: 4 phases x 2 x 2 taps per phase
+    assert nb2 >= 32 * 64 * 128 * 128 * 2 + 4 * 4 * 64 * 64 * 2
+
+
 def test_workspace_sizes(lib):
     assert ct.ct_workspace_size_1d(16, 32, 64, 131072, 3, 1, 2, 1, 0, 2, ct.CT_F32) == 0
     # FP32 3-D tensor-core path: channels-last hi and lo copies of x, hi and lo

@@ -38,16 +38,21 @@ def path_of(c):
     if c["nd"] == 1:
         return ct.ct_path_1d(c["N"], c["C_in"], c["C_out"], c["L"][0], c["K"][0], c["G"], c["S"][0],
                              c["P"][0], c["OP"][0], c["DL"][0], dt)
+    if c["nd"] == 2:
+        return ct.ct_path_2d(c["N"], c["C_in"], c["C_out"], c["L"], c["K"], c["G"], c["S"], c["P"],
+                             c["OP"], c["DL"], dt, c["add"])
     return ct.ct_path_3d(c["N"], c["C_in"], c["C_out"], c["L"], c["K"], c["G"], c["S"], c["P"],
                          c["OP"], c["DL"], dt, c["add"])
 
 
 # Reduced-batch versions of every workload, compared element by element.  The
-# bf16 workload is also reduced in space (8^3 input) so the scatter oracle
-# finishes in seconds; its full spatial size is covered by the sampled test.
+# bf16 workloads are also reduced in space (8^3 and 32^2 inputs) so the scatter
+# oracle finishes in seconds; their full spatial size is covered by the sampled
+# test.
 REDUCED = {"convT1d_tiny": dict(N=2), "convT1d_L131072": dict(N=1),
            "convT3d_grouped": dict(N=2), "convT3d_add_hswish": dict(N=2),
-           "convT3d_bf16_dense": dict(N=1, L=[8, 8, 8])}
+           "convT3d_bf16_dense": dict(N=1, L=[8, 8, 8]), "convT2d_f32": dict(N=1),
+           "convT2d_bf16_dense": dict(N=1, L=[32, 32])}
 
 
 @pytest.mark.parametrize("name", CONFIGS)
@@ -69,6 +74,8 @@ def test_config_integer_exact(name):
     c = cc.case_from_config(name, N=1)
     if name == "convT3d_bf16_dense":
         c["L"] = [8, 8, 8]
+    elif name == "convT2d_bf16_dense":
+        c["L"] = [32, 32]
     t = cc.make_inputs(c, seed=200 + CONFIGS.index(name), int_range=3)
     y = cc.run_gpu(c, t).cpu().numpy()
     ref = cc.run_oracle(c, t)
@@ -124,7 +131,8 @@ def _random_cases(n, seed, nd_choices=(1, 3), scale=1):
 @pytest.mark.parametrize("forced_generic", [False, True])
 def test_random_small_shapes(forced_generic):
     import transposed_convolution_convtranspose_gb300 as ct
-    cases = _random_cases(80, seed=31) + _random_cases(20, seed=32, scale=4)
+    cases = (_random_cases(80, seed=31) + _random_cases(20, seed=32, scale=4)
+             + _random_cases(30, seed=33, nd_choices=(2,)))
     ct.ct_set_path_override(1 if forced_generic else 0)
     try:
         for k, c in enumerate(cases):
@@ -235,6 +243,86 @@ def test_fp32_3d_grouped_tensor_core_shapes(k):
         ti = cc.make_inputs(c, seed=950 + k, int_range=3)
         yi = cc.run_gpu(c, ti).cpu().numpy()
         assert np.array_equal(yi.astype(np.float64), cc.run_oracle(c, ti)), "tc3dg integer case %d" % k
+
+
+# ConvTranspose2d: the 3-D operator with a unit D dimension, through the same
+# kernels.  FP32 dense shapes for the tensor-core path (plain and fused): C_in
+# 32 and 64, C_out 16..128, kernel extents 2..4 mixed across H and W, padding
+# even and odd, an odd H output (ragged qh block), W outputs from 8 to 256
+# (tiles of 16 qh rows down to one qh row of 128 qw) and a case with several
+# units per persistent CTA.
+TC2D = [
+    dict(N=2, C_in=32, C_out=64, L=[8, 16], K=[4, 4], P=[1, 1], OP=[0, 0]),
+    dict(N=1, C_in=64, C_out=32, L=[5, 8], K=[3, 3], P=[1, 1], OP=[1, 1]),
+    dict(N=1, C_in=32, C_out=16, L=[3, 4], K=[2, 3], P=[0, 1], OP=[1, 1]),
+    dict(N=1, C_in=32, C_out=128, L=[4, 64], K=[4, 4], P=[1, 1], OP=[0, 0]),
+    dict(N=3, C_in=32, C_out=48, L=[7, 128], K=[3, 3], P=[1, 1], OP=[1, 1]),
+    dict(N=8, C_in=32, C_out=32, L=[32, 32], K=[4, 4], P=[1, 1], OP=[0, 0]),
+]
+
+
+@pytest.mark.parametrize("add", [False, True])
+@pytest.mark.parametrize("k", range(len(TC2D)))
+def test_fp32_2d_tensor_core_shapes(k, add):
+    c = dict(nd=2, G=1, S=[2, 2], DL=[1, 1], bias=bool(k % 2 == 0), add=add, dtype="f32", **TC2D[k])
+    assert path_of(c) == "tc3d_tf32x3", (c, path_of(c))
+    t = cc.make_inputs(c, seed=1000 + k + (50 if add else 0))
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), "f32", "2-D tc case %d add=%s %r" % (k, add, c))
+    if k < 2 and not add:
+        ti = cc.make_inputs(c, seed=1100 + k, int_range=3)
+        yi = cc.run_gpu(c, ti).cpu().numpy()
+        assert np.array_equal(yi.astype(np.float64), cc.run_oracle(c, ti)), "2-D tc integer case %d" % k
+
+
+# bf16 ConvTranspose2d on the bf16 tensor-core path: kernel extents 4 and 8
+# (the weight repack moves 16-byte pieces, so kH*kW must be a multiple of 8),
+# C_out 16..256, odd H output, padding 0..3, several tiles per CTA.
+UMMA2D = [
+    dict(N=1, C_in=64, C_out=64, L=[8, 16], K=[4, 4], P=[1, 1], OP=[0, 0]),
+    dict(N=2, C_in=128, C_out=128, L=[5, 12], K=[4, 4], P=[1, 1], OP=[1, 0]),
+    dict(N=1, C_in=64, C_out=256, L=[4, 8], K=[4, 4], P=[1, 1], OP=[0, 0]),
+    dict(N=1, C_in=64, C_out=32, L=[3, 4], K=[8, 8], P=[3, 3], OP=[0, 0]),
+    dict(N=4, C_in=64, C_out=16, L=[32, 32], K=[4, 4], P=[0, 0], OP=[0, 0]),
+]
+
+
+@pytest.mark.parametrize("k", range(len(UMMA2D)))
+def test_bf16_2d_tensor_core_shapes(k):
+    c = dict(nd=2, G=1, S=[2, 2], DL=[1, 1], bias=bool(k % 2 == 0), add=False, dtype="bf16",
+             **UMMA2D[k])
+    assert path_of(c) == "umma_bf16", (c, path_of(c))
+    t = cc.make_inputs(c, seed=1200 + k)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), "bf16", "2-D umma case %d %r" % (k, c))
+    if k == 0:
+        ti = cc.make_inputs(c, seed=1250, int_range=3)
+        yi = cc.run_gpu(c, ti).cpu().numpy()
+        assert np.array_equal(yi.astype(np.float64), cc.run_oracle(c, ti)), "2-D umma integer case"
+
+
+# 2-D shapes outside the tuned kernels' range take the generic kernel: groups,
+# stride 3 and 1, dilation, a bf16 kernel of extent 2, the fused epilogue on
+# a grouped layer.
+GEN2D = [
+    dict(N=2, C_in=6, C_out=4, G=2, L=[5, 7], K=[3, 2], S=[2, 3], P=[1, 0], OP=[1, 2], DL=[1, 1],
+         dtype="f32", add=False),
+    dict(N=1, C_in=4, C_out=8, G=1, L=[6, 5], K=[3, 3], S=[1, 2], P=[2, 1], OP=[0, 1], DL=[2, 1],
+         dtype="f32", add=False),
+    dict(N=1, C_in=64, C_out=32, G=1, L=[4, 8], K=[2, 2], S=[2, 2], P=[0, 0], OP=[0, 0], DL=[1, 1],
+         dtype="bf16", add=False),
+    dict(N=2, C_in=8, C_out=8, G=4, L=[4, 6], K=[3, 3], S=[2, 2], P=[1, 1], OP=[1, 1], DL=[1, 1],
+         dtype="f32", add=True),
+]
+
+
+@pytest.mark.parametrize("k", range(len(GEN2D)))
+def test_2d_generic_shapes(k):
+    c = dict(nd=2, bias=True, **GEN2D[k])
+    assert path_of(c) == "gather_generic", (c, path_of(c))
+    t = cc.make_inputs(c, seed=1300 + k)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), c["dtype"], "2-D generic case %d %r" % (k, c))
 
 
 def test_fp32_3d_without_workspace_takes_ffma():

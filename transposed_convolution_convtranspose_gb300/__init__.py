@@ -26,8 +26,9 @@ CT_STATUS = {0: "CT_OK", 1: "CT_ERR_ARG", 2: "CT_ERR_SHAPE", 3: "CT_ERR_ALIGN",
              4: "CT_ERR_WORKSPACE", 5: "CT_ERR_UNSUPPORTED", 6: "CT_ERR_CUDA",
              7: "CT_ERR_DEVICE_TIMEOUT"}
 
-EXPORTED = ["ct_out_len", "ct_workspace_size_1d", "ct_workspace_size_3d", "ct_forward_1d",
-            "ct_forward_3d", "ct_forward_3d_add_hswish", "ct_path_1d", "ct_path_3d",
+EXPORTED = ["ct_out_len", "ct_workspace_size_1d", "ct_workspace_size_2d", "ct_workspace_size_3d",
+            "ct_forward_1d", "ct_forward_2d", "ct_forward_2d_add_hswish", "ct_forward_3d",
+            "ct_forward_3d_add_hswish", "ct_path_1d", "ct_path_2d", "ct_path_3d",
             "ct_set_path_override", "ct_status_str", "ct_last_device_error",
             "ct_forward_3d_noalloc", "ct_selftest_wait_timeout"]
 
@@ -48,6 +49,7 @@ _load_error = None
 
 _I = ctypes.c_int
 _P = ctypes.c_void_p
+_I2 = ctypes.c_int * 2
 _I3 = ctypes.c_int * 3
 
 
@@ -59,6 +61,17 @@ def _setup(lib):
     lib.ct_workspace_size_3d.restype = _I
     lib.ct_workspace_size_3d.argtypes = [_I, _I, _I, _I3, _I3, _I, _I3, _I3, _I3, _I3, _I,
                                          ctypes.POINTER(ctypes.c_size_t)]
+    lib.ct_workspace_size_2d.restype = _I
+    lib.ct_workspace_size_2d.argtypes = [_I, _I, _I, _I2, _I2, _I, _I2, _I2, _I2, _I2, _I,
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.ct_forward_2d.restype = _I
+    lib.ct_forward_2d.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I2, _I2, _I, _I2, _I2, _I2, _I2,
+                                  _I, _P, ctypes.c_size_t, _P]
+    lib.ct_forward_2d_add_hswish.restype = _I
+    lib.ct_forward_2d_add_hswish.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I2, _I2, _I, _I2,
+                                             _I2, _I2, _I2, _I, _P, ctypes.c_size_t, _P]
+    lib.ct_path_2d.restype = ctypes.c_char_p
+    lib.ct_path_2d.argtypes = [_I, _I, _I, _I2, _I2, _I, _I2, _I2, _I2, _I2, _I, _I]
     lib.ct_forward_1d.restype = _I
     lib.ct_forward_1d.argtypes = [_P, _P, _P, _P] + [_I] * 10 + [_I, _P, ctypes.c_size_t, _P]
     lib.ct_forward_3d.restype = _I
@@ -120,6 +133,13 @@ def _stream(s):
     return s.cuda_stream or None  # torch.cuda.Stream
 
 
+def _i2(v):
+    v = tuple(int(t) for t in v)
+    if len(v) != 2:
+        raise ValueError("expected 2 values (H, W)")
+    return _I2(*v)
+
+
 def _i3(v):
     v = tuple(int(t) for t in v)
     if len(v) != 3:
@@ -164,6 +184,35 @@ def ct_forward_1d(x, w, bias, y, N, C_in, C_out, L_in, k, groups, stride, paddin
            "ct_forward_1d")
 
 
+def ct_workspace_size_2d(N, C_in, C_out, in_hw, k_hw, groups, stride, padding, output_padding,
+                         dilation, dtype):
+    n = ctypes.c_size_t(0)
+    _check(load().ct_workspace_size_2d(N, C_in, C_out, _i2(in_hw), _i2(k_hw), groups, _i2(stride),
+                                       _i2(padding), _i2(output_padding), _i2(dilation), dtype,
+                                       ctypes.byref(n)),
+           "ct_workspace_size_2d")
+    return int(n.value)
+
+
+def ct_forward_2d(x, w, bias, y, N, C_in, C_out, in_hw, k_hw, groups, stride, padding,
+                  output_padding, dilation, dtype, workspace=None, ws_bytes=0, stream=None):
+    _check(load().ct_forward_2d(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), N, C_in, C_out,
+                                _i2(in_hw), _i2(k_hw), groups, _i2(stride), _i2(padding),
+                                _i2(output_padding), _i2(dilation), dtype, _ptr(workspace),
+                                ws_bytes, _stream(stream)),
+           "ct_forward_2d")
+
+
+def ct_forward_2d_add_hswish(x, w, bias, add, y, N, C_in, C_out, in_hw, k_hw, groups, stride,
+                             padding, output_padding, dilation, dtype, workspace=None, ws_bytes=0,
+                             stream=None):
+    _check(load().ct_forward_2d_add_hswish(_ptr(x), _ptr(w), _ptr(bias), _ptr(add), _ptr(y), N,
+                                           C_in, C_out, _i2(in_hw), _i2(k_hw), groups, _i2(stride),
+                                           _i2(padding), _i2(output_padding), _i2(dilation), dtype,
+                                           _ptr(workspace), ws_bytes, _stream(stream)),
+           "ct_forward_2d_add_hswish")
+
+
 def ct_forward_3d(x, w, bias, y, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding,
                   output_padding, dilation, dtype, workspace=None, ws_bytes=0, stream=None):
     _check(load().ct_forward_3d(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), N, C_in, C_out,
@@ -197,6 +246,13 @@ def ct_forward_3d_noalloc(x, w, bias, y, N, C_in, C_out, in_dhw, k_dhw, groups, 
 def ct_path_1d(N, C_in, C_out, L_in, k, groups, stride, padding, output_padding, dilation, dtype):
     r = load().ct_path_1d(N, C_in, C_out, L_in, k, groups, stride, padding, output_padding,
                           dilation, dtype)
+    return None if r is None else r.decode()
+
+
+def ct_path_2d(N, C_in, C_out, in_hw, k_hw, groups, stride, padding, output_padding, dilation,
+               dtype, fused=False):
+    r = load().ct_path_2d(N, C_in, C_out, _i2(in_hw), _i2(k_hw), groups, _i2(stride),
+                          _i2(padding), _i2(output_padding), _i2(dilation), dtype, int(bool(fused)))
     return None if r is None else r.decode()
 
 
@@ -328,5 +384,61 @@ def conv_transpose3d_add_hswish(x, w, bias, add, stride=1, padding=0, output_pad
     nb = ct_workspace_size_3d(N, C_in, C_out, L, K, groups, S, P, OP, D, dt)
     ws = _workspace(nb, x.device)
     ct_forward_3d_add_hswish(x, w, bias, add, y, N, C_in, C_out, L, K, groups, S, P, OP, D, dt,
+                             ws, nb, torch.cuda.current_stream(x.device))
+    return y
+
+
+def _pair(v):
+    if isinstance(v, int):
+        return (v, v)
+    v = tuple(int(t) for t in v)
+    if len(v) != 2:
+        raise ValueError("expected an int or 2 values")
+    return v
+
+
+def _out2(x, w, stride, padding, output_padding, dilation):
+    S, P, OP, D = _pair(stride), _pair(padding), _pair(output_padding), _pair(dilation)
+    K = tuple(w.shape[2:])
+    L = tuple(x.shape[2:])
+    Lo = tuple(ct_out_len(L[i], K[i], S[i], P[i], OP[i], D[i]) for i in range(2))
+    if min(Lo) < 1:
+        raise CTError(2, "conv_transpose2d")
+    return S, P, OP, D, K, L, Lo
+
+
+def conv_transpose2d(x, w, bias=None, stride=1, padding=0, output_padding=0, dilation=1,
+                     groups=1, out=None):
+    import torch
+    for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (out, "out")):
+        _need(t, nm)
+    N, C_in = x.shape[:2]
+    C_out = w.shape[1] * groups
+    dt = _dtype_code(x)
+    S, P, OP, D, K, L, Lo = _out2(x, w, stride, padding, output_padding, dilation)
+    y = out if out is not None else torch.empty((N, C_out) + Lo, dtype=torch.float32,
+                                                device=x.device)
+    nb = ct_workspace_size_2d(N, C_in, C_out, L, K, groups, S, P, OP, D, dt)
+    ws = _workspace(nb, x.device)
+    ct_forward_2d(x, w, bias, y, N, C_in, C_out, L, K, groups, S, P, OP, D, dt, ws, nb,
+                  torch.cuda.current_stream(x.device))
+    return y
+
+
+def conv_transpose2d_add_hswish(x, w, bias, add, stride=1, padding=0, output_padding=0,
+                                dilation=1, groups=1, out=None):
+    import torch
+    for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (add, "add"), (out, "out")):
+        _need(t, nm)
+    N, C_in = x.shape[:2]
+    C_out = w.shape[1] * groups
+    dt = _dtype_code(x)
+    S, P, OP, D, K, L, Lo = _out2(x, w, stride, padding, output_padding, dilation)
+    if tuple(add.shape) != (N, C_out) + Lo or add.dtype != torch.float32:
+        raise CTError(1, "conv_transpose2d_add_hswish: add must be fp32 with the output's shape")
+    y = out if out is not None else torch.empty_like(add)
+    nb = ct_workspace_size_2d(N, C_in, C_out, L, K, groups, S, P, OP, D, dt)
+    ws = _workspace(nb, x.device)
+    ct_forward_2d_add_hswish(x, w, bias, add, y, N, C_in, C_out, L, K, groups, S, P, OP, D, dt,
                              ws, nb, torch.cuda.current_stream(x.device))
     return y

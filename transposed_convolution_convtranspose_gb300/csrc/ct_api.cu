@@ -66,7 +66,7 @@ ct_status make_problem(int nd, int N, int C_in, int C_out, const int *Li, const 
                        const int *S, const int *P, const int *OP, const int *DL, ct_dtype dtype,
                        bool has_bias, bool has_add, Problem *pb)
 {
-    if (nd != 1 && nd != 3) return CT_ERR_ARG;
+    if (nd < 1 || nd > 3) return CT_ERR_ARG;
     if (dtype != CT_F32 && dtype != CT_BF16) return CT_ERR_ARG;
     if (N < 0 || C_in < 1 || C_out < 1 || G < 1) return CT_ERR_ARG;
     if (C_in % G || C_out % G) return CT_ERR_SHAPE;
@@ -108,15 +108,16 @@ Path choose_path(const Problem &pb, const Args *a)
         // the 3-D tensor-core path works in the caller's workspace: a call without
         // enough of it takes the FFMA kernel (a query without arguments, a == NULL,
         // reports the tensor-core path and its workspace size)
-        if (ov != 2 && pb.nd == 3 && tc3d_supported(pb, a) &&
+        // a 2-D problem is a 3-D one with a unit D dimension (same layouts)
+        if (ov != 2 && pb.nd >= 2 && tc3d_supported(pb, a) &&
             (!a || (a->ws && ((uintptr_t)a->ws % 256) == 0 && a->ws_bytes >= tc3d_workspace_bytes(pb))))
             return Path::Tc3d;
-        if (ov != 2 && pb.nd == 3 && tc3dg_supported(pb, a) &&
+        if (ov != 2 && pb.nd >= 2 && tc3dg_supported(pb, a) &&
             (!a || (a->ws && ((uintptr_t)a->ws % 256) == 0 && a->ws_bytes >= tc3dg_workspace_bytes(pb))))
             return Path::Tc3dg;
-        if (pb.nd == 3 && phase3d_supported(pb, a)) return Path::Phase3d;
+        if (pb.nd >= 2 && phase3d_supported(pb, a)) return Path::Phase3d;
     } else {
-        if (pb.nd == 3 && umma_supported(pb, a)) return Path::Umma;
+        if (pb.nd >= 2 && umma_supported(pb, a)) return Path::Umma;
     }
     return Path::Generic;
 }
@@ -241,6 +242,21 @@ ct_status ct_workspace_size_3d(int N, int C_in, int C_out, const int in_dhw[3],
     return CT_OK;
 }
 
+ct_status ct_workspace_size_2d(int N, int C_in, int C_out, const int in_hw[2], const int k_hw[2],
+                               int groups, const int stride[2], const int padding[2],
+                               const int output_padding[2], const int dilation[2], ct_dtype dtype,
+                               size_t *bytes)
+{
+    if (!bytes || !in_hw || !k_hw || !stride || !padding || !output_padding || !dilation)
+        return CT_ERR_ARG;
+    Problem pb;
+    ct_status st = make_problem(2, N, C_in, C_out, in_hw, k_hw, groups, stride, padding,
+                                output_padding, dilation, dtype, false, false, &pb);
+    if (st != CT_OK) return st;
+    *bytes = workspace_bytes(pb);
+    return CT_OK;
+}
+
 ct_status ct_forward_1d(const void *x, const void *w, const float *bias, float *y,
                         int N, int C_in, int C_out, int L_in, int k, int groups,
                         int stride, int padding, int output_padding, int dilation,
@@ -289,6 +305,41 @@ ct_status ct_forward_3d_add_hswish(const void *x, const void *w, const float *bi
     return run(pb, a);
 }
 
+ct_status ct_forward_2d(const void *x, const void *w, const float *bias, float *y,
+                        int N, int C_in, int C_out, const int in_hw[2], const int k_hw[2],
+                        int groups, const int stride[2], const int padding[2],
+                        const int output_padding[2], const int dilation[2],
+                        ct_dtype dtype, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!in_hw || !k_hw || !stride || !padding || !output_padding || !dilation)
+        return CT_ERR_ARG;
+    Problem pb;
+    ct_status st = make_problem(2, N, C_in, C_out, in_hw, k_hw, groups, stride, padding,
+                                output_padding, dilation, dtype, bias != nullptr, false, &pb);
+    if (st != CT_OK) return st;
+    Args a{x, w, bias, nullptr, y, workspace, ws_bytes, (cudaStream_t)stream};
+    return run(pb, a);
+}
+
+ct_status ct_forward_2d_add_hswish(const void *x, const void *w, const float *bias,
+                                   const float *add, float *y,
+                                   int N, int C_in, int C_out, const int in_hw[2],
+                                   const int k_hw[2], int groups, const int stride[2],
+                                   const int padding[2], const int output_padding[2],
+                                   const int dilation[2], ct_dtype dtype,
+                                   void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!in_hw || !k_hw || !stride || !padding || !output_padding || !dilation)
+        return CT_ERR_ARG;
+    if (!add) return CT_ERR_ARG;
+    Problem pb;
+    ct_status st = make_problem(2, N, C_in, C_out, in_hw, k_hw, groups, stride, padding,
+                                output_padding, dilation, dtype, bias != nullptr, true, &pb);
+    if (st != CT_OK) return st;
+    Args a{x, w, bias, add, y, workspace, ws_bytes, (cudaStream_t)stream};
+    return run(pb, a);
+}
+
 const char *ct_path_1d(int N, int C_in, int C_out, int L_in, int k, int groups, int stride,
                        int padding, int output_padding, int dilation, ct_dtype dtype)
 {
@@ -307,6 +358,19 @@ const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const in
     if (!in_dhw || !k_dhw || !stride || !padding || !output_padding || !dilation) return nullptr;
     Problem pb;
     if (make_problem(3, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding, output_padding,
+                     dilation, dtype, false, fused != 0, &pb) != CT_OK)
+        return nullptr;
+    return path_name(choose_path(pb, nullptr));
+}
+
+const char *ct_path_2d(int N, int C_in, int C_out, const int in_hw[2], const int k_hw[2],
+                       int groups, const int stride[2], const int padding[2],
+                       const int output_padding[2], const int dilation[2], ct_dtype dtype,
+                       int fused)
+{
+    if (!in_hw || !k_hw || !stride || !padding || !output_padding || !dilation) return nullptr;
+    Problem pb;
+    if (make_problem(2, N, C_in, C_out, in_hw, k_hw, groups, stride, padding, output_padding,
                      dilation, dtype, false, fused != 0, &pb) != CT_OK)
         return nullptr;
     return path_name(choose_path(pb, nullptr));

@@ -12,7 +12,7 @@ namespace ct {
 // One validated forward problem.  Spatial dims are right-aligned into three
 // slots (D, H, W); a 1-D problem has D = H = 1 with unit kernel/stride.
 struct Problem {
-    int nd;                                  // 1 or 3 (as called)
+    int nd;                                  // 1, 2 or 3 (as called; dims right-aligned in 3 slots)
     int N, C_in, C_out, G, Cig, Cog;         // Cig = C_in/G, Cog = C_out/G
     int Li[3], K[3], S[3], P[3], OP[3], DL[3], Lo[3];
     ct_dtype dtype;

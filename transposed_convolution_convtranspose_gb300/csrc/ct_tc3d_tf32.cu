@@ -106,6 +106,7 @@ struct Run {
 
 struct T3Params {
     int N, C_in, C_out;
+    int SD;                      // D stride: 2, or 1 for a unit D dimension (a 2-D problem)
     int Lo0, Lo1, Lo2;
     int QD, QH, QW, MH, n_qhb;
     int n_kb;                    // C_in / 32
@@ -239,7 +240,8 @@ prep_kernel(const float *__restrict__ x, float *__restrict__ xhi, uint16_t *__re
 }
 
 // ---- GEMM kernel ----------------------------------------------------------------
-// unit -> (n, qd, qh block, rD).  The two D residues of one position block are
+// unit -> (n, qd, qh block, rD); a unit D dimension (stride 1) has the one residue
+// 0 and the unit index is (n, qd, qh block).  The two D residues of one position block are
 // neighbours (their shared A tiles are reused from L2).  Units are dealt to the
 // CTAs round-robin; rD = 1 has more taps than rD = 0 when the kernel extent is
 // odd, and with an even grid a CTA would see one residue only, so the residue
@@ -252,8 +254,11 @@ struct UnitCoord {
 __device__ __forceinline__ UnitCoord unit_coord(int u, const T3Params &p)
 {
     UnitCoord c;
-    c.rd = (u ^ (u / (int)gridDim.x)) & 1;
-    u >>= 1;
+    c.rd = 0;
+    if (p.SD == 2) {
+        c.rd = (u ^ (u / (int)gridDim.x)) & 1;
+        u >>= 1;
+    }
     c.qhb = u % p.n_qhb;
     u /= p.n_qhb;
     c.qd = u % p.QD;
@@ -462,7 +467,7 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
             if (ADD) {
                 const UnitCoord v = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
                 dev::mbar_arrive_expect_tx(&e_full[b], kEChunk);
-                dev::tma_load_4d(sE + (size_t)b * kEChunk, &tmAdd, &e_full[b], 0, 2 * v.qhb * p.MH, 2 * v.qd + v.rd,
+                dev::tma_load_4d(sE + (size_t)b * kEChunk, &tmAdd, &e_full[b], 0, 2 * v.qhb * p.MH, p.SD * v.qd + v.rd,
                                  v.n * C_out + (gc % nchunk) * 16);
             } else {
                 dev::mbar_arrive(&e_full[b]);
@@ -480,7 +485,7 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
                 }
                 const UnitCoord u = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
                 // rows and planes past the output are clipped by the store
-                dev::tma_store_4d(&tmY, sE + (size_t)(gc % NE) * kEChunk, 0, 2 * u.qhb * p.MH, 2 * u.qd + u.rd,
+                dev::tma_store_4d(&tmY, sE + (size_t)(gc % NE) * kEChunk, 0, 2 * u.qhb * p.MH, p.SD * u.qd + u.rd,
                                   u.n * C_out + (gc % nchunk) * 16);
                 dev::bulk_commit();
                 dev::bulk_wait_read<1>();               // chunk gc - 1's store has read its buffer
@@ -595,8 +600,13 @@ int dim_taps(int K, int P, int r, int *k_out, int *d_out)
 
 bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
 {
-    if (pb.nd != 3 || pb.dtype != CT_F32 || pb.G != 1) return false;
-    for (int d = 0; d < 3; ++d)
+    if ((pb.nd != 3 && pb.nd != 2) || pb.dtype != CT_F32 || pb.G != 1) return false;
+    // D has stride 2 like H and W, or is a unit dimension (extent 1, stride 1, no
+    // padding: a 2-D problem, or a 3-D one that maps planes to planes), whose
+    // single residue takes tap 0 at offset 0
+    const int SD = pb.S[0];
+    if (SD == 1 && (pb.K[0] != 1 || pb.P[0] != 0 || pb.OP[0] != 0)) return false;
+    for (int d = SD == 1 ? 1 : 0; d < 3; ++d)
         if (pb.S[d] != 2 || pb.DL[d] != 1 || pb.K[d] < 2 || pb.K[d] > 4) return false;
     if (pb.C_in % CK != 0 || pb.C_out % 16 != 0 || pb.C_out < 16 || pb.C_out > 128) return false;
     // the epilogue moves whole output rows by TMA: 16-byte rows and bases
@@ -606,15 +616,16 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     T3Params p;
     memset(&p, 0, sizeof(p));
     p.N = pb.N; p.C_in = pb.C_in; p.C_out = pb.C_out;
+    p.SD = SD;
     p.Lo0 = pb.Lo[0]; p.Lo1 = pb.Lo[1]; p.Lo2 = pb.Lo[2];
     p.QW = p.Lo2 / 2;
     if (p.QW > BM || BM % p.QW != 0) return false;
     p.MH = BM / p.QW;
-    p.QD = (p.Lo0 + 1) / 2;
+    p.QD = (p.Lo0 + SD - 1) / SD;
     p.QH = (p.Lo1 + 1) / 2;
     p.n_qhb = (p.QH + p.MH - 1) / p.MH;
     p.n_kb = pb.C_in / CK;
-    const int64_t units = (int64_t)pb.N * p.QD * p.n_qhb * 2;
+    const int64_t units = (int64_t)pb.N * p.QD * p.n_qhb * SD;
     if (units > 0x7fffffff || units == 0) return false;
     p.nunits = (int)units;
 
@@ -622,6 +633,11 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     int tk[3][2][4], td[3][2][4], nt[3][2];
     for (int d = 0; d < 3; ++d)
         for (int r = 0; r < 2; ++r) {
+            if (d == 0 && SD == 1) {
+                nt[0][r] = r == 0 ? 1 : 0;
+                tk[0][r][0] = td[0][r][0] = 0;
+                continue;
+            }
             nt[d][r] = dim_taps(pb.K[d], pb.P[d], r, tk[d][r], td[d][r]);
             if (nt[d][r] < 1) return false;       // every phase must receive a tap
         }
@@ -643,7 +659,7 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     WPanels wq;
     memset(&wq, 0, sizeof(wq));
     int nblk = 0;
-    for (int rd = 0; rd < 2; ++rd) {
+    for (int rd = 0; rd < SD; ++rd) {
         int ne = 0, nr = 0;
         uint32_t init = 0;                        // accumulators written by earlier runs
         for (int jd = 0; jd < nt[0][rd]; ++jd)
@@ -819,7 +835,7 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.nunits) grid = p.nunits;
-    if (grid > 1 && (grid & 1)) --grid;   // an even grid: the residue flip of unit_coord permutes units
+    if (p.SD == 2 && grid > 1 && (grid & 1)) --grid;   // an even grid: the residue flip of unit_coord permutes units
     if (a.add)
         return launch_dependent(tc3d_tf32_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXh,
                                 tmXc, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);

@@ -92,7 +92,8 @@ struct UParams {
     int N, C_in, C_out;
     int Lo0, Lo1, Lo2;
     int QD, QH, QW, n_qhb, n_qwp;   // n_qwp: pairs of 8-column qw blocks
-    int nT;                  // taps per dimension and class (kernel extent / 2)
+    int nT;                  // taps per class of H and W (kernel extent / 2)
+    int SD, nTD;             // D: stride 2 and nT taps, or a unit dimension (stride 1, one tap)
     int n_kb;                // C_in / BK
     int ntiles;
     int nacc;                // TMEM accumulators = MMA issuers = tiles per pair (1 or 2)
@@ -121,7 +122,11 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const UParams &p)
 {
     TileCoord c;
     c.rH = t & 1; t >>= 1;
-    c.rD = t & 1; t >>= 1;
+    c.rD = 0;
+    if (p.SD == 2) {
+        c.rD = t & 1;
+        t >>= 1;
+    }
     c.qwp = t % p.n_qwp; t /= p.n_qwp;
     c.qhb = t % p.n_qhb; t /= p.n_qhb;
     c.qd = t % p.QD; t /= p.QD;
@@ -194,8 +199,8 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     // A unit is a pair of tiles (two 8-row qh blocks) when two accumulators fit:
     // both issuers consume every stage, issuer j computing tile j from the shared
     // input window (8 rows further down for tile 1) and the shared weight panel.
-    const int nT = p.nT, n_kb = p.n_kb;
-    const int spa = 2 * nT * n_kb;
+    const int nT = p.nT, nTD = p.nTD, n_kb = p.n_kb;
+    const int spa = 2 * nTD * n_kb;
     const int spb = spa * nT * (nT / p.wg);
     const uint32_t b_slot = (uint32_t)p.wg * p.b_bytes;
     const int ni = p.nacc;
@@ -227,7 +232,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     break;
                 }
                 if (isA) {
-                    const int wr = i / (nT * n_kb), r = i % (nT * n_kb);
+                    const int wr = i / (nTD * n_kb), r = i % (nTD * n_kb);
                     const int jd = r / n_kb, kb = r % n_kb;
                     dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(p.hspan * p.wspan) * 128u);
                     // x_t viewed as (C, W, H, D, N): W phase wr's window from
@@ -243,9 +248,9 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     r /= nT;
                     const int kb = r % n_kb;
                     r /= n_kb;
-                    const int jd = r % nT, wr = r / nT;
+                    const int jd = r % nTD, wr = r / nTD;
                     const int ph2 = tcd.rD * 2 + tcd.rH;
-                    const int brow = (((ph2 * nT + jd) * nT + jh) * p.blk_units + wr * nT + jw) * p.C_out;
+                    const int brow = (((ph2 * nTD + jd) * nT + jh) * p.blk_units + wr * nT + jw) * p.C_out;
                     // the panels of W taps jw .. jw + wg - 1 are consecutive rows
                     dev::mbar_arrive_expect_tx(&fullb[s], b_slot);
                     dev::tma_load_2d(sB + (size_t)s * b_slot, &tmB, &fullb[s], kb * BK, brow);
@@ -290,7 +295,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const uint32_t awstep = 128u;
                     const uint32_t aw0 = (uint32_t)(nT - 1) * awstep;
                     bool init = false;
-                    for (int jd = 0; jd < nT && ok; ++jd)
+                    for (int jd = 0; jd < nTD && ok; ++jd)
                         for (int kb = 0; kb < n_kb && ok; ++kb) {
                             if (!dev::mbar_wait_bounded(&a_full[sa], pa, kWaitLimitNs)) {
                                 ok = false;
@@ -362,7 +367,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const TileCoord tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
             const int m = ew * 32 + lane;
             const int qw = (tcd.qwp * ni + a) * QWT + (m & 7), qh = tcd.qhb * MHT + (m >> 3);
-            const int od = 2 * tcd.qd + tcd.rD, oh = 2 * qh + tcd.rH;
+            const int od = p.SD * tcd.qd + tcd.rD, oh = 2 * qh + tcd.rH;
             const bool valid = qw < p.QW && od < p.Lo0 && oh < p.Lo1;
             for (int wr = 0; wr < 2; ++wr) {
                 if (ok && !dev::mbar_wait_bounded(&acc_full[a][wr], k & 1, kWaitLimitNs)) {
@@ -510,7 +515,7 @@ repack_x_scalar_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, in
 }
 
 struct WPackParams {
-    int C_in, C_out, K0, K1, K2, nT;
+    int C_in, C_out, K0, K1, K2, nT, nTD;
     int r_of[3][8];          // residue and tap index that kernel index k belongs to
     int j_of[3][8];
     int blk_units;
@@ -520,7 +525,7 @@ struct WPackParams {
 // H tap), the C_out rows of each (W phase, W tap), C_in fastest.  Every kernel index (kd, kh, kw) belongs to
 // exactly one (phase, tap), so each (ic, oc) row of kD*kH*kW weights is
 // scattered once.  Block = (64 input channels, one oc); columns = kernel
-// indices in chunks of 64 (kD*kH*kW is a multiple of 8: even extents).
+// indices in chunks of 64 (kD*kH*kW a multiple of 8: rows of 16-byte loads).
 __device__ __forceinline__ void repack_w_block(const bf16_t *__restrict__ w, bf16_t *__restrict__ wp,
                                                const WPackParams &q, int bx, int oc)
 {
@@ -542,7 +547,7 @@ __device__ __forceinline__ void repack_w_block(const bf16_t *__restrict__ w, bf1
                 const int kw = k % q.K2, kh = (k / q.K2) % q.K1, kd = k / (q.K1 * q.K2);
                 const int ph2 = (q.r_of[0][kd] << 1) | q.r_of[1][kh];
                 const int rw = q.r_of[2][kw], jw = q.j_of[2][kw];
-                const int unit = ((ph2 * q.nT + q.j_of[0][kd]) * q.nT + q.j_of[1][kh]) * q.blk_units +
+                const int unit = ((ph2 * q.nTD + q.j_of[0][kd]) * q.nT + q.j_of[1][kh]) * q.blk_units +
                                  rw * q.nT + jw;
                 const uint4 v = make_uint4(tile[row][4 * qq], tile[row][4 * qq + 1],
                                            tile[row][4 * qq + 2], tile[row][4 * qq + 3]);
@@ -588,12 +593,18 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 bool make_uplan(const Problem &pb, UPlan *out)
 {
-    if (pb.nd != 3 || pb.dtype != CT_BF16 || pb.G != 1) return false;
-    for (int d = 0; d < 3; ++d) {
+    if ((pb.nd != 3 && pb.nd != 2) || pb.dtype != CT_BF16 || pb.G != 1) return false;
+    // D has stride 2 and the extent of H and W, or is a unit dimension (extent 1,
+    // stride 1, no padding: a 2-D problem), whose single residue takes tap 0 at
+    // offset 0
+    const int SD = pb.S[0];
+    if (SD == 1 && (pb.K[0] != 1 || pb.P[0] != 0 || pb.OP[0] != 0)) return false;
+    for (int d = SD == 1 ? 1 : 0; d < 3; ++d) {
         if (pb.S[d] != 2 || pb.DL[d] != 1) return false;
         if (pb.K[d] % 2 != 0 || pb.K[d] / 2 > 4) return false;
-        if (pb.K[d] != pb.K[0]) return false;
+        if (pb.K[d] != pb.K[2]) return false;
     }
+    if (pb.kvol() % 8 != 0) return false;     // the weight repack moves 16-byte pieces of a row
     if (pb.C_in % BK != 0 || pb.C_out % 16 != 0 || pb.C_out < 16 || pb.C_out > 256) return false;
     if (pb.Lo[2] % 2 != 0) return false;
     UParams p;
@@ -601,21 +612,23 @@ bool make_uplan(const Problem &pb, UPlan *out)
     p.N = pb.N; p.C_in = pb.C_in; p.C_out = pb.C_out;
     p.Lo0 = pb.Lo[0]; p.Lo1 = pb.Lo[1]; p.Lo2 = pb.Lo[2];
     p.QW = p.Lo2 / 2;
-    p.QD = (p.Lo0 + 1) / 2;
+    p.SD = SD;
+    p.QD = (p.Lo0 + SD - 1) / SD;
     p.QH = (p.Lo1 + 1) / 2;
     p.nacc = 4 * pb.C_out <= 512 ? 2 : 1;     // tiles per unit
     p.n_qhb = (p.QH + MHT - 1) / MHT;
     p.n_qwp = ((p.QW + QWT - 1) / QWT + p.nacc - 1) / p.nacc;
-    p.nT = pb.K[0] / 2;
+    p.nT = pb.K[2] / 2;
+    p.nTD = SD == 2 ? p.nT : 1;
     p.n_kb = pb.C_in / BK;
-    const int64_t tiles = (int64_t)pb.N * p.QD * p.n_qhb * p.n_qwp * 4;
+    const int64_t tiles = (int64_t)pb.N * p.QD * p.n_qhb * p.n_qwp * 2 * SD;
     if (tiles > 0x7fffffff || tiles == 0) return false;
     p.ntiles = (int)tiles;
     // residue r of a stride-2 dimension takes the taps k == (r + p) mod 2, i.e.
     // k = c + 2j, reading input q + floor((r + p)/2) - j
     WPackParams wq;
     memset(&wq, 0, sizeof(wq));
-    for (int d = 0; d < 3; ++d) {
+    for (int d = SD == 1 ? 1 : 0; d < 3; ++d) {
         for (int r = 0; r < 2; ++r) {
             const int c = (r + pb.P[d]) % 2;
             const int base = (r + pb.P[d] - c) / 2;
@@ -646,7 +659,7 @@ bool make_uplan(const Problem &pb, UPlan *out)
     // (W phase, W tap)
     p.blk_units = 2 * p.nT;
     wq.blk_units = p.blk_units;
-    wq.C_in = pb.C_in; wq.C_out = pb.C_out; wq.nT = p.nT;
+    wq.C_in = pb.C_in; wq.C_out = pb.C_out; wq.nT = p.nT; wq.nTD = p.nTD;
     wq.K0 = pb.K[0]; wq.K1 = pb.K[1]; wq.K2 = pb.K[2];
     p.idesc = tc::idesc(1, pb.C_out, BM);
     p.acc_cols = (uint32_t)(2 * pb.C_out);
@@ -676,7 +689,7 @@ bool make_uplan(const Problem &pb, UPlan *out)
     out->p = p;
     out->wq = wq;
     out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * 2);
-    out->w_bytes = align256((size_t)8 * pb.C_out * p.nT * p.nT * p.nT * pb.C_in * 2);
+    out->w_bytes = align256((size_t)4 * SD * p.nTD * p.nT * p.nT * pb.C_out * pb.C_in * 2);
     out->smem = smem;
     return true;
 }
@@ -743,7 +756,7 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     if (!encode_tiled(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xt, adims, astr, abox,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)8 * p.nT * p.nT * p.nT * pb.C_out};
+    const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)4 * p.SD * p.nTD * p.nT * p.nT * pb.C_out};
     const uint64_t bstr[1] = {(uint64_t)pb.C_in * 2};
     const uint32_t bbox[2] = {(uint32_t)BK, (uint32_t)(p.wg * pb.C_out)};
     if (!encode_tiled(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wp, bdims, bstr, bbox,

@@ -49,10 +49,25 @@ CONFIGS = {
         nd=3, N=16, C_in=256, C_out=128, groups=1, L_in=(16, 16, 16), k=(4, 4, 4),
         stride=(2, 2, 2), padding=(1, 1, 1), output_padding=(0, 0, 0), dilation=(1, 1, 1),
         bias=True, add=False, dtype="bf16", bound=1.0 / math.sqrt(128 * 64), seed=5),
+    # ConvTranspose2d: the fused workload's layer (32 -> 64, k3 s2 p1 op1) and
+    # the bf16 workload's layer (256 -> 128, k4 s2 p1) on 2-D images; no page
+    # states a 2-D size, so these take the 3-D workloads' channel counts,
+    # kernels and output bytes (1.07 GB and 134 MB of fp32 output)
+    "convT2d_f32": dict(
+        desc="ConvTranspose2d fp32 N=64 C_in=32 C_out=64 k=3 s=2 p=1 op=1 in=128x128 bias",
+        nd=2, N=64, C_in=32, C_out=64, groups=1, L_in=(128, 128), k=(3, 3), stride=(2, 2),
+        padding=(1, 1), output_padding=(1, 1), dilation=(1, 1), bias=True, add=False,
+        dtype="f32", bound=1.0 / math.sqrt(64 * 9), seed=6),
+    "convT2d_bf16_dense": dict(
+        desc=("ConvTranspose2d bf16-in/fp32-accumulate N=16 C_in=256 C_out=128 k=4 s=2 p=1 "
+              "in=64x64 bias"),
+        nd=2, N=16, C_in=256, C_out=128, groups=1, L_in=(64, 64), k=(4, 4), stride=(2, 2),
+        padding=(1, 1), output_padding=(0, 0), dilation=(1, 1), bias=True, add=False,
+        dtype="bf16", bound=1.0 / math.sqrt(128 * 16), seed=7),
 }
 
 CONFIG_ORDER = ["convT1d_tiny", "convT1d_L131072", "convT3d_grouped",
-                "convT3d_add_hswish", "convT3d_bf16_dense"]
+                "convT3d_add_hswish", "convT3d_bf16_dense", "convT2d_f32", "convT2d_bf16_dense"]
 
 
 def bf16_round(a):

@@ -276,7 +276,11 @@ class Runner:
         self.ws = (torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
                    if self.ws_bytes else None)
         # kernels the library launches per forward pass on this path
-        self.launches_per_step = {"umma_bf16": 3, "tc3d_tf32x3": 3, "tc3dg_tf32x3": 3}.get(self.path, 1)
+        # (a prep / repack launch, then the GEMM kernel; the bf16 repack splits in
+        # two when D*H*W is not a multiple of 8)
+        in_sp = int(np.prod(c["L_in"]))
+        self.launches_per_step = {"umma_bf16": 2 if in_sp % 8 == 0 else 3, "tc3d_bf16split": 2,
+                                  "tc3dg_bf16split": 2}.get(self.path, 1)
 
     def forward(self, stream):
         c, d, ct = self.cfg, self.d, self.ct
@@ -402,7 +406,7 @@ def roofline(name, cfg, path, wm, sec, peaks):
         return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peaks["source"] + " cuBLAS bf16 burst"}
-    if path in ("tc1d_tf32x3", "tc3d_tf32x3", "tc3dg_tf32x3"):
+    if path in ("tc1d_tf32x3", "tc3d_bf16split", "tc3dg_bf16split"):
         # FP32 on the tensor cores.  The 1-D kernel does 3 tf32 products per
         # multiply-add at the tf32 rate (half the bf16 rate); the 3-D kernels one
         # tf32 product plus one bf16 MMA over twice the K (the two corrections),

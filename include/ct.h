@@ -179,8 +179,8 @@ ct_status ct_forward_3d_noalloc(const void *x, const void *w, const float *bias,
 
 /* Name of the kernel family the 1-D / 2-D / 3-D / fused call with these arguments
  * would launch when given the workspace ct_workspace_size_* reports
- * ("gather_generic", "phase1d_f32", "tc1d_tf32x3", "phase3d_f32", "tc3d_tf32x3",
- * "tc3dg_tf32x3" -- 32 input channels in 1, 2 or 4 groups -- or "umma_bf16"),
+ * ("gather_generic", "phase1d_f32", "tc1d_tf32x3", "phase3d_f32", "tc3d_bf16split",
+ * "tc3dg_bf16split" -- 32 input channels in 1, 2 or 4 groups -- or "umma_bf16"),
  * or NULL if the arguments are invalid.  Host only; launches
  * nothing.  `fused` selects the add + hardswish variant for the 2-D and 3-D queries. */
 const char *ct_path_1d(int N, int C_in, int C_out, int L_in, int k, int groups, int stride,

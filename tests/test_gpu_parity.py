@@ -207,7 +207,7 @@ TC3D = [
 def test_fp32_3d_tensor_core_shapes(k, add):
     c = dict(nd=3, G=1, S=[2, 2, 2], DL=[1, 1, 1], bias=bool(k % 2 == 0), add=add, dtype="f32",
              **TC3D[k])
-    assert path_of(c) == "tc3d_tf32x3", (c, path_of(c))
+    assert path_of(c) == "tc3d_bf16split", (c, path_of(c))
     t = cc.make_inputs(c, seed=800 + k + (50 if add else 0))
     y = cc.run_gpu(c, t).cpu().numpy()
     cc.assert_close(y, cc.run_oracle(c, t), "f32", "tc3d case %d add=%s %r" % (k, add, c))
@@ -233,7 +233,7 @@ TC3DG = [
 @pytest.mark.parametrize("k", range(len(TC3DG)))
 def test_fp32_3d_grouped_tensor_core_shapes(k):
     c = dict(nd=3, S=[2, 2, 2], DL=[1, 1, 1], bias=bool(k % 2 == 0), add=False, dtype="f32", **TC3DG[k])
-    assert path_of(c) == "tc3dg_tf32x3", (c, path_of(c))
+    assert path_of(c) == "tc3dg_bf16split", (c, path_of(c))
     t = cc.make_inputs(c, seed=900 + k)
     y = cc.run_gpu(c, t).cpu().numpy()
     cc.assert_close(y, cc.run_oracle(c, t), "f32", "tc3dg case %d %r" % (k, c))
@@ -265,7 +265,7 @@ TC2D = [
 @pytest.mark.parametrize("k", range(len(TC2D)))
 def test_fp32_2d_tensor_core_shapes(k, add):
     c = dict(nd=2, G=1, S=[2, 2], DL=[1, 1], bias=bool(k % 2 == 0), add=add, dtype="f32", **TC2D[k])
-    assert path_of(c) == "tc3d_tf32x3", (c, path_of(c))
+    assert path_of(c) == "tc3d_bf16split", (c, path_of(c))
     t = cc.make_inputs(c, seed=1000 + k + (50 if add else 0))
     y = cc.run_gpu(c, t).cpu().numpy()
     cc.assert_close(y, cc.run_oracle(c, t), "f32", "2-D tc case %d add=%s %r" % (k, add, c))

@@ -130,8 +130,8 @@ const char *path_name(Path p)
     case Path::Phase3d: return "phase3d_f32";
     case Path::Umma: return "umma_bf16";
     case Path::Tc1d: return "tc1d_tf32x3";
-    case Path::Tc3d: return "tc3d_tf32x3";
-    case Path::Tc3dg: return "tc3dg_tf32x3";
+    case Path::Tc3d: return "tc3d_bf16split";
+    case Path::Tc3dg: return "tc3dg_bf16split";
     }
     return "gather_generic";
 }

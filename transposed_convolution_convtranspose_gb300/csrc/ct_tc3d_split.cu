@@ -1,6 +1,7 @@
-// ct_tc3d_tf32.cu -- FP32 ConvTranspose3d, plain or with the fused
-// add + t*hardswish(t) epilogue, on the tensor cores (tcgen05 kind::tf32)
-// with a split into tf32 and bf16 terms that keeps fp32-level accuracy.
+// ct_tc3d_split.cu -- FP32 ConvTranspose3d (and 2-D: a unit D dimension),
+// plain or with the fused add + t*hardswish(t) epilogue, on the tensor cores
+// (tcgen05 kind::f16 with bf16 operands) with a two-term split of every
+// operand that keeps the result within ~2^-16 of fp32 arithmetic.
 //
 // Method ([l1_p72] stride-phase classes: residue r of a dimension receives
 // the taps k with (r + p - k) even, reading input q + (r + p - k)/2;
@@ -11,16 +12,16 @@
 //                x[ic][qd+dd][qh+dh][qw+dw] * w[ic][oc][kd][kh][kw]
 // -- for 128 positions q a GEMM with M = 128, N = C_out, K = C_in per tap.
 //
-// Operands (caller's workspace, written by the two prep kernels):
-//   x (N, C_in, D, H, W) -> x_hi (N, D, H, W, C_in) tf32 and x_c (N, D, H, W,
-//                           2 C_in) bf16, channels-last
+// Operands (caller's workspace, written by one prep launch):
+//   x (N, C_in, D, H, W) -> x_c (N, D, H, W, 2 C_in) bf16, channels-last
 //   w (C_in, C_out, kD, kH, kW) -> weight panels, K-major (C_in fastest)
-// with hi = v rounded to tf32 (cvt.rna) and lo = v - hi (exact in fp32); per
-// K step a kind::tf32 MMA accumulates hi*hi and ONE kind::f16 MMA over twice
-// the K accumulates both corrections hi*lo + lo*hi, on bf16 copies of
-// [x_hi | x_lo] and [w_lo | w_hi] of the step's 8 channels (the corrections
-// are ~2^-11 of a product, so their bf16 factors leave ~2^-19 of it; the
-// dropped lo*lo term is below 2^-21).
+// Every value v is split as hi = bf16(v) (round to nearest even) and lo =
+// bf16(v - hi); the dropped remainder is below 2^-17 |v|.  Per K step of 8
+// input channels the A row holds [x_hi | x_lo] of the 8 (16 bf16 = 32
+// bytes), and two kind::f16 MMAs of K = 16 multiply it by [w_hi | w_hi] and
+// by [w_lo | w_lo]: together x_hi w_hi + x_lo w_hi + x_hi w_lo + x_lo w_lo =
+// (x_hi + x_lo)(w_hi + w_lo), every bf16 product exact in the fp32
+// accumulator, so a product carries a relative error of about 2^-16 at most.
 //
 // Schedule.  A unit of work is 128 positions (whole W rows of MH H rows of
 // one D plane) and one D residue rD, with the four (rH, rW) phases as four
@@ -28,15 +29,15 @@
 // across units when they fit, so the epilogue of one unit overlaps the MMAs
 // of the next).  Every distinct input offset (dd, dh, dw) the unit reads is
 // one A tile; the phases that read it with some tap form runs of adjacent
-// accumulators, and the weights of a run are stored as one panel -- tf32 rows
-// of its phases, then bf16 correction rows -- so that one MMA with N = run length x C_out
+// accumulators, and the weights of a run are stored as one panel -- hi rows
+// of its phases, then lo rows -- so that one MMA with N = run length x C_out
 // serves the whole run.  An MMA instruction costs the issuing thread about
 // 100 clocks whatever its N, so wide runs are what keeps the tensor cores
 // busy; the issue loop carries ring slots and parities as counters.
 //
 // Roles (persistent CTA, one per SM):
-//   warp 0      TMA producer of the A ring (x_hi and x_c 5-D boxes of 128
-//               positions x 128 bytes of channels at the offset; boxes reaching outside
+//   warp 0      TMA producer of the A ring (x_c 5-D boxes of 128 positions
+//               x 128 bytes of channels at the offset; boxes reaching outside
 //               the input read zeros, which is the boundary handling)
 //   warp 1      TMA producer of the B ring (a run's panel is one box).  Each
 //               ring slot has exactly one producer, which refills it only after
@@ -71,7 +72,7 @@ namespace {
 
 constexpr int BM = 128;          // positions per unit (UMMA M)
 constexpr int CK = 32;           // fp32 K per stage: one 128-byte swizzle row
-constexpr int NA = 2;            // A stages (one producer warp)
+constexpr int NA = 4;            // A stages (one producer warp; deep enough to cover DRAM latency)
 constexpr int NB = 2;            // B stages
 constexpr int NE = 3;            // epilogue chunk buffers (16 channels of a unit, 32 KB each)
 constexpr int NPB = 1;           // B producer warps: warp q loads the B stages g with g mod NPB == q
@@ -85,7 +86,7 @@ constexpr int kMmaWarp = kBWarp0 + NPB;
 constexpr int kEpiWarp0 = kMmaWarp + 1;
 constexpr int kStoreWarp = kEpiWarp0 + 4 * EPW;
 constexpr int kThreads = 32 * (kStoreWarp + 1);
-constexpr uint32_t kATile = BM * CK * 4;       // the tf32 tile or the bf16 correction tile: 16 KB
+constexpr uint32_t kATile = BM * CK * 4;       // 128 positions x 32 channels x (hi, lo) bf16: 16 KB
 constexpr uint32_t kEChunk = 16 * 4 * BM * 4;  // 16 channels x 4 phases x 128 positions, fp32: 32 KB
 constexpr int kEpiThreads = 32 * 4 * EPW;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -97,7 +98,7 @@ struct Entry {
     int16_t run0, pad;
 };
 // Adjacent accumulators p0 .. p0 + len - 1 served by one weight panel whose
-// tf32 rows start at row brow (correction rows follow after len x C_out rows).  fresh:
+// hi rows start at row brow (lo rows follow after len x C_out rows).  fresh:
 // the first MMA of the run writes (rather than adds to) its accumulators.
 struct Run {
     int8_t p0, len, fresh, pad;
@@ -115,43 +116,37 @@ struct T3Params {
     uint32_t acc_cols;           // 4 x C_out
     uint32_t tmem_cols;
     uint32_t bslot;              // bytes of a B ring slot
-    uint32_t idesc[5];           // kind::tf32 instruction descriptor for N = len x C_out, len 1..4
-    uint32_t idesc_b[5];         // kind::f16 (bf16), the same N
+    uint32_t idesc_b[5];         // kind::f16 (bf16) instruction descriptor for N = len x C_out, len 1..4
     int nE[2];
     Entry ent[2][MAXE];
     Run run[2][MAXR];
 };
 
-// Weight panel rows: block b (C_out rows) holds tap blk_tap[b]: its tf32 part
-// (blk_lo 0) or its bf16 correction rows (blk_lo 1).
+// Weight panel rows: block b (C_out rows) holds tap blk_tap[b]: its bf16 hi
+// parts (blk_lo 0) or its lo parts (blk_lo 1), each twice per K step.
 struct WPanels {
     int C_in, C_out, ntap, nblk;
     int8_t blk_tap[MAXBLK];
     int8_t blk_lo[MAXBLK];
 };
 
-__device__ __forceinline__ float tf32_hi(float v)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(v));
-    return __uint_as_float(r);
-}
-
 // ---- prep kernels ------------------------------------------------------------
-// x (N, C, S) -> x_hi (N, S, C) tf32 and x_c (N, S, 2C) bf16 where, per 32
-// channels and K step of 8, x_c holds [bf16(hi) of the 8 | bf16(lo) of the 8];
-// S = D*H*W a multiple of 4, C of 32.  Block = 32 channels x 64 positions:
-// 16-byte loads of 4 positions of one channel (a warp reads 2 x 256
-// contiguous bytes), a shared tile of pitch 33, then per thread 4 channels of
-// one position: a 16-byte store of the tf32 parts, two 8-byte stores of the
-// bf16 ones.
+// x (N, C, S) -> x_c (N, S, 2C) bf16 where, per 32 channels and K step of 8,
+// x_c holds [hi of the 8 | lo of the 8]; S = D*H*W a multiple of 4, C of 32.
+// Block = 32 channels x 64 positions: 16-byte loads of 4 positions of one
+// channel (a warp reads 2 x 256 contiguous bytes), a shared tile of pitch 33,
+// then per thread 4 channels of one position: two 8-byte stores.
+__device__ __forceinline__ float bf16_round(float v)
+{
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
 __device__ __forceinline__ uint32_t bf16_bits(float v)
 {
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-__device__ __forceinline__ void prep_x_block(const float *__restrict__ x, float *__restrict__ xhi,
-                                             uint16_t *__restrict__ xc, int C, int64_t SP, int bx, int by, int n)
+__device__ __forceinline__ void prep_x_block(const float *__restrict__ x, uint16_t *__restrict__ xc, int C,
+                                             int64_t SP, int bx, int by, int n)
 {
     __shared__ float tile[64][33];
     const int c0 = by * 32;
@@ -176,17 +171,14 @@ __device__ __forceinline__ void prep_x_block(const float *__restrict__ x, float 
         const int idx = threadIdx.x + 256 * it;
         const int q = idx & 7, pos = idx >> 3;
         if (pos < ncols) {
-            float h[4];
             uint32_t hb[4], lb[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float v = tile[pos][4 * q + i];
-                h[i] = tf32_hi(v);
-                hb[i] = bf16_bits(h[i]);
-                lb[i] = bf16_bits(v - h[i]);
+                const float h = bf16_round(v);
+                hb[i] = bf16_bits(h);
+                lb[i] = bf16_bits(v - h);       // v - h is exact in fp32
             }
-            const int64_t o = ob + (int64_t)pos * C + 4 * q;
-            *reinterpret_cast<float4 *>(xhi + o) = make_float4(h[0], h[1], h[2], h[3]);
             // channels 4q..4q+3 of this block: K step q / 2, elements 4 (q & 1) ..
             uint16_t *cr = xc + 2 * (ob + (int64_t)pos * C) + (q >> 1) * 16 + (q & 1) * 4;
             *reinterpret_cast<uint2 *>(cr) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
@@ -196,8 +188,8 @@ __device__ __forceinline__ void prep_x_block(const float *__restrict__ x, float 
 }
 
 // w (C_in, C_out, K0, K1, K2) -> weight panels [block][C_out][C_in x 4 bytes]:
-// block b holds tap blk_tap[b] as tf32 values, or (blk_lo) as bf16 rows of
-// [bf16(lo) | bf16(hi)] per K step of 8 input channels.
+// block b holds tap blk_tap[b] as bf16 rows of [hi | hi] (blk_lo 0) or [lo |
+// lo] (blk_lo 1) per K step of 8 input channels.
 __device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float *__restrict__ wp, const WPanels &q,
                                              int bw, int nbw)
 {
@@ -208,16 +200,13 @@ __device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float 
         const int64_t r = e % per;
         const int oc = (int)(r / q.C_in), ic = (int)(r % q.C_in);
         const float v = __ldg(w + ((int64_t)ic * q.C_out + oc) * q.ntap + q.blk_tap[b]);
-        const float h = tf32_hi(v);
-        if (!q.blk_lo[b]) {
-            wp[e] = h;
-        } else {
-            // the row's bf16 view: K step ic / 8 of its 32-channel block
-            uint16_t *row = reinterpret_cast<uint16_t *>(wp + (e - ic));
-            const int kb = ic >> 5, kk = (ic & 31) >> 3, el = ic & 7;
-            row[kb * 64 + kk * 16 + el] = (uint16_t)bf16_bits(v - h);
-            row[kb * 64 + kk * 16 + 8 + el] = (uint16_t)bf16_bits(h);
-        }
+        const float h = bf16_round(v);
+        const uint16_t t = (uint16_t)bf16_bits(q.blk_lo[b] ? v - h : h);
+        // the row's bf16 view: K step ic / 8 of its 32-channel block
+        uint16_t *row = reinterpret_cast<uint16_t *>(wp + (e - ic));
+        const int kb = ic >> 5, kk = (ic & 31) >> 3, el = ic & 7;
+        row[kb * 64 + kk * 16 + el] = t;
+        row[kb * 64 + kk * 16 + 8 + el] = t;
     }
 }
 
@@ -225,7 +214,7 @@ __device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float 
 // remaining nbw blocks build the panels.  The GEMM kernel is launched as its
 // programmatic dependent.
 __global__ void __launch_bounds__(256)
-prep_kernel(const float *__restrict__ x, float *__restrict__ xhi, uint16_t *__restrict__ xc, int C, int64_t SP,
+prep_kernel(const float *__restrict__ x, uint16_t *__restrict__ xc, int C, int64_t SP,
             int nbx, int nby, int nxb, const float *__restrict__ w, float *__restrict__ wp,
             const __grid_constant__ WPanels q, int nbw)
 {
@@ -233,7 +222,7 @@ prep_kernel(const float *__restrict__ x, float *__restrict__ xhi, uint16_t *__re
     const int b = (int)blockIdx.x;
     if (b < nxb) {
         const int per = nbx * nby;
-        prep_x_block(x, xhi, xc, C, SP, (b % per) % nbx, (b % per) / nbx, b / per);
+        prep_x_block(x, xc, C, SP, (b % per) % nbx, (b % per) / nbx, b / per);
     } else {
         prep_w_block(w, wp, q, b - nxb, nbw);
     }
@@ -268,7 +257,7 @@ __device__ __forceinline__ UnitCoord unit_coord(int u, const T3Params &p)
 
 template <bool ADD>
 __global__ void __launch_bounds__(kThreads, 1)
-tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant__ CUtensorMap tmXc,
+tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                  const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
                  const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmW4,
                  const __grid_constant__ CUtensorMap tmAdd, const __grid_constant__ CUtensorMap tmY,
@@ -280,13 +269,12 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
     __shared__ uint32_t tmem_slot;
     __shared__ float s_bias[128];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = sm;                                  // NA x (tf32 tile, bf16 correction tile)
-    uint8_t *sB = sm + NA * 2 * kATile;                // NB x bslot
+    uint8_t *sA = sm;                                  // NA x kATile
+    uint8_t *sB = sm + NA * kATile;                    // NB x bslot
     uint8_t *sE = sB + NB * p.bslot;                   // NE x kEChunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        dev::prefetch_tensormap(&tmXh);
         dev::prefetch_tensormap(&tmXc);
         dev::prefetch_tensormap(&tmW1);
         dev::prefetch_tensormap(&tmW2);
@@ -353,12 +341,9 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
                                     break;
                                 }
                                 if (isA) {
-                                    uint8_t *ah = sA + (size_t)s * 2 * kATile;
-                                    dev::mbar_arrive_expect_tx(&fullb[s], 2 * kATile);
-                                    dev::tma_load_5d(ah, &tmXh, &fullb[s], kb * CK, en.dw, qh0 + en.dh,
-                                                     u.qd + en.dd, u.n);
-                                    dev::tma_load_5d(ah + kATile, &tmXc, &fullb[s], kb * 2 * CK, en.dw, qh0 + en.dh,
-                                                     u.qd + en.dd, u.n);
+                                    dev::mbar_arrive_expect_tx(&fullb[s], kATile);
+                                    dev::tma_load_5d(sA + (size_t)s * kATile, &tmXc, &fullb[s], kb * 2 * CK, en.dw,
+                                                     qh0 + en.dh, u.qd + en.dd, u.n);
                                 } else {
                                     // the run's panel exactly: a box of 2 x len x C_out rows
                                     const Run &ru = p.run[u.rd][en.run0 + j];
@@ -412,8 +397,7 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
                             break;
                         }
                         tc::fence_after();
-                        const uint32_t ah = sAb + (uint32_t)sa * 2u * kATile;
-                        const uint64_t dah = tc::desc_sw128(ah), dal = tc::desc_sw128(ah + kATile);
+                        const uint64_t da = tc::desc_sw128(sAb + (uint32_t)sa * kATile);
                         for (int j = 0; j < en.nrun; ++j) {
                             const Run &ru = p.run[rd][en.run0 + j];
                             if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
@@ -424,15 +408,15 @@ tc3d_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant
                             const uint32_t bh = sBb + (uint32_t)sb * bslot;
                             const uint64_t dbh = tc::desc_sw128(bh);
                             const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(ru.len * C_out) * 128u);
-                            const uint32_t id = p.idesc[ru.len], idb = p.idesc_b[ru.len];
+                            const uint32_t idb = p.idesc_b[ru.len];
                             const uint32_t dd = d + (uint32_t)(ru.p0 * C_out);
                             const uint32_t acc0 = (ru.fresh && kb == 0) ? 0u : 1u;
 #pragma unroll
                             for (int kk = 0; kk < CK / 8; ++kk) {
-                                // advance 8 tf32 = 32 bytes along K inside the swizzle atom
-                                // 32 bytes per step: 8 tf32, or 16 bf16 (the 8 channels' hi and lo)
-                                tc::mma_tf32(dd, dah + 2 * kk, dbh + 2 * kk, id, kk ? 1u : acc0);   // hi x hi
-                                tc::mma_bf16(dd, dal + 2 * kk, dbl + 2 * kk, idb, 1u);             // corrections
+                                // 32 bytes along K inside the swizzle atom: 16 bf16, the
+                                // hi and lo parts of 8 channels
+                                tc::mma_bf16(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x * w_hi
+                                tc::mma_bf16(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x * w_lo
                             }
                             tc::commit(&b_empty[sb]);
                             if (++sb == NB) {
@@ -725,17 +709,15 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     wq.C_out = pb.C_out;
     wq.ntap = pb.kvol();
     wq.nblk = nblk;
-    for (int len = 1; len <= 4; ++len) {
-        p.idesc[len] = len * pb.C_out <= 256 ? tc::idesc(2, len * pb.C_out, BM) : 0u;
+    for (int len = 1; len <= 4; ++len)
         p.idesc_b[len] = len * pb.C_out <= 256 ? tc::idesc(1, len * pb.C_out, BM) : 0u;
-    }
     p.acc_cols = (uint32_t)(4 * pb.C_out);
     p.nacc = 8 * pb.C_out <= 512 ? 2 : 1;
     uint32_t cols = 32;
     while (cols < (uint32_t)p.nacc * p.acc_cols) cols <<= 1;
     p.tmem_cols = cols;
     p.bslot = (uint32_t)(2 * maxlen * pb.C_out) * 128u;
-    const size_t smem = (size_t)NA * 2 * kATile + (size_t)NB * p.bslot + (size_t)NE * kEChunk + 1024;
+    const size_t smem = (size_t)NA * kATile + (size_t)NB * p.bslot + (size_t)NE * kEChunk + 1024;
     if (smem > 227 * 1024 - 1024) return false;   // room for the static barriers
     out->p = p;
     out->wq = wq;
@@ -758,7 +740,7 @@ size_t tc3d_workspace_bytes(const Problem &pb)
 {
     T3Plan pl;
     if (!make_t3plan(pb, nullptr, &pl)) return 0;
-    return 2 * pl.x_bytes + pl.w_bytes;
+    return pl.x_bytes + pl.w_bytes;
 }
 
 cudaError_t launch_tc3d(const Problem &pb, const Args &a)
@@ -767,11 +749,10 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     if (!make_t3plan(pb, &a, &pl)) return cudaErrorNotSupported;
     const T3Params &p = pl.p;
     uint8_t *ws = static_cast<uint8_t *>(a.ws);
-    float *xhi = reinterpret_cast<float *>(ws);
-    uint16_t *xc = reinterpret_cast<uint16_t *>(ws + pl.x_bytes);
-    float *wp = reinterpret_cast<float *>(ws + 2 * pl.x_bytes);
+    uint16_t *xc = reinterpret_cast<uint16_t *>(ws);
+    float *wp = reinterpret_cast<float *>(ws + pl.x_bytes);
 
-    // 1) one launch: x -> channels-last tf32 + bf16 corrections, weights -> run panels
+    // 1) one launch: x -> channels-last bf16 (hi, lo) pairs, weights -> run panels
     const int64_t SP = pb.in_sp();
     const int64_t nbx = (SP + 63) / 64, nby = pb.C_in / 32;
     const int64_t nxb = nbx * nby * pb.N;
@@ -779,30 +760,25 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     int nbw = (int)((wtot + 255) / 256);
     if (nbw > 4 * sm_count()) nbw = 4 * sm_count();
     if (nxb + nbw > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    prep_kernel<<<(unsigned)(nxb + nbw), 256, 0, a.stream>>>(static_cast<const float *>(a.x), xhi, xc, pb.C_in, SP,
+    prep_kernel<<<(unsigned)(nxb + nbw), 256, 0, a.stream>>>(static_cast<const float *>(a.x), xc, pb.C_in, SP,
                                                             (int)nbx, (int)nby, (int)nxb,
                                                             static_cast<const float *>(a.w), wp, pl.wq, nbw);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // 3) tensor maps: A over x_hi (C, W, H, D, N) fp32 and x_c (2C, W, H, D, N)
-    // bf16 -- 128-byte rows either way; B over the panels
-    // (C_in, rows), one map per run length len (a box of 2 x len x C_out rows:
-    // the run's hi and lo panels)
-    CUtensorMap tmXh, tmXc, tmW[4];
-    const uint64_t adims[5] = {(uint64_t)pb.C_in, (uint64_t)pb.Li[2], (uint64_t)pb.Li[1], (uint64_t)pb.Li[0],
-                               (uint64_t)pb.N};
+    // 2) tensor maps: A over x_c (2C, W, H, D, N) bf16, 128-byte rows; B over
+    // the panels (C_in x 4 bytes, rows), one map per run length len (a box of
+    // 2 x len x C_out rows: the run's hi and lo panels)
+    CUtensorMap tmXc, tmW[4];
     const uint64_t astr[4] = {(uint64_t)pb.C_in * 4, (uint64_t)pb.C_in * pb.Li[2] * 4,
                               (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * 4,
                               (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * pb.Li[0] * 4};
-    const uint32_t abox[5] = {(uint32_t)CK, (uint32_t)p.QW, (uint32_t)p.MH, 1u, 1u};
     const uint64_t cdims[5] = {(uint64_t)pb.C_in * 2, (uint64_t)pb.Li[2], (uint64_t)pb.Li[1], (uint64_t)pb.Li[0],
                                (uint64_t)pb.N};
     const uint32_t cbox[5] = {(uint32_t)CK * 2, (uint32_t)p.QW, (uint32_t)p.MH, 1u, 1u};
     const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)pl.wq.nblk * pb.C_out};
     const uint64_t bstr[1] = {(uint64_t)pb.C_in * 4};
-    if (!encode_tiled(&tmXh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xhi, adims, astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&tmXc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc, cdims, astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_tiled(&tmXc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc, cdims, astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     for (int len = 1; len <= 4; ++len) {
         // lengths beyond the longest run keep a valid map of the longest box
@@ -826,7 +802,7 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
-    const void *fn = a.add ? (const void *)&tc3d_tf32_kernel<true> : (const void *)&tc3d_tf32_kernel<false>;
+    const void *fn = a.add ? (const void *)&tc3d_split_kernel<true> : (const void *)&tc3d_split_kernel<false>;
     int per_sm = 0;
     e = prepare_kernel(fn, kThreads, pl.smem, &per_sm);
     if (e != cudaSuccess) return e;
@@ -837,9 +813,9 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     if (grid > p.nunits) grid = p.nunits;
     if (p.SD == 2 && grid > 1 && (grid & 1)) --grid;   // an even grid: the residue flip of unit_coord permutes units
     if (a.add)
-        return launch_dependent(tc3d_tf32_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXh,
+        return launch_dependent(tc3d_split_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
                                 tmXc, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
-    return launch_dependent(tc3d_tf32_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXh,
+    return launch_dependent(tc3d_split_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
                             tmXc, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
 }
 

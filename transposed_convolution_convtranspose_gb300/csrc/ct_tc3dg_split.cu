@@ -1,12 +1,11 @@
-// ct_tc3dg_tf32.cu -- FP32 ConvTranspose3d with 32 input channels in 1, 2 or
-// 4 groups (asymmetric kernels up to 8 per dimension, any padding) on the
-// tensor cores, with a split that keeps fp32-level accuracy: per product
-// a*b = (a_hi + a_lo)(b_hi + b_lo), the main term a_hi*b_hi as a tcgen05
-// kind::tf32 MMA (a_hi, b_hi: the operands rounded to tf32) and the two
-// correction terms a_hi*b_lo + a_lo*b_hi as ONE kind::f16 MMA over twice the
-// K, on bf16 copies of [a_hi | a_lo] and [b_lo | b_hi].  The corrections are
-// about 2^-11 of the product, so their bf16 factors (8-bit mantissa) leave
-// about 2^-19 of it; the dropped a_lo*b_lo is below 2^-21.
+// ct_tc3dg_split.cu -- FP32 ConvTranspose3d with 32 input channels in 1, 2
+// or 4 groups (asymmetric kernels up to 8 per dimension, any padding) on the
+// tensor cores (tcgen05 kind::f16 with bf16 operands), with a two-term split of
+// every operand: v = hi + lo with hi = bf16(v) and lo = bf16(v - hi), leaving
+// less than 2^-17 |v|.  Per K step the A row holds [a_hi | a_lo] of 8 (or 16)
+// channels and two MMAs multiply it by [b_hi | b_hi] and by [b_lo | b_lo]:
+// together (a_hi + a_lo)(b_hi + b_lo), every bf16 product exact in the fp32
+// accumulator, so a product carries a relative error of about 2^-16 at most.
 //
 // Method ([l1_p72] stride-phase classes: residue r of a stride-2 dimension
 // receives the taps k with (r + p - k) even, reading input q + (r + p - k)/2;
@@ -16,15 +15,14 @@
 //                        input channels ic of x[n, ic, q + delta_t] * w[ic, oc_l, k_t]
 // For one input offset (dd, dh, dw) every output phase (rD, rH, rW) that reads
 // it with some tap contributes; with 128 positions q as the M rows, a group's
-// contraction over its Cig = 32 / G channels is Cig / 8 tf32 MMAs of K = 8
-// plus Cig / 8 bf16 MMAs of K = 16 for the corrections.
+// contraction over its Cig = 32 / G channels (2 Cig bf16 values of K: hi and
+// lo parts) is 2 x Cig / 8 bf16 MMAs of K = 16.
 //
 // Groups without block-diagonal zeros.  All 32 input channels of a position
 // are one 128-byte row of the A operand (K-major, 128-byte swizzle), so group
-// g's channels are the K steps g * Cig/8 .. of that row: the MMAs of group g
-// start their A and B descriptors Cig * 4 * g bytes into the rows (the bf16
-// correction rows hold [hi | lo] of each group's channels in the same 128
-// bytes, so the offset is the same).  The weight panels hold, in the same K
+// g's values (its channels' hi parts, then their lo parts) are the K steps
+// g * Cig/8 .. of that row: the MMAs of group g start their A and B
+// descriptors Cig * 4 * g bytes into the rows.  The weight panels hold, in the same K
 // positions of one row, the weights of every group for that row's (phase,
 // output channel within the group).  One MMA-issuing
 // warp per group owns that group's TMEM columns; all of them read the same
@@ -43,8 +41,8 @@
 //
 // Operand A without shifted copies (the 128-byte swizzle is a function of the
 // absolute shared-memory address): x is repacked channels-last with H fastest
-// after the channels, (N, D, W, H, 32) as tf32 parts and (N, D, W, H, 64)
-// as bf16 [hi | lo] per group; per D offset one TMA box per copy brings the
+// after the channels, (N, D, W, H, 64) bf16, per group [hi | lo]; per D
+// offset one TMA box brings the
 // unit's input window, (8 + H halo) x (16 + W halo) positions of 128 bytes,
 // rows ordered (w, h).  The A operand of offset (dh, dw) is
 // that window read from row (dw - dw_lo) * hspan + (dh - dh_lo) with a stride
@@ -52,9 +50,9 @@
 // D plane; TMEM row m holds (qw, qh) = (m / 8, m mod 8).
 //
 // Roles (persistent CTA, one per SM):
-//   warp 0      TMA producer of the A ring (tf32 and bf16 windows of a D offset)
-//   warps 1-4   TMA producers of the B ring (one input offset's panel: tf32
-//               rows, then bf16 correction rows), one per slot
+//   warp 0      TMA producer of the A ring (the window of a D offset)
+//   warps 1-4   TMA producers of the B ring (one input offset's panel: hi
+//               rows, then lo rows), one per slot
 //   warps 5-8   MMA issue, one warp per group (one thread issues an MMA only
 //               every ~100 clocks, so the groups' MMAs run from separate
 //               threads); TMEM allocation by warp 5
@@ -80,8 +78,8 @@ namespace {
 constexpr int BM = 128;          // positions per unit (UMMA M)
 constexpr int QWT = 16;          // qw per unit (TMEM row m: qw = m / 8)
 constexpr int MHT = 8;           // qh per unit (one 8-row swizzle group per qw)
-constexpr int CK = 32;           // input channels: one 128-byte row of tf32
-constexpr int NA = 2;            // A ring slots (hi + lo windows each)
+constexpr int CK = 32;           // input channels: one 128-byte row of bf16 (hi, lo) pairs
+constexpr int NA = 3;            // A ring slots (one window each)
 constexpr int MAXB = 8;          // B ring slots at most
 constexpr int BROWS = 256;       // rows of a B stage at most (one 32 KB slot)
 constexpr int NPB = 4;           // B producer warps at most
@@ -98,8 +96,8 @@ constexpr int kEpiThreads = 32 * 4 * EPW;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // One input offset of a unit: the pairs (rD, rH) q0 .. q0 + nq - 1 receive
-// its MMAs; its panel is 2 x R rows from row0 (tf32 rows, then bf16
-// correction rows), R = nq x 2 x Cog.
+// its MMAs; its panel is 2 x R rows from row0 (hi rows, then lo rows),
+// R = nq x 2 x Cog.
 struct GEntry {
     int8_t dh, dw, q0, nq;
     int row0;
@@ -119,12 +117,11 @@ struct GParams {
     int bs_units[MAXE];          // rows of B stage j in units of 4 x Cog rows
     int nb, npb;                 // B ring slots and producers (nb a multiple of npb)
     int hspan, wspan, dh_lo, dw_lo;
-    uint32_t a_half;             // bytes of one window part (hi or lo), 1024-aligned
+    uint32_t a_slot;             // bytes of one window, 1024-aligned
     uint32_t bslot;              // bytes of a B ring slot (the widest panel)
     uint32_t set_cols;           // 8 x C_out
     uint32_t tmem_cols;
-    uint32_t idesc_t[5];         // kind::tf32, N = 2 x Cog x pairs, pairs 1..4
-    uint32_t idesc_b[5];         // kind::f16 (bf16), the same N
+    uint32_t idesc_b[5];         // kind::f16 (bf16), N = 2 x Cog x pairs, pairs 1..4
     GEntry ent[MAXE];
 };
 
@@ -142,11 +139,9 @@ __device__ __forceinline__ uint32_t bf16_bits(float v)
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-__device__ __forceinline__ float tf32_hi(float v)
+__device__ __forceinline__ float bf16_round(float v)
 {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(v));
-    return __uint_as_float(r);
+    return __bfloat162float(__float2bfloat16_rn(v));
 }
 
 // 8 columns of the warp's 32 TMEM lanes set to zero.
@@ -172,15 +167,13 @@ __device__ __forceinline__ uint64_t desc_sbo(uint32_t saddr, uint32_t sbo)
 }
 
 // ---- prep kernels --------------------------------------------------------------
-// x (N, 32, D, H, W) -> x_t (N, D, W, H, 32) tf32 parts and x_c (N, D, W, H,
-// 64) bf16, per group [hi of its Cig channels | lo of them].  Block = 32
-// channels x 64 consecutive source positions (16-byte loads along W, a shared
-// tile of pitch 33); a thread then writes 4 channels of one position: a
-// 16-byte store of the tf32 parts and two 8-byte stores of the bf16 hi and lo.
-// D*H*W is a multiple of 4.
-__device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, float *__restrict__ xhi,
-                                              uint16_t *__restrict__ xc, int D, int H, int W, int Cig, int bx,
-                                              int n)
+// x (N, 32, D, H, W) -> x_c (N, D, W, H, 64) bf16, per group [hi of its Cig
+// channels | lo of them].  Block = 32 channels x 64 consecutive source
+// positions (16-byte loads along W, a shared tile of pitch 33); a thread then
+// writes 4 channels of one position: two 8-byte stores, hi and lo.  D*H*W is
+// a multiple of 4.
+__device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, uint16_t *__restrict__ xc, int D, int H,
+                                              int W, int Cig, int bx, int n)
 {
     __shared__ float tile[64][33];
     const int64_t SP = (int64_t)D * H * W;
@@ -206,17 +199,15 @@ __device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, float
         if (pos < ncols) {
             const int64_t s = s0 + pos;
             const int w = (int)(s % W), h = (int)((s / W) % H), d = (int)(s / ((int64_t)W * H));
-            float hv[4];
             uint32_t hb[4], lb[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float v = tile[pos][4 * q + i];
-                hv[i] = tf32_hi(v);
-                hb[i] = bf16_bits(hv[i]);
-                lb[i] = bf16_bits(v - hv[i]);
+                const float hv = bf16_round(v);
+                hb[i] = bf16_bits(hv);
+                lb[i] = bf16_bits(v - hv);      // v - hv is exact in fp32
             }
             const int64_t prow = (((int64_t)n * D + d) * W + w) * H + h;
-            *reinterpret_cast<float4 *>(xhi + prow * CK + 4 * q) = make_float4(hv[0], hv[1], hv[2], hv[3]);
             // channels 4q..4q+3 lie in one group g: hi at g*2Cig + i, lo Cig further
             const int c0 = 4 * q, g = c0 / Cig, i0 = c0 % Cig;
             uint16_t *cr = xc + prow * (2 * CK) + g * 2 * Cig + i0;
@@ -229,17 +220,16 @@ __device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, float
 // w (32, Cog, K0, K1, K2) -> panels.  Blocks (entry e, part hl, slice z), rows
 // rr = (pair index i, rW, oc_l) of the entry; the weight of a row for input
 // channel ic is w[ic][oc_l][kd][kh][kw] for the tap of phase (q0 + i, rW)
-// reading the entry's offset, zero where that phase reads none.  Part 0: 32
-// floats per row, the weights rounded to tf32.  Part 1: 64 bf16 per row, per
-// group [lo of its Cig channels | hi of them] (hi = the tf32 rounding, lo =
-// the remainder), the partner of the [hi | lo] order of x_c.
+// reading the entry's offset, zero where that phase reads none.  64 bf16 per
+// row, per group: part 0 [hi of its Cig channels | hi again], part 1 [lo | lo],
+// the partners of the [hi | lo] order of x_c.
 constexpr int kWSlices = 8;      // blocks per (entry, part) of the panel prep
 
 __device__ __forceinline__ void prepg_w_block(const float *__restrict__ w, uint8_t *__restrict__ wp,
                                               const GPanels &q, int e, int hl, int z)
 {
     const int R = q.enq[e] * 2 * q.Cog;
-    const int ncol = hl ? 2 * CK : CK;
+    const int ncol = 2 * CK;
     for (int idx = threadIdx.x + z * blockDim.x; idx < R * ncol; idx += blockDim.x * kWSlices) {
         const int rr = idx / ncol, k = idx % ncol;
         const int i = rr / (2 * q.Cog);
@@ -249,22 +239,14 @@ __device__ __forceinline__ void prepg_w_block(const float *__restrict__ w, uint8
         const int kd = q.tap[0][rD][q.edd[e] - q.off_lo[0]];
         const int kh = q.tap[1][rH][q.edh[e] - q.off_lo[1]];
         const int kw = q.tap[2][rW][q.edw[e] - q.off_lo[2]];
-        int ic = k;
-        bool want_lo = false;
-        if (hl) {
-            const int g = k / (2 * q.Cig), within = k % (2 * q.Cig);
-            ic = g * q.Cig + (within % q.Cig);
-            want_lo = within < q.Cig;
-        }
+        const int g = k / (2 * q.Cig), within = k % (2 * q.Cig);
+        const int ic = g * q.Cig + (within % q.Cig);
         float v = 0.f;
         if (((q.emask[e] >> pq) & 1) && kd >= 0 && kh >= 0 && kw >= 0)
             v = __ldg(w + (((int64_t)ic * q.Cog + oc_l) * q.K0 + kd) * (q.K1 * q.K2) + kh * q.K2 + kw);
-        const float hv = tf32_hi(v);
+        const float hv = bf16_round(v);
         uint8_t *row = wp + ((int64_t)q.erow0[e] + hl * R + rr) * 128;
-        if (hl)
-            reinterpret_cast<uint16_t *>(row)[k] = (uint16_t)bf16_bits(want_lo ? v - hv : hv);
-        else
-            reinterpret_cast<float *>(row)[k] = hv;
+        reinterpret_cast<uint16_t *>(row)[k] = (uint16_t)bf16_bits(hl ? v - hv : hv);
     }
 }
 
@@ -273,14 +255,14 @@ __device__ __forceinline__ void prepg_w_block(const float *__restrict__ w, uint8
 // as its programmatic dependent, so its CTAs may be scheduled while this
 // kernel drains.
 __global__ void __launch_bounds__(256)
-prepg_kernel(const float *__restrict__ x, float *__restrict__ xhi, uint16_t *__restrict__ xc, int D, int H, int W,
+prepg_kernel(const float *__restrict__ x, uint16_t *__restrict__ xc, int D, int H, int W,
              int Cig, int nbx, int nxb, const float *__restrict__ w, uint8_t *__restrict__ wp,
              const __grid_constant__ GPanels q)
 {
     dev::griddep_launch_dependents();
     const int b = (int)blockIdx.x;
     if (b < nxb) {
-        prepg_x_block(x, xhi, xc, D, H, W, Cig, b % nbx, b / nbx);
+        prepg_x_block(x, xc, D, H, W, Cig, b % nbx, b / nbx);
     } else {
         const int r = b - nxb;
         prepg_w_block(w, wp, q, r / (2 * kWSlices), (r / kWSlices) & 1, r % kWSlices);
@@ -305,7 +287,7 @@ __device__ __forceinline__ GUnit g_unit(int u, const GParams &p)
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-tc3dg_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant__ CUtensorMap tmXc,
+tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                   const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW4,
                   const float *__restrict__ bias,
                   float *__restrict__ y, const __grid_constant__ GParams p, unsigned int *status)
@@ -315,18 +297,17 @@ tc3dg_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constan
         acc_empty[2], drain_bar[MAXG];
     __shared__ uint32_t tmem_slot;
     __shared__ float s_bias[64];
-    // per entry: A window offset, B offset in its stage, hi -> bf16 rows, TMEM
-    // column within the group; instruction descriptors (tf32, bf16)
+    // per entry: A window offset, B offset in its stage, hi -> lo rows, TMEM
+    // column within the group; instruction descriptor
     __shared__ uint4 s_ent[MAXE];
-    __shared__ uint2 s_id[MAXE];
+    __shared__ uint32_t s_id[MAXE];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = sm;                                  // NA x (tf32 window, bf16 window)
-    uint8_t *sB = sm + (size_t)NA * 2 * p.a_half;      // nb x bslot
+    uint8_t *sA = sm;                                  // NA x a_slot
+    uint8_t *sB = sm + (size_t)NA * p.a_slot;          // nb x bslot
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G;
 
     if (threadIdx.x == 0) {
-        dev::prefetch_tensormap(&tmXh);
         dev::prefetch_tensormap(&tmXc);
         dev::prefetch_tensormap(&tmW1);
         dev::prefetch_tensormap(&tmW4);
@@ -356,7 +337,7 @@ tc3dg_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constan
             s_ent[e] = make_uint4((uint32_t)((en.dw - p.dw_lo) * p.hspan + (en.dh - p.dh_lo)) * 128u,
                                   (uint32_t)(en.row0 - rb) * 128u, (uint32_t)(en.nq * 2 * p.Cog) * 128u,
                                   (uint32_t)(en.q0 * 2 * p.Cog));
-            s_id[e] = make_uint2(p.idesc_t[en.nq], p.idesc_b[en.nq]);
+            s_id[e] = p.idesc_b[en.nq];
         }
     }
     tc::fence_before();
@@ -395,12 +376,10 @@ tc3dg_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constan
                     break;
                 }
                 if (isA) {
-                    // x_t and x_c viewed as (C, H, W, D, N): the window of D offset dd[i]
-                    uint8_t *ah = sA + (size_t)s * 2 * p.a_half;
+                    // x_c viewed as (C, H, W, D, N): the window of D offset dd[i]
                     const int h0 = u.qhb * MHT + p.dh_lo, w0 = u.qwb * QWT + p.dw_lo, d0 = u.qd + p.dd[i];
-                    dev::mbar_arrive_expect_tx(&fullb[s], 2u * (uint32_t)(p.hspan * p.wspan) * 128u);
-                    dev::tma_load_5d(ah, &tmXh, &fullb[s], 0, h0, w0, d0, u.n);
-                    dev::tma_load_5d(ah + p.a_half, &tmXc, &fullb[s], 0, h0, w0, d0, u.n);
+                    dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(p.hspan * p.wspan) * 128u);
+                    dev::tma_load_5d(sA + (size_t)s * p.a_slot, &tmXc, &fullb[s], 0, h0, w0, d0, u.n);
                 } else {
                     // the stage's panels (consecutive rows): boxes of 4 and of 1 unit
                     const int units = p.bs_units[i];
@@ -430,10 +409,10 @@ tc3dg_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constan
         if (lane == 0 && g < G) {
             bool ok = true;
             const uint32_t sAb = dev::smem_u32(sA), sBb = dev::smem_u32(sB);
-            const uint32_t a_half = p.a_half, bslot = p.bslot, sbo = (uint32_t)p.hspan * 128u;
+            const uint32_t a_slot = p.a_slot, bslot = p.bslot, sbo = (uint32_t)p.hspan * 128u;
             const int Cog = p.Cog, ksteps = p.Cig / 8, nb = p.nb;
-            // K step j of group g sits (g * ksteps + j) * 32 bytes into every row,
-            // tf32 and bf16 alike (a bf16 step covers hi and lo of 8 channels)
+            // K step j of group g (16 bf16: hi or lo parts) sits (g * ksteps + j) *
+            // 32 bytes into every row
             const uint64_t kgrp = (uint64_t)(g * ksteps * 2);         // in 16-byte units
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
@@ -451,7 +430,7 @@ tc3dg_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constan
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t wh = sAb + (uint32_t)sa * 2u * a_half, wc = wh + a_half;
+                    const uint32_t wc = sAb + (uint32_t)sa * a_slot;
                     for (int j = p.s0[i]; j < p.s0[i + 1] && ok; ++j) {
                         if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
                             ok = false;
@@ -460,17 +439,16 @@ tc3dg_tf32_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constan
                         tc::fence_after();
                         const uint32_t bb = sBb + (uint32_t)sb * bslot;
                         for (int e = p.bs_e0[j]; e < p.bs_e0[j + 1]; ++e) {
-                            const uint4 t0 = s_ent[e];      // A offset, B offset, hi -> bf16 rows, column
-                            const uint2 t1 = s_id[e];       // instruction descriptors
-                            const uint64_t dah = desc_sbo(wh + t0.x, sbo) + kgrp;
-                            const uint64_t dac = desc_sbo(wc + t0.x, sbo) + kgrp;
+                            const uint4 t0 = s_ent[e];      // A offset, B offset, hi -> lo rows, column
+                            const uint32_t id = s_id[e];    // instruction descriptor
+                            const uint64_t da = desc_sbo(wc + t0.x, sbo) + kgrp;
                             const uint64_t dbh = tc::desc_sw128(bb + t0.y) + kgrp;
-                            const uint64_t dbc = tc::desc_sw128(bb + t0.y + t0.z) + kgrp;
+                            const uint64_t dbl = tc::desc_sw128(bb + t0.y + t0.z) + kgrp;
                             const uint32_t d = dg + t0.w;
                             for (int kk = 0; kk < ksteps; ++kk) {
-                                const uint64_t kj = (uint64_t)(2 * kk);   // 32 bytes: 8 tf32 or 16 bf16
-                                tc::mma_tf32(d, dah + kj, dbh + kj, t1.x, 1u);   // a_hi x b_hi
-                                tc::mma_bf16(d, dac + kj, dbc + kj, t1.y, 1u);   // [a_hi|a_lo] x [b_lo|b_hi]
+                                const uint64_t kj = (uint64_t)(2 * kk);   // 32 bytes: 16 bf16
+                                tc::mma_bf16(d, da + kj, dbh + kj, id, 1u);   // [a_hi|a_lo] x [b_hi|b_hi]
+                                tc::mma_bf16(d, da + kj, dbl + kj, id, 1u);   // [a_hi|a_lo] x [b_lo|b_lo]
                             }
                         }
                         tc::commit(&b_empty[sb]);
@@ -703,18 +681,15 @@ bool make_gplan(const Problem &pb, const Args *a, GPlan *out)
     p.dw_lo = lo[2];
     p.hspan = MHT + hi[1] - lo[1];
     p.wspan = QWT + hi[2] - lo[2];
-    p.a_half = (uint32_t)((p.hspan * p.wspan * 128 + 1023) & ~1023);
-    for (int nq = 1; nq <= 4; ++nq) {
-        p.idesc_t[nq] = tc::idesc(2, 2 * nq * pb.Cog, BM);
-        p.idesc_b[nq] = tc::idesc(1, 2 * nq * pb.Cog, BM);
-    }
+    p.a_slot = (uint32_t)((p.hspan * p.wspan * 128 + 1023) & ~1023);
+    for (int nq = 1; nq <= 4; ++nq) p.idesc_b[nq] = tc::idesc(1, 2 * nq * pb.Cog, BM);
     p.set_cols = (uint32_t)(8 * pb.C_out);
     uint32_t cols = 32;
     while (cols < 2 * p.set_cols) cols <<= 1;
     p.tmem_cols = cols;
     p.bslot = (uint32_t)BROWS * 128u;
     const size_t budget = 227 * 1024 - 2048;
-    const size_t a_area = (size_t)NA * 2 * p.a_half;
+    const size_t a_area = (size_t)NA * p.a_slot;
     if (a_area + 2 * (size_t)p.bslot > budget) return false;
     int nb = (int)((budget - a_area) / p.bslot);
     if (nb >= 8) { nb = 8; p.npb = 4; }
@@ -743,7 +718,7 @@ size_t tc3dg_workspace_bytes(const Problem &pb)
 {
     GPlan pl;
     if (!make_gplan(pb, nullptr, &pl)) return 0;
-    return 2 * pl.x_bytes + pl.w_bytes;
+    return pl.x_bytes + pl.w_bytes;
 }
 
 cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
@@ -752,38 +727,32 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
     if (!make_gplan(pb, &a, &pl)) return cudaErrorNotSupported;
     const GParams &p = pl.p;
     uint8_t *ws = static_cast<uint8_t *>(a.ws);
-    float *xhi = reinterpret_cast<float *>(ws);
-    uint16_t *xc = reinterpret_cast<uint16_t *>(ws + pl.x_bytes);
-    uint8_t *wp = ws + 2 * pl.x_bytes;
+    uint16_t *xc = reinterpret_cast<uint16_t *>(ws);
+    uint8_t *wp = ws + pl.x_bytes;
 
-    // 1) one launch: x -> (N, D, W, H, 32) tf32 parts and (N, D, W, H, 64) bf16
-    // [hi | lo]; weights -> one panel per input offset (tf32 rows, then bf16
-    // correction rows)
+    // 1) one launch: x -> (N, D, W, H, 64) bf16 [hi | lo] per group; weights ->
+    // one panel per input offset (hi rows, then lo rows)
     const int64_t SP = pb.in_sp();
     const int64_t nbx = (SP + 63) / 64;
     const int64_t nxb = nbx * pb.N;
     const int64_t nblocks = nxb + (int64_t)p.ne * 2 * kWSlices;
     if (nblocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    prepg_kernel<<<(unsigned)nblocks, 256, 0, a.stream>>>(static_cast<const float *>(a.x), xhi, xc, pb.Li[0],
+    prepg_kernel<<<(unsigned)nblocks, 256, 0, a.stream>>>(static_cast<const float *>(a.x), xc, pb.Li[0],
                                                          pb.Li[1], pb.Li[2], pb.Cig, (int)nbx, (int)nxb,
                                                          static_cast<const float *>(a.w), wp, pl.wq);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // 3) tensor maps: A over x_t (fp32) and x_c (bf16) viewed as (C, H, W, D, N),
-    // one window per box, 128-byte rows; B over the panels (32 x 4 bytes, rows),
-    // boxes of 4 x Cog and 16 x Cog rows
-    CUtensorMap tmXh, tmXc, tmW[2];
-    const uint64_t adims[5] = {(uint64_t)CK, (uint64_t)pb.Li[1], (uint64_t)pb.Li[2], (uint64_t)pb.Li[0],
-                               (uint64_t)pb.N};
+    // 2) tensor maps: A over x_c (bf16) viewed as (C, H, W, D, N), one window per
+    // box, 128-byte rows; B over the panels (32 x 4 bytes, rows), boxes of
+    // 4 x Cog and 16 x Cog rows
+    CUtensorMap tmXc, tmW[2];
     const uint64_t cdims[5] = {(uint64_t)(2 * CK), (uint64_t)pb.Li[1], (uint64_t)pb.Li[2], (uint64_t)pb.Li[0],
                                (uint64_t)pb.N};
     const uint64_t astr[4] = {(uint64_t)CK * 4, (uint64_t)CK * pb.Li[1] * 4, (uint64_t)CK * pb.Li[1] * pb.Li[2] * 4,
                               (uint64_t)CK * pb.Li[1] * pb.Li[2] * pb.Li[0] * 4};
-    const uint32_t abox[5] = {(uint32_t)CK, (uint32_t)p.hspan, (uint32_t)p.wspan, 1u, 1u};
     const uint32_t cbox[5] = {(uint32_t)(2 * CK), (uint32_t)p.hspan, (uint32_t)p.wspan, 1u, 1u};
-    if (!encode_tiled(&tmXh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, xhi, adims, astr, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&tmXc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc, cdims, astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_tiled(&tmXc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc, cdims, astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const uint64_t bdims[2] = {(uint64_t)CK, (uint64_t)pl.rows};
     const uint64_t bstr[1] = {(uint64_t)CK * 4};
@@ -796,14 +765,14 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
     }
 
     int per_sm = 0;
-    e = prepare_kernel((const void *)&tc3dg_tf32_kernel, kThreads, pl.smem, &per_sm);
+    e = prepare_kernel((const void *)&tc3dg_split_kernel, kThreads, pl.smem, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     unsigned int *status = device_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.nunits) grid = p.nunits;
-    return launch_dependent(tc3dg_tf32_kernel, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXh, tmXc,
+    return launch_dependent(tc3dg_split_kernel, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXc,
                             tmW[0], tmW[1], a.bias, a.y, p, status);
 }
 

@@ -443,6 +443,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // contiguous bytes; the tile pitch of 33 words keeps the store side free of
 // bank conflicts.
 constexpr int RB = 64;                    // channels and columns per repack block
+constexpr int RX = 128;                   // x positions per repack block: two halves of RB
 
 __device__ __forceinline__ void repack_load_pairs(const bf16_t *__restrict__ src, int64_t row_stride,
                                                   int ncols, uint32_t (*tile)[33])
@@ -463,19 +464,43 @@ __device__ __forceinline__ void repack_load_pairs(const bf16_t *__restrict__ src
 }
 
 // x (N, C, D, H, W) -> x_t (N, D, H, W, C); D*H*W a multiple of 8, C of 64.
-// Block (bx, by, n): positions bx*64.., channels by*64...
+// Block (bx, by, n): positions bx*128.., channels by*64..: each channel row
+// is read as 256 contiguous bytes, and all four 16-byte loads of a thread are
+// in flight before the first shared-memory store.
 __device__ __forceinline__ void repack_x_block(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, int C, int D,
                                                int H, int W, int bx, int by, int n)
 {
-    __shared__ uint32_t tile[RB][33];
+    __shared__ uint32_t tile[RX][33];
     const int64_t SP = (int64_t)D * H * W;
     const int c0 = by * RB;
-    const int64_t s0 = (int64_t)bx * RB;
-    const int ncols = (int)((SP - s0) < RB ? (SP - s0) : RB);
-    repack_load_pairs(x + ((int64_t)n * C + c0) * SP + s0, SP, ncols, tile);
+    const int64_t s0 = (int64_t)bx * RX;
+    const int ncols = (int)((SP - s0) < RX ? (SP - s0) : RX);
+    const bf16_t *src = x + ((int64_t)n * C + c0) * SP + s0;
+    const int icp = threadIdx.x >> 3, k8 = threadIdx.x & 7;
+    uint4 v[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int col = h * RB + k8 * 8;
+        v[h][0] = v[h][1] = make_uint4(0, 0, 0, 0);
+        if (col < ncols) {
+            v[h][0] = __ldcs(reinterpret_cast<const uint4 *>(src + (int64_t)(2 * icp) * SP + col));
+            v[h][1] = __ldcs(reinterpret_cast<const uint4 *>(src + (int64_t)(2 * icp + 1) * SP + col));
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int col = h * RB + k8 * 8;
+        const uint32_t a[4] = {v[h][0].x, v[h][0].y, v[h][0].z, v[h][0].w};
+        const uint32_t b[4] = {v[h][1].x, v[h][1].y, v[h][1].z, v[h][1].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            tile[col + 2 * j][icp] = __byte_perm(a[j], b[j], 0x5410);
+            tile[col + 2 * j + 1][icp] = __byte_perm(a[j], b[j], 0x7632);
+        }
+    }
     __syncthreads();
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < 4; ++t) {
         const int o = threadIdx.x + 256 * t;
         const int q = o & 7, row = o >> 3;
         if (row < ncols) {
@@ -722,9 +747,10 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     // 1) x -> (N, D, H, W, C) and weights -> panels: one launch when D*H*W is
     // a multiple of 8, else the scalar x repack and the weight repack
     const int64_t SP = pb.in_sp();
-    const int64_t nbx = (SP + 63) / 64, nby = (pb.C_in + 63) / 64;
+    const int64_t nby = (pb.C_in + 63) / 64;
     cudaError_t e;
     if (SP % 8 == 0) {
+        const int64_t nbx = (SP + RX - 1) / RX;
         const int64_t nxb = nbx * nby * pb.N;
         const int64_t nblocks = nxb + (int64_t)(pb.C_in / RB) * pb.C_out;
         if (nblocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -732,6 +758,7 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
                                                               pb.Li[0], pb.Li[1], pb.Li[2], (int)nbx, (int)nby,
                                                               (int)nxb, static_cast<const bf16_t *>(a.w), wp, pl.wq);
     } else {
+        const int64_t nbx = (SP + 63) / 64;
         dim3 gx((unsigned)nbx, (unsigned)nby, (unsigned)pb.N);
         if (gx.x > 0x7fffffffu || gx.y > 65535 || gx.z > 65535) return cudaErrorInvalidConfiguration;
         repack_x_scalar_kernel<<<gx, 256, 0, a.stream>>>(static_cast<const bf16_t *>(a.x), xt, pb.C_in, pb.Li[0],

@@ -325,6 +325,32 @@ def test_2d_generic_shapes(k):
     cc.assert_close(y, cc.run_oracle(c, t), c["dtype"], "2-D generic case %d %r" % (k, c))
 
 
+# The two-term bf16 split of the FP32 3-D / 2-D kernels: every product is
+# (x_hi + x_lo)(w_hi + w_lo) with each part's bf16 product exact, so the error
+# of an output is bounded by a small multiple of 2^-16 times the sum of the
+# magnitudes of its products, S = sum |x| |w| (plus fp32 accumulation).  S is
+# the oracle run on |x|, |w| without bias.
+SPLIT_CASES = [("convT3d_add_hswish", dict(N=1), False), ("convT3d_grouped", dict(N=1), False),
+               ("convT2d_f32", dict(N=1), False)]
+
+
+@pytest.mark.parametrize("k", range(len(SPLIT_CASES)))
+def test_fp32_split_error_bound(k):
+    name, over, _ = SPLIT_CASES[k]
+    c = cc.case_from_config(name, N=over["N"])
+    c["add"] = False                      # the bound concerns the convolution itself
+    assert path_of(c) in ("tc3d_bf16split", "tc3dg_bf16split"), path_of(c)
+    t = cc.make_inputs(c, seed=1400 + k, bound=workloads.CONFIGS[name]["bound"])
+    y = cc.run_gpu(c, t).cpu().numpy().astype(np.float64)
+    ref = cc.run_oracle(c, t)
+    mag = dict(t, x=np.abs(t["x"]), w=np.abs(t["w"]), bias=None)
+    S = cc.run_oracle(dict(c, bias=False), mag)
+    ratio = np.abs(y - ref) / (S + 1e-30)
+    worst = float(ratio.max())
+    print("%s: max |err| / sum|x||w| = %.3g (2^%.1f)" % (name, worst, np.log2(max(worst, 1e-300))))
+    assert worst < 2.0 ** -14, (name, worst)
+
+
 def test_fp32_3d_without_workspace_takes_ffma():
     """A call given no workspace runs the FFMA kernel, with the same result."""
     import torch

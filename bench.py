@@ -225,6 +225,11 @@ def _inputs_to_device(cfg_name, dev, pinned=False, batch=None):
         host["w"] = torch.from_numpy(t["w"])
     host["bias"] = torch.from_numpy(t["bias"]) if t["bias"] is not None else None
     host["add"] = torch.from_numpy(t["add"]) if t["add"] is not None else None
+    if cfg.get("layout", "cf") == "cl":
+        # channels-last workloads store x (and add) as (N, spatial..., C)
+        for k in ("x", "add"):
+            if host[k] is not None:
+                host[k] = host[k].movedim(1, -1).contiguous()
     if pinned:
         host = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
     devt = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
@@ -248,11 +253,20 @@ class Runner:
         self.host, self.d = _inputs_to_device(cfg_name, dev, pinned=True, batch=batch)
         wm = work_model(self.cfg)
         self.wm = wm
-        self.y = torch.empty(wm["out_shape"], dtype=torch.float32, device=dev)
-        self.y_host = torch.empty(wm["out_shape"], dtype=torch.float32).pin_memory()
+        self.cl = self.cfg.get("layout", "cf") == "cl"
+        y_shape = list(wm["out_shape"])
+        if self.cl:
+            y_shape = [y_shape[0]] + y_shape[2:] + [y_shape[1]]
+        self.y = torch.empty(y_shape, dtype=torch.float32, device=dev)
+        self.y_host = torch.empty(y_shape, dtype=torch.float32).pin_memory()
         c = self.cfg
         self.dt = ct.CT_BF16 if c["dtype"] == "bf16" else ct.CT_F32
-        if c["nd"] == 1:
+        if self.cl:
+            args = (c["nd"], c["N"], c["C_in"], c["C_out"], c["L_in"], c["k"], c["groups"], c["stride"],
+                    c["padding"], c["output_padding"], c["dilation"], self.dt)
+            self.ws_bytes = ct.ct_workspace_size_cl(*args)
+            self.path = ct.ct_path_cl(*args, c["add"])
+        elif c["nd"] == 1:
             self.ws_bytes = ct.ct_workspace_size_1d(c["N"], c["C_in"], c["C_out"], c["L_in"][0], c["k"][0],
                                                     c["groups"], c["stride"][0], c["padding"][0],
                                                     c["output_padding"][0], c["dilation"][0], self.dt)
@@ -277,16 +291,21 @@ class Runner:
                    if self.ws_bytes else None)
         # kernels the library launches per forward pass on this path
         # (a prep / repack launch, then the GEMM kernel; the bf16 repack splits in
-        # two when D*H*W is not a multiple of 8)
+        # two when D*H*W is not a multiple of 8; channels last it is the weight
+        # repack alone)
         in_sp = int(np.prod(c["L_in"]))
-        self.launches_per_step = {"umma_bf16": 2 if in_sp % 8 == 0 else 3, "tc3d_bf16split": 2,
+        self.launches_per_step = {"umma_bf16": 2 if (in_sp % 8 == 0 or self.cl) else 3, "tc3d_bf16split": 2,
                                   "tc3dg_bf16split": 2}.get(self.path, 1)
 
     def forward(self, stream, d=None, y=None):
         c, ct = self.cfg, self.ct
         d = self.d if d is None else d
         y_out = self.y if y is None else y
-        if c["nd"] == 1:
+        if self.cl:
+            ct.ct_forward_cl(c["nd"], d["x"], d["w"], d["bias"], d["add"], y_out, c["N"], c["C_in"],
+                             c["C_out"], c["L_in"], c["k"], c["groups"], c["stride"], c["padding"],
+                             c["output_padding"], c["dilation"], self.dt, self.ws, self.ws_bytes, stream)
+        elif c["nd"] == 1:
             ct.ct_forward_1d(d["x"], d["w"], d["bias"], y_out, c["N"], c["C_in"], c["C_out"],
                              c["L_in"][0], c["k"][0], c["groups"], c["stride"][0], c["padding"][0],
                              c["output_padding"][0], c["dilation"][0], self.dt, self.ws,

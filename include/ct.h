@@ -134,6 +134,27 @@ ct_status ct_forward_2d_add_hswish(const void *x, const void *w, const float *bi
                                    const int dilation[2], ct_dtype dtype,
                                    void *workspace, size_t ws_bytes, void *stream);
 
+/* Channels-last layouts, for 1-D, 2-D or 3-D (nd = 1, 2, 3; the array
+ * arguments have nd entries, outermost spatial dimension first): x (N,
+ * spatial..., C_in), y and add (N, spatial out..., C_out), w (C_in,
+ * C_out/groups, k...) as in the other calls.  The same operator as
+ * ct_forward_1d/2d/3d (and, with add != NULL, the fused epilogue of
+ * ct_forward_3d_add_hswish; add may equal y), only the memory order of x, y
+ * and add differs: channels are the fastest index.  A bf16 call of a shape
+ * the bf16 tensor-core kernel takes (stride 2, even kernel extents, ...) reads
+ * x in place -- no repacked copy -- and needs workspace only for the weight
+ * panels (ct_workspace_size_cl); x and y then need 16-byte alignment.  Other
+ * shapes run the generic kernel.  Errors as ct_forward_3d. */
+ct_status ct_workspace_size_cl(int nd, int N, int C_in, int C_out, const int *in_size, const int *k,
+                               int groups, const int *stride, const int *padding,
+                               const int *output_padding, const int *dilation, ct_dtype dtype,
+                               size_t *bytes);
+ct_status ct_forward_cl(int nd, const void *x, const void *w, const float *bias, const float *add,
+                        float *y, int N, int C_in, int C_out, const int *in_size, const int *k,
+                        int groups, const int *stride, const int *padding,
+                        const int *output_padding, const int *dilation, ct_dtype dtype,
+                        void *workspace, size_t ws_bytes, void *stream);
+
 /* Fused ConvTranspose3d + add + x*hardswish(x) ([l2_p26]):
  *     t = convT(x) + bias + add;  y = t * (t * clamp(t + 3, 0, 6) / 6).
  * add has the shape of y (fp32) and must not be NULL; y may equal add. */
@@ -178,7 +199,8 @@ ct_status ct_forward_3d_noalloc(const void *x, const void *w, const float *bias,
                                 ct_dtype dtype, void *stream);
 
 /* Name of the kernel family the 1-D / 2-D / 3-D / fused call with these arguments
- * would launch when given the workspace ct_workspace_size_* reports
+ * (ct_path_cl: in channels-last layouts) would launch when given the workspace
+ * ct_workspace_size_* reports
  * ("gather_generic", "phase1d_f32", "tc1d_tf32x3", "phase3d_f32", "tc3d_bf16split",
  * "tc3dg_bf16split" -- 32 input channels in 1, 2 or 4 groups -- or "umma_bf16"),
  * or NULL if the arguments are invalid.  Host only; launches
@@ -189,6 +211,9 @@ const char *ct_path_2d(int N, int C_in, int C_out, const int in_hw[2], const int
                        int groups, const int stride[2], const int padding[2],
                        const int output_padding[2], const int dilation[2], ct_dtype dtype,
                        int fused);
+const char *ct_path_cl(int nd, int N, int C_in, int C_out, const int *in_size, const int *k, int groups,
+                       const int *stride, const int *padding, const int *output_padding,
+                       const int *dilation, ct_dtype dtype, int fused);
 const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
                        int groups, const int stride[3], const int padding[3],
                        const int output_padding[3], const int dilation[3], ct_dtype dtype,

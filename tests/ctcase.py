@@ -14,7 +14,7 @@ def case_from_config(name, N=None):
     return dict(nd=c["nd"], N=c["N"] if N is None else N, C_in=c["C_in"], C_out=c["C_out"],
                 G=c["groups"], L=list(c["L_in"]), K=list(c["k"]), S=list(c["stride"]),
                 P=list(c["padding"]), OP=list(c["output_padding"]), DL=list(c["dilation"]),
-                bias=c["bias"], add=c["add"], dtype=c["dtype"])
+                bias=c["bias"], add=c["add"], dtype=c["dtype"], layout=c.get("layout", "cf"))
 
 
 def out_shape(c):
@@ -61,6 +61,15 @@ def run_gpu(c, t, dev="cuda:0", inplace_add=False):
     import transposed_convolution_convtranspose_gb300 as ct
     x, w, b, a = to_device(t, c, dev)
     kw = kwargs(c)
+    if c.get("layout", "cf") == "cl":
+        # channels-last call on the same values; the result is returned in the
+        # oracle's channels-first order
+        xcl = x.movedim(1, -1).contiguous()
+        acl = a.movedim(1, -1).contiguous() if a is not None else None
+        if c["nd"] == 1:
+            kw = {k: (v if k == "groups" else (v,)) for k, v in kw.items()}
+        y = ct.conv_transpose_cl(xcl, w, b, acl, out=acl if inplace_add else None, **kw)
+        return y.movedim(-1, 1).contiguous()
     if c["nd"] == 1:
         y = ct.conv_transpose1d(x, w, b, **kw)
     elif c["nd"] == 2:

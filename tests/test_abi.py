@@ -170,6 +170,29 @@ def test_path_selection_2d(lib):
     assert nb2 >= 32 * 64 * 128 * 128 * 2 + 4 * 4 * 64 * 64 * 2
 
 
+def test_path_selection_channels_last(lib):
+    """Channels-last calls: bf16 shapes of the bf16 tensor-core kernel take it
+    (x read in place: workspace only for the weight panels), the rest the
+    generic kernel."""
+    dense = (16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1))
+    assert ct.ct_path_cl(3, *dense, ct.CT_BF16) == "umma_bf16"
+    assert ct.ct_path_cl(3, *dense, ct.CT_BF16, fused=True) == "gather_generic"
+    assert ct.ct_path_cl(3, *dense, ct.CT_F32) == "gather_generic"
+    d2 = (16, 256, 128, (64, 64), (4, 4), 1, (2, 2), (1, 1), (0, 0), (1, 1))
+    assert ct.ct_path_cl(2, *d2, ct.CT_BF16) == "umma_bf16"
+    assert ct.ct_path_cl(1, 16, 32, 64, (131072,), (3,), 1, (2,), (1,), (0,), (2,), ct.CT_F32) == "gather_generic"
+    n_cf = ct.ct_workspace_size_3d(*dense, ct.CT_BF16)
+    n_cl = ct.ct_workspace_size_cl(3, *dense, ct.CT_BF16)
+    x_bytes = 16 * 256 * 16 ** 3 * 2
+    assert n_cl == n_cf - x_bytes and n_cl >= 8 * 128 * 8 * 256 * 2
+    assert ct.ct_workspace_size_cl(3, *dense, ct.CT_F32) == 0
+    assert ct.ct_path_cl(4, *dense, ct.CT_BF16) is None
+    with pytest.raises(ct.CTError) as e:
+        ct.ct_workspace_size_cl(3, 1, 4, 8, (4, 4, 4), (3, 3, 3), 3, (2, 2, 2), (1, 1, 1), (0, 0, 0),
+                                (1, 1, 1), ct.CT_F32)
+    assert e.value.code == ct.CT_ERR_SHAPE
+
+
 def test_workspace_sizes(lib):
     assert ct.ct_workspace_size_1d(16, 32, 64, 131072, 3, 1, 2, 1, 0, 2, ct.CT_F32) == 0
     # FP32 3-D tensor-core path: a channels-last copy of x as bf16 (hi, lo)

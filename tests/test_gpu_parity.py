@@ -35,6 +35,9 @@ def _sync():
 def path_of(c):
     import transposed_convolution_convtranspose_gb300 as ct
     dt = ct.CT_BF16 if c["dtype"] == "bf16" else ct.CT_F32
+    if c.get("layout", "cf") == "cl":
+        return ct.ct_path_cl(c["nd"], c["N"], c["C_in"], c["C_out"], c["L"], c["K"], c["G"], c["S"],
+                             c["P"], c["OP"], c["DL"], dt, c["add"])
     if c["nd"] == 1:
         return ct.ct_path_1d(c["N"], c["C_in"], c["C_out"], c["L"][0], c["K"][0], c["G"], c["S"][0],
                              c["P"][0], c["OP"][0], c["DL"][0], dt)
@@ -52,7 +55,7 @@ def path_of(c):
 REDUCED = {"convT1d_tiny": dict(N=2), "convT1d_L131072": dict(N=1),
            "convT3d_grouped": dict(N=2), "convT3d_add_hswish": dict(N=2),
            "convT3d_bf16_dense": dict(N=1, L=[8, 8, 8]), "convT2d_f32": dict(N=1),
-           "convT2d_bf16_dense": dict(N=1, L=[32, 32])}
+           "convT2d_bf16_dense": dict(N=1, L=[32, 32]), "convT3d_bf16_dense_cl": dict(N=1, L=[8, 8, 8])}
 
 
 @pytest.mark.parametrize("name", CONFIGS)
@@ -72,7 +75,7 @@ def test_config_integer_exact(name):
     so the conv + bias result is exact in any order (the fused epilogue's
     division by 6 is compared at fp32 tolerance instead)."""
     c = cc.case_from_config(name, N=1)
-    if name == "convT3d_bf16_dense":
+    if name in ("convT3d_bf16_dense", "convT3d_bf16_dense_cl"):
         c["L"] = [8, 8, 8]
     elif name == "convT2d_bf16_dense":
         c["L"] = [32, 32]
@@ -349,6 +352,101 @@ def test_fp32_split_error_bound(k):
     worst = float(ratio.max())
     print("%s: max |err| / sum|x||w| = %.3g (2^%.1f)" % (name, worst, np.log2(max(worst, 1e-300))))
     assert worst < 2.0 ** -14, (name, worst)
+
+
+# Shapes with s > (k - 1) d: the stride phases do not overlap, every output
+# receives at most one tap per dimension (some none), and a scatter
+# formulation would write disjoint outputs.  The gather kernels compute each
+# output once in any case; integer inputs make every result exact.  Covers the
+# FP32 and bf16 3-D tensor-core kernels (s = 2, k = 2) and the generic kernel
+# (s = 3, 4; 1-D, 2-D, 3-D, groups).
+DISJOINT = [
+    dict(nd=1, N=2, C_in=8, C_out=16, G=1, L=[300], K=[2], S=[3], P=[0], OP=[2], DL=[1], dtype="f32"),
+    dict(nd=1, N=1, C_in=4, C_out=4, G=2, L=[77], K=[3], S=[4], P=[1], OP=[3], DL=[1], dtype="f32"),
+    dict(nd=3, N=1, C_in=32, C_out=32, G=1, L=[4, 6, 8], K=[2, 2, 2], S=[2, 2, 2], P=[0, 0, 0],
+         OP=[1, 0, 0], DL=[1, 1, 1], dtype="f32"),
+    dict(nd=3, N=1, C_in=64, C_out=32, G=1, L=[3, 4, 8], K=[2, 2, 2], S=[2, 2, 2], P=[0, 0, 0],
+         OP=[0, 0, 0], DL=[1, 1, 1], dtype="bf16"),
+    dict(nd=3, N=1, C_in=6, C_out=9, G=3, L=[3, 4, 5], K=[3, 2, 3], S=[3, 3, 4], P=[1, 0, 2],
+         OP=[2, 1, 0], DL=[1, 1, 1], dtype="f32"),
+    dict(nd=2, N=2, C_in=5, C_out=7, G=1, L=[6, 9], K=[2, 3], S=[3, 4], P=[0, 1], OP=[1, 3], DL=[1, 1],
+         dtype="f32"),
+]
+
+
+@pytest.mark.parametrize("k", range(len(DISJOINT)))
+def test_disjoint_phase_shapes_exact(k):
+    c = dict(DISJOINT[k], bias=True, add=False)
+    if k in (2, 3):
+        assert path_of(c) in ("tc3d_bf16split", "umma_bf16"), path_of(c)
+    t = cc.make_inputs(c, seed=1500 + k, int_range=3)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    ref = cc.run_oracle(c, t)
+    assert y.shape == ref.shape
+    assert np.array_equal(y.astype(np.float64), ref), "disjoint case %d (%s) not exact" % (k, path_of(c))
+
+
+# Channels-last layouts (x (N, spatial..., C_in), y and add (N, spatial...,
+# C_out)): the inputs are the same draws moved to channels-last on the device,
+# the result is moved back and compared with the oracle.  bf16 shapes of the
+# bf16 tensor-core kernel (3-D and 2-D: x read in place), and the generic
+# kernel for FP32, groups, 1-D and the fused epilogue (also in place).
+CL = [
+    dict(nd=3, N=1, C_in=64, C_out=16, G=1, L=[2, 3, 8], K=[4] * 3, S=[2] * 3, P=[1] * 3, OP=[1, 0, 0],
+         DL=[1] * 3, dtype="bf16", add=False, path="umma_bf16"),
+    dict(nd=3, N=2, C_in=128, C_out=128, G=1, L=[2, 4, 16], K=[4] * 3, S=[2] * 3, P=[1] * 3,
+         OP=[0] * 3, DL=[1] * 3, dtype="bf16", add=False, path="umma_bf16"),
+    dict(nd=3, N=1, C_in=64, C_out=256, G=1, L=[2, 2, 8], K=[4] * 3, S=[2] * 3, P=[1] * 3,
+         OP=[1, 1, 0], DL=[1] * 3, dtype="bf16", add=False, path="umma_bf16"),
+    dict(nd=3, N=1, C_in=64, C_out=48, G=1, L=[2, 2, 9], K=[2] * 3, S=[2] * 3, P=[1] * 3, OP=[0] * 3,
+         DL=[1] * 3, dtype="bf16", add=False, path="umma_bf16"),
+    dict(nd=2, N=2, C_in=128, C_out=128, G=1, L=[5, 12], K=[4, 4], S=[2, 2], P=[1, 1], OP=[1, 0],
+         DL=[1, 1], dtype="bf16", add=False, path="umma_bf16"),
+    dict(nd=3, N=1, C_in=32, C_out=64, G=1, L=[3, 4, 8], K=[3] * 3, S=[2] * 3, P=[1] * 3, OP=[1] * 3,
+         DL=[1] * 3, dtype="f32", add=True, path="gather_generic"),
+    dict(nd=3, N=2, C_in=6, C_out=4, G=2, L=[3, 4, 5], K=[2, 3, 4], S=[3, 1, 2], P=[1, 0, 2], OP=[2, 0, 1],
+         DL=[1, 2, 1], dtype="f32", add=False, path="gather_generic"),
+    dict(nd=2, N=2, C_in=8, C_out=8, G=4, L=[4, 6], K=[3, 3], S=[2, 2], P=[1, 1], OP=[1, 1], DL=[1, 1],
+         dtype="f32", add=False, path="gather_generic"),
+    dict(nd=1, N=2, C_in=32, C_out=64, G=1, L=[777], K=[3], S=[2], P=[1], OP=[0], DL=[2], dtype="f32",
+         add=False, path="gather_generic"),
+    dict(nd=3, N=1, C_in=64, C_out=32, G=1, L=[3, 3, 4], K=[3] * 3, S=[2] * 3, P=[1] * 3, OP=[1] * 3,
+         DL=[1] * 3, dtype="bf16", add=True, path="gather_generic"),
+]
+
+
+def _path_cl(c):
+    import transposed_convolution_convtranspose_gb300 as ct
+    dt = ct.CT_BF16 if c["dtype"] == "bf16" else ct.CT_F32
+    return ct.ct_path_cl(c["nd"], c["N"], c["C_in"], c["C_out"], c["L"], c["K"], c["G"], c["S"], c["P"],
+                         c["OP"], c["DL"], dt, c["add"])
+
+
+def _run_cl(c, t, inplace=False):
+    import transposed_convolution_convtranspose_gb300 as ct
+    x, w, b, a = cc.to_device(t, c, "cuda:0")
+    xcl = x.movedim(1, -1).contiguous()
+    acl = a.movedim(1, -1).contiguous() if a is not None else None
+    kw = cc.kwargs(c)
+    if c["nd"] == 1:
+        kw = {k: (v if k == "groups" else (v,)) for k, v in kw.items()}
+    y = ct.conv_transpose_cl(xcl, w, b, acl, out=acl if inplace else None, **kw)
+    return y.movedim(-1, 1).contiguous().cpu().numpy()
+
+
+@pytest.mark.parametrize("k", range(len(CL)))
+def test_channels_last_shapes(k):
+    c = dict(CL[k], bias=bool(k % 2 == 0))
+    want = c.pop("path")
+    assert _path_cl(c) == want, (c, _path_cl(c))
+    t = cc.make_inputs(c, seed=1600 + k)
+    ref = cc.run_oracle(c, t)
+    cc.assert_close(_run_cl(c, t), ref, c["dtype"], "channels-last case %d %r" % (k, c))
+    if c["add"]:
+        cc.assert_close(_run_cl(c, t, inplace=True), ref, c["dtype"], "channels-last in place %d" % k)
+    if k in (1, 6):
+        ti = cc.make_inputs(c, seed=1650 + k, int_range=3)
+        assert np.array_equal(_run_cl(c, ti).astype(np.float64), cc.run_oracle(c, ti)), "cl integer %d" % k
 
 
 def test_fp32_3d_without_workspace_takes_ffma():

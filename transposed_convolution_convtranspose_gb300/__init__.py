@@ -29,6 +29,7 @@ CT_STATUS = {0: "CT_OK", 1: "CT_ERR_ARG", 2: "CT_ERR_SHAPE", 3: "CT_ERR_ALIGN",
 EXPORTED = ["ct_out_len", "ct_workspace_size_1d", "ct_workspace_size_2d", "ct_workspace_size_3d",
             "ct_forward_1d", "ct_forward_2d", "ct_forward_2d_add_hswish", "ct_forward_3d",
             "ct_forward_3d_add_hswish", "ct_path_1d", "ct_path_2d", "ct_path_3d",
+            "ct_workspace_size_cl", "ct_forward_cl", "ct_path_cl",
             "ct_set_path_override", "ct_status_str", "ct_last_device_error",
             "ct_forward_3d_noalloc", "ct_selftest_wait_timeout"]
 
@@ -72,6 +73,15 @@ def _setup(lib):
                                              _I2, _I2, _I2, _I, _P, ctypes.c_size_t, _P]
     lib.ct_path_2d.restype = ctypes.c_char_p
     lib.ct_path_2d.argtypes = [_I, _I, _I, _I2, _I2, _I, _I2, _I2, _I2, _I2, _I, _I]
+    _IP = ctypes.POINTER(_I)
+    lib.ct_workspace_size_cl.restype = _I
+    lib.ct_workspace_size_cl.argtypes = [_I, _I, _I, _I, _IP, _IP, _I, _IP, _IP, _IP, _IP, _I,
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.ct_forward_cl.restype = _I
+    lib.ct_forward_cl.argtypes = [_I, _P, _P, _P, _P, _P, _I, _I, _I, _IP, _IP, _I, _IP, _IP, _IP, _IP,
+                                  _I, _P, ctypes.c_size_t, _P]
+    lib.ct_path_cl.restype = ctypes.c_char_p
+    lib.ct_path_cl.argtypes = [_I, _I, _I, _I, _IP, _IP, _I, _IP, _IP, _IP, _IP, _I, _I]
     lib.ct_forward_1d.restype = _I
     lib.ct_forward_1d.argtypes = [_P, _P, _P, _P] + [_I] * 10 + [_I, _P, ctypes.c_size_t, _P]
     lib.ct_forward_3d.restype = _I
@@ -138,6 +148,13 @@ def _i2(v):
     if len(v) != 2:
         raise ValueError("expected 2 values (H, W)")
     return _I2(*v)
+
+
+def _ivec(v):
+    v = tuple(int(t) for t in v)
+    if not 1 <= len(v) <= 3:
+        raise ValueError("expected 1 to 3 values")
+    return (_I * len(v))(*v)
 
 
 def _i3(v):
@@ -246,6 +263,33 @@ def ct_forward_3d_noalloc(x, w, bias, y, N, C_in, C_out, in_dhw, k_dhw, groups, 
 def ct_path_1d(N, C_in, C_out, L_in, k, groups, stride, padding, output_padding, dilation, dtype):
     r = load().ct_path_1d(N, C_in, C_out, L_in, k, groups, stride, padding, output_padding,
                           dilation, dtype)
+    return None if r is None else r.decode()
+
+
+def ct_workspace_size_cl(nd, N, C_in, C_out, in_size, k, groups, stride, padding, output_padding,
+                         dilation, dtype):
+    n = ctypes.c_size_t(0)
+    _check(load().ct_workspace_size_cl(nd, N, C_in, C_out, _ivec(in_size), _ivec(k), groups,
+                                       _ivec(stride), _ivec(padding), _ivec(output_padding),
+                                       _ivec(dilation), dtype, ctypes.byref(n)),
+           "ct_workspace_size_cl")
+    return int(n.value)
+
+
+def ct_forward_cl(nd, x, w, bias, add, y, N, C_in, C_out, in_size, k, groups, stride, padding,
+                  output_padding, dilation, dtype, workspace=None, ws_bytes=0, stream=None):
+    _check(load().ct_forward_cl(nd, _ptr(x), _ptr(w), _ptr(bias), _ptr(add), _ptr(y), N, C_in, C_out,
+                                _ivec(in_size), _ivec(k), groups, _ivec(stride), _ivec(padding),
+                                _ivec(output_padding), _ivec(dilation), dtype, _ptr(workspace),
+                                ws_bytes, _stream(stream)),
+           "ct_forward_cl")
+
+
+def ct_path_cl(nd, N, C_in, C_out, in_size, k, groups, stride, padding, output_padding, dilation,
+               dtype, fused=False):
+    r = load().ct_path_cl(nd, N, C_in, C_out, _ivec(in_size), _ivec(k), groups, _ivec(stride),
+                          _ivec(padding), _ivec(output_padding), _ivec(dilation), dtype,
+                          int(bool(fused)))
     return None if r is None else r.decode()
 
 
@@ -441,4 +485,41 @@ def conv_transpose2d_add_hswish(x, w, bias, add, stride=1, padding=0, output_pad
     ws = _workspace(nb, x.device)
     ct_forward_2d_add_hswish(x, w, bias, add, y, N, C_in, C_out, L, K, groups, S, P, OP, D, dt,
                              ws, nb, torch.cuda.current_stream(x.device))
+    return y
+
+
+def conv_transpose_cl(x, w, bias=None, add=None, stride=1, padding=0, output_padding=0, dilation=1,
+                      groups=1, out=None):
+    """Transposed convolution of a channels-last x (N, spatial..., C_in), 1 to 3
+    spatial dimensions; returns y (N, spatial out..., C_out) fp32.  With add
+    (channels-last, y's shape) the fused add + t*hardswish(t) epilogue."""
+    import torch
+    for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (add, "add"), (out, "out")):
+        _need(t, nm)
+    nd = x.dim() - 2
+    if not 1 <= nd <= 3 or w.dim() != nd + 2:
+        raise CTError(1, "conv_transpose_cl: x must be (N, spatial..., C_in), 1 to 3 spatial dims")
+
+    def vec(v):
+        v = (v,) * nd if isinstance(v, int) else tuple(int(t) for t in v)
+        if len(v) != nd:
+            raise ValueError("expected an int or %d values" % nd)
+        return v
+    S, P, OP, D = vec(stride), vec(padding), vec(output_padding), vec(dilation)
+    N, C_in = x.shape[0], x.shape[-1]
+    L = tuple(x.shape[1:-1])
+    K = tuple(w.shape[2:])
+    C_out = w.shape[1] * groups
+    dt = _dtype_code(x)
+    Lo = tuple(ct_out_len(L[i], K[i], S[i], P[i], OP[i], D[i]) for i in range(nd))
+    if min(Lo) < 1:
+        raise CTError(2, "conv_transpose_cl")
+    shape = (N,) + Lo + (C_out,)
+    if add is not None and (tuple(add.shape) != shape or add.dtype != torch.float32):
+        raise CTError(1, "conv_transpose_cl: add must be fp32 with the output's shape")
+    y = out if out is not None else torch.empty(shape, dtype=torch.float32, device=x.device)
+    nb = ct_workspace_size_cl(nd, N, C_in, C_out, L, K, groups, S, P, OP, D, dt)
+    ws = _workspace(nb, x.device)
+    ct_forward_cl(nd, x, w, bias, add, y, N, C_in, C_out, L, K, groups, S, P, OP, D, dt, ws, nb,
+                  torch.cuda.current_stream(x.device))
     return y

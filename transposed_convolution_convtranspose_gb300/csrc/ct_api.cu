@@ -102,6 +102,12 @@ Path choose_path(const Problem &pb, const Args *a)
 {
     const int ov = g_override.load();
     if (ov == 1) return Path::Generic;
+    if (pb.cl) {
+        // channels-last layouts: the bf16 tensor-core kernel reads x in place and
+        // writes y channels-last; every other shape takes the generic kernel
+        if (pb.dtype == CT_BF16 && pb.nd >= 2 && !pb.has_add && umma_supported(pb, a)) return Path::Umma;
+        return Path::Generic;
+    }
     if (pb.dtype == CT_F32) {
         if (ov != 2 && pb.nd == 1 && tc1d_supported(pb, a)) return Path::Tc1d;
         if (pb.nd == 1 && phase1d_supported(pb, a)) return Path::Phase1d;
@@ -360,6 +366,50 @@ const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const in
     if (make_problem(3, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding, output_padding,
                      dilation, dtype, false, fused != 0, &pb) != CT_OK)
         return nullptr;
+    return path_name(choose_path(pb, nullptr));
+}
+
+ct_status ct_workspace_size_cl(int nd, int N, int C_in, int C_out, const int *in_size, const int *k,
+                               int groups, const int *stride, const int *padding,
+                               const int *output_padding, const int *dilation, ct_dtype dtype,
+                               size_t *bytes)
+{
+    if (!bytes || !in_size || !k || !stride || !padding || !output_padding || !dilation) return CT_ERR_ARG;
+    Problem pb;
+    ct_status st = make_problem(nd, N, C_in, C_out, in_size, k, groups, stride, padding, output_padding,
+                                dilation, dtype, false, false, &pb);
+    if (st != CT_OK) return st;
+    pb.cl = true;
+    *bytes = workspace_bytes(pb);
+    return CT_OK;
+}
+
+ct_status ct_forward_cl(int nd, const void *x, const void *w, const float *bias, const float *add,
+                        float *y, int N, int C_in, int C_out, const int *in_size, const int *k,
+                        int groups, const int *stride, const int *padding,
+                        const int *output_padding, const int *dilation, ct_dtype dtype,
+                        void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!in_size || !k || !stride || !padding || !output_padding || !dilation) return CT_ERR_ARG;
+    Problem pb;
+    ct_status st = make_problem(nd, N, C_in, C_out, in_size, k, groups, stride, padding, output_padding,
+                                dilation, dtype, bias != nullptr, add != nullptr, &pb);
+    if (st != CT_OK) return st;
+    pb.cl = true;
+    Args a{x, w, bias, add, y, workspace, ws_bytes, (cudaStream_t)stream};
+    return run(pb, a);
+}
+
+const char *ct_path_cl(int nd, int N, int C_in, int C_out, const int *in_size, const int *k, int groups,
+                       const int *stride, const int *padding, const int *output_padding,
+                       const int *dilation, ct_dtype dtype, int fused)
+{
+    if (!in_size || !k || !stride || !padding || !output_padding || !dilation) return nullptr;
+    Problem pb;
+    if (make_problem(nd, N, C_in, C_out, in_size, k, groups, stride, padding, output_padding, dilation,
+                     dtype, false, fused != 0, &pb) != CT_OK)
+        return nullptr;
+    pb.cl = true;
     return path_name(choose_path(pb, nullptr));
 }
 

@@ -1,7 +1,7 @@
 // ct_gather_generic.cu -- gather ("output-stationary") transposed convolution
-// for any valid problem: 1-D or 3-D, any groups, stride, padding,
+// for any valid problem: 1-D, 2-D or 3-D, any groups, stride, padding,
 // output_padding, dilation, fp32 or bf16 inputs, optional bias, optional
-// add + t*hardswish(t) epilogue.
+// add + t*hardswish(t) epilogue, channels-first or channels-last layouts.
 //
 // Formulation ([l1_p79] gather check, [l1_p72] tap-range analysis): output o
 // of one dimension receives tap k from input i = (o + p - k*dl) / s when that
@@ -25,6 +25,9 @@ struct GenParams {
     int Li0, Li1, Li2, Lo0, Lo1, Lo2;
     int K0, K1, K2, S0, S1, S2, P0, P1, P2, D0, D1, D2;
     int QW;
+    // element strides of x and y (and add): image, channel, position.  Channels
+    // first (N, C, spatial): C*sp, sp, 1; channels last (N, spatial, C): sp*C, 1, C
+    int64_t xs_n, xs_c, xs_p, ys_n, ys_c, ys_p;
 };
 
 template <typename TIN, int OCV, bool ADD>
@@ -47,9 +50,7 @@ gather_generic_kernel(const TIN *__restrict__ x, const TIN *__restrict__ w,
     const int ocl0 = occ * OCV;
     const int jmax = min(OCV, g.Cog - ocl0);
     const int kvol = g.K0 * g.K1 * g.K2;
-    const int64_t in_sp = (int64_t)g.Li0 * g.Li1 * g.Li2;
-    const int64_t out_sp = (int64_t)g.Lo0 * g.Lo1 * g.Lo2;
-    const TIN *xg = x + ((int64_t)n * g.C_in + (int64_t)grp * g.Cig) * in_sp;
+    const TIN *xg = x + (int64_t)n * g.xs_n + (int64_t)grp * g.Cig * g.xs_c;
     const TIN *wg = w + ((int64_t)grp * g.Cig * g.Cog + ocl0) * kvol;
 
     for (int r = 0; r < g.S2; ++r) {
@@ -75,10 +76,10 @@ gather_generic_kernel(const TIN *__restrict__ x, const TIN *__restrict__ w,
                     const int iw = nw / g.S2;
                     if (iw >= g.Li2) continue;
                     const int tap = (kd * g.K1 + kh) * g.K2 + kw;
-                    const TIN *xp = xg + ((int64_t)id * g.Li1 + ih) * g.Li2 + iw;
+                    const TIN *xp = xg + (((int64_t)id * g.Li1 + ih) * g.Li2 + iw) * g.xs_p;
                     const TIN *wp = wg + tap;
                     for (int ic = 0; ic < g.Cig; ++ic) {
-                        const float xv = to_float(ldg(xp + (int64_t)ic * in_sp));
+                        const float xv = to_float(ldg(xp + (int64_t)ic * g.xs_c));
                         const TIN *wr = wp + (int64_t)ic * g.Cog * kvol;
 #pragma unroll
                         for (int j = 0; j < OCV; ++j)
@@ -92,7 +93,7 @@ gather_generic_kernel(const TIN *__restrict__ x, const TIN *__restrict__ w,
         for (int j = 0; j < OCV; ++j) {
             if (j < jmax) {
                 const int oc = grp * g.Cog + ocl0 + j;
-                const int64_t off = ((int64_t)n * g.C_out + oc) * out_sp + sp;
+                const int64_t off = (int64_t)n * g.ys_n + (int64_t)oc * g.ys_c + sp * g.ys_p;
                 float v = acc[j] + (bias ? __ldg(bias + oc) : 0.f);
                 if (ADD) v = add_hswish(v, add[off]);
                 y[off] = v;
@@ -114,6 +115,13 @@ cudaError_t launch_t(const Problem &pb, const Args &a)
     g.P0 = pb.P[0]; g.P1 = pb.P[1]; g.P2 = pb.P[2];
     g.D0 = pb.DL[0]; g.D1 = pb.DL[1]; g.D2 = pb.DL[2];
     g.QW = (pb.Lo[2] + pb.S[2] - 1) / pb.S[2];
+    const int64_t in_sp = pb.in_sp(), out_sp = pb.out_sp();
+    g.xs_n = (int64_t)pb.C_in * in_sp;
+    g.ys_n = (int64_t)pb.C_out * out_sp;
+    g.xs_c = pb.cl ? 1 : in_sp;
+    g.xs_p = pb.cl ? pb.C_in : 1;
+    g.ys_c = pb.cl ? 1 : out_sp;
+    g.ys_p = pb.cl ? pb.C_out : 1;
     const int64_t total = (int64_t)g.N * g.G * g.n_occ * g.Lo0 * g.Lo1 * g.QW;
     if (total == 0) return cudaSuccess;
     const int threads = 256;

@@ -17,6 +17,7 @@ struct Problem {
     int Li[3], K[3], S[3], P[3], OP[3], DL[3], Lo[3];
     ct_dtype dtype;
     bool has_bias, has_add;
+    bool cl = false;                         // channels-last x, y, add: (N, spatial..., C)
 
     int64_t in_sp() const { return (int64_t)Li[0] * Li[1] * Li[2]; }
     int64_t out_sp() const { return (int64_t)Lo[0] * Lo[1] * Lo[2]; }

@@ -94,6 +94,7 @@ struct UParams {
     int QD, QH, QW, n_qhb, n_qwp;   // n_qwp: pairs of 8-column qw blocks
     int nT;                  // taps per class of H and W (kernel extent / 2)
     int SD, nTD;             // D: stride 2 and nT taps, or a unit dimension (stride 1, one tap)
+    int cl;                  // channels-last y (N, D, H, W, C_out); x is then the caller's own
     int n_kb;                // C_in / BK
     int ntiles;
     int nacc;                // TMEM accumulators = MMA issuers = tiles per pair (1 or 2)
@@ -377,6 +378,8 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 ok = __all_sync(0xffffffffu, ok);    // warp-uniform before .sync.aligned loads
                 tc::fence_after();
                 float *yrow = y + (int64_t)tcd.n * p.C_out * sp + ((int64_t)od * p.Lo1 + oh) * p.Lo2 + 2 * qw;
+                // channels last: output position 2 qw + wr holds C_out consecutive values
+                float *ycl = y + ((((int64_t)tcd.n * p.Lo0 + od) * p.Lo1 + oh) * p.Lo2 + 2 * qw + wr) * p.C_out;
                 const uint32_t tbase =
                     tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols + (uint32_t)wr * p.C_out;
                 // EB chunks per batch; the half is released as soon as the warp's
@@ -399,7 +402,21 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         dev::mbar_arrive(&acc_empty[a][wr]);
                         released = true;
                     }
-                    if (ok && valid) {
+                    if (ok && valid && p.cl) {
+                        // 16 channels of one position: 64 contiguous bytes
+#pragma unroll
+                        for (int b = 0; b < EB; ++b) {
+                            if (b >= nc) break;
+                            const int c0 = (ci + b * cstep) * 16;
+                            float4 *dst = reinterpret_cast<float4 *>(ycl + c0);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                __stcs(dst + i, make_float4(v[b][4 * i] + s_bias[c0 + 4 * i],
+                                                            v[b][4 * i + 1] + s_bias[c0 + 4 * i + 1],
+                                                            v[b][4 * i + 2] + s_bias[c0 + 4 * i + 2],
+                                                            v[b][4 * i + 3] + s_bias[c0 + 4 * i + 3]));
+                        }
+                    } else if (ok && valid) {
 #pragma unroll
                         for (int b = 0; b < EB; ++b) {
                             if (b >= nc) break;
@@ -638,6 +655,7 @@ bool make_uplan(const Problem &pb, UPlan *out)
     p.Lo0 = pb.Lo[0]; p.Lo1 = pb.Lo[1]; p.Lo2 = pb.Lo[2];
     p.QW = p.Lo2 / 2;
     p.SD = SD;
+    p.cl = pb.cl ? 1 : 0;
     p.QD = (p.Lo0 + SD - 1) / SD;
     p.QH = (p.Lo1 + 1) / 2;
     p.nacc = 4 * pb.C_out <= 512 ? 2 : 1;     // tiles per unit
@@ -713,7 +731,8 @@ bool make_uplan(const Problem &pb, UPlan *out)
     const size_t smem = a_area + (size_t)nb * b_slot + 1024;
     out->p = p;
     out->wq = wq;
-    out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * 2);
+    // channels-last x is read in place: no repacked copy
+    out->x_bytes = pb.cl ? 0 : align256((size_t)pb.N * pb.C_in * pb.in_sp() * 2);
     out->w_bytes = align256((size_t)4 * SD * p.nTD * p.nT * p.nT * pb.C_out * pb.C_in * 2);
     out->smem = smem;
     return true;
@@ -725,7 +744,8 @@ bool umma_supported(const Problem &pb, const Args *a)
 {
     UPlan pl;
     if (!make_uplan(pb, &pl)) return false;
-    if (a && (((uintptr_t)a->y % 8) || ((uintptr_t)a->x % 16) || ((uintptr_t)a->w % 16))) return false;
+    if (a && (((uintptr_t)a->y % (pb.cl ? 16 : 8)) || ((uintptr_t)a->x % 16) || ((uintptr_t)a->w % 16)))
+        return false;
     return true;
 }
 
@@ -741,7 +761,8 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     UPlan pl;
     if (!make_uplan(pb, &pl)) return cudaErrorNotSupported;
     const UParams &p = pl.p;
-    bf16_t *xt = static_cast<bf16_t *>(a.ws);
+    // channels last: x is already (N, D, H, W, C), the layout the A operand reads
+    bf16_t *xt = pb.cl ? const_cast<bf16_t *>(static_cast<const bf16_t *>(a.x)) : static_cast<bf16_t *>(a.ws);
     bf16_t *wp = reinterpret_cast<bf16_t *>(static_cast<uint8_t *>(a.ws) + pl.x_bytes);
 
     // 1) x -> (N, D, H, W, C) and weights -> panels: one launch when D*H*W is
@@ -749,7 +770,10 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     const int64_t SP = pb.in_sp();
     const int64_t nby = (pb.C_in + 63) / 64;
     cudaError_t e;
-    if (SP % 8 == 0) {
+    if (pb.cl) {
+        repack_w_kernel<<<dim3((unsigned)(pb.C_in / RB), (unsigned)pb.C_out), 256, 0, a.stream>>>(
+            static_cast<const bf16_t *>(a.w), wp, pl.wq);
+    } else if (SP % 8 == 0) {
         const int64_t nbx = (SP + RX - 1) / RX;
         const int64_t nxb = nbx * nby * pb.N;
         const int64_t nblocks = nxb + (int64_t)(pb.C_in / RB) * pb.C_out;

@@ -64,10 +64,19 @@ CONFIGS = {
         nd=2, N=16, C_in=256, C_out=128, groups=1, L_in=(64, 64), k=(4, 4), stride=(2, 2),
         padding=(1, 1), output_padding=(0, 0), dilation=(1, 1), bias=True, add=False,
         dtype="bf16", bound=1.0 / math.sqrt(128 * 16), seed=7),
+    # the bf16 workload with channels-last x and y (N, D, H, W, C): the same
+    # draws, stored channels-last
+    "convT3d_bf16_dense_cl": dict(
+        desc=("ConvTranspose3d bf16-in/fp32-accumulate N=16 C_in=256 C_out=128 k=4 s=2 p=1 "
+              "in=16^3 bias, channels-last x and y"),
+        nd=3, N=16, C_in=256, C_out=128, groups=1, L_in=(16, 16, 16), k=(4, 4, 4),
+        stride=(2, 2, 2), padding=(1, 1, 1), output_padding=(0, 0, 0), dilation=(1, 1, 1),
+        bias=True, add=False, dtype="bf16", bound=1.0 / math.sqrt(128 * 64), seed=5, layout="cl"),
 }
 
 CONFIG_ORDER = ["convT1d_tiny", "convT1d_L131072", "convT3d_grouped",
-                "convT3d_add_hswish", "convT3d_bf16_dense", "convT2d_f32", "convT2d_bf16_dense"]
+                "convT3d_add_hswish", "convT3d_bf16_dense", "convT2d_f32", "convT2d_bf16_dense",
+                "convT3d_bf16_dense_cl"]
 
 
 def bf16_round(a):

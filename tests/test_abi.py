@@ -172,12 +172,15 @@ def test_path_selection_2d(lib):
 
 def test_path_selection_channels_last(lib):
     """Channels-last calls: bf16 shapes of the bf16 tensor-core kernel take it
-    (x read in place: workspace only for the weight panels), the rest the
-    generic kernel."""
+    (x read in place: workspace only for the weight panels), dense FP32 shapes
+    the FP32 tensor-core kernel, the rest the generic kernel."""
     dense = (16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1))
     assert ct.ct_path_cl(3, *dense, ct.CT_BF16) == "umma_bf16"
     assert ct.ct_path_cl(3, *dense, ct.CT_BF16, fused=True) == "gather_generic"
-    assert ct.ct_path_cl(3, *dense, ct.CT_F32) == "gather_generic"
+    assert ct.ct_path_cl(3, *dense, ct.CT_F32) == "tc3d_bf16split"
+    assert ct.ct_path_cl(3, *dense, ct.CT_F32, fused=True) == "tc3d_bf16split"
+    grouped = (8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3), (1, 1, 1), (1, 1, 1))
+    assert ct.ct_path_cl(3, *grouped, ct.CT_F32) == "gather_generic"
     d2 = (16, 256, 128, (64, 64), (4, 4), 1, (2, 2), (1, 1), (0, 0), (1, 1))
     assert ct.ct_path_cl(2, *d2, ct.CT_BF16) == "umma_bf16"
     assert ct.ct_path_cl(1, 16, 32, 64, (131072,), (3,), 1, (2,), (1,), (0,), (2,), ct.CT_F32) == "gather_generic"
@@ -185,7 +188,8 @@ def test_path_selection_channels_last(lib):
     n_cl = ct.ct_workspace_size_cl(3, *dense, ct.CT_BF16)
     x_bytes = 16 * 256 * 16 ** 3 * 2
     assert n_cl == n_cf - x_bytes and n_cl >= 8 * 128 * 8 * 256 * 2
-    assert ct.ct_workspace_size_cl(3, *dense, ct.CT_F32) == 0
+    # FP32: the bf16 (hi, lo) copy of x and the panels, as channels first
+    assert ct.ct_workspace_size_cl(3, *dense, ct.CT_F32) == ct.ct_workspace_size_3d(*dense, ct.CT_F32)
     assert ct.ct_path_cl(4, *dense, ct.CT_BF16) is None
     with pytest.raises(ct.CTError) as e:
         ct.ct_workspace_size_cl(3, 1, 4, 8, (4, 4, 4), (3, 3, 3), 3, (2, 2, 2), (1, 1, 1), (0, 0, 0),

@@ -55,7 +55,8 @@ def path_of(c):
 REDUCED = {"convT1d_tiny": dict(N=2), "convT1d_L131072": dict(N=1),
            "convT3d_grouped": dict(N=2), "convT3d_add_hswish": dict(N=2),
            "convT3d_bf16_dense": dict(N=1, L=[8, 8, 8]), "convT2d_f32": dict(N=1),
-           "convT2d_bf16_dense": dict(N=1, L=[32, 32]), "convT3d_bf16_dense_cl": dict(N=1, L=[8, 8, 8])}
+           "convT2d_bf16_dense": dict(N=1, L=[32, 32]), "convT3d_bf16_dense_cl": dict(N=1, L=[8, 8, 8]),
+           "convT3d_add_hswish_cl": dict(N=2)}
 
 
 @pytest.mark.parametrize("name", CONFIGS)
@@ -389,8 +390,10 @@ def test_disjoint_phase_shapes_exact(k):
 # Channels-last layouts (x (N, spatial..., C_in), y and add (N, spatial...,
 # C_out)): the inputs are the same draws moved to channels-last on the device,
 # the result is moved back and compared with the oracle.  bf16 shapes of the
-# bf16 tensor-core kernel (3-D and 2-D: x read in place), and the generic
-# kernel for FP32, groups, 1-D and the fused epilogue (also in place).
+# bf16 tensor-core kernel (3-D and 2-D: x read in place), dense FP32 shapes of
+# the FP32 tensor-core kernel (3-D and 2-D, plain and fused, odd D and H
+# outputs), and the generic kernel for groups, 1-D, other strides and the
+# bf16 fused epilogue (fused cases also in place).
 CL = [
     dict(nd=3, N=1, C_in=64, C_out=16, G=1, L=[2, 3, 8], K=[4] * 3, S=[2] * 3, P=[1] * 3, OP=[1, 0, 0],
          DL=[1] * 3, dtype="bf16", add=False, path="umma_bf16"),
@@ -403,7 +406,13 @@ CL = [
     dict(nd=2, N=2, C_in=128, C_out=128, G=1, L=[5, 12], K=[4, 4], S=[2, 2], P=[1, 1], OP=[1, 0],
          DL=[1, 1], dtype="bf16", add=False, path="umma_bf16"),
     dict(nd=3, N=1, C_in=32, C_out=64, G=1, L=[3, 4, 8], K=[3] * 3, S=[2] * 3, P=[1] * 3, OP=[1] * 3,
-         DL=[1] * 3, dtype="f32", add=True, path="gather_generic"),
+         DL=[1] * 3, dtype="f32", add=True, path="tc3d_bf16split"),
+    dict(nd=3, N=2, C_in=64, C_out=32, G=1, L=[2, 3, 4], K=[4] * 3, S=[2] * 3, P=[1] * 3, OP=[0] * 3,
+         DL=[1] * 3, dtype="f32", add=False, path="tc3d_bf16split"),
+    dict(nd=2, N=2, C_in=32, C_out=48, G=1, L=[7, 64], K=[3, 3], S=[2, 2], P=[1, 1], OP=[1, 1],
+         DL=[1, 1], dtype="f32", add=False, path="tc3d_bf16split"),
+    dict(nd=2, N=1, C_in=32, C_out=16, G=1, L=[3, 4], K=[2, 3], S=[2, 2], P=[0, 1], OP=[1, 1],
+         DL=[1, 1], dtype="f32", add=True, path="tc3d_bf16split"),
     dict(nd=3, N=2, C_in=6, C_out=4, G=2, L=[3, 4, 5], K=[2, 3, 4], S=[3, 1, 2], P=[1, 0, 2], OP=[2, 0, 1],
          DL=[1, 2, 1], dtype="f32", add=False, path="gather_generic"),
     dict(nd=2, N=2, C_in=8, C_out=8, G=4, L=[4, 6], K=[3, 3], S=[2, 2], P=[1, 1], OP=[1, 1], DL=[1, 1],
@@ -444,7 +453,7 @@ def test_channels_last_shapes(k):
     cc.assert_close(_run_cl(c, t), ref, c["dtype"], "channels-last case %d %r" % (k, c))
     if c["add"]:
         cc.assert_close(_run_cl(c, t, inplace=True), ref, c["dtype"], "channels-last in place %d" % k)
-    if k in (1, 6):
+    if k in (1, 6, 9):
         ti = cc.make_inputs(c, seed=1650 + k, int_range=3)
         assert np.array_equal(_run_cl(c, ti).astype(np.float64), cc.run_oracle(c, ti)), "cl integer %d" % k
 

@@ -104,8 +104,12 @@ Path choose_path(const Problem &pb, const Args *a)
     if (ov == 1) return Path::Generic;
     if (pb.cl) {
         // channels-last layouts: the bf16 tensor-core kernel reads x in place and
-        // writes y channels-last; every other shape takes the generic kernel
+        // writes y channels-last; the dense FP32 one splits x without a transpose
+        // and stores y channels-last; every other shape takes the generic kernel
         if (pb.dtype == CT_BF16 && pb.nd >= 2 && !pb.has_add && umma_supported(pb, a)) return Path::Umma;
+        if (pb.dtype == CT_F32 && ov != 2 && pb.nd >= 2 && tc3d_supported(pb, a) &&
+            (!a || (a->ws && ((uintptr_t)a->ws % 256) == 0 && a->ws_bytes >= tc3d_workspace_bytes(pb))))
+            return Path::Tc3d;
         return Path::Generic;
     }
     if (pb.dtype == CT_F32) {

@@ -210,17 +210,44 @@ __device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float 
     }
 }
 
-// Both preps in one launch: blocks [0, nxb) move x (nbx x nby per image), the
-// remaining nbw blocks build the panels.  The GEMM kernel is launched as its
-// programmatic dependent.
+// Channels-last x (N, S, C) -> x_c (N, S, 2C): the same split, no transpose.
+// Block = 1024 consecutive values (256 threads x 4 channels: one 16-byte load
+// and two 8-byte stores each); C a multiple of 32, so 4 channels never cross a
+// position.
+__device__ __forceinline__ void prep_x_cl_block(const float *__restrict__ x, uint16_t *__restrict__ xc,
+                                                int64_t total, int bx)
+{
+    const int64_t e = ((int64_t)bx * 256 + threadIdx.x) * 4;    // first of 4 values
+    if (e >= total) return;
+    const float4 v = __ldcs(reinterpret_cast<const float4 *>(x + e));
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hb[4], lb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float h = bf16_round(vv[i]);
+        hb[i] = bf16_bits(h);
+        lb[i] = bf16_bits(vv[i] - h);
+    }
+    // value e = (position, channel c): K step (c mod 32) / 8 of its 32-channel block
+    const int c = (int)(e & 31);
+    uint16_t *cr = xc + 2 * (e - c) + (c >> 3) * 16 + (c & 4);
+    *reinterpret_cast<uint2 *>(cr) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+    *reinterpret_cast<uint2 *>(cr + 8) = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+}
+
+// Both preps in one launch: blocks [0, nxb) move x (nbx x nby per image; or,
+// channels last, 1024 consecutive values each), the remaining nbw blocks build
+// the panels.  The GEMM kernel is launched as its programmatic dependent.
 __global__ void __launch_bounds__(256)
 prep_kernel(const float *__restrict__ x, uint16_t *__restrict__ xc, int C, int64_t SP,
             int nbx, int nby, int nxb, const float *__restrict__ w, float *__restrict__ wp,
-            const __grid_constant__ WPanels q, int nbw)
+            const __grid_constant__ WPanels q, int nbw, int64_t cl_total)
 {
     dev::griddep_launch_dependents();
     const int b = (int)blockIdx.x;
-    if (b < nxb) {
+    if (b < nxb && cl_total > 0) {
+        prep_x_cl_block(x, xc, cl_total, b);
+    } else if (b < nxb) {
         const int per = nbx * nby;
         prep_x_block(x, xc, C, SP, (b % per) % nbx, (b % per) / nbx, b / per);
     } else {
@@ -255,7 +282,7 @@ __device__ __forceinline__ UnitCoord unit_coord(int u, const T3Params &p)
     return c;
 }
 
-template <bool ADD>
+template <bool ADD, bool CL>
 __global__ void __launch_bounds__(kThreads, 1)
 tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                  const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
@@ -451,8 +478,12 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             if (ADD) {
                 const UnitCoord v = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
                 dev::mbar_arrive_expect_tx(&e_full[b], kEChunk);
-                dev::tma_load_4d(sE + (size_t)b * kEChunk, &tmAdd, &e_full[b], 0, 2 * v.qhb * p.MH, p.SD * v.qd + v.rd,
-                                 v.n * C_out + (gc % nchunk) * 16);
+                if (CL)    // (C_out, W, H, D, N): 16 channels of every position of the chunk
+                    dev::tma_load_5d(sE + (size_t)b * kEChunk, &tmAdd, &e_full[b], (gc % nchunk) * 16, 0,
+                                     2 * v.qhb * p.MH, p.SD * v.qd + v.rd, v.n);
+                else
+                    dev::tma_load_4d(sE + (size_t)b * kEChunk, &tmAdd, &e_full[b], 0, 2 * v.qhb * p.MH,
+                                     p.SD * v.qd + v.rd, v.n * C_out + (gc % nchunk) * 16);
             } else {
                 dev::mbar_arrive(&e_full[b]);
             }
@@ -469,8 +500,12 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                 }
                 const UnitCoord u = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
                 // rows and planes past the output are clipped by the store
-                dev::tma_store_4d(&tmY, sE + (size_t)(gc % NE) * kEChunk, 0, 2 * u.qhb * p.MH, p.SD * u.qd + u.rd,
-                                  u.n * C_out + (gc % nchunk) * 16);
+                if (CL)
+                    dev::tma_store_5d(&tmY, sE + (size_t)(gc % NE) * kEChunk, (gc % nchunk) * 16, 0,
+                                      2 * u.qhb * p.MH, p.SD * u.qd + u.rd, u.n);
+                else
+                    dev::tma_store_4d(&tmY, sE + (size_t)(gc % NE) * kEChunk, 0, 2 * u.qhb * p.MH,
+                                      p.SD * u.qd + u.rd, u.n * C_out + (gc % nchunk) * 16);
                 dev::bulk_commit();
                 dev::bulk_wait_read<1>();               // chunk gc - 1's store has read its buffer
                 if (gc + 2 < total) ready(gc + 2);      // into that buffer
@@ -526,6 +561,39 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                 if (c == nchunk - 1) {                  // the unit's last loads: free the accumulators
                     tc::fence_before();
                     dev::mbar_arrive(&acc_empty[a]);
+                }
+                if (CL) {
+                    // channels last: the chunk buffer is the (16 channels, W, 2 MH rows)
+                    // box of the 5-D maps, 64-byte rows (one position's 16 channels) in
+                    // the 64-byte swizzle -- the 16-byte unit index (address bits 4-5)
+                    // XORed with address bits 7-8 -- which spreads a warp's accesses
+                    // (positions 128 bytes apart) over four bank groups.  This warp's
+                    // 8 channels of positions 2 qw and 2 qw + 1: two 16-byte units each.
+                    if (ok) {
+                        uint8_t *buf = sE + (size_t)b * kEChunk;
+#pragma unroll
+                        for (int w2 = 0; w2 < 2; ++w2) {
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const uint32_t L = (uint32_t)(((row * Lo2 + 2 * qw + w2) * 16 + ch * 8 + 4 * j) * 4);
+                                float4 *ptr = reinterpret_cast<float4 *>(buf + (L ^ (((L >> 7) & 3u) << 4)));
+                                const int cc = c0 + 4 * j;
+                                const float e0 = w2 ? v1[4 * j] : v0[4 * j], e1 = w2 ? v1[4 * j + 1] : v0[4 * j + 1];
+                                const float e2 = w2 ? v1[4 * j + 2] : v0[4 * j + 2], e3 = w2 ? v1[4 * j + 3] : v0[4 * j + 3];
+                                float4 t = make_float4(e0 + s_bias[cc], e1 + s_bias[cc + 1], e2 + s_bias[cc + 2],
+                                                       e3 + s_bias[cc + 3]);
+                                if (ADD) {
+                                    const float4 av = *ptr;
+                                    t = make_float4(add_hswish(t.x, av.x), add_hswish(t.y, av.y), add_hswish(t.z, av.z),
+                                                    add_hswish(t.w, av.w));
+                                }
+                                *ptr = t;
+                            }
+                        }
+                    }
+                    dev::fence_proxy_async();
+                    dev::mbar_arrive(&c_full[b]);
+                    continue;
                 }
                 if (ok) {
                     // all loads first, then the arithmetic and the stores
@@ -753,16 +821,19 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     float *wp = reinterpret_cast<float *>(ws + pl.x_bytes);
 
     // 1) one launch: x -> channels-last bf16 (hi, lo) pairs, weights -> run panels
+    // (channels-last x: the split alone, 1024 values per block)
     const int64_t SP = pb.in_sp();
     const int64_t nbx = (SP + 63) / 64, nby = pb.C_in / 32;
-    const int64_t nxb = nbx * nby * pb.N;
+    const int64_t cl_total = pb.cl ? (int64_t)pb.N * SP * pb.C_in : 0;
+    const int64_t nxb = pb.cl ? (cl_total + 1023) / 1024 : nbx * nby * pb.N;
     const int64_t wtot = (int64_t)pl.wq.nblk * pb.C_out * pb.C_in;
     int nbw = (int)((wtot + 255) / 256);
     if (nbw > 4 * sm_count()) nbw = 4 * sm_count();
     if (nxb + nbw > 0x7fffffff) return cudaErrorInvalidConfiguration;
     prep_kernel<<<(unsigned)(nxb + nbw), 256, 0, a.stream>>>(static_cast<const float *>(a.x), xc, pb.C_in, SP,
                                                             (int)nbx, (int)nby, (int)nxb,
-                                                            static_cast<const float *>(a.w), wp, pl.wq, nbw);
+                                                            static_cast<const float *>(a.w), wp, pl.wq, nbw,
+                                                            cl_total);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -797,12 +868,30 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     const uint64_t ystr[3] = {(uint64_t)pb.Lo[2] * 4, (uint64_t)pb.Lo[2] * pb.Lo[1] * 4,
                               (uint64_t)pb.out_sp() * 4};
     const uint32_t ybox[4] = {(uint32_t)pb.Lo[2], (uint32_t)(2 * p.MH), 1u, 16u};
-    if (!encode_tiled(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, ydims, ystr, ybox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_tiled(&tmAdd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.add ? a.add : a.y, ydims, ystr, ybox,
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (pb.cl) {
+        // channels last: (C_out, W, H, D, N), a box of 16 channels x the whole W
+        // extent x the unit's 2 MH rows, 64-byte rows in the 64-byte swizzle
+        const uint64_t cdims[5] = {(uint64_t)pb.C_out, (uint64_t)pb.Lo[2], (uint64_t)pb.Lo[1], (uint64_t)pb.Lo[0],
+                                   (uint64_t)pb.N};
+        const uint64_t cstr[4] = {(uint64_t)pb.C_out * 4, (uint64_t)pb.C_out * pb.Lo[2] * 4,
+                                  (uint64_t)pb.C_out * pb.Lo[2] * pb.Lo[1] * 4, (uint64_t)pb.C_out * pb.out_sp() * 4};
+        const uint32_t cbox5[5] = {16u, (uint32_t)pb.Lo[2], (uint32_t)(2 * p.MH), 1u, 1u};
+        if (!encode_tiled(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.y, cdims, cstr, cbox5,
+                          CU_TENSOR_MAP_SWIZZLE_64B) ||
+            !encode_tiled(&tmAdd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.add ? a.add : a.y, cdims, cstr, cbox5,
+                          CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    } else if (!encode_tiled(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, ydims, ystr, ybox,
+                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
+               !encode_tiled(&tmAdd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.add ? a.add : a.y, ydims, ystr, ybox,
+                             CU_TENSOR_MAP_SWIZZLE_NONE)) {
         return cudaErrorInvalidValue;
+    }
 
-    const void *fn = a.add ? (const void *)&tc3d_split_kernel<true> : (const void *)&tc3d_split_kernel<false>;
+    const void *fn = pb.cl ? (a.add ? (const void *)&tc3d_split_kernel<true, true>
+                                    : (const void *)&tc3d_split_kernel<false, true>)
+                           : (a.add ? (const void *)&tc3d_split_kernel<true, false>
+                                    : (const void *)&tc3d_split_kernel<false, false>);
     int per_sm = 0;
     e = prepare_kernel(fn, kThreads, pl.smem, &per_sm);
     if (e != cudaSuccess) return e;
@@ -812,11 +901,13 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     int grid = sm_count();
     if (grid > p.nunits) grid = p.nunits;
     if (p.SD == 2 && grid > 1 && (grid & 1)) --grid;   // an even grid: the residue flip of unit_coord permutes units
-    if (a.add)
-        return launch_dependent(tc3d_split_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
-                                tmXc, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
-    return launch_dependent(tc3d_split_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
-                            tmXc, tmW[0], tmW[1], tmW[2], tmW[3], tmAdd, tmY, a.bias, p, status);
+    const dim3 gd((unsigned)grid), bd(kThreads);
+#define CT_TC3D_LAUNCH(ADD_, CL_)                                                                                  \
+    launch_dependent(tc3d_split_kernel<ADD_, CL_>, gd, bd, pl.smem, a.stream, tmXc, tmW[0], tmW[1], tmW[2], tmW[3], \
+                     tmAdd, tmY, a.bias, p, status)
+    if (pb.cl) return a.add ? CT_TC3D_LAUNCH(true, true) : CT_TC3D_LAUNCH(false, true);
+    return a.add ? CT_TC3D_LAUNCH(true, false) : CT_TC3D_LAUNCH(false, false);
+#undef CT_TC3D_LAUNCH
 }
 
 }  // namespace ct

@@ -72,11 +72,19 @@ CONFIGS = {
         nd=3, N=16, C_in=256, C_out=128, groups=1, L_in=(16, 16, 16), k=(4, 4, 4),
         stride=(2, 2, 2), padding=(1, 1, 1), output_padding=(0, 0, 0), dilation=(1, 1, 1),
         bias=True, add=False, dtype="bf16", bound=1.0 / math.sqrt(128 * 64), seed=5, layout="cl"),
+    # the fused workload with channels-last x, add and y (N, D, H, W, C)
+    "convT3d_add_hswish_cl": dict(
+        desc=("ConvTranspose3d fp32 N=128 C_in=32 C_out=64 k=3 s=2 p=1 op=1 in=16^3 bias, "
+              "+ add, out = t*hardswish(t), channels-last x, add and y"),
+        nd=3, N=128, C_in=32, C_out=64, groups=1, L_in=(16, 16, 16), k=(3, 3, 3),
+        stride=(2, 2, 2), padding=(1, 1, 1), output_padding=(1, 1, 1), dilation=(1, 1, 1),
+        bias=True, add=True, out_shape=(128, 64, 32, 32, 32), dtype="f32",
+        bound=1.0 / math.sqrt(64 * 27), seed=4, layout="cl"),
 }
 
 CONFIG_ORDER = ["convT1d_tiny", "convT1d_L131072", "convT3d_grouped",
                 "convT3d_add_hswish", "convT3d_bf16_dense", "convT2d_f32", "convT2d_bf16_dense",
-                "convT3d_bf16_dense_cl"]
+                "convT3d_bf16_dense_cl", "convT3d_add_hswish_cl"]
 
 
 def bf16_round(a):

@@ -88,6 +88,27 @@ def test_argument_errors_before_launch(lib):
     assert call1d(lib, N=0) == 0                 # empty batch: valid, nothing launched
 
 
+def callcl(lib, nd=3, **kw):
+    a = dict(x=FAKE, w=FAKE + (1 << 24), bias=None, add=None, y=FAKE + (1 << 26), N=2, C_in=4, C_out=8,
+             dtype=ct.CT_F32)
+    a.update(kw)
+    v = lambda t: (ctypes.c_int * max(1, nd))(*([t] * max(1, nd)))
+    return lib.ct_forward_cl(nd, a["x"], a["w"], a["bias"], a["add"], a["y"], a["N"], a["C_in"], a["C_out"],
+                             v(5), v(3), 1, v(2), v(1), v(0), v(1), a["dtype"], None, 0, None)
+
+
+def test_channels_last_argument_errors_before_launch(lib):
+    assert callcl(lib, nd=0) == 1                      # 1 to 3 spatial dimensions
+    assert callcl(lib, nd=4) == 1
+    assert callcl(lib, x=None) == 1
+    assert callcl(lib, y=FAKE + 16) == 1               # y overlaps x
+    assert callcl(lib, add=FAKE + (1 << 26) + 8) == 1  # add overlaps y without being y
+    assert callcl(lib, x=FAKE + 2) == 3                # misaligned fp32
+    assert callcl(lib, C_in=0) == 1
+    assert callcl(lib, N=0) == 0                       # empty batch: valid, nothing launched
+    assert callcl(lib, nd=1, N=0) == 0 and callcl(lib, nd=2, N=0) == 0
+
+
 def test_fused_requires_add(lib):
     i3 = ct._I3
     st = lib.ct_forward_3d_add_hswish(FAKE, FAKE + (1 << 24), None, None, FAKE + (1 << 26), 1, 4,

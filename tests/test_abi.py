@@ -172,6 +172,11 @@ def test_path_selection_2d(lib):
                          ct.CT_BF16) == "gather_generic"
     assert ct.ct_path_2d(2, 6, 4, (5, 7), (3, 2), 2, (2, 3), (1, 0), (1, 2), (1, 1),
                          ct.CT_F32) == "gather_generic"
+    # 32 input channels in groups: the grouped tensor-core path (fused: generic)
+    assert ct.ct_path_2d(2, 32, 32, (16, 16), (5, 7), 4, (2, 2), (2, 3), (1, 1), (1, 1),
+                         ct.CT_F32) == "tc3dg_bf16split"
+    assert ct.ct_path_2d(2, 32, 32, (16, 16), (5, 7), 4, (2, 2), (2, 3), (1, 1), (1, 1),
+                         ct.CT_F32, fused=True) == "gather_generic"
     ct.ct_set_path_override(2)
     try:
         assert ct.ct_path_2d(*dense, ct.CT_F32) == "gather_generic"

@@ -279,6 +279,30 @@ def test_fp32_2d_tensor_core_shapes(k, add):
         assert np.array_equal(yi.astype(np.float64), cc.run_oracle(c, ti)), "2-D tc integer case %d" % k
 
 
+# Grouped ConvTranspose2d (32 input channels in 4, 2 or 1 groups) on the
+# grouped tensor-core path: the unit D dimension planned as a stride-2 D of
+# extent 1 (its odd residue has no plane); asymmetric kernels, and a case with
+# several units per persistent CTA.
+TC2DG = [
+    dict(N=2, C_in=32, C_out=32, G=4, L=[16, 16], K=[5, 7], P=[2, 3], OP=[1, 1]),
+    dict(N=1, C_in=32, C_out=32, G=2, L=[8, 12], K=[4, 6], P=[1, 2], OP=[0, 0]),
+    dict(N=4, C_in=32, C_out=8, G=1, L=[32, 32], K=[3, 3], P=[1, 1], OP=[1, 1]),
+]
+
+
+@pytest.mark.parametrize("k", range(len(TC2DG)))
+def test_fp32_2d_grouped_tensor_core_shapes(k):
+    c = dict(nd=2, S=[2, 2], DL=[1, 1], bias=bool(k % 2 == 0), add=False, dtype="f32", **TC2DG[k])
+    assert path_of(c) == "tc3dg_bf16split", (c, path_of(c))
+    t = cc.make_inputs(c, seed=1700 + k)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), "f32", "2-D grouped case %d %r" % (k, c))
+    if k == 0:
+        ti = cc.make_inputs(c, seed=1750, int_range=3)
+        yi = cc.run_gpu(c, ti).cpu().numpy()
+        assert np.array_equal(yi.astype(np.float64), cc.run_oracle(c, ti)), "2-D grouped integer case"
+
+
 # bf16 ConvTranspose2d on the bf16 tensor-core path: kernel extents 4 and 8
 # (the weight repack moves 16-byte pieces, so kH*kW must be a multiple of 8),
 # C_out 16..256, odd H output, padding 0..3, several tiles per CTA.

@@ -564,7 +564,26 @@ int taps_of(int K, int P, int r, int *k_out, int *d_out)
     return n;
 }
 
+bool make_gplan_3d(const Problem &pb, const Args *a, GPlan *out);
+
+// A unit D dimension (a 2-D call: one input plane, extent 1, stride 1, no
+// padding) is the same operator as a D dimension of stride 2 and extent 1:
+// one output plane, residue 0 takes tap 0 at offset 0, residue 1 no tap (its
+// plane lies past the output).  The 2-D call is planned as that 3-D one.
 bool make_gplan(const Problem &pb, const Args *a, GPlan *out)
+{
+    if (pb.cl) return false;
+    if (pb.nd == 2 || (pb.S[0] == 1 && pb.Li[0] == 1)) {
+        if (pb.Li[0] != 1 || pb.K[0] != 1 || pb.S[0] != 1 || pb.P[0] != 0 || pb.OP[0] != 0) return false;
+        Problem q = pb;
+        q.nd = 3;
+        q.S[0] = 2;
+        return make_gplan_3d(q, a, out);
+    }
+    return make_gplan_3d(pb, a, out);
+}
+
+bool make_gplan_3d(const Problem &pb, const Args *a, GPlan *out)
 {
     if (pb.nd != 3 || pb.dtype != CT_F32 || pb.has_add) return false;
     for (int d = 0; d < 3; ++d)

@@ -1,9 +1,13 @@
 #!/usr/bin/env python3
 """Benchmark of the GB300 transposed-convolution library.
 
-Default workload: ConvTranspose1d fp32, N=16, C_in=32, C_out=64, k=3, s=2,
-p=1, d=2, L_in=131072 (L_out=262145), no bias -- inputs resident in HBM, one
-step = one forward pass over the whole batch through the C ABI.
+Default workload: the fused ConvTranspose3d + add + x*hardswish(x) in fp32,
+x (128, 32, 16, 16, 16), w (32, 64, 3, 3, 3), k=3, s=2, p=1, op=1, bias, add
+(128, 64, 32, 32, 32) -- the largest workload of the set (2.2 GB per step) --
+inputs resident in HBM, one step = one forward pass over the whole batch
+through the C ABI, at FP32 accuracy (CT_F32: the three-term tf32 split on the
+tensor cores).  `--split2` runs the opt-in two-term bf16 split
+(CT_F32_BF16X2) instead and says so in the line.
 
 Prints ONE JSON line (rank 0).  `value` is throughput in GFLOP/s of
 algorithmic work (2 x the multiply-adds whose tap lands inside the output),
@@ -33,7 +37,7 @@ if ROOT not in sys.path:
 
 import workloads  # noqa: E402
 
-HEADLINE = "convT1d_L131072"
+HEADLINE = "convT3d_add_hswish"
 METRIC = "ConvTranspose fwd GFLOP/s (and GB/s) on 1 GB300; % of roofline vs CPU oracle"
 L2_BYTES = 129 * 1024 * 1024
 SMS = 152
@@ -239,7 +243,7 @@ def _inputs_to_device(cfg_name, dev, pinned=False, batch=None):
 class Runner:
     """One forward pass of a workload through the C ABI, buffers pre-allocated."""
 
-    def __init__(self, cfg_name, dev, batch=None):
+    def __init__(self, cfg_name, dev, batch=None, split2=False):
         import torch
         import transposed_convolution_convtranspose_gb300 as ct
         self.ct = ct
@@ -260,7 +264,8 @@ class Runner:
         self.y = torch.empty(y_shape, dtype=torch.float32, device=dev)
         self.y_host = torch.empty(y_shape, dtype=torch.float32).pin_memory()
         c = self.cfg
-        self.dt = ct.CT_BF16 if c["dtype"] == "bf16" else ct.CT_F32
+        self.split2 = bool(split2) and c["dtype"] != "bf16"
+        self.dt = ct.CT_BF16 if c["dtype"] == "bf16" else (ct.CT_F32_BF16X2 if self.split2 else ct.CT_F32)
         if self.cl:
             args = (c["nd"], c["N"], c["C_in"], c["C_out"], c["L_in"], c["k"], c["groups"], c["stride"],
                     c["padding"], c["output_padding"], c["dilation"], self.dt)
@@ -294,8 +299,8 @@ class Runner:
         # two when D*H*W is not a multiple of 8; channels last it is the weight
         # repack alone)
         in_sp = int(np.prod(c["L_in"]))
-        self.launches_per_step = {"umma_bf16": 2 if (in_sp % 8 == 0 or self.cl) else 3, "tc3d_bf16split": 2,
-                                  "tc3dg_bf16split": 2}.get(self.path, 1)
+        self.launches_per_step = {"umma_bf16": 2 if (in_sp % 8 == 0 or self.cl) else 3, "tc3d_tf32x3": 2,
+                                  "tc3dg_tf32x3": 2, "tc3d_bf16x2": 2, "tc3dg_bf16x2": 2}.get(self.path, 1)
 
     def forward(self, stream, d=None, y=None):
         c, ct = self.cfg, self.ct
@@ -461,8 +466,15 @@ def time_steps(fn, steps, warmup, ws, flush=None, graph=True):
     return reduce_max(ms / 1e3, ws)
 
 
-def dtype_of(cfg):
-    return "bf16-in/f32-acc" if cfg["dtype"] == "bf16" else "f32"
+def dtype_of(cfg, path):
+    """Arithmetic of the path: bf16 products with fp32 accumulation; fp32
+    (FFMA, or the three-term tf32 split, whose error is that of fp32
+    arithmetic); or the opt-in two-term bf16 split of fp32 operands."""
+    if cfg["dtype"] == "bf16":
+        return "bf16-in/f32-acc"
+    if path.endswith("_bf16x2"):
+        return "f32 operands as bf16 hi+lo pairs (opt-in, ~2^-16 per product)"
+    return "f32"
 
 
 def traffic_for(name, path):
@@ -494,13 +506,13 @@ def roofline(name, cfg, path, wm, sec, peaks):
         return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peaks["source"] + " cuBLAS bf16 burst"}
-    if path in ("tc1d_tf32x3", "tc3d_bf16split", "tc3dg_bf16split"):
-        # FP32 on the tensor cores.  The 1-D kernel does 3 tf32 products per
-        # multiply-add at the tf32 rate (half the bf16 rate); the 3-D kernels one
-        # tf32 product plus one bf16 MMA over twice the K (the two corrections),
-        # i.e. the time of 2 + 2 bf16 products.  The roofline is the slower of
-        # that tensor time and the HBM time of the algorithmic bytes.
-        bf16_products = 6 if path == "tc1d_tf32x3" else 4
+    if path in ("tc1d_tf32x3", "tc3d_tf32x3", "tc3dg_tf32x3", "tc3d_bf16x2", "tc3dg_bf16x2"):
+        # FP32 on the tensor cores.  The tf32x3 kernels do 3 tf32 products per
+        # multiply-add at the tf32 rate (half the bf16 rate): the time of 6 bf16
+        # products; the opt-in bf16x2 kernels 2 bf16 MMAs over twice the K: the
+        # time of 4.  The roofline is the slower of that tensor time and the HBM
+        # time of the algorithmic bytes.
+        bf16_products = 4 if path.endswith("_bf16x2") else 6
         tensor_s = bf16_products * wm["flops"] / (peaks["bf16_tflops"] * 1e12)
         hbm_s = wm["bytes"] / (peaks["hbm_gbs"] * 1e9)
         if hbm_s >= tensor_s:
@@ -541,7 +553,7 @@ def run_gpu_arm(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     name = args.config
-    r = Runner(name, dev, batch=args.batch)
+    r = Runner(name, dev, batch=args.batch, split2=args.split2)
     wm = r.wm
     big = wm["bytes"] > L2_BYTES
     flush_buf = None if big else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -569,9 +581,10 @@ def run_gpu_arm(args, ws, rank, local):
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(r.cfg),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(r.cfg, r.path),
         "data": "synthetic (seeded numpy PCG64; x~N(0,1), w~U(-b,b))",
-        "config": {"workload": name if args.batch is None else "%s (batch %d)" % (name, args.batch),
+        "config": {"workload": (name if args.batch is None else "%s (batch %d)" % (name, args.batch)) +
+                   (" [CT_F32_BF16X2 opt-in]" if r.split2 else ""),
                    "desc": r.cfg["desc"], "global_batch": r.cfg["N"] * ws,
                    "parallelism": "replicas" if ws > 1 else "single",
                    "l2": ("inputs larger than L2 (%.0f MB per step)" % (wm["bytes"] / 1e6)) if big
@@ -592,81 +605,126 @@ def run_gpu_arm(args, ws, rank, local):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def _slice_cfg(cfg, frac):
-    """The workload with batch 1 and its outermost spatial input extent cut to
+def _slice_cfg(cfg, frac, nb=1):
+    """The workload with batch nb and its outermost spatial input extent cut to
     a fraction (same channels, kernel, stride, padding, dilation)."""
     c = dict(cfg)
     L = list(cfg["L_in"])
     L[0] = max(1, int(round(L[0] * frac)))
     c["L_in"] = tuple(L)
-    c["N"] = 1
+    c["N"] = nb
     return c
 
 
-def _oracle_run(cfg, t):
+def _oracle_run(cfg, t, threads=None):
+    """The oracle on one sample: the single-threaded parity oracle
+    (threads=None) or the same scatter definition on `threads` host threads."""
     import oracle
     kw = dict(stride=tuple(cfg["stride"]), padding=tuple(cfg["padding"]),
               output_padding=tuple(cfg["output_padding"]), dilation=tuple(cfg["dilation"]),
               groups=cfg["groups"])
-    y = oracle.conv_transpose(t["x"], t["w"], t["bias"], **kw)
+    if threads is None:
+        y = oracle.conv_transpose(t["x"], t["w"], t["bias"], **kw)
+    else:
+        y = oracle.conv_transpose_mt(t["x"], t["w"], t["bias"], threads=threads, **kw)
     if cfg["add"]:
         y = oracle.add_hswish(y, t["add"])
     return y
 
 
 def _sample_inputs(cfg, seed):
-    x_shape = (1, cfg["C_in"]) + tuple(cfg["L_in"])
+    x_shape = (cfg["N"], cfg["C_in"]) + tuple(cfg["L_in"])
     w_shape = (cfg["C_in"], cfg["C_out"] // cfg["groups"]) + tuple(cfg["k"])
     add_shape = None
     if cfg["add"]:
-        add_shape = tuple(work_model(cfg, N=1)["out_shape"])
+        add_shape = tuple(work_model(cfg)["out_shape"])
     return workloads.make_tensors(seed, x_shape, w_shape, cfg["bound"],
                                   bias_len=cfg["C_out"] if cfg["bias"] else None,
                                   add_shape=add_shape, dtype=cfg["dtype"])
 
 
-def oracle_sample_plan(name, seconds):
-    """Pick the fraction of one batch item that the oracle finishes in about
-    `seconds` (calibrated on a 1/64 slice)."""
+def oracle_sample_plan(name, seconds, threads=None):
+    """The sample the oracle (single-threaded, or on `threads` threads)
+    finishes in about `seconds`: a fraction of one batch item, or as many
+    whole batch items as fit (calibrated on a 1/64 slice of one item)."""
     import oracle
     oracle.build_oracle()
+    oracle.build_oracle_mt()
     cfg = workloads.CONFIGS[name]
     small = _slice_cfg(cfg, 1.0 / 64)
+    part = small["L_in"][0] / cfg["L_in"][0]       # the slice actually cut (at least one plane)
     t = _sample_inputs(small, cfg["seed"])
     t0 = time.perf_counter()
-    _oracle_run(small, t)
+    _oracle_run(small, t, threads)
     dt = max(time.perf_counter() - t0, 1e-4)
-    frac = min(1.0, max(1.0 / 64, seconds / (dt * 64)))
+    items = seconds * part / dt
+    if items >= 2:
+        # a slice that fits in cache runs faster than a whole item: time one item
+        one = _slice_cfg(cfg, 1.0, 1)
+        t = _sample_inputs(one, cfg["seed"])
+        t0 = time.perf_counter()
+        _oracle_run(one, t, threads)
+        items = seconds / max(time.perf_counter() - t0, 1e-4)
+    if items >= 2:
+        nb = int(min(cfg["N"], items))
+        return _slice_cfg(cfg, 1.0, nb), float(nb)
+    frac = min(1.0, max(1.0 / 64, items))
     return _slice_cfg(cfg, frac), frac
 
 
-def oracle_time(scfg, name):
-    """Run the single-threaded oracle once on the sampled workload; returns
-    (GFLOP/s of algorithmic work, seconds)."""
+def oracle_time(scfg, name, threads=None):
+    """Run the oracle once on the sampled workload; returns (GFLOP/s of
+    algorithmic work, seconds)."""
     t = _sample_inputs(scfg, workloads.CONFIGS[name]["seed"])
     t0 = time.perf_counter()
-    _oracle_run(scfg, t)
+    _oracle_run(scfg, t, threads)
     sec = time.perf_counter() - t0
-    return work_model(scfg, N=1)["flops"] / sec / 1e9, sec
+    return work_model(scfg)["flops"] / sec / 1e9, sec
 
 
-def sample_desc(scfg, name, frac):
-    return ("batch 1 of %s with the outermost input extent cut to %s (%.3f of one batch item "
-            "of %d), single-threaded C oracle in float64" % (name, tuple(scfg["L_in"]), frac,
-                                                             workloads.CONFIGS[name]["N"]))
+def sample_desc(scfg, name, frac, threads=None):
+    how = ("single-threaded C oracle in float64" if threads is None else
+           "the oracle's scatter definition in float64 on %d host threads (C, pthreads, one output slice "
+           "(n, oc) per task)" % threads)
+    N = workloads.CONFIGS[name]["N"]
+    if scfg["N"] > 1:
+        what = "batch %d of %s at full spatial size (%d of its %d batch items)" % (scfg["N"], name, scfg["N"], N)
+    else:
+        what = ("batch 1 of %s with the outermost input extent cut to %s (%.3f of one batch item of %d)"
+                % (name, tuple(scfg["L_in"]), frac, N))
+    return "%s, %s" % (what, how)
+
+
+def cpu_baseline(name, seconds):
+    """The CPU baseline: the oracle's definition on every host core, with the
+    single-threaded parity oracle beside it, each on a bounded sample."""
+    import oracle
+    cores = oracle.host_cores()
+    scfg, frac = oracle_sample_plan(name, seconds, threads=cores)
+    v, sec = oracle_time(scfg, name, threads=cores)
+    scfg1, frac1 = oracle_sample_plan(name, seconds)
+    v1, sec1 = oracle_time(scfg1, name)
+    return {"value": round(v, 4), "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": sample_desc(scfg, name, frac, cores), "seconds": round(sec, 2),
+            "hardware_concurrency": os.cpu_count(),
+            "single_core": {"value": round(v1, 4), "unit": "GFLOP/s", "cores": 1,
+                            "sample": sample_desc(scfg1, name, frac1), "seconds": round(sec1, 2)}}
 
 
 def run_reference_arm(args):
-    """The CPU oracle as the reference arm: every step is one bounded sample."""
+    """The CPU oracle as the reference arm: every step is one bounded sample,
+    the oracle's definition on every host core."""
+    import oracle
     cfg = workloads.CONFIGS[args.config]
+    cores = oracle.host_cores()
     per_step = max(0.2, min(20.0, args.ref_seconds / (args.steps + args.warmup)))
-    scfg, frac = oracle_sample_plan(args.config, per_step)
+    scfg, frac = oracle_sample_plan(args.config, per_step, threads=cores)
     for _ in range(args.warmup):
-        oracle_time(scfg, args.config)
-    runs = [oracle_time(scfg, args.config) for _ in range(args.steps)]
+        oracle_time(scfg, args.config, threads=cores)
+    runs = [oracle_time(scfg, args.config, threads=cores) for _ in range(args.steps)]
     tot = sum(s for _, s in runs)
-    value = work_model(scfg, N=1)["flops"] * len(runs) / tot / 1e9
-    desc = sample_desc(scfg, args.config, frac)
+    value = work_model(scfg)["flops"] * len(runs) / tot / 1e9
+    desc = sample_desc(scfg, args.config, frac, cores)
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -674,8 +732,8 @@ def run_reference_arm(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded numpy PCG64)",
         "config": {"workload": args.config, "desc": cfg["desc"]},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
-                         "sample": desc + ", per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc + ", per step", "hardware_concurrency": os.cpu_count()},
         "e2e": {"value": round(value, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -696,6 +754,8 @@ def main(argv=None):
                     help="override the workload's batch size (small cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of a CUDA graph")
+    ap.add_argument("--split2", action="store_true",
+                    help="fp32 workloads with the opt-in two-term bf16 split (CT_F32_BF16X2)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="total oracle time budget of the reference arm")
@@ -719,23 +779,26 @@ def main(argv=None):
     if args.table:
         import torch
         for name in workloads.CONFIG_ORDER:
-            a2 = argparse.Namespace(**vars(args))
-            a2.config = name
-            res, r = run_gpu_arm(a2, ws, rank, local)
-            del r
-            torch.cuda.empty_cache()
-            if rank == 0:
-                print(json.dumps(res), flush=True)
+            # every workload at its default arithmetic; the FP32 tensor-core
+            # workloads a second time with the opt-in two-term bf16 split
+            for split2 in (False, True):
+                a2 = argparse.Namespace(**vars(args))
+                a2.config = name
+                a2.split2 = split2
+                res, r = run_gpu_arm(a2, ws, rank, local)
+                has_opt_in = r.path in ("tc3d_tf32x3", "tc3dg_tf32x3")
+                del r
+                torch.cuda.empty_cache()
+                if rank == 0:
+                    print(json.dumps(res), flush=True)
+                if not has_opt_in:
+                    break
         return 0
 
     res, r = run_gpu_arm(args, ws, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
-            scfg, frac = oracle_sample_plan(args.config, args.cpu_seconds)
-            v, sec = oracle_time(scfg, args.config)
-            res["cpu_baseline"] = {"value": round(v, 4), "unit": "GFLOP/s", "cores": 1,
-                                   "kind": "oracle", "sample": sample_desc(scfg, args.config, frac),
-                                   "seconds": round(sec, 2)}
+            res["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
         print(json.dumps(res), flush=True)
     if ws > 1:
         import torch.distributed as dist

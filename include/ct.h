@@ -36,20 +36,27 @@
  *
  * Execution: every forward call only validates its arguments on the host,
  * then enqueues kernels on `stream` (a cudaStream_t; NULL = the legacy
- * default stream) and returns; nothing is synchronised and nothing is
- * allocated.  The tensor-core paths keep repacked operands in scratch memory
- * taken from the caller-supplied `workspace` of at least the size that
- * ct_workspace_size_* reports (256-byte aligned).  The bf16 path requires it
- * (CT_ERR_WORKSPACE otherwise); a FP32 3-D call given less than the reported
- * size runs the FFMA kernel instead, with the same results up to rounding.
- * Paths that report 0 accept workspace = NULL, ws_bytes = 0.  The workspace
- * is overwritten; calls that share one must not overlap on the GPU.
+ * default stream) and returns; nothing is synchronised and no device memory
+ * is allocated.  The tensor-core paths keep repacked operands in scratch
+ * memory taken from the caller-supplied `workspace`.  A workspace is either
+ * absent (workspace = NULL or ws_bytes = 0) or at least the size that
+ * ct_workspace_size_* reports for the same arguments and 256-byte aligned;
+ * anything in between returns CT_ERR_WORKSPACE.  The bf16 tensor-core path
+ * requires it (CT_ERR_WORKSPACE without); an FP32 2-D or 3-D call without a
+ * workspace runs the kernels that need none (the FFMA or generic kernel,
+ * same results up to rounding, slower) -- ct_path_call in ct_introspect.h
+ * reports which.  The workspace is overwritten; calls that share one must
+ * not overlap on the GPU.
  *
  * Errors: argument and shape errors are returned synchronously before any
- * launch and leave y untouched.  A failed launch returns CT_ERR_CUDA.  The
- * bf16 tensor-core kernel bounds every wait; a wait that runs out records
- * CT_ERR_DEVICE_TIMEOUT in a device status word, read (and cleared) by
- * ct_last_device_error().
+ * launch and leave y untouched.  A failed launch returns CT_ERR_CUDA.  Every
+ * wait of the pipelined kernels is bounded; a wait that runs out records
+ * CT_ERR_DEVICE_TIMEOUT in a status word in page-locked host memory that the
+ * kernels write directly.  The next forward call that finds it set returns
+ * CT_ERR_DEVICE_TIMEOUT without launching (and clears it), as does
+ * ct_last_device_error(), which synchronises the stream first.  The word is
+ * registered with cudaHostRegister on the first launch; make that first call
+ * before any stream capture.
  */
 #ifndef CT_H
 #define CT_H
@@ -73,7 +80,19 @@ typedef enum {
     CT_ERR_DEVICE_TIMEOUT = 7  /* a bounded device-side wait ran out                */
 } ct_status;
 
-typedef enum { CT_F32 = 0, CT_BF16 = 1 } ct_dtype;
+/* dtype of x and w (bias, add and y are always fp32):
+ *   CT_F32         fp32.  The result is FP32-accurate: every path computes in
+ *                  fp32, or on the tensor cores from a three-term tf32 split of
+ *                  each operand (error within about 2^-20 of sum |x||w| per
+ *                  output, the accuracy of fp32 arithmetic over the same sum).
+ *   CT_BF16        bf16 x and w, fp32 accumulation.
+ *   CT_F32_BF16X2  fp32 x and w, as CT_F32, for callers that accept about
+ *                  16-bit operand precision: the 2-D and 3-D FP32 tensor-core
+ *                  paths multiply a two-term bf16 split of each operand
+ *                  (relative error up to about 2^-16 of sum |x||w| per output)
+ *                  and issue fewer MMAs.  Opt-in only; every other path computes
+ *                  as with CT_F32. */
+typedef enum { CT_F32 = 0, CT_BF16 = 1, CT_F32_BF16X2 = 2 } ct_dtype;
 
 /* Output length of one spatial dimension ([l1_p79] output-length formula),
  * or -1 if the parameters are invalid (k, s, dl < 1; p, op < 0; result < 1). */
@@ -177,10 +196,12 @@ ct_status ct_forward_3d_add_hswish(const void *x, const void *w, const float *bi
  *
  * Scratch: a buffer of CT_NOALLOC_SCRATCH_BYTES (48 MiB) that the library
  * owns, a static device array that every GPU which loads libct.so keeps
- * until the process exits.  The first call on a device looks up the
- * buffer's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every call on a device
- * shares the one buffer, so calls that overlap on the GPU (different
+ * until the process exits.  Every call looks up the buffer's device address
+ * (cudaGetSymbolAddress) with the caller's device and context current, so
+ * the address is always that of the current context, also after a
+ * cudaDeviceReset; the first call on a device loads the library's module
+ * there, so make that first call before any stream capture.  Every call on a
+ * device shares the one buffer, so calls that overlap on the GPU (different
  * streams, or other threads) race and must be serialised by the caller.
  * Each call rewrites every scratch byte it reads, so no state carries over
  * from the last call and nothing needs clearing.
@@ -188,9 +209,9 @@ ct_status ct_forward_3d_add_hswish(const void *x, const void *w, const float *bi
  * Arguments and layouts as ct_forward_3d with dtype CT_BF16.  Returns
  * CT_ERR_UNSUPPORTED when the arguments do not take the bf16 tensor-core
  * path (other paths need no scratch: use ct_forward_3d), CT_ERR_WORKSPACE
- * when the problem needs more scratch than CT_NOALLOC_SCRATCH_BYTES
- * (2*(N*C_in*D*H*W + 8*C_out*(k/2)^3*C_in) bytes, each part rounded up to
- * 256), CT_ERR_CUDA when the set-up or a launch fails. */
+ * when the problem needs more scratch than CT_NOALLOC_SCRATCH_BYTES (the
+ * size ct_workspace_size_3d reports for the same arguments), CT_ERR_CUDA
+ * when the address lookup or a launch fails. */
 #define CT_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
 ct_status ct_forward_3d_noalloc(const void *x, const void *w, const float *bias, float *y,
                                 int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
@@ -198,39 +219,13 @@ ct_status ct_forward_3d_noalloc(const void *x, const void *w, const float *bias,
                                 const int output_padding[3], const int dilation[3],
                                 ct_dtype dtype, void *stream);
 
-/* Name of the kernel family the 1-D / 2-D / 3-D / fused call with these arguments
- * (ct_path_cl: in channels-last layouts) would launch when given the workspace
- * ct_workspace_size_* reports
- * ("gather_generic", "phase1d_f32", "tc1d_tf32x3", "phase3d_f32", "tc3d_bf16split",
- * "tc3dg_bf16split" -- 32 input channels in 1, 2 or 4 groups -- or "umma_bf16"),
- * or NULL if the arguments are invalid.  Host only; launches
- * nothing.  `fused` selects the add + hardswish variant for the 2-D and 3-D queries. */
-const char *ct_path_1d(int N, int C_in, int C_out, int L_in, int k, int groups, int stride,
-                       int padding, int output_padding, int dilation, ct_dtype dtype);
-const char *ct_path_2d(int N, int C_in, int C_out, const int in_hw[2], const int k_hw[2],
-                       int groups, const int stride[2], const int padding[2],
-                       const int output_padding[2], const int dilation[2], ct_dtype dtype,
-                       int fused);
-const char *ct_path_cl(int nd, int N, int C_in, int C_out, const int *in_size, const int *k, int groups,
-                       const int *stride, const int *padding, const int *output_padding,
-                       const int *dilation, ct_dtype dtype, int fused);
-const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
-                       int groups, const int stride[3], const int padding[3],
-                       const int output_padding[3], const int dilation[3], ct_dtype dtype,
-                       int fused);
-
-/* Process-wide path override for testing the dispatcher: 0 = automatic
- * (default), 1 = always use the generic gather kernel, 2 = automatic but
- * without the FP32 tensor-core paths (the FFMA phase kernels instead).  Not
- * thread-safe against concurrent forward calls. */
-void ct_set_path_override(int mode);
-
 /* Human-readable name of a status code (static string, never NULL). */
 const char *ct_status_str(ct_status s);
 
-/* Synchronises `stream`, then returns and clears the device status word of
- * the current device: CT_OK, or CT_ERR_DEVICE_TIMEOUT if a bounded wait in a
- * kernel ran out since the last query; CT_ERR_CUDA if synchronising failed. */
+/* Synchronises `stream`, then returns and clears the status word: CT_OK, or
+ * CT_ERR_DEVICE_TIMEOUT if a bounded wait in a kernel ran out since the last
+ * query (by this call or by a forward call); CT_ERR_CUDA if synchronising
+ * failed. */
 ct_status ct_last_device_error(void *stream);
 
 /* Failure-detection self-test: launches on `stream` a one-thread kernel that

@@ -41,6 +41,33 @@ def build_oracle(src=_SRC, out=_LIB_PATH, force=False):
     return out
 
 
+_MT_SRC = os.path.join(_HERE, "ct_oracle_mt.c")
+_MT_LIB_PATH = os.path.join(_BUILD_DIR, "libct_oracle_mt.so")
+_mt_lib = None
+
+
+def build_oracle_mt(src=_MT_SRC, out=_MT_LIB_PATH, force=False):
+    """Compile the all-cores baseline (pthreads) with the oracle's flags."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-o", tmp, src]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def host_cores():
+    """Cores this process may run on (the affinity mask; os.cpu_count otherwise)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
 def load_library(path):
     lib = ctypes.CDLL(path)
     lib.ora_out_len.restype = ctypes.c_int64
@@ -176,3 +203,37 @@ def add_hswish(y, add=None, lib=None):
     out = np.empty_like(y)
     lib.ora_add_hswish(y.size, _dp(y), _dp(a), _dp(out))
     return out
+
+
+def _get_mt():
+    global _mt_lib
+    with _lock:
+        if _mt_lib is None:
+            lib = ctypes.CDLL(build_oracle_mt())
+            lib.ora_mt_conv_transpose.restype = ctypes.c_int
+            lib.ora_mt_conv_transpose.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.c_int64, _I64P, _I64P, _I64P, _I64P,
+                                                  _I64P, _I64P, _DP, _DP, _DP, _DP]
+            _mt_lib = lib
+    return _mt_lib
+
+
+def conv_transpose_mt(x, w, bias=None, stride=1, padding=0, output_padding=0, dilation=1,
+                      groups=1, threads=None):
+    """The scatter definition on `threads` host threads (default: every core
+    of the affinity mask), split by output slice (n, oc) -- the CPU baseline
+    of the benchmark.  Same result as conv_transpose up to summation order."""
+    lib = _get_mt()
+    threads = host_cores() if threads is None else int(threads)
+    x, w, bias = _f64(x), _f64(w), _f64(bias)
+    nd, N, C_in, C_out, L, K, S, P, OP, DL = _args(x, w, groups, stride, padding,
+                                                   output_padding, dilation)
+    Lo = [out_len(L[d], K[d], S[d], P[d], OP[d], DL[d]) for d in range(nd)]
+    if min(Lo) <= 0:
+        raise ValueError("non-positive output length %r" % (Lo,))
+    y = np.empty([N, C_out] + Lo, dtype=np.float64)
+    rc = lib.ora_mt_conv_transpose(threads, nd, N, C_in, C_out, groups, _i64(L), _i64(K), _i64(S),
+                                   _i64(P), _i64(OP), _i64(DL), _dp(x), _dp(w), _dp(bias), _dp(y))
+    if rc != 0:
+        raise ValueError("all-cores oracle rejected the arguments (rc=%d)" % rc)
+    return y

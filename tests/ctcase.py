@@ -61,13 +61,14 @@ def run_gpu(c, t, dev="cuda:0", inplace_add=False):
     import transposed_convolution_convtranspose_gb300 as ct
     x, w, b, a = to_device(t, c, dev)
     kw = kwargs(c)
+    kw["split2"] = bool(c.get("split2", False))
     if c.get("layout", "cf") == "cl":
         # channels-last call on the same values; the result is returned in the
         # oracle's channels-first order
         xcl = x.movedim(1, -1).contiguous()
         acl = a.movedim(1, -1).contiguous() if a is not None else None
         if c["nd"] == 1:
-            kw = {k: (v if k == "groups" else (v,)) for k, v in kw.items()}
+            kw = {k: (v if k in ("groups", "split2") else (v,)) for k, v in kw.items()}
         y = ct.conv_transpose_cl(xcl, w, b, acl, out=acl if inplace_add else None, **kw)
         return y.movedim(-1, 1).contiguous()
     if c["nd"] == 1:

@@ -137,7 +137,7 @@ def test_path_selection(lib):
     # the grouped workload: the grouped FP32 tensor-core path, the FFMA kernel
     # under override 2
     grouped = (8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3), (1, 1, 1), (1, 1, 1), ct.CT_F32)
-    assert ct.ct_path_3d(*grouped) == "tc3dg_bf16split"
+    assert ct.ct_path_3d(*grouped) == "tc3dg_tf32x3"
     ct.ct_set_path_override(2)
     try:
         assert ct.ct_path_3d(*grouped) == "phase3d_f32"
@@ -152,7 +152,7 @@ def test_path_selection(lib):
     # the fused workload: FP32 tensor-core path, FFMA kernel under override 2
     fused = (128, 32, 64, (16, 16, 16), (3, 3, 3), 1, (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1),
              ct.CT_F32, 1)
-    assert ct.ct_path_3d(*fused) == "tc3d_bf16split"
+    assert ct.ct_path_3d(*fused) == "tc3d_tf32x3"
     ct.ct_set_path_override(2)
     try:
         assert ct.ct_path_3d(*fused) == "phase3d_f32"
@@ -164,8 +164,8 @@ def test_path_selection_2d(lib):
     """A 2-D call is the 3-D operator with a unit D dimension: dense stride-2
     layers take the tensor-core kernels, the rest the generic kernel."""
     dense = (32, 64, 64, (128, 128), (4, 4), 1, (2, 2), (1, 1), (0, 0), (1, 1))
-    assert ct.ct_path_2d(*dense, ct.CT_F32) == "tc3d_bf16split"
-    assert ct.ct_path_2d(*dense, ct.CT_F32, fused=True) == "tc3d_bf16split"
+    assert ct.ct_path_2d(*dense, ct.CT_F32) == "tc3d_tf32x3"
+    assert ct.ct_path_2d(*dense, ct.CT_F32, fused=True) == "tc3d_tf32x3"
     assert ct.ct_path_2d(*dense, ct.CT_BF16) == "umma_bf16"
     # kH * kW = 4: the bf16 weight repack needs multiples of 8 -> generic
     assert ct.ct_path_2d(1, 64, 32, (4, 8), (2, 2), 1, (2, 2), (0, 0), (0, 0), (1, 1),
@@ -174,7 +174,7 @@ def test_path_selection_2d(lib):
                          ct.CT_F32) == "gather_generic"
     # 32 input channels in groups: the grouped tensor-core path (fused: generic)
     assert ct.ct_path_2d(2, 32, 32, (16, 16), (5, 7), 4, (2, 2), (2, 3), (1, 1), (1, 1),
-                         ct.CT_F32) == "tc3dg_bf16split"
+                         ct.CT_F32) == "tc3dg_tf32x3"
     assert ct.ct_path_2d(2, 32, 32, (16, 16), (5, 7), 4, (2, 2), (2, 3), (1, 1), (1, 1),
                          ct.CT_F32, fused=True) == "gather_generic"
     ct.ct_set_path_override(2)
@@ -203,8 +203,8 @@ def test_path_selection_channels_last(lib):
     dense = (16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1))
     assert ct.ct_path_cl(3, *dense, ct.CT_BF16) == "umma_bf16"
     assert ct.ct_path_cl(3, *dense, ct.CT_BF16, fused=True) == "gather_generic"
-    assert ct.ct_path_cl(3, *dense, ct.CT_F32) == "tc3d_bf16split"
-    assert ct.ct_path_cl(3, *dense, ct.CT_F32, fused=True) == "tc3d_bf16split"
+    assert ct.ct_path_cl(3, *dense, ct.CT_F32) == "tc3d_tf32x3"
+    assert ct.ct_path_cl(3, *dense, ct.CT_F32, fused=True) == "tc3d_tf32x3"
     grouped = (8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3), (1, 1, 1), (1, 1, 1))
     assert ct.ct_path_cl(3, *grouped, ct.CT_F32) == "gather_generic"
     d2 = (16, 256, 128, (64, 64), (4, 4), 1, (2, 2), (1, 1), (0, 0), (1, 1))
@@ -225,16 +225,20 @@ def test_path_selection_channels_last(lib):
 
 def test_workspace_sizes(lib):
     assert ct.ct_workspace_size_1d(16, 32, 64, 131072, 3, 1, 2, 1, 0, 2, ct.CT_F32) == 0
-    # FP32 3-D tensor-core path: a channels-last copy of x as bf16 (hi, lo)
-    # pairs, hi and lo per-tap weight panels
-    nf = ct.ct_workspace_size_3d(128, 32, 64, (16, 16, 16), (3, 3, 3), 1, (2, 2, 2), (1, 1, 1),
-                                 (1, 1, 1), (1, 1, 1), ct.CT_F32)
-    assert nf >= 128 * 32 * 16 ** 3 * 4 + 2 * 27 * 64 * 32 * 4
-    # the grouped workload: an (N, D, W, H, 64) bf16 (hi, lo) copy of x and one
-    # hi + lo panel per input offset (24 offsets, 1920 rows of 128 bytes)
+    # FP32 3-D tensor-core path: a channels-last copy of x as tf32 (t, l) pairs
+    # (8 bytes per value) and the per-tap weight panels (8 bytes per weight);
+    # the opt-in bf16 split keeps (hi, lo) bf16 pairs (4 bytes per value)
+    fused = (128, 32, 64, (16, 16, 16), (3, 3, 3), 1, (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1))
+    nf = ct.ct_workspace_size_3d(*fused, ct.CT_F32)
+    assert nf >= 128 * 32 * 16 ** 3 * 8 + 27 * 64 * 32 * 8
+    nf2 = ct.ct_workspace_size_3d(*fused, ct.CT_F32_BF16X2)
+    assert 128 * 32 * 16 ** 3 * 4 + 2 * 27 * 64 * 32 * 4 <= nf2 < nf
+    # the grouped workload: an (N, D, W, H, 64) copy of x (tf32 t and l parts:
+    # 8 bytes per value) and one t + l panel per input offset (24 offsets, 1920
+    # rows of 128 bytes)
     ng = ct.ct_workspace_size_3d(8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3),
                                  (1, 1, 1), (1, 1, 1), ct.CT_F32)
-    assert ng >= 8 * 32 * 16 * 32 * 32 * 4 + 1920 * 32 * 4
+    assert ng >= 8 * 32 * 16 * 32 * 32 * 8 + 1920 * 32 * 4
     nb = ct.ct_workspace_size_3d(16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1),
                                  (0, 0, 0), (1, 1, 1), ct.CT_BF16)
     path = ct.ct_path_3d(16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1),
@@ -252,3 +256,66 @@ def test_selftest_rejects_out_of_range_limits(lib):
         with pytest.raises(ct.CTError) as ei:
             ct.ct_selftest_wait_timeout(bad)
         assert ei.value.code == ct.CT_ERR_ARG
+
+
+def test_opt_in_split_path_names(lib):
+    """CT_F32_BF16X2 stores x and w as fp32 and selects the two-term bf16 split
+    on the FP32 2-D / 3-D tensor-core paths only; every other path is the
+    CT_F32 one."""
+    fused = (128, 32, 64, (16, 16, 16), (3, 3, 3), 1, (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1))
+    assert ct.ct_path_3d(*fused, ct.CT_F32_BF16X2, 1) == "tc3d_bf16x2"
+    grouped = (8, 32, 32, (16, 32, 32), (3, 5, 7), 4, (2, 2, 2), (1, 2, 3), (1, 1, 1), (1, 1, 1))
+    assert ct.ct_path_3d(*grouped, ct.CT_F32_BF16X2, 0) == "tc3dg_bf16x2"
+    assert ct.ct_path_2d(64, 32, 64, (128, 128), (3, 3), 1, (2, 2), (1, 1), (1, 1), (1, 1),
+                         ct.CT_F32_BF16X2, 0) == "tc3d_bf16x2"
+    assert ct.ct_path_1d(16, 32, 64, 131072, 3, 1, 2, 1, 0, 2, ct.CT_F32_BF16X2) == "tc1d_tf32x3"
+    assert ct.ct_path_3d(1, 6, 4, (3, 4, 5), (2, 3, 4), 2, (3, 1, 2), (1, 0, 2), (2, 0, 1), (1, 2, 1),
+                         ct.CT_F32_BF16X2, 0) == "gather_generic"
+    assert call1d(lib, dtype=ct.CT_F32_BF16X2, N=0) == 0
+    assert call1d(lib, dtype=3) == 1
+
+
+def _fused_call(lib, ws, ws_bytes):
+    i3 = ct._I3
+    return lib.ct_forward_3d_add_hswish(FAKE, FAKE + (1 << 24), None, FAKE + (1 << 26), FAKE + (1 << 28), 1, 32,
+                                        64, i3(4, 4, 4), i3(3, 3, 3), 1, i3(2, 2, 2), i3(1, 1, 1),
+                                        i3(1, 1, 1), i3(1, 1, 1), ct.CT_F32, ws, ws_bytes, None)
+
+
+def test_workspace_rule(lib):
+    """A workspace is absent or at least the reported size: a non-zero one that
+    is too small (or misaligned, or a NULL pointer with a size) is rejected
+    before any launch instead of silently changing the kernel; ct_path_call
+    reports the kernel of a call with a given workspace size."""
+    args = (3, 0, 1, 32, 64, (4, 4, 4), (3, 3, 3), 1, (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1))
+    need = ct.ct_workspace_size_3d(1, 32, 64, (4, 4, 4), (3, 3, 3), 1, (2, 2, 2), (1, 1, 1), (1, 1, 1),
+                                   (1, 1, 1), ct.CT_F32)
+    assert need > 0
+    WS = FAKE + (1 << 30)
+    assert _fused_call(lib, WS, need - 256) == ct.CT_ERR_WORKSPACE
+    assert _fused_call(lib, WS + 16, need) == ct.CT_ERR_WORKSPACE     # not 256-byte aligned
+    assert _fused_call(lib, None, need) == ct.CT_ERR_WORKSPACE         # a size without a buffer
+    assert ct.ct_path_call(*args, ct.CT_F32, 1, need) == "tc3d_tf32x3"
+    assert ct.ct_path_call(*args, ct.CT_F32, 1, need + 4096) == "tc3d_tf32x3"
+    assert ct.ct_path_call(*args, ct.CT_F32, 1, need - 256) is None
+    assert ct.ct_path_call(*args, ct.CT_F32, 1, 0) == "phase3d_f32"   # no workspace: the FFMA kernel
+    assert ct.ct_path_call(*args, ct.CT_F32_BF16X2, 1, 0) == "phase3d_f32"
+    # bf16 on the tensor cores needs its workspace; channels-last bf16 only the panels
+    dense = (3, 0, 16, 256, 128, (16, 16, 16), (4, 4, 4), 1, (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1))
+    nb = ct.ct_workspace_size_3d(*dense[2:], ct.CT_BF16)
+    assert ct.ct_path_call(*dense, ct.CT_BF16, 0, 0) is None
+    assert ct.ct_path_call(*dense, ct.CT_BF16, 0, nb) == "umma_bf16"
+    dense_cl = (3, 1) + dense[2:]
+    ncl = ct.ct_workspace_size_cl(3, *dense[2:], ct.CT_BF16)
+    assert ct.ct_path_call(*dense_cl, ct.CT_BF16, 0, ncl) == "umma_bf16"
+    # paths without scratch accept any workspace and none
+    assert ct.ct_path_call(1, 0, 16, 32, 64, (131072,), (3,), 1, (2,), (1,), (0,), (2,), ct.CT_F32, 0, 0) == \
+        "tc1d_tf32x3"
+    assert ct.ct_path_call(1, 0, 16, 32, 64, (0,), (3,), 1, (2,), (1,), (0,), (2,), ct.CT_F32, 0, 0) is None
+
+
+def test_noalloc_scratch_constant_matches_header(lib):
+    txt = open(os.path.join(ROOT, "include", "ct.h")).read()
+    m = re.search(r"#define\s+CT_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*\*\s*(\d+)u\s*\*\s*(\d+)u\)", txt)
+    assert m, "CT_NOALLOC_SCRATCH_BYTES not found in include/ct.h"
+    assert int(m.group(1)) * int(m.group(2)) * int(m.group(3)) == ct.CT_NOALLOC_SCRATCH_BYTES

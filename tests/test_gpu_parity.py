@@ -34,7 +34,7 @@ def _sync():
 
 def path_of(c):
     import transposed_convolution_convtranspose_gb300 as ct
-    dt = ct.CT_BF16 if c["dtype"] == "bf16" else ct.CT_F32
+    dt = ct.CT_BF16 if c["dtype"] == "bf16" else (ct.CT_F32_BF16X2 if c.get("split2") else ct.CT_F32)
     if c.get("layout", "cf") == "cl":
         return ct.ct_path_cl(c["nd"], c["N"], c["C_in"], c["C_out"], c["L"], c["K"], c["G"], c["S"],
                              c["P"], c["OP"], c["DL"], dt, c["add"])
@@ -211,7 +211,7 @@ TC3D = [
 def test_fp32_3d_tensor_core_shapes(k, add):
     c = dict(nd=3, G=1, S=[2, 2, 2], DL=[1, 1, 1], bias=bool(k % 2 == 0), add=add, dtype="f32",
              **TC3D[k])
-    assert path_of(c) == "tc3d_bf16split", (c, path_of(c))
+    assert path_of(c) == "tc3d_tf32x3", (c, path_of(c))
     t = cc.make_inputs(c, seed=800 + k + (50 if add else 0))
     y = cc.run_gpu(c, t).cpu().numpy()
     cc.assert_close(y, cc.run_oracle(c, t), "f32", "tc3d case %d add=%s %r" % (k, add, c))
@@ -237,7 +237,7 @@ TC3DG = [
 @pytest.mark.parametrize("k", range(len(TC3DG)))
 def test_fp32_3d_grouped_tensor_core_shapes(k):
     c = dict(nd=3, S=[2, 2, 2], DL=[1, 1, 1], bias=bool(k % 2 == 0), add=False, dtype="f32", **TC3DG[k])
-    assert path_of(c) == "tc3dg_bf16split", (c, path_of(c))
+    assert path_of(c) == "tc3dg_tf32x3", (c, path_of(c))
     t = cc.make_inputs(c, seed=900 + k)
     y = cc.run_gpu(c, t).cpu().numpy()
     cc.assert_close(y, cc.run_oracle(c, t), "f32", "tc3dg case %d %r" % (k, c))
@@ -269,7 +269,7 @@ TC2D = [
 @pytest.mark.parametrize("k", range(len(TC2D)))
 def test_fp32_2d_tensor_core_shapes(k, add):
     c = dict(nd=2, G=1, S=[2, 2], DL=[1, 1], bias=bool(k % 2 == 0), add=add, dtype="f32", **TC2D[k])
-    assert path_of(c) == "tc3d_bf16split", (c, path_of(c))
+    assert path_of(c) == "tc3d_tf32x3", (c, path_of(c))
     t = cc.make_inputs(c, seed=1000 + k + (50 if add else 0))
     y = cc.run_gpu(c, t).cpu().numpy()
     cc.assert_close(y, cc.run_oracle(c, t), "f32", "2-D tc case %d add=%s %r" % (k, add, c))
@@ -293,7 +293,7 @@ TC2DG = [
 @pytest.mark.parametrize("k", range(len(TC2DG)))
 def test_fp32_2d_grouped_tensor_core_shapes(k):
     c = dict(nd=2, S=[2, 2], DL=[1, 1], bias=bool(k % 2 == 0), add=False, dtype="f32", **TC2DG[k])
-    assert path_of(c) == "tc3dg_bf16split", (c, path_of(c))
+    assert path_of(c) == "tc3dg_tf32x3", (c, path_of(c))
     t = cc.make_inputs(c, seed=1700 + k)
     y = cc.run_gpu(c, t).cpu().numpy()
     cc.assert_close(y, cc.run_oracle(c, t), "f32", "2-D grouped case %d %r" % (k, c))
@@ -353,30 +353,74 @@ def test_2d_generic_shapes(k):
     cc.assert_close(y, cc.run_oracle(c, t), c["dtype"], "2-D generic case %d %r" % (k, c))
 
 
-# The two-term bf16 split of the FP32 3-D / 2-D kernels: every product is
-# (x_hi + x_lo)(w_hi + w_lo) with each part's bf16 product exact, so the error
-# of an output is bounded by a small multiple of 2^-16 times the sum of the
-# magnitudes of its products, S = sum |x| |w| (plus fp32 accumulation).  S is
-# the oracle run on |x|, |w| without bias.
-SPLIT_CASES = [("convT3d_add_hswish", dict(N=1), False), ("convT3d_grouped", dict(N=1), False),
-               ("convT2d_f32", dict(N=1), False)]
+# Accuracy of the splits of the FP32 tensor-core kernels, measured against
+# S = sum |x| |w| of each output (the oracle run on |x|, |w| without bias):
+#  * tf32x3 (CT_F32, the default): every product is x_t w_t + x_t w_l + x_l w_t
+#    with the dropped terms below 3 x 2^-22 |x||w|; with the fp32 accumulation
+#    an output must stay within 2^-19 S -- and within a small factor of the
+#    error the FP32 FFMA kernel (plain fp32 multiply-adds) makes on the same
+#    inputs, i.e. as accurate as fp32 arithmetic;
+#  * bf16x2 (CT_F32_BF16X2, opt-in): every product is (x_hi + x_lo)(w_hi +
+#    w_lo) with each part's remainder below 2^-17, so an output stays within a
+#    small multiple of 2^-16 S.
+SPLIT_CASES = ["convT3d_add_hswish", "convT3d_grouped", "convT2d_f32"]
+
+
+def _split_ratio(c, t, split2):
+    y = cc.run_gpu(dict(c, split2=split2), t).cpu().numpy().astype(np.float64)
+    ref = cc.run_oracle(c, t)
+    mag = dict(t, x=np.abs(t["x"]), w=np.abs(t["w"]), bias=None)
+    S = cc.run_oracle(dict(c, bias=False), mag)
+    return float((np.abs(y - ref) / (S + 1e-30)).max())
 
 
 @pytest.mark.parametrize("k", range(len(SPLIT_CASES)))
 def test_fp32_split_error_bound(k):
-    name, over, _ = SPLIT_CASES[k]
-    c = cc.case_from_config(name, N=over["N"])
+    import transposed_convolution_convtranspose_gb300 as ct
+    name = SPLIT_CASES[k]
+    c = cc.case_from_config(name, N=1)
     c["add"] = False                      # the bound concerns the convolution itself
-    assert path_of(c) in ("tc3d_bf16split", "tc3dg_bf16split"), path_of(c)
     t = cc.make_inputs(c, seed=1400 + k, bound=workloads.CONFIGS[name]["bound"])
-    y = cc.run_gpu(c, t).cpu().numpy().astype(np.float64)
-    ref = cc.run_oracle(c, t)
-    mag = dict(t, x=np.abs(t["x"]), w=np.abs(t["w"]), bias=None)
-    S = cc.run_oracle(dict(c, bias=False), mag)
-    ratio = np.abs(y - ref) / (S + 1e-30)
-    worst = float(ratio.max())
-    print("%s: max |err| / sum|x||w| = %.3g (2^%.1f)" % (name, worst, np.log2(max(worst, 1e-300))))
-    assert worst < 2.0 ** -14, (name, worst)
+    assert path_of(c) in ("tc3d_tf32x3", "tc3dg_tf32x3"), path_of(c)
+    r3 = _split_ratio(c, t, False)
+    assert path_of(dict(c, split2=True)) in ("tc3d_bf16x2", "tc3dg_bf16x2"), path_of(dict(c, split2=True))
+    r2 = _split_ratio(c, t, True)
+    ct.ct_set_path_override(2)            # the FFMA kernels: plain fp32 arithmetic
+    try:
+        assert path_of(c) in ("phase3d_f32", "gather_generic"), path_of(c)
+        rf = _split_ratio(c, t, False)
+    finally:
+        ct.ct_set_path_override(0)
+    print("%s: max |err| / sum|x||w|: tf32x3 2^%.1f, fp32 FFMA 2^%.1f, bf16x2 2^%.1f"
+          % (name, np.log2(max(r3, 1e-300)), np.log2(max(rf, 1e-300)), np.log2(max(r2, 1e-300))))
+    assert r3 < 2.0 ** -19, (name, r3)
+    assert r3 < 4.0 * rf + 2.0 ** -22, (name, r3, rf)
+    assert r2 < 2.0 ** -14, (name, r2)
+
+
+# The opt-in two-term bf16 split (CT_F32_BF16X2) on the dense, grouped and
+# 2-D FP32 tensor-core shapes: within the FP32 tolerance of the oracle, and
+# exact on small integers (each integer in [-3, 3] is its own bf16 hi part).
+SPLIT2_CASES = [
+    dict(nd=3, G=1, S=[2, 2, 2], DL=[1, 1, 1], add=True, **TC3D[0]),
+    dict(nd=3, G=1, S=[2, 2, 2], DL=[1, 1, 1], add=False, **TC3D[1]),
+    dict(nd=3, S=[2, 2, 2], DL=[1, 1, 1], add=False, **TC3DG[0]),
+    dict(nd=2, G=1, S=[2, 2], DL=[1, 1], add=False, **TC2D[1]),
+    dict(nd=2, S=[2, 2], DL=[1, 1], add=False, **TC2DG[1]),
+]
+
+
+@pytest.mark.parametrize("k", range(len(SPLIT2_CASES)))
+def test_fp32_bf16x2_opt_in_shapes(k):
+    c = dict(SPLIT2_CASES[k], bias=True, dtype="f32", split2=True)
+    want = "tc3dg_bf16x2" if c["G"] > 1 else "tc3d_bf16x2"
+    assert path_of(c) == want, (c, path_of(c))
+    t = cc.make_inputs(c, seed=1450 + k)
+    cc.assert_close(cc.run_gpu(c, t).cpu().numpy(), cc.run_oracle(c, t), "f32", "bf16x2 case %d %r" % (k, c))
+    if not c["add"]:
+        ti = cc.make_inputs(c, seed=1470 + k, int_range=3)
+        yi = cc.run_gpu(c, ti).cpu().numpy()
+        assert np.array_equal(yi.astype(np.float64), cc.run_oracle(c, ti)), "bf16x2 integer case %d" % k
 
 
 # Shapes with s > (k - 1) d: the stride phases do not overlap, every output
@@ -403,7 +447,7 @@ DISJOINT = [
 def test_disjoint_phase_shapes_exact(k):
     c = dict(DISJOINT[k], bias=True, add=False)
     if k in (2, 3):
-        assert path_of(c) in ("tc3d_bf16split", "umma_bf16"), path_of(c)
+        assert path_of(c) in ("tc3d_tf32x3", "umma_bf16"), path_of(c)
     t = cc.make_inputs(c, seed=1500 + k, int_range=3)
     y = cc.run_gpu(c, t).cpu().numpy()
     ref = cc.run_oracle(c, t)
@@ -430,13 +474,13 @@ CL = [
     dict(nd=2, N=2, C_in=128, C_out=128, G=1, L=[5, 12], K=[4, 4], S=[2, 2], P=[1, 1], OP=[1, 0],
          DL=[1, 1], dtype="bf16", add=False, path="umma_bf16"),
     dict(nd=3, N=1, C_in=32, C_out=64, G=1, L=[3, 4, 8], K=[3] * 3, S=[2] * 3, P=[1] * 3, OP=[1] * 3,
-         DL=[1] * 3, dtype="f32", add=True, path="tc3d_bf16split"),
+         DL=[1] * 3, dtype="f32", add=True, path="tc3d_tf32x3"),
     dict(nd=3, N=2, C_in=64, C_out=32, G=1, L=[2, 3, 4], K=[4] * 3, S=[2] * 3, P=[1] * 3, OP=[0] * 3,
-         DL=[1] * 3, dtype="f32", add=False, path="tc3d_bf16split"),
+         DL=[1] * 3, dtype="f32", add=False, path="tc3d_tf32x3"),
     dict(nd=2, N=2, C_in=32, C_out=48, G=1, L=[7, 64], K=[3, 3], S=[2, 2], P=[1, 1], OP=[1, 1],
-         DL=[1, 1], dtype="f32", add=False, path="tc3d_bf16split"),
+         DL=[1, 1], dtype="f32", add=False, path="tc3d_tf32x3"),
     dict(nd=2, N=1, C_in=32, C_out=16, G=1, L=[3, 4], K=[2, 3], S=[2, 2], P=[0, 1], OP=[1, 1],
-         DL=[1, 1], dtype="f32", add=True, path="tc3d_bf16split"),
+         DL=[1, 1], dtype="f32", add=True, path="tc3d_tf32x3"),
     dict(nd=3, N=2, C_in=6, C_out=4, G=2, L=[3, 4, 5], K=[2, 3, 4], S=[3, 1, 2], P=[1, 0, 2], OP=[2, 0, 1],
          DL=[1, 2, 1], dtype="f32", add=False, path="gather_generic"),
     dict(nd=2, N=2, C_in=8, C_out=8, G=4, L=[4, 6], K=[3, 3], S=[2, 2], P=[1, 1], OP=[1, 1], DL=[1, 1],
@@ -623,4 +667,23 @@ def test_bounded_wait_timeout_reports_and_recovers():
     t = cc.make_inputs(c, seed=880)
     y = cc.run_gpu(c, t).cpu().numpy()
     cc.assert_close(y, cc.run_oracle(c, t), "f32", "after a reported timeout")
+    assert ct.ct_last_device_error_code(s) == ct.CT_OK
+
+
+def test_timeout_is_reported_by_the_next_forward_call():
+    """A timeout recorded by one launch is returned by the next forward call
+    (before it launches anything), once; the call after that runs normally."""
+    import torch
+    import transposed_convolution_convtranspose_gb300 as ct
+    s = torch.cuda.current_stream()
+    assert ct.ct_last_device_error_code(s) == ct.CT_OK
+    c = dict(nd=3, G=1, S=[2, 2, 2], DL=[1, 1, 1], bias=True, add=False, dtype="f32", **TC3D[1])
+    t = cc.make_inputs(c, seed=890)
+    ct.ct_selftest_wait_timeout(1_000_000, s)                  # 1 ms limit, nothing arrives
+    torch.cuda.synchronize()                                   # the kernel has written the word
+    with pytest.raises(ct.CTError) as ei:
+        cc.run_gpu(c, t)
+    assert ei.value.code == ct.CT_ERR_DEVICE_TIMEOUT
+    y = cc.run_gpu(c, t).cpu().numpy()                         # reported once: this call runs
+    cc.assert_close(y, cc.run_oracle(c, t), "f32", "after a timeout reported by a forward call")
     assert ct.ct_last_device_error_code(s) == ct.CT_OK

@@ -86,3 +86,22 @@ def test_rejects_invalid(lib):
         ora.conv_transpose(np.ones((1, 3, 4)), np.ones((3, 1, 3)), groups=2, lib=lib)
     with pytest.raises(ValueError):   # L_out <= 0
         ora.conv_transpose(np.ones((1, 1, 1)), np.ones((1, 1, 1)), padding=1, lib=lib)
+
+
+def test_all_cores_baseline_matches_oracle():
+    """The all-cores baseline (ct_oracle_mt.c) computes the same definition as
+    the parity oracle, split by output slice: equal up to summation order on
+    random small cases of every dimensionality, with groups, on 1, 3 and 8
+    threads."""
+    rng = np.random.default_rng(23)
+    for t in range(24):
+        nd = 1 + t % 3
+        c = pins.random_case(rng, nd)
+        x = rng.standard_normal([c["N"], c["C_in"]] + c["L"])
+        w = rng.standard_normal([c["C_in"], c["C_out"] // c["G"]] + c["K"])
+        b = rng.standard_normal(c["C_out"]) if t % 2 else None
+        kw = dict(stride=c["S"], padding=c["P"], output_padding=c["OP"], dilation=c["DL"], groups=c["G"])
+        ref = ora.conv_transpose(x, w, b, **kw)
+        got = ora.conv_transpose_mt(x, w, b, threads=(1, 3, 8)[t % 3], **kw)
+        assert got.shape == ref.shape
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-12), (t, c)

@@ -1,10 +1,14 @@
 """GPU test of ct_forward_3d_noalloc, the entry point for callers that cannot
 allocate device memory (for instance an engine that reserves all device
-memory at start-up and forbids allocation afterwards).  It runs the bf16
-tensor-core ConvTranspose3d with the library's own fixed scratch buffer
-instead of a caller-supplied workspace; its output must match the regular
-ct_forward_3d (which gets a workspace) on two calls in a row with different
-inputs, so that leftovers from the first call cannot leak into the second.
+memory at start-up and forbids allocation afterwards, or a plugin inside a
+framework that owns the device memory pool).  It runs the bf16 tensor-core
+ConvTranspose3d with the library's own fixed scratch buffer instead of a
+caller-supplied workspace.  On two calls in a row with different inputs (so
+that leftovers of the first call cannot hide in the second) its output must
+be bit for bit the output of the regular ct_forward_3d -- the same kernels on
+the same bits, so any difference is a scratch-offset mistake -- and must match
+the CPU oracle: within the bf16 tolerance for random inputs, exactly for
+small integers.
 
 The file name makes pytest collect it last."""
 import numpy as np
@@ -37,13 +41,15 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
     import torch
     ct = lib
     name = "convT3d_bf16_dense"
+    # the bf16 workload's layer on 8^3 inputs, batch 2 (the oracle finishes in seconds)
     c = cc.case_from_config(name, N=2)
+    c["L"] = [8, 8, 8]
     N, C_in, C_out, L, K, G, S, P, OP, DL = _args(c)
     assert ct.ct_path_3d(N, C_in, C_out, L, K, G, S, P, OP, DL, ct.CT_BF16) == "umma_bf16"
     out_shape = cc.out_shape(c)
     stream = torch.cuda.current_stream()
-    for call, seed in enumerate((901, 902)):
-        t = cc.make_inputs(c, seed=seed, bound=workloads.CONFIGS[name]["bound"])
+    for call, (seed, int_range) in enumerate(((901, None), (902, 3))):
+        t = cc.make_inputs(c, seed=seed, bound=workloads.CONFIGS[name]["bound"], int_range=int_range)
         x, w, b, _ = cc.to_device(t, c, "cuda:0")
         # the regular entry point, with a workspace
         nb = ct.ct_workspace_size_3d(N, C_in, C_out, L, K, G, S, P, OP, DL, ct.CT_BF16)
@@ -57,9 +63,14 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
         ct.ct_forward_3d_noalloc(x, w, b, y, N, C_in, C_out, L, K, G, S, P, OP, DL, ct.CT_BF16,
                                  stream)
         torch.cuda.synchronize()
-        ct.ct_last_device_error(stream)
-        cc.assert_close(y.cpu().numpy(), y_ref.cpu().numpy().astype(np.float64), "bf16",
-                        "no-alloc call %d vs ct_forward_3d" % (call + 1))
+        assert ct.ct_last_device_error_code(stream) == ct.CT_OK
+        assert torch.equal(y, y_ref), "no-alloc call %d differs from ct_forward_3d" % (call + 1)
+        ref = cc.run_oracle(c, t)
+        got = y.cpu().numpy()
+        if int_range is None:
+            cc.assert_close(got, ref, "bf16", "no-alloc call %d vs oracle" % (call + 1))
+        else:
+            assert np.array_equal(got.astype(np.float64), ref), "no-alloc integer call %d not exact" % (call + 1)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):

@@ -6,7 +6,9 @@ may be given as an int or as a torch tensor, whose ``data_ptr()`` is used) and
 raise :class:`CTError` on a non-zero status.  Every step of the computation
 runs in the library's CUDA kernels.  The ``conv_transpose*`` helpers allocate
 the fp32 output (and the workspace, if the chosen path needs one) with torch
-and call the corresponding entry point on torch's current stream.
+and call the corresponding entry point on torch's current stream; with
+``split2=True`` an fp32 call passes ``CT_F32_BF16X2`` (the opt-in two-term bf16
+split of the FP32 tensor-core paths) instead of ``CT_F32``.
 
 There is no fallback: if ``libct.so`` has not been built, every call raises.
 Build it with ``python -m transposed_convolution_convtranspose_gb300.build``.
@@ -19,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libct.so")
 
 CT_F32 = 0
 CT_BF16 = 1
+CT_F32_BF16X2 = 2   # fp32 x and w; opt-in two-term bf16 split on the FP32 tensor-core paths
 
 CT_OK, CT_ERR_ARG, CT_ERR_SHAPE, CT_ERR_ALIGN = 0, 1, 2, 3
 CT_ERR_WORKSPACE, CT_ERR_UNSUPPORTED, CT_ERR_CUDA, CT_ERR_DEVICE_TIMEOUT = 4, 5, 6, 7
@@ -29,7 +32,7 @@ CT_STATUS = {0: "CT_OK", 1: "CT_ERR_ARG", 2: "CT_ERR_SHAPE", 3: "CT_ERR_ALIGN",
 EXPORTED = ["ct_out_len", "ct_workspace_size_1d", "ct_workspace_size_2d", "ct_workspace_size_3d",
             "ct_forward_1d", "ct_forward_2d", "ct_forward_2d_add_hswish", "ct_forward_3d",
             "ct_forward_3d_add_hswish", "ct_path_1d", "ct_path_2d", "ct_path_3d",
-            "ct_workspace_size_cl", "ct_forward_cl", "ct_path_cl",
+            "ct_workspace_size_cl", "ct_forward_cl", "ct_path_cl", "ct_path_call",
             "ct_set_path_override", "ct_status_str", "ct_last_device_error",
             "ct_forward_3d_noalloc", "ct_selftest_wait_timeout"]
 
@@ -82,6 +85,8 @@ def _setup(lib):
                                   _I, _P, ctypes.c_size_t, _P]
     lib.ct_path_cl.restype = ctypes.c_char_p
     lib.ct_path_cl.argtypes = [_I, _I, _I, _I, _IP, _IP, _I, _IP, _IP, _IP, _IP, _I, _I]
+    lib.ct_path_call.restype = ctypes.c_char_p
+    lib.ct_path_call.argtypes = [_I, _I, _I, _I, _I, _IP, _IP, _I, _IP, _IP, _IP, _IP, _I, _I, ctypes.c_size_t]
     lib.ct_forward_1d.restype = _I
     lib.ct_forward_1d.argtypes = [_P, _P, _P, _P] + [_I] * 10 + [_I, _P, ctypes.c_size_t, _P]
     lib.ct_forward_3d.restype = _I
@@ -293,6 +298,17 @@ def ct_path_cl(nd, N, C_in, C_out, in_size, k, groups, stride, padding, output_p
     return None if r is None else r.decode()
 
 
+def ct_path_call(nd, channels_last, N, C_in, C_out, in_size, k, groups, stride, padding, output_padding,
+                 dilation, dtype, fused, ws_bytes):
+    """Kernel family a forward call with exactly ws_bytes of workspace launches
+    (None if the arguments are invalid or the call would fail with
+    CT_ERR_WORKSPACE)."""
+    r = load().ct_path_call(nd, int(bool(channels_last)), N, C_in, C_out, _ivec(in_size), _ivec(k), groups,
+                            _ivec(stride), _ivec(padding), _ivec(output_padding), _ivec(dilation), dtype,
+                            int(bool(fused)), int(ws_bytes))
+    return r.decode() if r is not None else None
+
+
 def ct_path_2d(N, C_in, C_out, in_hw, k_hw, groups, stride, padding, output_padding, dilation,
                dtype, fused=False):
     r = load().ct_path_2d(N, C_in, C_out, _i2(in_hw), _i2(k_hw), groups, _i2(stride),
@@ -346,10 +362,10 @@ def _need(t, name):
         raise CTError(1, "%s must be a contiguous CUDA tensor" % name)
 
 
-def _dtype_code(t):
+def _dtype_code(t, split2=False):
     import torch
     if t.dtype == torch.float32:
-        return CT_F32
+        return CT_F32_BF16X2 if split2 else CT_F32
     if t.dtype == torch.bfloat16:
         return CT_BF16
     raise TypeError("x and w must be float32 or bfloat16, got %s" % t.dtype)
@@ -364,14 +380,14 @@ def _workspace(nbytes, device):
 
 
 def conv_transpose1d(x, w, bias=None, stride=1, padding=0, output_padding=0, dilation=1,
-                     groups=1, out=None):
+                     groups=1, out=None, split2=False):
     import torch
     for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (out, "out")):
         _need(t, nm)
     N, C_in, L_in = x.shape
     k = w.shape[2]
     C_out = w.shape[1] * groups
-    dt = _dtype_code(x)
+    dt = _dtype_code(x, split2)
     L_out = ct_out_len(L_in, k, stride, padding, output_padding, dilation)
     if L_out < 1:
         raise CTError(2, "conv_transpose1d")
@@ -396,13 +412,13 @@ def _out3(x, w, groups, stride, padding, output_padding, dilation):
 
 
 def conv_transpose3d(x, w, bias=None, stride=1, padding=0, output_padding=0, dilation=1,
-                     groups=1, out=None):
+                     groups=1, out=None, split2=False):
     import torch
     for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (out, "out")):
         _need(t, nm)
     N, C_in = x.shape[:2]
     C_out = w.shape[1] * groups
-    dt = _dtype_code(x)
+    dt = _dtype_code(x, split2)
     S, P, OP, D, K, L, Lo = _out3(x, w, groups, stride, padding, output_padding, dilation)
     y = out if out is not None else torch.empty((N, C_out) + Lo, dtype=torch.float32,
                                                 device=x.device)
@@ -414,13 +430,13 @@ def conv_transpose3d(x, w, bias=None, stride=1, padding=0, output_padding=0, dil
 
 
 def conv_transpose3d_add_hswish(x, w, bias, add, stride=1, padding=0, output_padding=0,
-                                dilation=1, groups=1, out=None):
+                                dilation=1, groups=1, out=None, split2=False):
     import torch
     for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (add, "add"), (out, "out")):
         _need(t, nm)
     N, C_in = x.shape[:2]
     C_out = w.shape[1] * groups
-    dt = _dtype_code(x)
+    dt = _dtype_code(x, split2)
     S, P, OP, D, K, L, Lo = _out3(x, w, groups, stride, padding, output_padding, dilation)
     if tuple(add.shape) != (N, C_out) + Lo or add.dtype != torch.float32:
         raise CTError(1, "conv_transpose3d_add_hswish: add must be fp32 with the output's shape")
@@ -452,13 +468,13 @@ def _out2(x, w, stride, padding, output_padding, dilation):
 
 
 def conv_transpose2d(x, w, bias=None, stride=1, padding=0, output_padding=0, dilation=1,
-                     groups=1, out=None):
+                     groups=1, out=None, split2=False):
     import torch
     for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (out, "out")):
         _need(t, nm)
     N, C_in = x.shape[:2]
     C_out = w.shape[1] * groups
-    dt = _dtype_code(x)
+    dt = _dtype_code(x, split2)
     S, P, OP, D, K, L, Lo = _out2(x, w, stride, padding, output_padding, dilation)
     y = out if out is not None else torch.empty((N, C_out) + Lo, dtype=torch.float32,
                                                 device=x.device)
@@ -470,13 +486,13 @@ def conv_transpose2d(x, w, bias=None, stride=1, padding=0, output_padding=0, dil
 
 
 def conv_transpose2d_add_hswish(x, w, bias, add, stride=1, padding=0, output_padding=0,
-                                dilation=1, groups=1, out=None):
+                                dilation=1, groups=1, out=None, split2=False):
     import torch
     for t, nm in ((x, "x"), (w, "w"), (bias, "bias"), (add, "add"), (out, "out")):
         _need(t, nm)
     N, C_in = x.shape[:2]
     C_out = w.shape[1] * groups
-    dt = _dtype_code(x)
+    dt = _dtype_code(x, split2)
     S, P, OP, D, K, L, Lo = _out2(x, w, stride, padding, output_padding, dilation)
     if tuple(add.shape) != (N, C_out) + Lo or add.dtype != torch.float32:
         raise CTError(1, "conv_transpose2d_add_hswish: add must be fp32 with the output's shape")
@@ -489,7 +505,7 @@ def conv_transpose2d_add_hswish(x, w, bias, add, stride=1, padding=0, output_pad
 
 
 def conv_transpose_cl(x, w, bias=None, add=None, stride=1, padding=0, output_padding=0, dilation=1,
-                      groups=1, out=None):
+                      groups=1, out=None, split2=False):
     """Transposed convolution of a channels-last x (N, spatial..., C_in), 1 to 3
     spatial dimensions; returns y (N, spatial out..., C_out) fp32.  With add
     (channels-last, y's shape) the fused add + t*hardswish(t) epilogue."""
@@ -510,7 +526,7 @@ def conv_transpose_cl(x, w, bias=None, add=None, stride=1, padding=0, output_pad
     L = tuple(x.shape[1:-1])
     K = tuple(w.shape[2:])
     C_out = w.shape[1] * groups
-    dt = _dtype_code(x)
+    dt = _dtype_code(x, split2)
     Lo = tuple(ct_out_len(L[i], K[i], S[i], P[i], OP[i], D[i]) for i in range(nd))
     if min(Lo) < 1:
         raise CTError(2, "conv_transpose_cl")

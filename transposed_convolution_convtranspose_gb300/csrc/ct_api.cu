@@ -4,25 +4,55 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "ct_internal.h"
+#include "ct_introspect.h"
 
 namespace ct {
 
-__device__ unsigned int g_ct_status;   // CT_OK or CT_ERR_DEVICE_TIMEOUT
+namespace {
+// The status word (element 0: CT_OK or CT_ERR_DEVICE_TIMEOUT) lives in static
+// host memory that is page-locked and mapped into the devices' address space
+// (cudaHostRegister, on first use): a kernel whose bounded wait runs out
+// writes the timeout there, and the host reads it without synchronising --
+// every forward call checks it before launching, ct_last_device_error after
+// synchronising.  A whole 64 KB page of its own, so that registering it pins
+// nothing else of the library on hosts with pages of up to 64 KB.
+alignas(65536) unsigned int g_status_page[65536 / sizeof(unsigned int)];
+std::mutex g_status_mu;
+}  // namespace
 
 unsigned int *device_status_ptr()
 {
-    static unsigned int *cache[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_ct_status) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<unsigned int *>(p);
+    // Looked up on every launch, under a lock: the registration and the device
+    // address belong to the current context, which a cudaDeviceReset (or a
+    // caller's own context) replaces; a page found unregistered is registered
+    // again.
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, g_status_page);
+    if (e != cudaSuccess || at.type == cudaMemoryTypeUnregistered || !at.devicePointer) {
+        (void)cudaGetLastError();
+        e = cudaHostRegister(g_status_page, sizeof(g_status_page), cudaHostRegisterMapped | cudaHostRegisterPortable);
+        if (e != cudaSuccess && e != cudaErrorHostMemoryAlreadyRegistered) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        (void)cudaGetLastError();
+        if (cudaPointerGetAttributes(&at, g_status_page) != cudaSuccess || !at.devicePointer) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
     }
-    return cache[dev];
+    return static_cast<unsigned int *>(at.devicePointer);
+}
+
+// Take (read and clear) a timeout recorded by an earlier launch.
+ct_status take_device_status()
+{
+    const unsigned int v = __atomic_exchange_n(&g_status_page[0], 0u, __ATOMIC_ACQ_REL);
+    return v != 0 ? CT_ERR_DEVICE_TIMEOUT : CT_OK;
 }
 
 // Output length of one dimension ([l1_p79] output-length formula).
@@ -67,13 +97,17 @@ ct_status make_problem(int nd, int N, int C_in, int C_out, const int *Li, const 
                        bool has_bias, bool has_add, Problem *pb)
 {
     if (nd < 1 || nd > 3) return CT_ERR_ARG;
-    if (dtype != CT_F32 && dtype != CT_BF16) return CT_ERR_ARG;
+    if (dtype != CT_F32 && dtype != CT_BF16 && dtype != CT_F32_BF16X2) return CT_ERR_ARG;
+    // CT_F32_BF16X2 stores x and w as fp32 like CT_F32; only the split the FP32
+    // tensor-core kernels use differs
+    const bool split2 = dtype == CT_F32_BF16X2;
+    if (split2) dtype = CT_F32;
     if (N < 0 || C_in < 1 || C_out < 1 || G < 1) return CT_ERR_ARG;
     if (C_in % G || C_out % G) return CT_ERR_SHAPE;
     Problem p;
     p.nd = nd; p.N = N; p.C_in = C_in; p.C_out = C_out; p.G = G;
     p.Cig = C_in / G; p.Cog = C_out / G;
-    p.dtype = dtype; p.has_bias = has_bias; p.has_add = has_add;
+    p.dtype = dtype; p.split2 = split2; p.has_bias = has_bias; p.has_add = has_add;
     for (int d = 0; d < 3; ++d) {
         p.Li[d] = 1; p.K[d] = 1; p.S[d] = 1; p.P[d] = 0; p.OP[d] = 0; p.DL[d] = 1; p.Lo[d] = 1;
     }
@@ -132,7 +166,7 @@ Path choose_path(const Problem &pb, const Args *a)
     return Path::Generic;
 }
 
-const char *path_name(Path p)
+const char *path_name(Path p, const Problem &pb)
 {
     switch (p) {
     case Path::Generic: return "gather_generic";
@@ -140,8 +174,8 @@ const char *path_name(Path p)
     case Path::Phase3d: return "phase3d_f32";
     case Path::Umma: return "umma_bf16";
     case Path::Tc1d: return "tc1d_tf32x3";
-    case Path::Tc3d: return "tc3d_bf16split";
-    case Path::Tc3dg: return "tc3dg_bf16split";
+    case Path::Tc3d: return pb.split2 ? "tc3d_bf16x2" : "tc3d_tf32x3";
+    case Path::Tc3dg: return pb.split2 ? "tc3dg_bf16x2" : "tc3dg_tf32x3";
     }
     return "gather_generic";
 }
@@ -182,11 +216,22 @@ ct_status run(const Problem &pb, Args a)
         return CT_ERR_ARG;
     if (a.add && a.add != a.y && overlaps(a.y, yb, a.add, yb)) return CT_ERR_ARG;
 
+    // A workspace is either absent (NULL or 0 bytes: then the kernels that need
+    // none run) or at least as large as ct_workspace_size_* reports for these
+    // arguments, and 256-byte aligned; anything in between is an error rather
+    // than a silent change of kernel.
+    if (!a.ws && a.ws_bytes != 0) return CT_ERR_WORKSPACE;
+    if (a.ws_bytes == 0) a.ws = nullptr;
+    if (a.ws && (!aligned(a.ws, 256) || a.ws_bytes < workspace_bytes(pb))) return CT_ERR_WORKSPACE;
     const Path path = choose_path(pb, &a);
     if (path == Path::Umma) {
         const size_t need = umma_workspace_bytes(pb);
         if (a.ws_bytes < need || !a.ws || !aligned(a.ws, 256)) return CT_ERR_WORKSPACE;
     }
+    // a bounded wait of an earlier launch that ran out is reported here, before
+    // this call launches anything
+    const ct_status pending = take_device_status();
+    if (pending != CT_OK) return pending;
     cudaError_t e = cudaSuccess;
     switch (path) {
     case Path::Generic: e = launch_gather_generic(pb, a); break;
@@ -357,7 +402,7 @@ const char *ct_path_1d(int N, int C_in, int C_out, int L_in, int k, int groups, 
     if (make_problem(1, N, C_in, C_out, &L_in, &k, groups, &stride, &padding, &output_padding,
                      &dilation, dtype, false, false, &pb) != CT_OK)
         return nullptr;
-    return path_name(choose_path(pb, nullptr));
+    return path_name(choose_path(pb, nullptr), pb);
 }
 
 const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const int k_dhw[3],
@@ -370,7 +415,7 @@ const char *ct_path_3d(int N, int C_in, int C_out, const int in_dhw[3], const in
     if (make_problem(3, N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding, output_padding,
                      dilation, dtype, false, fused != 0, &pb) != CT_OK)
         return nullptr;
-    return path_name(choose_path(pb, nullptr));
+    return path_name(choose_path(pb, nullptr), pb);
 }
 
 ct_status ct_workspace_size_cl(int nd, int N, int C_in, int C_out, const int *in_size, const int *k,
@@ -414,7 +459,7 @@ const char *ct_path_cl(int nd, int N, int C_in, int C_out, const int *in_size, c
                      dtype, false, fused != 0, &pb) != CT_OK)
         return nullptr;
     pb.cl = true;
-    return path_name(choose_path(pb, nullptr));
+    return path_name(choose_path(pb, nullptr), pb);
 }
 
 const char *ct_path_2d(int N, int C_in, int C_out, const int in_hw[2], const int k_hw[2],
@@ -427,7 +472,28 @@ const char *ct_path_2d(int N, int C_in, int C_out, const int in_hw[2], const int
     if (make_problem(2, N, C_in, C_out, in_hw, k_hw, groups, stride, padding, output_padding,
                      dilation, dtype, false, fused != 0, &pb) != CT_OK)
         return nullptr;
-    return path_name(choose_path(pb, nullptr));
+    return path_name(choose_path(pb, nullptr), pb);
+}
+
+const char *ct_path_call(int nd, int channels_last, int N, int C_in, int C_out, const int *in_size, const int *k,
+                         int groups, const int *stride, const int *padding, const int *output_padding,
+                         const int *dilation, ct_dtype dtype, int fused, size_t ws_bytes)
+{
+    if (!in_size || !k || !stride || !padding || !output_padding || !dilation) return nullptr;
+    Problem pb;
+    if (make_problem(nd, N, C_in, C_out, in_size, k, groups, stride, padding, output_padding, dilation, dtype,
+                     false, fused != 0, &pb) != CT_OK)
+        return nullptr;
+    pb.cl = channels_last != 0;
+    if (ws_bytes > 0 && ws_bytes < workspace_bytes(pb)) return nullptr;     // the call returns CT_ERR_WORKSPACE
+    // 256-byte aligned stand-ins for the tensors (never dereferenced: the path
+    // checks look at alignment only)
+    void *const any = reinterpret_cast<void *>((uintptr_t)1 << 20);
+    Args a{any, any, nullptr, fused ? static_cast<const float *>(any) : nullptr, static_cast<float *>(any),
+           ws_bytes ? any : nullptr, ws_bytes, nullptr};
+    const Path path = choose_path(pb, &a);
+    if (path == Path::Umma && ws_bytes < umma_workspace_bytes(pb)) return nullptr;
+    return path_name(path, pb);
 }
 
 void ct_set_path_override(int mode) { g_override.store(mode == 1 || mode == 2 ? mode : 0); }
@@ -450,14 +516,7 @@ const char *ct_status_str(ct_status s)
 ct_status ct_last_device_error(void *stream)
 {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CT_ERR_CUDA;
-    unsigned int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_ct_status, sizeof(v)) != cudaSuccess) return CT_ERR_CUDA;
-    if (v != 0) {
-        const unsigned int zero = 0;
-        if (cudaMemcpyToSymbol(g_ct_status, &zero, sizeof(zero)) != cudaSuccess) return CT_ERR_CUDA;
-        return CT_ERR_DEVICE_TIMEOUT;
-    }
-    return CT_OK;
+    return take_device_status();
 }
 
 }  // extern "C"

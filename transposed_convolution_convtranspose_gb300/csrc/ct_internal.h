@@ -15,7 +15,8 @@ struct Problem {
     int nd;                                  // 1, 2 or 3 (as called; dims right-aligned in 3 slots)
     int N, C_in, C_out, G, Cig, Cog;         // Cig = C_in/G, Cog = C_out/G
     int Li[3], K[3], S[3], P[3], OP[3], DL[3], Lo[3];
-    ct_dtype dtype;
+    ct_dtype dtype;                          // storage type of x and w: CT_F32 or CT_BF16
+    bool split2 = false;                     // CT_F32_BF16X2: fp32 storage, two-term bf16 split opted into
     bool has_bias, has_add;
     bool cl = false;                         // channels-last x, y, add: (N, spatial..., C)
 
@@ -70,13 +71,15 @@ cudaError_t launch_gather_generic(const Problem &pb, const Args &a);
 bool tc1d_supported(const Problem &pb, const Args *a);
 cudaError_t launch_tc1d(const Problem &pb, const Args &a);
 
-// ---- FP32 3-D on the tensor cores (3-term tf32 split; workspace) ----
+// ---- FP32 3-D / 2-D on the tensor cores (3-term tf32 split, or the two-term
+// bf16 split when opted into; workspace) ----
 bool tc3d_supported(const Problem &pb, const Args *a);
 size_t tc3d_workspace_bytes(const Problem &pb);
 cudaError_t launch_tc3d(const Problem &pb, const Args &a);
 
 // ---- FP32 3-D, 32 input channels in 1/2/4 groups, on the tensor cores
-// (3-term tf32 split, one MMA-issuing warp per group; workspace) ----
+// (3-term tf32 split, or the two-term bf16 split when opted into; one
+// MMA-issuing warp per group; workspace) ----
 bool tc3dg_supported(const Problem &pb, const Args *a);
 size_t tc3dg_workspace_bytes(const Problem &pb);
 cudaError_t launch_tc3dg(const Problem &pb, const Args &a);

@@ -11,11 +11,13 @@
 // cudaFree or any other allocating routine.
 //
 // Host code must not use the array's name as a device pointer: in host code
-// it only stands for the symbol.  The device address is looked up once per
-// device with cudaGetSymbolAddress, with that device current, on the first
-// call made on that device, and cached.
-#include <mutex>
-
+// it only stands for the symbol.  The device address belongs to the context
+// that is current when it is looked up (the module is loaded per context),
+// so every call looks it up with cudaGetSymbolAddress, with the caller's
+// device and context current, and checks the result.  A cached address
+// could outlive its context (cudaDeviceReset, or a context the caller made
+// current); the lookup costs microseconds once the module is loaded.  The
+// first call on a device sets the module up there.
 #include "ct_internal.h"
 
 namespace ct {
@@ -26,27 +28,14 @@ static_assert(CT_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-b
 // The library-owned scratch of ct_forward_3d_noalloc (one per device).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[CT_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
-std::mutex g_scratch_mu;
-
-// Device address of the scratch array on the current device (set-up on the
-// first call per device).
+// Device address of the scratch array in the current context.
 cudaError_t scratch_address(void **out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        if (!p || ((uintptr_t)p % 256) != 0) return cudaErrorInvalidValue;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    if (!p || ((uintptr_t)p % 256) != 0) return cudaErrorInvalidValue;
+    *out = p;
     return cudaSuccess;
 }
 

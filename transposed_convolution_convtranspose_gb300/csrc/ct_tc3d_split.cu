@@ -1,7 +1,7 @@
 // ct_tc3d_split.cu -- FP32 ConvTranspose3d (and 2-D: a unit D dimension),
 // plain or with the fused add + t*hardswish(t) epilogue, on the tensor cores
-// (tcgen05 kind::f16 with bf16 operands) with a two-term split of every
-// operand that keeps the result within ~2^-16 of fp32 arithmetic.
+// (tcgen05), every operand split into parts whose products the tensor cores
+// form exactly.
 //
 // Method ([l1_p72] stride-phase classes: residue r of a dimension receives
 // the taps k with (r + p - k) even, reading input q + (r + p - k)/2;
@@ -12,46 +12,57 @@
 //                x[ic][qd+dd][qh+dh][qw+dw] * w[ic][oc][kd][kh][kw]
 // -- for 128 positions q a GEMM with M = 128, N = C_out, K = C_in per tap.
 //
-// Operands (caller's workspace, written by one prep launch):
-//   x (N, C_in, D, H, W) -> x_c (N, D, H, W, 2 C_in) bf16, channels-last
-//   w (C_in, C_out, kD, kH, kW) -> weight panels, K-major (C_in fastest)
-// Every value v is split as hi = bf16(v) (round to nearest even) and lo =
-// bf16(v - hi); the dropped remainder is below 2^-17 |v|.  Per K step of 8
-// input channels the A row holds [x_hi | x_lo] of the 8 (16 bf16 = 32
-// bytes), and two kind::f16 MMAs of K = 16 multiply it by [w_hi | w_hi] and
-// by [w_lo | w_lo]: together x_hi w_hi + x_lo w_hi + x_hi w_lo + x_lo w_lo =
-// (x_hi + x_lo)(w_hi + w_lo), every bf16 product exact in the fp32
-// accumulator, so a product carries a relative error of about 2^-16 at most.
+// Two splits, chosen by the caller:
+//  * tf32x3 (CT_F32, the default).  v = t + l with t = tf32(v) (cvt.rna) and
+//    l = tf32(v - t); v - t is exact in fp32, |v - t| <= 2^-11 |v| and
+//    |v - t - l| <= 2^-22 |v|.  Per K step of 8 channels three kind::tf32
+//    MMAs accumulate x_t w_t + x_t w_l + x_l w_t, every product exact in the
+//    fp32 accumulator; the dropped x_l w_l and the two remainders are each
+//    at most 2^-22 |x||w|, so an output lies within about 2^-20 of
+//    sum |x||w| of the exact sum -- the accuracy of fp32 arithmetic over the
+//    same terms.  An operand row holds 16 channels, [t of the 16 | l of the
+//    16] (128 bytes): the A stage of a K block is one 128-byte row per
+//    position and the B panel one row per output channel.
+//  * bf16x2 (CT_F32_BF16X2, opt-in).  hi = bf16(v) (round to nearest even),
+//    lo = bf16(v - hi); the dropped remainder is below 2^-17 |v|.  Per K step
+//    of 8 input channels the A row holds [x_hi | x_lo] of the 8 (16 bf16 =
+//    32 bytes), and two kind::f16 MMAs of K = 16 multiply it by [w_hi | w_hi]
+//    and by [w_lo | w_lo]: together (x_hi + x_lo)(w_hi + w_lo), so a product
+//    carries a relative error of about 2^-16 at most.  An A row holds 32
+//    channels; a run's panel is its hi rows, then its lo rows.
 //
 // Schedule.  A unit of work is 128 positions (whole W rows of MH H rows of
 // one D plane) and one D residue rD, with the four (rH, rW) phases as four
 // accumulators of C_out TMEM columns side by side (two such sets alternate
 // across units when they fit, so the epilogue of one unit overlaps the MMAs
 // of the next).  Every distinct input offset (dd, dh, dw) the unit reads is
-// one A tile; the phases that read it with some tap form runs of adjacent
-// accumulators, and the weights of a run are stored as one panel -- hi rows
-// of its phases, then lo rows -- so that one MMA with N = run length x C_out
-// serves the whole run.  An MMA instruction costs the issuing thread about
-// 100 clocks whatever its N, so wide runs are what keeps the tensor cores
-// busy; the issue loop carries ring slots and parities as counters.
+// one A tile per K block; the phases that read it with some tap form runs of
+// adjacent accumulators, and the weights of a run are stored as one panel, so
+// that one MMA with N = run length x C_out serves the whole run.  The host
+// orders the four accumulators so that the phases sharing an offset are
+// adjacent as often as possible (with a 3-tap kernel the order (0,0), (0,1),
+// (1,1), (1,0) makes every offset one run).  An MMA instruction costs the
+// issuing thread about 100 clocks whatever its N, so wide runs are what keeps
+// the tensor cores busy; the issue loop carries ring slots and parities as
+// counters.
 //
 // Roles (persistent CTA, one per SM):
-//   warp 0      TMA producer of the A ring (x_c 5-D boxes of 128 positions
+//   warps 0-1   TMA producers of the A ring (x_c 5-D boxes of 128 positions
 //               x 128 bytes of channels at the offset; boxes reaching outside
 //               the input read zeros, which is the boundary handling)
-//   warp 1      TMA producer of the B ring (a run's panel is one box).  Each
+//   warps 2-3   TMA producers of the B ring (a run's panel is one box).  Each
 //               ring slot has exactly one producer, which refills it only after
 //               waiting for its previous round, so a parity wait never has to
 //               tell two phases apart
-//   warp 2      TMEM allocation and MMA issue
-//   warps 3-18  epilogue, in chunks of 16 channels of a unit (16 channels x
+//   warp 4      TMEM allocation and MMA issue
+//   warps 5-20  epilogue, in chunks of 16 channels of a unit (16 channels x
 //               the unit's 2 MH output rows x the whole W extent, 32 KB): the
 //               add values arrive in one of three shared-memory buffers by a
 //               TMA load two chunks ahead; warp w reads TMEM lane quarter
 //               w mod 4 for one H phase and 8 channels, adds bias (and
 //               applies the fused epilogue) in place, writing each position's
 //               even and odd W outputs as one float2
-//   warp 19     chunk mover: makes chunks ready two ahead (the TMA load of the
+//   warp 21     chunk mover: makes chunks ready two ahead (the TMA load of the
 //               add values, or the release of the buffer) and stores each
 //               written chunk with one TMA store (rows and planes past the
 //               output are clipped)
@@ -71,26 +82,28 @@ namespace ct {
 namespace {
 
 constexpr int BM = 128;          // positions per unit (UMMA M)
-constexpr int CK = 32;           // fp32 K per stage: one 128-byte swizzle row
+constexpr int CKB = 32;          // bf16x2: input channels per K block (one 128-byte row of (hi, lo) pairs)
+constexpr int CKT = 16;          // tf32x3: input channels per K block (one 128-byte row [t x 16 | l x 16])
 constexpr int NA = 4;            // A stages (one producer warp; deep enough to cover DRAM latency)
 constexpr int NB = 2;            // B stages
 constexpr int NE = 3;            // epilogue chunk buffers (16 channels of a unit, 32 KB each)
-constexpr int NPB = 1;           // B producer warps: warp q loads the B stages g with g mod NPB == q
+constexpr int NPA = 2;           // A producer warps: warp q loads the A stages g with g mod NPA == q
+constexpr int NPB = 2;           // B producer warps: warp q loads the B stages g with g mod NPB == q
 constexpr int MAXE = 18;         // input offsets per D residue (2 x 3 x 3 for extents <= 4)
 constexpr int MAXR = 64;         // runs per D residue
 constexpr int MAXBLK = 128;      // C_out-row blocks of the weight panels (2 x taps)
 constexpr int EPW = 4;           // epilogue warps per TMEM lane quarter (H phase x channel half)
-constexpr int kAWarp = 0;
-constexpr int kBWarp0 = 1;
+constexpr int kAWarp0 = 0;
+constexpr int kBWarp0 = kAWarp0 + NPA;
 constexpr int kMmaWarp = kBWarp0 + NPB;
 constexpr int kEpiWarp0 = kMmaWarp + 1;
 constexpr int kStoreWarp = kEpiWarp0 + 4 * EPW;
 constexpr int kThreads = 32 * (kStoreWarp + 1);
-constexpr uint32_t kATile = BM * CK * 4;       // 128 positions x 32 channels x (hi, lo) bf16: 16 KB
+constexpr uint32_t kATile = BM * 128;          // 128 positions x one 128-byte row: 16 KB
 constexpr uint32_t kEChunk = 16 * 4 * BM * 4;  // 16 channels x 4 phases x 128 positions, fp32: 32 KB
 constexpr int kEpiThreads = 32 * 4 * EPW;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-static_assert(NB % NPB == 0, "one producer per B slot");
+static_assert(NB % NPB == 0 && NA % NPA == 0, "one producer per ring slot");
 
 // One input offset a unit reads; its runs are run[rd][run0 .. run0 + nrun).
 struct Entry {
@@ -110,32 +123,32 @@ struct T3Params {
     int SD;                      // D stride: 2, or 1 for a unit D dimension (a 2-D problem)
     int Lo0, Lo1, Lo2;
     int QD, QH, QW, MH, n_qhb;
-    int n_kb;                    // C_in / 32
+    int n_kb;                    // K blocks: C_in / 16 (tf32x3) or C_in / 32 (bf16x2)
+    int a_kstep;                 // A map coordinate of K block 1 (elements of x_c)
+    int bmul;                    // panel rows per accumulator column block: 1 (tf32x3) or 2 (bf16x2: hi, lo)
     int nunits;
     int nacc;                    // accumulator sets (1 or 2)
     uint32_t acc_cols;           // 4 x C_out
     uint32_t tmem_cols;
     uint32_t bslot;              // bytes of a B ring slot
-    uint32_t idesc_b[5];         // kind::f16 (bf16) instruction descriptor for N = len x C_out, len 1..4
+    uint32_t idesc_b[5];         // instruction descriptor for N = len x C_out, len 1..4
+    int8_t slot[4];              // accumulator slot of phase (rH, rW) = index 2 rH + rW
     int nE[2];
     Entry ent[2][MAXE];
     Run run[2][MAXR];
 };
 
-// Weight panel rows: block b (C_out rows) holds tap blk_tap[b]: its bf16 hi
-// parts (blk_lo 0) or its lo parts (blk_lo 1), each twice per K step.
+// Weight panel rows.  tf32x3: block b (C_out rows) holds tap blk_tap[b], each
+// row [t x 16 | l x 16] per K block.  bf16x2: block b holds tap blk_tap[b]:
+// its bf16 hi parts (blk_lo 0) or its lo parts (blk_lo 1), each twice per K
+// step.
 struct WPanels {
-    int C_in, C_out, ntap, nblk;
+    int C_in, C_out, ntap, nblk, tf;
     int8_t blk_tap[MAXBLK];
     int8_t blk_lo[MAXBLK];
 };
 
 // ---- prep kernels ------------------------------------------------------------
-// x (N, C, S) -> x_c (N, S, 2C) bf16 where, per 32 channels and K step of 8,
-// x_c holds [hi of the 8 | lo of the 8]; S = D*H*W a multiple of 4, C of 32.
-// Block = 32 channels x 64 positions: 16-byte loads of 4 positions of one
-// channel (a warp reads 2 x 256 contiguous bytes), a shared tile of pitch 33,
-// then per thread 4 channels of one position: two 8-byte stores.
 __device__ __forceinline__ float bf16_round(float v)
 {
     return __bfloat162float(__float2bfloat16_rn(v));
@@ -144,9 +157,54 @@ __device__ __forceinline__ uint32_t bf16_bits(float v)
 {
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
+// v rounded to tf32 (10 fraction bits, nearest, ties away from zero): the low
+// 13 bits of the result are zero, so the tensor cores read it exactly
+__device__ __forceinline__ float tf32_round(float v)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
+}
 
-__device__ __forceinline__ void prep_x_block(const float *__restrict__ x, uint16_t *__restrict__ xc, int C,
-                                             int64_t SP, int bx, int by, int n)
+// The split of 4 consecutive channels c .. c + 3 of one position, stored at
+// the channel's place in x_c.  tf32x3: row of 16 channels [t x 16 | l x 16],
+// 32 floats per 16 channels; bf16x2: per K step of 8 channels [hi x 8 | lo x
+// 8], 16 bf16 per 8 channels.  `pos` points at the position's x_c row (its
+// element 0) in 4-byte units; c is a multiple of 4.
+__device__ __forceinline__ void store_split4(uint32_t *pos, int c, const float (&v)[4], bool tf)
+{
+    if (tf) {
+        float t[4], l[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            t[i] = tf32_round(v[i]);
+            l[i] = tf32_round(v[i] - t[i]);       // v - t is exact in fp32
+        }
+        uint32_t *r = pos + (c >> 4) * 32 + (c & 15);
+        *reinterpret_cast<float4 *>(r) = make_float4(t[0], t[1], t[2], t[3]);
+        *reinterpret_cast<float4 *>(r + 16) = make_float4(l[0], l[1], l[2], l[3]);
+    } else {
+        uint32_t hb[4], lb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float h = bf16_round(v[i]);
+            hb[i] = bf16_bits(h);
+            lb[i] = bf16_bits(v[i] - h);          // v - h is exact in fp32
+        }
+        // K step c / 8 of the row (32 bytes = 8 words each), elements c mod 8 ..
+        uint16_t *r = reinterpret_cast<uint16_t *>(pos) + (c >> 3) * 16 + (c & 4);
+        *reinterpret_cast<uint2 *>(r) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+        *reinterpret_cast<uint2 *>(r + 8) = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+    }
+}
+
+// x (N, C, S) -> x_c (N, S, 2C x 4 bytes (tf32x3) or 2C x 2 bytes (bf16x2));
+// S = D*H*W a multiple of 4, C of 32.  Block = 32 channels x 64 positions:
+// 16-byte loads of 4 positions of one channel (a warp reads 2 x 256
+// contiguous bytes), a shared tile of pitch 33, then per thread 4 channels
+// of one position.
+__device__ __forceinline__ void prep_x_block(const float *__restrict__ x, uint32_t *__restrict__ xc, int C,
+                                             int64_t SP, int bx, int by, int n, bool tf)
 {
     __shared__ float tile[64][33];
     const int c0 = by * 32;
@@ -165,31 +223,25 @@ __device__ __forceinline__ void prep_x_block(const float *__restrict__ x, uint16
         tile[p4 * 4 + 3][c] = v.w;
     }
     __syncthreads();
-    const int64_t ob = ((int64_t)n * SP + s0) * C + c0;
+    // 4-byte words of x_c per position: 2C (tf32x3) or C (bf16x2)
+    const int64_t wpp = tf ? 2 * (int64_t)C : (int64_t)C;
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
         const int idx = threadIdx.x + 256 * it;
         const int q = idx & 7, pos = idx >> 3;
         if (pos < ncols) {
-            uint32_t hb[4], lb[4];
+            float v[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float v = tile[pos][4 * q + i];
-                const float h = bf16_round(v);
-                hb[i] = bf16_bits(h);
-                lb[i] = bf16_bits(v - h);       // v - h is exact in fp32
-            }
-            // channels 4q..4q+3 of this block: K step q / 2, elements 4 (q & 1) ..
-            uint16_t *cr = xc + 2 * (ob + (int64_t)pos * C) + (q >> 1) * 16 + (q & 1) * 4;
-            *reinterpret_cast<uint2 *>(cr) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
-            *reinterpret_cast<uint2 *>(cr + 8) = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+            for (int i = 0; i < 4; ++i) v[i] = tile[pos][4 * q + i];
+            store_split4(xc + ((int64_t)n * SP + s0 + pos) * wpp, c0 + 4 * q, v, tf);
         }
     }
 }
 
-// w (C_in, C_out, K0, K1, K2) -> weight panels [block][C_out][C_in x 4 bytes]:
-// block b holds tap blk_tap[b] as bf16 rows of [hi | hi] (blk_lo 0) or [lo |
-// lo] (blk_lo 1) per K step of 8 input channels.
+// w (C_in, C_out, K0, K1, K2) -> weight panels [block][C_out rows]: tf32x3
+// rows of [t x 16 | l x 16] per K block (8 bytes per input channel); bf16x2
+// rows of [hi | hi] (blk_lo 0) or [lo | lo] (blk_lo 1) per K step of 8 input
+// channels (4 bytes per input channel).
 __device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float *__restrict__ wp, const WPanels &q,
                                              int bw, int nbw)
 {
@@ -200,56 +252,54 @@ __device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float 
         const int64_t r = e % per;
         const int oc = (int)(r / q.C_in), ic = (int)(r % q.C_in);
         const float v = __ldg(w + ((int64_t)ic * q.C_out + oc) * q.ntap + q.blk_tap[b]);
-        const float h = bf16_round(v);
-        const uint16_t t = (uint16_t)bf16_bits(q.blk_lo[b] ? v - h : h);
-        // the row's bf16 view: K step ic / 8 of its 32-channel block
-        uint16_t *row = reinterpret_cast<uint16_t *>(wp + (e - ic));
-        const int kb = ic >> 5, kk = (ic & 31) >> 3, el = ic & 7;
-        row[kb * 64 + kk * 16 + el] = t;
-        row[kb * 64 + kk * 16 + 8 + el] = t;
+        if (q.tf) {
+            const float t = tf32_round(v);
+            float *row = wp + 2 * (e - ic);
+            row[(ic >> 4) * 32 + (ic & 15)] = t;
+            row[(ic >> 4) * 32 + 16 + (ic & 15)] = tf32_round(v - t);
+        } else {
+            const float h = bf16_round(v);
+            const uint16_t t = (uint16_t)bf16_bits(q.blk_lo[b] ? v - h : h);
+            // the row's bf16 view: K step ic / 8 of its 32-channel block
+            uint16_t *row = reinterpret_cast<uint16_t *>(wp + (e - ic));
+            const int kb = ic >> 5, kk = (ic & 31) >> 3, el = ic & 7;
+            row[kb * 64 + kk * 16 + el] = t;
+            row[kb * 64 + kk * 16 + 8 + el] = t;
+        }
     }
 }
 
-// Channels-last x (N, S, C) -> x_c (N, S, 2C): the same split, no transpose.
-// Block = 1024 consecutive values (256 threads x 4 channels: one 16-byte load
-// and two 8-byte stores each); C a multiple of 32, so 4 channels never cross a
-// position.
-__device__ __forceinline__ void prep_x_cl_block(const float *__restrict__ x, uint16_t *__restrict__ xc,
-                                                int64_t total, int bx)
+// Channels-last x (N, S, C) -> x_c: the same split, no transpose.  Block =
+// 1024 consecutive values (256 threads x 4 channels: one 16-byte load each);
+// C a multiple of 32, so 4 channels never cross a position.
+__device__ __forceinline__ void prep_x_cl_block(const float *__restrict__ x, uint32_t *__restrict__ xc, int C,
+                                                int64_t total, int bx, bool tf)
 {
     const int64_t e = ((int64_t)bx * 256 + threadIdx.x) * 4;    // first of 4 values
     if (e >= total) return;
-    const float4 v = __ldcs(reinterpret_cast<const float4 *>(x + e));
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-    uint32_t hb[4], lb[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float h = bf16_round(vv[i]);
-        hb[i] = bf16_bits(h);
-        lb[i] = bf16_bits(vv[i] - h);
-    }
-    // value e = (position, channel c): K step (c mod 32) / 8 of its 32-channel block
-    const int c = (int)(e & 31);
-    uint16_t *cr = xc + 2 * (e - c) + (c >> 3) * 16 + (c & 4);
-    *reinterpret_cast<uint2 *>(cr) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
-    *reinterpret_cast<uint2 *>(cr + 8) = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
+    const float4 v4 = __ldcs(reinterpret_cast<const float4 *>(x + e));
+    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+    const int c = (int)(e % C);
+    const int64_t pos = e / C;
+    store_split4(xc + pos * (tf ? 2 * (int64_t)C : (int64_t)C), c, v, tf);
 }
 
 // Both preps in one launch: blocks [0, nxb) move x (nbx x nby per image; or,
 // channels last, 1024 consecutive values each), the remaining nbw blocks build
 // the panels.  The GEMM kernel is launched as its programmatic dependent.
 __global__ void __launch_bounds__(256)
-prep_kernel(const float *__restrict__ x, uint16_t *__restrict__ xc, int C, int64_t SP,
+prep_kernel(const float *__restrict__ x, uint32_t *__restrict__ xc, int C, int64_t SP,
             int nbx, int nby, int nxb, const float *__restrict__ w, float *__restrict__ wp,
             const __grid_constant__ WPanels q, int nbw, int64_t cl_total)
 {
     dev::griddep_launch_dependents();
     const int b = (int)blockIdx.x;
+    const bool tf = q.tf != 0;
     if (b < nxb && cl_total > 0) {
-        prep_x_cl_block(x, xc, cl_total, b);
+        prep_x_cl_block(x, xc, C, cl_total, b, tf);
     } else if (b < nxb) {
         const int per = nbx * nby;
-        prep_x_block(x, xc, C, SP, (b % per) % nbx, (b % per) / nbx, b / per);
+        prep_x_block(x, xc, C, SP, (b % per) % nbx, (b % per) / nbx, b / per, tf);
     } else {
         prep_w_block(w, wp, q, b - nxb, nbw);
     }
@@ -282,7 +332,7 @@ __device__ __forceinline__ UnitCoord unit_coord(int u, const T3Params &p)
     return c;
 }
 
-template <bool ADD, bool CL>
+template <bool ADD, bool CL, bool TF>
 __global__ void __launch_bounds__(kThreads, 1)
 tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                  const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
@@ -340,12 +390,15 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         p.nunits > (int)blockIdx.x ? (p.nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int C_out = p.C_out, n_kb = p.n_kb;
 
-    if (warp == kAWarp || (warp >= kBWarp0 && warp < kBWarp0 + NPB)) {
-        // ---------------- TMA producers
+    if (warp < kBWarp0 + NPB) {
+        // ---------------- TMA producers.  One thread streams TMA boxes at about one
+        // per 400 ns however deep the ring, so each ring has several producers,
+        // warp q of a ring taking the stages g with g mod (producers) == q: the
+        // ring slots g mod nst of one producer are its own.
         if (lane == 0) {
-            const bool isA = warp == kAWarp;
-            const int q = isA ? 0 : warp - kBWarp0;
-            const int np = isA ? 1 : NPB;
+            const bool isA = warp < kBWarp0;
+            const int q = isA ? warp - kAWarp0 : warp - kBWarp0;
+            const int np = isA ? NPA : NPB;
             const int nst = isA ? NA : NB;
             uint64_t *fullb = isA ? a_full : b_full;
             uint64_t *emptyb = isA ? a_empty : b_empty;
@@ -361,7 +414,7 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                     for (int kb = 0; kb < n_kb && !failed; ++kb) {
                         const int nload = isA ? 1 : en.nrun;
                         for (int j = 0; j < nload; ++j) {
-                            if (isA || (g & (NPB - 1)) == q) {
+                            if (g % np == q) {
                                 if (g >= nst &&
                                     !dev::mbar_wait_bounded(&emptyb[s], round_par ^ 1u, kWaitLimitNs)) {
                                     failed = true;
@@ -369,15 +422,17 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                                 }
                                 if (isA) {
                                     dev::mbar_arrive_expect_tx(&fullb[s], kATile);
-                                    dev::tma_load_5d(sA + (size_t)s * kATile, &tmXc, &fullb[s], kb * 2 * CK, en.dw,
-                                                     qh0 + en.dh, u.qd + en.dd, u.n);
+                                    dev::tma_load_5d(sA + (size_t)s * kATile, &tmXc, &fullb[s], kb * p.a_kstep,
+                                                     en.dw, qh0 + en.dh, u.qd + en.dd, u.n);
                                 } else {
-                                    // the run's panel exactly: a box of 2 x len x C_out rows
+                                    // the run's panel exactly: a box of bmul x len x C_out rows of
+                                    // the K block's 128 bytes
                                     const Run &ru = p.run[u.rd][en.run0 + j];
                                     const CUtensorMap *tm = ru.len == 1 ? &tmW1 : ru.len == 2 ? &tmW2
                                                           : ru.len == 3 ? &tmW3 : &tmW4;
-                                    dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * ru.len * C_out) * 128u);
-                                    dev::tma_load_2d(sB + (size_t)s * p.bslot, tm, &fullb[s], kb * CK, ru.brow);
+                                    dev::mbar_arrive_expect_tx(&fullb[s],
+                                                               (uint32_t)(p.bmul * ru.len * C_out) * 128u);
+                                    dev::tma_load_2d(sB + (size_t)s * p.bslot, tm, &fullb[s], kb * 32, ru.brow);
                                 }
                                 last = g;
                             }
@@ -434,16 +489,28 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                             tc::fence_after();
                             const uint32_t bh = sBb + (uint32_t)sb * bslot;
                             const uint64_t dbh = tc::desc_sw128(bh);
-                            const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(ru.len * C_out) * 128u);
                             const uint32_t idb = p.idesc_b[ru.len];
                             const uint32_t dd = d + (uint32_t)(ru.p0 * C_out);
                             const uint32_t acc0 = (ru.fresh && kb == 0) ? 0u : 1u;
+                            if (TF) {
+                                // the 128-byte rows hold [t x 16 | l x 16]: K step kk (8
+                                // channels, 32 bytes) of the t parts at 32 kk bytes, of the
+                                // l parts 64 bytes further (descriptor units of 16 bytes)
 #pragma unroll
-                            for (int kk = 0; kk < CK / 8; ++kk) {
-                                // 32 bytes along K inside the swizzle atom: 16 bf16, the
-                                // hi and lo parts of 8 channels
-                                tc::mma_bf16(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x * w_hi
-                                tc::mma_bf16(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x * w_lo
+                                for (int kk = 0; kk < CKT / 8; ++kk) {
+                                    tc::mma_tf32(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x_t w_t
+                                    tc::mma_tf32(dd, da + 2 * kk, dbh + 4 + 2 * kk, idb, 1u);         // x_t w_l
+                                    tc::mma_tf32(dd, da + 4 + 2 * kk, dbh + 2 * kk, idb, 1u);         // x_l w_t
+                                }
+                            } else {
+                                const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(ru.len * C_out) * 128u);
+#pragma unroll
+                                for (int kk = 0; kk < CKB / 8; ++kk) {
+                                    // 32 bytes along K inside the swizzle atom: 16 bf16, the
+                                    // hi and lo parts of 8 channels
+                                    tc::mma_bf16(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x * w_hi
+                                    tc::mma_bf16(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x * w_lo
+                                }
                             }
                             tc::commit(&b_empty[sb]);
                             if (++sb == NB) {
@@ -549,8 +616,9 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                             ch * 8 * cstride;
                 float v0[8], v1[8];
                 if (ok) {
-                    tc::tmem_ld8(tbase + (uint32_t)((rh * 2) * C_out + c0), v0);
-                    tc::tmem_ld8(tbase + (uint32_t)((rh * 2 + 1) * C_out + c0), v1);
+                    // the accumulators of phases (rh, 0) and (rh, 1)
+                    tc::tmem_ld8(tbase + (uint32_t)(p.slot[rh * 2] * C_out + c0), v0);
+                    tc::tmem_ld8(tbase + (uint32_t)(p.slot[rh * 2 + 1] * C_out + c0), v1);
                 }
                 if (ok && !dev::mbar_wait_bounded(&e_full[b], (gc / NE) & 1, kWaitLimitNs)) {
                     atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
@@ -650,9 +718,94 @@ int dim_taps(int K, int P, int r, int *k_out, int *d_out)
     return n;
 }
 
+// Entries and runs of both D residues for one order of the accumulators
+// (phase_of_slot[s] = phase 2 rH + rW held in slot s).  Fills p.ent, p.run,
+// p.nE and the panel blocks of wq; *cost estimates the MMA-issue time of a
+// unit pair: per run and K block a B stage (~150 clocks of waits and a
+// commit) and its MMAs (~80 clocks each up to N = 128, the tensor-pipe time
+// beyond).
+bool plan_runs(const Problem &pb, int SD, const int (&nt)[3][2], const int (&tk)[3][2][4],
+               const int (&td)[3][2][4], const int (&uo)[3][4], const int (&nu)[3], const int *phase_of_slot,
+               int maxlen, int bmul, int mma_per_stage, T3Params *pp, WPanels *wq, double *cost)
+{
+    T3Params &p = *pp;
+    int nblk = 0;
+    double c = 0;
+    for (int rd = 0; rd < SD; ++rd) {
+        int ne = 0, nr = 0;
+        uint32_t init = 0;                        // accumulator slots written by earlier runs
+        for (int jd = 0; jd < nt[0][rd]; ++jd)
+            for (int ih = 0; ih < nu[1]; ++ih)
+                for (int iw = 0; iw < nu[2]; ++iw) {
+                    // phases reading offset (dd, dh, dw), with their taps
+                    int tap_ph[4] = {-1, -1, -1, -1};
+                    for (int rh = 0; rh < 2; ++rh)
+                        for (int jh = 0; jh < nt[1][rh]; ++jh) {
+                            if (td[1][rh][jh] != uo[1][ih]) continue;
+                            for (int rw = 0; rw < 2; ++rw)
+                                for (int jw = 0; jw < nt[2][rw]; ++jw) {
+                                    if (td[2][rw][jw] != uo[2][iw]) continue;
+                                    tap_ph[rh * 2 + rw] =
+                                        (tk[0][rd][jd] * pb.K[1] + tk[1][rh][jh]) * pb.K[2] + tk[2][rw][jw];
+                                }
+                        }
+                    int tap_of[4];
+                    for (int sl = 0; sl < 4; ++sl) tap_of[sl] = tap_ph[phase_of_slot[sl]];
+                    Entry en;
+                    memset(&en, 0, sizeof(en));
+                    en.dd = (int8_t)td[0][rd][jd];
+                    en.dh = (int8_t)uo[1][ih];
+                    en.dw = (int8_t)uo[2][iw];
+                    en.run0 = (int16_t)nr;
+                    int ph = 0;
+                    while (ph < 4) {
+                        if (tap_of[ph] < 0) {
+                            ++ph;
+                            continue;
+                        }
+                        // a run: adjacent slots with a tap here, the same written state,
+                        // at most maxlen long
+                        const bool st = (init >> ph) & 1u;
+                        int len = 1;
+                        while (ph + len < 4 && len < maxlen && tap_of[ph + len] >= 0 &&
+                               (((init >> (ph + len)) & 1u) != 0) == st)
+                            ++len;
+                        if (nr >= MAXR || nblk + bmul * len > MAXBLK) return false;
+                        Run ru;
+                        memset(&ru, 0, sizeof(ru));
+                        ru.p0 = (int8_t)ph;
+                        ru.len = (int8_t)len;
+                        ru.fresh = st ? 0 : 1;
+                        ru.brow = nblk * pb.C_out;
+                        for (int hl = 0; hl < bmul; ++hl)
+                            for (int i = 0; i < len; ++i) {
+                                wq->blk_tap[nblk] = (int8_t)tap_of[ph + i];
+                                wq->blk_lo[nblk] = (int8_t)hl;
+                                ++nblk;
+                            }
+                        for (int i = 0; i < len; ++i) init |= 1u << (ph + i);
+                        p.run[rd][nr++] = ru;
+                        ++en.nrun;
+                        const double n = (double)(len * pb.C_out);
+                        c += 150.0 + mma_per_stage * (n <= 128 ? 80.0 : 80.0 * n / 128.0);
+                        ph += len;
+                    }
+                    if (en.nrun == 0) continue;
+                    if (ne >= MAXE) return false;
+                    p.ent[rd][ne++] = en;
+                }
+        if (init != 0xFu) return false;           // every accumulator of the unit is written
+        p.nE[rd] = ne;
+    }
+    wq->nblk = nblk;
+    *cost = c;
+    return true;
+}
+
 bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
 {
     if ((pb.nd != 3 && pb.nd != 2) || pb.dtype != CT_F32 || pb.G != 1) return false;
+    const bool tf = !pb.split2;          // tf32x3 unless the caller opted into the bf16 pair
     // D has stride 2 like H and W, or is a unit dimension (extent 1, stride 1, no
     // padding: a 2-D problem, or a 3-D one that maps planes to planes), whose
     // single residue takes tap 0 at offset 0
@@ -660,7 +813,7 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     if (SD == 1 && (pb.K[0] != 1 || pb.P[0] != 0 || pb.OP[0] != 0)) return false;
     for (int d = SD == 1 ? 1 : 0; d < 3; ++d)
         if (pb.S[d] != 2 || pb.DL[d] != 1 || pb.K[d] < 2 || pb.K[d] > 4) return false;
-    if (pb.C_in % CK != 0 || pb.C_out % 16 != 0 || pb.C_out < 16 || pb.C_out > 128) return false;
+    if (pb.C_in % 32 != 0 || pb.C_out % 16 != 0 || pb.C_out < 16 || pb.C_out > 128) return false;
     // the epilogue moves whole output rows by TMA: 16-byte rows and bases
     if (pb.Lo[2] % 4 != 0 || pb.in_sp() % 4 != 0) return false;
     if (a && (((uintptr_t)a->x % 16) || ((uintptr_t)a->y % 16) || (a->add && ((uintptr_t)a->add % 16))))
@@ -676,7 +829,9 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     p.QD = (p.Lo0 + SD - 1) / SD;
     p.QH = (p.Lo1 + 1) / 2;
     p.n_qhb = (p.QH + p.MH - 1) / p.MH;
-    p.n_kb = pb.C_in / CK;
+    p.n_kb = pb.C_in / (tf ? CKT : CKB);
+    p.a_kstep = tf ? 32 : 2 * CKB;        // fp32 words (tf32x3) or bf16 elements (bf16x2) of x_c
+    p.bmul = tf ? 1 : 2;
     const int64_t units = (int64_t)pb.N * p.QD * p.n_qhb * SD;
     if (units > 0x7fffffff || units == 0) return false;
     p.nunits = (int)units;
@@ -706,92 +861,55 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
                 }
             }
     // runs of adjacent accumulators: at most 4 phases, N = len x C_out <= 256 and
-    // a panel of 2 x len x C_out rows <= 256 (one TMA box)
-    const int maxlen = 128 / pb.C_out < 4 ? 128 / pb.C_out : 4;
+    // a panel of bmul x len x C_out rows <= 256 (one TMA box)
+    const int ml = 256 / (p.bmul * pb.C_out);
+    const int maxlen = ml < 4 ? ml : 4;
+    // the order of the four accumulators with the cheapest MMA schedule (the
+    // first of equal ones, so the natural order when it is as good)
+    static const int kPerm[24][4] = {
+        {0, 1, 2, 3}, {0, 1, 3, 2}, {0, 2, 1, 3}, {0, 2, 3, 1}, {0, 3, 1, 2}, {0, 3, 2, 1},
+        {1, 0, 2, 3}, {1, 0, 3, 2}, {1, 2, 0, 3}, {1, 2, 3, 0}, {1, 3, 0, 2}, {1, 3, 2, 0},
+        {2, 0, 1, 3}, {2, 0, 3, 1}, {2, 1, 0, 3}, {2, 1, 3, 0}, {2, 3, 0, 1}, {2, 3, 1, 0},
+        {3, 0, 1, 2}, {3, 0, 2, 1}, {3, 1, 0, 2}, {3, 1, 2, 0}, {3, 2, 0, 1}, {3, 2, 1, 0}};
     WPanels wq;
-    memset(&wq, 0, sizeof(wq));
-    int nblk = 0;
-    for (int rd = 0; rd < SD; ++rd) {
-        int ne = 0, nr = 0;
-        uint32_t init = 0;                        // accumulators written by earlier runs
-        for (int jd = 0; jd < nt[0][rd]; ++jd)
-            for (int ih = 0; ih < nu[1]; ++ih)
-                for (int iw = 0; iw < nu[2]; ++iw) {
-                    // phases reading offset (dd, dh, dw), with their taps
-                    int tap_of[4] = {-1, -1, -1, -1};
-                    for (int rh = 0; rh < 2; ++rh)
-                        for (int jh = 0; jh < nt[1][rh]; ++jh) {
-                            if (td[1][rh][jh] != uo[1][ih]) continue;
-                            for (int rw = 0; rw < 2; ++rw)
-                                for (int jw = 0; jw < nt[2][rw]; ++jw) {
-                                    if (td[2][rw][jw] != uo[2][iw]) continue;
-                                    tap_of[rh * 2 + rw] =
-                                        (tk[0][rd][jd] * pb.K[1] + tk[1][rh][jh]) * pb.K[2] + tk[2][rw][jw];
-                                }
-                        }
-                    Entry en;
-                    memset(&en, 0, sizeof(en));
-                    en.dd = (int8_t)td[0][rd][jd];
-                    en.dh = (int8_t)uo[1][ih];
-                    en.dw = (int8_t)uo[2][iw];
-                    en.run0 = (int16_t)nr;
-                    int ph = 0;
-                    while (ph < 4) {
-                        if (tap_of[ph] < 0) {
-                            ++ph;
-                            continue;
-                        }
-                        // a run: adjacent phases with a tap here, the same written state,
-                        // at most maxlen long
-                        const bool st = (init >> ph) & 1u;
-                        int len = 1;
-                        while (ph + len < 4 && len < maxlen && tap_of[ph + len] >= 0 &&
-                               (((init >> (ph + len)) & 1u) != 0) == st)
-                            ++len;
-                        if (nr >= MAXR || nblk + 2 * len > MAXBLK) return false;
-                        Run ru;
-                        memset(&ru, 0, sizeof(ru));
-                        ru.p0 = (int8_t)ph;
-                        ru.len = (int8_t)len;
-                        ru.fresh = st ? 0 : 1;
-                        ru.brow = nblk * pb.C_out;
-                        for (int hl = 0; hl < 2; ++hl)
-                            for (int i = 0; i < len; ++i) {
-                                wq.blk_tap[nblk] = (int8_t)tap_of[ph + i];
-                                wq.blk_lo[nblk] = (int8_t)hl;
-                                ++nblk;
-                            }
-                        for (int i = 0; i < len; ++i) init |= 1u << (ph + i);
-                        p.run[rd][nr++] = ru;
-                        ++en.nrun;
-                        ph += len;
-                    }
-                    if (en.nrun == 0) continue;
-                    if (ne >= MAXE) return false;
-                    p.ent[rd][ne++] = en;
-                }
-        if (init != 0xFu) return false;           // every accumulator of the unit is written
-        p.nE[rd] = ne;
+    double best = 0;
+    int bi = -1;
+    for (int i = 0; i < 24; ++i) {
+        WPanels wt;
+        memset(&wt, 0, sizeof(wt));
+        double c = 0;
+        if (!plan_runs(pb, SD, nt, tk, td, uo, nu, kPerm[i], maxlen, p.bmul, tf ? 6 : 8, &p, &wt, &c)) continue;
+        if (bi < 0 || c < best - 1e-9) {
+            best = c;
+            bi = i;
+        }
     }
+    if (bi < 0) return false;
+    memset(&wq, 0, sizeof(wq));
+    double c = 0;
+    if (!plan_runs(pb, SD, nt, tk, td, uo, nu, kPerm[bi], maxlen, p.bmul, tf ? 6 : 8, &p, &wq, &c)) return false;
+    for (int sl = 0; sl < 4; ++sl) p.slot[kPerm[bi][sl]] = (int8_t)sl;
     wq.C_in = pb.C_in;
     wq.C_out = pb.C_out;
     wq.ntap = pb.kvol();
-    wq.nblk = nblk;
+    wq.tf = tf ? 1 : 0;
     for (int len = 1; len <= 4; ++len)
-        p.idesc_b[len] = len * pb.C_out <= 256 ? tc::idesc(1, len * pb.C_out, BM) : 0u;
+        p.idesc_b[len] = len * pb.C_out <= 256 ? tc::idesc(tf ? 2 : 1, len * pb.C_out, BM) : 0u;
     p.acc_cols = (uint32_t)(4 * pb.C_out);
     p.nacc = 8 * pb.C_out <= 512 ? 2 : 1;
     uint32_t cols = 32;
     while (cols < (uint32_t)p.nacc * p.acc_cols) cols <<= 1;
     p.tmem_cols = cols;
-    p.bslot = (uint32_t)(2 * maxlen * pb.C_out) * 128u;
+    p.bslot = (uint32_t)(p.bmul * maxlen * pb.C_out) * 128u;
     const size_t smem = (size_t)NA * kATile + (size_t)NB * p.bslot + (size_t)NE * kEChunk + 1024;
     if (smem > 227 * 1024 - 1024) return false;   // room for the static barriers
     out->p = p;
     out->wq = wq;
     out->maxlen = maxlen;
-    out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * 4);
-    out->w_bytes = align256((size_t)nblk * pb.C_out * pb.C_in * 4);
+    // x_c: 8 bytes per value (tf32 t and l) or 4 (bf16 hi and lo); panels the same per weight row entry
+    const size_t vb = tf ? 8 : 4;
+    out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * vb);
+    out->w_bytes = align256((size_t)wq.nblk * pb.C_out * pb.C_in * vb);
     out->smem = smem;
     return true;
 }
@@ -816,12 +934,13 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     T3Plan pl;
     if (!make_t3plan(pb, &a, &pl)) return cudaErrorNotSupported;
     const T3Params &p = pl.p;
+    const bool tf = pl.wq.tf != 0;
     uint8_t *ws = static_cast<uint8_t *>(a.ws);
-    uint16_t *xc = reinterpret_cast<uint16_t *>(ws);
+    uint32_t *xc = reinterpret_cast<uint32_t *>(ws);
     float *wp = reinterpret_cast<float *>(ws + pl.x_bytes);
 
-    // 1) one launch: x -> channels-last bf16 (hi, lo) pairs, weights -> run panels
-    // (channels-last x: the split alone, 1024 values per block)
+    // 1) one launch: x -> channels-last split (tf32 t, l or bf16 hi, lo), weights ->
+    // run panels (channels-last x: the split alone, 1024 values per block)
     const int64_t SP = pb.in_sp();
     const int64_t nbx = (SP + 63) / 64, nby = pb.C_in / 32;
     const int64_t cl_total = pb.cl ? (int64_t)pb.N * SP * pb.C_in : 0;
@@ -837,24 +956,27 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // 2) tensor maps: A over x_c (2C, W, H, D, N) bf16, 128-byte rows; B over
-    // the panels (C_in x 4 bytes, rows), one map per run length len (a box of
-    // 2 x len x C_out rows: the run's hi and lo panels)
+    // 2) tensor maps: A over x_c (2C, W, H, D, N) of fp32 words (tf32x3) or bf16
+    // (bf16x2), a box of one 128-byte row per position; B over the panels (rows
+    // of 2 C_in fp32 words or of C_in words), one map per run length len (a box
+    // of bmul x len x C_out rows: the run's panel)
     CUtensorMap tmXc, tmW[4];
-    const uint64_t astr[4] = {(uint64_t)pb.C_in * 4, (uint64_t)pb.C_in * pb.Li[2] * 4,
-                              (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * 4,
-                              (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * pb.Li[0] * 4};
+    const uint64_t vb = tf ? 8 : 4;          // bytes of x_c (and of a panel row) per input channel
+    const uint64_t astr[4] = {(uint64_t)pb.C_in * vb, (uint64_t)pb.C_in * pb.Li[2] * vb,
+                              (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * vb,
+                              (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * pb.Li[0] * vb};
     const uint64_t cdims[5] = {(uint64_t)pb.C_in * 2, (uint64_t)pb.Li[2], (uint64_t)pb.Li[1], (uint64_t)pb.Li[0],
                                (uint64_t)pb.N};
-    const uint32_t cbox[5] = {(uint32_t)CK * 2, (uint32_t)p.QW, (uint32_t)p.MH, 1u, 1u};
-    const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)pl.wq.nblk * pb.C_out};
-    const uint64_t bstr[1] = {(uint64_t)pb.C_in * 4};
-    if (!encode_tiled(&tmXc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc, cdims, astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint32_t cbox[5] = {tf ? 32u : 64u, (uint32_t)p.QW, (uint32_t)p.MH, 1u, 1u};
+    const uint64_t bdims[2] = {(uint64_t)pb.C_in * (tf ? 2 : 1), (uint64_t)pl.wq.nblk * pb.C_out};
+    const uint64_t bstr[1] = {(uint64_t)pb.C_in * vb};
+    if (!encode_tiled(&tmXc, tf ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc,
+                      cdims, astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     for (int len = 1; len <= 4; ++len) {
         // lengths beyond the longest run keep a valid map of the longest box
         const int l = len <= pl.maxlen ? len : pl.maxlen;
-        const uint32_t bbox[2] = {(uint32_t)CK, (uint32_t)(2 * l * pb.C_out)};
+        const uint32_t bbox[2] = {32u, (uint32_t)(p.bmul * l * pb.C_out)};
         if (!encode_tiled(&tmW[len - 1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, wp, bdims, bstr, bbox,
                           CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
@@ -888,10 +1010,14 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
         return cudaErrorInvalidValue;
     }
 
-    const void *fn = pb.cl ? (a.add ? (const void *)&tc3d_split_kernel<true, true>
-                                    : (const void *)&tc3d_split_kernel<false, true>)
-                           : (a.add ? (const void *)&tc3d_split_kernel<true, false>
-                                    : (const void *)&tc3d_split_kernel<false, false>);
+    const void *fn;
+#define CT_TC3D_FN(ADD_, CL_) (tf ? (const void *)&tc3d_split_kernel<ADD_, CL_, true> \
+                                  : (const void *)&tc3d_split_kernel<ADD_, CL_, false>)
+    if (pb.cl)
+        fn = a.add ? CT_TC3D_FN(true, true) : CT_TC3D_FN(false, true);
+    else
+        fn = a.add ? CT_TC3D_FN(true, false) : CT_TC3D_FN(false, false);
+#undef CT_TC3D_FN
     int per_sm = 0;
     e = prepare_kernel(fn, kThreads, pl.smem, &per_sm);
     if (e != cudaSuccess) return e;
@@ -902,11 +1028,15 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     if (grid > p.nunits) grid = p.nunits;
     if (p.SD == 2 && grid > 1 && (grid & 1)) --grid;   // an even grid: the residue flip of unit_coord permutes units
     const dim3 gd((unsigned)grid), bd(kThreads);
-#define CT_TC3D_LAUNCH(ADD_, CL_)                                                                                  \
-    launch_dependent(tc3d_split_kernel<ADD_, CL_>, gd, bd, pl.smem, a.stream, tmXc, tmW[0], tmW[1], tmW[2], tmW[3], \
-                     tmAdd, tmY, a.bias, p, status)
-    if (pb.cl) return a.add ? CT_TC3D_LAUNCH(true, true) : CT_TC3D_LAUNCH(false, true);
-    return a.add ? CT_TC3D_LAUNCH(true, false) : CT_TC3D_LAUNCH(false, false);
+#define CT_TC3D_LAUNCH(ADD_, CL_, TF_)                                                                       \
+    launch_dependent(tc3d_split_kernel<ADD_, CL_, TF_>, gd, bd, pl.smem, a.stream, tmXc, tmW[0], tmW[1], tmW[2], \
+                     tmW[3], tmAdd, tmY, a.bias, p, status)
+    if (tf) {
+        if (pb.cl) return a.add ? CT_TC3D_LAUNCH(true, true, true) : CT_TC3D_LAUNCH(false, true, true);
+        return a.add ? CT_TC3D_LAUNCH(true, false, true) : CT_TC3D_LAUNCH(false, false, true);
+    }
+    if (pb.cl) return a.add ? CT_TC3D_LAUNCH(true, true, false) : CT_TC3D_LAUNCH(false, true, false);
+    return a.add ? CT_TC3D_LAUNCH(true, false, false) : CT_TC3D_LAUNCH(false, false, false);
 #undef CT_TC3D_LAUNCH
 }
 

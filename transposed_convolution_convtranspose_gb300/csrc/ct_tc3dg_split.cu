@@ -1,32 +1,40 @@
 // ct_tc3dg_split.cu -- FP32 ConvTranspose3d with 32 input channels in 1, 2
 // or 4 groups (asymmetric kernels up to 8 per dimension, any padding) on the
-// tensor cores (tcgen05 kind::f16 with bf16 operands), with a two-term split of
-// every operand: v = hi + lo with hi = bf16(v) and lo = bf16(v - hi), leaving
-// less than 2^-17 |v|.  Per K step the A row holds [a_hi | a_lo] of 8 (or 16)
-// channels and two MMAs multiply it by [b_hi | b_hi] and by [b_lo | b_lo]:
-// together (a_hi + a_lo)(b_hi + b_lo), every bf16 product exact in the fp32
-// accumulator, so a product carries a relative error of about 2^-16 at most.
+// tensor cores (tcgen05), every operand split into parts whose products the
+// tensor cores form exactly.  Two splits, chosen by the caller:
+//  * tf32x3 (CT_F32, the default): v = t + l with t = tf32(v) (cvt.rna) and
+//    l = tf32(v - t), |v - t - l| <= 2^-22 |v|; per K step of 8 channels
+//    three kind::tf32 MMAs accumulate a_t b_t + a_t b_l + a_l b_t, so an
+//    output lies within about 2^-20 of sum |x||w| of the exact sum, the
+//    accuracy of fp32 arithmetic over the same terms.  x_c holds per position
+//    the t parts of the 32 channels (one 128-byte row), then their l parts
+//    (a second row); a panel row holds the t (or l) parts of the weights.
+//  * bf16x2 (CT_F32_BF16X2, opt-in): v = hi + lo with hi = bf16(v) and
+//    lo = bf16(v - hi), leaving less than 2^-17 |v|.  Per K step the A row
+//    holds [a_hi | a_lo] of 8 (or 16) channels and two MMAs multiply it by
+//    [b_hi | b_hi] and by [b_lo | b_lo]: together (a_hi + a_lo)(b_hi + b_lo),
+//    a relative error of about 2^-16 per product at most.
 //
 // Method ([l1_p72] stride-phase classes: residue r of a stride-2 dimension
 // receives the taps k with (r + p - k) even, reading input q + (r + p - k)/2;
-// [l1_p79] the grouped layer: output channel oc of group g sums over the
-// input channels of group g only):
+// and its grouped layer: output channel oc of group g sums over the input
+// channels of group g only):
 //     y[n, oc, 2q + r] = bias[oc] + sum over the phase's taps t and the group's
 //                        input channels ic of x[n, ic, q + delta_t] * w[ic, oc_l, k_t]
 // For one input offset (dd, dh, dw) every output phase (rD, rH, rW) that reads
 // it with some tap contributes; with 128 positions q as the M rows, a group's
-// contraction over its Cig = 32 / G channels (2 Cig bf16 values of K: hi and
-// lo parts) is 2 x Cig / 8 bf16 MMAs of K = 16.
+// contraction over its Cig = 32 / G channels is Cig / 8 K steps, each of
+// three tf32 MMAs of K = 8 (or two bf16 MMAs of K = 16 over the hi and lo
+// parts).
 //
 // Groups without block-diagonal zeros.  All 32 input channels of a position
 // are one 128-byte row of the A operand (K-major, 128-byte swizzle), so group
-// g's values (its channels' hi parts, then their lo parts) are the K steps
-// g * Cig/8 .. of that row: the MMAs of group g start their A and B
-// descriptors Cig * 4 * g bytes into the rows.  The weight panels hold, in the same K
-// positions of one row, the weights of every group for that row's (phase,
-// output channel within the group).  One MMA-issuing
-// warp per group owns that group's TMEM columns; all of them read the same
-// operand stages.
+// g's values are the K steps g * Cig/8 .. of that row: the MMAs of group g
+// start their A and B descriptors Cig * 4 * g bytes into the rows.  The
+// weight panels hold, in the same K positions of one row, the weights of
+// every group for that row's (phase, output channel within the group).  One
+// MMA-issuing warp per group owns that group's TMEM columns; all of them
+// read the same operand stages.
 //
 // Accumulators: per group, the 8 phases x Cog channels, ordered (rD, rH, rW,
 // oc_l), so the phases of one (rD, rH) pair -- both W residues -- are 2 x Cog
@@ -41,13 +49,13 @@
 //
 // Operand A without shifted copies (the 128-byte swizzle is a function of the
 // absolute shared-memory address): x is repacked channels-last with H fastest
-// after the channels, (N, D, W, H, 64) bf16, per group [hi | lo]; per D
-// offset one TMA box brings the
-// unit's input window, (8 + H halo) x (16 + W halo) positions of 128 bytes,
-// rows ordered (w, h).  The A operand of offset (dh, dw) is
-// that window read from row (dw - dw_lo) * hspan + (dh - dh_lo) with a stride
-// of hspan rows between 8-row groups.  A unit is 16 qw x 8 qh positions of one
-// D plane; TMEM row m holds (qw, qh) = (m / 8, m mod 8).
+// after the channels, (N, D, W, H, channels); per D offset one TMA box (two
+// for tf32x3: the t rows, then the l rows) brings the unit's input window,
+// (8 + H halo) x (16 + W halo) positions of 128 bytes, rows ordered (w, h).
+// The A operand of offset (dh, dw) is that window read from row (dw - dw_lo)
+// * hspan + (dh - dh_lo) with a stride of hspan rows between 8-row groups.  A
+// unit is 16 qw x 8 qh positions of one D plane; TMEM row m holds (qw, qh) =
+// (m / 8, m mod 8).
 //
 // Roles (persistent CTA, one per SM):
 //   warp 0      TMA producer of the A ring (the window of a D offset)
@@ -78,7 +86,7 @@ namespace {
 constexpr int BM = 128;          // positions per unit (UMMA M)
 constexpr int QWT = 16;          // qw per unit (TMEM row m: qw = m / 8)
 constexpr int MHT = 8;           // qh per unit (one 8-row swizzle group per qw)
-constexpr int CK = 32;           // input channels: one 128-byte row of bf16 (hi, lo) pairs
+constexpr int CK = 32;           // input channels: one 128-byte row of tf32 parts or of bf16 (hi, lo) pairs
 constexpr int NA = 3;            // A ring slots (one window each)
 constexpr int MAXB = 8;          // B ring slots at most
 constexpr int BROWS = 256;       // rows of a B stage at most (one 32 KB slot)
@@ -117,17 +125,18 @@ struct GParams {
     int bs_units[MAXE];          // rows of B stage j in units of 4 x Cog rows
     int nb, npb;                 // B ring slots and producers (nb a multiple of npb)
     int hspan, wspan, dh_lo, dw_lo;
-    uint32_t a_slot;             // bytes of one window, 1024-aligned
+    uint32_t a_half;             // bytes of the window's rows of one kind (t or l; all of bf16x2), 1024-aligned
+    uint32_t a_slot;             // bytes of one window: a_half (bf16x2) or 2 a_half (tf32x3: t rows, then l rows)
     uint32_t bslot;              // bytes of a B ring slot (the widest panel)
     uint32_t set_cols;           // 8 x C_out
     uint32_t tmem_cols;
-    uint32_t idesc_b[5];         // kind::f16 (bf16), N = 2 x Cog x pairs, pairs 1..4
+    uint32_t idesc_b[5];         // instruction descriptor, N = 2 x Cog x pairs, pairs 1..4
     GEntry ent[MAXE];
 };
 
 // Weight panel description for the prep kernel.
 struct GPanels {
-    int Cig, Cog, K0, K1, K2, ne;
+    int Cig, Cog, K0, K1, K2, ne, tf;
     int off_lo[3];               // smallest input offset per dimension
     int8_t tap[3][2][8];         // tap of residue r reading offset off_lo + i (-1: none)
     int8_t edd[MAXE], edh[MAXE], edw[MAXE], eq0[MAXE], enq[MAXE], emask[MAXE];   // emask: pairs reading it
@@ -142,6 +151,14 @@ __device__ __forceinline__ uint32_t bf16_bits(float v)
 __device__ __forceinline__ float bf16_round(float v)
 {
     return __bfloat162float(__float2bfloat16_rn(v));
+}
+// v rounded to tf32 (10 fraction bits, nearest, ties away from zero): the low
+// 13 bits are zero, so the tensor cores read it exactly
+__device__ __forceinline__ float tf32_round(float v)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
 }
 
 // 8 columns of the warp's 32 TMEM lanes set to zero.
@@ -167,13 +184,14 @@ __device__ __forceinline__ uint64_t desc_sbo(uint32_t saddr, uint32_t sbo)
 }
 
 // ---- prep kernels --------------------------------------------------------------
-// x (N, 32, D, H, W) -> x_c (N, D, W, H, 64) bf16, per group [hi of its Cig
-// channels | lo of them].  Block = 32 channels x 64 consecutive source
-// positions (16-byte loads along W, a shared tile of pitch 33); a thread then
-// writes 4 channels of one position: two 8-byte stores, hi and lo.  D*H*W is
-// a multiple of 4.
+// x (N, 32, D, H, W) -> x_c (N, D, W, H, channels): tf32x3 64 fp32 words
+// per position, [t of the 32 channels | l of them]; bf16x2 64 bf16, per group
+// [hi of its Cig channels | lo of them].  Block = 32 channels x 64
+// consecutive source positions (16-byte loads along W, a shared tile of pitch
+// 33); a thread then writes 4 channels of one position: two stores of their
+// two parts.  D*H*W is a multiple of 4.
 __device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, uint16_t *__restrict__ xc, int D, int H,
-                                              int W, int Cig, int bx, int n)
+                                              int W, int Cig, int bx, int n, bool tf)
 {
     __shared__ float tile[64][33];
     const int64_t SP = (int64_t)D * H * W;
@@ -199,6 +217,20 @@ __device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, uint1
         if (pos < ncols) {
             const int64_t s = s0 + pos;
             const int w = (int)(s % W), h = (int)((s / W) % H), d = (int)(s / ((int64_t)W * H));
+            const int64_t prow = (((int64_t)n * D + d) * W + w) * H + h;
+            if (tf) {
+                float t[4], l[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float v = tile[pos][4 * q + i];
+                    t[i] = tf32_round(v);
+                    l[i] = tf32_round(v - t[i]);    // v - t is exact in fp32
+                }
+                float *cr = reinterpret_cast<float *>(xc) + prow * (2 * CK) + 4 * q;
+                *reinterpret_cast<float4 *>(cr) = make_float4(t[0], t[1], t[2], t[3]);
+                *reinterpret_cast<float4 *>(cr + CK) = make_float4(l[0], l[1], l[2], l[3]);
+                continue;
+            }
             uint32_t hb[4], lb[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -207,7 +239,6 @@ __device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, uint1
                 hb[i] = bf16_bits(hv);
                 lb[i] = bf16_bits(v - hv);      // v - hv is exact in fp32
             }
-            const int64_t prow = (((int64_t)n * D + d) * W + w) * H + h;
             // channels 4q..4q+3 lie in one group g: hi at g*2Cig + i, lo Cig further
             const int c0 = 4 * q, g = c0 / Cig, i0 = c0 % Cig;
             uint16_t *cr = xc + prow * (2 * CK) + g * 2 * Cig + i0;
@@ -220,16 +251,18 @@ __device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, uint1
 // w (32, Cog, K0, K1, K2) -> panels.  Blocks (entry e, part hl, slice z), rows
 // rr = (pair index i, rW, oc_l) of the entry; the weight of a row for input
 // channel ic is w[ic][oc_l][kd][kh][kw] for the tap of phase (q0 + i, rW)
-// reading the entry's offset, zero where that phase reads none.  64 bf16 per
-// row, per group: part 0 [hi of its Cig channels | hi again], part 1 [lo | lo],
-// the partners of the [hi | lo] order of x_c.
+// reading the entry's offset, zero where that phase reads none.  tf32x3: 32
+// fp32 words per row, the t parts (part 0) or l parts (part 1) of the 32
+// input channels.  bf16x2: 64 bf16 per row, per group: part 0 [hi of its Cig
+// channels | hi again], part 1 [lo | lo], the partners of the [hi | lo] order
+// of x_c.
 constexpr int kWSlices = 8;      // blocks per (entry, part) of the panel prep
 
 __device__ __forceinline__ void prepg_w_block(const float *__restrict__ w, uint8_t *__restrict__ wp,
                                               const GPanels &q, int e, int hl, int z)
 {
     const int R = q.enq[e] * 2 * q.Cog;
-    const int ncol = 2 * CK;
+    const int ncol = q.tf ? CK : 2 * CK;
     for (int idx = threadIdx.x + z * blockDim.x; idx < R * ncol; idx += blockDim.x * kWSlices) {
         const int rr = idx / ncol, k = idx % ncol;
         const int i = rr / (2 * q.Cog);
@@ -240,13 +273,18 @@ __device__ __forceinline__ void prepg_w_block(const float *__restrict__ w, uint8
         const int kh = q.tap[1][rH][q.edh[e] - q.off_lo[1]];
         const int kw = q.tap[2][rW][q.edw[e] - q.off_lo[2]];
         const int g = k / (2 * q.Cig), within = k % (2 * q.Cig);
-        const int ic = g * q.Cig + (within % q.Cig);
+        const int ic = q.tf ? k : g * q.Cig + (within % q.Cig);
         float v = 0.f;
         if (((q.emask[e] >> pq) & 1) && kd >= 0 && kh >= 0 && kw >= 0)
             v = __ldg(w + (((int64_t)ic * q.Cog + oc_l) * q.K0 + kd) * (q.K1 * q.K2) + kh * q.K2 + kw);
-        const float hv = bf16_round(v);
         uint8_t *row = wp + ((int64_t)q.erow0[e] + hl * R + rr) * 128;
-        reinterpret_cast<uint16_t *>(row)[k] = (uint16_t)bf16_bits(hl ? v - hv : hv);
+        if (q.tf) {
+            const float t = tf32_round(v);
+            reinterpret_cast<float *>(row)[k] = hl ? tf32_round(v - t) : t;
+        } else {
+            const float hv = bf16_round(v);
+            reinterpret_cast<uint16_t *>(row)[k] = (uint16_t)bf16_bits(hl ? v - hv : hv);
+        }
     }
 }
 
@@ -262,7 +300,7 @@ prepg_kernel(const float *__restrict__ x, uint16_t *__restrict__ xc, int D, int 
     dev::griddep_launch_dependents();
     const int b = (int)blockIdx.x;
     if (b < nxb) {
-        prepg_x_block(x, xc, D, H, W, Cig, b % nbx, b / nbx);
+        prepg_x_block(x, xc, D, H, W, Cig, b % nbx, b / nbx, q.tf != 0);
     } else {
         const int r = b - nxb;
         prepg_w_block(w, wp, q, r / (2 * kWSlices), (r / kWSlices) & 1, r % kWSlices);
@@ -286,6 +324,7 @@ __device__ __forceinline__ GUnit g_unit(int u, const GParams &p)
     return c;
 }
 
+template <bool TF>
 __global__ void __launch_bounds__(kThreads, 1)
 tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                   const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW4,
@@ -376,10 +415,14 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                     break;
                 }
                 if (isA) {
-                    // x_c viewed as (C, H, W, D, N): the window of D offset dd[i]
+                    // x_c viewed as (C, H, W, D, N): the window of D offset dd[i] (tf32x3:
+                    // the t rows, then the l rows a_half further)
                     const int h0 = u.qhb * MHT + p.dh_lo, w0 = u.qwb * QWT + p.dw_lo, d0 = u.qd + p.dd[i];
-                    dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(p.hspan * p.wspan) * 128u);
+                    dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)((TF ? 2 : 1) * p.hspan * p.wspan) * 128u);
                     dev::tma_load_5d(sA + (size_t)s * p.a_slot, &tmXc, &fullb[s], 0, h0, w0, d0, u.n);
+                    if (TF)
+                        dev::tma_load_5d(sA + (size_t)s * p.a_slot + p.a_half, &tmXc, &fullb[s], CK, h0, w0, d0,
+                                         u.n);
                 } else {
                     // the stage's panels (consecutive rows): boxes of 4 and of 1 unit
                     const int units = p.bs_units[i];
@@ -411,8 +454,9 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             const uint32_t sAb = dev::smem_u32(sA), sBb = dev::smem_u32(sB);
             const uint32_t a_slot = p.a_slot, bslot = p.bslot, sbo = (uint32_t)p.hspan * 128u;
             const int Cog = p.Cog, ksteps = p.Cig / 8, nb = p.nb;
-            // K step j of group g (16 bf16: hi or lo parts) sits (g * ksteps + j) *
-            // 32 bytes into every row
+            // K step j of group g (tf32x3: 8 channels, 32 bytes of t or of l parts;
+            // bf16x2: 16 bf16, hi or lo parts) sits (g * ksteps + j) * 32 bytes into
+            // every row
             const uint64_t kgrp = (uint64_t)(g * ksteps * 2);         // in 16-byte units
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
@@ -445,10 +489,20 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                             const uint64_t dbh = tc::desc_sw128(bb + t0.y) + kgrp;
                             const uint64_t dbl = tc::desc_sw128(bb + t0.y + t0.z) + kgrp;
                             const uint32_t d = dg + t0.w;
-                            for (int kk = 0; kk < ksteps; ++kk) {
-                                const uint64_t kj = (uint64_t)(2 * kk);   // 32 bytes: 16 bf16
-                                tc::mma_bf16(d, da + kj, dbh + kj, id, 1u);   // [a_hi|a_lo] x [b_hi|b_hi]
-                                tc::mma_bf16(d, da + kj, dbl + kj, id, 1u);   // [a_hi|a_lo] x [b_lo|b_lo]
+                            if (TF) {
+                                const uint64_t dal = desc_sbo(wc + p.a_half + t0.x, sbo) + kgrp;
+                                for (int kk = 0; kk < ksteps; ++kk) {
+                                    const uint64_t kj = (uint64_t)(2 * kk);   // 32 bytes: 8 channels
+                                    tc::mma_tf32(d, da + kj, dbh + kj, id, 1u);    // a_t b_t
+                                    tc::mma_tf32(d, da + kj, dbl + kj, id, 1u);    // a_t b_l
+                                    tc::mma_tf32(d, dal + kj, dbh + kj, id, 1u);   // a_l b_t
+                                }
+                            } else {
+                                for (int kk = 0; kk < ksteps; ++kk) {
+                                    const uint64_t kj = (uint64_t)(2 * kk);   // 32 bytes: 16 bf16
+                                    tc::mma_bf16(d, da + kj, dbh + kj, id, 1u);   // [a_hi|a_lo] x [b_hi|b_hi]
+                                    tc::mma_bf16(d, da + kj, dbl + kj, id, 1u);   // [a_hi|a_lo] x [b_lo|b_lo]
+                                }
                             }
                         }
                         tc::commit(&b_empty[sb]);
@@ -586,6 +640,7 @@ bool make_gplan(const Problem &pb, const Args *a, GPlan *out)
 bool make_gplan_3d(const Problem &pb, const Args *a, GPlan *out)
 {
     if (pb.nd != 3 || pb.dtype != CT_F32 || pb.has_add) return false;
+    const bool tf = !pb.split2;          // tf32x3 unless the caller opted into the bf16 pair
     for (int d = 0; d < 3; ++d)
         if (pb.S[d] != 2 || pb.DL[d] != 1 || pb.K[d] < 1 || pb.K[d] > 8) return false;
     if (pb.C_in != CK || (pb.G != 1 && pb.G != 2 && pb.G != 4)) return false;
@@ -693,6 +748,7 @@ bool make_gplan_3d(const Problem &pb, const Args *a, GPlan *out)
     p.s0[p.ndd] = p.nbs;
     p.bs_e0[p.nbs] = p.ne;
     wq.Cig = pb.Cig; wq.Cog = pb.Cog;
+    wq.tf = tf ? 1 : 0;
     wq.K0 = pb.K[0]; wq.K1 = pb.K[1]; wq.K2 = pb.K[2];
     wq.ne = p.ne;
     // input windows
@@ -700,8 +756,9 @@ bool make_gplan_3d(const Problem &pb, const Args *a, GPlan *out)
     p.dw_lo = lo[2];
     p.hspan = MHT + hi[1] - lo[1];
     p.wspan = QWT + hi[2] - lo[2];
-    p.a_slot = (uint32_t)((p.hspan * p.wspan * 128 + 1023) & ~1023);
-    for (int nq = 1; nq <= 4; ++nq) p.idesc_b[nq] = tc::idesc(1, 2 * nq * pb.Cog, BM);
+    p.a_half = (uint32_t)((p.hspan * p.wspan * 128 + 1023) & ~1023);
+    p.a_slot = (tf ? 2 : 1) * p.a_half;
+    for (int nq = 1; nq <= 4; ++nq) p.idesc_b[nq] = tc::idesc(tf ? 2 : 1, 2 * nq * pb.Cog, BM);
     p.set_cols = (uint32_t)(8 * pb.C_out);
     uint32_t cols = 32;
     while (cols < 2 * p.set_cols) cols <<= 1;
@@ -719,7 +776,7 @@ bool make_gplan_3d(const Problem &pb, const Args *a, GPlan *out)
     out->p = p;
     out->wq = wq;
     out->rows = row;
-    out->x_bytes = align256((size_t)pb.N * CK * pb.in_sp() * 4);
+    out->x_bytes = align256((size_t)pb.N * CK * pb.in_sp() * (tf ? 8 : 4));
     out->w_bytes = align256((size_t)row * CK * 4);
     out->smem = a_area + (size_t)nb * p.bslot + 1024;
     return true;
@@ -749,8 +806,10 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
     uint16_t *xc = reinterpret_cast<uint16_t *>(ws);
     uint8_t *wp = ws + pl.x_bytes;
 
-    // 1) one launch: x -> (N, D, W, H, 64) bf16 [hi | lo] per group; weights ->
-    // one panel per input offset (hi rows, then lo rows)
+    const bool tf = pl.wq.tf != 0;
+    // 1) one launch: x -> (N, D, W, H, channels) split (tf32 [t x 32 | l x 32] or
+    // bf16 [hi | lo] per group); weights -> one panel per input offset (hi / t
+    // rows, then lo / l rows)
     const int64_t SP = pb.in_sp();
     const int64_t nbx = (SP + 63) / 64;
     const int64_t nxb = nbx * pb.N;
@@ -762,16 +821,19 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // 2) tensor maps: A over x_c (bf16) viewed as (C, H, W, D, N), one window per
-    // box, 128-byte rows; B over the panels (32 x 4 bytes, rows), boxes of
-    // 4 x Cog and 16 x Cog rows
+    // 2) tensor maps: A over x_c viewed as (C, H, W, D, N), one window per box
+    // (tf32x3: 64 fp32 words per position, a box of 32, the t or the l rows;
+    // bf16x2: 64 bf16, one box), 128-byte rows; B over the panels (32 x 4
+    // bytes, rows), boxes of 4 x Cog and 16 x Cog rows
     CUtensorMap tmXc, tmW[2];
+    const uint64_t pb_bytes = tf ? 8 * CK : 4 * CK;     // bytes of x_c per position
     const uint64_t cdims[5] = {(uint64_t)(2 * CK), (uint64_t)pb.Li[1], (uint64_t)pb.Li[2], (uint64_t)pb.Li[0],
                                (uint64_t)pb.N};
-    const uint64_t astr[4] = {(uint64_t)CK * 4, (uint64_t)CK * pb.Li[1] * 4, (uint64_t)CK * pb.Li[1] * pb.Li[2] * 4,
-                              (uint64_t)CK * pb.Li[1] * pb.Li[2] * pb.Li[0] * 4};
-    const uint32_t cbox[5] = {(uint32_t)(2 * CK), (uint32_t)p.hspan, (uint32_t)p.wspan, 1u, 1u};
-    if (!encode_tiled(&tmXc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc, cdims, astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t astr[4] = {pb_bytes, pb_bytes * pb.Li[1], pb_bytes * pb.Li[1] * pb.Li[2],
+                              pb_bytes * pb.Li[1] * pb.Li[2] * pb.Li[0]};
+    const uint32_t cbox[5] = {tf ? (uint32_t)CK : (uint32_t)(2 * CK), (uint32_t)p.hspan, (uint32_t)p.wspan, 1u, 1u};
+    if (!encode_tiled(&tmXc, tf ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc, cdims,
+                      astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const uint64_t bdims[2] = {(uint64_t)CK, (uint64_t)pl.rows};
     const uint64_t bstr[1] = {(uint64_t)CK * 4};
@@ -784,15 +846,19 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
     }
 
     int per_sm = 0;
-    e = prepare_kernel((const void *)&tc3dg_split_kernel, kThreads, pl.smem, &per_sm);
+    const void *fn = tf ? (const void *)&tc3dg_split_kernel<true> : (const void *)&tc3dg_split_kernel<false>;
+    e = prepare_kernel(fn, kThreads, pl.smem, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     unsigned int *status = device_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.nunits) grid = p.nunits;
-    return launch_dependent(tc3dg_split_kernel, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmXc,
-                            tmW[0], tmW[1], a.bias, a.y, p, status);
+    if (tf)
+        return launch_dependent(tc3dg_split_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
+                                tmXc, tmW[0], tmW[1], a.bias, a.y, p, status);
+    return launch_dependent(tc3dg_split_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
+                            tmXc, tmW[0], tmW[1], a.bias, a.y, p, status);
 }
 
 }  // namespace ct

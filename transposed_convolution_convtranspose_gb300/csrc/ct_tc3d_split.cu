@@ -20,9 +20,9 @@
 //    fp32 accumulator; the dropped x_l w_l and the two remainders are each
 //    at most 2^-22 |x||w|, so an output lies within about 2^-20 of
 //    sum |x||w| of the exact sum -- the accuracy of fp32 arithmetic over the
-//    same terms.  An operand row holds 16 channels, [t of the 16 | l of the
-//    16] (128 bytes): the A stage of a K block is one 128-byte row per
-//    position and the B panel one row per output channel.
+//    same terms.  A K block is 32 channels: the A stage holds, per position,
+//    a 128-byte row of their t parts and one of their l parts (two TMA boxes,
+//    two 16 KB halves); a run's panel its t rows, then its l rows.
 //  * bf16x2 (CT_F32_BF16X2, opt-in).  hi = bf16(v) (round to nearest even),
 //    lo = bf16(v - hi); the dropped remainder is below 2^-17 |v|.  Per K step
 //    of 8 input channels the A row holds [x_hi | x_lo] of the 8 (16 bf16 =
@@ -77,21 +77,21 @@
 #include "ct_device.cuh"
 #include "ct_tma.h"
 #include "ct_tcgen05.cuh"
+#include "ct_split.cuh"
 
 namespace ct {
 namespace {
 
 constexpr int BM = 128;          // positions per unit (UMMA M)
-constexpr int CKB = 32;          // bf16x2: input channels per K block (one 128-byte row of (hi, lo) pairs)
-constexpr int CKT = 16;          // tf32x3: input channels per K block (one 128-byte row [t x 16 | l x 16])
-constexpr int NA = 4;            // A stages (one producer warp; deep enough to cover DRAM latency)
+constexpr int CK = 32;           // input channels per K block: one 128-byte row of bf16 (hi, lo) pairs, or
+                                 // of tf32 t parts plus one of l parts
+constexpr int NA = 4;            // A ring slots at most (bf16x2: 4 of 16 KB; tf32x3: 2 of 32 KB)
 constexpr int NB = 2;            // B stages
 constexpr int NE = 3;            // epilogue chunk buffers (16 channels of a unit, 32 KB each)
 constexpr int NPA = 2;           // A producer warps: warp q loads the A stages g with g mod NPA == q
 constexpr int NPB = 2;           // B producer warps: warp q loads the B stages g with g mod NPB == q
 constexpr int MAXE = 18;         // input offsets per D residue (2 x 3 x 3 for extents <= 4)
 constexpr int MAXR = 64;         // runs per D residue
-constexpr int MAXBLK = 128;      // C_out-row blocks of the weight panels (2 x taps)
 constexpr int EPW = 4;           // epilogue warps per TMEM lane quarter (H phase x channel half)
 constexpr int kAWarp0 = 0;
 constexpr int kBWarp0 = kAWarp0 + NPA;
@@ -99,7 +99,7 @@ constexpr int kMmaWarp = kBWarp0 + NPB;
 constexpr int kEpiWarp0 = kMmaWarp + 1;
 constexpr int kStoreWarp = kEpiWarp0 + 4 * EPW;
 constexpr int kThreads = 32 * (kStoreWarp + 1);
-constexpr uint32_t kATile = BM * 128;          // 128 positions x one 128-byte row: 16 KB
+constexpr uint32_t kAHalf = BM * 128;          // 128 positions x one 128-byte row: 16 KB
 constexpr uint32_t kEChunk = 16 * 4 * BM * 4;  // 16 channels x 4 phases x 128 positions, fp32: 32 KB
 constexpr int kEpiThreads = 32 * 4 * EPW;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -123,9 +123,9 @@ struct T3Params {
     int SD;                      // D stride: 2, or 1 for a unit D dimension (a 2-D problem)
     int Lo0, Lo1, Lo2;
     int QD, QH, QW, MH, n_qhb;
-    int n_kb;                    // K blocks: C_in / 16 (tf32x3) or C_in / 32 (bf16x2)
-    int a_kstep;                 // A map coordinate of K block 1 (elements of x_c)
-    int bmul;                    // panel rows per accumulator column block: 1 (tf32x3) or 2 (bf16x2: hi, lo)
+    int n_kb;                    // K blocks: C_in / 32
+    int na;                      // A ring slots
+    uint32_t aslot;              // bytes of an A ring slot: 16 KB (bf16x2) or 32 KB (tf32x3: t rows, l rows)
     int nunits;
     int nacc;                    // accumulator sets (1 or 2)
     uint32_t acc_cols;           // 4 x C_out
@@ -138,172 +138,6 @@ struct T3Params {
     Run run[2][MAXR];
 };
 
-// Weight panel rows.  tf32x3: block b (C_out rows) holds tap blk_tap[b], each
-// row [t x 16 | l x 16] per K block.  bf16x2: block b holds tap blk_tap[b]:
-// its bf16 hi parts (blk_lo 0) or its lo parts (blk_lo 1), each twice per K
-// step.
-struct WPanels {
-    int C_in, C_out, ntap, nblk, tf;
-    int8_t blk_tap[MAXBLK];
-    int8_t blk_lo[MAXBLK];
-};
-
-// ---- prep kernels ------------------------------------------------------------
-__device__ __forceinline__ float bf16_round(float v)
-{
-    return __bfloat162float(__float2bfloat16_rn(v));
-}
-__device__ __forceinline__ uint32_t bf16_bits(float v)
-{
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
-}
-// v rounded to tf32 (10 fraction bits, nearest, ties away from zero): the low
-// 13 bits of the result are zero, so the tensor cores read it exactly
-__device__ __forceinline__ float tf32_round(float v)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(v));
-    return __uint_as_float(r);
-}
-
-// The split of 4 consecutive channels c .. c + 3 of one position, stored at
-// the channel's place in x_c.  tf32x3: row of 16 channels [t x 16 | l x 16],
-// 32 floats per 16 channels; bf16x2: per K step of 8 channels [hi x 8 | lo x
-// 8], 16 bf16 per 8 channels.  `pos` points at the position's x_c row (its
-// element 0) in 4-byte units; c is a multiple of 4.
-__device__ __forceinline__ void store_split4(uint32_t *pos, int c, const float (&v)[4], bool tf)
-{
-    if (tf) {
-        float t[4], l[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            t[i] = tf32_round(v[i]);
-            l[i] = tf32_round(v[i] - t[i]);       // v - t is exact in fp32
-        }
-        uint32_t *r = pos + (c >> 4) * 32 + (c & 15);
-        *reinterpret_cast<float4 *>(r) = make_float4(t[0], t[1], t[2], t[3]);
-        *reinterpret_cast<float4 *>(r + 16) = make_float4(l[0], l[1], l[2], l[3]);
-    } else {
-        uint32_t hb[4], lb[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float h = bf16_round(v[i]);
-            hb[i] = bf16_bits(h);
-            lb[i] = bf16_bits(v[i] - h);          // v - h is exact in fp32
-        }
-        // K step c / 8 of the row (32 bytes = 8 words each), elements c mod 8 ..
-        uint16_t *r = reinterpret_cast<uint16_t *>(pos) + (c >> 3) * 16 + (c & 4);
-        *reinterpret_cast<uint2 *>(r) = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
-        *reinterpret_cast<uint2 *>(r + 8) = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
-    }
-}
-
-// x (N, C, S) -> x_c (N, S, 2C x 4 bytes (tf32x3) or 2C x 2 bytes (bf16x2));
-// S = D*H*W a multiple of 4, C of 32.  Block = 32 channels x 64 positions:
-// 16-byte loads of 4 positions of one channel (a warp reads 2 x 256
-// contiguous bytes), a shared tile of pitch 33, then per thread 4 channels
-// of one position.
-__device__ __forceinline__ void prep_x_block(const float *__restrict__ x, uint32_t *__restrict__ xc, int C,
-                                             int64_t SP, int bx, int by, int n, bool tf)
-{
-    __shared__ float tile[64][33];
-    const int c0 = by * 32;
-    const int64_t s0 = (int64_t)bx * 64;
-    const int ncols = (int)((SP - s0) < 64 ? (SP - s0) : 64);
-    const float *xs = x + ((int64_t)n * C + c0) * SP + s0;
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int idx = threadIdx.x + 256 * it;
-        const int c = idx >> 4, p4 = idx & 15;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p4 * 4 < ncols) v = __ldcs(reinterpret_cast<const float4 *>(xs + (int64_t)c * SP + p4 * 4));
-        tile[p4 * 4 + 0][c] = v.x;
-        tile[p4 * 4 + 1][c] = v.y;
-        tile[p4 * 4 + 2][c] = v.z;
-        tile[p4 * 4 + 3][c] = v.w;
-    }
-    __syncthreads();
-    // 4-byte words of x_c per position: 2C (tf32x3) or C (bf16x2)
-    const int64_t wpp = tf ? 2 * (int64_t)C : (int64_t)C;
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int idx = threadIdx.x + 256 * it;
-        const int q = idx & 7, pos = idx >> 3;
-        if (pos < ncols) {
-            float v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = tile[pos][4 * q + i];
-            store_split4(xc + ((int64_t)n * SP + s0 + pos) * wpp, c0 + 4 * q, v, tf);
-        }
-    }
-}
-
-// w (C_in, C_out, K0, K1, K2) -> weight panels [block][C_out rows]: tf32x3
-// rows of [t x 16 | l x 16] per K block (8 bytes per input channel); bf16x2
-// rows of [hi | hi] (blk_lo 0) or [lo | lo] (blk_lo 1) per K step of 8 input
-// channels (4 bytes per input channel).
-__device__ __forceinline__ void prep_w_block(const float *__restrict__ w, float *__restrict__ wp, const WPanels &q,
-                                             int bw, int nbw)
-{
-    const int64_t per = (int64_t)q.C_out * q.C_in;
-    const int64_t total = (int64_t)q.nblk * per;
-    for (int64_t e = (int64_t)bw * blockDim.x + threadIdx.x; e < total; e += (int64_t)nbw * blockDim.x) {
-        const int b = (int)(e / per);
-        const int64_t r = e % per;
-        const int oc = (int)(r / q.C_in), ic = (int)(r % q.C_in);
-        const float v = __ldg(w + ((int64_t)ic * q.C_out + oc) * q.ntap + q.blk_tap[b]);
-        if (q.tf) {
-            const float t = tf32_round(v);
-            float *row = wp + 2 * (e - ic);
-            row[(ic >> 4) * 32 + (ic & 15)] = t;
-            row[(ic >> 4) * 32 + 16 + (ic & 15)] = tf32_round(v - t);
-        } else {
-            const float h = bf16_round(v);
-            const uint16_t t = (uint16_t)bf16_bits(q.blk_lo[b] ? v - h : h);
-            // the row's bf16 view: K step ic / 8 of its 32-channel block
-            uint16_t *row = reinterpret_cast<uint16_t *>(wp + (e - ic));
-            const int kb = ic >> 5, kk = (ic & 31) >> 3, el = ic & 7;
-            row[kb * 64 + kk * 16 + el] = t;
-            row[kb * 64 + kk * 16 + 8 + el] = t;
-        }
-    }
-}
-
-// Channels-last x (N, S, C) -> x_c: the same split, no transpose.  Block =
-// 1024 consecutive values (256 threads x 4 channels: one 16-byte load each);
-// C a multiple of 32, so 4 channels never cross a position.
-__device__ __forceinline__ void prep_x_cl_block(const float *__restrict__ x, uint32_t *__restrict__ xc, int C,
-                                                int64_t total, int bx, bool tf)
-{
-    const int64_t e = ((int64_t)bx * 256 + threadIdx.x) * 4;    // first of 4 values
-    if (e >= total) return;
-    const float4 v4 = __ldcs(reinterpret_cast<const float4 *>(x + e));
-    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-    const int c = (int)(e % C);
-    const int64_t pos = e / C;
-    store_split4(xc + pos * (tf ? 2 * (int64_t)C : (int64_t)C), c, v, tf);
-}
-
-// Both preps in one launch: blocks [0, nxb) move x (nbx x nby per image; or,
-// channels last, 1024 consecutive values each), the remaining nbw blocks build
-// the panels.  The GEMM kernel is launched as its programmatic dependent.
-__global__ void __launch_bounds__(256)
-prep_kernel(const float *__restrict__ x, uint32_t *__restrict__ xc, int C, int64_t SP,
-            int nbx, int nby, int nxb, const float *__restrict__ w, float *__restrict__ wp,
-            const __grid_constant__ WPanels q, int nbw, int64_t cl_total)
-{
-    dev::griddep_launch_dependents();
-    const int b = (int)blockIdx.x;
-    const bool tf = q.tf != 0;
-    if (b < nxb && cl_total > 0) {
-        prep_x_cl_block(x, xc, C, cl_total, b, tf);
-    } else if (b < nxb) {
-        const int per = nbx * nby;
-        prep_x_block(x, xc, C, SP, (b % per) % nbx, (b % per) / nbx, b / per, tf);
-    } else {
-        prep_w_block(w, wp, q, b - nxb, nbw);
-    }
-}
 
 // ---- GEMM kernel ----------------------------------------------------------------
 // unit -> (n, qd, qh block, rD); a unit D dimension (stride 1) has the one residue
@@ -346,8 +180,8 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
     __shared__ uint32_t tmem_slot;
     __shared__ float s_bias[128];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = sm;                                  // NA x kATile
-    uint8_t *sB = sm + NA * kATile;                    // NB x bslot
+    uint8_t *sA = sm;                                  // na x aslot
+    uint8_t *sB = sm + (size_t)p.na * p.aslot;         // NB x bslot
     uint8_t *sE = sB + NB * p.bslot;                   // NE x kEChunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -359,7 +193,7 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         dev::prefetch_tensormap(&tmW4);
         dev::prefetch_tensormap(&tmY);
         if (ADD) dev::prefetch_tensormap(&tmAdd);
-        for (int s = 0; s < NA; ++s) {
+        for (int s = 0; s < p.na; ++s) {
             dev::mbar_init(&a_full[s], 1);
             dev::mbar_init(&a_empty[s], 1);
         }
@@ -399,7 +233,7 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             const bool isA = warp < kBWarp0;
             const int q = isA ? warp - kAWarp0 : warp - kBWarp0;
             const int np = isA ? NPA : NPB;
-            const int nst = isA ? NA : NB;
+            const int nst = isA ? p.na : NB;
             uint64_t *fullb = isA ? a_full : b_full;
             uint64_t *emptyb = isA ? a_empty : b_empty;
             int g = 0, s = 0, last = -1;             // ring position, slot
@@ -421,18 +255,23 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                                     break;
                                 }
                                 if (isA) {
-                                    dev::mbar_arrive_expect_tx(&fullb[s], kATile);
-                                    dev::tma_load_5d(sA + (size_t)s * kATile, &tmXc, &fullb[s], kb * p.a_kstep,
-                                                     en.dw, qh0 + en.dh, u.qd + en.dd, u.n);
+                                    // the K block's 128-byte rows (tf32x3: the t rows, then
+                                    // the l rows 16 KB further)
+                                    uint8_t *dst = sA + (size_t)s * p.aslot;
+                                    dev::mbar_arrive_expect_tx(&fullb[s], p.aslot);
+                                    dev::tma_load_5d(dst, &tmXc, &fullb[s], kb * 64, en.dw, qh0 + en.dh,
+                                                     u.qd + en.dd, u.n);
+                                    if (TF)
+                                        dev::tma_load_5d(dst + kAHalf, &tmXc, &fullb[s], kb * 64 + 32, en.dw,
+                                                         qh0 + en.dh, u.qd + en.dd, u.n);
                                 } else {
-                                    // the run's panel exactly: a box of bmul x len x C_out rows of
-                                    // the K block's 128 bytes
+                                    // the run's panel exactly: a box of 2 x len x C_out rows (hi / t
+                                    // rows, then lo / l rows) of the K block's 128 bytes
                                     const Run &ru = p.run[u.rd][en.run0 + j];
                                     const CUtensorMap *tm = ru.len == 1 ? &tmW1 : ru.len == 2 ? &tmW2
                                                           : ru.len == 3 ? &tmW3 : &tmW4;
-                                    dev::mbar_arrive_expect_tx(&fullb[s],
-                                                               (uint32_t)(p.bmul * ru.len * C_out) * 128u);
-                                    dev::tma_load_2d(sB + (size_t)s * p.bslot, tm, &fullb[s], kb * 32, ru.brow);
+                                    dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * ru.len * C_out) * 128u);
+                                    dev::tma_load_2d(sB + (size_t)s * p.bslot, tm, &fullb[s], kb * CK, ru.brow);
                                 }
                                 last = g;
                             }
@@ -457,7 +296,8 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         if (lane == 0) {
             bool ok = true;
             const uint32_t sAb = dev::smem_u32(sA), sBb = dev::smem_u32(sB);
-            const uint32_t bslot = p.bslot;
+            const uint32_t bslot = p.bslot, aslot = p.aslot;
+            const int na = p.na;
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
             for (int k = 0; k < nunit_cta && ok; ++k) {
@@ -479,7 +319,7 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                             break;
                         }
                         tc::fence_after();
-                        const uint64_t da = tc::desc_sw128(sAb + (uint32_t)sa * kATile);
+                        const uint64_t da = tc::desc_sw128(sAb + (uint32_t)sa * aslot);
                         for (int j = 0; j < en.nrun; ++j) {
                             const Run &ru = p.run[rd][en.run0 + j];
                             if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
@@ -489,23 +329,24 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                             tc::fence_after();
                             const uint32_t bh = sBb + (uint32_t)sb * bslot;
                             const uint64_t dbh = tc::desc_sw128(bh);
+                            const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(ru.len * C_out) * 128u);
                             const uint32_t idb = p.idesc_b[ru.len];
                             const uint32_t dd = d + (uint32_t)(ru.p0 * C_out);
                             const uint32_t acc0 = (ru.fresh && kb == 0) ? 0u : 1u;
                             if (TF) {
-                                // the 128-byte rows hold [t x 16 | l x 16]: K step kk (8
-                                // channels, 32 bytes) of the t parts at 32 kk bytes, of the
-                                // l parts 64 bytes further (descriptor units of 16 bytes)
+                                // K step kk: 8 channels, 32 bytes of the t rows (A, and the
+                                // panel's t rows) and of the l rows (A 16 KB further, the
+                                // panel's l rows after its t rows); descriptor units of 16 bytes
+                                const uint64_t dal = da + (kAHalf >> 4);
 #pragma unroll
-                                for (int kk = 0; kk < CKT / 8; ++kk) {
+                                for (int kk = 0; kk < CK / 8; ++kk) {
                                     tc::mma_tf32(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x_t w_t
-                                    tc::mma_tf32(dd, da + 2 * kk, dbh + 4 + 2 * kk, idb, 1u);         // x_t w_l
-                                    tc::mma_tf32(dd, da + 4 + 2 * kk, dbh + 2 * kk, idb, 1u);         // x_l w_t
+                                    tc::mma_tf32(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x_t w_l
+                                    tc::mma_tf32(dd, dal + 2 * kk, dbh + 2 * kk, idb, 1u);            // x_l w_t
                                 }
                             } else {
-                                const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(ru.len * C_out) * 128u);
 #pragma unroll
-                                for (int kk = 0; kk < CKB / 8; ++kk) {
+                                for (int kk = 0; kk < CK / 8; ++kk) {
                                     // 32 bytes along K inside the swizzle atom: 16 bf16, the
                                     // hi and lo parts of 8 channels
                                     tc::mma_bf16(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x * w_hi
@@ -519,7 +360,7 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                             }
                         }
                         tc::commit(&a_empty[sa]);
-                        if (++sa == NA) {
+                        if (++sa == na) {
                             sa = 0;
                             pa ^= 1u;
                         }
@@ -701,8 +542,6 @@ struct T3Plan {
     size_t x_bytes, w_bytes, smem;
 };
 
-size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
-
 // Taps of residue r in one stride-2, dilation-1 dimension: k with (r + P - k)
 // even, input offset (r + P - k) / 2 (exact).
 int dim_taps(int K, int P, int r, int *k_out, int *d_out)
@@ -770,7 +609,7 @@ bool plan_runs(const Problem &pb, int SD, const int (&nt)[3][2], const int (&tk)
                         while (ph + len < 4 && len < maxlen && tap_of[ph + len] >= 0 &&
                                (((init >> (ph + len)) & 1u) != 0) == st)
                             ++len;
-                        if (nr >= MAXR || nblk + bmul * len > MAXBLK) return false;
+                        if (nr >= MAXR || nblk + bmul * len > kMaxBlk) return false;
                         Run ru;
                         memset(&ru, 0, sizeof(ru));
                         ru.p0 = (int8_t)ph;
@@ -779,7 +618,7 @@ bool plan_runs(const Problem &pb, int SD, const int (&nt)[3][2], const int (&tk)
                         ru.brow = nblk * pb.C_out;
                         for (int hl = 0; hl < bmul; ++hl)
                             for (int i = 0; i < len; ++i) {
-                                wq->blk_tap[nblk] = (int8_t)tap_of[ph + i];
+                                wq->blk_tap[nblk] = (int16_t)tap_of[ph + i];
                                 wq->blk_lo[nblk] = (int8_t)hl;
                                 ++nblk;
                             }
@@ -829,9 +668,9 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     p.QD = (p.Lo0 + SD - 1) / SD;
     p.QH = (p.Lo1 + 1) / 2;
     p.n_qhb = (p.QH + p.MH - 1) / p.MH;
-    p.n_kb = pb.C_in / (tf ? CKT : CKB);
-    p.a_kstep = tf ? 32 : 2 * CKB;        // fp32 words (tf32x3) or bf16 elements (bf16x2) of x_c
-    p.bmul = tf ? 1 : 2;
+    p.n_kb = pb.C_in / CK;
+    p.na = tf ? 2 : NA;
+    p.aslot = (tf ? 2 : 1) * kAHalf;
     const int64_t units = (int64_t)pb.N * p.QD * p.n_qhb * SD;
     if (units > 0x7fffffff || units == 0) return false;
     p.nunits = (int)units;
@@ -861,8 +700,8 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
                 }
             }
     // runs of adjacent accumulators: at most 4 phases, N = len x C_out <= 256 and
-    // a panel of bmul x len x C_out rows <= 256 (one TMA box)
-    const int ml = 256 / (p.bmul * pb.C_out);
+    // a panel of 2 x len x C_out rows <= 256 (one TMA box)
+    const int ml = 128 / pb.C_out;
     const int maxlen = ml < 4 ? ml : 4;
     // the order of the four accumulators with the cheapest MMA schedule (the
     // first of equal ones, so the natural order when it is as good)
@@ -878,7 +717,7 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
         WPanels wt;
         memset(&wt, 0, sizeof(wt));
         double c = 0;
-        if (!plan_runs(pb, SD, nt, tk, td, uo, nu, kPerm[i], maxlen, p.bmul, tf ? 6 : 8, &p, &wt, &c)) continue;
+        if (!plan_runs(pb, SD, nt, tk, td, uo, nu, kPerm[i], maxlen, 2, tf ? 12 : 8, &p, &wt, &c)) continue;
         if (bi < 0 || c < best - 1e-9) {
             best = c;
             bi = i;
@@ -887,7 +726,7 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     if (bi < 0) return false;
     memset(&wq, 0, sizeof(wq));
     double c = 0;
-    if (!plan_runs(pb, SD, nt, tk, td, uo, nu, kPerm[bi], maxlen, p.bmul, tf ? 6 : 8, &p, &wq, &c)) return false;
+    if (!plan_runs(pb, SD, nt, tk, td, uo, nu, kPerm[bi], maxlen, 2, tf ? 12 : 8, &p, &wq, &c)) return false;
     for (int sl = 0; sl < 4; ++sl) p.slot[kPerm[bi][sl]] = (int8_t)sl;
     wq.C_in = pb.C_in;
     wq.C_out = pb.C_out;
@@ -900,16 +739,16 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     uint32_t cols = 32;
     while (cols < (uint32_t)p.nacc * p.acc_cols) cols <<= 1;
     p.tmem_cols = cols;
-    p.bslot = (uint32_t)(p.bmul * maxlen * pb.C_out) * 128u;
-    const size_t smem = (size_t)NA * kATile + (size_t)NB * p.bslot + (size_t)NE * kEChunk + 1024;
+    p.bslot = (uint32_t)(2 * maxlen * pb.C_out) * 128u;
+    const size_t smem = (size_t)p.na * p.aslot + (size_t)NB * p.bslot + (size_t)NE * kEChunk + 1024;
     if (smem > 227 * 1024 - 1024) return false;   // room for the static barriers
     out->p = p;
     out->wq = wq;
     out->maxlen = maxlen;
-    // x_c: 8 bytes per value (tf32 t and l) or 4 (bf16 hi and lo); panels the same per weight row entry
-    const size_t vb = tf ? 8 : 4;
-    out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * vb);
-    out->w_bytes = align256((size_t)wq.nblk * pb.C_out * pb.C_in * vb);
+    // x_c: 8 bytes per value (tf32 t and l) or 4 (bf16 hi and lo); a panel row 4
+    // bytes per input channel (a tf32 part, or a pair of bf16 parts)
+    out->x_bytes = align256((size_t)pb.N * pb.C_in * pb.in_sp() * (tf ? 8 : 4));
+    out->w_bytes = align256((size_t)wq.nblk * pb.C_out * pb.C_in * 4);
     out->smem = smem;
     return true;
 }
@@ -958,25 +797,25 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
 
     // 2) tensor maps: A over x_c (2C, W, H, D, N) of fp32 words (tf32x3) or bf16
     // (bf16x2), a box of one 128-byte row per position; B over the panels (rows
-    // of 2 C_in fp32 words or of C_in words), one map per run length len (a box
-    // of bmul x len x C_out rows: the run's panel)
+    // of C_in words), one map per run length len (a box of 2 x len x C_out
+    // rows: the run's panel)
     CUtensorMap tmXc, tmW[4];
-    const uint64_t vb = tf ? 8 : 4;          // bytes of x_c (and of a panel row) per input channel
+    const uint64_t vb = tf ? 8 : 4;          // bytes of x_c per input channel
     const uint64_t astr[4] = {(uint64_t)pb.C_in * vb, (uint64_t)pb.C_in * pb.Li[2] * vb,
                               (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * vb,
                               (uint64_t)pb.C_in * pb.Li[2] * pb.Li[1] * pb.Li[0] * vb};
     const uint64_t cdims[5] = {(uint64_t)pb.C_in * 2, (uint64_t)pb.Li[2], (uint64_t)pb.Li[1], (uint64_t)pb.Li[0],
                                (uint64_t)pb.N};
     const uint32_t cbox[5] = {tf ? 32u : 64u, (uint32_t)p.QW, (uint32_t)p.MH, 1u, 1u};
-    const uint64_t bdims[2] = {(uint64_t)pb.C_in * (tf ? 2 : 1), (uint64_t)pl.wq.nblk * pb.C_out};
-    const uint64_t bstr[1] = {(uint64_t)pb.C_in * vb};
+    const uint64_t bdims[2] = {(uint64_t)pb.C_in, (uint64_t)pl.wq.nblk * pb.C_out};
+    const uint64_t bstr[1] = {(uint64_t)pb.C_in * 4};
     if (!encode_tiled(&tmXc, tf ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, xc,
                       cdims, astr, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     for (int len = 1; len <= 4; ++len) {
         // lengths beyond the longest run keep a valid map of the longest box
         const int l = len <= pl.maxlen ? len : pl.maxlen;
-        const uint32_t bbox[2] = {32u, (uint32_t)(p.bmul * l * pb.C_out)};
+        const uint32_t bbox[2] = {32u, (uint32_t)(2 * l * pb.C_out)};
         if (!encode_tiled(&tmW[len - 1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, wp, bdims, bstr, bbox,
                           CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;

@@ -300,7 +300,8 @@ class Runner:
         # repack alone)
         in_sp = int(np.prod(c["L_in"]))
         self.launches_per_step = {"umma_bf16": 2 if (in_sp % 8 == 0 or self.cl) else 3, "tc3d_tf32x3": 2,
-                                  "tc3dg_tf32x3": 2, "tc3d_bf16x2": 2, "tc3dg_bf16x2": 2}.get(self.path, 1)
+                                  "tc3dg_tf32x3": 2, "tc3s_tf32x3": 2, "tc3d_bf16x2": 2, "tc3dg_bf16x2": 2,
+                                  "tc3s_bf16x2": 2}.get(self.path, 1)
 
     def forward(self, stream, d=None, y=None):
         c, ct = self.cfg, self.ct
@@ -506,7 +507,8 @@ def roofline(name, cfg, path, wm, sec, peaks):
         return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peaks["source"] + " cuBLAS bf16 burst"}
-    if path in ("tc1d_tf32x3", "tc3d_tf32x3", "tc3dg_tf32x3", "tc3d_bf16x2", "tc3dg_bf16x2"):
+    if path in ("tc1d_tf32x3", "tc3d_tf32x3", "tc3dg_tf32x3", "tc3s_tf32x3", "tc3d_bf16x2", "tc3dg_bf16x2",
+                "tc3s_bf16x2"):
         # FP32 on the tensor cores.  The tf32x3 kernels do 3 tf32 products per
         # multiply-add at the tf32 rate (half the bf16 rate): the time of 6 bf16
         # products; the opt-in bf16x2 kernels 2 bf16 MMAs over twice the K: the
@@ -584,7 +586,8 @@ def run_gpu_arm(args, ws, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(r.cfg, r.path),
         "data": "synthetic (seeded numpy PCG64; x~N(0,1), w~U(-b,b))",
         "config": {"workload": (name if args.batch is None else "%s (batch %d)" % (name, args.batch)) +
-                   (" [CT_F32_BF16X2 opt-in]" if r.split2 else ""),
+                   (" [CT_F32_BF16X2 opt-in]" if r.split2 else "") +
+                   (" [path override %d]" % args.path_override if args.path_override else ""),
                    "desc": r.cfg["desc"], "global_batch": r.cfg["N"] * ws,
                    "parallelism": "replicas" if ws > 1 else "single",
                    "l2": ("inputs larger than L2 (%.0f MB per step)" % (wm["bytes"] / 1e6)) if big
@@ -793,6 +796,18 @@ def main(argv=None):
                     print(json.dumps(res), flush=True)
                 if not has_opt_in:
                     break
+            if name in ("convT3d_s3_disjoint", "convT3d_s3_k5"):
+                # the generic gather kernel these shapes took before, for comparison
+                a2 = argparse.Namespace(**vars(args))
+                a2.config = name
+                a2.path_override = 1
+                res, r = run_gpu_arm(a2, ws, rank, local)
+                del r
+                torch.cuda.empty_cache()
+                if rank == 0:
+                    print(json.dumps(res), flush=True)
+                ct_mod = __import__("transposed_convolution_convtranspose_gb300")
+                ct_mod.ct_set_path_override(0)
         return 0
 
     res, r = run_gpu_arm(args, ws, rank, local)

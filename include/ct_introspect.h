@@ -15,6 +15,9 @@
  *   "tc3dg_tf32x3"    FP32 2-D / 3-D, 32 input channels in 1, 2 or 4 groups,
  *                     tensor cores, tf32 split
  *   "tc3dg_bf16x2"    the same with the opt-in two-term bf16 split
+ *   "tc3s_tf32x3"     FP32 1-D / 2-D / 3-D with strides 1 to 4 and any
+ *                     dilation (groups 1), tensor cores, tf32 split
+ *   "tc3s_bf16x2"     the same with the opt-in two-term bf16 split
  *   "umma_bf16"       bf16 2-D / 3-D on the tensor cores
  */
 #ifndef CT_INTROSPECT_H

@@ -56,7 +56,8 @@ REDUCED = {"convT1d_tiny": dict(N=2), "convT1d_L131072": dict(N=1),
            "convT3d_grouped": dict(N=2), "convT3d_add_hswish": dict(N=2),
            "convT3d_bf16_dense": dict(N=1, L=[8, 8, 8]), "convT2d_f32": dict(N=1),
            "convT2d_bf16_dense": dict(N=1, L=[32, 32]), "convT3d_bf16_dense_cl": dict(N=1, L=[8, 8, 8]),
-           "convT3d_add_hswish_cl": dict(N=2)}
+           "convT3d_add_hswish_cl": dict(N=2), "convT3d_s3_disjoint": dict(N=1, L=[8, 8, 8]),
+           "convT3d_s3_k5": dict(N=1, L=[8, 8, 8])}
 
 
 @pytest.mark.parametrize("name", CONFIGS)
@@ -453,6 +454,51 @@ def test_disjoint_phase_shapes_exact(k):
     ref = cc.run_oracle(c, t)
     assert y.shape == ref.shape
     assert np.array_equal(y.astype(np.float64), ref), "disjoint case %d (%s) not exact" % (k, path_of(c))
+
+
+# The FP32 tensor-core path for strides 1 to 4 and any dilation (one residue
+# pair per unit, the W phases as accumulators): stride 3 with k = s (every
+# output one tap, disjoint phases), stride 3 with overlapping k = 5, stride 4
+# with k = 2 (residues without a tap: bias only), mixed strides (1, 3, 2) with
+# dilation 2, stride 2 with kernel 5, stride 1, 2-D and long 1-D shapes (W
+# split into several unit blocks), and the fused epilogue with several W
+# blocks.  Random inputs within the FP32 tolerance; integer inputs exact.
+TC3S = [
+    dict(nd=3, N=1, C_in=32, C_out=32, L=[3, 4, 4], K=[3, 3, 3], S=[3, 3, 3], P=[0, 0, 0], OP=[0, 0, 0],
+         DL=[1, 1, 1], add=False),
+    dict(nd=3, N=1, C_in=32, C_out=16, L=[2, 3, 4], K=[5, 5, 5], S=[3, 3, 3], P=[2, 2, 2], OP=[1, 1, 2],
+         DL=[1, 1, 1], add=True),
+    dict(nd=3, N=2, C_in=32, C_out=32, L=[2, 3, 4], K=[2, 2, 2], S=[4, 4, 4], P=[0, 0, 0], OP=[1, 0, 2],
+         DL=[1, 1, 1], add=False),
+    dict(nd=3, N=1, C_in=64, C_out=48, L=[3, 4, 6], K=[2, 3, 3], S=[1, 3, 2], P=[0, 1, 1], OP=[0, 2, 1],
+         DL=[1, 2, 1], add=False),
+    dict(nd=3, N=1, C_in=64, C_out=32, L=[3, 4, 8], K=[5, 5, 5], S=[2, 2, 2], P=[2, 2, 2], OP=[1, 1, 1],
+         DL=[1, 1, 1], add=True),
+    dict(nd=2, N=2, C_in=32, C_out=64, L=[5, 8], K=[3, 3], S=[3, 3], P=[1, 1], OP=[0, 2], DL=[1, 1], add=False),
+    dict(nd=1, N=2, C_in=32, C_out=32, L=[300], K=[3], S=[4], P=[0], OP=[1], DL=[1], add=False),
+    dict(nd=2, N=1, C_in=32, C_out=32, L=[6, 12], K=[3, 3], S=[1, 1], P=[1, 1], OP=[0, 0], DL=[1, 1], add=False),
+    dict(nd=3, N=1, C_in=32, C_out=16, L=[2, 2, 40], K=[3, 3, 3], S=[3, 3, 3], P=[0, 0, 0], OP=[0, 0, 0],
+         DL=[1, 1, 1], add=True),
+    dict(nd=3, N=3, C_in=32, C_out=128, L=[4, 4, 4], K=[4, 4, 4], S=[4, 4, 4], P=[0, 0, 0], OP=[0, 0, 0],
+         DL=[1, 1, 1], add=False),
+]
+
+
+@pytest.mark.parametrize("k", range(len(TC3S)))
+def test_fp32_any_stride_tensor_core_shapes(k):
+    c = dict(G=1, bias=bool(k % 2 == 0), dtype="f32", **TC3S[k])
+    assert path_of(c) == "tc3s_tf32x3", (c, path_of(c))
+    t = cc.make_inputs(c, seed=1800 + k)
+    y = cc.run_gpu(c, t).cpu().numpy()
+    cc.assert_close(y, cc.run_oracle(c, t), "f32", "tc3s case %d %r" % (k, c))
+    if not c["add"]:
+        ti = cc.make_inputs(c, seed=1850 + k, int_range=3)
+        yi = cc.run_gpu(c, ti).cpu().numpy()
+        assert np.array_equal(yi.astype(np.float64), cc.run_oracle(c, ti)), "tc3s integer case %d" % k
+    if k in (0, 2):
+        c2 = dict(c, split2=True)
+        assert path_of(c2) == "tc3s_bf16x2", path_of(c2)
+        cc.assert_close(cc.run_gpu(c2, t).cpu().numpy(), cc.run_oracle(c, t), "f32", "tc3s bf16x2 case %d" % k)
 
 
 # Channels-last layouts (x (N, spatial..., C_in), y and add (N, spatial...,

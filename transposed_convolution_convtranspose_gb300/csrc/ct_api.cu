@@ -130,7 +130,7 @@ ct_status make_problem(int nd, int N, int C_in, int C_out, const int *Li, const 
     return CT_OK;
 }
 
-enum class Path { Generic, Phase1d, Phase3d, Umma, Tc1d, Tc3d, Tc3dg };
+enum class Path { Generic, Phase1d, Phase3d, Umma, Tc1d, Tc3d, Tc3dg, Tc3s };
 
 Path choose_path(const Problem &pb, const Args *a)
 {
@@ -146,8 +146,15 @@ Path choose_path(const Problem &pb, const Args *a)
             return Path::Tc3d;
         return Path::Generic;
     }
+    // the FP32 tensor-core paths with scratch need the caller's workspace: a call
+    // without it takes the kernels that need none (a query without arguments,
+    // a == NULL, reports the tensor-core path and its workspace size)
+    auto has_ws = [&](size_t need) {
+        return !a || (a->ws && ((uintptr_t)a->ws % 256) == 0 && a->ws_bytes >= need);
+    };
     if (pb.dtype == CT_F32) {
         if (ov != 2 && pb.nd == 1 && tc1d_supported(pb, a)) return Path::Tc1d;
+        if (ov != 2 && pb.nd == 1 && tc3s_supported(pb, a) && has_ws(tc3s_workspace_bytes(pb))) return Path::Tc3s;
         if (pb.nd == 1 && phase1d_supported(pb, a)) return Path::Phase1d;
         // the 3-D tensor-core path works in the caller's workspace: a call without
         // enough of it takes the FFMA kernel (a query without arguments, a == NULL,
@@ -159,6 +166,8 @@ Path choose_path(const Problem &pb, const Args *a)
         if (ov != 2 && pb.nd >= 2 && tc3dg_supported(pb, a) &&
             (!a || (a->ws && ((uintptr_t)a->ws % 256) == 0 && a->ws_bytes >= tc3dg_workspace_bytes(pb))))
             return Path::Tc3dg;
+        // strides 1 to 4, any dilation, groups 1
+        if (ov != 2 && pb.nd >= 2 && tc3s_supported(pb, a) && has_ws(tc3s_workspace_bytes(pb))) return Path::Tc3s;
         if (pb.nd >= 2 && phase3d_supported(pb, a)) return Path::Phase3d;
     } else {
         if (pb.nd >= 2 && umma_supported(pb, a)) return Path::Umma;
@@ -176,6 +185,7 @@ const char *path_name(Path p, const Problem &pb)
     case Path::Tc1d: return "tc1d_tf32x3";
     case Path::Tc3d: return pb.split2 ? "tc3d_bf16x2" : "tc3d_tf32x3";
     case Path::Tc3dg: return pb.split2 ? "tc3dg_bf16x2" : "tc3dg_tf32x3";
+    case Path::Tc3s: return pb.split2 ? "tc3s_bf16x2" : "tc3s_tf32x3";
     }
     return "gather_generic";
 }
@@ -189,6 +199,7 @@ size_t workspace_bytes(const Problem &pb)
     case Path::Umma: return umma_workspace_bytes(pb);
     case Path::Tc3d: return tc3d_workspace_bytes(pb);
     case Path::Tc3dg: return tc3dg_workspace_bytes(pb);
+    case Path::Tc3s: return tc3s_workspace_bytes(pb);
     default: return 0;
     }
 }
@@ -241,6 +252,7 @@ ct_status run(const Problem &pb, Args a)
     case Path::Tc1d: e = launch_tc1d(pb, a); break;
     case Path::Tc3d: e = launch_tc3d(pb, a); break;
     case Path::Tc3dg: e = launch_tc3dg(pb, a); break;
+    case Path::Tc3s: e = launch_tc3s(pb, a); break;
     }
     return e == cudaSuccess ? CT_OK : CT_ERR_CUDA;
 }

@@ -77,6 +77,13 @@ bool tc3d_supported(const Problem &pb, const Args *a);
 size_t tc3d_workspace_bytes(const Problem &pb);
 cudaError_t launch_tc3d(const Problem &pb, const Args &a);
 
+// ---- FP32 1-D / 2-D / 3-D with strides 1 to 4 and any dilation (groups 1) on
+// the tensor cores (3-term tf32 split, or the two-term bf16 split when opted
+// into; one residue pair (rD, rH) per unit; workspace) ----
+bool tc3s_supported(const Problem &pb, const Args *a);
+size_t tc3s_workspace_bytes(const Problem &pb);
+cudaError_t launch_tc3s(const Problem &pb, const Args &a);
+
 // ---- FP32 3-D, 32 input channels in 1/2/4 groups, on the tensor cores
 // (3-term tf32 split, or the two-term bf16 split when opted into; one
 // MMA-issuing warp per group; workspace) ----

@@ -80,11 +80,27 @@ CONFIGS = {
         stride=(2, 2, 2), padding=(1, 1, 1), output_padding=(1, 1, 1), dilation=(1, 1, 1),
         bias=True, add=True, out_shape=(128, 64, 32, 32, 32), dtype="f32",
         bound=1.0 / math.sqrt(64 * 27), seed=4, layout="cl"),
+    # strides other than 2 (the l1_p79 "wavefronts" passage: s phases per
+    # dimension with disjoint writes): no page states such a size, so these
+    # take the grouped workload's 16^3 input with 32 -> 32 channels.  k = s = 3
+    # lies in the disjoint regime s > (k - 1) d (every output receives exactly
+    # one tap per dimension); k = 5, s = 3, p = 1 has overlapping phases (1 or
+    # 2 taps per dimension)
+    "convT3d_s3_disjoint": dict(
+        desc="ConvTranspose3d fp32 N=16 C_in=32 C_out=32 k=3 s=3 p=0 in=16^3 (out 48^3) bias",
+        nd=3, N=16, C_in=32, C_out=32, groups=1, L_in=(16, 16, 16), k=(3, 3, 3),
+        stride=(3, 3, 3), padding=(0, 0, 0), output_padding=(0, 0, 0), dilation=(1, 1, 1),
+        bias=True, add=False, dtype="f32", bound=1.0 / math.sqrt(32 * 27), seed=8),
+    "convT3d_s3_k5": dict(
+        desc="ConvTranspose3d fp32 N=16 C_in=32 C_out=32 k=5 s=3 p=1 in=16^3 (out 48^3) bias",
+        nd=3, N=16, C_in=32, C_out=32, groups=1, L_in=(16, 16, 16), k=(5, 5, 5),
+        stride=(3, 3, 3), padding=(1, 1, 1), output_padding=(0, 0, 0), dilation=(1, 1, 1),
+        bias=True, add=False, dtype="f32", bound=1.0 / math.sqrt(32 * 125), seed=9),
 }
 
 CONFIG_ORDER = ["convT1d_tiny", "convT1d_L131072", "convT3d_grouped",
                 "convT3d_add_hswish", "convT3d_bf16_dense", "convT2d_f32", "convT2d_bf16_dense",
-                "convT3d_bf16_dense_cl", "convT3d_add_hswish_cl"]
+                "convT3d_bf16_dense_cl", "convT3d_add_hswish_cl", "convT3d_s3_disjoint", "convT3d_s3_k5"]
 
 
 def bf16_round(a):

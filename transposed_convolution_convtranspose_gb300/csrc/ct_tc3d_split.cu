@@ -92,6 +92,7 @@ constexpr int NPA = 2;           // A producer warps: warp q loads the A stages 
 constexpr int NPB = 2;           // B producer warps: warp q loads the B stages g with g mod NPB == q
 constexpr int MAXE = 18;         // input offsets per D residue (2 x 3 x 3 for extents <= 4)
 constexpr int MAXR = 64;         // runs per D residue
+constexpr int MAXSTEP = 320;     // MMA steps (B stages) per D residue
 constexpr int EPW = 4;           // epilogue warps per TMEM lane quarter (H phase x channel half)
 constexpr int kAWarp0 = 0;
 constexpr int kBWarp0 = kAWarp0 + NPA;
@@ -117,6 +118,14 @@ struct Run {
     int8_t p0, len, fresh, pad;
     int brow;
 };
+// One B stage of the issuer's schedule, in issue order (entries, then K
+// blocks, then runs): flags bit 0 -- a new A stage starts here (wait for it),
+// bit 1 -- the A stage is done after this one (release it), bit 2 -- the first
+// MMA writes its accumulators; len: run length; col: first TMEM column.
+struct Step {
+    uint8_t flags, len;
+    uint16_t col;
+};
 
 struct T3Params {
     int N, C_in, C_out;
@@ -134,8 +143,10 @@ struct T3Params {
     uint32_t idesc_b[5];         // instruction descriptor for N = len x C_out, len 1..4
     int8_t slot[4];              // accumulator slot of phase (rH, rW) = index 2 rH + rW
     int nE[2];
+    int nstep[2];
     Entry ent[2][MAXE];
     Run run[2][MAXR];
+    Step step[2][MAXSTEP];
 };
 
 
@@ -300,65 +311,71 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             const int na = p.na;
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
+            // instruction descriptors by run length, held in registers
+            const uint32_t id1 = p.idesc_b[1], id2 = p.idesc_b[2], id3 = p.idesc_b[3], id4 = p.idesc_b[4];
             for (int k = 0; k < nunit_cta && ok; ++k) {
                 const int rd = unit_coord((int)blockIdx.x + k * (int)gridDim.x, p).rd;
                 const int a = p.nacc == 2 ? (k & 1) : 0;
                 const int use = p.nacc == 2 ? (k >> 1) : k;     // earlier units in accumulator set a
+                const int nst = p.nstep[rd];
+                Step nxt = p.step[rd][0];
                 if (use > 0 && !dev::mbar_wait_bounded(&acc_empty[a], (use - 1) & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after();
                 const uint32_t d = tmem + (uint32_t)a * p.acc_cols;
-                const int ne = p.nE[rd];
-                for (int e = 0; e < ne && ok; ++e) {
-                    const Entry &en = p.ent[rd][e];
-                    for (int kb = 0; kb < n_kb && ok; ++kb) {
+                uint64_t da = 0;
+                // one flat schedule per residue; the next step's record is read while
+                // this one waits and issues
+                for (int i = 0; i < nst && ok; ++i) {
+                    const Step st = nxt;
+                    if (i + 1 < nst) nxt = p.step[rd][i + 1];
+                    if (st.flags & 1u) {
                         if (!dev::mbar_wait_bounded(&a_full[sa], pa, kWaitLimitNs)) {
                             ok = false;
                             break;
                         }
                         tc::fence_after();
-                        const uint64_t da = tc::desc_sw128(sAb + (uint32_t)sa * aslot);
-                        for (int j = 0; j < en.nrun; ++j) {
-                            const Run &ru = p.run[rd][en.run0 + j];
-                            if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
-                                ok = false;
-                                break;
-                            }
-                            tc::fence_after();
-                            const uint32_t bh = sBb + (uint32_t)sb * bslot;
-                            const uint64_t dbh = tc::desc_sw128(bh);
-                            const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(ru.len * C_out) * 128u);
-                            const uint32_t idb = p.idesc_b[ru.len];
-                            const uint32_t dd = d + (uint32_t)(ru.p0 * C_out);
-                            const uint32_t acc0 = (ru.fresh && kb == 0) ? 0u : 1u;
-                            if (TF) {
-                                // K step kk: 8 channels, 32 bytes of the t rows (A, and the
-                                // panel's t rows) and of the l rows (A 16 KB further, the
-                                // panel's l rows after its t rows); descriptor units of 16 bytes
-                                const uint64_t dal = da + (kAHalf >> 4);
+                        da = tc::desc_sw128(sAb + (uint32_t)sa * aslot);
+                    }
+                    if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t bh = sBb + (uint32_t)sb * bslot;
+                    const uint64_t dbh = tc::desc_sw128(bh);
+                    const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(st.len * C_out) * 128u);
+                    const uint32_t idb = st.len == 1 ? id1 : st.len == 2 ? id2 : st.len == 3 ? id3 : id4;
+                    const uint32_t dd = d + (uint32_t)st.col;
+                    const uint32_t acc0 = (st.flags & 4u) ? 0u : 1u;
+                    if (TF) {
+                        // K step kk: 8 channels, 32 bytes of the t rows (A, and the
+                        // panel's t rows) and of the l rows (A 16 KB further, the
+                        // panel's l rows after its t rows); descriptor units of 16 bytes
+                        const uint64_t dal = da + (kAHalf >> 4);
 #pragma unroll
-                                for (int kk = 0; kk < CK / 8; ++kk) {
-                                    tc::mma_tf32(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x_t w_t
-                                    tc::mma_tf32(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x_t w_l
-                                    tc::mma_tf32(dd, dal + 2 * kk, dbh + 2 * kk, idb, 1u);            // x_l w_t
-                                }
-                            } else {
-#pragma unroll
-                                for (int kk = 0; kk < CK / 8; ++kk) {
-                                    // 32 bytes along K inside the swizzle atom: 16 bf16, the
-                                    // hi and lo parts of 8 channels
-                                    tc::mma_bf16(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x * w_hi
-                                    tc::mma_bf16(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x * w_lo
-                                }
-                            }
-                            tc::commit(&b_empty[sb]);
-                            if (++sb == NB) {
-                                sb = 0;
-                                pb ^= 1u;
-                            }
+                        for (int kk = 0; kk < CK / 8; ++kk) {
+                            tc::mma_tf32(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x_t w_t
+                            tc::mma_tf32(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x_t w_l
+                            tc::mma_tf32(dd, dal + 2 * kk, dbh + 2 * kk, idb, 1u);            // x_l w_t
                         }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < CK / 8; ++kk) {
+                            // 32 bytes along K inside the swizzle atom: 16 bf16, the
+                            // hi and lo parts of 8 channels
+                            tc::mma_bf16(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x * w_hi
+                            tc::mma_bf16(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x * w_lo
+                        }
+                    }
+                    tc::commit(&b_empty[sb]);
+                    if (++sb == NB) {
+                        sb = 0;
+                        pb ^= 1u;
+                    }
+                    if (st.flags & 2u) {
                         tc::commit(&a_empty[sa]);
                         if (++sa == na) {
                             sa = 0;
@@ -728,6 +745,25 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     double c = 0;
     if (!plan_runs(pb, SD, nt, tk, td, uo, nu, kPerm[bi], maxlen, 2, tf ? 12 : 8, &p, &wq, &c)) return false;
     for (int sl = 0; sl < 4; ++sl) p.slot[kPerm[bi][sl]] = (int8_t)sl;
+    // the issuer's flat schedule per residue: entries, K blocks, runs
+    for (int rd = 0; rd < SD; ++rd) {
+        int ns = 0;
+        for (int e = 0; e < p.nE[rd]; ++e) {
+            const Entry &en = p.ent[rd][e];
+            for (int kb = 0; kb < p.n_kb; ++kb)
+                for (int j = 0; j < en.nrun; ++j) {
+                    if (ns >= MAXSTEP) return false;
+                    const Run &ru = p.run[rd][en.run0 + j];
+                    Step st;
+                    st.flags = (uint8_t)((j == 0 ? 1 : 0) | (j == en.nrun - 1 ? 2 : 0) |
+                                         ((ru.fresh && kb == 0) ? 4 : 0));
+                    st.len = (uint8_t)ru.len;
+                    st.col = (uint16_t)(ru.p0 * pb.C_out);
+                    p.step[rd][ns++] = st;
+                }
+        }
+        p.nstep[rd] = ns;
+    }
     wq.C_in = pb.C_in;
     wq.C_out = pb.C_out;
     wq.ntap = pb.kvol();

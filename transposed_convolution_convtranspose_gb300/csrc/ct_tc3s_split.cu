@@ -68,6 +68,7 @@ constexpr int MAXT = 8;          // taps of one residue of one dimension at most
 constexpr int MAXP = MAXS * MAXS;    // residue pairs (rD, rH)
 constexpr int MAXE = 128;        // input offsets over all pairs
 constexpr int MAXR = 192;        // runs over all pairs
+constexpr int MAXSTEP = 768;     // MMA steps (B stages) over all pairs
 constexpr int kAWarp0 = 0;
 constexpr int kBWarp0 = kAWarp0 + NPA;
 constexpr int kMmaWarp = kBWarp0 + NPB;
@@ -91,6 +92,14 @@ struct SRun {
     int8_t p0, len, fresh, pad;
     int brow;
 };
+// One B stage of the issuer's schedule, in issue order (entries, then K
+// blocks, then runs): flags bit 0 -- a new A stage starts here, bit 1 -- the
+// A stage is done after this one, bit 2 -- the first MMA writes its
+// accumulators; len: run length; col: first TMEM column.
+struct SStep {
+    uint8_t flags, len;
+    uint16_t col;
+};
 
 struct SParams {
     int N, C_in, C_out;
@@ -112,8 +121,10 @@ struct SParams {
     uint8_t wmask[MAXP];         // W phases of pair k that receive a tap (bit rW)
     uint8_t hrows[MAXS];         // 1 if H residue rH has output rows
     int e0[MAXP + 1];            // entries of pair k: ent[e0[k] .. e0[k + 1])
+    int s0[MAXP + 1];            // steps of pair k: step[s0[k] .. s0[k + 1])
     SEntry ent[MAXE];
     SRun run[MAXR];
+    SStep step[MAXSTEP];
 };
 
 struct SUnit {
@@ -269,62 +280,68 @@ tc3s_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             const int na = p.na;
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
+            const uint32_t id1 = p.idesc_b[1], id2 = p.idesc_b[2], id3 = p.idesc_b[3], id4 = p.idesc_b[4];
             for (int k = 0; k < nunit_cta && ok; ++k) {
                 const int rp = s_unit((int)blockIdx.x + k * (int)gridDim.x, p).rp;
                 const int a = p.nacc == 2 ? (k & 1) : 0;
                 const int use = p.nacc == 2 ? (k >> 1) : k;
+                const int i0 = p.s0[rp], i1 = p.s0[rp + 1];
+                SStep nxt = p.step[i0 < i1 ? i0 : 0];
                 if (use > 0 && !dev::mbar_wait_bounded(&acc_empty[a], (use - 1) & 1, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after();
                 const uint32_t d = tmem + (uint32_t)a * p.acc_cols;
-                for (int e = p.e0[rp]; e < p.e0[rp + 1] && ok; ++e) {
-                    const SEntry &en = p.ent[e];
-                    for (int kb = 0; kb < n_kb && ok; ++kb) {
+                uint64_t da = 0;
+                // the pair's flat schedule; the next step's record is read while this
+                // one waits and issues
+                for (int i = i0; i < i1 && ok; ++i) {
+                    const SStep st = nxt;
+                    if (i + 1 < i1) nxt = p.step[i + 1];
+                    if (st.flags & 1u) {
                         if (!dev::mbar_wait_bounded(&a_full[sa], pa, kWaitLimitNs)) {
                             ok = false;
                             break;
                         }
                         tc::fence_after();
-                        const uint64_t da = tc::desc_sw128(sAb + (uint32_t)sa * aslot);
-                        for (int j = 0; j < en.nrun; ++j) {
-                            const SRun &ru = p.run[en.run0 + j];
-                            if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
-                                ok = false;
-                                break;
-                            }
-                            tc::fence_after();
-                            const uint32_t bh = sBb + (uint32_t)sb * bslot;
-                            const uint64_t dbh = tc::desc_sw128(bh);
-                            const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(ru.len * C_out) * 128u);
-                            const uint32_t idb = p.idesc_b[ru.len];
-                            const uint32_t dd = d + (uint32_t)(ru.p0 * C_out);
-                            const uint32_t acc0 = (ru.fresh && kb == 0) ? 0u : 1u;
-                            if (TF) {
-                                // K step kk: 8 channels, 32 bytes of the t rows (A, and the
-                                // panel's t rows) and of the l rows (A 16 KB further, the
-                                // panel's l rows after its t rows)
-                                const uint64_t dal = da + (kAHalf >> 4);
+                        da = tc::desc_sw128(sAb + (uint32_t)sa * aslot);
+                    }
+                    if (!dev::mbar_wait_bounded(&b_full[sb], pb, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t bh = sBb + (uint32_t)sb * bslot;
+                    const uint64_t dbh = tc::desc_sw128(bh);
+                    const uint64_t dbl = tc::desc_sw128(bh + (uint32_t)(st.len * C_out) * 128u);
+                    const uint32_t idb = st.len == 1 ? id1 : st.len == 2 ? id2 : st.len == 3 ? id3 : id4;
+                    const uint32_t dd = d + (uint32_t)st.col;
+                    const uint32_t acc0 = (st.flags & 4u) ? 0u : 1u;
+                    if (TF) {
+                        // K step kk: 8 channels, 32 bytes of the t rows (A, and the
+                        // panel's t rows) and of the l rows (A 16 KB further, the
+                        // panel's l rows after its t rows)
+                        const uint64_t dal = da + (kAHalf >> 4);
 #pragma unroll
-                                for (int kk = 0; kk < CK / 8; ++kk) {
-                                    tc::mma_tf32(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x_t w_t
-                                    tc::mma_tf32(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x_t w_l
-                                    tc::mma_tf32(dd, dal + 2 * kk, dbh + 2 * kk, idb, 1u);            // x_l w_t
-                                }
-                            } else {
-#pragma unroll
-                                for (int kk = 0; kk < CK / 8; ++kk) {
-                                    tc::mma_bf16(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x * w_hi
-                                    tc::mma_bf16(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x * w_lo
-                                }
-                            }
-                            tc::commit(&b_empty[sb]);
-                            if (++sb == NB) {
-                                sb = 0;
-                                pb ^= 1u;
-                            }
+                        for (int kk = 0; kk < CK / 8; ++kk) {
+                            tc::mma_tf32(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x_t w_t
+                            tc::mma_tf32(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x_t w_l
+                            tc::mma_tf32(dd, dal + 2 * kk, dbh + 2 * kk, idb, 1u);            // x_l w_t
                         }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < CK / 8; ++kk) {
+                            tc::mma_bf16(dd, da + 2 * kk, dbh + 2 * kk, idb, kk ? 1u : acc0);   // x * w_hi
+                            tc::mma_bf16(dd, da + 2 * kk, dbl + 2 * kk, idb, 1u);             // x * w_lo
+                        }
+                    }
+                    tc::commit(&b_empty[sb]);
+                    if (++sb == NB) {
+                        sb = 0;
+                        pb ^= 1u;
+                    }
+                    if (st.flags & 2u) {
                         tc::commit(&a_empty[sa]);
                         if (++sa == na) {
                             sa = 0;
@@ -639,6 +656,26 @@ bool make_splan(const Problem &pb, const Args *a, SPlan *out)
     double c = 0;
     if (!plan_pairs(pb, dt, uo, nuo, kPerm[bi], maxlen, tf ? 12 : 8, &p, &wq, &c)) return false;
     for (int sl = 0; sl < p.SW; ++sl) p.slot[kPerm[bi][sl]] = (int8_t)sl;
+    // the issuer's flat schedule per pair: entries, K blocks, runs
+    int ns = 0;
+    for (int rp = 0; rp < p.nrp; ++rp) {
+        p.s0[rp] = ns;
+        for (int e = p.e0[rp]; e < p.e0[rp + 1]; ++e) {
+            const SEntry &en = p.ent[e];
+            for (int kb = 0; kb < p.n_kb; ++kb)
+                for (int j = 0; j < en.nrun; ++j) {
+                    if (ns >= MAXSTEP) return false;
+                    const SRun &ru = p.run[en.run0 + j];
+                    SStep st;
+                    st.flags = (uint8_t)((j == 0 ? 1 : 0) | (j == en.nrun - 1 ? 2 : 0) |
+                                         ((ru.fresh && kb == 0) ? 4 : 0));
+                    st.len = (uint8_t)ru.len;
+                    st.col = (uint16_t)(ru.p0 * pb.C_out);
+                    p.step[ns++] = st;
+                }
+        }
+    }
+    p.s0[p.nrp] = ns;
     wq.C_in = pb.C_in;
     wq.C_out = pb.C_out;
     wq.ntap = pb.kvol();

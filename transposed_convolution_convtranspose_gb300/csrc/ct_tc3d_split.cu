@@ -50,22 +50,27 @@
 //   warps 0-1   TMA producers of the A ring (x_c 5-D boxes of 128 positions
 //               x 128 bytes of channels at the offset; boxes reaching outside
 //               the input read zeros, which is the boundary handling)
-//   warps 2-3   TMA producers of the B ring (a run's panel is one box).  Each
-//               ring slot has exactly one producer, which refills it only after
-//               waiting for its previous round, so a parity wait never has to
-//               tell two phases apart
+//   warps 2-3   TMA producers of the B ring (a run's panel is two boxes: its
+//               hi / t rows, then its lo / l rows).  Each ring slot has
+//               exactly one producer, which refills it only after waiting for
+//               its previous round, so a parity wait never has to tell two
+//               phases apart
 //   warp 4      TMEM allocation and MMA issue
-//   warps 5-20  epilogue, in chunks of 16 channels of a unit (16 channels x
-//               the unit's 2 MH output rows x the whole W extent, 32 KB): the
-//               add values arrive in one of three shared-memory buffers by a
-//               TMA load two chunks ahead; warp w reads TMEM lane quarter
-//               w mod 4 for one H phase and 8 channels, adds bias (and
-//               applies the fused epilogue) in place, writing each position's
-//               even and odd W outputs as one float2
-//   warp 21     chunk mover: makes chunks ready two ahead (the TMA load of the
-//               add values, or the release of the buffer) and stores each
-//               written chunk with one TMA store (rows and planes past the
-//               output are clipped)
+//   warps 5-20  epilogue, in chunks of 16 channels of a unit; warp w reads TMEM
+//               lane quarter w mod 4 for one H phase and 8 channels and adds
+//               bias (and applies the fused epilogue) to each position's even
+//               and odd W outputs, one float2.  Fused and channels first, the
+//               warps load the add values from global memory a chunk ahead and
+//               store y straight from registers (a warp's store covers whole
+//               128-byte segments), so the kernel needs no staging buffers and
+//               its B slots hold runs of N = 256.  Otherwise each chunk (16
+//               channels x the unit's 2 MH output rows x the whole W extent,
+//               32 KB) is staged in one of three shared-memory buffers, the add
+//               values arriving there by a TMA load two chunks ahead
+//   warp 21     chunk mover (staged epilogue): makes chunks ready two ahead
+//               (the TMA load of the add values, or the release of the buffer)
+//               and stores each written chunk with one TMA store (rows and
+//               planes past the output are clipped)
 // Every mbarrier wait is bounded: a timeout records CT_ERR_DEVICE_TIMEOUT in
 // the device status word and the roles unwind (each producer waits, bounded,
 // for its own TMA copies and the MMA issuer for its own MMAs before the TMEM
@@ -183,7 +188,8 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                  const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
                  const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmW4,
                  const __grid_constant__ CUtensorMap tmAdd, const __grid_constant__ CUtensorMap tmY,
-                 const float *__restrict__ bias, const __grid_constant__ T3Params p, unsigned int *status)
+                 const float *__restrict__ bias, const float *add_g, float *y_g,
+                 const __grid_constant__ T3Params p, unsigned int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t a_full[NA], a_empty[NA], b_full[NB], b_empty[NB], acc_full[2],
@@ -193,7 +199,7 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = sm;                                  // na x aslot
     uint8_t *sB = sm + (size_t)p.na * p.aslot;         // NB x bslot
-    uint8_t *sE = sB + NB * p.bslot;                   // NE x kEChunk
+    uint8_t *sE = sB + NB * p.bslot;                   // NE x kEChunk (channels last only)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -276,13 +282,16 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                                         dev::tma_load_5d(dst + kAHalf, &tmXc, &fullb[s], kb * 64 + 32, en.dw,
                                                          qh0 + en.dh, u.qd + en.dd, u.n);
                                 } else {
-                                    // the run's panel exactly: a box of 2 x len x C_out rows (hi / t
-                                    // rows, then lo / l rows) of the K block's 128 bytes
+                                    // the run's panel exactly: two boxes of len x C_out rows of the
+                                    // K block's 128 bytes, the hi / t rows, then the lo / l rows
                                     const Run &ru = p.run[u.rd][en.run0 + j];
                                     const CUtensorMap *tm = ru.len == 1 ? &tmW1 : ru.len == 2 ? &tmW2
                                                           : ru.len == 3 ? &tmW3 : &tmW4;
-                                    dev::mbar_arrive_expect_tx(&fullb[s], (uint32_t)(2 * ru.len * C_out) * 128u);
-                                    dev::tma_load_2d(sB + (size_t)s * p.bslot, tm, &fullb[s], kb * CK, ru.brow);
+                                    const uint32_t half = (uint32_t)(ru.len * C_out) * 128u;
+                                    uint8_t *dst = sB + (size_t)s * p.bslot;
+                                    dev::mbar_arrive_expect_tx(&fullb[s], 2 * half);
+                                    dev::tma_load_2d(dst, tm, &fullb[s], kb * CK, ru.brow);
+                                    dev::tma_load_2d(dst + half, tm, &fullb[s], kb * CK, ru.brow + ru.len * C_out);
                                 }
                                 last = g;
                             }
@@ -391,7 +400,8 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
     } else if (warp == kStoreWarp) {
-        // ---------------- chunk mover.  Buffer gc mod NE holds chunk gc (16 channels of a
+        if (ADD && !CL) goto done;                  // fused, channels first: the epilogue warps store directly
+        // ---------------- chunk mover (channels last).  Buffer gc mod NE holds chunk gc (16 channels of a
         // unit: 16 x 2 MH rows x the whole W extent, 32 KB).  Chunk gc is made ready
         // two chunks ahead -- its add values loaded by TMA, or (no add) the buffer
         // released -- and stored by TMA once the epilogue warps have written it.
@@ -455,6 +465,92 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         const int cstride = 2 * p.MH * Lo2 / 2;         // float2 between channels of a chunk
         bool ok = true;
         int gc = 0;
+        if (ADD && !CL) {
+            // fused, channels first, straight from the accumulators to y: a thread holds
+            // position m, output row 2 qh + rh, and for 8 channels of a 16-channel
+            // chunk its two W outputs 2 qw, 2 qw + 1 -- one float2 per channel; a
+            // warp's 32 positions are whole runs of a row (QW >= 16), so every store
+            // instruction covers whole 128-byte segments.  The add values of the
+            // next chunk are loaded while this one is computed (and the chunk after
+            // is prefetched into L2), so the add stream keeps a chunk in flight.
+            const int m = ew * 32 + lane;
+            const int qwp = m % p.QW, qhl = m / p.QW;
+            const int64_t sp = (int64_t)p.Lo0 * p.Lo1 * Lo2;
+            // output offset (floats) of the thread's first channel for unit k, or -1
+            auto out_off = [&](int k2) -> int64_t {
+                const UnitCoord v = unit_coord((int)blockIdx.x + k2 * (int)gridDim.x, p);
+                const int od = p.SD * v.qd + v.rd, oh = 2 * (v.qhb * p.MH + qhl) + rh;
+                if (od >= p.Lo0 || oh >= p.Lo1) return -1;
+                return ((int64_t)v.n * C_out * p.Lo0 + od) * p.Lo1 * (int64_t)Lo2 + (int64_t)oh * Lo2 + 2 * qwp;
+            };
+            float2 av[8], an[8];
+            int64_t off = nunit_cta > 0 ? out_off(0) : -1;
+            if (ADD && off >= 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    av[i] = __ldcs(reinterpret_cast<const float2 *>(add_g + off + (int64_t)(ch * 8 + i) * sp));
+            }
+            for (int k = 0; k < nunit_cta; ++k) {
+                const int a = p.nacc == 2 ? (k & 1) : 0;
+                const int use = p.nacc == 2 ? (k >> 1) : k;
+                const int64_t off_next = k + 1 < nunit_cta ? out_off(k + 1) : -1;
+                if (ok && !dev::mbar_wait_bounded(&acc_full[a], use & 1, kWaitLimitNs)) {
+                    atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
+                    ok = false;
+                }
+                ok = __all_sync(0xffffffffu, ok);        // warp-uniform before .sync.aligned loads
+                tc::fence_after();
+                const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols;
+                for (int c = 0; c < nchunk; ++c) {
+                    const int c0 = c * 16 + ch * 8;             // this warp's first channel
+                    float v0[8], v1[8];
+                    if (ok) {
+                        // the accumulators of phases (rh, 0) and (rh, 1)
+                        tc::tmem_ld8(tbase + (uint32_t)(p.slot[rh * 2] * C_out + c0), v0);
+                        tc::tmem_ld8(tbase + (uint32_t)(p.slot[rh * 2 + 1] * C_out + c0), v1);
+                    }
+                    // the next chunk's add values (this unit's, or the next unit's first)
+                    const int64_t noff = c + 1 < nchunk ? (off >= 0 ? off + (int64_t)16 * sp : -1) : off_next;
+                    const int nc0 = c + 1 < nchunk ? c0 + 16 : ch * 8;
+                    if (ADD && noff >= 0) {
+                        const int64_t base = c + 1 < nchunk ? off : off_next;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            an[i] = __ldcs(reinterpret_cast<const float2 *>(add_g + base + (int64_t)(nc0 + i) * sp));
+                    }
+                    if (ADD && c + 2 < nchunk) {
+                        // two chunks ahead, into L2: the warp's 8 channels cover two
+                        // 128-byte lines each (positions of lanes 0-15 and 16-31); lane l
+                        // < 16 prefetches line l & 1 of channel l >> 1
+                        const int64_t src = __shfl_sync(0xffffffffu, off, (lane & 1) * 16);
+                        if (lane < 16 && src >= 0)
+                            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(add_g + src + (int64_t)(c0 + 32 + (lane >> 1)) * sp));
+                    }
+                    tc::tmem_wait_ld();
+                    if (c == nchunk - 1) {                  // the unit's last loads: free the accumulators
+                        tc::fence_before();
+                        dev::mbar_arrive(&acc_empty[a]);
+                    }
+                    if (ok && off >= 0) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float bb = s_bias[c0 + i];
+                            float t0 = v0[i] + bb, t1 = v1[i] + bb;
+                            if (ADD) {
+                                t0 = add_hswish(t0, av[i].x);
+                                t1 = add_hswish(t1, av[i].y);
+                            }
+                            __stcs(reinterpret_cast<float2 *>(y_g + off + (int64_t)(c0 + i) * sp), make_float2(t0, t1));
+                        }
+                    }
+                    if (ADD) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) av[i] = an[i];
+                    }
+                    if (c + 1 == nchunk) off = off_next;
+                }
+            }
+        } else {
         for (int k = 0; k < nunit_cta; ++k) {
             const int a = p.nacc == 2 ? (k & 1) : 0;
             const int use = p.nacc == 2 ? (k >> 1) : k;
@@ -543,8 +639,10 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                 dev::mbar_arrive(&c_full[b]);
             }
         }
+        }
     }
 
+done:
     __syncwarp();
     tc::fence_before();
     __syncthreads();
@@ -686,7 +784,7 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     p.QH = (p.Lo1 + 1) / 2;
     p.n_qhb = (p.QH + p.MH - 1) / p.MH;
     p.n_kb = pb.C_in / CK;
-    p.na = tf ? 2 : NA;
+    p.na = NA;                   // reduced to fit below
     p.aslot = (tf ? 2 : 1) * kAHalf;
     const int64_t units = (int64_t)pb.N * p.QD * p.n_qhb * SD;
     if (units > 0x7fffffff || units == 0) return false;
@@ -716,10 +814,26 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
                     uo[d][nu[d]++] = td[d][r][j];
                 }
             }
-    // runs of adjacent accumulators: at most 4 phases, N = len x C_out <= 256 and
-    // a panel of 2 x len x C_out rows <= 256 (one TMA box)
-    const int ml = 128 / pb.C_out;
-    const int maxlen = ml < 4 ? ml : 4;
+    // runs of adjacent accumulators: at most 4 phases, N = len x C_out <= 256 (a
+    // panel is two boxes of len x C_out rows).
+    // fused and channels first, the epilogue stores from registers (no staging
+    // buffers): B slots of 256 panel rows (runs of N = 256); otherwise the
+    // staging buffers leave room for 128 rows
+    const bool direct = pb.has_add && !pb.cl;
+    int maxlen = (direct ? 256 : 128) / pb.C_out;
+    if (maxlen > 4) maxlen = 4;
+    // shared memory: A ring, B ring (slots of the longest run's panel) and, channels
+    // last, the epilogue's staging buffers; a ring of four A slots gives way to
+    // two, then runs get shorter, until they fit
+    {
+        const size_t ebytes = direct ? 0 : (size_t)NE * kEChunk;
+        const size_t budget = 227 * 1024 - 2048;   // room for the alignment pad and the static barriers
+        while ((size_t)p.na * p.aslot + (size_t)NB * (2 * maxlen * pb.C_out) * 128 + ebytes > budget) {
+            if (p.na > 2) p.na = 2;
+            else if (maxlen > 1) --maxlen;
+            else return false;
+        }
+    }
     // the order of the four accumulators with the cheapest MMA schedule (the
     // first of equal ones, so the natural order when it is as good)
     static const int kPerm[24][4] = {
@@ -776,7 +890,7 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     while (cols < (uint32_t)p.nacc * p.acc_cols) cols <<= 1;
     p.tmem_cols = cols;
     p.bslot = (uint32_t)(2 * maxlen * pb.C_out) * 128u;
-    const size_t smem = (size_t)p.na * p.aslot + (size_t)NB * p.bslot + (size_t)NE * kEChunk + 1024;
+    const size_t smem = (size_t)p.na * p.aslot + (size_t)NB * p.bslot + (direct ? 0 : (size_t)NE * kEChunk) + 1024;
     if (smem > 227 * 1024 - 1024) return false;   // room for the static barriers
     out->p = p;
     out->wq = wq;
@@ -851,7 +965,7 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     for (int len = 1; len <= 4; ++len) {
         // lengths beyond the longest run keep a valid map of the longest box
         const int l = len <= pl.maxlen ? len : pl.maxlen;
-        const uint32_t bbox[2] = {32u, (uint32_t)(2 * l * pb.C_out)};
+        const uint32_t bbox[2] = {32u, (uint32_t)(l * pb.C_out)};
         if (!encode_tiled(&tmW[len - 1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, wp, bdims, bstr, bbox,
                           CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
@@ -905,7 +1019,7 @@ cudaError_t launch_tc3d(const Problem &pb, const Args &a)
     const dim3 gd((unsigned)grid), bd(kThreads);
 #define CT_TC3D_LAUNCH(ADD_, CL_, TF_)                                                                       \
     launch_dependent(tc3d_split_kernel<ADD_, CL_, TF_>, gd, bd, pl.smem, a.stream, tmXc, tmW[0], tmW[1], tmW[2], \
-                     tmW[3], tmAdd, tmY, a.bias, p, status)
+                     tmW[3], tmAdd, tmY, a.bias, a.add, a.y, p, status)
     if (tf) {
         if (pb.cl) return a.add ? CT_TC3D_LAUNCH(true, true, true) : CT_TC3D_LAUNCH(false, true, true);
         return a.add ? CT_TC3D_LAUNCH(true, false, true) : CT_TC3D_LAUNCH(false, false, true);

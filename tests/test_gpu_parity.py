@@ -481,6 +481,10 @@ TC3S = [
          DL=[1, 1, 1], add=True),
     dict(nd=3, N=3, C_in=32, C_out=128, L=[4, 4, 4], K=[4, 4, 4], S=[4, 4, 4], P=[0, 0, 0], OP=[0, 0, 0],
          DL=[1, 1, 1], add=False),
+    # outputs shorter than the stride: one output row at H stride 3 (H residues 1
+    # and 2 have no rows), two output planes at D stride 4 (D residues 2, 3 none)
+    dict(nd=3, N=2, C_in=32, C_out=16, L=[1, 1, 8], K=[2, 1, 3], S=[4, 3, 3], P=[0, 0, 1], OP=[0, 0, 2],
+         DL=[1, 1, 1], add=True),
 ]
 
 

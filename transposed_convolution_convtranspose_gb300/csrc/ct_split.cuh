@@ -164,7 +164,10 @@ __device__ __forceinline__ void prep_x_cl_block(const float *__restrict__ x, uin
 
 // Both preps in one launch: blocks [0, nxb) move x (nbx x nby per image; or,
 // channels last, 1024 consecutive values each), the remaining nbw blocks build
-// the panels.  The GEMM kernel is launched as its programmatic dependent.
+// the panels.  The GEMM kernel is launched as its programmatic dependent.  The
+// x blocks run from the end of x backwards: the GEMM consumes x_c from the
+// first image on, so its first reads are the lines written last, the ones
+// still in L2.
 __global__ void __launch_bounds__(256)
 prep_kernel(const float *__restrict__ x, uint32_t *__restrict__ xc, int C, int64_t SP,
             int nbx, int nby, int nxb, const float *__restrict__ w, float *__restrict__ wp,
@@ -174,10 +177,10 @@ prep_kernel(const float *__restrict__ x, uint32_t *__restrict__ xc, int C, int64
     const int b = (int)blockIdx.x;
     const bool tf = q.tf != 0;
     if (b < nxb && cl_total > 0) {
-        prep_x_cl_block(x, xc, C, cl_total, b, tf);
+        prep_x_cl_block(x, xc, C, cl_total, nxb - 1 - b, tf);
     } else if (b < nxb) {
-        const int per = nbx * nby;
-        prep_x_block(x, xc, C, SP, (b % per) % nbx, (b % per) / nbx, b / per, tf);
+        const int per = nbx * nby, rb = nxb - 1 - b;
+        prep_x_block(x, xc, C, SP, (rb % per) % nbx, (rb % per) / nbx, rb / per, tf);
     } else {
         prep_w_block(w, wp, q, b - nxb, nbw);
     }

@@ -216,7 +216,17 @@ __device__ __forceinline__ void prepg_x_block(const float *__restrict__ x, uint1
         const int q = idx & 7, pos = idx >> 3;
         if (pos < ncols) {
             const int64_t s = s0 + pos;
-            const int w = (int)(s % W), h = (int)((s / W) % H), d = (int)(s / ((int64_t)W * H));
+            int w, h, d;
+            if (SP <= 0x7fffffff) {                 // 32-bit divisions where the image allows
+                const int si = (int)s;
+                w = si % W;
+                h = (si / W) % H;
+                d = si / (W * H);
+            } else {
+                w = (int)(s % W);
+                h = (int)((s / W) % H);
+                d = (int)(s / ((int64_t)W * H));
+            }
             const int64_t prow = (((int64_t)n * D + d) * W + w) * H + h;
             if (tf) {
                 float t[4], l[4];

@@ -87,7 +87,7 @@ constexpr int BM = 128;          // positions per unit (UMMA M)
 constexpr int QWT = 16;          // qw per unit (TMEM row m: qw = m / 8)
 constexpr int MHT = 8;           // qh per unit (one 8-row swizzle group per qw)
 constexpr int CK = 32;           // input channels: one 128-byte row of tf32 parts or of bf16 (hi, lo) pairs
-constexpr int NA = 3;            // A ring slots (one window each)
+constexpr int NA = 3;            // A ring slots at most (one window each)
 constexpr int MAXB = 8;          // B ring slots at most
 constexpr int BROWS = 256;       // rows of a B stage at most (one 32 KB slot)
 constexpr int NPB = 4;           // B producer warps at most
@@ -99,8 +99,11 @@ constexpr int kAWarp = 0;
 constexpr int kBWarp0 = 1;
 constexpr int kMmaWarp0 = kBWarp0 + NPB;
 constexpr int kEpiWarp0 = kMmaWarp0 + MAXG;
-constexpr int kThreads = 32 * (kEpiWarp0 + 4 * EPW);
+constexpr int kStoreWarp = kEpiWarp0 + 4 * EPW;
+constexpr int kThreads = 32 * (kStoreWarp + 1);
 constexpr int kEpiThreads = 32 * 4 * EPW;
+constexpr int NSB = 2;           // staging buffers per epilogue half
+constexpr uint32_t kSChunk = 8 * MHT * 2 * QWT * 4;   // 8 channels x 8 rows x 32 W outputs, fp32: 8 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // One input offset of a unit: the pairs (rD, rH) q0 .. q0 + nq - 1 receive
@@ -131,6 +134,8 @@ struct GParams {
     uint32_t set_cols;           // 8 x C_out
     uint32_t tmem_cols;
     uint32_t idesc_b[5];         // instruction descriptor, N = 2 x Cog x pairs, pairs 1..4
+    int na;                      // A ring slots
+    int stg;                     // staged epilogue: 8-channel chunks stored by TMA (else direct stores)
     GEntry ent[MAXE];
 };
 
@@ -338,12 +343,12 @@ template <bool TF>
 __global__ void __launch_bounds__(kThreads, 1)
 tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                   const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW4,
-                  const float *__restrict__ bias,
+                  const __grid_constant__ CUtensorMap tmY, const float *__restrict__ bias,
                   float *__restrict__ y, const __grid_constant__ GParams p, unsigned int *status)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t a_full[NA], a_empty[NA], b_full[MAXB], b_empty[MAXB], acc_full[2],
-        acc_empty[2], drain_bar[MAXG];
+        acc_empty[2], drain_bar[MAXG], c_done[2][NSB], e_free[2][NSB];
     __shared__ uint32_t tmem_slot;
     __shared__ float s_bias[64];
     // per entry: A window offset, B offset in its stage, hi -> lo rows, TMEM
@@ -351,8 +356,9 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
     __shared__ uint4 s_ent[MAXE];
     __shared__ uint32_t s_id[MAXE];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = sm;                                  // NA x a_slot
-    uint8_t *sB = sm + (size_t)NA * p.a_slot;          // nb x bslot
+    uint8_t *sA = sm;                                  // na x a_slot
+    uint8_t *sB = sm + (size_t)p.na * p.a_slot;        // nb x bslot
+    uint8_t *sE = sB + (size_t)p.nb * p.bslot;         // 2 x NSB x kSChunk (staged epilogue)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G;
 
@@ -360,9 +366,16 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         dev::prefetch_tensormap(&tmXc);
         dev::prefetch_tensormap(&tmW1);
         dev::prefetch_tensormap(&tmW4);
+        if (p.stg) dev::prefetch_tensormap(&tmY);
         // a stage is released by every group's issuer, a set of accumulators by
-        // every epilogue thread
-        for (int s = 0; s < NA; ++s) {
+        // every epilogue thread; a staged chunk is written by the 128 threads of
+        // its epilogue half and freed by the store warp
+        for (int h = 0; h < 2; ++h)
+            for (int b = 0; b < NSB; ++b) {
+                dev::mbar_init(&c_done[h][b], 32 * 4);
+                dev::mbar_init(&e_free[h][b], 1);
+            }
+        for (int s = 0; s < p.na; ++s) {
             dev::mbar_init(&a_full[s], 1);
             dev::mbar_init(&a_empty[s], G);
         }
@@ -404,7 +417,7 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         const int q = isA ? 0 : warp - kBWarp0;
         if (lane == 0 && (isA || q < p.npb)) {
             const int np = isA ? 1 : p.npb;
-            const int nst = isA ? NA : p.nb;
+            const int nst = isA ? p.na : p.nb;
             const int sp = isA ? p.ndd : p.nbs;
             uint64_t *fullb = isA ? a_full : b_full;
             uint64_t *emptyb = isA ? a_empty : b_empty;
@@ -522,7 +535,7 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                         }
                     }
                     tc::commit(&a_empty[sa]);
-                    if (++sa == NA) {
+                    if (++sa == p.na) {
                         sa = 0;
                         pa ^= 1u;
                     }
@@ -534,11 +547,56 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             if (!dev::mbar_wait_bounded(&drain_bar[g], 0, kWaitLimitNs)) ok = false;
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
+    } else if (warp == kStoreWarp) {
+        // ---------------- store warp (staged epilogue): each epilogue half writes its
+        // chunks (8 channels of one (group, pair) block: 8 output rows of the pair's
+        // H residue x 32 W outputs) into its two buffers in turn; this warp stores a
+        // written chunk with one TMA store through the map of the rows of one H
+        // residue (rows, planes and columns past the output are clipped) and frees
+        // a buffer once its store has read it.  Chunks are taken in the order
+        // (chunk index, half), the order the halves produce them.
+        if (p.stg && lane == 0) {
+            const int Cog = p.Cog, ncc = Cog / 8, nch = (G * 4 / 2) * ncc;   // chunks per half and unit
+            bool ok = true;
+            int issued = 0;
+            for (int k = 0; k < nunit_cta && ok; ++k) {
+                const GUnit u = g_unit((int)blockIdx.x + k * (int)gridDim.x, p);
+                for (int jj = 0; jj < nch && ok; ++jj) {
+                    const int gc = k * nch + jj;                 // the half's chunk counter
+                    const int bi = gc % NSB;
+                    for (int h = 0; h < 2; ++h) {
+                        if (!dev::mbar_wait_bounded(&c_done[h][bi], (gc / NSB) & 1, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        const int b = h + 2 * (jj / ncc), c = (jj % ncc) * 8;   // block (group, pair), channels
+                        const int g = b >> 2, pq = b & 3;
+                        dev::tma_store_5d(&tmY, sE + (size_t)(h * NSB + bi) * kSChunk, 2 * u.qwb * QWT,
+                                          u.qhb * MHT, pq & 1, 2 * u.qd + (pq >> 1),
+                                          u.n * p.C_out + g * Cog + c);
+                        dev::bulk_commit();
+                        ++issued;
+                        // the store issued two before this one (the same half's previous
+                        // chunk) has read its buffer
+                        dev::bulk_wait_read<2>();
+                        if (gc >= 1) dev::mbar_arrive(&e_free[h][(gc - 1) % NSB]);
+                    }
+                }
+            }
+            dev::bulk_wait_all();
+            if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
+            (void)issued;
+        }
     } else {
         // ---------------- epilogue: EPW warps per TMEM lane quarter (32 positions:
         // 4 qw x 8 qh); half h of the warps takes the (group, pair) blocks of
         // parity h.  A block is 2 x Cog columns: W residue 0's channels, then W
         // residue 1's.  Both sets are cleared once before the first unit.
+        // Staged: per 8 channels the half's four warps write the chunk's 8 KB (8
+        // channels x 8 rows x 32 W outputs, 128-byte rows in the 128-byte swizzle)
+        // into the half's next buffer and the store warp stores it: whole
+        // 128-byte lines instead of a warp's 8 rows x 32 bytes.  Otherwise each
+        // position's even and odd W outputs go out as one float2.
         const int ew = warp & 3;
         const int half = (warp - kEpiWarp0) >> 2;
         const int Cog = p.Cog, nblk = G * 4;
@@ -553,6 +611,7 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             dev::mbar_arrive(&acc_empty[set]);
         }
         bool ok = true;
+        int gc = 0;                                  // staged: this half's chunk counter
         for (int k = 0; k < nunit_cta; ++k) {
             const int set = k & 1;
             const GUnit u = g_unit((int)blockIdx.x + k * (int)gridDim.x, p);
@@ -563,7 +622,8 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             ok = __all_sync(0xffffffffu, ok);        // warp-uniform before .sync.aligned loads
             tc::fence_after();
             const int m = ew * 32 + lane;
-            const int qw = u.qwb * QWT + (m >> 3), qh = u.qhb * MHT + (m & 7);
+            const int qwl = m >> 3, qhl = m & 7;
+            const int qw = u.qwb * QWT + qwl, qh = u.qhb * MHT + qhl;
             const bool inw = qw < p.QW && qh < p.QH;
             const uint32_t sbase = lane_base + (uint32_t)set * p.set_cols;
             for (int b = half; b < nblk; b += 2) {
@@ -581,7 +641,30 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                         tmem_st8_zero(t0);
                         tmem_st8_zero(t0 + (uint32_t)Cog);
                     }
-                    if (ok && valid) {
+                    if (p.stg) {
+                        // the buffer's previous chunk (two before) has been stored
+                        const int bi = gc % NSB;
+                        if (gc >= NSB && ok &&
+                            !dev::mbar_wait_bounded(&e_free[half][bi], ((gc / NSB) - 1) & 1, kWaitLimitNs)) {
+                            atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
+                            ok = false;
+                        }
+                        if (ok) {
+                            // row qhl of channel i: 16-byte unit (qwl / 2) ^ qhl, the float2 of
+                            // qwl at byte 8 (qwl & 1) within it
+                            uint8_t *buf = sE + (size_t)(half * NSB + bi) * kSChunk;
+                            const uint32_t off = (uint32_t)((((qwl >> 1) ^ qhl) << 4) + ((qwl & 1) << 3));
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float bb = s_bias[g * Cog + c + i];
+                                *reinterpret_cast<float2 *>(buf + (size_t)(i * MHT + qhl) * 128 + off) =
+                                    make_float2(v0[i] + bb, v1[i] + bb);
+                            }
+                        }
+                        dev::fence_proxy_async();
+                        dev::mbar_arrive(&c_done[half][bi]);
+                        ++gc;
+                    } else if (ok && valid) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float bb = s_bias[g * Cog + c + i];
@@ -775,9 +858,16 @@ bool make_gplan_3d(const Problem &pb, const Args *a, GPlan *out)
     p.tmem_cols = cols;
     p.bslot = (uint32_t)BROWS * 128u;
     const size_t budget = 227 * 1024 - 2048;
-    const size_t a_area = (size_t)NA * p.a_slot;
-    if (a_area + 2 * (size_t)p.bslot > budget) return false;
-    int nb = (int)((budget - a_area) / p.bslot);
+    // staged epilogue (TMA stores of whole 128-byte lines): the output rows of
+    // one H residue as a tensor dimension need an even H extent, and rows of
+    // 16-byte multiples; its 32 KB of buffers take the third A slot
+    const bool stg = pb.Lo[1] % 2 == 0 && pb.Lo[2] % 4 == 0 && (!a || ((uintptr_t)a->y % 16) == 0);
+    p.stg = stg ? 1 : 0;
+    p.na = stg ? 2 : NA;
+    const size_t e_area = stg ? (size_t)2 * NSB * kSChunk : 0;
+    const size_t a_area = (size_t)p.na * p.a_slot;
+    if (a_area + e_area + 2 * (size_t)p.bslot > budget) return false;
+    int nb = (int)((budget - a_area - e_area) / p.bslot);
     if (nb >= 8) { nb = 8; p.npb = 4; }
     else if (nb >= 6) { nb = 6; p.npb = 3; }
     else if (nb >= 4) { nb = 4; p.npb = 4; }
@@ -788,7 +878,7 @@ bool make_gplan_3d(const Problem &pb, const Args *a, GPlan *out)
     out->rows = row;
     out->x_bytes = align256((size_t)pb.N * CK * pb.in_sp() * (tf ? 8 : 4));
     out->w_bytes = align256((size_t)row * CK * 4);
-    out->smem = a_area + (size_t)nb * p.bslot + 1024;
+    out->smem = a_area + (size_t)nb * p.bslot + e_area + 1024;
     return true;
 }
 
@@ -855,6 +945,20 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
             return cudaErrorInvalidValue;
     }
 
+    // y for the staged epilogue: (W, H / 2, H residue, D, N x C_out), a box of a
+    // chunk: 32 W outputs x 8 rows of one residue x 8 channels, 128-byte swizzle
+    CUtensorMap tmY;
+    memset(&tmY, 0, sizeof(tmY));
+    if (p.stg) {
+        const uint64_t ydims[5] = {(uint64_t)pb.Lo[2], (uint64_t)(pb.Lo[1] / 2), 2u, (uint64_t)pb.Lo[0],
+                                   (uint64_t)pb.N * pb.C_out};
+        const uint64_t ystr[4] = {(uint64_t)pb.Lo[2] * 8, (uint64_t)pb.Lo[2] * 4, (uint64_t)pb.Lo[2] * pb.Lo[1] * 4,
+                                  (uint64_t)pb.out_sp() * 4};
+        const uint32_t ybox[5] = {(uint32_t)(2 * QWT), (uint32_t)MHT, 1u, 1u, 8u};
+        if (!encode_tiled(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.y, ydims, ystr, ybox,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
     int per_sm = 0;
     const void *fn = tf ? (const void *)&tc3dg_split_kernel<true> : (const void *)&tc3dg_split_kernel<false>;
     e = prepare_kernel(fn, kThreads, pl.smem, &per_sm);
@@ -866,9 +970,9 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
     if (grid > p.nunits) grid = p.nunits;
     if (tf)
         return launch_dependent(tc3dg_split_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
-                                tmXc, tmW[0], tmW[1], a.bias, a.y, p, status);
+                                tmXc, tmW[0], tmW[1], tmY, a.bias, a.y, p, status);
     return launch_dependent(tc3dg_split_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
-                            tmXc, tmW[0], tmW[1], a.bias, a.y, p, status);
+                            tmXc, tmW[0], tmW[1], tmY, a.bias, a.y, p, status);
 }
 
 }  // namespace ct

@@ -65,8 +65,14 @@
 //               every ~100 clocks, so the groups' MMAs run from separate
 //               threads); TMEM allocation by warp 5
 //   warps 9-16  epilogue, two per TMEM lane quarter: tcgen05.ld of a (group,
-//               pair) block, zeros stored back, bias added, each position's
-//               even and odd W outputs written as one float2
+//               pair) block, zeros stored back, bias added.  When the output
+//               has an even H extent, each 8-channel chunk (8 output rows of
+//               the pair's H residue x 32 W outputs) is written into one of the
+//               half's two staging buffers (128-byte rows, 128-byte swizzle);
+//               otherwise each position's even and odd W outputs go out as one
+//               float2 (a warp's store then covers 8 rows x 32 bytes)
+//   warp 17     store warp (staged epilogue): one TMA store per chunk through
+//               the map of y's rows of one H residue, then frees the buffer
 // Every ring slot has exactly one producer, which refills it only after
 // waiting for its previous round.  Every mbarrier wait is bounded: a timeout
 // records CT_ERR_DEVICE_TIMEOUT in the device status word and the roles

@@ -306,13 +306,15 @@ def test_fp32_2d_grouped_tensor_core_shapes(k):
 
 # bf16 ConvTranspose2d on the bf16 tensor-core path: kernel extents 4 and 8
 # (the weight repack moves 16-byte pieces, so kH*kW must be a multiple of 8),
-# C_out 16..256, odd H output, padding 0..3, several tiles per CTA.
+# C_out 16..256, odd H output, padding 0..3, several tiles per CTA, and 160
+# tile pairs (on 152 SMs the last round's 8 pairs run as 16 single tiles).
 UMMA2D = [
     dict(N=1, C_in=64, C_out=64, L=[8, 16], K=[4, 4], P=[1, 1], OP=[0, 0]),
     dict(N=2, C_in=128, C_out=128, L=[5, 12], K=[4, 4], P=[1, 1], OP=[1, 0]),
     dict(N=1, C_in=64, C_out=256, L=[4, 8], K=[4, 4], P=[1, 1], OP=[0, 0]),
     dict(N=1, C_in=64, C_out=32, L=[3, 4], K=[8, 8], P=[3, 3], OP=[0, 0]),
     dict(N=4, C_in=64, C_out=16, L=[32, 32], K=[4, 4], P=[0, 0], OP=[0, 0]),
+    dict(N=20, C_in=64, C_out=32, L=[32, 32], K=[4, 4], P=[1, 1], OP=[0, 0]),
 ]
 
 

@@ -20,7 +20,12 @@
 // TMEM lanes are 4 qh rows of 8 qw: its stores cover 4 rows x 64 bytes.
 // When two accumulators fit, a unit of work is a pair of tiles (two
 // neighbouring 8-column qw blocks): they share every input window and weight
-// panel, and each of two MMA-issuing warps computes one of them.
+// panel, and each of two MMA-issuing warps computes one of them.  When the
+// pairs fill whole rounds of the grid but the last round would leave more
+// than half the CTAs idle, that round's pairs run as single tiles (twice as
+// many units, each a little over half a pair's time): the other issuer and
+// epilogue half keep the barrier protocol without MMAs or stores (the SPLIT
+// instantiation; without it the issue loop carries no such test).
 //
 // Order within a unit: all of W phase 0, then all of W phase 1.  The TMEM
 // holds no second accumulator to switch to while one is drained, so the
@@ -96,7 +101,11 @@ struct UParams {
     int SD, nTD;             // D: stride 2 and nT taps, or a unit dimension (stride 1, one tap)
     int cl;                  // channels-last y (N, D, H, W, C_out); x is then the caller's own
     int n_kb;                // C_in / BK
-    int ntiles;
+    int ntiles;              // units of work: tile pairs (or single tiles when nacc = 1)
+    // the last, partial round of pairs split into single tiles: units
+    // [0, npair) are pairs, the next nunits - npair are single tiles, two per
+    // remaining pair (nunits = ntiles when no pair is split)
+    int npair, nunits;
     int nacc;                // TMEM accumulators = MMA issuers = tiles per pair (1 or 2)
     int na, nb, npb;         // A ring slots, B ring slots, B producers (nb a multiple of npb)
     uint32_t acc_cols;       // columns of one accumulator (2 x C_out: W phase 0, then W phase 1)
@@ -119,6 +128,23 @@ struct UParams {
 struct TileCoord {
     int n, qd, qhb, qwp, rD, rH;
 };
+__device__ __forceinline__ TileCoord tile_coord(int t, const UParams &p);
+
+// Unit u of the schedule: its pair's coordinates, and for a single-tile unit
+// the tile of the pair it computes (*js = 0 or 1; -1 for a whole pair).
+// Without SPLIT every unit is a pair (the issue loop keeps no test).
+template <bool SPLIT>
+__device__ __forceinline__ TileCoord unit_tiles(int u, const UParams &p, int *js)
+{
+    if (!SPLIT || u < p.npair) {
+        *js = -1;
+        return tile_coord(u, p);
+    }
+    const int s = u - p.npair;
+    *js = s & 1;
+    return tile_coord(p.npair + (s >> 1), p);
+}
+
 __device__ __forceinline__ TileCoord tile_coord(int t, const UParams &p)
 {
     TileCoord c;
@@ -148,6 +174,7 @@ __device__ __forceinline__ uint64_t desc_sw128_sbo(uint32_t saddr, uint32_t sbo)
 }
 
 // ---- GEMM kernel -------------------------------------------------------------
+template <bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const float *__restrict__ bias, float *__restrict__ y, const __grid_constant__ UParams p,
@@ -194,7 +221,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     dev::griddep_wait();
     const uint32_t tmem = tmem_slot;
     const int ntile_cta =
-        p.ntiles > (int)blockIdx.x ? (p.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        p.nunits > (int)blockIdx.x ? (p.nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     // stages per unit, W phase 0 first, then W phase 1:
     //   A = (W phase, D tap, K block), B = (W phase, D tap, K block, H tap, W tap).
     // A unit is a pair of tiles (two 8-row qh blocks) when two accumulators fit:
@@ -225,7 +252,8 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int k = g / sp, i = g % sp;
                 if (k != kc) {
                     kc = k;
-                    tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
+                    int js;
+                    tcd = unit_tiles<SPLIT>((int)blockIdx.x + k * (int)gridDim.x, p, &js);   // a single tile loads its pair's operands
                 }
                 const int s = g % nst;
                 if (g >= nst && !dev::mbar_wait_bounded(&emptyb[s], ((g / nst) - 1) & 1, kWaitLimitNs)) {
@@ -284,7 +312,11 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
             for (int k = 0; k < ntile_cta && ok; ++k) {
-                const TileCoord tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
+                int js;
+                const TileCoord tcd = unit_tiles<SPLIT>((int)blockIdx.x + k * (int)gridDim.x, p, &js);
+                // a single-tile unit: the other issuer keeps the protocol (waits,
+                // commits) but issues no MMAs
+                const bool act = !SPLIT || js < 0 || js == j;
                 for (int wr = 0; wr < 2 && ok; ++wr) {
                     if (k > 0 && !dev::mbar_wait_bounded(&acc_empty[j][wr], (k - 1) & 1, kWaitLimitNs)) {
                         ok = false;
@@ -318,9 +350,11 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                                         const uint64_t da =
                                             desc_sw128_sbo(wbase + aw0 - (uint32_t)jw * awstep + hoff, sbo);
                                         const uint64_t db = tc::desc_sw128(bslot + (uint32_t)t * b_bytes);
+                                        if (act) {
 #pragma unroll
-                                        for (int kk = 0; kk < BK / UK; ++kk)   // 16 bf16 = 32 bytes along K
-                                            tc::mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (init || kk) ? 1u : 0u);
+                                            for (int kk = 0; kk < BK / UK; ++kk)   // 16 bf16 = 32 bytes along K
+                                                tc::mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (init || kk) ? 1u : 0u);
+                                        }
                                         init = true;
                                     }
                                     tc::commit(&b_empty[sb]);
@@ -365,11 +399,13 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int64_t sp = (int64_t)p.Lo0 * p.Lo1 * p.Lo2;
         bool ok = true;
         for (int k = 0; k < ntile_cta; ++k) {
-            const TileCoord tcd = tile_coord((int)blockIdx.x + k * (int)gridDim.x, p);
+            int js;
+            const TileCoord tcd = unit_tiles<SPLIT>((int)blockIdx.x + k * (int)gridDim.x, p, &js);
+            const bool act = !SPLIT || js < 0 || js == a;   // a single-tile unit: the other half only releases
             const int m = ew * 32 + lane;
             const int qw = (tcd.qwp * ni + a) * QWT + (m & 7), qh = tcd.qhb * MHT + (m >> 3);
             const int od = p.SD * tcd.qd + tcd.rD, oh = 2 * qh + tcd.rH;
-            const bool valid = qw < p.QW && od < p.Lo0 && oh < p.Lo1;
+            const bool valid = act && qw < p.QW && od < p.Lo0 && oh < p.Lo1;
             for (int wr = 0; wr < 2; ++wr) {
                 if (ok && !dev::mbar_wait_bounded(&acc_full[a][wr], k & 1, kWaitLimitNs)) {
                     atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
@@ -388,7 +424,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 for (int ci = cfirst; ci < nchunk; ci += EB * cstep) {
                     float v[EB][16];
                     int nc = 0;
-                    if (ok) {
+                    if (ok && act) {
 #pragma unroll
                         for (int b = 0; b < EB; ++b)
                             if (ci + b * cstep < nchunk) {
@@ -667,6 +703,7 @@ bool make_uplan(const Problem &pb, UPlan *out)
     const int64_t tiles = (int64_t)pb.N * p.QD * p.n_qhb * p.n_qwp * 2 * SD;
     if (tiles > 0x7fffffff || tiles == 0) return false;
     p.ntiles = (int)tiles;
+    p.npair = p.nunits = p.ntiles;           // the launch may split the last round
     // residue r of a stride-2 dimension takes the taps k == (r + p) mod 2, i.e.
     // k = c + 2j, reading input q + floor((r + p)/2) - j
     WPackParams wq;
@@ -815,15 +852,27 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
         return cudaErrorInvalidValue;
 
     int per_sm = 0;
-    e = prepare_kernel((const void *)&umma_ct3d_kernel, kThreads, pl.smem, &per_sm);
+    e = prepare_kernel((const void *)&umma_ct3d_kernel<false>, kThreads, pl.smem, &per_sm);
+    if (e == cudaSuccess) e = prepare_kernel((const void *)&umma_ct3d_kernel<true>, kThreads, pl.smem, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     unsigned int *status = device_status_ptr();
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.ntiles) grid = p.ntiles;
-    return launch_dependent(umma_ct3d_kernel, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmA, tmB,
-                            a.bias, a.y, p, status);
+    // tile pairs fill whole rounds of the grid; when the last round would leave
+    // more than half the CTAs idle, its pairs are split into single tiles (a
+    // single takes a little over half a pair's time), one round of them
+    UParams pk = p;
+    const int rem = grid > 0 ? p.ntiles % grid : 0;
+    if (p.nacc == 2 && rem > 0 && 2 * rem <= grid) {
+        pk.npair = p.ntiles - rem;
+        pk.nunits = pk.npair + 2 * rem;
+        return launch_dependent(umma_ct3d_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmA,
+                                tmB, a.bias, a.y, pk, status);
+    }
+    return launch_dependent(umma_ct3d_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmA, tmB,
+                            a.bias, a.y, pk, status);
 }
 
 }  // namespace ct

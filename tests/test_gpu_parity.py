@@ -167,7 +167,8 @@ def test_random_fused_and_bf16_generic():
 # per dimension 1..4), even and odd padding (input W offsets shared by both W
 # phases or not), C_out from 16 (one 16-channel chunk, N = 2 C_out = 32) to
 # 256 (N = 2 C_out too wide for one MMA, a single TMEM accumulator), ragged
-# H blocks and odd D, and one case with several tiles per persistent CTA.
+# H blocks and odd D, one case with several tiles per persistent CTA, and 160
+# tile pairs (on 152 SMs the last round's 8 pairs run as 16 single tiles).
 UMMA = [
     dict(N=1, C_in=64, C_out=16, L=[2, 3, 8], K=[4] * 3, P=[1] * 3, OP=[1, 0, 0]),
     dict(N=1, C_in=64, C_out=32, L=[3, 2, 4], K=[2] * 3, P=[0] * 3, OP=[0, 1, 0]),
@@ -179,6 +180,7 @@ UMMA = [
     dict(N=1, C_in=64, C_out=96, L=[2, 3, 7], K=[4] * 3, P=[0] * 3, OP=[0, 0, 0]),
     dict(N=1, C_in=64, C_out=64, L=[3, 5, 16], K=[4] * 3, P=[1] * 3, OP=[1, 1, 0]),
     dict(N=8, C_in=64, C_out=16, L=[16, 16, 16], K=[2] * 3, P=[0] * 3, OP=[0, 0, 0]),
+    dict(N=10, C_in=64, C_out=32, L=[4, 16, 16], K=[4] * 3, P=[1] * 3, OP=[0, 0, 0]),
 ]
 
 

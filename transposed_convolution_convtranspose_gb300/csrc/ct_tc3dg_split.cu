@@ -61,17 +61,19 @@
 //   warp 0      TMA producer of the A ring (the window of a D offset)
 //   warps 1-4   TMA producers of the B ring (one input offset's panel: hi
 //               rows, then lo rows), one per slot
-//   warps 5-8   MMA issue, one warp per group (one thread issues an MMA only
-//               every ~100 clocks, so the groups' MMAs run from separate
-//               threads); TMEM allocation by warp 5
-//   warps 9-16  epilogue, two per TMEM lane quarter: tcgen05.ld of a (group,
+//   warps 5-12  MMA issue, two warps per group, each taking alternate entries
+//               of every stage (one thread issues an MMA only every ~100
+//               clocks, so the MMAs run from separate threads; the MMAs of a
+//               group's two warps all accumulate into its columns, so their
+//               order does not matter); TMEM allocation by warp 5
+//   warps 13-20 epilogue, two per TMEM lane quarter: tcgen05.ld of a (group,
 //               pair) block, zeros stored back, bias added.  When the output
 //               has an even H extent, each 8-channel chunk (8 output rows of
 //               the pair's H residue x 32 W outputs) is written into one of the
 //               half's two staging buffers (128-byte rows, 128-byte swizzle);
 //               otherwise each position's even and odd W outputs go out as one
 //               float2 (a warp's store then covers 8 rows x 32 bytes)
-//   warp 17     store warp (staged epilogue): one TMA store per chunk through
+//   warp 21     store warp (staged epilogue): one TMA store per chunk through
 //               the map of y's rows of one H residue, then frees the buffer
 // Every ring slot has exactly one producer, which refills it only after
 // waiting for its previous round.  Every mbarrier wait is bounded: a timeout
@@ -97,14 +99,15 @@ constexpr int NA = 3;            // A ring slots at most (one window each)
 constexpr int MAXB = 8;          // B ring slots at most
 constexpr int BROWS = 256;       // rows of a B stage at most (one 32 KB slot)
 constexpr int NPB = 4;           // B producer warps at most
-constexpr int MAXG = 4;          // groups = MMA-issuing warps at most
+constexpr int MAXG = 4;          // groups at most
+constexpr int IPG = 2;           // MMA-issuing warps per group (alternate entries of every stage)
 constexpr int MAXE = 64;         // input offsets per unit at most
 constexpr int MAXDD = 5;         // distinct D offsets at most
 constexpr int EPW = 2;           // epilogue warps per TMEM lane quarter
 constexpr int kAWarp = 0;
 constexpr int kBWarp0 = 1;
 constexpr int kMmaWarp0 = kBWarp0 + NPB;
-constexpr int kEpiWarp0 = kMmaWarp0 + MAXG;
+constexpr int kEpiWarp0 = kMmaWarp0 + MAXG * IPG;
 constexpr int kStoreWarp = kEpiWarp0 + 4 * EPW;
 constexpr int kThreads = 32 * (kStoreWarp + 1);
 constexpr int kEpiThreads = 32 * 4 * EPW;
@@ -354,7 +357,7 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t a_full[NA], a_empty[NA], b_full[MAXB], b_empty[MAXB], acc_full[2],
-        acc_empty[2], drain_bar[MAXG], c_done[2][NSB], e_free[2][NSB];
+        acc_empty[2], drain_bar[MAXG * IPG], c_done[2][NSB], e_free[2][NSB];
     __shared__ uint32_t tmem_slot;
     __shared__ float s_bias[64];
     // per entry: A window offset, B offset in its stage, hi -> lo rows, TMEM
@@ -383,17 +386,17 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             }
         for (int s = 0; s < p.na; ++s) {
             dev::mbar_init(&a_full[s], 1);
-            dev::mbar_init(&a_empty[s], G);
+            dev::mbar_init(&a_empty[s], G * IPG);
         }
         for (int s = 0; s < p.nb; ++s) {
             dev::mbar_init(&b_full[s], 1);
-            dev::mbar_init(&b_empty[s], G);
+            dev::mbar_init(&b_empty[s], G * IPG);
         }
         for (int a = 0; a < 2; ++a) {
-            dev::mbar_init(&acc_full[a], G);
+            dev::mbar_init(&acc_full[a], G * IPG);
             dev::mbar_init(&acc_empty[a], kEpiThreads);
         }
-        for (int j = 0; j < MAXG; ++j) dev::mbar_init(&drain_bar[j], 1);
+        for (int j = 0; j < MAXG * IPG; ++j) dev::mbar_init(&drain_bar[j], 1);
         dev::fence_mbar_init();
     }
     if (warp == kMmaWarp0) tc::tmem_alloc(&tmem_slot, p.tmem_cols);
@@ -474,10 +477,11 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                     dev::mbar_wait_bounded(&fullb[r % nst], (r / nst) & 1, kWaitLimitNs);
             }
         }
-    } else if (warp < kMmaWarp0 + MAXG) {
-        // ---------------- MMA issuers, one per group: every MMA accumulates (the
-        // epilogue leaves the set cleared)
-        const int g = warp - kMmaWarp0;
+    } else if (warp < kMmaWarp0 + MAXG * IPG) {
+        // ---------------- MMA issuers, IPG per group, each taking the entries e with
+        // e mod IPG == its index: every MMA accumulates (the epilogue leaves the
+        // set cleared)
+        const int wi = warp - kMmaWarp0, g = wi / IPG, sub = wi % IPG;
         if (lane == 0 && g < G) {
             bool ok = true;
             const uint32_t sAb = dev::smem_u32(sA), sBb = dev::smem_u32(sB);
@@ -511,7 +515,7 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                         }
                         tc::fence_after();
                         const uint32_t bb = sBb + (uint32_t)sb * bslot;
-                        for (int e = p.bs_e0[j]; e < p.bs_e0[j + 1]; ++e) {
+                        for (int e = p.bs_e0[j] + sub; e < p.bs_e0[j + 1]; e += IPG) {
                             const uint4 t0 = s_ent[e];      // A offset, B offset, hi -> lo rows, column
                             const uint32_t id = s_id[e];    // instruction descriptor
                             const uint64_t da = desc_sbo(wc + t0.x, sbo) + kgrp;
@@ -549,8 +553,8 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                 if (ok) tc::commit(&acc_full[set]);
             }
             // every MMA issued has to complete before the TMEM is freed
-            tc::commit(&drain_bar[g]);
-            if (!dev::mbar_wait_bounded(&drain_bar[g], 0, kWaitLimitNs)) ok = false;
+            tc::commit(&drain_bar[wi]);
+            if (!dev::mbar_wait_bounded(&drain_bar[wi], 0, kWaitLimitNs)) ok = false;
             if (!ok) atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
         }
     } else if (warp == kStoreWarp) {

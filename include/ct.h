@@ -219,6 +219,19 @@ ct_status ct_forward_3d_noalloc(const void *x, const void *w, const float *bias,
                                 const int output_padding[3], const int dilation[3],
                                 ct_dtype dtype, void *stream);
 
+/* Bitwise reproducibility (process-wide, read at each forward call's launch).
+ * Every path computes each output in a fixed order, so repeated calls on the
+ * same inputs give identical bits, except the grouped FP32 tensor-core path
+ * ("tc3dg_*" in ct_introspect.h), which by default issues each group's MMAs
+ * from two threads whose contributions to an output accumulate in no fixed
+ * order (results then differ between calls in the last bits, within the
+ * path's stated error).  ct_set_deterministic(1) makes that path issue from
+ * one thread per group (about 12 % slower on the grouped workload) and every
+ * call reproducible; 0 (the default) restores it.  Not synchronised with
+ * forward calls in flight on other threads. */
+void ct_set_deterministic(int on);
+int ct_get_deterministic(void);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *ct_status_str(ct_status s);
 

@@ -665,6 +665,29 @@ def test_repeat_is_deterministic():
     assert torch.equal(y1, y2)
 
 
+def test_grouped_reproducible_when_asked():
+    """ct_set_deterministic(1): the grouped FP32 tensor-core path issues each
+    group's MMAs from one thread, so repeated calls give identical bits (by
+    default two threads per group accumulate in no fixed order); both within
+    the path's tolerance of the oracle."""
+    import torch
+    import transposed_convolution_convtranspose_gb300 as ct
+    c = cc.case_from_config("convT3d_grouped", N=2)
+    assert path_of(c) == "tc3dg_tf32x3"
+    t = cc.make_inputs(c, seed=710)
+    ref = cc.run_oracle(c, t)
+    ct.ct_set_deterministic(1)
+    try:
+        y1 = cc.run_gpu(c, t)
+        y2 = cc.run_gpu(c, t)
+    finally:
+        ct.ct_set_deterministic(0)
+    assert torch.equal(y1, y2)
+    cc.assert_close(y1.cpu().numpy(), ref, "f32", "grouped, reproducible order")
+    y3 = cc.run_gpu(c, t)
+    cc.assert_close(y3.cpu().numpy(), ref, "f32", "grouped, two issuers per group")
+
+
 TC1D = [
     # (C_in, C_out, L_in, k, s, p, op, d): C_in = 32 and d a multiple of s take
     # the FP32 tensor-core path; ragged lengths end tiles mid-way

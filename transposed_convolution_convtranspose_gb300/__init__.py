@@ -33,7 +33,8 @@ EXPORTED = ["ct_out_len", "ct_workspace_size_1d", "ct_workspace_size_2d", "ct_wo
             "ct_forward_1d", "ct_forward_2d", "ct_forward_2d_add_hswish", "ct_forward_3d",
             "ct_forward_3d_add_hswish", "ct_path_1d", "ct_path_2d", "ct_path_3d",
             "ct_workspace_size_cl", "ct_forward_cl", "ct_path_cl", "ct_path_call",
-            "ct_set_path_override", "ct_status_str", "ct_last_device_error",
+            "ct_set_path_override", "ct_set_deterministic", "ct_get_deterministic", "ct_status_str",
+            "ct_last_device_error",
             "ct_forward_3d_noalloc", "ct_selftest_wait_timeout"]
 
 # bytes of the library-owned scratch buffer used by ct_forward_3d_noalloc
@@ -104,6 +105,10 @@ def _setup(lib):
     lib.ct_path_3d.argtypes = [_I, _I, _I, _I3, _I3, _I, _I3, _I3, _I3, _I3, _I, _I]
     lib.ct_set_path_override.restype = None
     lib.ct_set_path_override.argtypes = [_I]
+    lib.ct_set_deterministic.restype = None
+    lib.ct_set_deterministic.argtypes = [_I]
+    lib.ct_get_deterministic.restype = _I
+    lib.ct_get_deterministic.argtypes = []
     lib.ct_status_str.restype = ctypes.c_char_p
     lib.ct_status_str.argtypes = [_I]
     lib.ct_last_device_error.restype = _I
@@ -325,6 +330,15 @@ def ct_path_3d(N, C_in, C_out, in_dhw, k_dhw, groups, stride, padding, output_pa
 
 def ct_set_path_override(mode):
     load().ct_set_path_override(int(mode))
+
+
+def ct_set_deterministic(on):
+    """Bitwise-reproducible results on every path (process-wide); see include/ct.h."""
+    load().ct_set_deterministic(int(bool(on)))
+
+
+def ct_get_deterministic():
+    return bool(load().ct_get_deterministic())
 
 
 def ct_status_str(code):

@@ -83,6 +83,9 @@ bool build_phase_dim(int L_out, int K, int S, int P, int DL, PhaseDim *pd)
 }
 
 static std::atomic<int> g_override{0};
+static std::atomic<int> g_deterministic{0};
+
+bool deterministic() { return g_deterministic.load() != 0; }
 
 }  // namespace ct
 
@@ -509,6 +512,10 @@ const char *ct_path_call(int nd, int channels_last, int N, int C_in, int C_out, 
 }
 
 void ct_set_path_override(int mode) { g_override.store(mode == 1 || mode == 2 ? mode : 0); }
+
+void ct_set_deterministic(int on) { g_deterministic.store(on ? 1 : 0); }
+
+int ct_get_deterministic(void) { return g_deterministic.load(); }
 
 const char *ct_status_str(ct_status s)
 {

@@ -56,6 +56,8 @@ bool build_phase_dim(int L_out, int K, int S, int P, int DL, PhaseDim *pd);
 // Device address of the library's device status word (timeouts of bounded
 // waits).  Valid on the current device after the first call.
 unsigned int *device_status_ptr();
+// Process-wide: results must be bitwise reproducible (ct_set_deterministic).
+bool deterministic();
 
 // Validation, path choice and launch of ct_api.cu, for other entry points.
 ct_status make_problem_3d(int N, int C_in, int C_out, const int *in_dhw, const int *k_dhw, int groups,

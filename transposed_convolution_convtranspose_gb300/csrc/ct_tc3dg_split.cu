@@ -100,7 +100,7 @@ constexpr int MAXB = 8;          // B ring slots at most
 constexpr int BROWS = 256;       // rows of a B stage at most (one 32 KB slot)
 constexpr int NPB = 4;           // B producer warps at most
 constexpr int MAXG = 4;          // groups at most
-constexpr int IPG = 2;           // MMA-issuing warps per group (alternate entries of every stage)
+constexpr int IPG = 2;           // MMA-issuing warps per group: p.ipg of them take alternate entries of every stage
 constexpr int MAXE = 64;         // input offsets per unit at most
 constexpr int MAXDD = 5;         // distinct D offsets at most
 constexpr int EPW = 2;           // epilogue warps per TMEM lane quarter
@@ -144,6 +144,7 @@ struct GParams {
     uint32_t tmem_cols;
     uint32_t idesc_b[5];         // instruction descriptor, N = 2 x Cog x pairs, pairs 1..4
     int na;                      // A ring slots
+    int ipg;                     // issuers per group that issue MMAs (1: reproducible order; up to IPG)
     int stg;                     // staged epilogue: 8-channel chunks stored by TMA (else direct stores)
     GEntry ent[MAXE];
 };
@@ -174,16 +175,6 @@ __device__ __forceinline__ float tf32_round(float v)
     asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(v));
     return __uint_as_float(r);
 }
-
-// 8 columns of the warp's 32 TMEM lanes set to zero.
-__device__ __forceinline__ void tmem_st8_zero(uint32_t taddr)
-{
-    const uint32_t z = 0u;
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(z),
-                 "r"(z), "r"(z), "r"(z), "r"(z), "r"(z), "r"(z), "r"(z)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 // K-major, 128-byte swizzled operand with 8-row groups `sbo` bytes apart
 __device__ __forceinline__ uint64_t desc_sbo(uint32_t saddr, uint32_t sbo)
@@ -478,9 +469,10 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             }
         }
     } else if (warp < kMmaWarp0 + MAXG * IPG) {
-        // ---------------- MMA issuers, IPG per group, each taking the entries e with
-        // e mod IPG == its index: every MMA accumulates (the epilogue leaves the
-        // set cleared)
+        // ---------------- MMA issuers, IPG warps per group; p.ipg of them issue, each
+        // taking the entries e with e mod p.ipg == its index (the others only keep
+        // the barrier protocol): every MMA accumulates (the epilogue leaves the set
+        // cleared)
         const int wi = warp - kMmaWarp0, g = wi / IPG, sub = wi % IPG;
         if (lane == 0 && g < G) {
             bool ok = true;
@@ -515,7 +507,9 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                         }
                         tc::fence_after();
                         const uint32_t bb = sBb + (uint32_t)sb * bslot;
-                        for (int e = p.bs_e0[j] + sub; e < p.bs_e0[j + 1]; e += IPG) {
+                        // with one issuing warp per group the MMAs into a column run in a fixed
+                        // order (bitwise reproducible results); with two, in no fixed order
+                        for (int e = p.bs_e0[j] + sub; sub < p.ipg && e < p.bs_e0[j + 1]; e += p.ipg) {
                             const uint4 t0 = s_ent[e];      // A offset, B offset, hi -> lo rows, column
                             const uint32_t id = s_id[e];    // instruction descriptor
                             const uint64_t da = desc_sbo(wc + t0.x, sbo) + kgrp;
@@ -615,8 +609,8 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         for (int set = 0; set < 2; ++set) {
             for (int b = half; b < nblk; b += 2)
                 for (int c = 0; c < 2 * Cog; c += 8)
-                    tmem_st8_zero(lane_base + (uint32_t)set * p.set_cols + (uint32_t)(b * 2 * Cog + c));
-            tmem_wait_st();
+                    tc::tmem_st8_zero(lane_base + (uint32_t)set * p.set_cols + (uint32_t)(b * 2 * Cog + c));
+            tc::tmem_wait_st();
             tc::fence_before();
             dev::mbar_arrive(&acc_empty[set]);
         }
@@ -648,8 +642,8 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                         tc::tmem_ld8(t0, v0);
                         tc::tmem_ld8(t0 + (uint32_t)Cog, v1);
                         tc::tmem_wait_ld();
-                        tmem_st8_zero(t0);
-                        tmem_st8_zero(t0 + (uint32_t)Cog);
+                        tc::tmem_st8_zero(t0);
+                        tc::tmem_st8_zero(t0 + (uint32_t)Cog);
                     }
                     if (p.stg) {
                         // the buffer's previous chunk (two before) has been stored
@@ -684,7 +678,7 @@ tc3dg_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                     }
                 }
             }
-            tmem_wait_st();
+            tc::tmem_wait_st();
             tc::fence_before();
             dev::mbar_arrive(&acc_empty[set]);
         }
@@ -873,6 +867,7 @@ bool make_gplan_3d(const Problem &pb, const Args *a, GPlan *out)
     // 16-byte multiples; its 32 KB of buffers take the third A slot
     const bool stg = pb.Lo[1] % 2 == 0 && pb.Lo[2] % 4 == 0 && (!a || ((uintptr_t)a->y % 16) == 0);
     p.stg = stg ? 1 : 0;
+    p.ipg = IPG;                 // the launch lowers it to 1 for reproducible results
     p.na = stg ? 2 : NA;
     const size_t e_area = stg ? (size_t)2 * NSB * kSChunk : 0;
     const size_t a_area = (size_t)p.na * p.a_slot;
@@ -978,11 +973,14 @@ cudaError_t launch_tc3dg(const Problem &pb, const Args &a)
     if (!status) return cudaErrorInvalidValue;
     int grid = sm_count();
     if (grid > p.nunits) grid = p.nunits;
+    // two issuing warps per group unless the caller asked for reproducible results
+    GParams pk = p;
+    pk.ipg = deterministic() ? 1 : IPG;
     if (tf)
         return launch_dependent(tc3dg_split_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
-                                tmXc, tmW[0], tmW[1], tmY, a.bias, a.y, p, status);
+                                tmXc, tmW[0], tmW[1], tmY, a.bias, a.y, pk, status);
     return launch_dependent(tc3dg_split_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
-                            tmXc, tmW[0], tmW[1], tmY, a.bias, a.y, p, status);
+                            tmXc, tmW[0], tmW[1], tmY, a.bias, a.y, pk, status);
 }
 
 }  // namespace ct

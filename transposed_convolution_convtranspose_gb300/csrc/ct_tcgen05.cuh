@@ -108,5 +108,15 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
+// Warp-wide: 8 consecutive 32-bit columns of the warp's 32 TMEM lanes set to zero.
+__device__ __forceinline__ void tmem_st8_zero(uint32_t taddr)
+{
+    const uint32_t z = 0u;
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(z),
+                 "r"(z), "r"(z), "r"(z), "r"(z), "r"(z), "r"(z), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
 }  // namespace tc
 }  // namespace ct

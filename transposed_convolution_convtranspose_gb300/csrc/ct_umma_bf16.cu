@@ -174,7 +174,10 @@ __device__ __forceinline__ uint64_t desc_sw128_sbo(uint32_t saddr, uint32_t sbo)
 }
 
 // ---- GEMM kernel -------------------------------------------------------------
-template <bool SPLIT>
+// SPLIT: the last round's pairs run as single tiles.  CL: channels-last y (a
+// template parameter so that each layout's epilogue is compiled alone: the
+// two share the kernel's 80 registers).
+template <bool SPLIT, bool CL>
 __global__ void __launch_bounds__(kThreads, 1)
 umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const float *__restrict__ bias, float *__restrict__ y, const __grid_constant__ UParams p,
@@ -184,7 +187,8 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __shared__ __align__(8) uint64_t a_full[MAXA], a_empty[MAXA], b_full[MAXB], b_empty[MAXB], acc_full[2][2],
         acc_empty[2][2], drain_bar[NMMA];
     __shared__ uint32_t tmem_slot;
-    __shared__ float s_bias[256];
+    // channels last, the epilogue reads 4 bias values per 16-byte load
+    __shared__ alignas(CL ? 16 : 4) float s_bias[256];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;                                // na x a_slot
     uint8_t *sB = smem + (size_t)p.na * p.a_slot;      // nb x (wg x b_bytes)
@@ -438,7 +442,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         dev::mbar_arrive(&acc_empty[a][wr]);
                         released = true;
                     }
-                    if (ok && valid && p.cl) {
+                    if (ok && valid && CL) {
                         // 16 channels of one position: 64 contiguous bytes
 #pragma unroll
                         for (int b = 0; b < EB; ++b) {
@@ -852,8 +856,12 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
         return cudaErrorInvalidValue;
 
     int per_sm = 0;
-    e = prepare_kernel((const void *)&umma_ct3d_kernel<false>, kThreads, pl.smem, &per_sm);
-    if (e == cudaSuccess) e = prepare_kernel((const void *)&umma_ct3d_kernel<true>, kThreads, pl.smem, &per_sm);
+    const void *fn_pair = pb.cl ? (const void *)&umma_ct3d_kernel<false, true>
+                                : (const void *)&umma_ct3d_kernel<false, false>;
+    const void *fn_split = pb.cl ? (const void *)&umma_ct3d_kernel<true, true>
+                                 : (const void *)&umma_ct3d_kernel<true, false>;
+    e = prepare_kernel(fn_pair, kThreads, pl.smem, &per_sm);
+    if (e == cudaSuccess) e = prepare_kernel(fn_split, kThreads, pl.smem, &per_sm);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     unsigned int *status = device_status_ptr();
@@ -868,11 +876,17 @@ cudaError_t launch_umma(const Problem &pb, const Args &a)
     if (p.nacc == 2 && rem > 0 && 2 * rem <= grid) {
         pk.npair = p.ntiles - rem;
         pk.nunits = pk.npair + 2 * rem;
-        return launch_dependent(umma_ct3d_kernel<true>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmA,
-                                tmB, a.bias, a.y, pk, status);
+        if (pb.cl)
+            return launch_dependent(umma_ct3d_kernel<true, true>, dim3((unsigned)grid), dim3(kThreads), pl.smem,
+                                    a.stream, tmA, tmB, a.bias, a.y, pk, status);
+        return launch_dependent(umma_ct3d_kernel<true, false>, dim3((unsigned)grid), dim3(kThreads), pl.smem,
+                                a.stream, tmA, tmB, a.bias, a.y, pk, status);
     }
-    return launch_dependent(umma_ct3d_kernel<false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream, tmA, tmB,
-                            a.bias, a.y, pk, status);
+    if (pb.cl)
+        return launch_dependent(umma_ct3d_kernel<false, true>, dim3((unsigned)grid), dim3(kThreads), pl.smem,
+                                a.stream, tmA, tmB, a.bias, a.y, pk, status);
+    return launch_dependent(umma_ct3d_kernel<false, false>, dim3((unsigned)grid), dim3(kThreads), pl.smem, a.stream,
+                            tmA, tmB, a.bias, a.y, pk, status);
 }
 
 }  // namespace ct

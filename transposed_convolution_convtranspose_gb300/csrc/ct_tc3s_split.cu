@@ -34,9 +34,10 @@
 //               ring slot has exactly one producer
 //   warp 4      TMEM allocation and MMA issue
 //   warps 5-20  epilogue: 16-channel chunks of a unit (16 channels x MH rows x
-//               s_W QWp outputs); warp w reads TMEM lane quarter w mod 4 for
-//               4 channels of every W phase, adds bias (and applies the fused
-//               epilogue) in the chunk buffer
+//               s_W QWp outputs), in two groups of 8 warps that take alternate
+//               chunks, so that two are written at once; warp w reads TMEM lane
+//               quarter w mod 4 for 8 channels of every W phase, adds bias (and
+//               applies the fused epilogue) in the chunk buffer
 //   warp 21     chunk mover: makes chunks ready two ahead (TMA load of the add
 //               values, or the release of the buffer) and stores each written
 //               chunk with one TMA store through the tensor map of the unit's H
@@ -196,7 +197,7 @@ tc3s_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         dev::mbar_init(&drain_bar, 1);
         for (int b = 0; b < NE; ++b) {
             dev::mbar_init(&e_full[b], 1);
-            dev::mbar_init(&c_full[b], kEpiThreads);
+            dev::mbar_init(&c_full[b], kEpiThreads / 2);   // one group of epilogue warps writes a chunk
         }
         dev::fence_mbar_init();
     }
@@ -404,12 +405,15 @@ tc3s_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                     dev::mbar_wait_bounded(&e_full[r % NE], (r / NE) & 1, kWaitLimitNs);
         }
     } else {
-        // ---------------- epilogue: warp w reads TMEM lane quarter w mod 4; the four
-        // warps of a quarter take 4 channels each of the 16 of a chunk.  A thread
-        // holds position m = 32 (w mod 4) + lane: row m / QWp, q m mod QWp, whose
-        // s_W outputs s_W q + rW are consecutive in the chunk's row.
+        // ---------------- epilogue: warp w reads TMEM lane quarter w mod 4.  The
+        // warps form two groups that take alternate chunks (chunk gc goes to group
+        // gc mod 2), so two chunks are written at once; the two warps of a group
+        // and lane quarter take 8 channels each of the chunk's 16.  A thread holds
+        // position m = 32 (w mod 4) + lane: row m / QWp, q m mod QWp, whose s_W
+        // outputs s_W q + rW are consecutive in the chunk's row.
         const int ew = warp & 3;
-        const int cq = (warp - kEpiWarp0) >> 2;
+        const int e = (warp - kEpiWarp0) >> 2;          // 0 .. 3
+        const int grp = e >> 1, ch = e & 1;
         const int nchunk = C_out / 16;
         const int SW = p.SW;
         const int rowlen = SW * p.QWp;                  // floats of a chunk row
@@ -422,6 +426,8 @@ tc3s_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             const int use = p.nacc == 2 ? (k >> 1) : k;
             const int rp = s_unit((int)blockIdx.x + k * (int)gridDim.x, p).rp;
             const uint32_t wm = p.wmask[rp];
+            // every thread waits for every unit, so that no arrival on acc_empty
+            // runs a phase ahead
             if (ok && !dev::mbar_wait_bounded(&acc_full[a], use & 1, kWaitLimitNs)) {
                 atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
                 ok = false;
@@ -429,32 +435,43 @@ tc3s_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             ok = __all_sync(0xffffffffu, ok);        // warp-uniform before .sync.aligned loads
             tc::fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols;
-            for (int c = 0; c < nchunk; ++c, ++gc) {
-                const int b = gc % NE;
-                const int c0 = c * 16 + cq * 4;            // this warp's first channel
-                float v[MAXS][4];
+            // this group's chunks of the unit: gc0 + c with (gc0 + c) mod 2 == grp
+            const int gc0 = gc;
+            const int cfirst = (gc0 & 1) == grp ? 0 : 1;
+            int clast = -1;
+            for (int c = cfirst; c < nchunk; c += 2) clast = c;
+            if (clast < 0) {                           // no chunk of this unit: release at once
+                tc::fence_before();
+                dev::mbar_arrive(&acc_empty[a]);
+            }
+            for (int c = cfirst; c < nchunk; c += 2) {
+                const int g2 = gc0 + c;
+                const int b = g2 % NE;
+                const int c0 = c * 16 + ch * 8;            // this warp's first channel
+                float v[MAXS][8];
 #pragma unroll
                 for (int rw = 0; rw < MAXS; ++rw) {
-                    v[rw][0] = v[rw][1] = v[rw][2] = v[rw][3] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[rw][i] = 0.f;
                     if (ok && rw < SW && ((wm >> rw) & 1u))   // unit-uniform: the warp loads or skips together
-                        tmem_ld4(tbase + (uint32_t)(p.slot[rw] * C_out + c0), v[rw]);
+                        tc::tmem_ld8(tbase + (uint32_t)(p.slot[rw] * C_out + c0), v[rw]);
                 }
-                if (ok && !dev::mbar_wait_bounded(&e_full[b], (gc / NE) & 1, kWaitLimitNs)) {
+                if (ok && !dev::mbar_wait_bounded(&e_full[b], (g2 / NE) & 1, kWaitLimitNs)) {
                     atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
                     ok = false;
                 }
                 ok = __all_sync(0xffffffffu, ok);
                 tc::tmem_wait_ld();
-                if (c == nchunk - 1) {                  // the unit's last loads: free the accumulators
+                if (c == clast) {                       // this thread's last loads of the unit
                     tc::fence_before();
                     dev::mbar_arrive(&acc_empty[a]);
                 }
                 if (ok) {
                     float *buf = reinterpret_cast<float *>(sE + (size_t)b * p.echunk);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < 8; ++i) {
                         const float bb = s_bias[c0 + i];
-                        float *row = buf + ((cq * 4 + i) * p.MH + qh_l) * rowlen + SW * qw;
+                        float *row = buf + ((ch * 8 + i) * p.MH + qh_l) * rowlen + SW * qw;
 #pragma unroll
                         for (int rw = 0; rw < MAXS; ++rw) {
                             if (rw < SW) {
@@ -468,6 +485,7 @@ tc3s_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                 dev::fence_proxy_async();
                 dev::mbar_arrive(&c_full[b]);
             }
+            gc = gc0 + nchunk;
         }
     }
 

@@ -47,16 +47,17 @@
 // counters.
 //
 // Roles (persistent CTA, one per SM):
-//   warps 0-1   TMA producers of the A ring (x_c 5-D boxes of 128 positions
+//   warps 0-2   TMA producers of the A ring (x_c 5-D boxes of 128 positions
 //               x 128 bytes of channels at the offset; boxes reaching outside
-//               the input read zeros, which is the boundary handling)
-//   warps 2-3   TMA producers of the B ring (a run's panel is two boxes: its
+//               the input read zeros, which is the boundary handling): three
+//               for a ring of three slots, else two of them
+//   warps 3-4   TMA producers of the B ring (a run's panel is two boxes: its
 //               hi / t rows, then its lo / l rows).  Each ring slot has
 //               exactly one producer, which refills it only after waiting for
 //               its previous round, so a parity wait never has to tell two
 //               phases apart
-//   warp 4      TMEM allocation and MMA issue
-//   warps 5-20  epilogue, in chunks of 16 channels of a unit; warp w reads TMEM
+//   warp 5      TMEM allocation and MMA issue
+//   warps 6-21  epilogue, in chunks of 16 channels of a unit; warp w reads TMEM
 //               lane quarter w mod 4 for one H phase and 8 channels and adds
 //               bias (and applies the fused epilogue) to each position's even
 //               and odd W outputs, one float2.  Fused and channels first, the
@@ -65,12 +66,12 @@
 //               128-byte segments), so the kernel needs no staging buffers and
 //               its B slots hold runs of N = 256.  Otherwise each chunk (16
 //               channels x the unit's 2 MH output rows x the whole W extent,
-//               32 KB) is staged in one of three shared-memory buffers, the add
-//               values arriving there by a TMA load two chunks ahead
-//   warp 21     chunk mover (staged epilogue): makes chunks ready two ahead
-//               (the TMA load of the add values, or the release of the buffer)
-//               and stores each written chunk with one TMA store (rows and
-//               planes past the output are clipped)
+//               32 KB) is staged in one of two or three shared-memory buffers,
+//               the add values arriving there by a TMA load two chunks ahead
+//   warp 22     chunk mover (staged epilogue): makes chunks ready one or two
+//               ahead (the TMA load of the add values, or the release of the
+//               buffer) and stores each written chunk with one TMA store (rows
+//               and planes past the output are clipped)
 // Every mbarrier wait is bounded: a timeout records CT_ERR_DEVICE_TIMEOUT in
 // the device status word and the roles unwind (each producer waits, bounded,
 // for its own TMA copies and the MMA issuer for its own MMAs before the TMEM
@@ -90,10 +91,11 @@ namespace {
 constexpr int BM = 128;          // positions per unit (UMMA M)
 constexpr int CK = 32;           // input channels per K block: one 128-byte row of bf16 (hi, lo) pairs, or
                                  // of tf32 t parts plus one of l parts
-constexpr int NA = 4;            // A ring slots at most (bf16x2: 4 of 16 KB; tf32x3: 2 of 32 KB)
+constexpr int NA = 4;            // A ring slots at most (bf16x2: up to 4 of 16 KB; tf32x3: 2 or 3 of 32 KB)
 constexpr int NB = 2;            // B stages
-constexpr int NE = 3;            // epilogue chunk buffers (16 channels of a unit, 32 KB each)
-constexpr int NPA = 2;           // A producer warps: warp q loads the A stages g with g mod NPA == q
+constexpr int NE = 3;            // epilogue chunk buffers at most (16 channels of a unit, 32 KB each)
+constexpr int NPA = 3;           // A producer warps: p.npa of them, warp q loading the A stages g with
+                                 // g mod p.npa == q (p.npa divides the ring's p.na slots)
 constexpr int NPB = 2;           // B producer warps: warp q loads the B stages g with g mod NPB == q
 constexpr int MAXE = 18;         // input offsets per D residue (2 x 3 x 3 for extents <= 4)
 constexpr int MAXR = 64;         // runs per D residue
@@ -109,7 +111,7 @@ constexpr uint32_t kAHalf = BM * 128;          // 128 positions x one 128-byte r
 constexpr uint32_t kEChunk = 16 * 4 * BM * 4;  // 16 channels x 4 phases x 128 positions, fp32: 32 KB
 constexpr int kEpiThreads = 32 * 4 * EPW;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-static_assert(NB % NPB == 0 && NA % NPA == 0, "one producer per ring slot");
+static_assert(NB % NPB == 0, "one producer per ring slot");
 
 // One input offset a unit reads; its runs are run[rd][run0 .. run0 + nrun).
 struct Entry {
@@ -139,6 +141,8 @@ struct T3Params {
     int QD, QH, QW, MH, n_qhb;
     int n_kb;                    // K blocks: C_in / 32
     int na;                      // A ring slots
+    int npa;                     // A producers (3 for a ring of 3 slots, else 2)
+    int ne;                      // epilogue chunk buffers (staged epilogue: 2 or 3)
     uint32_t aslot;              // bytes of an A ring slot: 16 KB (bf16x2) or 32 KB (tf32x3: t rows, l rows)
     int nunits;
     int nacc;                    // accumulator sets (1 or 2)
@@ -199,7 +203,7 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = sm;                                  // na x aslot
     uint8_t *sB = sm + (size_t)p.na * p.aslot;         // NB x bslot
-    uint8_t *sE = sB + NB * p.bslot;                   // NE x kEChunk (channels last only)
+    uint8_t *sE = sB + NB * p.bslot;                   // ne x kEChunk (staged epilogue only)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -246,10 +250,10 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         // per 400 ns however deep the ring, so each ring has several producers,
         // warp q of a ring taking the stages g with g mod (producers) == q: the
         // ring slots g mod nst of one producer are its own.
-        if (lane == 0) {
-            const bool isA = warp < kBWarp0;
-            const int q = isA ? warp - kAWarp0 : warp - kBWarp0;
-            const int np = isA ? NPA : NPB;
+        const bool isA = warp < kBWarp0;
+        const int q = isA ? warp - kAWarp0 : warp - kBWarp0;
+        if (lane == 0 && (!isA || q < p.npa)) {
+            const int np = isA ? p.npa : NPB;
             const int nst = isA ? p.na : NB;
             uint64_t *fullb = isA ? a_full : b_full;
             uint64_t *emptyb = isA ? a_empty : b_empty;
@@ -401,15 +405,16 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
         }
     } else if (warp == kStoreWarp) {
         if (ADD && !CL) goto done;                  // fused, channels first: the epilogue warps store directly
-        // ---------------- chunk mover (channels last).  Buffer gc mod NE holds chunk gc (16 channels of a
+        // ---------------- chunk mover (staged epilogue).  Buffer gc mod ne holds chunk gc (16 channels of a
         // unit: 16 x 2 MH rows x the whole W extent, 32 KB).  Chunk gc is made ready
-        // two chunks ahead -- its add values loaded by TMA, or (no add) the buffer
+        // ne - 1 chunks ahead -- its add values loaded by TMA, or (no add) the buffer
         // released -- and stored by TMA once the epilogue warps have written it.
         const int nchunk = C_out / 16;
         const int total = nunit_cta * nchunk;
+        const int ne = p.ne;
         bool ok = true;
         auto ready = [&](int gc) {
-            const int b = gc % NE;
+            const int b = gc % ne;
             if (ADD) {
                 const UnitCoord v = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
                 dev::mbar_arrive_expect_tx(&e_full[b], kEChunk);
@@ -424,11 +429,11 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             }
         };
         if (lane == 0) {
-            for (int gc = 0; gc < 2 && gc < total; ++gc) ready(gc);
+            for (int gc = 0; gc < ne - 1 && gc < total; ++gc) ready(gc);
             for (int gc = 0; gc < total && ok; ++gc) {
-                // the epilogue threads wrote chunk gc (they run at most two chunks ahead,
+                // the epilogue threads wrote chunk gc (they run at most ne - 1 chunks ahead,
                 // so the parity of a buffer's barrier is unambiguous)
-                if (!dev::mbar_wait_bounded(&c_full[gc % NE], (gc / NE) & 1, kWaitLimitNs)) {
+                if (!dev::mbar_wait_bounded(&c_full[gc % ne], (gc / ne) & 1, kWaitLimitNs)) {
                     atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
                     ok = false;
                     break;
@@ -436,20 +441,20 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                 const UnitCoord u = unit_coord((int)blockIdx.x + (gc / nchunk) * (int)gridDim.x, p);
                 // rows and planes past the output are clipped by the store
                 if (CL)
-                    dev::tma_store_5d(&tmY, sE + (size_t)(gc % NE) * kEChunk, (gc % nchunk) * 16, 0,
+                    dev::tma_store_5d(&tmY, sE + (size_t)(gc % ne) * kEChunk, (gc % nchunk) * 16, 0,
                                       2 * u.qhb * p.MH, p.SD * u.qd + u.rd, u.n);
                 else
-                    dev::tma_store_4d(&tmY, sE + (size_t)(gc % NE) * kEChunk, 0, 2 * u.qhb * p.MH,
+                    dev::tma_store_4d(&tmY, sE + (size_t)(gc % ne) * kEChunk, 0, 2 * u.qhb * p.MH,
                                       p.SD * u.qd + u.rd, u.n * C_out + (gc % nchunk) * 16);
                 dev::bulk_commit();
                 dev::bulk_wait_read<1>();               // chunk gc - 1's store has read its buffer
-                if (gc + 2 < total) ready(gc + 2);      // into that buffer
+                if (gc + ne - 1 < total) ready(gc + ne - 1);   // into that buffer
             }
             dev::bulk_wait_all();
             // loads this thread issued that nobody consumed (only after a timeout)
             if (ADD)
-                for (int r = total - 2 > 0 ? total - 2 : 0; r < total; ++r)
-                    dev::mbar_wait_bounded(&e_full[r % NE], (r / NE) & 1, kWaitLimitNs);
+                for (int r = total - (ne - 1) > 0 ? total - (ne - 1) : 0; r < total; ++r)
+                    dev::mbar_wait_bounded(&e_full[r % ne], (r / ne) & 1, kWaitLimitNs);
         }
     } else {
         // ---------------- epilogue: warp w reads TMEM lane quarter w mod 4; the four
@@ -564,7 +569,7 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
             const int row = 2 * (m / p.QW) + rh, qw = m % p.QW;
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols;
             for (int c = 0; c < nchunk; ++c, ++gc) {
-                const int b = gc % NE;
+                const int b = gc % p.ne;
                 const int c0 = c * 16 + ch * 8;             // this warp's first channel
                 float2 *q = reinterpret_cast<float2 *>(sE + (size_t)b * kEChunk) + (row * Lo2 + 2 * qw) / 2 +
                             ch * 8 * cstride;
@@ -574,7 +579,7 @@ tc3d_split_kernel(const __grid_constant__ CUtensorMap tmXc,
                     tc::tmem_ld8(tbase + (uint32_t)(p.slot[rh * 2] * C_out + c0), v0);
                     tc::tmem_ld8(tbase + (uint32_t)(p.slot[rh * 2 + 1] * C_out + c0), v1);
                 }
-                if (ok && !dev::mbar_wait_bounded(&e_full[b], (gc / NE) & 1, kWaitLimitNs)) {
+                if (ok && !dev::mbar_wait_bounded(&e_full[b], (gc / p.ne) & 1, kWaitLimitNs)) {
                     atomicExch(status, (unsigned)CT_ERR_DEVICE_TIMEOUT);
                     ok = false;
                 }
@@ -822,18 +827,26 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     const bool direct = pb.has_add && !pb.cl;
     int maxlen = (direct ? 256 : 128) / pb.C_out;
     if (maxlen > 4) maxlen = 4;
-    // shared memory: A ring, B ring (slots of the longest run's panel) and, channels
-    // last, the epilogue's staging buffers; a ring of four A slots gives way to
-    // two, then runs get shorter, until they fit
+    // shared memory: A ring, B ring (slots of the longest run's panel) and, staged,
+    // the epilogue's chunk buffers.  Without an add, a ring of four A slots
+    // gives way to three and the third chunk buffer goes next (the A loads'
+    // latency, not the stores', holds the MMAs up there: 2-D 0.303 against
+    // 0.317 ms); with one, four A slots give way to two (three measured 5 %
+    // slower on the fused workload).  Then runs get shorter, until they fit
+    int ne = direct ? 0 : NE;
     {
-        const size_t ebytes = direct ? 0 : (size_t)NE * kEChunk;
         const size_t budget = 227 * 1024 - 2048;   // room for the alignment pad and the static barriers
-        while ((size_t)p.na * p.aslot + (size_t)NB * (2 * maxlen * pb.C_out) * 128 + ebytes > budget) {
-            if (p.na > 2) p.na = 2;
+        while ((size_t)p.na * p.aslot + (size_t)NB * (2 * maxlen * pb.C_out) * 128 + (size_t)ne * kEChunk >
+               budget) {
+            if (p.na > 3) p.na = pb.has_add ? 2 : 3;
+            else if (!pb.has_add && ne > 2) ne = 2;
+            else if (p.na > 2) p.na = 2;
             else if (maxlen > 1) --maxlen;
             else return false;
         }
     }
+    p.npa = p.na == 3 ? 3 : 2;
+    p.ne = direct ? 1 : ne;
     // the order of the four accumulators with the cheapest MMA schedule (the
     // first of equal ones, so the natural order when it is as good)
     static const int kPerm[24][4] = {
@@ -890,7 +903,7 @@ bool make_t3plan(const Problem &pb, const Args *a, T3Plan *out)
     while (cols < (uint32_t)p.nacc * p.acc_cols) cols <<= 1;
     p.tmem_cols = cols;
     p.bslot = (uint32_t)(2 * maxlen * pb.C_out) * 128u;
-    const size_t smem = (size_t)p.na * p.aslot + (size_t)NB * p.bslot + (direct ? 0 : (size_t)NE * kEChunk) + 1024;
+    const size_t smem = (size_t)p.na * p.aslot + (size_t)NB * p.bslot + (size_t)ne * kEChunk + 1024;
     if (smem > 227 * 1024 - 1024) return false;   // room for the static barriers
     out->p = p;
     out->wq = wq;

@@ -561,9 +561,8 @@ __device__ __forceinline__ void repack_x_block(const bf16_t *__restrict__ x, bf1
         const int o = threadIdx.x + 256 * t;
         const int q = o & 7, row = o >> 3;
         if (row < ncols) {
-            const int64_t s = s0 + row;                 // (d, h, w) of the source position
-            const int w = (int)(s % W), h = (int)((s / W) % H), d = (int)(s / ((int64_t)W * H));
-            const int64_t dst = ((((int64_t)n * D + d) * H + h) * W + w) * C + c0 + 8 * q;
+            // x_t's position index is the flat spatial index of x
+            const int64_t dst = ((int64_t)n * SP + s0 + row) * C + c0 + 8 * q;
             const uint4 v = make_uint4(tile[row][4 * q], tile[row][4 * q + 1], tile[row][4 * q + 2],
                                        tile[row][4 * q + 3]);
             *reinterpret_cast<uint4 *>(xt + dst) = v;
@@ -641,12 +640,13 @@ __device__ __forceinline__ void repack_w_block(const bf16_t *__restrict__ w, bf1
 
 // Both repacks in one launch: blocks [0, nxb) move x (nbx x nby per image),
 // the rest the weights (C_in / 64 per output channel).  The GEMM kernel is
-// launched as its programmatic dependent.
+// launched as its programmatic dependent once every block has done its work
+// (a trigger at the blocks' start let GEMM CTAs take SMs, and wait, while
+// repack blocks still needed them: 0.2184 against 0.2006 ms a step).
 __global__ void __launch_bounds__(256)
 repack_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, int C, int D, int H, int W, int nbx, int nby,
               int nxb, const bf16_t *__restrict__ w, bf16_t *__restrict__ wp, const __grid_constant__ WPackParams q)
 {
-    dev::griddep_launch_dependents();
     const int b = (int)blockIdx.x;
     if (b < nxb) {
         const int per = nbx * nby;
@@ -655,6 +655,7 @@ repack_kernel(const bf16_t *__restrict__ x, bf16_t *__restrict__ xt, int C, int 
         const int r = b - nxb, nwx = q.C_in / RB;
         repack_w_block(w, wp, q, r % nwx, r / nwx);
     }
+    dev::griddep_launch_dependents();
 }
 
 // The weight repack alone (after the scalar x repack).

@@ -422,22 +422,24 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 float *ycl = y + ((((int64_t)tcd.n * p.Lo0 + od) * p.Lo1 + oh) * p.Lo2 + 2 * qw + wr) * p.C_out;
                 const uint32_t tbase =
                     tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols + (uint32_t)wr * p.C_out;
-                // EB chunks per batch; the half is released as soon as the warp's
+                // one chunk a batch in the split instance: its registers then need no spills
+                constexpr int EBK = SPLIT ? 1 : EB;
+                // EBK chunks per batch; the half is released as soon as the warp's
                 // last batch is in registers
                 bool released = false;
-                for (int ci = cfirst; ci < nchunk; ci += EB * cstep) {
-                    float v[EB][16];
+                for (int ci = cfirst; ci < nchunk; ci += EBK * cstep) {
+                    float v[EBK][16];
                     int nc = 0;
                     if (ok && act) {
 #pragma unroll
-                        for (int b = 0; b < EB; ++b)
+                        for (int b = 0; b < EBK; ++b)
                             if (ci + b * cstep < nchunk) {
                                 tc::tmem_ld16(tbase + (uint32_t)((ci + b * cstep) * 16), v[b]);
                                 nc = b + 1;
                             }
                         tc::tmem_wait_ld();
                     }
-                    if (ci + EB * cstep >= nchunk) {
+                    if (ci + EBK * cstep >= nchunk) {
                         tc::fence_before();
                         dev::mbar_arrive(&acc_empty[a][wr]);
                         released = true;
@@ -445,7 +447,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     if (ok && valid && CL) {
                         // 16 channels of one position: 64 contiguous bytes
 #pragma unroll
-                        for (int b = 0; b < EB; ++b) {
+                        for (int b = 0; b < EBK; ++b) {
                             if (b >= nc) break;
                             const int c0 = (ci + b * cstep) * 16;
                             float4 *dst = reinterpret_cast<float4 *>(ycl + c0);
@@ -458,7 +460,7 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         }
                     } else if (ok && valid) {
 #pragma unroll
-                        for (int b = 0; b < EB; ++b) {
+                        for (int b = 0; b < EBK; ++b) {
                             if (b >= nc) break;
                             const int c0 = (ci + b * cstep) * 16;
                             float *yc = yrow + (int64_t)c0 * sp;

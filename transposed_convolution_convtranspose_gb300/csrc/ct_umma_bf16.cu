@@ -422,8 +422,9 @@ umma_ct3d_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 float *ycl = y + ((((int64_t)tcd.n * p.Lo0 + od) * p.Lo1 + oh) * p.Lo2 + 2 * qw + wr) * p.C_out;
                 const uint32_t tbase =
                     tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)a * p.acc_cols + (uint32_t)wr * p.C_out;
-                // one chunk a batch in the split instance: its registers then need no spills
-                constexpr int EBK = SPLIT ? 1 : EB;
+                // one chunk a batch in the split and channels-last instances: their
+                // registers then need no spills
+                constexpr int EBK = (SPLIT || CL) ? 1 : EB;
                 // EBK chunks per batch; the half is released as soon as the warp's
                 // last batch is in registers
                 bool released = false;

@@ -759,8 +759,7 @@ bool make_uplan(const Problem &pb, UPlan *out)
     const size_t b_slot = (size_t)p.wg * p.b_bytes;
     // three A slots when at least four B slots still fit, else two; then 8, 6 or
     // 3 B slots, one producer per slot (3 measured faster than 4 when 4 fit:
-    // fewer panels in flight; and three A slots beside three B slots, where
-    // four would not fit, measured 2-5 % slower than two)
+    // fewer panels in flight)
     const size_t budget = 227 * 1024 - 3072;
     p.na = MAXA;
     while (p.na > 2 && (size_t)p.na * p.a_slot + 4 * b_slot > budget) --p.na;

@@ -1,5 +1,6 @@
 // ct_tma.cu -- host helpers: tensor-map encoding through the driver entry
-// point, SM count and per-kernel launch attributes (cached).
+// point, SM count (cached per device) and per-kernel launch attributes.
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -55,15 +56,15 @@ bool encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void
 
 int sm_count()
 {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];      // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!cache[dev]) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (!n) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *blocks_per_sm)
@@ -86,27 +87,26 @@ cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *blocks
             return std::hash<const void *>()(k.fn) ^ (k.smem * 131) ^ ((size_t)k.dev << 40) ^ k.threads;
         }
     };
+    // blocks per SM depend on the device, the function and the launch shape only
     static std::unordered_map<Key, int, Hash> cache;
-    // The shared-memory limit is an attribute of the function on a device, not
-    // of a launch: keep it at the largest size requested so far, so that a
-    // smaller request never lowers it under a larger one that was cached.
-    static std::unordered_map<Key, size_t, Hash> limit;
     const Key key{fn, dev, threads, smem};
-    const Key fkey{fn, dev, 0, 0};
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto it = cache.find(key);
-        if (it != cache.end()) {
-            *blocks_per_sm = it->second;
-            return cudaSuccess;
-        }
-    }
     std::lock_guard<std::mutex> lk(g_mu);
-    auto lt = limit.find(fkey);
-    if (lt == limit.end() || lt->second < smem) {
+    // The dynamic shared-memory limit is an attribute of the function in the
+    // current context, which a cudaDeviceReset (or a context of the caller's
+    // own) starts again from the default: it is read back on every call and
+    // raised when below the request -- never lowered, so that a smaller request
+    // does not undercut a larger launch of the same function.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    if ((size_t)fa.maxDynamicSharedSizeBytes < smem) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        limit[fkey] = smem;
+    }
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *blocks_per_sm = it->second;
+        return cudaSuccess;
     }
     int per = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fn, threads, smem);

@@ -19,8 +19,9 @@ bool encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
-// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (function, size)
-// and the resulting blocks per SM (cached).
+// Raise the function's dynamic shared-memory limit (MaxDynamicSharedMemorySize,
+// read back on every call: it belongs to the current context) to `smem` if it
+// is lower, and report the blocks per SM for the launch shape (cached).
 cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *blocks_per_sm);
 
 // Launch `kernel` on `stream` as a programmatic dependent of the kernel

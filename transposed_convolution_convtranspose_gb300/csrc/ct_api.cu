@@ -257,7 +257,11 @@ ct_status run(const Problem &pb, Args a)
     case Path::Tc3dg: e = launch_tc3dg(pb, a); break;
     case Path::Tc3s: e = launch_tc3s(pb, a); break;
     }
-    return e == cudaSuccess ? CT_OK : CT_ERR_CUDA;
+    if (e == cudaSuccess) return CT_OK;
+    // the failure is reported as CT_ERR_CUDA; clear the runtime's last-error slot
+    // so that the caller's next error check does not take it for its own
+    (void)cudaGetLastError();
+    return CT_ERR_CUDA;
 }
 
 }  // namespace

@@ -729,6 +729,85 @@ def test_fp32_1d_tensor_core_and_ffma_paths(k, mode):
         ct.ct_set_path_override(0)
 
 
+# A seeded sweep of the tensor-core planners: per family, random draws within
+# the family's range (channel counts, kernel extents, padding, output padding,
+# spatial extents with ragged tiles, batch, fused epilogue, channels-last
+# layout), kept when the host path query names the family's kernel.  Inputs
+# stay small enough for the oracle to finish each case in well under a second.
+def _tc_sweep(family, n, seed):
+    rng = np.random.default_rng(seed)
+    pick = lambda seq: seq[int(rng.integers(0, len(seq)))]
+    out = []
+    for _ in range(5000):
+        if len(out) == n:
+            break
+        layout, add, G, dtype = "cf", False, 1, "f32"
+        if family == "tc3d":
+            nd = pick([2, 3])
+            C_in, C_out = pick([32, 64]), pick([16, 32, 48, 64, 96, 128])
+            K = [int(rng.integers(2, 5)) for _ in range(nd)]
+            S, DL = [2] * nd, [1] * nd
+            L = ([int(rng.integers(1, 5))] if nd == 3 else []) + [int(rng.integers(1, 8)), pick([2, 4, 8, 16, 32])]
+            add, layout = bool(rng.integers(0, 2)), pick(["cf", "cf", "cl"])
+            want = "tc3d_tf32x3"
+        elif family == "tc3dg":
+            nd = pick([2, 3])
+            G = pick([1, 2, 4])
+            C_in, C_out = 32, G * pick([8, 16])
+            K = [int(rng.integers(1, 8)) for _ in range(nd)]
+            S, DL = [2] * nd, [1] * nd
+            L = ([int(rng.integers(1, 5))] if nd == 3 else []) + [int(rng.integers(1, 9)), int(rng.integers(2, 20))]
+            want = "tc3dg_tf32x3"
+        elif family == "tc3s":
+            nd = pick([1, 2, 3])
+            C_in, C_out = pick([32, 64]), pick([16, 32, 64])
+            S = [int(rng.integers(1, 5)) for _ in range(nd)]
+            DL = [pick([1, 1, 2]) for _ in range(nd)]
+            K = [int(rng.integers(1, 6)) for _ in range(nd)]
+            L = [int(rng.integers(1, 5)) for _ in range(nd - 1)] + [int(rng.integers(2, 12))]
+            if nd == 1:
+                L = [int(rng.integers(8, 200))]
+            add = bool(rng.integers(0, 3) == 0)
+            want = "tc3s_tf32x3"
+        else:
+            nd = pick([2, 3])
+            C_in, C_out = pick([64, 128]), pick([16, 32, 48, 64, 96, 128, 256])
+            k = pick([2, 4]) if nd == 3 else pick([4, 4, 8])
+            K, S, DL = [k] * nd, [2] * nd, [1] * nd
+            L = ([int(rng.integers(1, 4))] if nd == 3 else []) + [int(rng.integers(1, 8)), int(rng.integers(2, 20))]
+            dtype, layout = "bf16", pick(["cf", "cl"])
+            want = "umma_bf16"
+        P = [int(rng.integers(0, max(1, DL[d] * (K[d] - 1) // 2 + 1))) for d in range(nd)]
+        OP = [int(rng.integers(0, max(S[d], DL[d]))) for d in range(nd)]
+        c = dict(nd=nd, N=pick([1, 1, 2]), C_in=C_in, C_out=C_out, G=G, L=L, K=K, S=S, P=P, OP=OP,
+                 DL=DL, bias=bool(rng.integers(0, 2)), add=add, dtype=dtype, layout=layout)
+        if min(cc.out_shape(c)[2:]) < 1:
+            continue
+        if path_of(c) == want:
+            out.append(c)
+    assert len(out) == n, "%s: only %d of %d shapes found" % (family, len(out), n)
+    return out
+
+
+@pytest.mark.parametrize("family,n,seed", [("tc3d", 16, 51), ("tc3dg", 10, 52), ("tc3s", 14, 53),
+                                           ("umma", 12, 54)])
+def test_random_tensor_core_planner_sweep(family, n, seed):
+    for k, c in enumerate(_tc_sweep(family, n, seed)):
+        t = cc.make_inputs(c, seed=2000 + 100 * seed + k)
+        y = cc.run_gpu(c, t).cpu().numpy()
+        cc.assert_close(y, cc.run_oracle(c, t), c["dtype"], "%s sweep case %d %r" % (family, k, c))
+        if k % 3 == 0:
+            # small integers: every product and partial sum is exact (the fused
+            # epilogue's division by 6 is compared at fp32 tolerance)
+            ti = cc.make_inputs(c, seed=3000 + 100 * seed + k, int_range=3)
+            yi = cc.run_gpu(c, ti).cpu().numpy()
+            ri = cc.run_oracle(c, ti)
+            if c["add"]:
+                cc.assert_close(yi, ri, "f32", "%s sweep integer case %d" % (family, k))
+            else:
+                assert np.array_equal(yi.astype(np.float64), ri), "%s sweep integer case %d %r" % (family, k, c)
+
+
 def test_bounded_wait_timeout_reports_and_recovers():
     """A kernel whose bounded mbarrier wait runs out records the timeout in the
     device status word; the host reads it once, and the context stays usable."""

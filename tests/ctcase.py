@@ -72,6 +72,9 @@ def run_gpu(c, t, dev="cuda:0", inplace_add=False):
         y = ct.conv_transpose_cl(xcl, w, b, acl, out=acl if inplace_add else None, **kw)
         return y.movedim(-1, 1).contiguous()
     if c["nd"] == 1:
+        if c["add"]:
+            # no channels-first 1-D fused entry point (the channels-last one has it)
+            raise ValueError("fused 1-D case needs layout 'cl': %r" % (c,))
         y = ct.conv_transpose1d(x, w, b, **kw)
     elif c["nd"] == 2:
         if c["add"]:

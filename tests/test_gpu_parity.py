@@ -756,7 +756,7 @@ def _tc_sweep(family, n, seed):
             C_in, C_out = 32, G * pick([8, 16])
             K = [int(rng.integers(1, 8)) for _ in range(nd)]
             S, DL = [2] * nd, [1] * nd
-            L = ([int(rng.integers(1, 5))] if nd == 3 else []) + [int(rng.integers(1, 9)), int(rng.integers(2, 20))]
+            L = ([int(rng.integers(1, 5))] if nd == 3 else []) + [int(rng.integers(1, 17)), int(rng.integers(2, 40))]
             want = "tc3dg_tf32x3"
         elif family == "tc3s":
             nd = pick([1, 2, 3])
@@ -767,7 +767,7 @@ def _tc_sweep(family, n, seed):
             L = [int(rng.integers(1, 5)) for _ in range(nd - 1)] + [int(rng.integers(2, 12))]
             if nd == 1:
                 L = [int(rng.integers(8, 200))]
-            add = bool(rng.integers(0, 3) == 0)
+            add = nd > 1 and bool(rng.integers(0, 3) == 0)     # no channels-first 1-D fused call
             want = "tc3s_tf32x3"
         else:
             nd = pick([2, 3])
@@ -779,7 +779,7 @@ def _tc_sweep(family, n, seed):
             want = "umma_bf16"
         P = [int(rng.integers(0, max(1, DL[d] * (K[d] - 1) // 2 + 1))) for d in range(nd)]
         OP = [int(rng.integers(0, max(S[d], DL[d]))) for d in range(nd)]
-        c = dict(nd=nd, N=pick([1, 1, 2]), C_in=C_in, C_out=C_out, G=G, L=L, K=K, S=S, P=P, OP=OP,
+        c = dict(nd=nd, N=pick([1, 1, 2, 4]), C_in=C_in, C_out=C_out, G=G, L=L, K=K, S=S, P=P, OP=OP,
                  DL=DL, bias=bool(rng.integers(0, 2)), add=add, dtype=dtype, layout=layout)
         if min(cc.out_shape(c)[2:]) < 1:
             continue
@@ -789,8 +789,8 @@ def _tc_sweep(family, n, seed):
     return out
 
 
-@pytest.mark.parametrize("family,n,seed", [("tc3d", 16, 51), ("tc3dg", 10, 52), ("tc3s", 14, 53),
-                                           ("umma", 12, 54)])
+@pytest.mark.parametrize("family,n,seed", [("tc3d", 32, 51), ("tc3dg", 24, 52), ("tc3s", 32, 53),
+                                           ("umma", 24, 54)])
 def test_random_tensor_core_planner_sweep(family, n, seed):
     for k, c in enumerate(_tc_sweep(family, n, seed)):
         t = cc.make_inputs(c, seed=2000 + 100 * seed + k)

@@ -732,9 +732,10 @@ def test_fp32_1d_tensor_core_and_ffma_paths(k, mode):
 # A seeded sweep of the tensor-core planners: per family, random draws within
 # the family's range (channel counts, kernel extents, padding, output padding,
 # spatial extents with ragged tiles, batch, fused epilogue, channels-last
-# layout), kept when the host path query names the family's kernel.  Inputs
-# stay small enough for the oracle to finish each case in well under a second.
-def _tc_sweep(family, n, seed):
+# layout), kept when the host path query names the family's kernel (with
+# split2, the opt-in bf16 pair's).  Inputs stay small enough for the oracle to
+# finish each case in well under a second.
+def _tc_sweep(family, n, seed, split2=False):
     rng = np.random.default_rng(seed)
     pick = lambda seq: seq[int(rng.integers(0, len(seq)))]
     out = []
@@ -780,7 +781,9 @@ def _tc_sweep(family, n, seed):
         P = [int(rng.integers(0, max(1, DL[d] * (K[d] - 1) // 2 + 1))) for d in range(nd)]
         OP = [int(rng.integers(0, max(S[d], DL[d]))) for d in range(nd)]
         c = dict(nd=nd, N=pick([1, 1, 2, 4]), C_in=C_in, C_out=C_out, G=G, L=L, K=K, S=S, P=P, OP=OP,
-                 DL=DL, bias=bool(rng.integers(0, 2)), add=add, dtype=dtype, layout=layout)
+                 DL=DL, bias=bool(rng.integers(0, 2)), add=add, dtype=dtype, layout=layout, split2=split2)
+        if split2:
+            want = want.replace("tf32x3", "bf16x2")
         if min(cc.out_shape(c)[2:]) < 1:
             continue
         if path_of(c) == want:
@@ -789,13 +792,35 @@ def _tc_sweep(family, n, seed):
     return out
 
 
-@pytest.mark.parametrize("family,n,seed", [("tc3d", 32, 51), ("tc3dg", 24, 52), ("tc3s", 32, 53),
-                                           ("umma", 24, 54)])
-def test_random_tensor_core_planner_sweep(family, n, seed):
-    for k, c in enumerate(_tc_sweep(family, n, seed)):
+@pytest.mark.parametrize("family,n,seed,split2", [
+    ("tc3d", 32, 51, False), ("tc3dg", 24, 52, False), ("tc3s", 32, 53, False), ("umma", 24, 54, False),
+    ("tc3d", 12, 61, True), ("tc3dg", 12, 62, True), ("tc3s", 12, 63, True)])
+def test_random_tensor_core_planner_sweep(family, n, seed, split2):
+    import torch
+    import transposed_convolution_convtranspose_gb300 as ct
+    for k, c in enumerate(_tc_sweep(family, n, seed, split2)):
         t = cc.make_inputs(c, seed=2000 + 100 * seed + k)
-        y = cc.run_gpu(c, t).cpu().numpy()
-        cc.assert_close(y, cc.run_oracle(c, t), c["dtype"], "%s sweep case %d %r" % (family, k, c))
+        yt = cc.run_gpu(c, t)
+        y = yt.cpu().numpy()
+        ref = cc.run_oracle(c, t)
+        cc.assert_close(y, ref, c["dtype"], "%s sweep case %d %r" % (family, k, c))
+        if c["dtype"] == "f32" and not c["add"]:
+            # the split's bound against sum |x||w| (+ |bias|, added in fp32):
+            # tf32x3 at fp32 level, the bf16 pair at about 16-bit operands
+            mag = dict(t, x=np.abs(t["x"]), w=np.abs(t["w"]), bias=None)
+            den = cc.run_oracle(dict(c, bias=False), mag)
+            if t["bias"] is not None:
+                den = den + np.abs(np.asarray(t["bias"], np.float64)).reshape([1, -1] + [1] * c["nd"])
+            r = float((np.abs(y.astype(np.float64) - ref) / (den + 1e-30)).max())
+            assert r < (2.0 ** -14 if split2 else 2.0 ** -19), "%s sweep case %d: error 2^%.1f of sum|x||w| %r" % (
+                family, k, np.log2(max(r, 1e-300)), c)
+        if family == "tc3dg" and k % 2 == 0:
+            # one issuing thread per group: repeated calls agree bit for bit
+            ct.ct_set_deterministic(1)
+            try:
+                assert torch.equal(cc.run_gpu(c, t), cc.run_gpu(c, t)), "%s sweep case %d" % (family, k)
+            finally:
+                ct.ct_set_deterministic(0)
         if k % 3 == 0:
             # small integers: every product and partial sum is exact (the fused
             # epilogue's division by 6 is compared at fp32 tolerance)

@@ -770,6 +770,31 @@ def _tc_sweep(family, n, seed, split2=False):
                 L = [int(rng.integers(8, 200))]
             add = nd > 1 and bool(rng.integers(0, 3) == 0)     # no channels-first 1-D fused call
             want = "tc3s_tf32x3"
+        elif family == "tc1d":
+            nd = 1
+            C_in, C_out = 32, pick([16, 32, 48, 64, 96, 128])
+            K, S = [int(rng.integers(1, 5))], [int(rng.integers(1, 5))]
+            DL = [S[0] * pick([1, 2])]
+            L = [4 * int(rng.integers(1, 600))]
+            want = "tc1d_tf32x3"
+        elif family == "ffma":
+            # the FFMA phase kernels (path override 2 keeps the tensor cores out):
+            # any 1-D shape; in 3-D the compiled kernel shapes, k 3 (W padding 1)
+            # and the grouped k (3, 5, 7) (W padding 3)
+            nd = pick([1, 3])
+            if nd == 1:
+                C_in, C_out = pick([4, 8, 16, 32]), pick([4, 8, 16, 32, 64])
+                K, S, DL = [int(rng.integers(1, 5))], [int(rng.integers(1, 4))], [pick([1, 1, 2])]
+                L = [int(rng.integers(2, 700))]
+            else:
+                grouped = bool(rng.integers(0, 2))
+                G = pick([1, 2, 4]) if grouped else 1
+                K = [3, 5, 7] if grouped else [3, 3, 3]
+                C_in, C_out = G * pick([4, 8]), G * (8 if grouped else 16) * pick([1, 2])
+                S, DL = [2] * 3, [1] * 3
+                L = [int(rng.integers(1, 5)), int(rng.integers(1, 9)), 4 * int(rng.integers(1, 9))]
+                add = bool(rng.integers(0, 3) == 0)
+            want = "phase1d_f32" if nd == 1 else "phase3d_f32"
         else:
             nd = pick([2, 3])
             C_in, C_out = pick([64, 128]), pick([16, 32, 48, 64, 96, 128, 256])
@@ -779,6 +804,8 @@ def _tc_sweep(family, n, seed, split2=False):
             dtype, layout = "bf16", pick(["cf", "cl"])
             want = "umma_bf16"
         P = [int(rng.integers(0, max(1, DL[d] * (K[d] - 1) // 2 + 1))) for d in range(nd)]
+        if family == "ffma" and nd == 3:
+            P[2] = (K[2] - 1) // 2                 # the compiled W padding
         OP = [int(rng.integers(0, max(S[d], DL[d]))) for d in range(nd)]
         c = dict(nd=nd, N=pick([1, 1, 2, 4]), C_in=C_in, C_out=C_out, G=G, L=L, K=K, S=S, P=P, OP=OP,
                  DL=DL, bias=bool(rng.integers(0, 2)), add=add, dtype=dtype, layout=layout, split2=split2)
@@ -794,8 +821,18 @@ def _tc_sweep(family, n, seed, split2=False):
 
 @pytest.mark.parametrize("family,n,seed,split2", [
     ("tc3d", 32, 51, False), ("tc3dg", 24, 52, False), ("tc3s", 32, 53, False), ("umma", 24, 54, False),
+    ("tc1d", 16, 55, False), ("ffma", 24, 56, False),
     ("tc3d", 12, 61, True), ("tc3dg", 12, 62, True), ("tc3s", 12, 63, True)])
 def test_random_tensor_core_planner_sweep(family, n, seed, split2):
+    import transposed_convolution_convtranspose_gb300 as ct
+    ct.ct_set_path_override(2 if family == "ffma" else 0)
+    try:
+        _run_sweep(family, n, seed, split2)
+    finally:
+        ct.ct_set_path_override(0)
+
+
+def _run_sweep(family, n, seed, split2):
     import torch
     import transposed_convolution_convtranspose_gb300 as ct
     for k, c in enumerate(_tc_sweep(family, n, seed, split2)):
@@ -804,7 +841,7 @@ def test_random_tensor_core_planner_sweep(family, n, seed, split2):
         y = yt.cpu().numpy()
         ref = cc.run_oracle(c, t)
         cc.assert_close(y, ref, c["dtype"], "%s sweep case %d %r" % (family, k, c))
-        if c["dtype"] == "f32" and not c["add"]:
+        if c["dtype"] == "f32" and not c["add"] and family != "ffma":
             # the split's bound against sum |x||w| (+ |bias|, added in fp32):
             # tf32x3 at fp32 level, the bf16 pair at about 16-bit operands
             mag = dict(t, x=np.abs(t["x"]), w=np.abs(t["w"]), bias=None)

@@ -795,6 +795,17 @@ def _tc_sweep(family, n, seed, split2=False):
                 L = [int(rng.integers(1, 5)), int(rng.integers(1, 9)), 4 * int(rng.integers(1, 9))]
                 add = bool(rng.integers(0, 3) == 0)
             want = "phase1d_f32" if nd == 1 else "phase3d_f32"
+        elif family == "cl_generic":
+            # channels-last shapes no tensor-core kernel takes: the generic kernel
+            # with layout strides (groups, any stride and dilation, fused 1-D too)
+            nd = pick([1, 2, 3])
+            r = oracle_pins.random_case(rng, nd)
+            C_in, C_out, G, K, S, DL, L = r["C_in"], r["C_out"], r["G"], r["K"], r["S"], r["DL"], r["L"]
+            add, layout = bool(rng.integers(0, 2)), "cl"
+            dtype = pick(["f32", "f32", "bf16"])
+            if dtype == "bf16":
+                add = False
+            want = "gather_generic"
         else:
             nd = pick([2, 3])
             C_in, C_out = pick([64, 128]), pick([16, 32, 48, 64, 96, 128, 256])
@@ -821,7 +832,7 @@ def _tc_sweep(family, n, seed, split2=False):
 
 @pytest.mark.parametrize("family,n,seed,split2", [
     ("tc3d", 32, 51, False), ("tc3dg", 24, 52, False), ("tc3s", 32, 53, False), ("umma", 24, 54, False),
-    ("tc1d", 16, 55, False), ("ffma", 24, 56, False),
+    ("tc1d", 16, 55, False), ("ffma", 24, 56, False), ("cl_generic", 40, 57, False),
     ("tc3d", 12, 61, True), ("tc3dg", 12, 62, True), ("tc3s", 12, 63, True)])
 def test_random_tensor_core_planner_sweep(family, n, seed, split2):
     import transposed_convolution_convtranspose_gb300 as ct
@@ -841,7 +852,7 @@ def _run_sweep(family, n, seed, split2):
         y = yt.cpu().numpy()
         ref = cc.run_oracle(c, t)
         cc.assert_close(y, ref, c["dtype"], "%s sweep case %d %r" % (family, k, c))
-        if c["dtype"] == "f32" and not c["add"] and family != "ffma":
+        if c["dtype"] == "f32" and not c["add"] and family not in ("ffma", "cl_generic"):
             # the split's bound against sum |x||w| (+ |bias|, added in fp32):
             # tf32x3 at fp32 level, the bf16 pair at about 16-bit operands
             mag = dict(t, x=np.abs(t["x"]), w=np.abs(t["w"]), bias=None)

@@ -319,3 +319,76 @@ def test_noalloc_scratch_constant_matches_header(lib):
     m = re.search(r"#define\s+CT_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*\*\s*(\d+)u\s*\*\s*(\d+)u\)", txt)
     assert m, "CT_NOALLOC_SCRATCH_BYTES not found in include/ct.h"
     assert int(m.group(1)) * int(m.group(2)) * int(m.group(3)) == ct.CT_NOALLOC_SCRATCH_BYTES
+
+
+_SCRATCH_FREE = {"gather_generic", "phase1d_f32", "phase3d_f32", "tc1d_tf32x3"}
+_SCRATCH = {"umma_bf16", "tc3d_tf32x3", "tc3d_bf16x2", "tc3dg_tf32x3", "tc3dg_bf16x2", "tc3s_tf32x3",
+            "tc3s_bf16x2"}
+
+
+def test_path_and_workspace_queries_agree(lib):
+    """For random shapes, small ones and ones in the tensor-core kernels'
+    ranges: the kernel a path query names needs scratch exactly when the
+    workspace query reports some (a multiple of 256 bytes); a call given that
+    much takes that kernel, one given 256 bytes less is rejected, and one given
+    none runs a kernel without scratch (fp32) or is rejected (bf16)."""
+    rng = np.random.default_rng(77)
+    pick = lambda seq: seq[int(rng.integers(0, len(seq)))]
+    seen = set()
+    for t in range(800):
+        nd = 1 + t % 3
+        mode = (t // 3) % 4          # 0 any; 1 tensor-core channel counts; 2 stride 2; 3 FFMA 3-D shapes
+        G = pick([1, 1, 2, 4])
+        C_in, C_out = G * pick([1, 2, 8, 16, 32]), G * pick([1, 4, 8, 16, 32])
+        dt = pick([ct.CT_F32, ct.CT_F32, ct.CT_BF16, ct.CT_F32_BF16X2])
+        if mode in (1, 2):
+            G = pick([1, 1, 1, 2, 4])
+            C_in, C_out = pick([32, 64, 128]), pick([16, 32, 64, 128])
+        K = [int(rng.integers(1, 6)) for _ in range(nd)]
+        S = [pick([1, 2, 2, 3, 4]) for _ in range(nd)]
+        DL = [pick([1, 1, 2]) for _ in range(nd)]
+        if mode == 2:
+            K = [pick([2, 3, 4]) for _ in range(nd)]
+            S, DL = [2] * nd, [1] * nd
+            if dt == ct.CT_BF16:            # the bf16 kernel: equal even extents, dense channels
+                K, G, C_in = [pick([2, 4]) if nd == 3 else 4] * nd, 1, pick([64, 128])
+        if mode == 1 and nd == 1 and t % 2:     # the 1-D tensor-core kernel's range
+            C_in, G, K, DL = 32, 1, [pick([1, 2, 3, 4])], [S[0] * pick([1, 2])]
+        if mode == 3 and nd == 3:
+            dt, G = ct.CT_F32, pick([1, 2])
+            C_in, C_out = G * pick([4, 8]), G * 16
+            K, S, DL = pick([[3, 3, 3], [3, 5, 7]]), [2] * 3, [1] * 3
+        P = [int(rng.integers(0, DL[d] * (K[d] - 1) // 2 + 1)) for d in range(nd)]
+        if mode == 3 and nd == 3:
+            P[2] = (K[2] - 1) // 2
+        OP = [int(rng.integers(0, max(S[d], DL[d]))) for d in range(nd)]
+        L = [int(rng.integers(1, 9)) for _ in range(nd - 1)] + [pick([2, 4, 8, 16, 32, 5, 12, 60])]
+        if nd == 1:
+            L = [4 * int(rng.integers(1, 1000))]
+        if C_in % G or C_out % G:
+            G = 1
+        N = pick([1, 2])
+        if any(ct.ct_out_len(L[d], K[d], S[d], P[d], OP[d], DL[d]) < 1 for d in range(nd)):
+            continue
+        if nd == 1:
+            a1 = (N, C_in, C_out, L[0], K[0], G, S[0], P[0], OP[0], DL[0], dt)
+            path, need = ct.ct_path_1d(*a1), ct.ct_workspace_size_1d(*a1)
+        elif nd == 2:
+            a2 = (N, C_in, C_out, L, K, G, S, P, OP, DL, dt)
+            path, need = ct.ct_path_2d(*a2), ct.ct_workspace_size_2d(*a2)
+        else:
+            a3 = (N, C_in, C_out, L, K, G, S, P, OP, DL, dt)
+            path, need = ct.ct_path_3d(*a3), ct.ct_workspace_size_3d(*a3)
+        what = (nd, N, C_in, C_out, G, L, K, S, P, OP, DL, dt, path, need)
+        assert path in _SCRATCH_FREE | _SCRATCH, what
+        assert (need > 0) == (path in _SCRATCH), what
+        assert need % 256 == 0, what
+        call = (nd, 0, N, C_in, C_out, L, K, G, S, P, OP, DL, dt, 0)
+        assert ct.ct_path_call(*call, need) == path, what
+        if need:
+            assert ct.ct_path_call(*call, need - 256) is None, what
+            bare = ct.ct_path_call(*call, 0)
+            assert (bare is None) if dt == ct.CT_BF16 else (bare in _SCRATCH_FREE), (what, bare)
+            seen.add(bare)
+        seen.add(path)
+    assert seen >= _SCRATCH_FREE | _SCRATCH, sorted(x for x in seen if x)
